@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Throughput of one GPT-2 training step (forward, backward, AdamW) on a B300.
+
+Default workload: GPT-2 124M (V 50257, L 12, H 12, C 768) at B=16, T=1024 with
+tensor-core (tf32) contractions, seeded synthetic parameters and a Zipf(1.1)
+token stream.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single-precision build, OpenMP on the
+host cores) on a bounded sample of the same workload.  Under torchrun every
+rank runs an independent replica of the step (the path has no collective on
+one GPU per rank); the timed region is bracketed by a barrier and the slowest
+rank's time is used.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gpt_decoder_step_train_b300 import synthetic as syn  # noqa: E402
+
+METRIC = "train tokens/s per fwd+bwd+AdamW step (GPT-2 124M, B16 T1024); % roofline"
+UNIT = "tokens/s"
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25 -> ratio used to derive the
+# tf32 peak from the measured bf16 peak
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="124M", choices=list(syn.CONFIGS))
+    ap.add_argument("--mode", default="tf32", choices=["tf32", "fp32"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--cpu-sample-T", type=int, default=256,
+                    help="positions of the single sequence the CPU baseline runs")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def gemm_flops(cfg, B, T):
+    """Algorithmic FLOPs of every linear layer's forward, dX and dW product."""
+    BT = B * T
+    return 6.0 * BT * (12 * cfg.L * cfg.C ** 2 + cfg.C * cfg.V)
+
+
+def step_flops(cfg, B, T):
+    """Matmul FLOPs plus causal attention FLOPs (fwd + bwd) of one step."""
+    return gemm_flops(cfg, B, T) + 6.0 * cfg.L * T * cfg.C * B * T
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        mx = max(r[1] for r in rows)
+        loaded = [r[0] for r in rows if r[0] > 0.3 * mx] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def time_oracle(cfg, T_sample, steps, warmup=0):
+    """Time the single-precision oracle on one sequence of T_sample positions of
+    the workload (fwd + bwd + AdamW over all parameters).  Returns (tokens/s, cores)."""
+    from oracle import Oracle
+    o = Oracle("f32")
+    params = syn.init_params(cfg)
+    tok, tgt = syn.draw_tokens(cfg, B=1, T=T_sample)
+    m = o.model(cfg.dims(), 1, T_sample)
+    am, av = np.zeros_like(params), np.zeros_like(params)
+    times = []
+    for t in range(1, warmup + steps + 1):
+        t0 = time.perf_counter()
+        m.forward(params, tok, tgt)
+        g = m.backward(params)
+        m.adamw(params, g, am, av, cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.wd, t)
+        if t > warmup:
+            times.append(time.perf_counter() - t0)
+    return T_sample * len(times) / sum(times), o.num_threads(), sum(times)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, cfg):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    T_sample = 64
+    tps, cores, total = time_oracle(cfg, T_sample, args.steps, args.warmup)
+    sample = (f"{args.steps} timed steps (+{args.warmup} warm-up), each fwd+bwd+AdamW of the "
+              f"{cfg.name} model on one sequence of {T_sample} positions")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * T_sample / tps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded init, Zipf(1.1) tokens)",
+        "config": {"workload": cfg.name, "global_batch": cfg.B, "seq_len": cfg.T,
+                   "sample": f"B=1 T={T_sample}", "parallelism": "cpu-openmp"},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, cfg):
+    import torch
+    from gpt_decoder_step_train_b300 import binding
+    from gpt_decoder_step_train_b300.binding import GPT2
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, T = cfg.B, cfg.T
+
+    params = torch.from_numpy(syn.init_params(cfg)).to(dev)
+    model = GPT2(cfg, params, maxB=B, mode=args.mode)
+    stream = model.stream
+    # a pool of distinct batches (seeded per rank), resident on the device
+    pool = []
+    for i in range(4):
+        tok, tgt = syn.draw_tokens(cfg, seed=cfg.token_seed + 1000 * rank + i)
+        pool.append((tok, tgt))
+    dev_pool = [(torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)) for a, b in pool]
+    host_pool = [(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory())
+                 for a, b in pool]
+
+    t_step = [0]
+
+    def step(tokens, targets):
+        t_step[0] += 1
+        loss = model.forward(tokens, targets)
+        rc = model.backward()
+        if rc != 0:
+            raise RuntimeError(f"backward failed: {binding.strerror(rc)}")
+        rc = model.adamw(cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.wd, t_step[0])
+        if rc != 0:
+            raise RuntimeError(f"adamw failed: {binding.strerror(rc)}")
+        return loss
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    for i in range(args.warmup):
+        loss = step(*dev_pool[i % len(dev_pool)])
+    st = model.status()
+    if st != 0:
+        raise RuntimeError(f"warm-up failed: {binding.strerror(st)}")
+
+    # ---- timed region: inputs resident in HBM -------------------------------
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    clocks = ClockSampler(gpu_index)
+    if not args.no_trace:
+        model.trace(True)
+    barrier()
+    clocks.start()
+    n_launch0 = binding.lib().gpt2_kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    losses = []
+    for i in range(args.steps):
+        losses.append(step(*dev_pool[i % len(dev_pool)]))
+    e1.record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    launches = binding.lib().gpt2_kernel_launches() - n_launch0
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    kernels = model.trace_read() if not args.no_trace else {}
+    model.trace(False)
+    st = model.status()
+    if st != 0:
+        raise RuntimeError(f"timed steps failed: {binding.strerror(st)}")
+    if not all(np.isfinite(losses)):
+        raise RuntimeError(f"non-finite loss: {losses}")
+
+    ms_per_step = ms_total / args.steps
+    tokens_total = world * B * T * args.steps
+    value = tokens_total / (ms_total / 1000.0)
+
+    # ---- end to end: pinned host inputs copied every step, loss read back ---
+    e2e = None
+    if not args.no_e2e:
+        ke = max(3, min(args.steps, 10))
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(ke):
+            step(*host_pool[i % len(host_pool)])
+        barrier()
+        wall = max_over_ranks(time.perf_counter() - t0)
+        e2e = {"value": world * B * T * ke / wall, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4, "steps": ke}
+
+    # ---- roofline of the dominant kernel (the tcgen05 GEMM) ------------------
+    peaks, peak_src = load_peaks()
+    roofline = None
+    per_class = {}
+    if kernels:
+        for name, (ms, nl) in kernels.items():
+            per_class[name] = {"ms_per_step": round(ms / args.steps, 4),
+                               "launches_per_step": nl / args.steps}
+        gemm_names = ("matmul_fwd", "matmul_bwd_input", "matmul_bwd_weight")
+        gemm_ms = sum(kernels[n][0] for n in gemm_names) / args.steps
+        if args.mode == "tf32":
+            peak = peaks["bf16_tflops_sustained"] * TF32_OVER_BF16
+            peak_note = f"tf32 = bf16 sustained x 1.1/2.25 ({peak_src})"
+        else:
+            peak = None
+            peak_note = "fp32 SIMT mode"
+        achieved = gemm_flops(cfg, B, T) / (gemm_ms / 1000.0) / 1e12
+        roofline = {"kernel": "gemm_tf32 (all linear fwd/dX/dW products)", "bound": "tensor",
+                    "achieved": round(achieved, 1), "peak": round(peak, 1) if peak else None,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
+                    "traffic": None, "peak_source": peak_note,
+                    "share_of_step": round(gemm_ms / ms_per_step, 4)}
+
+    mfu = step_flops(cfg, B, T) / (ms_per_step / 1000.0) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if args.mode == "tf32" else "f32",
+        "data": "synthetic (seeded N(0,0.02) init, Zipf(1.1) tokens, next-token targets)",
+        "config": {"workload": cfg.name, "global_batch": B * world, "seq_len": T,
+                   "mode": args.mode, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "working set ~15 GB >> 126 MB L2, no flush"},
+        "loss_first_last": [round(losses[0], 5), round(losses[-1], 5)],
+        "step_tflops": round(mfu, 1),
+        "roofline": roofline,
+        "kernels": per_class,
+        "gpu_launches": int(launches),
+        "clocks": clock_info,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, cores, total = time_oracle(cfg, args.cpu_sample_T, 1)
+        line["cpu_baseline"] = {
+            "value": round(tps, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one fwd+bwd+AdamW step of the same model on B=1, T={args.cpu_sample_T} "
+                      f"(oracle, single-precision build), {total:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    cfg = syn.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,314 @@
+// attention.cu -- causal multi-head self-attention, forward and backward.
+//
+// Per (batch b, head h): S = Q K^T / sqrt(hs), S[i,j] = -inf for j > i,
+// P = softmax_rows(S), O = P V ("GPT-2 from scratch with torch", section
+// 自注意力: c_attn output split at C into q, k, v, viewed as (B,T,NH,hs), causal
+// mask applied with -Inf before the softmax; 1/sqrt(d_k) scaling explained in
+// "从头搭建GPT(Andrej Karpathy) 笔记", section attention中为什么要做scaling).
+//
+// The T x T matrix is never stored: the forward keeps a running row maximum
+// and sum (online softmax) and saves the row log-sum-exp; the backward
+// recomputes P from Q, K and the saved log-sum-exp.  Backward formulas:
+//   D_i = dO_i . O_i,  dV_j = sum_i P_ij dO_i,  dP_ij = dO_i . V_j,
+//   dS_ij = P_ij (dP_ij - D_i),  dQ_i = sum_j dS_ij K_j / sqrt(hs),
+//   dK_j = sum_i dS_ij Q_i / sqrt(hs).
+// Every output element is owned by exactly one thread, so there are no atomics
+// and results are deterministic.
+//
+// This file holds the CUDA-core kernels: one thread per query row (forward,
+// dQ) or per key row (dK, dV), with the row and its accumulator in registers
+// and tiles of the other side staged in shared memory.  Keys past a block's
+// last query are skipped (causal tile skipping).
+#include "common.cuh"
+
+namespace gpt2k {
+
+constexpr int AT_ROWS = 128;   // rows (threads) per block
+constexpr int AT_KT = 32;      // rows of the other side per shared-memory tile
+
+// Load `HSP` floats of row r of a [.., ld] matrix at column c0, hs of them real.
+template <int HSP>
+__device__ __forceinline__ void load_row(float* dst, const float* src, int hs, float mul) {
+#pragma unroll
+    for (int d = 0; d < HSP; d += 4) {
+        float4 v = d < hs ? *reinterpret_cast<const float4*>(src + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[d] = v.x * mul; dst[d + 1] = v.y * mul; dst[d + 2] = v.z * mul; dst[d + 3] = v.w * mul;
+    }
+}
+
+// Cooperative load of rows [r0, r0+AT_KT) (zeros past T) of up to two column
+// blocks into shared tiles [AT_KT][HSP].
+template <int HSP>
+__device__ __forceinline__ void load_tile(float (*dst)[HSP], const float* base, size_t ld, int r0,
+                                          int T, int hs) {
+    for (int idx = threadIdx.x; idx < AT_KT * (HSP / 4); idx += blockDim.x) {
+        int r = idx / (HSP / 4), d = (idx % (HSP / 4)) * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + r < T && d < hs) v = *reinterpret_cast<const float4*>(base + (size_t)(r0 + r) * ld + d);
+        *reinterpret_cast<float4*>(&dst[r][d]) = v;
+    }
+}
+
+template <int HSP>
+__device__ __forceinline__ float dot_row(const float* a, const float* b) {
+    float s = 0.f;
+#pragma unroll
+    for (int d = 0; d < HSP; d++) s = fmaf(a[d], b[d], s);
+    return s;
+}
+
+template <int HSP>
+__global__ void __launch_bounds__(AT_ROWS)
+attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __restrict__ qkv, int T,
+              int C, int H, int hs, float scale) {
+    __shared__ __align__(16) float Ks[AT_KT][HSP];
+    __shared__ __align__(16) float Vs[AT_KT][HSP];
+    const int b = blockIdx.z, h = blockIdx.y, q0 = blockIdx.x * AT_ROWS;
+    const int i = q0 + threadIdx.x;
+    const bool active = i < T;
+    const size_t ld = 3 * (size_t)C;
+    const float* base = qkv + (size_t)b * T * ld;
+    float q[HSP], o[HSP];
+    if (active) load_row<HSP>(q, base + (size_t)i * ld + h * hs, hs, scale);
+#pragma unroll
+    for (int d = 0; d < HSP; d++) o[d] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    const int kend = min(T, q0 + AT_ROWS);
+    for (int k0 = 0; k0 < kend; k0 += AT_KT) {
+        __syncthreads();
+        load_tile<HSP>(Ks, base + C + h * hs, ld, k0, T, hs);
+        load_tile<HSP>(Vs, base + 2 * C + h * hs, ld, k0, T, hs);
+        __syncthreads();
+        if (!active) continue;
+        const int jn = min(AT_KT, i - k0 + 1);
+        if (jn <= 0) continue;
+        float s[AT_KT];
+        float tmax = m;
+#pragma unroll
+        for (int j = 0; j < AT_KT; j++) {
+            if (j < jn) {
+                s[j] = dot_row<HSP>(q, Ks[j]);
+                tmax = fmaxf(tmax, s[j]);
+            }
+        }
+        const float corr = expf(m - tmax);
+        l *= corr;
+#pragma unroll
+        for (int d = 0; d < HSP; d++) o[d] *= corr;
+#pragma unroll
+        for (int j = 0; j < AT_KT; j++) {
+            if (j < jn) {
+                float p = expf(s[j] - tmax);
+                l += p;
+#pragma unroll
+                for (int d = 0; d < HSP; d++) o[d] = fmaf(p, Vs[j][d], o[d]);
+            }
+        }
+        m = tmax;
+    }
+    if (!active) return;
+    const float inv = 1.f / l;
+    float* yr = y + ((size_t)b * T + i) * C + h * hs;
+#pragma unroll
+    for (int d = 0; d < HSP; d += 4)
+        if (d < hs) *reinterpret_cast<float4*>(yr + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+    lse[((size_t)b * H + h) * T + i] = m + logf(l);
+}
+
+// D[b,h,i] = dO_i . O_i
+__global__ void attn_bwd_dot_kernel(float* __restrict__ D, const float* __restrict__ dy,
+                                    const float* __restrict__ y, int B, int T, int C, int H, int hs) {
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)B * H * T) return;
+    int i = (int)(idx % T);
+    int h = (int)((idx / T) % H);
+    int b = (int)(idx / ((long long)T * H));
+    const float* a = dy + ((size_t)b * T + i) * C + h * hs;
+    const float* o = y + ((size_t)b * T + i) * C + h * hs;
+    float s = 0.f;
+    for (int d = 0; d < hs; d += 4) {
+        float4 u = *reinterpret_cast<const float4*>(a + d), v = *reinterpret_cast<const float4*>(o + d);
+        s += (u.x * v.x + u.y * v.y) + (u.z * v.z + u.w * v.w);
+    }
+    D[idx] = s;
+}
+
+// dQ: one thread per query row i; key/value tiles j <= i in shared memory.
+template <int HSP>
+__global__ void __launch_bounds__(AT_ROWS)
+attn_bwd_dq_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
+                 const float* __restrict__ qkv, const float* __restrict__ lse,
+                 const float* __restrict__ D, int T, int C, int H, int hs, float scale) {
+    __shared__ __align__(16) float Ks[AT_KT][HSP];
+    __shared__ __align__(16) float Vs[AT_KT][HSP];
+    const int b = blockIdx.z, h = blockIdx.y, q0 = blockIdx.x * AT_ROWS;
+    const int i = q0 + threadIdx.x;
+    const bool active = i < T;
+    const size_t ld = 3 * (size_t)C;
+    const float* base = qkv + (size_t)b * T * ld;
+    float q[HSP], g[HSP], dq[HSP];
+    float li = 0.f, Di = 0.f;
+    if (active) {
+        load_row<HSP>(q, base + (size_t)i * ld + h * hs, hs, scale);
+        load_row<HSP>(g, dy + ((size_t)b * T + i) * C + h * hs, hs, 1.f);
+        li = lse[((size_t)b * H + h) * T + i];
+        Di = D[((size_t)b * H + h) * T + i];
+    }
+#pragma unroll
+    for (int d = 0; d < HSP; d++) dq[d] = 0.f;
+    const int kend = min(T, q0 + AT_ROWS);
+    for (int k0 = 0; k0 < kend; k0 += AT_KT) {
+        __syncthreads();
+        load_tile<HSP>(Ks, base + C + h * hs, ld, k0, T, hs);
+        load_tile<HSP>(Vs, base + 2 * C + h * hs, ld, k0, T, hs);
+        __syncthreads();
+        if (!active) continue;
+        const int jn = min(AT_KT, i - k0 + 1);
+#pragma unroll 4
+        for (int j = 0; j < jn; j++) {
+            float p = expf(dot_row<HSP>(q, Ks[j]) - li);
+            float ds = p * (dot_row<HSP>(g, Vs[j]) - Di);
+#pragma unroll
+            for (int d = 0; d < HSP; d++) dq[d] = fmaf(ds, Ks[j][d], dq[d]);
+        }
+    }
+    if (!active) return;
+    float* out = dqkv + ((size_t)b * T + i) * ld + h * hs;
+#pragma unroll
+    for (int d = 0; d < HSP; d += 4)
+        if (d < hs) *reinterpret_cast<float4*>(out + d) = make_float4(dq[d] * scale, dq[d + 1] * scale, dq[d + 2] * scale, dq[d + 3] * scale);
+}
+
+// dK and dV: one thread per key row j; query tiles i >= j in shared memory.
+// WANT_DK selects dK (needs V_j too) or dV.
+template <int HSP, bool WANT_DK>
+__global__ void __launch_bounds__(AT_ROWS)
+attn_bwd_dkv_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
+                  const float* __restrict__ qkv, const float* __restrict__ lse,
+                  const float* __restrict__ D, int T, int C, int H, int hs, float scale) {
+    __shared__ __align__(16) float Qs[AT_KT][HSP];
+    __shared__ __align__(16) float Gs[AT_KT][HSP];
+    __shared__ float Ls[AT_KT], Ds[AT_KT];
+    const int b = blockIdx.z, h = blockIdx.y, k0b = blockIdx.x * AT_ROWS;
+    const int j = k0b + threadIdx.x;
+    const bool active = j < T;
+    const size_t ld = 3 * (size_t)C;
+    const float* base = qkv + (size_t)b * T * ld;
+    const float* lse_bh = lse + ((size_t)b * H + h) * T;
+    const float* D_bh = D + ((size_t)b * H + h) * T;
+    float k[HSP], v[HSP], acc[HSP];
+    if (active) {
+        load_row<HSP>(k, base + (size_t)j * ld + C + h * hs, hs, scale);
+        if (WANT_DK) load_row<HSP>(v, base + (size_t)j * ld + 2 * C + h * hs, hs, 1.f);
+    }
+#pragma unroll
+    for (int d = 0; d < HSP; d++) acc[d] = 0.f;
+    for (int i0 = k0b; i0 < T; i0 += AT_KT) {
+        __syncthreads();
+        load_tile<HSP>(Qs, base + h * hs, ld, i0, T, hs);
+        load_tile<HSP>(Gs, dy + (size_t)b * T * C + h * hs, C, i0, T, hs);
+        if (threadIdx.x < AT_KT) {
+            int ii = i0 + threadIdx.x;
+            Ls[threadIdx.x] = ii < T ? lse_bh[ii] : 0.f;
+            Ds[threadIdx.x] = ii < T ? D_bh[ii] : 0.f;
+        }
+        __syncthreads();
+        if (!active) continue;
+        const int ibeg = max(0, j - i0), iend = min(AT_KT, T - i0);
+#pragma unroll 4
+        for (int r = ibeg; r < iend; r++) {
+            float p = expf(dot_row<HSP>(k, Qs[r]) - Ls[r]);
+            if (WANT_DK) {
+                float ds = p * (dot_row<HSP>(v, Gs[r]) - Ds[r]);
+#pragma unroll
+                for (int d = 0; d < HSP; d++) acc[d] = fmaf(ds, Qs[r][d], acc[d]);
+            } else {
+#pragma unroll
+                for (int d = 0; d < HSP; d++) acc[d] = fmaf(p, Gs[r][d], acc[d]);
+            }
+        }
+    }
+    if (!active) return;
+    const float mul = WANT_DK ? scale : 1.f;
+    float* out = dqkv + ((size_t)b * T + j) * ld + (WANT_DK ? C : 2 * C) + h * hs;
+#pragma unroll
+    for (int d = 0; d < HSP; d += 4)
+        if (d < hs) *reinterpret_cast<float4*>(out + d) = make_float4(acc[d] * mul, acc[d + 1] * mul, acc[d + 2] * mul, acc[d + 3] * mul);
+}
+
+template <int HSP>
+static void launch_fwd(float* y, float* lse, const float* qkv, int B, int T, int C, int H, int hs,
+                       cudaStream_t st) {
+    dim3 grid(ceil_div(T, AT_ROWS), H, B);
+    count_launch(), attn_fwd_simt<HSP><<<grid, AT_ROWS, 0, st>>>(y, lse, qkv, T, C, H, hs, 1.f / sqrtf((float)hs));
+}
+
+template <int HSP>
+static void launch_bwd(float* dqkv, const float* dy, const float* qkv, const float* lse,
+                       const float* D, int B, int T, int C, int H, int hs, cudaStream_t st) {
+    dim3 grid(ceil_div(T, AT_ROWS), H, B);
+    float scale = 1.f / sqrtf((float)hs);
+    count_launch(), attn_bwd_dq_simt<HSP><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
+    count_launch(), attn_bwd_dkv_simt<HSP, true><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
+    count_launch(), attn_bwd_dkv_simt<HSP, false><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
+}
+
+int attention_tc_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int H,
+                         int* status, cudaStream_t st);
+int attention_tc_backward(float* dqkv, const float* dy, const float* qkv, const float* lse,
+                          const float* D, int B, int T, int C, int H, int* status,
+                          cudaStream_t st);
+bool attention_tc_supported(int hs);
+
+}  // namespace gpt2k
+
+using namespace gpt2k;
+
+static bool attn_args_ok(int B, int T, int C, int H) {
+    if (B < 1 || T < 1 || C < 4 || H < 1 || C % H) return false;
+    int hs = C / H;
+    return hs % 4 == 0 && hs <= 64;
+}
+
+GPT2_API int gpt2_op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C,
+                                       int H, int mode, int* status, void* stream) {
+    if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
+    if (!aligned16(y) || !aligned16(qkv)) return GPT2_EINVAL;
+    int hs = C / H;
+    cudaStream_t st = as_stream(stream);
+    if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
+        return attention_tc_forward(y, lse, qkv, B, T, C, H, status, st);
+    if (hs <= 16) launch_fwd<16>(y, lse, qkv, B, T, C, H, hs, st);
+    else if (hs <= 32) launch_fwd<32>(y, lse, qkv, B, T, C, H, hs, st);
+    else launch_fwd<64>(y, lse, qkv, B, T, C, H, hs, st);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+GPT2_API size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
+    if (B < 1 || T < 1 || H < 1) return 0;
+    return round_up((size_t)B * H * T * sizeof(float), 256);
+}
+
+GPT2_API int gpt2_op_attention_backward(float* dqkv, const float* dy, const float* qkv,
+                                        const float* y, const float* lse, int B, int T, int C,
+                                        int H, void* scratch, size_t scratch_bytes, int mode,
+                                        int* status, void* stream) {
+    if (!dqkv || !dy || !qkv || !y || !lse || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
+    if (!aligned16(dqkv) || !aligned16(dy) || !aligned16(qkv) || !aligned16(y)) return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < gpt2_op_attention_backward_scratch_bytes(B, T, H))
+        return GPT2_ENOMEM;
+    int hs = C / H;
+    cudaStream_t st = as_stream(stream);
+    float* D = reinterpret_cast<float*>(scratch);
+    long long n = (long long)B * H * T;
+    count_launch(), attn_bwd_dot_kernel<<<ceil_div(n, 256), 256, 0, st>>>(D, dy, y, B, T, C, H, hs);
+    GPT2_LAUNCH_CHECK();
+    if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
+        return attention_tc_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st);
+    if (hs <= 16) launch_bwd<16>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
+    else if (hs <= 32) launch_bwd<32>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
+    else launch_bwd<64>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}

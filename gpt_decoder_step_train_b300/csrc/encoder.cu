@@ -1,0 +1,208 @@
+// encoder.cu -- token + position embedding, forward and deterministic backward.
+//
+// Forward: x[b,t,:] = wte[tok[b,t],:] + wpe[t,:]  ("GPT-2 from scratch with
+// torch", section 从词到编码: the two embeddings are added).
+//
+// Backward: dwte[v,:] += sum_{pos: tok[pos]=v} dx[pos,:] and dwpe[t,:] =
+// sum_b dx[b,t,:].  The token-side scatter-add is made deterministic without
+// float atomics: positions are bucketed by token id with an integer counting
+// sort, each bucket is put in ascending position order, and one thread block
+// per distinct token sums its bucket's rows in that order.
+#include "common.cuh"
+
+namespace gpt2k {
+
+__global__ void encoder_fwd_kernel(float4* __restrict__ x, const int* __restrict__ tok,
+                                   const float4* __restrict__ wte, const float4* __restrict__ wpe,
+                                   int BT, int T, int C4, int V, int* status) {
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)BT * C4) return;
+    int row = (int)(idx / C4), c = (int)(idx % C4);
+    int t = row % T;
+    int id = tok[row];
+    if (id < 0 || id >= V) {
+        if (c == 0) set_status(status, GPT2_STATUS_BAD_TOKEN);
+        x[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    float4 e = wte[(size_t)id * C4 + c];
+    float4 p = wpe[(size_t)t * C4 + c];
+    x[idx] = make_float4(e.x + p.x, e.y + p.y, e.z + p.z, e.w + p.w);
+}
+
+// ---- counting sort of positions by token id -------------------------------
+
+__global__ void enc_histogram_kernel(int* __restrict__ count, const int* __restrict__ tok, int BT,
+                                     int V) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BT) return;
+    int id = tok[i];
+    if (id >= 0 && id < V) atomicAdd(&count[id], 1);
+}
+
+// One block: exclusive scan of count[0..V) into offset[], and the list of
+// distinct ids present (in increasing id order) into uniq[]; *n_uniq its length.
+__global__ void enc_scan_kernel(int* __restrict__ offset, int* __restrict__ uniq,
+                                int* __restrict__ n_uniq, const int* __restrict__ count, int V) {
+    __shared__ int s_sum[1024], s_nz[1024];
+    int tid = threadIdx.x, nt = blockDim.x;
+    int per = (V + nt - 1) / nt;
+    int lo = min(V, tid * per), hi = min(V, lo + per);
+    int sum = 0, nz = 0;
+    for (int v = lo; v < hi; v++) { sum += count[v]; nz += count[v] > 0; }
+    s_sum[tid] = sum;
+    s_nz[tid] = nz;
+    __syncthreads();
+    // Hillis-Steele inclusive scan over the per-thread totals
+    for (int o = 1; o < nt; o <<= 1) {
+        int a = tid >= o ? s_sum[tid - o] : 0;
+        int b = tid >= o ? s_nz[tid - o] : 0;
+        __syncthreads();
+        s_sum[tid] += a;
+        s_nz[tid] += b;
+        __syncthreads();
+    }
+    int run = s_sum[tid] - sum, runu = s_nz[tid] - nz;
+    for (int v = lo; v < hi; v++) {
+        offset[v] = run;
+        run += count[v];
+        if (count[v] > 0) uniq[runu++] = v;
+    }
+    if (tid == nt - 1) { offset[V] = s_sum[tid]; *n_uniq = s_nz[tid]; }
+}
+
+__global__ void enc_fill_kernel(int* __restrict__ list, int* __restrict__ cursor,
+                                const int* __restrict__ offset, const int* __restrict__ tok, int BT,
+                                int V) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BT) return;
+    int id = tok[i];
+    if (id < 0 || id >= V) return;
+    list[offset[id] + atomicAdd(&cursor[id], 1)] = i;
+}
+
+// Put each bucket in ascending position order: a position's rank in its bucket
+// is the number of bucket entries smaller than it (positions are distinct).
+__global__ void enc_rank_kernel(int* __restrict__ sorted, const int* __restrict__ list,
+                                const int* __restrict__ offset, const int* __restrict__ tok, int BT,
+                                int V) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BT) return;
+    int id = tok[i];
+    if (id < 0 || id >= V) return;
+    int lo = offset[id], hi = offset[id + 1];
+    int r = 0;
+    for (int e = lo; e < hi; e++) r += list[e] < i;
+    sorted[lo + r] = i;
+}
+
+// One block per distinct token; threads stride over the C/4 float4 columns.
+__global__ void enc_accumulate_kernel(float4* __restrict__ dwte, const float4* __restrict__ dx,
+                                      const int* __restrict__ sorted,
+                                      const int* __restrict__ offset, const int* __restrict__ uniq,
+                                      const int* __restrict__ n_uniq, int C4) {
+    int u = blockIdx.x;
+    if (u >= *n_uniq) return;
+    int id = uniq[u];
+    int lo = offset[id], hi = offset[id + 1];
+    for (int c = threadIdx.x; c < C4; c += blockDim.x) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = lo; e < hi; e++) {
+            float4 g = dx[(size_t)sorted[e] * C4 + c];
+            s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+        }
+        float4 d = dwte[(size_t)id * C4 + c];
+        d.x += s.x; d.y += s.y; d.z += s.z; d.w += s.w;
+        dwte[(size_t)id * C4 + c] = d;
+    }
+}
+
+__global__ void enc_dwpe_kernel(float4* __restrict__ dwpe, const float4* __restrict__ dx, int B,
+                                int T, int maxT, int C4) {
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)maxT * C4) return;
+    int t = (int)(idx / C4), c = (int)(idx % C4);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < T) {
+        for (int b = 0; b < B; b++) {
+            float4 g = dx[((size_t)b * T + t) * C4 + c];
+            s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+        }
+    }
+    dwpe[idx] = s;
+}
+
+struct EncScratch {
+    int *count, *cursor, *offset, *uniq, *n_uniq, *list, *sorted;
+};
+
+static size_t enc_layout(int BT, int V, char* base, EncScratch* s) {
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        char* p = base ? base + off : nullptr;
+        off += round_up(n * sizeof(int), 256);
+        return reinterpret_cast<int*>(p);
+    };
+    EncScratch t;
+    t.count = take(V);
+    t.cursor = take(V);
+    t.offset = take((size_t)V + 1);
+    t.uniq = take(BT);
+    t.n_uniq = take(1);
+    t.list = take(BT);
+    t.sorted = take(BT);
+    if (s) *s = t;
+    return off;
+}
+
+}  // namespace gpt2k
+
+using namespace gpt2k;
+
+GPT2_API int gpt2_op_encoder_forward(float* x, const int* tok, const float* wte, const float* wpe,
+                                     int B, int T, int C, int V, int* status, void* stream) {
+    if (!x || !tok || !wte || !wpe || B < 1 || T < 1 || C < 4 || C % 4 || V < 1) return GPT2_EINVAL;
+    if (!aligned16(x) || !aligned16(wte) || !aligned16(wpe)) return GPT2_EINVAL;
+    int C4 = C / 4, BT = B * T;
+    long long n = (long long)BT * C4;
+    count_launch(), encoder_fwd_kernel<<<ceil_div(n, 256), 256, 0, as_stream(stream)>>>(
+        reinterpret_cast<float4*>(x), tok, reinterpret_cast<const float4*>(wte),
+        reinterpret_cast<const float4*>(wpe), BT, T, C4, V, status);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+GPT2_API size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V) {
+    if (BT < 1 || V < 1) return 0;
+    return enc_layout(BT, V, nullptr, nullptr);
+}
+
+GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx, const int* tok,
+                                      int B, int T, int maxT, int C, int V, void* scratch,
+                                      size_t scratch_bytes, void* stream) {
+    if (!dwte || !dwpe || !dx || !tok || B < 1 || T < 1 || T > maxT || C < 4 || C % 4 || V < 1)
+        return GPT2_EINVAL;
+    if (!aligned16(dwte) || !aligned16(dwpe) || !aligned16(dx)) return GPT2_EINVAL;
+    int BT = B * T, C4 = C / 4;
+    if (!scratch || scratch_bytes < gpt2_op_encoder_backward_scratch_bytes(BT, V)) return GPT2_ENOMEM;
+    cudaStream_t st = as_stream(stream);
+    EncScratch s;
+    enc_layout(BT, V, reinterpret_cast<char*>(scratch), &s);
+    GPT2_CUDA_TRY(cudaMemsetAsync(s.count, 0, sizeof(int) * V, st));
+    GPT2_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * V, st));
+    int nb = ceil_div(BT, 256);
+    count_launch(), enc_histogram_kernel<<<nb, 256, 0, st>>>(s.count, tok, BT, V);
+    count_launch(), enc_scan_kernel<<<1, 1024, 0, st>>>(s.offset, s.uniq, s.n_uniq, s.count, V);
+    count_launch(), enc_fill_kernel<<<nb, 256, 0, st>>>(s.list, s.cursor, s.offset, tok, BT, V);
+    count_launch(), enc_rank_kernel<<<nb, 256, 0, st>>>(s.sorted, s.list, s.offset, tok, BT, V);
+    int threads = C4 < 256 ? ((C4 + 31) / 32) * 32 : 256;
+    count_launch(), enc_accumulate_kernel<<<min(BT, V), threads, 0, st>>>(
+        reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(dx), s.sorted, s.offset,
+        s.uniq, s.n_uniq, C4);
+    long long n = (long long)maxT * C4;
+    count_launch(), enc_dwpe_kernel<<<ceil_div(n, 256), 256, 0, st>>>(reinterpret_cast<float4*>(dwpe),
+                                                     reinterpret_cast<const float4*>(dx), B, T,
+                                                     maxT, C4);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}

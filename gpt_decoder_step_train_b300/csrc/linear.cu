@@ -1,0 +1,182 @@
+// linear.cu -- the linear layer (nn_linear convention, W is [out, in]) and its
+// two backward products, dispatched to the CUDA-core or the tcgen05 GEMM, plus
+// the deterministic bias-gradient reduction.
+//
+// Forward out = inp . W^T + b with the epilogues the block needs fused in
+// (bias, tanh-GELU keeping its input, residual add): "GPT-2 from scratch with
+// torch", sections 自注意力 (c_attn, c_proj) and 前馈网络（MLP）(c_fc, GELU,
+// c_proj).  Backward (hand-derived): dinp = dout . W, dW = dout^T . inp,
+// db = column sums of dout.
+#include "gemm.cuh"
+
+namespace gpt2k {
+
+// ---- bias gradient: db[o] = sum_n dout[n*ld + o], fixed order -------------
+// Stage 1: block (32 columns x 8 row-lanes) over one chunk of rows; lane y sums
+// rows y, y+8, ... of the chunk in order; the 8 lanes are combined in order.
+constexpr int BG_ROWS = 256;
+
+__global__ void bias_grad_partial_kernel(float* __restrict__ partial, const float* __restrict__ dout,
+                                         int N, int OC, int ld) {
+    __shared__ float sh[8][33];
+    int col = blockIdx.x * 32 + threadIdx.x;
+    int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
+    float s = 0.f;
+    if (col < OC)
+        for (int r = r0 + threadIdx.y; r < r1; r += 8) s += dout[(size_t)r * ld + col];
+    sh[threadIdx.y][threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.y == 0 && col < OC) {
+        float t = sh[0][threadIdx.x];
+        for (int k = 1; k < 8; k++) t += sh[k][threadIdx.x];
+        partial[(size_t)blockIdx.y * OC + col] = t;
+    }
+}
+
+__global__ void bias_grad_reduce_kernel(float* __restrict__ db, const float* __restrict__ partial,
+                                        int nchunk, int OC) {
+    int col = blockIdx.x * blockDim.x + threadIdx.x;
+    if (col >= OC) return;
+    float s = 0.f;
+    for (int k = 0; k < nchunk; k++) s += partial[(size_t)k * OC + col];
+    db[col] = s;
+}
+
+static size_t bias_scratch_bytes(int N, int OC) {
+    return round_up((size_t)ceil_div(N, BG_ROWS) * OC * sizeof(float), 256);
+}
+
+static int bias_grad(float* db, const float* dout, int N, int OC, int ld, float* scratch,
+                     cudaStream_t st) {
+    int nchunk = ceil_div(N, BG_ROWS);
+    count_launch(), bias_grad_partial_kernel<<<dim3(ceil_div(OC, 32), nchunk), dim3(32, 8), 0, st>>>(scratch, dout,
+                                                                                   N, OC, ld);
+    count_launch(), bias_grad_reduce_kernel<<<ceil_div(OC, 256), 256, 0, st>>>(db, scratch, nchunk, OC);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+// ---- split-K sum: out[i] = sum_s partial[s][i], in slice order -------------
+__global__ void splitk_reduce_kernel(float4* __restrict__ out, const float4* __restrict__ partial,
+                                     int split, size_t n4) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 s = partial[i];
+    for (int k = 1; k < split; k++) {
+        float4 v = partial[(size_t)k * n4 + i];
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    out[i] = s;
+}
+
+// Number of K slices for the tensor-core dW product: enough output tiles to
+// cover the SMs about twice, each slice at least 1024 rows of the reduction.
+static int dw_split(int N, int IC, int OC) {
+    long long tiles = (long long)ceil_div(OC, 128) * ceil_div(IC, 256);
+    int sms = num_sms();
+    int split = 1;
+    while (tiles * split < 2LL * sms && N / (split * 2) >= 1024 && split < 16) split *= 2;
+    return split;
+}
+
+static int run_gemm(const GemmProblem& p, const GemmEpilogue& e, int mode, cudaStream_t st) {
+    if (mode == GPT2_MODE_FP32) return gemm_simt(p, e, st);
+    if (mode == GPT2_MODE_TF32) {
+        // operands TMA cannot address (unaligned base or row stride) take the CUDA cores
+        if (!gemm_tc_supported(p)) return gemm_simt(p, e, st);
+        return gemm_tc(p, e, st);
+    }
+    return GPT2_EINVAL;
+}
+
+}  // namespace gpt2k
+
+using namespace gpt2k;
+
+GPT2_API int gpt2_op_linear_forward(float* out, float* out_pre, const float* inp, const float* w,
+                                    const float* bias, const float* residual, int N, int IC, int OC,
+                                    int ld_out, int flags, int mode, int* status, void* stream) {
+    if (!out || !inp || !w || N < 1 || IC < 1 || OC < 1 || ld_out < OC) return GPT2_EINVAL;
+    if ((flags & GPT2_LINEAR_GELU) && (!out_pre || residual)) return GPT2_EINVAL;
+    cudaStream_t st = as_stream(stream);
+    GemmProblem p{N, OC, IC, inp, IC, true, w, IC, true, status};
+    GemmEpilogue e{};
+    e.out = out;
+    e.ldo = ld_out;
+    e.out_pre = out_pre;
+    e.bias = bias;
+    e.residual = residual;
+    e.gelu = (flags & GPT2_LINEAR_GELU) ? 1 : 0;
+    int rc = run_gemm(p, e, mode, st);
+    if (rc) return rc;
+    if ((flags & GPT2_LINEAR_ZERO_PAD) && ld_out > OC) {
+        GPT2_CUDA_TRY(cudaMemset2DAsync(out + OC, (size_t)ld_out * sizeof(float), 0,
+                                        (size_t)(ld_out - OC) * sizeof(float), N, st));
+    }
+    return GPT2_OK;
+}
+
+GPT2_API int gpt2_op_linear_backward_input(float* dinp, const float* dout, const float* w,
+                                           const float* gelu_x, int N, int IC, int OC, int ld_dout,
+                                           int mode, int* status, void* stream) {
+    if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status};
+    GemmEpilogue e{};
+    e.out = dinp;
+    e.ldo = IC;
+    e.gelu_x = gelu_x;
+    e.ldg = IC;
+    return run_gemm(p, e, mode, as_stream(stream));
+}
+
+GPT2_API size_t gpt2_op_linear_backward_weight_scratch_bytes(int N, int IC, int OC, int mode) {
+    if (N < 1 || IC < 1 || OC < 1) return 0;
+    size_t s = bias_scratch_bytes(N, OC);
+    if (mode == GPT2_MODE_TF32) {
+        int split = dw_split(N, IC, OC);
+        if (split > 1) s = std::max(s, (size_t)split * OC * IC * sizeof(float));
+    }
+    return s;
+}
+
+GPT2_API int gpt2_op_linear_backward_weight(float* dw, float* dbias, const float* dout,
+                                            const float* inp, int N, int IC, int OC, int ld_dout,
+                                            void* scratch, size_t scratch_bytes, int mode,
+                                            int* status, void* stream) {
+    if (!dw || !dout || !inp || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    if (scratch_bytes < gpt2_op_linear_backward_weight_scratch_bytes(N, IC, OC, mode) || !scratch)
+        return GPT2_ENOMEM;
+    cudaStream_t st = as_stream(stream);
+    GemmProblem p{OC, IC, N, dout, ld_dout, false, inp, IC, false, status};
+    int rc;
+    int split = mode == GPT2_MODE_TF32 ? dw_split(N, IC, OC) : 1;
+    if (split > 1 && gemm_tc_supported(p) && (size_t)OC * IC % 4 == 0 && aligned16(dw)) {
+        float* partial = reinterpret_cast<float*>(scratch);
+        rc = gemm_tc_splitk(p, partial, split, st);
+        if (rc) return rc;
+        size_t n4 = (size_t)OC * IC / 4;
+        count_launch(), splitk_reduce_kernel<<<ceil_div((long long)n4, 256), 256, 0, st>>>(
+            reinterpret_cast<float4*>(dw), reinterpret_cast<const float4*>(partial), split, n4);
+        GPT2_LAUNCH_CHECK();
+    } else {
+        GemmEpilogue e{};
+        e.out = dw;
+        e.ldo = IC;
+        rc = run_gemm(p, e, mode, st);
+        if (rc) return rc;
+    }
+    if (dbias) return bias_grad(dbias, dout, N, OC, ld_dout, reinterpret_cast<float*>(scratch), st);
+    return GPT2_OK;
+}
+
+GPT2_API size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC) {
+    if (N < 1 || OC < 1) return 0;
+    return bias_scratch_bytes(N, OC);
+}
+
+GPT2_API int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int ld_dout,
+                               void* scratch, size_t scratch_bytes, void* stream) {
+    if (!db || !dout || N < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < bias_scratch_bytes(N, OC)) return GPT2_ENOMEM;
+    return bias_grad(db, dout, N, OC, ld_dout, reinterpret_cast<float*>(scratch), as_stream(stream));
+}

@@ -1,0 +1,559 @@
+// model.cu -- the GPT-2 training step behind the C ABI of gpt2.h.
+//
+// One workspace block holds every buffer the step touches (gradients, AdamW
+// moments, activations for maxB*maxT rows, logits, scratch), carved once at
+// create time; nothing is allocated or freed while training, as the llm.c
+// overview (bigegpt.com) describes for its single 1-D memory block.
+//
+// Forward ("GPT-2 from scratch with torch": nn_gpt2_model and the transformer
+// block's forward): x = wte[tok] + wpe[t]; per block x = x + attn(ln_1(x)),
+// x = x + mlp(ln_2(x)); ln_f; logits = ln_f(x) . wte^T; mean cross-entropy.
+// Backward: each layer's hand-derived backward in reverse order, the residual
+// stream's gradient accumulated in one buffer.  Update: AdamW.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#include <new>
+#include <atomic>
+#include <functional>
+#include <vector>
+
+#include "common.cuh"
+
+namespace gpt2k {
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            n = 148;
+    }
+    return n;
+}
+
+static std::atomic<long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+constexpr int NT = 16;
+static const bool kDecay[NT] = {true, true, false, false, true, false, true, false,
+                                false, false, true, false, true, false, false, false};
+enum { WTE, WPE, LN1W, LN1B, QKVW, QKVB, ATTPROJW, ATTPROJB, LN2W, LN2B, FCW, FCB, FCPROJW,
+       FCPROJB, LNFW, LNFB };
+
+static void tensor_sizes(const gpt2_config& c, size_t* s) {
+    size_t C = c.C, L = c.L;
+    s[WTE] = (size_t)c.V * C;  s[WPE] = (size_t)c.maxT * C;
+    s[LN1W] = L * C;           s[LN1B] = L * C;
+    s[QKVW] = L * 3 * C * C;   s[QKVB] = L * 3 * C;
+    s[ATTPROJW] = L * C * C;   s[ATTPROJB] = L * C;
+    s[LN2W] = L * C;           s[LN2B] = L * C;
+    s[FCW] = L * 4 * C * C;    s[FCB] = L * 4 * C;
+    s[FCPROJW] = L * C * 4 * C; s[FCPROJB] = L * C;
+    s[LNFW] = C;               s[LNFB] = C;
+}
+
+static bool config_ok(const gpt2_config* c) {
+    if (!c) return false;
+    if (c->V < 1 || c->maxT < 1 || c->L < 1 || c->H < 1 || c->C < 4 || c->maxB < 1) return false;
+    if (c->C % 4 || c->C % c->H) return false;
+    int hs = c->C / c->H;
+    if (hs % 4 || hs > 64 || c->C > 2048) return false;
+    if (c->mode != GPT2_MODE_FP32 && c->mode != GPT2_MODE_TF32) return false;
+    if ((long long)c->maxB * c->maxT > (1LL << 30)) return false;
+    return true;
+}
+
+static int padded_vocab(int V) { return (int)round_up((size_t)V, 128); }
+
+struct DevFlags {
+    float loss;
+    int status;
+};
+
+}  // namespace gpt2k
+
+using namespace gpt2k;
+
+struct gpt2 {
+    gpt2_config cfg;
+    int Vp, R;                  // padded vocabulary, activation row capacity
+    size_t nparams, off[NT], sz[NT];
+    float* params;
+    char* ws;
+    size_t ws_bytes;
+    bool owns_ws;
+    cudaStream_t st;
+    float *grads, *m, *v;
+    int *tok, *tgt;
+    DevFlags* flags;
+    // activations; per-layer arrays have a fixed stride of R rows
+    float *x0, *ln1, *ln1_mean, *ln1_rstd, *qkv, *atty, *lse, *res2, *ln2, *ln2_mean, *ln2_rstd;
+    float *fch, *fchg, *res3, *lnf, *lnf_mean, *lnf_rstd, *logits, *losses;
+    // backward buffers
+    float *dres, *dln, *dbig, *datty, *dqkv;
+    void* scratch;
+    size_t scratch_bytes;
+    int B, T;
+    bool fwd_targets, have_grads;
+    int err;
+    // tracing: event pairs recorded around each operation, with its class and launches
+    bool trace_on;
+    std::vector<cudaEvent_t> trace_events;
+    size_t trace_used;
+    std::vector<int> trace_cls;
+    std::vector<long long> trace_launches;
+};
+
+namespace gpt2k {
+
+// Lay out the workspace; with base == nullptr only computes the size.
+static size_t plan(gpt2* m, char* base) {
+    const gpt2_config& c = m->cfg;
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* p = base ? base + off : nullptr;
+        off += round_up(bytes, 256);
+        return p;
+    };
+    auto F = [&](size_t n) { return reinterpret_cast<float*>(take(n * sizeof(float))); };
+    const size_t R = m->R, C = c.C, L = c.L, H = c.H, N = m->nparams;
+    m->grads = F(N);
+    m->m = F(N);
+    m->v = F(N);
+    m->tok = reinterpret_cast<int*>(take(R * sizeof(int)));
+    m->tgt = reinterpret_cast<int*>(take(R * sizeof(int)));
+    m->flags = reinterpret_cast<DevFlags*>(take(sizeof(DevFlags)));
+    m->x0 = F(R * C);
+    m->ln1 = F(L * R * C);
+    m->ln1_mean = F(L * R);
+    m->ln1_rstd = F(L * R);
+    m->qkv = F(L * R * 3 * C);
+    m->atty = F(L * R * C);
+    m->lse = F(L * R * H);
+    m->res2 = F(L * R * C);
+    m->ln2 = F(L * R * C);
+    m->ln2_mean = F(L * R);
+    m->ln2_rstd = F(L * R);
+    m->fch = F(L * R * 4 * C);
+    m->fchg = F(L * R * 4 * C);
+    m->res3 = F(L * R * C);
+    m->lnf = F(R * C);
+    m->lnf_mean = F(R);
+    m->lnf_rstd = F(R);
+    m->logits = F(R * (size_t)m->Vp);
+    m->losses = F(R);
+    m->dres = F(R * C);
+    m->dln = F(R * C);
+    m->dbig = F(R * 4 * C);
+    m->datty = F(R * C);
+    m->dqkv = F(R * 3 * C);
+    // scratch: the largest need of any backward op at full capacity
+    const int Ri = (int)R, Ci = (int)C, mode = c.mode;
+    size_t s = 0;
+    s = std::max(s, gpt2_op_layernorm_backward_scratch_bytes(Ri, Ci));
+    s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, 3 * Ci, mode));
+    s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, Ci, mode));
+    s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, 4 * Ci, mode));
+    s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, 4 * Ci, Ci, mode));
+    s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, c.V, mode));
+    s = std::max(s, gpt2_op_attention_backward_scratch_bytes(c.maxB, c.maxT, c.H));
+    s = std::max(s, gpt2_op_encoder_backward_scratch_bytes(Ri, c.V));
+    s = std::max(s, gpt2_op_bias_grad_scratch_bytes(Ri, 4 * Ci));
+    m->scratch_bytes = s;
+    m->scratch = take(s);
+    return off;
+}
+
+static float* P(gpt2* m, int t) { return m->params + m->off[t]; }
+static float* G(gpt2* m, int t) { return m->grads + m->off[t]; }
+
+// Run one operation; when tracing, bracket it with events on the model's stream.
+static int trace_op(gpt2* m, int cls, const std::function<int()>& f) {
+    if (!m->trace_on) return f();
+    while (m->trace_used + 2 > m->trace_events.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+        m->trace_events.push_back(e);
+    }
+    cudaEvent_t e0 = m->trace_events[m->trace_used], e1 = m->trace_events[m->trace_used + 1];
+    long long n0 = g_launches.load(std::memory_order_relaxed);
+    if (cudaEventRecord(e0, m->st) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+    int rc = f();
+    if (cudaEventRecord(e1, m->st) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+    m->trace_used += 2;
+    m->trace_cls.push_back(cls);
+    m->trace_launches.push_back(g_launches.load(std::memory_order_relaxed) - n0);
+    return rc;
+}
+
+#define OP(cls, call)                                                      \
+    do {                                                                   \
+        int rc_ = trace_op(m, GPT2_TRACE_##cls, [&]() -> int { return (call); }); \
+        if (rc_) return rc_;                                               \
+    } while (0)
+
+static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
+    const gpt2_config& c = m->cfg;
+    const int C = c.C, L = c.L, H = c.H, N = B * T, mode = c.mode;
+    const size_t R = m->R;
+    void* st = m->st;
+    int* status = &m->flags->status;
+    OP(ENCODER_FWD, gpt2_op_encoder_forward(m->x0, m->tok, P(m, WTE), P(m, WPE), B, T, C, c.V, status, st));
+    for (int l = 0; l < L; l++) {
+        const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
+        float* ln1 = m->ln1 + l * R * C;
+        float* qkv = m->qkv + l * R * 3 * C;
+        float* atty = m->atty + l * R * C;
+        float* res2 = m->res2 + l * R * C;
+        float* ln2 = m->ln2 + l * R * C;
+        float* fch = m->fch + l * R * 4 * C;
+        float* fchg = m->fchg + l * R * 4 * C;
+        float* res3 = m->res3 + l * R * C;
+        size_t cc = (size_t)C * C;
+        OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(ln1, m->ln1_mean + l * R, m->ln1_rstd + l * R, x,
+                                       P(m, LN1W) + l * C, P(m, LN1B) + l * C, N, C, st));
+        OP(MATMUL_FWD, gpt2_op_linear_forward(qkv, nullptr, ln1, P(m, QKVW) + l * 3 * cc,
+                                    P(m, QKVB) + l * 3 * C, nullptr, N, C, 3 * C, 3 * C, 0, mode, status, st));
+        OP(ATTENTION_FWD, gpt2_op_attention_forward(atty, m->lse + l * R * H, qkv, B, T, C, H, mode, status, st));
+        OP(MATMUL_FWD, gpt2_op_linear_forward(res2, nullptr, atty, P(m, ATTPROJW) + l * cc,
+                                    P(m, ATTPROJB) + l * C, x, N, C, C, C, 0, mode, status, st));
+        OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(ln2, m->ln2_mean + l * R, m->ln2_rstd + l * R, res2,
+                                       P(m, LN2W) + l * C, P(m, LN2B) + l * C, N, C, st));
+        OP(MATMUL_FWD, gpt2_op_linear_forward(fchg, fch, ln2, P(m, FCW) + l * 4 * cc, P(m, FCB) + l * 4 * C,
+                                    nullptr, N, C, 4 * C, 4 * C, GPT2_LINEAR_GELU, mode, status, st));
+        OP(MATMUL_FWD, gpt2_op_linear_forward(res3, nullptr, fchg, P(m, FCPROJW) + l * 4 * cc,
+                                    P(m, FCPROJB) + l * C, res2, N, 4 * C, C, C, 0, mode, status, st));
+    }
+    const float* xL = m->res3 + (size_t)(L - 1) * R * C;
+    OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(m->lnf, m->lnf_mean, m->lnf_rstd, xL, P(m, LNFW), P(m, LNFB),
+                                   N, C, st));
+    OP(MATMUL_FWD, gpt2_op_linear_forward(m->logits, nullptr, m->lnf, P(m, WTE), nullptr, nullptr, N, C, c.V,
+                                m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
+    if (with_targets) {
+        OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->tgt, N, c.V, m->Vp, 1.0f / (float)N,
+                                  status, st));
+        OP(CROSSENTROPY, gpt2_op_sum(&m->flags->loss, m->losses, N, 1.0f / (float)N, st));
+    }
+    return GPT2_OK;
+}
+
+static int backward_impl(gpt2* m) {
+    const gpt2_config& c = m->cfg;
+    const int B = m->B, T = m->T, C = c.C, L = c.L, H = c.H, N = B * T, mode = c.mode;
+    const size_t R = m->R, cc = (size_t)C * C;
+    void* st = m->st;
+    void* sc = m->scratch;
+    const size_t sb = m->scratch_bytes;
+    int* status = &m->flags->status;
+    // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
+    OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->logits, P(m, WTE), nullptr, N, C, c.V, m->Vp,
+                                       mode, status, st));
+    OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, WTE), nullptr, m->logits, m->lnf, N, C, c.V, m->Vp,
+                                        sc, sb, mode, status, st));
+    OP(OTHER, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), m->st) == cudaSuccess
+                  ? GPT2_OK : GPT2_ECUDA);
+    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LNFW), G(m, LNFB), m->dln,
+                                    m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW), m->lnf_mean,
+                                    m->lnf_rstd, N, C, sc, sb, st));
+    for (int l = L - 1; l >= 0; l--) {
+        const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
+        const float* ln1 = m->ln1 + l * R * C;
+        const float* qkv = m->qkv + l * R * 3 * C;
+        const float* atty = m->atty + l * R * C;
+        const float* res2 = m->res2 + l * R * C;
+        const float* ln2 = m->ln2 + l * R * C;
+        const float* fch = m->fch + l * R * 4 * C;
+        const float* fchg = m->fchg + l * R * 4 * C;
+        // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g; dbfp
+        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dbig, m->dres, P(m, FCPROJW) + l * 4 * cc, fch, N,
+                                           4 * C, C, C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, nullptr, m->dres, fchg, N, 4 * C, C,
+                                                              C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, FCPROJB) + l * C, m->dres, N, C, C, sc, sb, st));
+        // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
+        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->dbig, P(m, FCW) + l * 4 * cc, nullptr, N, C,
+                                           4 * C, 4 * C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, FCW) + l * 4 * cc, nullptr, m->dbig, ln2, N, C, 4 * C,
+                                                              4 * C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, FCB) + l * 4 * C, m->dbig, N, 4 * C, 4 * C, sc, sb, st));
+        // ln_2: dres += LN'(dln2)
+        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LN2W) + l * C, G(m, LN2B) + l * C, m->dln,
+                                        res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
+                                        m->ln2_rstd + l * R, N, C, sc, sb, st));
+        // attention c_proj
+        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->datty, m->dres, P(m, ATTPROJW) + l * cc, nullptr, N,
+                                           C, C, C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, ATTPROJW) + l * cc, nullptr, m->dres, atty, N, C, C,
+                                                              C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, ATTPROJB) + l * C, m->dres, N, C, C, sc, sb, st));
+        // attention
+        OP(ATTENTION_BWD, gpt2_op_attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C,
+                                        H, sc, sb, mode, status, st));
+        // c_attn
+        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->dqkv, P(m, QKVW) + l * 3 * cc, nullptr, N, C,
+                                           3 * C, 3 * C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, QKVW) + l * 3 * cc, nullptr, m->dqkv, ln1, N, C, 3 * C,
+                                                              3 * C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, QKVB) + l * 3 * C, m->dqkv, N, 3 * C, 3 * C, sc, sb, st));
+        // ln_1: dres += LN'(dln1)
+        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LN1W) + l * C, G(m, LN1B) + l * C, m->dln, x,
+                                        P(m, LN1W) + l * C, m->ln1_mean + l * R,
+                                        m->ln1_rstd + l * R, N, C, sc, sb, st));
+    }
+    OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V, sc,
+                                  sb, st));
+    return GPT2_OK;
+}
+
+static void record(gpt2* m, int rc) {
+    if (rc && !m->err) m->err = rc;
+}
+
+}  // namespace gpt2k
+
+// ============================================================================
+// C ABI
+// ============================================================================
+
+GPT2_API size_t gpt2_num_params(const gpt2_config* cfg) {
+    if (!config_ok(cfg)) return 0;
+    size_t s[NT], n = 0;
+    tensor_sizes(*cfg, s);
+    for (int i = 0; i < NT; i++) n += s[i];
+    return n;
+}
+
+GPT2_API size_t gpt2_workspace_bytes(const gpt2_config* cfg) {
+    if (!config_ok(cfg)) return 0;
+    gpt2 tmp{};
+    tmp.cfg = *cfg;
+    tmp.Vp = padded_vocab(cfg->V);
+    tmp.R = cfg->maxB * cfg->maxT;
+    tmp.nparams = gpt2_num_params(cfg);
+    return plan(&tmp, nullptr);
+}
+
+GPT2_API int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out) {
+    if (out) *out = nullptr;
+    if (!out || !config_ok(cfg) || !params || !aligned16(params)) return GPT2_EINVAL;
+    gpt2* m = new (std::nothrow) gpt2{};
+    if (!m) return GPT2_ENOMEM;
+    m->cfg = *cfg;
+    m->Vp = padded_vocab(cfg->V);
+    m->R = cfg->maxB * cfg->maxT;
+    m->nparams = gpt2_num_params(cfg);
+    tensor_sizes(*cfg, m->sz);
+    size_t o = 0;
+    for (int i = 0; i < NT; i++) { m->off[i] = o; o += m->sz[i]; }
+    m->params = params;
+    m->st = as_stream(cfg->stream);
+    size_t need = plan(m, nullptr);
+    if (cfg->workspace) {
+        if (cfg->workspace_bytes < need || !aligned16(cfg->workspace)) { delete m; return GPT2_ENOMEM; }
+        m->ws = reinterpret_cast<char*>(cfg->workspace);
+        m->owns_ws = false;
+    } else {
+        if (cudaMalloc(&m->ws, need) != cudaSuccess) { (void)cudaGetLastError(); delete m; return GPT2_ENOMEM; }
+        m->owns_ws = true;
+    }
+    m->ws_bytes = need;
+    plan(m, m->ws);
+    bool ok = cudaMemsetAsync(m->m, 0, m->nparams * sizeof(float), m->st) == cudaSuccess &&
+              cudaMemsetAsync(m->v, 0, m->nparams * sizeof(float), m->st) == cudaSuccess &&
+              cudaMemsetAsync(m->flags, 0, sizeof(DevFlags), m->st) == cudaSuccess;
+    if (!ok) {
+        (void)cudaGetLastError();
+        if (m->owns_ws) cudaFree(m->ws);
+        delete m;
+        return GPT2_ECUDA;
+    }
+    *out = m;
+    return GPT2_OK;
+}
+
+GPT2_API float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int B, int T) {
+    if (!m) return NAN;
+    if (!tokens || B < 1 || T < 1 || B > m->cfg.maxB || T > m->cfg.maxT) {
+        record(m, GPT2_EINVAL);
+        return NAN;
+    }
+    size_t nb = (size_t)B * T * sizeof(int);
+    m->fwd_targets = false;
+    m->have_grads = false;
+    int crc = trace_op(m, GPT2_TRACE_OTHER, [&]() -> int {
+        bool ok = cudaMemcpyAsync(m->tok, tokens, nb, cudaMemcpyDefault, m->st) == cudaSuccess &&
+                  (!targets ||
+                   cudaMemcpyAsync(m->tgt, targets, nb, cudaMemcpyDefault, m->st) == cudaSuccess) &&
+                  cudaMemsetAsync(m->flags, 0, sizeof(DevFlags), m->st) == cudaSuccess;
+        if (!ok) (void)cudaGetLastError();
+        return ok ? GPT2_OK : GPT2_ECUDA;
+    });
+    if (crc) {
+        record(m, crc);
+        return NAN;
+    }
+    m->B = B;
+    m->T = T;
+    int rc = forward_impl(m, B, T, targets != nullptr);
+    if (rc) { record(m, rc); return NAN; }
+    DevFlags h{};
+    if (cudaMemcpyAsync(&h, m->flags, sizeof(h), cudaMemcpyDeviceToHost, m->st) != cudaSuccess ||
+        cudaStreamSynchronize(m->st) != cudaSuccess) {
+        (void)cudaGetLastError();
+        record(m, GPT2_ECUDA);
+        return NAN;
+    }
+    if (h.status & (GPT2_STATUS_BAD_TOKEN | GPT2_STATUS_BAD_TARGET)) {
+        record(m, GPT2_ETOKEN);
+        return NAN;
+    }
+    if (h.status & GPT2_STATUS_TIMEOUT) {
+        record(m, GPT2_ETIMEOUT);
+        return NAN;
+    }
+    if (!targets) return NAN;
+    m->fwd_targets = true;
+    return h.loss;
+}
+
+GPT2_API int gpt2_backward(gpt2* m) {
+    if (!m) return GPT2_EINVAL;
+    if (!m->fwd_targets) { record(m, GPT2_ESTATE); return GPT2_ESTATE; }
+    int rc = backward_impl(m);
+    if (rc) { record(m, rc); return rc; }
+    m->fwd_targets = false;     // dlogits were consumed; a new forward is needed
+    m->have_grads = true;
+    return GPT2_OK;
+}
+
+GPT2_API int gpt2_adamw(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t) {
+    if (!m) return GPT2_EINVAL;
+    if (t < 1) { record(m, GPT2_EINVAL); return GPT2_EINVAL; }
+    if (!m->have_grads) { record(m, GPT2_ESTATE); return GPT2_ESTATE; }
+    float bc1 = (float)(1.0 - pow((double)b1, (double)t));
+    float bc2 = (float)(1.0 - pow((double)b2, (double)t));
+    // consecutive tensors with the same decay setting share one launch
+    int i = 0;
+    while (i < NT) {
+        int j = i;
+        size_t n = 0;
+        while (j < NT && kDecay[j] == kDecay[i]) n += m->sz[j++];
+        int rc = trace_op(m, GPT2_TRACE_ADAMW, [&]() -> int {
+            return gpt2_op_adamw(m->params + m->off[i], m->grads + m->off[i], m->m + m->off[i],
+                                 m->v + m->off[i], n, lr, b1, b2, eps, kDecay[i] ? wd : 0.f, bc1,
+                                 bc2, m->st);
+        });
+        if (rc) { record(m, rc); return rc; }
+        i = j;
+    }
+    return GPT2_OK;
+}
+
+GPT2_API int gpt2_destroy(gpt2* m) {
+    if (!m) return GPT2_OK;
+    int rc = GPT2_OK;
+    if (cudaStreamSynchronize(m->st) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    if (m->owns_ws && cudaFree(m->ws) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    for (cudaEvent_t e : m->trace_events) cudaEventDestroy(e);
+    delete m;
+    return rc;
+}
+
+GPT2_API int gpt2_status(gpt2* m) {
+    if (!m) return GPT2_EINVAL;
+    DevFlags h{};
+    if (cudaStreamSynchronize(m->st) != cudaSuccess ||
+        cudaMemcpy(&h, m->flags, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        (void)cudaGetLastError();
+        record(m, GPT2_ECUDA);
+    }
+    if (h.status & (GPT2_STATUS_BAD_TOKEN | GPT2_STATUS_BAD_TARGET)) record(m, GPT2_ETOKEN);
+    if (h.status & GPT2_STATUS_TIMEOUT) record(m, GPT2_ETIMEOUT);
+    int rc = m->err;
+    m->err = GPT2_OK;
+    if (h.status) cudaMemsetAsync(&m->flags->status, 0, sizeof(int), m->st);
+    return rc;
+}
+
+GPT2_API const char* gpt2_strerror(int code) {
+    switch (code) {
+        case GPT2_OK: return "ok";
+        case GPT2_EINVAL: return "invalid argument, configuration or shape";
+        case GPT2_ENOMEM: return "workspace too small or allocation failed";
+        case GPT2_ECUDA: return "CUDA runtime error";
+        case GPT2_ETOKEN: return "token or target id outside [0, V)";
+        case GPT2_ESTATE: return "calls out of order";
+        case GPT2_ETIMEOUT: return "bounded device wait timed out";
+        case GPT2_ENOTSUP: return "mode or shape not supported";
+        default: return "unknown status";
+    }
+}
+
+GPT2_API const float* gpt2_grads(gpt2* m) { return m ? m->grads : nullptr; }
+GPT2_API float* gpt2_adam_m(gpt2* m) { return m ? m->m : nullptr; }
+GPT2_API float* gpt2_adam_v(gpt2* m) { return m ? m->v : nullptr; }
+GPT2_API const float* gpt2_logits(gpt2* m, int* row_stride) {
+    if (!m) return nullptr;
+    if (row_stride) *row_stride = m->Vp;
+    return m->logits;
+}
+GPT2_API const float* gpt2_losses(gpt2* m) { return m ? m->losses : nullptr; }
+
+GPT2_API const float* gpt2_activation(gpt2* m, int which, int layer) {
+    if (!m || layer < 0 || layer >= m->cfg.L) return nullptr;
+    const size_t R = m->R, C = m->cfg.C, l = layer;
+    switch (which) {
+        case 0: return m->x0;
+        case 1: return m->ln1 + l * R * C;
+        case 2: return m->qkv + l * R * 3 * C;
+        case 3: return m->atty + l * R * C;
+        case 4: return m->res2 + l * R * C;
+        case 5: return m->ln2 + l * R * C;
+        case 6: return m->fch + l * R * 4 * C;
+        case 7: return m->fchg + l * R * 4 * C;
+        case 8: return m->res3 + l * R * C;
+        case 9: return m->lnf;
+        default: return nullptr;
+    }
+}
+
+GPT2_API int gpt2_trace_enable(gpt2* m, int on) {
+    if (!m) return GPT2_EINVAL;
+    m->trace_on = on != 0;
+    m->trace_used = 0;
+    m->trace_cls.clear();
+    m->trace_launches.clear();
+    return GPT2_OK;
+}
+
+GPT2_API int gpt2_trace_read(gpt2* m, double* ms, long long* launches, int n) {
+    if (!m || n < 0) return GPT2_EINVAL;
+    if (cudaStreamSynchronize(m->st) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+    for (int c = 0; c < n; c++) {
+        if (ms) ms[c] = 0.0;
+        if (launches) launches[c] = 0;
+    }
+    int rc = GPT2_OK;
+    for (size_t i = 0; i < m->trace_cls.size(); i++) {
+        int c = m->trace_cls[i];
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, m->trace_events[2 * i], m->trace_events[2 * i + 1]) != cudaSuccess) {
+            (void)cudaGetLastError();
+            rc = GPT2_ECUDA;
+        }
+        if (c < n) {
+            if (ms) ms[c] += t;
+            if (launches) launches[c] += m->trace_launches[i];
+        }
+    }
+    m->trace_used = 0;
+    m->trace_cls.clear();
+    m->trace_launches.clear();
+    return rc;
+}
+
+GPT2_API long long gpt2_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -96,8 +96,15 @@ def tensor_offsets(cfg):
     return out
 
 
-def init_params(cfg, seed=None):
-    """Flat float32 parameter array in the 16-tensor layout."""
+ZERO_INIT = ("ln1b", "qkvb", "attprojb", "ln2b", "fcb", "fcprojb", "lnfb")
+
+
+def init_params(cfg, seed=None, perturbed=False):
+    """Flat float32 parameter array in the 16-tensor layout.
+
+    perturbed=True additionally draws the biases and LayerNorm shifts from
+    N(0, 0.02) and the LayerNorm gains from 1 + N(0, 0.02), so no tensor starts
+    at an exact constant (a parameter state reached after some training)."""
     rng = np.random.Generator(np.random.PCG64(cfg.param_seed if seed is None else seed))
     shapes = tensor_shapes(cfg)
     out = np.empty(num_params(cfg), dtype=np.float32)
@@ -110,8 +117,12 @@ def init_params(cfg, seed=None):
             seg[:] = rng.standard_normal(n, dtype=np.float32) * np.float32(resid_std)
         elif name in ("ln1w", "ln2w", "lnfw"):
             seg[:] = 1.0
+            if perturbed:
+                seg += rng.standard_normal(n, dtype=np.float32) * np.float32(0.02)
         else:
             seg[:] = 0.0
+            if perturbed:
+                seg[:] = rng.standard_normal(n, dtype=np.float32) * np.float32(0.02)
         assert seg.size == int(np.prod(shapes[name]))
     return out
 

@@ -1,0 +1,181 @@
+/*
+ * gpt2.h -- C ABI of one GPT-2 decoder training step on a B300 (sm_103a).
+ *
+ * The step: token + position encoder, L pre-norm blocks (LayerNorm, fused QKV
+ * projection, causal multi-head self-attention, output projection, residual,
+ * LayerNorm, c_fc, tanh-GELU, c_proj, residual), final LayerNorm, logits
+ * through the transposed token embedding (tied lm_head, no bias), and the
+ * mean softmax cross-entropy; then the backward pass of every layer and an
+ * AdamW update.  Architecture: "GPT-2 from scratch with torch" (Posit blog),
+ * sections 总体架构, Transformer block, 自注意力, 前馈网络（MLP）, 输出.
+ * Training loop and per-layer hand-written backward: "1000 行 C 代码完成 GPT-2
+ * 训练的 LLM.c" (bigegpt.com).
+ *
+ * Conventions
+ *   - All pointers marked "device" point to CUDA device memory of the current
+ *     device; "host" pointers to host memory.  Pointers marked "device or host"
+ *     accept either (copied with cudaMemcpyDefault; pinned host memory keeps
+ *     the copy asynchronous).
+ *   - Every call is ordered on the stream given in gpt2_config.stream (NULL:
+ *     the legacy default stream) and is asynchronous, except gpt2_forward,
+ *     which reads back the mean loss (one 4-byte device-to-host copy).
+ *   - Floating point data is IEEE fp32.  Token ids are int32.
+ *   - Functions returning int return GPT2_OK (0) or a negative GPT2_E* code.
+ *     No function aborts, throws, or traps on the device: device-side checks
+ *     (token ids out of range, bounded waits) raise bits in a status word that
+ *     the next synchronising call reports.
+ */
+#ifndef GPT2_B300_H
+#define GPT2_B300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define GPT2_OK        0
+#define GPT2_EINVAL   -1   /* bad configuration, shape or argument             */
+#define GPT2_ENOMEM   -2   /* workspace too small or allocation failed         */
+#define GPT2_ECUDA    -3   /* a CUDA runtime call failed                        */
+#define GPT2_ETOKEN   -4   /* a token or target id outside [0, V)               */
+#define GPT2_ESTATE   -5   /* calls out of order (backward before a forward
+                              with targets, adamw before backward)              */
+#define GPT2_ETIMEOUT -6   /* a bounded device wait gave up                     */
+#define GPT2_ENOTSUP  -7   /* mode or shape not supported on this device        */
+
+/* arithmetic modes for the contractions (GEMMs and attention) */
+#define GPT2_MODE_FP32 0   /* strict fp32 on the CUDA cores                     */
+#define GPT2_MODE_TF32 1   /* tensor cores: tf32 operands, fp32 accumulation    */
+
+typedef struct {
+    int V;           /* vocabulary size (50257 for GPT-2)                       */
+    int maxT;        /* context length, rows of the position table (1024)       */
+    int L;           /* number of blocks                                        */
+    int H;           /* attention heads; C % H == 0                             */
+    int C;           /* channels; C % 4 == 0                                    */
+    int maxB;        /* largest batch a forward may pass (activation capacity)  */
+    int mode;        /* GPT2_MODE_*                                             */
+    void* workspace; /* device memory of at least gpt2_workspace_bytes(cfg)
+                        bytes, owned by the caller and kept alive until
+                        gpt2_destroy; NULL: the library allocates its own       */
+    size_t workspace_bytes;
+    void* stream;    /* cudaStream_t for every launch; NULL: default stream     */
+} gpt2_config;
+
+typedef struct gpt2 gpt2;
+
+/* Number of fp32 parameters in the flat layout below (124,439,808 for GPT-2
+ * 124M, matching the llm.c run log on bigegpt.com).  0 for an invalid config.
+ *
+ * Flat parameter layout (sixteen tensors, contiguous, in this order; linear
+ * weights are [out, in]):
+ *   wte[V,C] wpe[maxT,C] ln1w[L,C] ln1b[L,C] qkvw[L,3C,C] qkvb[L,3C]
+ *   attprojw[L,C,C] attprojb[L,C] ln2w[L,C] ln2b[L,C] fcw[L,4C,C] fcb[L,4C]
+ *   fcprojw[L,C,4C] fcprojb[L,C] lnfw[C] lnfb[C]
+ * Gradients and both AdamW moments use the same layout. */
+size_t gpt2_num_params(const gpt2_config* cfg);
+
+/* Bytes of device workspace the model needs: gradients, AdamW moments,
+ * activations for maxB*maxT rows, logits, and scratch.  0 for an invalid cfg. */
+size_t gpt2_workspace_bytes(const gpt2_config* cfg);
+
+/* Create a model over caller-owned parameters.
+ *   cfg:    validated (C % H == 0, C % 4 == 0, head size <= 128, V, L, maxT,
+ *           maxB >= 1); copied.
+ *   params: device, gpt2_num_params(cfg) floats, 16-byte aligned; owned by the
+ *           caller, read by forward/backward and updated in place by adamw.
+ *   out:    receives the handle; *out is NULL on error.
+ * Zeroes both AdamW moments.  Errors: EINVAL, ENOMEM, ECUDA, ENOTSUP. */
+int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out);
+
+/* Forward pass on tokens[B,T] (device or host int32, row-major), 1 <= B <= maxB,
+ * 1 <= T <= maxT.  targets[B,T] (device or host int32, or NULL): the next-token
+ * ids.  With targets, returns the mean cross-entropy over the B*T positions
+ * (natural log) and leaves d(loss)/d(logits) in the logits buffer for the
+ * backward; without targets, keeps the logits and returns NaN.  The inputs are
+ * copied into the workspace, so the caller may reuse its buffers at once.
+ * Returns NaN on error; gpt2_status() then gives the code (EINVAL, ETOKEN,
+ * ECUDA).  Synchronises the stream once to read the loss. */
+float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int B, int T);
+
+/* Backward pass of the last forward (which must have had targets).
+ * Overwrites the gradient buffer (no accumulation across calls); gradients
+ * are those of the mean loss.  Errors: ESTATE, ECUDA. */
+int gpt2_backward(gpt2* m);
+
+/* AdamW update of the parameters in place from the current gradients, step
+ * t >= 1 (bias correction 1-b1^t, 1-b2^t):
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p -= lr * ( (m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) + wd_i * p )
+ * with wd_i = wd on the 2-D tensors (wte, wpe, qkvw, attprojw, fcw, fcprojw)
+ * and 0 elsewhere.  Errors: EINVAL (t < 1), ESTATE (no backward yet), ECUDA. */
+int gpt2_adamw(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t);
+
+/* Release the model (and its workspace if the library allocated it).
+ * Synchronises the stream.  NULL is accepted. */
+int gpt2_destroy(gpt2* m);
+
+/* Synchronise the stream and return the first error seen by this model
+ * (including device-side status bits), then clear it. */
+int gpt2_status(gpt2* m);
+
+/* Static description of a status code. */
+const char* gpt2_strerror(int code);
+
+/* Accessors: device pointers into the workspace, valid until gpt2_destroy.
+ * gpt2_grads / gpt2_adam_m / gpt2_adam_v: gpt2_num_params floats, flat layout.
+ * gpt2_logits: [B*T, row_stride] floats of the last forward; row_stride is the
+ * vocabulary padded to a multiple of 128 and written to *row_stride.  Columns
+ * >= V hold 0.  After a forward WITH targets the buffer holds d(loss)/d(logits)
+ * instead (padded columns 0).  gpt2_losses: the B*T per-position losses. */
+const float* gpt2_grads(gpt2* m);
+float* gpt2_adam_m(gpt2* m);
+float* gpt2_adam_v(gpt2* m);
+const float* gpt2_logits(gpt2* m, int* row_stride);
+const float* gpt2_losses(gpt2* m);
+
+/* Activation access for checks: device pointer to activation `which` of
+ * block `layer` from the last forward, rows B*T of the given width:
+ *   0 encoder output [C]   1 ln_1 output [C]   2 qkv [3C]   3 attention out [C]
+ *   4 residual after attention [C]   5 ln_2 output [C]   6 c_fc output [4C]
+ *   7 GELU output [4C]   8 block output [C]   9 ln_f output [C]
+ * NULL for an invalid index. */
+const float* gpt2_activation(gpt2* m, int which, int layer);
+
+/* ---- tracing -------------------------------------------------------------
+ * Per-kernel-class timing with CUDA events recorded on the model's stream
+ * around every operation of the step (off by default; the events cost about
+ * a microsecond of host time each).  Classes: */
+#define GPT2_TRACE_ENCODER_FWD      0
+#define GPT2_TRACE_LAYERNORM_FWD    1
+#define GPT2_TRACE_MATMUL_FWD       2   /* every linear layer's forward GEMM      */
+#define GPT2_TRACE_ATTENTION_FWD    3
+#define GPT2_TRACE_CROSSENTROPY     4   /* fused softmax-CE and the loss sum      */
+#define GPT2_TRACE_MATMUL_BWD_INPUT 5   /* dX GEMMs                               */
+#define GPT2_TRACE_MATMUL_BWD_WEIGHT 6  /* dW GEMMs and their split-K sums          */
+#define GPT2_TRACE_LAYERNORM_BWD    7
+#define GPT2_TRACE_ATTENTION_BWD    8
+#define GPT2_TRACE_ENCODER_BWD      9
+#define GPT2_TRACE_ADAMW           10
+#define GPT2_TRACE_OTHER           11   /* input copies and memsets               */
+#define GPT2_TRACE_BIAS_GRAD       12   /* column sums for the bias gradients     */
+#define GPT2_TRACE_CLASSES         13
+
+/* Turn tracing on (1) or off (0); turning it on discards earlier records. */
+int gpt2_trace_enable(gpt2* m, int on);
+
+/* Synchronise the stream, then write, for each of the first n classes, the
+ * summed device milliseconds (ms[c]) and the number of kernel launches
+ * (launches[c]) recorded since the last read; the records are then cleared.
+ * ms and launches are host arrays of at least n entries (either may be NULL). */
+int gpt2_trace_read(gpt2* m, double* ms, long long* launches, int n);
+
+/* Total number of kernels this library has launched in the process so far. */
+long long gpt2_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_H */

@@ -1,0 +1,141 @@
+/*
+ * gpt2_ops.h -- the individual kernels of the GPT-2 training step, callable on
+ * caller-owned device buffers.  gpt2.h chains exactly these operations; they
+ * are exported so each one can be checked and timed on its own.
+ *
+ * Common rules
+ *   - Every pointer is a device pointer unless marked otherwise; the caller
+ *     owns all buffers.  Float buffers used with 128-bit accesses (noted
+ *     "16B") must be 16-byte aligned with row strides that are multiples of 4.
+ *   - `stream` is a cudaStream_t (NULL: the default stream).  Every call is
+ *     asynchronous on it.  Return value: GPT2_OK or a negative GPT2_E* code for
+ *     argument errors or a failed launch.  Device-side data errors (ids
+ *     outside [0, V)) OR a GPT2_STATUS_* bit into *status when status != NULL.
+ *   - `mode` selects the contraction arithmetic: GPT2_MODE_FP32 (CUDA cores)
+ *     or GPT2_MODE_TF32 (tcgen05 tensor cores, fp32 accumulation).  In TF32
+ *     mode a product whose operands the tensor-memory-access unit cannot read
+ *     (a base address not 16-byte aligned, a row stride not a multiple of 4)
+ *     runs on the CUDA cores instead; the model's own buffers never do.
+ *   - A tensor-core kernel whose pipeline wait exceeds one second gives up,
+ *     sets GPT2_STATUS_TIMEOUT in *status and returns without faulting.
+ */
+#ifndef GPT2_B300_OPS_H
+#define GPT2_B300_OPS_H
+
+#include <stddef.h>
+#include "gpt2.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* device status bits */
+#define GPT2_STATUS_BAD_TOKEN   1
+#define GPT2_STATUS_BAD_TARGET  2
+#define GPT2_STATUS_TIMEOUT     4
+
+/* Encoder: x[b,t,:] = wte[tok[b,t],:] + wpe[t,:]  ("GPT-2 from scratch with
+ * torch", section 从词到编码).  tok [B*T] int32; wte [V,C], wpe [>=T,C],
+ * x [B*T,C] (16B).  An id outside [0,V) writes zeros and sets BAD_TOKEN. */
+int gpt2_op_encoder_forward(float* x, const int* tok, const float* wte, const float* wpe,
+                            int B, int T, int C, int V, int* status, void* stream);
+
+/* Encoder backward, deterministic.  dwte[v,:] += sum over positions with
+ * tok == v of dx[pos,:], summed in ascending position order; dwpe[t,:] =
+ * sum_b dx[b,t,:] for t < T (rows t >= T of dwpe are set to 0; dwpe has maxT
+ * rows).  scratch: gpt2_op_encoder_backward_scratch_bytes(B*T, V) bytes. */
+size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V);
+int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx, const int* tok,
+                             int B, int T, int maxT, int C, int V, void* scratch,
+                             size_t scratch_bytes, void* stream);
+
+/* LayerNorm over rows of x [N,C] (16B): mean, rstd = 1/sqrt(var + 1e-5)
+ * (biased variance), y = (x-mean)*rstd*w + b.  mean, rstd [N] are saved for
+ * the backward.  ("GPT-2 from scratch with torch", Transformer block, eps 1e-5.) */
+int gpt2_op_layernorm_forward(float* y, float* mean, float* rstd, const float* x,
+                              const float* w, const float* b, int N, int C, void* stream);
+
+/* LayerNorm backward.  dx += rstd*(g - mean(g) - xhat*mean(g*xhat)) with
+ * g = dy*w and xhat = (x-mean)*rstd (dx is ACCUMULATED: it is the residual
+ * stream's gradient); dw = sum_rows dy*xhat, db = sum_rows dy (OVERWRITTEN),
+ * reduced in a fixed order.  scratch: gpt2_op_layernorm_backward_scratch_bytes. */
+size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C);
+int gpt2_op_layernorm_backward(float* dx, float* dw, float* db, const float* dy,
+                               const float* x, const float* w, const float* mean,
+                               const float* rstd, int N, int C, void* scratch,
+                               size_t scratch_bytes, void* stream);
+
+/* Linear forward: out[n,o] = sum_i inp[n,i]*w[o,i] + bias[o] (w is [OC,IC]).
+ *   bias: [OC] or NULL.  residual: [N,ld_out] or NULL -> out = residual + ...
+ *   (residual may alias out).  flags & GPT2_LINEAR_GELU: the sum (+bias) goes
+ *   to out_pre [N,ld_out] and out = gelu_tanh(out_pre).
+ *   inp [N,IC] row stride IC; out row stride ld_out >= OC.  Columns o >= OC of
+ *   out (up to ld_out) are written with 0 when flags & GPT2_LINEAR_ZERO_PAD. */
+#define GPT2_LINEAR_GELU      1
+#define GPT2_LINEAR_ZERO_PAD  2
+int gpt2_op_linear_forward(float* out, float* out_pre, const float* inp, const float* w,
+                           const float* bias, const float* residual, int N, int IC, int OC,
+                           int ld_out, int flags, int mode, int* status, void* stream);
+
+/* Linear backward, input side: dinp[n,i] = sum_o dout[n,o]*w[o,i]  (OVERWRITES
+ * dinp [N,IC]).  dout row stride ld_dout >= OC (columns >= OC are ignored).
+ * gelu_x [N,IC] or NULL: dinp is multiplied by gelu_tanh'(gelu_x) (the GELU that
+ * produced this layer's input). */
+int gpt2_op_linear_backward_input(float* dinp, const float* dout, const float* w,
+                                  const float* gelu_x, int N, int IC, int OC, int ld_dout,
+                                  int mode, int* status, void* stream);
+
+/* Linear backward, weight side: dw[o,i] = sum_n dout[n,o]*inp[n,i] and, when
+ * dbias != NULL, dbias[o] = sum_n dout[n,o]; both OVERWRITTEN and reduced in a
+ * fixed order.  scratch: gpt2_op_linear_backward_weight_scratch_bytes. */
+size_t gpt2_op_linear_backward_weight_scratch_bytes(int N, int IC, int OC, int mode);
+int gpt2_op_linear_backward_weight(float* dw, float* dbias, const float* dout,
+                                   const float* inp, int N, int IC, int OC, int ld_dout,
+                                   void* scratch, size_t scratch_bytes, int mode, int* status,
+                                   void* stream);
+
+/* Bias gradient alone: db[o] = sum_n dout[n*ld_dout + o] for o < OC,
+ * OVERWRITTEN, summed in a fixed order (row chunks, then chunk order).
+ * scratch: gpt2_op_bias_grad_scratch_bytes(N, OC) bytes. */
+size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC);
+int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int ld_dout, void* scratch,
+                      size_t scratch_bytes, void* stream);
+
+/* Causal self-attention forward over qkv [B,T,3C] (queries, keys, values at
+ * column offsets 0, C, 2C; head h owns columns h*hs..h*hs+hs-1 of each):
+ * per (b,h), O = softmax(mask(Q K^T / sqrt(hs))) V, heads side by side in
+ * y [B,T,C]; lse [B,H,T] receives the row log-sum-exp of the scaled scores.
+ * ("GPT-2 from scratch with torch", section 自注意力.)  hs <= 128, hs % 4 == 0. */
+int gpt2_op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C,
+                              int H, int mode, int* status, void* stream);
+
+/* Causal self-attention backward: dqkv [B,T,3C] (OVERWRITTEN) from dy [B,T,C],
+ * the forward's qkv, y and lse.  scratch: gpt2_op_attention_backward_scratch_bytes. */
+size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
+int gpt2_op_attention_backward(float* dqkv, const float* dy, const float* qkv, const float* y,
+                               const float* lse, int B, int T, int C, int H, void* scratch,
+                               size_t scratch_bytes, int mode, int* status, void* stream);
+
+/* Fused softmax cross-entropy over logits z [N, ld] (16B, ld % 4 == 0, ld >= V):
+ * losses[n] = logsumexp(z[n,:V]) - z[n,tgt[n]]; then, IN PLACE,
+ * z[n,v] = (softmax(z[n,:V])[v] - [v == tgt[n]]) * dscale for v < V and 0 for
+ * V <= v < ld.  dscale is 1/(number of positions) for the mean loss; 0 skips
+ * the gradient (z is left unchanged).  A target outside [0,V) sets BAD_TARGET
+ * and that row's loss and gradient to 0.  ("从头搭建GPT 笔记", section 计算loss.) */
+int gpt2_op_crossentropy(float* losses, float* z, const int* tgt, int N, int V, int ld,
+                         float dscale, int* status, void* stream);
+
+/* Sum of losses[N] in a fixed order, times `scale`, written to *out (device). */
+int gpt2_op_sum(float* out, const float* losses, int N, float scale, void* stream);
+
+/* AdamW over n parameters (16B; n % 4 == 0), bias corrections passed in:
+ * m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+ * p -= lr * ((m/bc1) / (sqrt(v/bc2) + eps) + wd * p). */
+int gpt2_op_adamw(float* p, const float* g, float* m, float* v, size_t n, float lr,
+                  float b1, float b2, float eps, float wd, float bc1, float bc2,
+                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_OPS_H */

@@ -1,0 +1,89 @@
+"""The C-ABI library loads, exports every symbol the headers declare, and its
+host-only calls work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from gpt_decoder_step_train_b300 import synthetic as syn
+
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"\b(gpt2_[a-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gpt_decoder_step_train_b300 import binding
+    return binding.lib()
+
+
+def test_headers_declare_the_four_step_calls():
+    names = declared_functions()
+    for n in ("gpt2_create", "gpt2_forward", "gpt2_backward", "gpt2_adamw"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in sorted(declared_functions()) if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    from gpt_decoder_step_train_b300 import binding
+    assert declared_functions() == set(binding.SIGNATURES)
+
+
+def test_library_links_no_oracle_code():
+    from gpt_decoder_step_train_b300 import binding
+    data = open(binding.LIB_PATH, "rb").read()
+    assert b"oracle_" not in data
+
+
+@pytest.mark.parametrize("name", list(syn.CONFIGS))
+def test_num_params_matches_layout(L, name):
+    from gpt_decoder_step_train_b300 import binding
+    cfg = syn.CONFIGS[name]
+    c = binding.make_config(cfg)
+    assert L.gpt2_num_params(ctypes.byref(c)) == syn.num_params(cfg)
+    ws = L.gpt2_workspace_bytes(ctypes.byref(c))
+    # at least gradients and both moments, well inside one B300's memory
+    assert 3 * 4 * syn.num_params(cfg) < ws < 200 * 2**30
+
+
+def test_invalid_configs_are_rejected(L):
+    from gpt_decoder_step_train_b300 import binding
+    cfg = syn.CONFIGS["tiny"]
+    for bad in (dict(H=3), dict(C=62, H=2), dict(V=0), dict(L=0), dict(maxT=0)):
+        c = binding.make_config(cfg.with_(**bad))
+        assert L.gpt2_num_params(ctypes.byref(c)) == 0
+        assert L.gpt2_workspace_bytes(ctypes.byref(c)) == 0
+    c = binding.make_config(cfg, mode=7)
+    assert L.gpt2_num_params(ctypes.byref(c)) == 0
+    h = ctypes.c_void_p()
+    assert L.gpt2_create(ctypes.byref(binding.make_config(cfg)), None, ctypes.byref(h)) == -1
+    assert h.value is None
+
+
+def test_strerror_covers_codes(L):
+    from gpt_decoder_step_train_b300 import binding
+    for code in range(0, -8, -1):
+        assert binding.strerror(code) != "unknown status"
+
+
+def test_scratch_queries_are_host_only(L):
+    assert L.gpt2_op_layernorm_backward_scratch_bytes(16384, 768) > 0
+    assert L.gpt2_op_encoder_backward_scratch_bytes(16384, 50257) > 0
+    assert L.gpt2_op_attention_backward_scratch_bytes(16, 1024, 12) >= 16 * 12 * 1024 * 4
+    assert L.gpt2_op_linear_backward_weight_scratch_bytes(16384, 768, 3072, 1) > 0
