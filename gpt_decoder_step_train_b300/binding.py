@@ -19,6 +19,7 @@ GPT2_MODE_FP32, GPT2_MODE_TF32 = 0, 1
 MODES = {"fp32": GPT2_MODE_FP32, "tf32": GPT2_MODE_TF32}
 GPT2_LINEAR_GELU, GPT2_LINEAR_ZERO_PAD = 1, 2
 STATUS_BAD_TOKEN, STATUS_BAD_TARGET, STATUS_TIMEOUT = 1, 2, 4
+BIAS_GRAD_NOALLOC_MAX_PARTIALS = 1 << 20
 TRACE_CLASSES = ("encoder_fwd", "layernorm_fwd", "matmul_fwd", "attention_fwd", "crossentropy",
                  "matmul_bwd_input", "matmul_bwd_weight", "layernorm_bwd", "attention_bwd",
                  "encoder_bwd", "adamw", "other", "bias_grad")
@@ -66,6 +67,7 @@ SIGNATURES = {
                                             _vp, _vp]),
     "gpt2_op_bias_grad_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_bias_grad": (_i, [_vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "gpt2_op_bias_grad_noalloc": (_i, [_vp, _vp, _i, _i, _i, _vp]),
     "gpt2_op_attention_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,

@@ -7,6 +7,8 @@
 // torch", sections 自注意力 (c_attn, c_proj) and 前馈网络（MLP）(c_fc, GELU,
 // c_proj).  Backward (hand-derived): dinp = dout . W, dW = dout^T . inp,
 // db = column sums of dout.
+#include <mutex>
+
 #include "gemm.cuh"
 
 namespace gpt2k {
@@ -179,4 +181,45 @@ GPT2_API int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int 
     if (!db || !dout || N < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
     if (!scratch || scratch_bytes < bias_scratch_bytes(N, OC)) return GPT2_ENOMEM;
     return bias_grad(db, dout, N, OC, ld_dout, reinterpret_cast<float*>(scratch), as_stream(stream));
+}
+
+// ---- allocation-free bias gradient ----------------------------------------
+// The partial sums live in this file-scope device array instead of caller
+// scratch.  Host code must not pass the symbol itself to a kernel (on the host
+// it names a stand-in, not device memory): its device address is looked up
+// once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) float g_bias_scratch[GPT2_BIAS_GRAD_NOALLOC_MAX_PARTIALS];
+
+namespace gpt2k {
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static std::mutex g_noalloc_mu;
+static float* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+
+static int noalloc_scratch(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GPT2_ENOTSUP;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bias_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return GPT2_ECUDA;
+        }
+        g_noalloc_ptr[dev] = reinterpret_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return GPT2_OK;
+}
+}  // namespace gpt2k
+
+GPT2_API int gpt2_op_bias_grad_noalloc(float* db, const float* dout, int N, int OC, int ld_dout,
+                                       void* stream) {
+    if (!db || !dout || N < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    if ((size_t)ceil_div(N, BG_ROWS) * (size_t)OC > GPT2_BIAS_GRAD_NOALLOC_MAX_PARTIALS)
+        return GPT2_ENOMEM;
+    float* scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return bias_grad(db, dout, N, OC, ld_dout, scratch, as_stream(stream));
 }

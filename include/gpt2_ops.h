@@ -101,6 +101,27 @@ size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC);
 int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int ld_dout, void* scratch,
                       size_t scratch_bytes, void* stream);
 
+/* Allocation-free bias gradient.  Same result as gpt2_op_bias_grad, but the
+ * caller passes no scratch and the library allocates nothing: the partial sums
+ * live in a fixed device array inside the library (4 MiB, every GPU that loads
+ * the library holds it until the process exits).  It is for callers that
+ * cannot call cudaMalloc: a host application that owns the whole device memory
+ * budget through its own pool and gives a plugin only input and output
+ * buffers, or a loop that plans all memory at start-up and may not allocate
+ * (or synchronise the device, as cudaMalloc can) once it runs.  There is no
+ * counterpart on the pages; it exists for this calling convention only.
+ *   Limit: ceil(N / 256) * OC <= GPT2_BIAS_GRAD_NOALLOC_MAX_PARTIALS, otherwise
+ *   GPT2_ENOMEM is returned and nothing is launched.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other threads) race and must be serialised by the caller.  Every
+ *   partial read is written earlier in the same call, so no clearing is needed
+ *   between calls. */
+#define GPT2_BIAS_GRAD_NOALLOC_MAX_PARTIALS (1u << 20)
+int gpt2_op_bias_grad_noalloc(float* db, const float* dout, int N, int OC, int ld_dout,
+                              void* stream);
+
 /* Causal self-attention forward over qkv [B,T,3C] (queries, keys, values at
  * column offsets 0, C, 2C; head h owns columns h*hs..h*hs+hs-1 of each):
  * per (b,h), O = softmax(mask(Q K^T / sqrt(hs))) V, heads side by side in
