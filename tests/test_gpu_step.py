@@ -76,7 +76,8 @@ def test_step_matches_oracle(name, mode, init):
     assert max(perrs.values()) <= tol["rel"], _worst(perrs)
     kb_grad = gt["qkvb"].reshape(L, 3 * C)[:, C:2 * C]
     q_grad_rms = np.sqrt(np.mean(ot["qkvb"].reshape(L, 3 * C)[:, :C] ** 2))
-    assert np.abs(kb_grad).max() <= 1e-3 * q_grad_rms
+    # at the arithmetic's noise level: 1e-3 of a typical bias gradient in fp32, 1e-1 in tf32
+    assert np.abs(kb_grad).max() <= 10 * tol["rel"] * q_grad_rms
     kb0 = syn.init_params(cfg, perturbed=perturbed)[syn.tensor_offsets(cfg)["qkvb"][0]:][:L * 3 * C]
     kb0 = kb0.reshape(L, 3 * C)[:, C:2 * C]
     assert np.abs(qb_g[:, C:2 * C] - kb0).max() <= cfg.lr * steps * 1.0001 + cfg.wd * cfg.lr * steps
