@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--no-trace", action="store_true")
     ap.add_argument("--cpu-sample-T", type=int, default=256,
                     help="positions of the single sequence the CPU baseline runs")
+    ap.add_argument("--op", default=None, choices=sorted(OPS),
+                    help="time one kernel of the workload in isolation (prints its own JSON line)")
     return ap.parse_args()
 
 
@@ -341,8 +343,114 @@ def run_ours(args, cfg):
     return 0
 
 
+# ------------------------------------------------------------------ single-op timing
+# name -> (description, builder); a builder returns (callable, algorithmic flops, bytes)
+OPS = {}
+
+
+def _op(name):
+    def deco(f):
+        OPS[name] = f
+        return f
+    return deco
+
+
+def _gemm_case(kind, N, IC, OC, mode):
+    import torch
+    from gpt_decoder_step_train_b300 import binding as B_
+    L = B_.lib()
+    m = B_.MODES[mode]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn(N, IC, device="cuda", generator=g)
+    w = torch.randn(OC, IC, device="cuda", generator=g) * 0.02
+    dy = torch.randn(N, OC, device="cuda", generator=g)
+    out = torch.empty(N, max(IC, OC), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    keep = [x, w, dy, out, st]
+    if kind == "fwd":
+        fn = lambda: L.gpt2_op_linear_forward(B_.ptr(out), None, B_.ptr(x), B_.ptr(w), None, None,
+                                              N, IC, OC, OC, 0, m, B_.ptr(st), None)
+    elif kind == "dx":
+        fn = lambda: L.gpt2_op_linear_backward_input(B_.ptr(out), B_.ptr(dy), B_.ptr(w), None, N,
+                                                     IC, OC, OC, m, B_.ptr(st), None)
+    else:
+        nbytes = L.gpt2_op_linear_backward_weight_scratch_bytes(N, IC, OC, m)
+        sc = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        dw = torch.empty(OC, IC, device="cuda")
+        keep += [sc, dw]
+        fn = lambda: L.gpt2_op_linear_backward_weight(B_.ptr(dw), None, B_.ptr(dy), B_.ptr(x), N,
+                                                      IC, OC, OC, B_.ptr(sc), nbytes, m,
+                                                      B_.ptr(st), None)
+    return fn, 2.0 * N * IC * OC, 4.0 * (N * IC + IC * OC + N * OC), keep
+
+
+for _k in ("fwd", "dx", "dw"):
+    for _nm, (_ic, _oc) in {"qkv": (768, 2304), "fc": (768, 3072), "fcproj": (3072, 768),
+                           "attproj": (768, 768), "lmhead": (768, 50304)}.items():
+        OPS[f"gemm_{_k}_{_nm}"] = (lambda k, ic, oc: (lambda mode: _gemm_case(k, 16384, ic, oc, mode)))(_k, _ic, _oc)
+
+
+def _attn_case(kind, mode, B=16, T=1024, C=768, H=12):
+    import torch
+    from gpt_decoder_step_train_b300 import binding as B_
+    L = B_.lib()
+    m = B_.MODES[mode]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(B, T, 3 * C, device="cuda", generator=g)
+    y = torch.empty(B, T, C, device="cuda")
+    lse = torch.empty(B, H, T, device="cuda")
+    dy = torch.randn(B, T, C, device="cuda", generator=g)
+    dqkv = torch.empty_like(qkv)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = L.gpt2_op_attention_backward_scratch_bytes(B, T, H)
+    sc = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    keep = [qkv, y, lse, dy, dqkv, st, sc]
+    L.gpt2_op_attention_forward(B_.ptr(y), B_.ptr(lse), B_.ptr(qkv), B, T, C, H, m, B_.ptr(st), None)
+    causal_pairs = B * H * T * (T + 1) / 2
+    hs = C // H
+    if kind == "fwd":
+        fn = lambda: L.gpt2_op_attention_forward(B_.ptr(y), B_.ptr(lse), B_.ptr(qkv), B, T, C, H, m,
+                                                 B_.ptr(st), None)
+        flops = 4.0 * hs * causal_pairs
+    else:
+        fn = lambda: L.gpt2_op_attention_backward(B_.ptr(dqkv), B_.ptr(dy), B_.ptr(qkv), B_.ptr(y),
+                                                  B_.ptr(lse), B, T, C, H, B_.ptr(sc), nbytes, m,
+                                                  B_.ptr(st), None)
+        flops = 8.0 * hs * causal_pairs
+    return fn, flops, 4.0 * (qkv.numel() + 2 * y.numel()), keep
+
+
+OPS["attn_fwd"] = lambda mode: _attn_case("fwd", mode)
+OPS["attn_bwd"] = lambda mode: _attn_case("bwd", mode)
+
+
+def run_op(args):
+    import torch
+    torch.cuda.set_device(0)
+    fn, flops, nbytes, keep = OPS[args.op](args.mode)
+    for _ in range(args.warmup):
+        assert fn() == 0
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        assert fn() == 0
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"] * TF32_OVER_BF16 if args.mode == "tf32" else None
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"op": args.op, "mode": args.mode, "ms": round(ms, 4),
+                      "tflops": round(tf, 1), "frac_of_tf32_burst": round(tf / peak, 3) if peak else None,
+                      "gbs_algorithmic": round(nbytes / (ms / 1e3) / 1e9, 1)}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op:
+        return run_op(args)
     cfg = syn.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -1,0 +1,118 @@
+"""Parity at the workloads' full sizes (GPT-2 124M B16 T1024, 350M B8 T1024,
+1.5B B4 T1024), in the tensor-core mode and launch configuration the benchmark
+times, on outputs the oracle can compute one at a time:
+
+* forward: the logits and per-position loss at sampled (row, position) pairs,
+  which the oracle gets from the row's prefix alone (causality);
+* backward: the full-batch gradient equals the mean of the single-row gradients
+  (same GPU path, B = 1), and one row's gradients match the oracle's;
+* update: parameters after AdamW at sampled indices equal AdamW applied in
+  float64 to the GPU's own gradients (which checks the per-tensor decay map).
+
+The oracle here is the single-precision build (its error is far below the
+tensor-core bar), for CPU time.
+"""
+import numpy as np
+import pytest
+
+from gpt_decoder_step_train_b300 import synthetic as syn
+from gpu_util import TOL, per_tensor, rel_l2
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+MODE = "tf32"
+# (config, sampled (row, position) pairs, positions of the single row checked against the oracle)
+CASES = {
+    "124M": ([(0, 0), (3, 57), (15, 1023)], 1024),
+    "350M": ([(0, 5), (7, 1023)], 512),
+    "1.5B": ([(1, 3), (3, 255)], 192),
+}
+
+
+@pytest.fixture(scope="module")
+def o32():
+    from oracle import Oracle
+    return Oracle("f32")
+
+
+def _model(cfg, params, maxB=None):
+    from gpt_decoder_step_train_b300.binding import GPT2
+    p = torch.from_numpy(params.copy()).cuda()
+    return GPT2(cfg, p, maxB=maxB or cfg.B, mode=MODE), p
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fullsize_forward_rows_match_oracle(name, o32):
+    cfg = syn.CONFIGS[name]
+    pairs, _ = CASES[name]
+    params = syn.init_params(cfg)
+    tok, tgt = syn.draw_tokens(cfg)
+    model, _ = _model(cfg, params)
+    loss = model.forward(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+    assert model.status() == 0 and np.isfinite(loss)
+    losses = model.losses(cfg.B * cfg.T).cpu().numpy().reshape(cfg.B, cfg.T)
+    assert abs(losses.astype(np.float64).mean() - loss) < 1e-5
+    model.forward(torch.from_numpy(tok).cuda())               # keep the logits
+    assert model.status() == 0
+    z = model.logits(cfg.B * cfg.T)
+    for b, t in pairs:
+        om = o32.model(cfg.dims(), 1, t + 1, last_only=True)
+        o_loss = om.forward(params, tok[b:b + 1, :t + 1], tgt[b:b + 1, :t + 1])
+        o_z = om.logits()[0]
+        g_z = z[b * cfg.T + t, :cfg.V].cpu().numpy()
+        assert rel_l2(g_z, o_z) <= TOL[MODE]["rel"], (b, t)
+        assert abs(losses[b, t] - o_loss) <= TOL[MODE]["loss"], (b, t, losses[b, t], o_loss)
+    model.close()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fullsize_gradients_and_update(name, o32):
+    cfg = syn.CONFIGS[name]
+    _, T_row = CASES[name]
+    params = syn.init_params(cfg)
+    tok, tgt = syn.draw_tokens(cfg)
+    model, p = _model(cfg, params)
+    # full batch
+    model.forward(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+    assert model.backward() == 0 and model.status() == 0
+    g_full = model.grads().clone()
+    # the same path one row at a time: mean of the row gradients
+    acc = torch.zeros_like(g_full, dtype=torch.float64)
+    for b in range(cfg.B):
+        model.forward(torch.from_numpy(tok[b:b + 1]).cuda(), torch.from_numpy(tgt[b:b + 1]).cuda())
+        assert model.backward() == 0
+        acc += model.grads().double()
+    assert model.status() == 0
+    acc /= cfg.B
+    gt = per_tensor(cfg, g_full.cpu().numpy())
+    mt = per_tensor(cfg, acc.cpu().numpy())
+    errs = {k: rel_l2(gt[k], mt[k]) for k in gt}
+    assert max(errs.values()) <= TOL[MODE]["rel"], errs
+    # one row (its first T_row positions) against the oracle
+    model.forward(torch.from_numpy(tok[:1, :T_row]).cuda(), torch.from_numpy(tgt[:1, :T_row]).cuda())
+    assert model.backward() == 0 and model.status() == 0
+    g_row = model.grads().cpu().numpy()
+    om = o32.model(cfg.dims(), 1, T_row)
+    om.forward(params, tok[:1, :T_row], tgt[:1, :T_row])
+    o_row = om.backward(params)
+    del om
+    gr, orow = per_tensor(cfg, g_row), per_tensor(cfg, o_row)
+    errs = {k: rel_l2(gr[k], orow[k]) for k in gr}
+    assert max(errs.values()) <= TOL[MODE]["rel"], errs
+    # AdamW at sampled indices, from the GPU's own gradient of this row
+    rng = np.random.default_rng(0)
+    idx = np.concatenate([rng.integers(off, off + n, 500) for off, n in syn.tensor_offsets(cfg).values()])
+    p0 = p.cpu().numpy()[idx].astype(np.float64)
+    assert model.adamw(cfg.lr, cfg.b1, cfg.b2, cfg.eps, cfg.wd, 1) == 0 and model.status() == 0
+    p1 = p.cpu().numpy()[idx].astype(np.float64)
+    g = g_row[idx].astype(np.float64)
+    decay = np.zeros(idx.size)
+    for name_, (off, n) in syn.tensor_offsets(cfg).items():
+        if name_ in ("wte", "wpe", "qkvw", "attprojw", "fcw", "fcprojw"):
+            decay[(idx >= off) & (idx < off + n)] = cfg.wd
+    m = (1 - cfg.b1) * g
+    v = (1 - cfg.b2) * g * g
+    want = p0 - cfg.lr * ((m / (1 - cfg.b1)) / (np.sqrt(v / (1 - cfg.b2)) + cfg.eps) + decay * p0)
+    assert np.abs(p1 - want).max() <= 1e-6 * cfg.lr + 1e-7 * np.abs(p0).max()
+    model.close()
