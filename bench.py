@@ -43,7 +43,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="124M", choices=list(syn.CONFIGS))
-    ap.add_argument("--mode", default="tf32", choices=["tf32", "fp32"])
+    ap.add_argument("--mode", default="tf32", choices=["tf32", "bf16", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
@@ -301,11 +301,14 @@ def run_ours(args, cfg):
         if args.mode == "tf32":
             peak = peaks["bf16_tflops_sustained"] * TF32_OVER_BF16
             peak_note = f"tf32 = bf16 sustained x 1.1/2.25 ({peak_src})"
+        elif args.mode == "bf16":
+            peak = peaks["bf16_tflops_sustained"]
+            peak_note = f"bf16 sustained ({peak_src})"
         else:
             peak = None
             peak_note = "fp32 SIMT mode"
         achieved = gemm_flops(cfg, B, T) / (gemm_ms / 1000.0) / 1e12
-        roofline = {"kernel": "gemm_tf32 (all linear fwd/dX/dW products)", "bound": "tensor",
+        roofline = {"kernel": f"gemm_tc<{args.mode}> (all linear fwd/dX/dW products)", "bound": "tensor",
                     "achieved": round(achieved, 1), "peak": round(peak, 1) if peak else None,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                     "traffic": None, "peak_source": peak_note,
@@ -316,7 +319,7 @@ def run_ours(args, cfg):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "tf32" if args.mode == "tf32" else "f32",
+        "dtype": {"tf32": "tf32", "bf16": "bf16", "fp32": "f32"}[args.mode],
         "data": "synthetic (seeded N(0,0.02) init, Zipf(1.1) tokens, next-token targets)",
         "config": {"workload": cfg.name, "global_batch": B * world, "seq_len": T,
                    "mode": args.mode, "parallelism": f"replicas{world}" if world > 1 else "single",

@@ -15,14 +15,24 @@ LIB_PATH = os.path.join(HERE, "libgpt2_b300.so")
 
 GPT2_OK, GPT2_EINVAL, GPT2_ENOMEM, GPT2_ECUDA = 0, -1, -2, -3
 GPT2_ETOKEN, GPT2_ESTATE, GPT2_ETIMEOUT, GPT2_ENOTSUP = -4, -5, -6, -7
-GPT2_MODE_FP32, GPT2_MODE_TF32 = 0, 1
-MODES = {"fp32": GPT2_MODE_FP32, "tf32": GPT2_MODE_TF32}
+GPT2_MODE_FP32, GPT2_MODE_TF32, GPT2_MODE_BF16 = 0, 1, 2
+MODES = {"fp32": GPT2_MODE_FP32, "tf32": GPT2_MODE_TF32, "bf16": GPT2_MODE_BF16}
 GPT2_LINEAR_GELU, GPT2_LINEAR_ZERO_PAD = 1, 2
 STATUS_BAD_TOKEN, STATUS_BAD_TARGET, STATUS_TIMEOUT = 1, 2, 4
 BIAS_GRAD_NOALLOC_MAX_PARTIALS = 1 << 20
 TRACE_CLASSES = ("encoder_fwd", "layernorm_fwd", "matmul_fwd", "attention_fwd", "crossentropy",
                  "matmul_bwd_input", "matmul_bwd_weight", "layernorm_bwd", "attention_bwd",
                  "encoder_bwd", "adamw", "other", "bias_grad")
+
+
+class gpt2_gemm_args(C.Structure):
+    _fields_ = [("M", C.c_int), ("N", C.c_int), ("K", C.c_int),
+                ("A", C.c_void_p), ("lda", C.c_int), ("a_kmajor", C.c_int),
+                ("B", C.c_void_p), ("ldb", C.c_int), ("b_kmajor", C.c_int),
+                ("bf16", C.c_int),
+                ("out", C.c_void_p), ("ldo", C.c_int), ("out_bf16", C.c_int),
+                ("out_pre", C.c_void_p), ("bias", C.c_void_p), ("residual", C.c_void_p),
+                ("gelu_x", C.c_void_p), ("ldg", C.c_int), ("gelu", C.c_int)]
 
 
 class gpt2_config(C.Structure):
@@ -56,9 +66,10 @@ SIGNATURES = {
     "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_encoder_backward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_op_layernorm_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
+    "gpt2_op_layernorm_forward_bf16": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
-    "gpt2_op_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _sz,
-                                        _vp]),
+    "gpt2_op_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp,
+                                        _sz, _vp]),
     "gpt2_op_linear_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                     _vp]),
     "gpt2_op_linear_backward_input": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -66,13 +77,15 @@ SIGNATURES = {
     "gpt2_op_linear_backward_weight": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,
                                             _vp, _vp]),
     "gpt2_op_bias_grad_scratch_bytes": (_sz, [_i, _i]),
-    "gpt2_op_bias_grad": (_i, [_vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "gpt2_op_bias_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "gpt2_op_gemm": (_i, [_vp, _i, _vp, _vp]),
+    "gpt2_op_to_bf16": (_i, [_vp, _vp, _sz, _vp]),
     "gpt2_op_bias_grad_noalloc": (_i, [_vp, _vp, _i, _i, _i, _vp]),
     "gpt2_op_attention_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,
                                         _vp, _vp]),
-    "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
+    "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_sum": (_i, [_vp, _vp, _i, _f, _vp]),
     "gpt2_op_adamw": (_i, [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _f, _f, _vp]),
 }

@@ -19,6 +19,8 @@
 // dQ) or per key row (dK, dV), with the row and its accumulator in registers
 // and tiles of the other side staged in shared memory.  Keys past a block's
 // last query are skipped (causal tile skipping).
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace gpt2k {
@@ -113,6 +115,25 @@ attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __res
     for (int d = 0; d < HSP; d += 4)
         if (d < hs) *reinterpret_cast<float4*>(yr + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
     lse[((size_t)b * H + h) * T + i] = m + logf(l);
+}
+
+// D[b,h,i] = dO_i . O_i (bf16 inputs)
+__global__ void attn_bwd_dot_bf16_kernel(float* __restrict__ D, const __nv_bfloat16* __restrict__ dy,
+                                         const __nv_bfloat16* __restrict__ y, int B, int T, int C, int H,
+                                         int hs) {
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)B * H * T) return;
+    int i = (int)(idx % T);
+    int h = (int)((idx / T) % H);
+    int b = (int)(idx / ((long long)T * H));
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(dy + ((size_t)b * T + i) * C + h * hs);
+    const __nv_bfloat162* o = reinterpret_cast<const __nv_bfloat162*>(y + ((size_t)b * T + i) * C + h * hs);
+    float s = 0.f;
+    for (int d = 0; d < hs / 2; d++) {
+        float2 u = __bfloat1622float2(a[d]), v = __bfloat1622float2(o[d]);
+        s += u.x * v.x + u.y * v.y;
+    }
+    D[idx] = s;
 }
 
 // D[b,h,i] = dO_i . O_i
@@ -255,6 +276,10 @@ static void launch_bwd(float* dqkv, const float* dy, const float* qkv, const flo
 
 int attention_tc_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int H,
                          int* status, cudaStream_t st);
+int attention_bf16_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H,
+                           cudaStream_t st);
+int attention_bf16_backward(void* dqkv, const void* dy, const void* qkv, const float* lse,
+                            const float* D, int B, int T, int C, int H, cudaStream_t st);
 int attention_tc_backward(float* dqkv, const float* dy, const float* qkv, const float* lse,
                           const float* D, int B, int T, int C, int H, int* status,
                           cudaStream_t st);
@@ -270,17 +295,23 @@ static bool attn_args_ok(int B, int T, int C, int H) {
     return hs % 4 == 0 && hs <= 64;
 }
 
-GPT2_API int gpt2_op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C,
+GPT2_API int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
                                        int H, int mode, int* status, void* stream) {
     if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
     if (!aligned16(y) || !aligned16(qkv)) return GPT2_EINVAL;
     int hs = C / H;
     cudaStream_t st = as_stream(stream);
+    if (mode == GPT2_MODE_BF16) {
+        if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
+        return attention_bf16_forward(y, lse, qkv, B, T, C, H, st);
+    }
+    float* yf = static_cast<float*>(y);
+    const float* qf = static_cast<const float*>(qkv);
     if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
-        return attention_tc_forward(y, lse, qkv, B, T, C, H, status, st);
-    if (hs <= 16) launch_fwd<16>(y, lse, qkv, B, T, C, H, hs, st);
-    else if (hs <= 32) launch_fwd<32>(y, lse, qkv, B, T, C, H, hs, st);
-    else launch_fwd<64>(y, lse, qkv, B, T, C, H, hs, st);
+        return attention_tc_forward(yf, lse, qf, B, T, C, H, status, st);
+    if (hs <= 16) launch_fwd<16>(yf, lse, qf, B, T, C, H, hs, st);
+    else if (hs <= 32) launch_fwd<32>(yf, lse, qf, B, T, C, H, hs, st);
+    else launch_fwd<64>(yf, lse, qf, B, T, C, H, hs, st);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }
@@ -290,8 +321,8 @@ GPT2_API size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
     return round_up((size_t)B * H * T * sizeof(float), 256);
 }
 
-GPT2_API int gpt2_op_attention_backward(float* dqkv, const float* dy, const float* qkv,
-                                        const float* y, const float* lse, int B, int T, int C,
+GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv,
+                                        const void* y, const float* lse, int B, int T, int C,
                                         int H, void* scratch, size_t scratch_bytes, int mode,
                                         int* status, void* stream) {
     if (!dqkv || !dy || !qkv || !y || !lse || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
@@ -302,13 +333,23 @@ GPT2_API int gpt2_op_attention_backward(float* dqkv, const float* dy, const floa
     cudaStream_t st = as_stream(stream);
     float* D = reinterpret_cast<float*>(scratch);
     long long n = (long long)B * H * T;
-    count_launch(), attn_bwd_dot_kernel<<<ceil_div(n, 256), 256, 0, st>>>(D, dy, y, B, T, C, H, hs);
+    if (mode == GPT2_MODE_BF16) {
+        if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
+        count_launch(), attn_bwd_dot_bf16_kernel<<<ceil_div(n, 256), 256, 0, st>>>(
+            D, static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(y), B, T, C, H, hs);
+        GPT2_LAUNCH_CHECK();
+        return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
+    }
+    float* dq = static_cast<float*>(dqkv);
+    const float* g = static_cast<const float*>(dy);
+    const float* x = static_cast<const float*>(qkv);
+    count_launch(), attn_bwd_dot_kernel<<<ceil_div(n, 256), 256, 0, st>>>(D, g, static_cast<const float*>(y), B, T, C, H, hs);
     GPT2_LAUNCH_CHECK();
     if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
-        return attention_tc_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st);
-    if (hs <= 16) launch_bwd<16>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
-    else if (hs <= 32) launch_bwd<32>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
-    else launch_bwd<64>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, st);
+        return attention_tc_backward(dq, g, x, lse, D, B, T, C, H, status, st);
+    if (hs <= 16) launch_bwd<16>(dq, g, x, lse, D, B, T, C, H, hs, st);
+    else if (hs <= 32) launch_bwd<32>(dq, g, x, lse, D, B, T, C, H, hs, st);
+    else launch_bwd<64>(dq, g, x, lse, D, B, T, C, H, hs, st);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -9,6 +9,8 @@
 // per-thread running maximum and rescaled sum, combined across the block; pass
 // 2 re-reads the row (it is still in L2) and overwrites it with the gradient.
 // DRAM traffic is one read and one write of the logits.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace gpt2k {
@@ -23,8 +25,8 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
 }
 
 __global__ void __launch_bounds__(CE_THREADS)
-crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, const int* __restrict__ tgt,
-                    int V, int ld, float dscale, int* status) {
+crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bfloat16* __restrict__ dz16,
+                    const int* __restrict__ tgt, int V, int ld, float dscale, int* status) {
     __shared__ float sm[CE_THREADS / 32], ss[CE_THREADS / 32];
     __shared__ float s_lse, s_zt;
     const int row = blockIdx.x, tid = threadIdx.x;
@@ -76,7 +78,13 @@ crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, const int
             e[k] = (p - (idx == t ? 1.f : 0.f)) * dscale;
             if (idx >= V || lse == INFINITY) e[k] = 0.f;
         }
-        z4[c] = make_float4(e[0], e[1], e[2], e[3]);
+        if (dz16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(e[0], e[1]), hi = __floats2bfloat162_rn(e[2], e[3]);
+            reinterpret_cast<uint2*>(dz16 + (size_t)row * ld)[c] =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        } else {
+            z4[c] = make_float4(e[0], e[1], e[2], e[3]);
+        }
     }
 }
 
@@ -99,11 +107,13 @@ __global__ void __launch_bounds__(1024) sum_kernel(float* __restrict__ out, cons
 
 using namespace gpt2k;
 
-GPT2_API int gpt2_op_crossentropy(float* losses, float* z, const int* tgt, int N, int V, int ld,
-                                  float dscale, int* status, void* stream) {
+GPT2_API int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const int* tgt, int N,
+                                  int V, int ld, float dscale, int* status, void* stream) {
     if (!losses || !z || !tgt || N < 1 || V < 1 || ld < V || ld % 4 || !aligned16(z))
         return GPT2_EINVAL;
-    count_launch(), crossentropy_kernel<<<N, CE_THREADS, 0, as_stream(stream)>>>(losses, z, tgt, V, ld, dscale, status);
+    if (dz_bf16 && (reinterpret_cast<uintptr_t>(dz_bf16) & 7)) return GPT2_EINVAL;
+    count_launch(), crossentropy_kernel<<<N, CE_THREADS, 0, as_stream(stream)>>>(
+        losses, z, static_cast<__nv_bfloat16*>(dz_bf16), tgt, V, ld, dscale, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

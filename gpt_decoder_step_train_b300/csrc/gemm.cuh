@@ -9,13 +9,16 @@
 //   dX       dinp = dout . W    A = dout (K-major), B = W (N-major)
 //   dW       dW   = dout^T . inp  A = dout (M-major), B = inp (N-major)
 #pragma once
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace gpt2k {
 
 struct GemmEpilogue {
-    float* out;              // [M, ldo]
+    void* out;               // [M, ldo], fp32, or bf16 when out_bf16
     int ldo;
+    int out_bf16;
     float* out_pre;          // GELU: pre-activation written here (same ldo)
     const float* bias;       // [N] or null
     const float* residual;   // [M, ldo] or null: out = residual + (acc + bias)
@@ -26,9 +29,10 @@ struct GemmEpilogue {
 
 struct GemmProblem {
     int M, N, K;
-    const float* A; int lda; bool a_kmajor;
-    const float* B; int ldb; bool b_kmajor;
+    const void* A; int lda; bool a_kmajor;
+    const void* B; int ldb; bool b_kmajor;
     int* status;             // device status word for bounded-wait timeouts, or null
+    bool bf16 = false;       // A and B hold bf16 (tensor cores only); else fp32
 };
 
 // Epilogue of one output element; shared by every GEMM kernel.
@@ -42,17 +46,36 @@ __device__ __forceinline__ void epilogue_store(const GemmEpilogue& e, int m, int
     }
     if (e.residual) v += e.residual[o];
     if (e.gelu_x) v *= gelu_grad(e.gelu_x[(size_t)m * e.ldg + n]);
-    e.out[o] = v;
+    if (e.out_bf16) reinterpret_cast<__nv_bfloat16*>(e.out)[o] = __float2bfloat16_rn(v);
+    else reinterpret_cast<float*>(e.out)[o] = v;
 }
 
 // CUDA-core fp32 GEMM (strict mode).
 int gemm_simt(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st);
 
-// tcgen05 tensor-core GEMM with tf32 operands.  `split` > 1 splits K into
+// tcgen05 tensor-core GEMM, tf32 (fp32 operands) or bf16 operands (p.bf16).  `split` > 1 splits K into
 // that many contiguous ranges; each range writes its own [M, N] fp32 slice of
 // `partial` (plain accumulators, no epilogue), to be summed in a fixed order.
 int gemm_tc(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st);
 int gemm_tc_splitk(const GemmProblem& p, float* partial, int split, cudaStream_t st);
 bool gemm_tc_supported(const GemmProblem& p);
+bool gemm_tc_epilogue_supported(const GemmEpilogue& e);
+
+// Linear-layer products for any operand type (linear.cu); bf16 requires
+// mode GPT2_MODE_BF16.
+int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, const void* w,
+                   bool bf16, const float* bias, const float* residual, int N, int IC, int OC,
+                   int ld_out, int flags, int mode, int* status, cudaStream_t st);
+int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
+                          const float* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
+                          int* status, cudaStream_t st);
+int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
+                           int OC, int ld_dout, void* scratch, size_t scratch_bytes, int mode,
+                           int* status, cudaStream_t st);
+int bias_grad_any(float* db, const void* dout, bool bf16, int N, int OC, int ld, void* scratch,
+                  size_t scratch_bytes, cudaStream_t st);
+int layernorm_forward(void* y, bool out_bf16, float* mean, float* rstd, const float* x,
+                      const float* w, const float* b, int N, int C, cudaStream_t st);
+int to_bf16(void* dst, const float* src, size_t n, cudaStream_t st);
 
 }  // namespace gpt2k

@@ -94,8 +94,15 @@ sgemm_kernel(int M, int N, int K, const float* __restrict__ A, int lda,
     }
 }
 
-int gemm_simt(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st) {
-    if (p.M <= 0 || p.N <= 0) return GPT2_OK;
+int gemm_simt(const GemmProblem& gp, const GemmEpilogue& e, cudaStream_t st) {
+    if (gp.M <= 0 || gp.N <= 0) return GPT2_OK;
+    if (gp.bf16) return GPT2_ENOTSUP;
+    struct {
+        int M, N, K, lda, ldb;
+        const float *A, *B;
+        bool a_kmajor, b_kmajor;
+    } p{gp.M, gp.N, gp.K, gp.lda, gp.ldb, static_cast<const float*>(gp.A),
+        static_cast<const float*>(gp.B), gp.a_kmajor, gp.b_kmajor};
     dim3 grid(ceil_div(p.N, SG_BN), ceil_div(p.M, SG_BM));
     if (p.a_kmajor && p.b_kmajor)
         count_launch(), sgemm_kernel<true, true><<<grid, 256, 0, st>>>(p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, e);

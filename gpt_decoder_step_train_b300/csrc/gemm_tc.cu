@@ -1,5 +1,7 @@
-// gemm_tc.cu -- fp32-storage GEMM on the 5th-generation tensor cores (tcgen05,
-// kind::tf32, fp32 accumulation in tensor memory), fed by TMA.
+// gemm_tc.cu -- GEMM on the 5th-generation tensor cores (tcgen05), fed by TMA,
+// fp32 accumulation in tensor memory.  Two operand types: fp32 storage read as
+// tf32 (kind::tf32, K = 8 per MMA) and bf16 (kind::f16, K = 16 per MMA); a
+// k-block is one 128-byte swizzle row either way (32 fp32 or 64 bf16).
 //
 // Persistent, warp-specialised kernel, one CTA per SM, 192 threads:
 //   warp 0  TMA producer: fills a ring of shared-memory stages (A: 128 x 32,
@@ -32,17 +34,25 @@ namespace gpt2k {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BK = 32;                 // fp32 per k-block: one 128-byte swizzle row
-constexpr int UMMA_K = 8;              // K of one tf32 MMA
 constexpr int THREADS = 192;
-constexpr int ATOM_BYTES = 32 * BK * 4;   // one MN-major box: 32 MN x 32 k = 4 KB
 constexpr unsigned long long WAIT_NS = 1000000000ull;   // 1 s
 
-template <int BN>
+// Per operand type: element bytes, k-block (one 128-byte row), MMA K, and the
+// MN-major box (128 bytes of MN x BK k-rows).
+template <bool BF16>
+struct Elem {
+    static constexpr int BYTES = BF16 ? 2 : 4;
+    static constexpr int BK = 128 / BYTES;            // 32 fp32 or 64 bf16
+    static constexpr int UMMA_K = BF16 ? 16 : 8;
+    static constexpr int MN_BOX = 128 / BYTES;        // MN elements per MN-major box
+    static constexpr int BOX_BYTES = 128 * BK;        // 4 KB or 8 KB
+};
+
+template <int BN, bool BF16>
 struct Shape {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
-    static constexpr int A_BYTES = BM * BK * 4;
-    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int A_BYTES = BM * 128;          // BM rows x 128 bytes
+    static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
@@ -59,6 +69,12 @@ struct Params {
     int* status;            // device status word (timeouts), may be null
     // MN-major operand descriptor: swizzle layout type and the two byte strides
     uint32_t mn_layout, mn_lbo, mn_sbo;
+    // epilogue: which tensor maps are live
+    int has_aux;            // residual (aux_residual) or GELU-input tile loaded by TMA
+    int aux_residual;
+    int gelu;
+    int out_bf16;
+    const float* bias;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -123,6 +139,55 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// tanh on the special-function unit (relative error about 2^-11), for the
+// tensor-core modes' GELU epilogues
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_fwd_fast(float x) {
+    return 0.5f * x * (1.0f + tanh_fast(GPT2_GELU_S * (x + GPT2_GELU_K * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_fast(float x) {
+    const float x2 = x * x;
+    const float th = tanh_fast(GPT2_GELU_S * (x + GPT2_GELU_K * x2 * x));
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GPT2_GELU_S * (1.0f + 3.0f * GPT2_GELU_K * x2);
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -143,21 +208,30 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     return d;
 }
 
-// Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B tf32
-// (bits 7-9, 10-12 = 2), majorness bits 15 (A) and 16 (B), N>>3 at bit 17,
-// M>>4 at bit 24.
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn, bool b_mn) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor for kind::tf32 / kind::f16: D fp32 (bits 4-5 = 1),
+// A and B format in bits 7-9 and 10-12 (tf32 = 2, bf16 = 1), majorness bits 15
+// (A) and 16 (B), N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn, bool b_mn, bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 2u) << 7) | ((bf16 ? 1u : 2u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
+template <bool BF16>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if (BF16) {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -207,69 +281,42 @@ __device__ __forceinline__ Unit unit_coords(const Params& p, long long u) {
 }
 
 // ---------------------------------------------------------------- epilogue
-template <bool PARTIAL>
-__device__ __forceinline__ void store_row(const Params& p, int row, int n, int split,
-                                          const uint32_t (&r)[32]) {
-    if (PARTIAL) {
-        float* out = p.partial + ((size_t)split * p.M + row) * p.N + n;
-        if (n + 32 <= p.N && (p.N & 3) == 0) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(out + j) =
-                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-        } else {
-            for (int j = 0; j < 32 && n + j < p.N; j++) out[j] = __uint_as_float(r[j]);
-        }
-        return;
-    }
-    const GemmEpilogue& e = p.e;
-    const bool vec = n + 32 <= p.N && (e.ldo & 3) == 0 && (!e.gelu_x || (e.ldg & 3) == 0);
-    if (vec) {
-        size_t o = (size_t)row * e.ldo + n;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float v[4] = {__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                          __uint_as_float(r[j + 3])};
-            if (e.bias) {
-#pragma unroll
-                for (int k = 0; k < 4; k++) v[k] += __ldg(e.bias + n + j + k);
-            }
-            if (e.gelu) {
-                *reinterpret_cast<float4*>(e.out_pre + o + j) = make_float4(v[0], v[1], v[2], v[3]);
-#pragma unroll
-                for (int k = 0; k < 4; k++) v[k] = gelu_fwd(v[k]);
-            }
-            if (e.residual) {
-                float4 rr = *reinterpret_cast<const float4*>(e.residual + o + j);
-                v[0] += rr.x; v[1] += rr.y; v[2] += rr.z; v[3] += rr.w;
-            }
-            if (e.gelu_x) {
-                float4 h = *reinterpret_cast<const float4*>(e.gelu_x + (size_t)row * e.ldg + n + j);
-                v[0] *= gelu_grad(h.x); v[1] *= gelu_grad(h.y);
-                v[2] *= gelu_grad(h.z); v[3] *= gelu_grad(h.w);
-            }
-            *reinterpret_cast<float4*>(e.out + o + j) = make_float4(v[0], v[1], v[2], v[3]);
-        }
-    } else {
-        for (int j = 0; j < 32 && n + j < p.N; j++) epilogue_store(e, row, n + j, __uint_as_float(r[j]));
-    }
+// Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and walks
+// them 32 columns at a time: thread = row.  Per chunk it loads the accumulator
+// from tensor memory, applies the epilogue in registers and writes the chunk
+// into a swizzled shared-memory box that one lane stores with a TMA bulk copy
+// (clipped at the matrix edges).  A residual or GELU-input tile arrives by a
+// TMA load into a second box; for GELU that box holds the pre-activation
+// output instead.  Boxes: fp32 rows of 128 bytes (128-byte swizzle), bf16 rows
+// of 64 bytes (64-byte swizzle).
+constexpr int EPI_WARP_BYTES = 8192;              // 4 KB output box + 4 KB aux box
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t sw64(int row, int chunk) {
+    return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
 // ---------------------------------------------------------------- kernel
-template <int BN>
+template <int BN, bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const Params p) {
-    using S = Shape<BN>;
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux,
+               const __grid_constant__ CUtensorMap tmPre, const Params p) {
+    using S = Shape<BN, BF16>;
+    using E = Elem<BF16>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[S::STAGES], empty_bar[S::STAGES];
-    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, aux_bar[4];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
     auto stage_a = [&](int s) { return base + (uint32_t)(s * S::STAGE_BYTES); };
     auto stage_b = [&](int s) { return base + (uint32_t)(s * S::STAGE_BYTES + S::A_BYTES); };
 
@@ -284,9 +331,11 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(smem_u32(&tempty_bar[a]), 4);
         }
         mbar_init(smem_u32(&drain_bar), 1);
+        for (int w = 0; w < 4; w++) mbar_init(smem_u32(&aux_bar[w]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
         prefetch_map(&tmB);
+        prefetch_map(&tmOut);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -321,20 +370,20 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     mbar_expect_tx(fb, S::STAGE_BYTES);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-                    const int k0 = kb * BK;
+                    const int k0 = kb * E::BK;
                     if (p.a_kmajor) {
                         tma_load_2d(stage_a(stage), &tmA, k0, m0, fb);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BM / 32; j++)
-                            tma_load_2d(stage_a(stage) + j * ATOM_BYTES, &tmA, m0 + 32 * j, k0, fb);
+                        for (int j = 0; j < BM / E::MN_BOX; j++)
+                            tma_load_2d(stage_a(stage) + j * E::BOX_BYTES, &tmA, m0 + E::MN_BOX * j, k0, fb);
                     }
                     if (p.b_kmajor) {
                         tma_load_2d(stage_b(stage), &tmB, k0, n0, fb);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 32; j++)
-                            tma_load_2d(stage_b(stage) + j * ATOM_BYTES, &tmB, n0 + 32 * j, k0, fb);
+                        for (int j = 0; j < BN / E::MN_BOX; j++)
+                            tma_load_2d(stage_b(stage) + j * E::BOX_BYTES, &tmB, n0 + E::MN_BOX * j, k0, fb);
                     }
                     if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -353,7 +402,11 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(BM, BN, !p.a_kmajor, !p.b_kmajor);
+            const uint32_t idesc = instr_desc(BM, BN, !p.a_kmajor, !p.b_kmajor, BF16);
+            // one MMA consumes UMMA_K elements: 32 bytes of a K-major row, or UMMA_K
+            // 128-byte rows of an MN-major box
+            constexpr uint32_t KMAJ_STEP = E::UMMA_K * E::BYTES;
+            constexpr uint32_t MN_STEP = E::UMMA_K * 128;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -374,14 +427,14 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tc_fence_after();
                     const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; k++) {
+                    for (int k = 0; k < E::BK / E::UMMA_K; k++) {
                         uint64_t ad = p.a_kmajor
-                                          ? smem_desc(a0 + k * 32, 16, 1024, LAYOUT_SW128)
-                                          : smem_desc(a0 + k * 1024, p.mn_lbo, p.mn_sbo, p.mn_layout);
+                                          ? smem_desc(a0 + k * KMAJ_STEP, 16, 1024, LAYOUT_SW128)
+                                          : smem_desc(a0 + k * MN_STEP, p.mn_lbo, p.mn_sbo, p.mn_layout);
                         uint64_t bd = p.b_kmajor
-                                          ? smem_desc(b0 + k * 32, 16, 1024, LAYOUT_SW128)
-                                          : smem_desc(b0 + k * 1024, p.mn_lbo, p.mn_sbo, p.mn_layout);
-                        mma_tf32(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                                          ? smem_desc(b0 + k * KMAJ_STEP, 16, 1024, LAYOUT_SW128)
+                                          : smem_desc(b0 + k * MN_STEP, p.mn_lbo, p.mn_sbo, p.mn_layout);
+                        mma_issue<BF16>(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
@@ -399,22 +452,100 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int ew = warp - 2;
+        uint8_t* const outb = base_ptr + S::STAGES * S::STAGE_BYTES + ew * EPI_WARP_BYTES;
+        uint8_t* const auxb = outb + 4096;
+        const uint32_t outs = smem_u32(outb), auxs = smem_u32(auxb);
+        const uint32_t abar = smem_u32(&aux_bar[ew]);
+        uint32_t aux_phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (long long u = blockIdx.x; u < p.units; u += gridDim.x) {
+        bool ok = true;
+        for (long long u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             Unit c = unit_coords(p, u);
             const int m0 = c.m_tile * BM, n0 = c.n_tile * BN;
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, p.status)) break;
             tc_fence_after();
-            const int row = m0 + q * 32 + lane;
+            const int row0 = m0 + q * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             for (int cc = 0; cc < BN; cc += 32) {
-                if (n0 + cc >= p.N) break;
+                const int nc = n0 + cc;
+                if (nc >= p.N) break;
+                if (p.has_aux && lane == 0) {
+                    mbar_expect_tx(abar, 4096);
+                    tma_load_2d(auxs, &tmAux, nc, row0, abar);
+                }
                 uint32_t r[32];
                 tmem_ld32(taddr + (uint32_t)cc, r);
-                if (row < p.M) {
-                    if (p.partial) store_row<true>(p, row, n0 + cc, c.split, r);
-                    else store_row<false>(p, row, n0 + cc, c.split, r);
+                // the previous chunk's stores have finished reading both boxes
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                if (p.has_aux) {
+                    if (!mbar_wait(abar, aux_phase, &s_abort, p.status)) { ok = false; break; }
+                    aux_phase ^= 1u;
+                }
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) x[j] = __uint_as_float(r[j]);
+                if (!p.partial) {
+                    if (p.bias) {
+                        if (nc + 32 <= p.N) {
+                            const float4* b4 = reinterpret_cast<const float4*>(p.bias + nc);
+#pragma unroll
+                            for (int j = 0; j < 8; j++) {
+                                const float4 bv = __ldg(b4 + j);
+                                x[4 * j] += bv.x; x[4 * j + 1] += bv.y; x[4 * j + 2] += bv.z; x[4 * j + 3] += bv.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j++) x[j] += nc + j < p.N ? __ldg(p.bias + nc + j) : 0.f;
+                        }
+                    }
+                    if (p.gelu) {
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            *reinterpret_cast<float4*>(auxb + sw128(lane, j)) =
+                                make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; j++) x[j] = gelu_fwd_fast(x[j]);
+                    } else if (p.has_aux) {
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            const float4 a = *reinterpret_cast<const float4*>(auxb + sw128(lane, j));
+                            if (p.aux_residual) {
+                                x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
+                            } else {
+                                x[4 * j] *= gelu_grad_fast(a.x); x[4 * j + 1] *= gelu_grad_fast(a.y);
+                                x[4 * j + 2] *= gelu_grad_fast(a.z); x[4 * j + 3] *= gelu_grad_fast(a.w);
+                            }
+                        }
+                    }
+                }
+                if (p.out_bf16) {
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        __nv_bfloat162 h0 = __floats2bfloat162_rn(x[8 * k], x[8 * k + 1]);
+                        __nv_bfloat162 h1 = __floats2bfloat162_rn(x[8 * k + 2], x[8 * k + 3]);
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(x[8 * k + 4], x[8 * k + 5]);
+                        __nv_bfloat162 h3 = __floats2bfloat162_rn(x[8 * k + 6], x[8 * k + 7]);
+                        *reinterpret_cast<uint4*>(outb + sw64(lane, k)) =
+                            make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                       *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        *reinterpret_cast<float4*>(outb + sw128(lane, j)) =
+                            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    if (p.partial) tma_store_3d(&tmOut, nc, row0, c.split, outs);
+                    else tma_store_2d(&tmOut, nc, row0, outs);
+                    if (p.gelu && !p.partial) tma_store_2d(&tmPre, nc, row0, auxs);
+                    bulk_commit();
                 }
             }
             tc_fence_before();
@@ -422,6 +553,8 @@ gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -453,56 +586,106 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D fp32 tensor map over a row-major matrix [rows, cols] with row stride
-// `ld` elements; box {box_cols, box_rows}, zero fill.  K-major operands use the
-// 128-byte swizzle of 16-byte chunks; MN-major operands the 128-byte swizzle of
-// 32-byte chunks, the layout the tensor core reads tf32 MN-major tiles in.
-static bool make_map(CUtensorMap* map, const float* ptr, int cols, int rows, int ld, int box_cols,
-                     int box_rows, CUtensorMapSwizzle swz) {
+// 2-D tensor map over a row-major matrix [rows, cols] (fp32 or bf16) with row
+// stride `ld` elements; box {box_cols, box_rows}, zero fill.
+static bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int cols, int rows, int ld,
+                     int box_cols, int box_rows, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const size_t es = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * es};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// MN-major operand tiles are boxes of 128 bytes of MN x BK k-rows, side by side
+// along MN.  Descriptor: LBO = stride between MN boxes, SBO = stride between the
+// k-row groups of the swizzle atom.
+//   tf32: 128-byte swizzle of 32-byte chunks (UMMA layout 1, TMA ATOM_32B), 4-row
+//         groups: LBO 4096, SBO 512 (the layout the tensor core reads tf32
+//         MN-major operands in; with the 16-byte-chunk swizzle it returns zeros).
+//   bf16: 128-byte swizzle of 16-byte chunks (UMMA layout 2, TMA 128B), 8-row
+//         groups: LBO 8192, SBO 1024.
+// 3-D fp32 tensor map [z][rows][cols] (plain, contiguous slices) with box
+// {box_cols, box_rows, 1}: the split-K partial slices, clipped per slice.
+static bool make_map_3d(CUtensorMap* map, const float* ptr, int cols, int rows, int depth, int box_cols,
+                        int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)depth};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * rows * 4};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// MN-major operand tiles: boxes of 32 MN x 32 k (4 KB) side by side along MN;
-// within a box, k-rows of 128 bytes whose 32-byte chunks are swizzled over a
-// period of 4 rows.  Descriptor: LBO = stride between MN boxes, SBO = stride
-// between 4-row k groups.
-constexpr uint32_t MN_LBO = ATOM_BYTES, MN_SBO = 4 * 128;
+// MN-major operand tiles are boxes of 128 bytes of MN x BK k-rows, side by side
+// along MN.  Descriptor: LBO = stride between MN boxes, SBO = stride between the
+// k-row groups of the swizzle atom.
+//   tf32: 128-byte swizzle of 32-byte chunks (UMMA layout 1, TMA ATOM_32B), 4-row
+//         groups: LBO 4096, SBO 512 (the layout the tensor core reads tf32
+//         MN-major operands in; with the 16-byte-chunk swizzle it returns zeros).
+//   bf16: 128-byte swizzle of 16-byte chunks (UMMA layout 2, TMA 128B), 8-row
+//         groups: LBO 8192, SBO 1024.
+struct Maps {
+    CUtensorMap a, b, out, aux, pre;
+};
 
-template <int BN>
-static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
-                   CUtensorMap* ma, CUtensorMap* mb, Params* pp) {
-    using S = Shape<BN>;
+template <int BN, bool BF16>
+static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split, Maps* mp,
+                   Params* pp) {
+    using S = Shape<BN, BF16>;
+    using E = Elem<BF16>;
     static bool attr_done = false;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(gemm_tf32_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)S::SMEM) != cudaSuccess) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<BN, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(S::SMEM + EPI_BYTES)) != cudaSuccess) {
             (void)cudaGetLastError();
             return GPT2_ECUDA;
         }
         attr_done = true;
     }
-    const CUtensorMapSwizzle KSW = CU_TENSOR_MAP_SWIZZLE_128B, MSW = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
-    // A: K-major [M, K] (box {32, 128}); M-major [K, M] (box {32, 32})
-    bool ok = g.a_kmajor ? make_map(ma, g.A, g.K, g.M, g.lda, BK, BM, KSW)
-                         : make_map(ma, g.A, g.M, g.K, g.lda, 32, BK, MSW);
-    ok = ok && (g.b_kmajor ? make_map(mb, g.B, g.K, g.N, g.ldb, BK, BN, KSW)
-                           : make_map(mb, g.B, g.N, g.K, g.ldb, 32, BK, MSW));
-    if (!ok) return GPT2_ENOTSUP;
+    const CUtensorMapSwizzle KSW = CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle MSW = BF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+    // A: K-major [M, K] (box {BK, 128}); M-major [K, M] (box {MN_BOX, BK})
+    bool ok = g.a_kmajor ? make_map(&mp->a, g.A, BF16, g.K, g.M, g.lda, E::BK, BM, KSW)
+                         : make_map(&mp->a, g.A, BF16, g.M, g.K, g.lda, E::MN_BOX, E::BK, MSW);
+    ok = ok && (g.b_kmajor ? make_map(&mp->b, g.B, BF16, g.K, g.N, g.ldb, E::BK, BN, KSW)
+                           : make_map(&mp->b, g.B, BF16, g.N, g.K, g.ldb, E::MN_BOX, E::BK, MSW));
     Params p{};
+    // epilogue maps: output (fp32 128-byte rows or bf16 64-byte rows), aux, pre
+    if (partial) {
+        ok = ok && make_map_3d(&mp->out, partial, g.N, g.M, split, 32, 32);
+    } else {
+        ok = ok && make_map(&mp->out, e.out, e.out_bf16, g.N, g.M, e.ldo, 32, 32,
+                            e.out_bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e.residual) {
+            ok = ok && make_map(&mp->aux, e.residual, false, g.N, g.M, e.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+            p.has_aux = 1;
+            p.aux_residual = 1;
+        } else if (e.gelu_x) {
+            ok = ok && make_map(&mp->aux, e.gelu_x, false, g.N, g.M, e.ldg, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+            p.has_aux = 1;
+        }
+        if (e.gelu) ok = ok && make_map(&mp->pre, e.out_pre, false, g.N, g.M, e.ldo, 32, 32,
+                                        CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!ok) return GPT2_ENOTSUP;
+    if (!p.has_aux) mp->aux = mp->out;             // unused, but a valid map
+    if (!e.gelu || partial) mp->pre = mp->out;
     p.M = g.M; p.N = g.N; p.K = g.K;
     p.a_kmajor = g.a_kmajor; p.b_kmajor = g.b_kmajor;
     p.tiles_m = ceil_div(g.M, BM);
     p.tiles_n = ceil_div(g.N, BN);
-    p.num_kb = ceil_div(g.K, BK);
+    p.num_kb = ceil_div(g.K, E::BK);
     p.split = split;
     p.kb_per_split = ceil_div(p.num_kb, split);
     if (ceil_div(p.num_kb, p.kb_per_split) != split) return GPT2_EINVAL;   // an empty K slice
@@ -512,48 +695,70 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     p.e = e;
     p.partial = partial;
     p.status = g.status;
-    p.mn_layout = LAYOUT_SW128_32B;
-    p.mn_lbo = MN_LBO;
-    p.mn_sbo = MN_SBO;
+    p.mn_layout = BF16 ? LAYOUT_SW128 : LAYOUT_SW128_32B;
+    p.mn_lbo = E::BOX_BYTES;
+    p.mn_sbo = BF16 ? 8 * 128 : 4 * 128;
+    p.gelu = partial ? 0 : e.gelu;
+    p.out_bf16 = partial ? 0 : e.out_bf16;
+    p.bias = partial ? nullptr : e.bias;
     *pp = p;
     return GPT2_OK;
 }
 
-template <int BN>
-static int run(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, cudaStream_t st) {
+template <int BN, bool BF16>
+static int run(const Maps& mp, const Params& p, cudaStream_t st) {
     int grid = (int)std::min<long long>(p.units, num_sms());
-    count_launch(), gemm_tf32_kernel<BN><<<grid, THREADS, Shape<BN>::SMEM, st>>>(ma, mb, p);
+    count_launch(), gemm_tc_kernel<BN, BF16><<<grid, THREADS, Shape<BN, BF16>::SMEM + EPI_BYTES, st>>>(
+        mp.a, mp.b, mp.out, mp.aux, mp.pre, p);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }
 
-template <int BN>
+template <int BN, bool BF16>
 static int launch(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
                   cudaStream_t st) {
-    CUtensorMap ma, mb;
+    Maps mp;
     Params p;
-    int rc = prepare<BN>(g, e, partial, split, &ma, &mb, &p);
+    int rc = prepare<BN, BF16>(g, e, partial, split, &mp, &p);
     if (rc) return rc;
-    return run<BN>(ma, mb, p, st);
+    return run<BN, BF16>(mp, p, st);
+}
+
+template <bool BF16>
+static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
+                      cudaStream_t st) {
+    if (g.N <= 128) return launch<128, BF16>(g, e, partial, split, st);
+    return launch<256, BF16>(g, e, partial, split, st);
 }
 
 }  // namespace tc
 
 bool gemm_tc_supported(const GemmProblem& p) {
     if (p.M < 1 || p.N < 1 || p.K < 1) return false;
-    if (!aligned16(p.A) || !aligned16(p.B) || (p.lda & 3) || (p.ldb & 3)) return false;
+    const int align = p.bf16 ? 8 : 4;             // 16-byte row strides
+    if (!aligned16(p.A) || !aligned16(p.B) || (p.lda % align) || (p.ldb % align)) return false;
     return tc::encode_fn() != nullptr;
 }
 
+// The epilogue moves its tiles with TMA: 16-byte aligned bases and row strides.
+bool gemm_tc_epilogue_supported(const GemmEpilogue& e) {
+    const int oa = e.out_bf16 ? 8 : 4;
+    if (!aligned16(e.out) || e.ldo % oa) return false;
+    if (e.residual && (!aligned16(e.residual) || e.ldo % 4)) return false;
+    if (e.gelu && (!aligned16(e.out_pre) || e.ldo % 4)) return false;
+    if (e.gelu_x && (!aligned16(e.gelu_x) || e.ldg % 4)) return false;
+    if (e.bias && (reinterpret_cast<uintptr_t>(e.bias) & 15)) return false;
+    return true;
+}
+
 int gemm_tc(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st) {
-    if (p.N <= 128) return tc::launch<128>(p, e, nullptr, 1, st);
-    return tc::launch<256>(p, e, nullptr, 1, st);
+    return p.bf16 ? tc::launch_any<true>(p, e, nullptr, 1, st) : tc::launch_any<false>(p, e, nullptr, 1, st);
 }
 
 int gemm_tc_splitk(const GemmProblem& p, float* partial, int split, cudaStream_t st) {
     GemmEpilogue e{};
-    if (p.N <= 128) return tc::launch<128>(p, e, partial, split, st);
-    return tc::launch<256>(p, e, partial, split, st);
+    return p.bf16 ? tc::launch_any<true>(p, e, partial, split, st)
+                  : tc::launch_any<false>(p, e, partial, split, st);
 }
 
 }  // namespace gpt2k

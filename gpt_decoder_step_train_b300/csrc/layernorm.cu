@@ -12,6 +12,8 @@
 // dw/db are reduced deterministically: each block sums its rows in a fixed
 // order into a per-block partial, and a second kernel sums the partials in
 // block order.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace gpt2k {
@@ -20,9 +22,9 @@ constexpr float LN_EPS = 1e-5f;
 constexpr int LN_MAXV = 16;        // float4 per lane: C <= 32*4*16 = 2048
 constexpr int LN_WARPS = 8;
 
-template <int NV>
+template <int NV, bool OUT_BF16>
 __global__ void __launch_bounds__(LN_WARPS * 32)
-ln_fwd_kernel(float* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd,
+ln_fwd_kernel(void* __restrict__ yv, float* __restrict__ mean, float* __restrict__ rstd,
               const float* __restrict__ x, const float* __restrict__ w,
               const float* __restrict__ b, int N, int C) {
     int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
@@ -53,7 +55,6 @@ ln_fwd_kernel(float* __restrict__ y, float* __restrict__ mean, float* __restrict
     float r = rsqrtf(warp_sum(q) / (float)C + LN_EPS);
     const float4* w4 = reinterpret_cast<const float4*>(w);
     const float4* b4 = reinterpret_cast<const float4*>(b);
-    float4* yr = reinterpret_cast<float4*>(y + (size_t)row * C);
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         int c = lane + 32 * i;
@@ -63,7 +64,13 @@ ln_fwd_kernel(float* __restrict__ y, float* __restrict__ mean, float* __restrict
             o.y = (v[i].y - mu) * r * ww.y + bb.y;
             o.z = (v[i].z - mu) * r * ww.z + bb.z;
             o.w = (v[i].w - mu) * r * ww.w + bb.w;
-            yr[c] = o;
+            if (OUT_BF16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(yv) + (size_t)row * C)[c] =
+                    make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+            } else {
+                reinterpret_cast<float4*>(static_cast<float*>(yv) + (size_t)row * C)[c] = o;
+            }
         }
     }
     if (lane == 0) {
@@ -77,7 +84,8 @@ ln_fwd_kernel(float* __restrict__ y, float* __restrict__ mean, float* __restrict
 // partial[blk][1][C] = sum dy over the block's rows.
 template <int NV>
 __global__ void __launch_bounds__(LN_WARPS * 32)
-ln_bwd_kernel(float* __restrict__ dx, float* __restrict__ partial, const float* __restrict__ dy,
+ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* __restrict__ partial,
+              const float* __restrict__ dy,
               const float* __restrict__ x, const float* __restrict__ w,
               const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C,
               int rpb) {
@@ -126,6 +134,11 @@ ln_bwd_kernel(float* __restrict__ dx, float* __restrict__ partial, const float* 
                 xh = (xv.z - mu) * r; g = d.z * ww.z; o.z += r * (g - mg - xh * mgx);
                 xh = (xv.w - mu) * r; g = d.w * ww.w; o.w += r * (g - mg - xh * mgx);
                 dxr[c] = o;
+                if (dx16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                    reinterpret_cast<uint2*>(dx16 + (size_t)row * C)[c] =
+                        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                }
             }
         }
     }
@@ -174,22 +187,38 @@ static int ln_bwd_blocks(int N) { return std::min(ceil_div(N, 32), 512); }
 
 using namespace gpt2k;
 
-GPT2_API int gpt2_op_layernorm_forward(float* y, float* mean, float* rstd, const float* x,
-                                       const float* w, const float* b, int N, int C,
-                                       void* stream) {
+namespace gpt2k {
+int layernorm_forward(void* y, bool out_bf16, float* mean, float* rstd, const float* x,
+                      const float* w, const float* b, int N, int C, cudaStream_t st) {
     if (!y || !mean || !rstd || !x || !w || !b || N < 1 || C < 4 || C % 4 || C > 32 * 4 * LN_MAXV)
         return GPT2_EINVAL;
     if (!aligned16(y) || !aligned16(x) || !aligned16(w) || !aligned16(b)) return GPT2_EINVAL;
     dim3 grid(ceil_div(N, LN_WARPS));
     int nv = ceil_div(C / 4, 32);
-    cudaStream_t st = as_stream(stream);
-    if (nv <= 2) count_launch(), ln_fwd_kernel<2><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C);
-    else if (nv <= 6) count_launch(), ln_fwd_kernel<6><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C);
-    else if (nv <= 8) count_launch(), ln_fwd_kernel<8><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C);
-    else if (nv <= 13) count_launch(), ln_fwd_kernel<13><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C);
-    else count_launch(), ln_fwd_kernel<LN_MAXV><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C);
+#define LNF(NVV)                                                                                   \
+    (out_bf16 ? (count_launch(), ln_fwd_kernel<NVV, true><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C)) \
+              : (count_launch(), ln_fwd_kernel<NVV, false><<<grid, LN_WARPS * 32, 0, st>>>(y, mean, rstd, x, w, b, N, C)))
+    if (nv <= 2) LNF(2);
+    else if (nv <= 6) LNF(6);
+    else if (nv <= 8) LNF(8);
+    else if (nv <= 13) LNF(13);
+    else LNF(LN_MAXV);
+#undef LNF
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
+}
+}  // namespace gpt2k
+
+GPT2_API int gpt2_op_layernorm_forward(float* y, float* mean, float* rstd, const float* x,
+                                       const float* w, const float* b, int N, int C,
+                                       void* stream) {
+    return layernorm_forward(y, false, mean, rstd, x, w, b, N, C, as_stream(stream));
+}
+
+GPT2_API int gpt2_op_layernorm_forward_bf16(void* y, float* mean, float* rstd, const float* x,
+                                            const float* w, const float* b, int N, int C,
+                                            void* stream) {
+    return layernorm_forward(y, true, mean, rstd, x, w, b, N, C, as_stream(stream));
 }
 
 GPT2_API size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C) {
@@ -197,10 +226,10 @@ GPT2_API size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C) {
     return (size_t)ln_bwd_blocks(N) * 2 * C * sizeof(float);
 }
 
-GPT2_API int gpt2_op_layernorm_backward(float* dx, float* dw, float* db, const float* dy,
-                                        const float* x, const float* w, const float* mean,
-                                        const float* rstd, int N, int C, void* scratch,
-                                        size_t scratch_bytes, void* stream) {
+GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db,
+                                        const float* dy, const float* x, const float* w,
+                                        const float* mean, const float* rstd, int N, int C,
+                                        void* scratch, size_t scratch_bytes, void* stream) {
     if (!dx || !dw || !db || !dy || !x || !w || !mean || !rstd || N < 1 || C < 4 || C % 4 ||
         C > 32 * 4 * LN_MAXV)
         return GPT2_EINVAL;
@@ -213,7 +242,9 @@ GPT2_API int gpt2_op_layernorm_backward(float* dx, float* dw, float* db, const f
     size_t smem = 2 * (size_t)C * sizeof(float);
     int nv = ceil_div(C / 4, 32);
     cudaStream_t st = as_stream(stream);
-#define LNB(NVV) count_launch(), ln_bwd_kernel<NVV><<<nblk, LN_WARPS * 32, smem, st>>>(dx, partial, dy, x, w, mean, rstd, N, C, rpb)
+    __nv_bfloat16* dx16 = static_cast<__nv_bfloat16*>(dx_bf16);
+    if (dx16 && (reinterpret_cast<uintptr_t>(dx16) & 7)) return GPT2_EINVAL;
+#define LNB(NVV) count_launch(), ln_bwd_kernel<NVV><<<nblk, LN_WARPS * 32, smem, st>>>(dx, dx16, partial, dy, x, w, mean, rstd, N, C, rpb)
     if (nv <= 2) LNB(2);
     else if (nv <= 6) LNB(6);
     else if (nv <= 8) LNB(8);

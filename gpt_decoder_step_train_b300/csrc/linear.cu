@@ -9,6 +9,8 @@
 // db = column sums of dout.
 #include <mutex>
 
+#include <cuda_bf16.h>
+
 #include "gemm.cuh"
 
 namespace gpt2k {
@@ -18,14 +20,20 @@ namespace gpt2k {
 // rows y, y+8, ... of the chunk in order; the 8 lanes are combined in order.
 constexpr int BG_ROWS = 256;
 
-__global__ void bias_grad_partial_kernel(float* __restrict__ partial, const float* __restrict__ dout,
+template <typename T>
+__device__ __forceinline__ float to_f(T v) { return (float)v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__global__ void bias_grad_partial_kernel(float* __restrict__ partial, const T* __restrict__ dout,
                                          int N, int OC, int ld) {
     __shared__ float sh[8][33];
     int col = blockIdx.x * 32 + threadIdx.x;
     int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
     float s = 0.f;
     if (col < OC)
-        for (int r = r0 + threadIdx.y; r < r1; r += 8) s += dout[(size_t)r * ld + col];
+        for (int r = r0 + threadIdx.y; r < r1; r += 8) s += to_f(dout[(size_t)r * ld + col]);
     sh[threadIdx.y][threadIdx.x] = s;
     __syncthreads();
     if (threadIdx.y == 0 && col < OC) {
@@ -48,10 +56,11 @@ static size_t bias_scratch_bytes(int N, int OC) {
     return round_up((size_t)ceil_div(N, BG_ROWS) * OC * sizeof(float), 256);
 }
 
-static int bias_grad(float* db, const float* dout, int N, int OC, int ld, float* scratch,
+template <typename T>
+static int bias_grad(float* db, const T* dout, int N, int OC, int ld, float* scratch,
                      cudaStream_t st) {
     int nchunk = ceil_div(N, BG_ROWS);
-    count_launch(), bias_grad_partial_kernel<<<dim3(ceil_div(OC, 32), nchunk), dim3(32, 8), 0, st>>>(scratch, dout,
+    count_launch(), bias_grad_partial_kernel<T><<<dim3(ceil_div(OC, 32), nchunk), dim3(32, 8), 0, st>>>(scratch, dout,
                                                                                    N, OC, ld);
     count_launch(), bias_grad_reduce_kernel<<<ceil_div(OC, 256), 256, 0, st>>>(db, scratch, nchunk, OC);
     GPT2_LAUNCH_CHECK();
@@ -82,13 +91,90 @@ static int dw_split(int N, int IC, int OC) {
 }
 
 static int run_gemm(const GemmProblem& p, const GemmEpilogue& e, int mode, cudaStream_t st) {
+    if (p.bf16) {
+        if (mode != GPT2_MODE_BF16 || !gemm_tc_supported(p) || !gemm_tc_epilogue_supported(e))
+            return GPT2_ENOTSUP;
+        return gemm_tc(p, e, st);
+    }
     if (mode == GPT2_MODE_FP32) return gemm_simt(p, e, st);
     if (mode == GPT2_MODE_TF32) {
         // operands TMA cannot address (unaligned base or row stride) take the CUDA cores
-        if (!gemm_tc_supported(p)) return gemm_simt(p, e, st);
+        if (!gemm_tc_supported(p) || !gemm_tc_epilogue_supported(e)) return gemm_simt(p, e, st);
         return gemm_tc(p, e, st);
     }
     return GPT2_EINVAL;
+}
+
+// ---- the three products of a linear layer, for every operand type ---------
+int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, const void* w,
+                   bool bf16, const float* bias, const float* residual, int N, int IC, int OC,
+                   int ld_out, int flags, int mode, int* status, cudaStream_t st) {
+    if (!out || !inp || !w || N < 1 || IC < 1 || OC < 1 || ld_out < OC) return GPT2_EINVAL;
+    if ((flags & GPT2_LINEAR_GELU) && (!out_pre || residual)) return GPT2_EINVAL;
+    GemmProblem p{N, OC, IC, inp, IC, true, w, IC, true, status, bf16};
+    GemmEpilogue e{};
+    e.out = out;
+    e.ldo = ld_out;
+    e.out_bf16 = out_bf16;
+    e.out_pre = out_pre;
+    e.bias = bias;
+    e.residual = residual;
+    e.gelu = (flags & GPT2_LINEAR_GELU) ? 1 : 0;
+    int rc = run_gemm(p, e, mode, st);
+    if (rc) return rc;
+    if ((flags & GPT2_LINEAR_ZERO_PAD) && ld_out > OC) {
+        const size_t es = out_bf16 ? 2 : 4;
+        GPT2_CUDA_TRY(cudaMemset2DAsync(static_cast<char*>(out) + OC * es, (size_t)ld_out * es, 0,
+                                        (size_t)(ld_out - OC) * es, N, st));
+    }
+    return GPT2_OK;
+}
+
+int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
+                          const float* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
+                          int* status, cudaStream_t st) {
+    if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status, bf16};
+    GemmEpilogue e{};
+    e.out = dinp;
+    e.ldo = IC;
+    e.out_bf16 = dinp_bf16;
+    e.gelu_x = gelu_x;
+    e.ldg = IC;
+    return run_gemm(p, e, mode, st);
+}
+
+int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
+                           int OC, int ld_dout, void* scratch, size_t scratch_bytes, int mode,
+                           int* status, cudaStream_t st) {
+    if (!dw || !dout || !inp || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    if (scratch_bytes < gpt2_op_linear_backward_weight_scratch_bytes(N, IC, OC, mode) || !scratch)
+        return GPT2_ENOMEM;
+    GemmProblem p{OC, IC, N, dout, ld_dout, false, inp, IC, false, status, bf16};
+    int split = mode != GPT2_MODE_FP32 ? dw_split(N, IC, OC) : 1;
+    if (split > 1 && gemm_tc_supported(p) && (size_t)OC * IC % 4 == 0 && aligned16(dw)) {
+        float* partial = reinterpret_cast<float*>(scratch);
+        int rc = gemm_tc_splitk(p, partial, split, st);
+        if (rc) return rc;
+        size_t n4 = (size_t)OC * IC / 4;
+        count_launch(), splitk_reduce_kernel<<<ceil_div((long long)n4, 256), 256, 0, st>>>(
+            reinterpret_cast<float4*>(dw), reinterpret_cast<const float4*>(partial), split, n4);
+        GPT2_LAUNCH_CHECK();
+        return GPT2_OK;
+    }
+    GemmEpilogue e{};
+    e.out = dw;
+    e.ldo = IC;
+    return run_gemm(p, e, mode, st);
+}
+
+int bias_grad_any(float* db, const void* dout, bool bf16, int N, int OC, int ld, void* scratch,
+                  size_t scratch_bytes, cudaStream_t st) {
+    if (!db || !dout || N < 1 || OC < 1 || ld < OC) return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < bias_scratch_bytes(N, OC)) return GPT2_ENOMEM;
+    float* sc = reinterpret_cast<float*>(scratch);
+    if (bf16) return bias_grad(db, static_cast<const __nv_bfloat16*>(dout), N, OC, ld, sc, st);
+    return bias_grad(db, static_cast<const float*>(dout), N, OC, ld, sc, st);
 }
 
 }  // namespace gpt2k
@@ -98,43 +184,23 @@ using namespace gpt2k;
 GPT2_API int gpt2_op_linear_forward(float* out, float* out_pre, const float* inp, const float* w,
                                     const float* bias, const float* residual, int N, int IC, int OC,
                                     int ld_out, int flags, int mode, int* status, void* stream) {
-    if (!out || !inp || !w || N < 1 || IC < 1 || OC < 1 || ld_out < OC) return GPT2_EINVAL;
-    if ((flags & GPT2_LINEAR_GELU) && (!out_pre || residual)) return GPT2_EINVAL;
-    cudaStream_t st = as_stream(stream);
-    GemmProblem p{N, OC, IC, inp, IC, true, w, IC, true, status};
-    GemmEpilogue e{};
-    e.out = out;
-    e.ldo = ld_out;
-    e.out_pre = out_pre;
-    e.bias = bias;
-    e.residual = residual;
-    e.gelu = (flags & GPT2_LINEAR_GELU) ? 1 : 0;
-    int rc = run_gemm(p, e, mode, st);
-    if (rc) return rc;
-    if ((flags & GPT2_LINEAR_ZERO_PAD) && ld_out > OC) {
-        GPT2_CUDA_TRY(cudaMemset2DAsync(out + OC, (size_t)ld_out * sizeof(float), 0,
-                                        (size_t)(ld_out - OC) * sizeof(float), N, st));
-    }
-    return GPT2_OK;
+    if (mode == GPT2_MODE_BF16) return GPT2_EINVAL;
+    return linear_forward(out, false, out_pre, inp, w, false, bias, residual, N, IC, OC, ld_out, flags,
+                          mode, status, as_stream(stream));
 }
 
 GPT2_API int gpt2_op_linear_backward_input(float* dinp, const float* dout, const float* w,
                                            const float* gelu_x, int N, int IC, int OC, int ld_dout,
                                            int mode, int* status, void* stream) {
-    if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
-    GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status};
-    GemmEpilogue e{};
-    e.out = dinp;
-    e.ldo = IC;
-    e.gelu_x = gelu_x;
-    e.ldg = IC;
-    return run_gemm(p, e, mode, as_stream(stream));
+    if (mode == GPT2_MODE_BF16) return GPT2_EINVAL;
+    return linear_backward_input(dinp, false, dout, w, false, gelu_x, N, IC, OC, ld_dout, mode, status,
+                                 as_stream(stream));
 }
 
 GPT2_API size_t gpt2_op_linear_backward_weight_scratch_bytes(int N, int IC, int OC, int mode) {
     if (N < 1 || IC < 1 || OC < 1) return 0;
     size_t s = bias_scratch_bytes(N, OC);
-    if (mode == GPT2_MODE_TF32) {
+    if (mode != GPT2_MODE_FP32) {
         int split = dw_split(N, IC, OC);
         if (split > 1) s = std::max(s, (size_t)split * OC * IC * sizeof(float));
     }
@@ -145,30 +211,33 @@ GPT2_API int gpt2_op_linear_backward_weight(float* dw, float* dbias, const float
                                             const float* inp, int N, int IC, int OC, int ld_dout,
                                             void* scratch, size_t scratch_bytes, int mode,
                                             int* status, void* stream) {
-    if (!dw || !dout || !inp || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
-    if (scratch_bytes < gpt2_op_linear_backward_weight_scratch_bytes(N, IC, OC, mode) || !scratch)
-        return GPT2_ENOMEM;
+    if (mode == GPT2_MODE_BF16) return GPT2_EINVAL;
     cudaStream_t st = as_stream(stream);
-    GemmProblem p{OC, IC, N, dout, ld_dout, false, inp, IC, false, status};
-    int rc;
-    int split = mode == GPT2_MODE_TF32 ? dw_split(N, IC, OC) : 1;
-    if (split > 1 && gemm_tc_supported(p) && (size_t)OC * IC % 4 == 0 && aligned16(dw)) {
-        float* partial = reinterpret_cast<float*>(scratch);
-        rc = gemm_tc_splitk(p, partial, split, st);
-        if (rc) return rc;
-        size_t n4 = (size_t)OC * IC / 4;
-        count_launch(), splitk_reduce_kernel<<<ceil_div((long long)n4, 256), 256, 0, st>>>(
-            reinterpret_cast<float4*>(dw), reinterpret_cast<const float4*>(partial), split, n4);
-        GPT2_LAUNCH_CHECK();
-    } else {
-        GemmEpilogue e{};
-        e.out = dw;
-        e.ldo = IC;
-        rc = run_gemm(p, e, mode, st);
-        if (rc) return rc;
-    }
+    int rc = linear_backward_weight(dw, dout, inp, false, N, IC, OC, ld_dout, scratch, scratch_bytes,
+                                    mode, status, st);
+    if (rc) return rc;
     if (dbias) return bias_grad(dbias, dout, N, OC, ld_dout, reinterpret_cast<float*>(scratch), st);
     return GPT2_OK;
+}
+
+GPT2_API int gpt2_op_gemm(const gpt2_gemm_args* a, int mode, int* status, void* stream) {
+    if (!a || !a->A || !a->B || !a->out || a->M < 1 || a->N < 1 || a->K < 1 || a->ldo < a->N)
+        return GPT2_EINVAL;
+    if (a->bf16 && mode != GPT2_MODE_BF16) return GPT2_EINVAL;
+    if (a->gelu && (!a->out_pre || a->residual)) return GPT2_EINVAL;
+    GemmProblem p{a->M, a->N, a->K, a->A, a->lda, a->a_kmajor != 0, a->B, a->ldb, a->b_kmajor != 0,
+                  status, a->bf16 != 0};
+    GemmEpilogue e{};
+    e.out = a->out;
+    e.ldo = a->ldo;
+    e.out_bf16 = a->out_bf16;
+    e.out_pre = a->out_pre;
+    e.bias = a->bias;
+    e.residual = a->residual;
+    e.gelu_x = a->gelu_x;
+    e.ldg = a->ldg;
+    e.gelu = a->gelu;
+    return run_gemm(p, e, mode, as_stream(stream));
 }
 
 GPT2_API size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC) {
@@ -176,11 +245,14 @@ GPT2_API size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC) {
     return bias_scratch_bytes(N, OC);
 }
 
-GPT2_API int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int ld_dout,
-                               void* scratch, size_t scratch_bytes, void* stream) {
+GPT2_API int gpt2_op_bias_grad(float* db, const void* dout, int dout_bf16, int N, int OC,
+                               int ld_dout, void* scratch, size_t scratch_bytes, void* stream) {
     if (!db || !dout || N < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
     if (!scratch || scratch_bytes < bias_scratch_bytes(N, OC)) return GPT2_ENOMEM;
-    return bias_grad(db, dout, N, OC, ld_dout, reinterpret_cast<float*>(scratch), as_stream(stream));
+    float* sc = reinterpret_cast<float*>(scratch);
+    if (dout_bf16)
+        return bias_grad(db, static_cast<const __nv_bfloat16*>(dout), N, OC, ld_dout, sc, as_stream(stream));
+    return bias_grad(db, static_cast<const float*>(dout), N, OC, ld_dout, sc, as_stream(stream));
 }
 
 // ---- allocation-free bias gradient ----------------------------------------

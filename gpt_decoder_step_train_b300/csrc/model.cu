@@ -18,7 +18,7 @@
 #include <functional>
 #include <vector>
 
-#include "common.cuh"
+#include "gemm.cuh"
 
 namespace gpt2k {
 
@@ -62,7 +62,8 @@ static bool config_ok(const gpt2_config* c) {
     if (c->C % 4 || c->C % c->H) return false;
     int hs = c->C / c->H;
     if (hs % 4 || hs > 64 || c->C > 2048) return false;
-    if (c->mode != GPT2_MODE_FP32 && c->mode != GPT2_MODE_TF32) return false;
+    if (c->mode != GPT2_MODE_FP32 && c->mode != GPT2_MODE_TF32 && c->mode != GPT2_MODE_BF16) return false;
+    if (c->mode == GPT2_MODE_BF16 && hs != 16 && hs != 32 && hs != 64) return false;
     if ((long long)c->maxB * c->maxT > (1LL << 30)) return false;
     return true;
 }
@@ -87,14 +88,20 @@ struct gpt2 {
     size_t ws_bytes;
     bool owns_ws;
     cudaStream_t st;
+    bool bf16;                  // GPT2_MODE_BF16: operands below are bf16 (es = 2)
+    size_t es;                  // bytes per element of the operand buffers
     float *grads, *m, *v;
+    void* w16;                  // bf16 copy of the parameters (BF16 mode)
     int *tok, *tgt;
     DevFlags* flags;
-    // activations; per-layer arrays have a fixed stride of R rows
-    float *x0, *ln1, *ln1_mean, *ln1_rstd, *qkv, *atty, *lse, *res2, *ln2, *ln2_mean, *ln2_rstd;
-    float *fch, *fchg, *res3, *lnf, *lnf_mean, *lnf_rstd, *logits, *losses;
-    // backward buffers
-    float *dres, *dln, *dbig, *datty, *dqkv;
+    // fp32 activations; per-layer arrays have a fixed stride of R rows
+    float *x0, *ln1_mean, *ln1_rstd, *lse, *res2, *ln2_mean, *ln2_rstd, *fch, *res3;
+    float *lnf_mean, *lnf_rstd, *logits, *losses;
+    // operand activations (es bytes per element): GEMM / attention inputs
+    char *ln1, *qkv, *atty, *ln2, *fchg, *lnf;
+    // backward: fp32 residual-stream gradient and LN-output gradient; operands
+    float *dres, *dln;
+    char *dres16, *dz16, *dbig, *datty, *dqkv;
     void* scratch;
     size_t scratch_bytes;
     int B, T;
@@ -120,37 +127,41 @@ static size_t plan(gpt2* m, char* base) {
         return p;
     };
     auto F = [&](size_t n) { return reinterpret_cast<float*>(take(n * sizeof(float))); };
+    auto O = [&](size_t n) { return take(n * m->es); };
     const size_t R = m->R, C = c.C, L = c.L, H = c.H, N = m->nparams;
     m->grads = F(N);
     m->m = F(N);
     m->v = F(N);
+    m->w16 = m->bf16 ? take(N * 2) : nullptr;
     m->tok = reinterpret_cast<int*>(take(R * sizeof(int)));
     m->tgt = reinterpret_cast<int*>(take(R * sizeof(int)));
     m->flags = reinterpret_cast<DevFlags*>(take(sizeof(DevFlags)));
     m->x0 = F(R * C);
-    m->ln1 = F(L * R * C);
+    m->ln1 = O(L * R * C);
     m->ln1_mean = F(L * R);
     m->ln1_rstd = F(L * R);
-    m->qkv = F(L * R * 3 * C);
-    m->atty = F(L * R * C);
+    m->qkv = O(L * R * 3 * C);
+    m->atty = O(L * R * C);
     m->lse = F(L * R * H);
     m->res2 = F(L * R * C);
-    m->ln2 = F(L * R * C);
+    m->ln2 = O(L * R * C);
     m->ln2_mean = F(L * R);
     m->ln2_rstd = F(L * R);
     m->fch = F(L * R * 4 * C);
-    m->fchg = F(L * R * 4 * C);
+    m->fchg = O(L * R * 4 * C);
     m->res3 = F(L * R * C);
-    m->lnf = F(R * C);
+    m->lnf = O(R * C);
     m->lnf_mean = F(R);
     m->lnf_rstd = F(R);
     m->logits = F(R * (size_t)m->Vp);
     m->losses = F(R);
     m->dres = F(R * C);
     m->dln = F(R * C);
-    m->dbig = F(R * 4 * C);
-    m->datty = F(R * C);
-    m->dqkv = F(R * 3 * C);
+    m->dres16 = m->bf16 ? O(R * C) : nullptr;
+    m->dz16 = m->bf16 ? O(R * (size_t)m->Vp) : nullptr;
+    m->dbig = O(R * 4 * C);
+    m->datty = O(R * C);
+    m->dqkv = O(R * 3 * C);
     // scratch: the largest need of any backward op at full capacity
     const int Ri = (int)R, Ci = (int)C, mode = c.mode;
     size_t s = 0;
@@ -170,6 +181,15 @@ static size_t plan(gpt2* m, char* base) {
 
 static float* P(gpt2* m, int t) { return m->params + m->off[t]; }
 static float* G(gpt2* m, int t) { return m->grads + m->off[t]; }
+// GEMM weight operand: the bf16 copy in BF16 mode, else the fp32 parameters
+static const void* W(gpt2* m, int t) {
+    return m->bf16 ? static_cast<const void*>(static_cast<const char*>(m->w16) + 2 * m->off[t])
+                   : static_cast<const void*>(m->params + m->off[t]);
+}
+// operand row r (per-layer stride R rows) of an es-byte buffer
+static char* Orow(gpt2* m, char* base, size_t layer, size_t width) {
+    return base + layer * (size_t)m->R * width * m->es;
+}
 
 // Run one operation; when tracing, bracket it with events on the model's stream.
 static int trace_op(gpt2* m, int cls, const std::function<int()>& f) {
@@ -199,43 +219,49 @@ static int trace_op(gpt2* m, int cls, const std::function<int()>& f) {
 static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
     const gpt2_config& c = m->cfg;
     const int C = c.C, L = c.L, H = c.H, N = B * T, mode = c.mode;
+    const bool b16 = m->bf16;
     const size_t R = m->R;
-    void* st = m->st;
+    cudaStream_t st = m->st;
     int* status = &m->flags->status;
+    if (b16) OP(OTHER, to_bf16(m->w16, m->params, m->nparams, st));
     OP(ENCODER_FWD, gpt2_op_encoder_forward(m->x0, m->tok, P(m, WTE), P(m, WPE), B, T, C, c.V, status, st));
     for (int l = 0; l < L; l++) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
-        float* ln1 = m->ln1 + l * R * C;
-        float* qkv = m->qkv + l * R * 3 * C;
-        float* atty = m->atty + l * R * C;
+        char* ln1 = Orow(m, m->ln1, l, C);
+        char* qkv = Orow(m, m->qkv, l, 3 * C);
+        char* atty = Orow(m, m->atty, l, C);
         float* res2 = m->res2 + l * R * C;
-        float* ln2 = m->ln2 + l * R * C;
+        char* ln2 = Orow(m, m->ln2, l, C);
         float* fch = m->fch + l * R * 4 * C;
-        float* fchg = m->fchg + l * R * 4 * C;
+        char* fchg = Orow(m, m->fchg, l, 4 * C);
         float* res3 = m->res3 + l * R * C;
-        size_t cc = (size_t)C * C;
-        OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(ln1, m->ln1_mean + l * R, m->ln1_rstd + l * R, x,
-                                       P(m, LN1W) + l * C, P(m, LN1B) + l * C, N, C, st));
-        OP(MATMUL_FWD, gpt2_op_linear_forward(qkv, nullptr, ln1, P(m, QKVW) + l * 3 * cc,
-                                    P(m, QKVB) + l * 3 * C, nullptr, N, C, 3 * C, 3 * C, 0, mode, status, st));
+        const size_t cc = (size_t)C * C;
+        const size_t wes = b16 ? 2 : 4;
+        auto Wl = [&](int t, size_t per_layer) {
+            return static_cast<const void*>(static_cast<const char*>(W(m, t)) + l * per_layer * wes);
+        };
+        OP(LAYERNORM_FWD, layernorm_forward(ln1, b16, m->ln1_mean + l * R, m->ln1_rstd + l * R, x,
+                                            P(m, LN1W) + l * C, P(m, LN1B) + l * C, N, C, st));
+        OP(MATMUL_FWD, linear_forward(qkv, b16, nullptr, ln1, Wl(QKVW, 3 * cc), b16, P(m, QKVB) + l * 3 * C,
+                                      nullptr, N, C, 3 * C, 3 * C, 0, mode, status, st));
         OP(ATTENTION_FWD, gpt2_op_attention_forward(atty, m->lse + l * R * H, qkv, B, T, C, H, mode, status, st));
-        OP(MATMUL_FWD, gpt2_op_linear_forward(res2, nullptr, atty, P(m, ATTPROJW) + l * cc,
-                                    P(m, ATTPROJB) + l * C, x, N, C, C, C, 0, mode, status, st));
-        OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(ln2, m->ln2_mean + l * R, m->ln2_rstd + l * R, res2,
-                                       P(m, LN2W) + l * C, P(m, LN2B) + l * C, N, C, st));
-        OP(MATMUL_FWD, gpt2_op_linear_forward(fchg, fch, ln2, P(m, FCW) + l * 4 * cc, P(m, FCB) + l * 4 * C,
-                                    nullptr, N, C, 4 * C, 4 * C, GPT2_LINEAR_GELU, mode, status, st));
-        OP(MATMUL_FWD, gpt2_op_linear_forward(res3, nullptr, fchg, P(m, FCPROJW) + l * 4 * cc,
-                                    P(m, FCPROJB) + l * C, res2, N, 4 * C, C, C, 0, mode, status, st));
+        OP(MATMUL_FWD, linear_forward(res2, false, nullptr, atty, Wl(ATTPROJW, cc), b16, P(m, ATTPROJB) + l * C,
+                                      x, N, C, C, C, 0, mode, status, st));
+        OP(LAYERNORM_FWD, layernorm_forward(ln2, b16, m->ln2_mean + l * R, m->ln2_rstd + l * R, res2,
+                                            P(m, LN2W) + l * C, P(m, LN2B) + l * C, N, C, st));
+        OP(MATMUL_FWD, linear_forward(fchg, b16, fch, ln2, Wl(FCW, 4 * cc), b16, P(m, FCB) + l * 4 * C, nullptr,
+                                      N, C, 4 * C, 4 * C, GPT2_LINEAR_GELU, mode, status, st));
+        OP(MATMUL_FWD, linear_forward(res3, false, nullptr, fchg, Wl(FCPROJW, 4 * cc), b16,
+                                      P(m, FCPROJB) + l * C, res2, N, 4 * C, C, C, 0, mode, status, st));
     }
     const float* xL = m->res3 + (size_t)(L - 1) * R * C;
-    OP(LAYERNORM_FWD, gpt2_op_layernorm_forward(m->lnf, m->lnf_mean, m->lnf_rstd, xL, P(m, LNFW), P(m, LNFB),
-                                   N, C, st));
-    OP(MATMUL_FWD, gpt2_op_linear_forward(m->logits, nullptr, m->lnf, P(m, WTE), nullptr, nullptr, N, C, c.V,
-                                m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
+    OP(LAYERNORM_FWD, layernorm_forward(m->lnf, b16, m->lnf_mean, m->lnf_rstd, xL, P(m, LNFW), P(m, LNFB),
+                                        N, C, st));
+    OP(MATMUL_FWD, linear_forward(m->logits, false, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N, C,
+                                  c.V, m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
     if (with_targets) {
-        OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->tgt, N, c.V, m->Vp, 1.0f / (float)N,
-                                  status, st));
+        OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->dz16, m->tgt, N, c.V, m->Vp,
+                                              1.0f / (float)N, status, st));
         OP(CROSSENTROPY, gpt2_op_sum(&m->flags->loss, m->losses, N, 1.0f / (float)N, st));
     }
     return GPT2_OK;
@@ -244,68 +270,76 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
 static int backward_impl(gpt2* m) {
     const gpt2_config& c = m->cfg;
     const int B = m->B, T = m->T, C = c.C, L = c.L, H = c.H, N = B * T, mode = c.mode;
+    const bool b16 = m->bf16;
     const size_t R = m->R, cc = (size_t)C * C;
-    void* st = m->st;
+    cudaStream_t st = m->st;
     void* sc = m->scratch;
     const size_t sb = m->scratch_bytes;
     int* status = &m->flags->status;
+    // operand views of the residual-stream gradient and of dlogits
+    const void* dres_op = b16 ? static_cast<const void*>(m->dres16) : static_cast<const void*>(m->dres);
+    const void* dz_op = b16 ? static_cast<const void*>(m->dz16) : static_cast<const void*>(m->logits);
+    const size_t wes = b16 ? 2 : 4;
     // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
-    OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->logits, P(m, WTE), nullptr, N, C, c.V, m->Vp,
-                                       mode, status, st));
-    OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, WTE), nullptr, m->logits, m->lnf, N, C, c.V, m->Vp,
-                                        sc, sb, mode, status, st));
+    OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, dz_op, W(m, WTE), b16, nullptr, N, C, c.V,
+                                               m->Vp, mode, status, st));
+    OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, WTE), dz_op, m->lnf, b16, N, C, c.V, m->Vp, sc, sb,
+                                                 mode, status, st));
     OP(OTHER, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), m->st) == cudaSuccess
                   ? GPT2_OK : GPT2_ECUDA);
-    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LNFW), G(m, LNFB), m->dln,
-                                    m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW), m->lnf_mean,
-                                    m->lnf_rstd, N, C, sc, sb, st));
+    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LNFW), G(m, LNFB), m->dln,
+                                                 m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW),
+                                                 m->lnf_mean, m->lnf_rstd, N, C, sc, sb, st));
     for (int l = L - 1; l >= 0; l--) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
-        const float* ln1 = m->ln1 + l * R * C;
-        const float* qkv = m->qkv + l * R * 3 * C;
-        const float* atty = m->atty + l * R * C;
+        const char* ln1 = Orow(m, m->ln1, l, C);
+        const char* qkv = Orow(m, m->qkv, l, 3 * C);
+        const char* atty = Orow(m, m->atty, l, C);
         const float* res2 = m->res2 + l * R * C;
-        const float* ln2 = m->ln2 + l * R * C;
+        const char* ln2 = Orow(m, m->ln2, l, C);
         const float* fch = m->fch + l * R * 4 * C;
-        const float* fchg = m->fchg + l * R * 4 * C;
+        const char* fchg = Orow(m, m->fchg, l, 4 * C);
+        auto Wl = [&](int t, size_t per_layer) {
+            return static_cast<const void*>(static_cast<const char*>(W(m, t)) + l * per_layer * wes);
+        };
         // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g; dbfp
-        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dbig, m->dres, P(m, FCPROJW) + l * 4 * cc, fch, N,
-                                           4 * C, C, C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, nullptr, m->dres, fchg, N, 4 * C, C,
-                                                              C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, FCPROJB) + l * C, m->dres, N, C, C, sc, sb, st));
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dres_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
+                                                   4 * C, C, C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dres_op, fchg, b16, N,
+                                                     4 * C, C, C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, bias_grad_any(G(m, FCPROJB) + l * C, m->dres, false, N, C, C, sc, sb, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
-        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->dbig, P(m, FCW) + l * 4 * cc, nullptr, N, C,
-                                           4 * C, 4 * C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, FCW) + l * 4 * cc, nullptr, m->dbig, ln2, N, C, 4 * C,
-                                                              4 * C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, FCB) + l * 4 * C, m->dbig, N, 4 * C, 4 * C, sc, sb, st));
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dbig, Wl(FCW, 4 * cc), b16, nullptr, N,
+                                                   C, 4 * C, 4 * C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCW) + l * 4 * cc, m->dbig, ln2, b16, N, C, 4 * C,
+                                                     4 * C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, bias_grad_any(G(m, FCB) + l * 4 * C, m->dbig, b16, N, 4 * C, 4 * C, sc, sb, st));
         // ln_2: dres += LN'(dln2)
-        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LN2W) + l * C, G(m, LN2B) + l * C, m->dln,
-                                        res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
-                                        m->ln2_rstd + l * R, N, C, sc, sb, st));
+        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN2W) + l * C, G(m, LN2B) + l * C,
+                                                     m->dln, res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
+                                                     m->ln2_rstd + l * R, N, C, sc, sb, st));
         // attention c_proj
-        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->datty, m->dres, P(m, ATTPROJW) + l * cc, nullptr, N,
-                                           C, C, C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, ATTPROJW) + l * cc, nullptr, m->dres, atty, N, C, C,
-                                                              C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, ATTPROJB) + l * C, m->dres, N, C, C, sc, sb, st));
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, dres_op, Wl(ATTPROJW, cc), b16, nullptr, N,
+                                                   C, C, C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dres_op, atty, b16, N, C, C, C,
+                                                     sc, sb, mode, status, st));
+        OP(BIAS_GRAD, bias_grad_any(G(m, ATTPROJB) + l * C, m->dres, false, N, C, C, sc, sb, st));
         // attention
-        OP(ATTENTION_BWD, gpt2_op_attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C,
-                                        H, sc, sb, mode, status, st));
+        OP(ATTENTION_BWD, gpt2_op_attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T,
+                                                     C, H, sc, sb, mode, status, st));
         // c_attn
-        OP(MATMUL_BWD_INPUT, gpt2_op_linear_backward_input(m->dln, m->dqkv, P(m, QKVW) + l * 3 * cc, nullptr, N, C,
-                                           3 * C, 3 * C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, gpt2_op_linear_backward_weight(G(m, QKVW) + l * 3 * cc, nullptr, m->dqkv, ln1, N, C, 3 * C,
-                                                              3 * C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, gpt2_op_bias_grad(G(m, QKVB) + l * 3 * C, m->dqkv, N, 3 * C, 3 * C, sc, sb, st));
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dqkv, Wl(QKVW, 3 * cc), b16, nullptr, N,
+                                                   C, 3 * C, 3 * C, mode, status, st));
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, QKVW) + l * 3 * cc, m->dqkv, ln1, b16, N, C, 3 * C,
+                                                     3 * C, sc, sb, mode, status, st));
+        OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->dqkv, b16, N, 3 * C, 3 * C, sc, sb, st));
         // ln_1: dres += LN'(dln1)
-        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, G(m, LN1W) + l * C, G(m, LN1B) + l * C, m->dln, x,
-                                        P(m, LN1W) + l * C, m->ln1_mean + l * R,
-                                        m->ln1_rstd + l * R, N, C, sc, sb, st));
+        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN1W) + l * C, G(m, LN1B) + l * C,
+                                                     m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R,
+                                                     m->ln1_rstd + l * R, N, C, sc, sb, st));
     }
-    OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V, sc,
-                                  sb, st));
+    OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V,
+                                             sc, sb, st));
     return GPT2_OK;
 }
 
@@ -334,6 +368,8 @@ GPT2_API size_t gpt2_workspace_bytes(const gpt2_config* cfg) {
     tmp.Vp = padded_vocab(cfg->V);
     tmp.R = cfg->maxB * cfg->maxT;
     tmp.nparams = gpt2_num_params(cfg);
+    tmp.bf16 = cfg->mode == GPT2_MODE_BF16;
+    tmp.es = tmp.bf16 ? 2 : 4;
     return plan(&tmp, nullptr);
 }
 
@@ -346,6 +382,8 @@ GPT2_API int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out) {
     m->Vp = padded_vocab(cfg->V);
     m->R = cfg->maxB * cfg->maxT;
     m->nparams = gpt2_num_params(cfg);
+    m->bf16 = cfg->mode == GPT2_MODE_BF16;
+    m->es = m->bf16 ? 2 : 4;
     tensor_sizes(*cfg, m->sz);
     size_t o = 0;
     for (int i = 0; i < NT; i++) { m->off[i] = o; o += m->sz[i]; }
@@ -506,17 +544,18 @@ GPT2_API const float* gpt2_losses(gpt2* m) { return m ? m->losses : nullptr; }
 GPT2_API const float* gpt2_activation(gpt2* m, int which, int layer) {
     if (!m || layer < 0 || layer >= m->cfg.L) return nullptr;
     const size_t R = m->R, C = m->cfg.C, l = layer;
+    auto op = [&](char* base, size_t width) { return reinterpret_cast<const float*>(Orow(m, base, l, width)); };
     switch (which) {
         case 0: return m->x0;
-        case 1: return m->ln1 + l * R * C;
-        case 2: return m->qkv + l * R * 3 * C;
-        case 3: return m->atty + l * R * C;
+        case 1: return op(m->ln1, C);
+        case 2: return op(m->qkv, 3 * C);
+        case 3: return op(m->atty, C);
         case 4: return m->res2 + l * R * C;
-        case 5: return m->ln2 + l * R * C;
+        case 5: return op(m->ln2, C);
         case 6: return m->fch + l * R * 4 * C;
-        case 7: return m->fchg + l * R * 4 * C;
+        case 7: return op(m->fchg, 4 * C);
         case 8: return m->res3 + l * R * C;
-        case 9: return m->lnf;
+        case 9: return reinterpret_cast<const float*>(m->lnf);
         default: return nullptr;
     }
 }

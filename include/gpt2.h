@@ -48,6 +48,14 @@ extern "C" {
 /* arithmetic modes for the contractions (GEMMs and attention) */
 #define GPT2_MODE_FP32 0   /* strict fp32 on the CUDA cores                     */
 #define GPT2_MODE_TF32 1   /* tensor cores: tf32 operands, fp32 accumulation    */
+#define GPT2_MODE_BF16 2   /* tensor cores: bf16 operands, fp32 accumulation;
+                              weights keep fp32 masters; the residual stream,
+                              LayerNorm statistics, softmax, loss and every
+                              gradient reduction stay fp32; GEMM and attention
+                              operands (LayerNorm outputs, qkv, attention
+                              output, GELU output, dlogits, residual-stream
+                              gradient copy, dh, d(attention out), dqkv) are
+                              stored in bf16 by the kernel that produces them */
 
 typedef struct {
     int V;           /* vocabulary size (50257 for GPT-2)                       */

@@ -11,8 +11,10 @@
  *     asynchronous on it.  Return value: GPT2_OK or a negative GPT2_E* code for
  *     argument errors or a failed launch.  Device-side data errors (ids
  *     outside [0, V)) OR a GPT2_STATUS_* bit into *status when status != NULL.
- *   - `mode` selects the contraction arithmetic: GPT2_MODE_FP32 (CUDA cores)
- *     or GPT2_MODE_TF32 (tcgen05 tensor cores, fp32 accumulation).  In TF32
+ *   - `mode` selects the contraction arithmetic: GPT2_MODE_FP32 (CUDA cores),
+ *     GPT2_MODE_TF32 or GPT2_MODE_BF16 (tensor cores, fp32 accumulation).  The
+ *     linear ops below take fp32 operands (FP32 and TF32 modes); bf16 products
+ *     go through gpt2_op_gemm.  In TF32
  *     mode a product whose operands the tensor-memory-access unit cannot read
  *     (a base address not 16-byte aligned, a row stride not a multiple of 4)
  *     runs on the CUDA cores instead; the model's own buffers never do.
@@ -51,16 +53,20 @@ int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx, const in
 
 /* LayerNorm over rows of x [N,C] (16B): mean, rstd = 1/sqrt(var + 1e-5)
  * (biased variance), y = (x-mean)*rstd*w + b.  mean, rstd [N] are saved for
- * the backward.  ("GPT-2 from scratch with torch", Transformer block, eps 1e-5.) */
+ * the backward.  ("GPT-2 from scratch with torch", Transformer block, eps 1e-5.)
+ * The _bf16 form writes y as bf16 (round to nearest even). */
 int gpt2_op_layernorm_forward(float* y, float* mean, float* rstd, const float* x,
                               const float* w, const float* b, int N, int C, void* stream);
+int gpt2_op_layernorm_forward_bf16(void* y, float* mean, float* rstd, const float* x,
+                                   const float* w, const float* b, int N, int C, void* stream);
 
 /* LayerNorm backward.  dx += rstd*(g - mean(g) - xhat*mean(g*xhat)) with
  * g = dy*w and xhat = (x-mean)*rstd (dx is ACCUMULATED: it is the residual
  * stream's gradient); dw = sum_rows dy*xhat, db = sum_rows dy (OVERWRITTEN),
- * reduced in a fixed order.  scratch: gpt2_op_layernorm_backward_scratch_bytes. */
+ * reduced in a fixed order.  dx_bf16 [N,C] (8-byte aligned) or NULL: also
+ * receives the updated dx in bf16.  scratch: gpt2_op_layernorm_backward_scratch_bytes. */
 size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C);
-int gpt2_op_layernorm_backward(float* dx, float* dw, float* db, const float* dy,
+int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, const float* dy,
                                const float* x, const float* w, const float* mean,
                                const float* rstd, int N, int C, void* scratch,
                                size_t scratch_bytes, void* stream);
@@ -95,11 +101,36 @@ int gpt2_op_linear_backward_weight(float* dw, float* dbias, const float* dout,
                                    void* stream);
 
 /* Bias gradient alone: db[o] = sum_n dout[n*ld_dout + o] for o < OC,
- * OVERWRITTEN, summed in a fixed order (row chunks, then chunk order).
+ * OVERWRITTEN, summed in fp32 in a fixed order (row chunks, then chunk order).
+ * dout is fp32, or bf16 when dout_bf16 != 0.
  * scratch: gpt2_op_bias_grad_scratch_bytes(N, OC) bytes. */
 size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC);
-int gpt2_op_bias_grad(float* db, const float* dout, int N, int OC, int ld_dout, void* scratch,
-                      size_t scratch_bytes, void* stream);
+int gpt2_op_bias_grad(float* db, const void* dout, int dout_bf16, int N, int OC, int ld_dout,
+                      void* scratch, size_t scratch_bytes, void* stream);
+
+/* General GEMM on one product: D[m,n] = sum_k A(m,k) B(n,k), fp32 accumulation,
+ * then the linear-layer epilogue.  A(m,k) = A[m*lda + k] when a_kmajor, else
+ * A[k*lda + m]; B(n,k) = B[n*ldb + k] when b_kmajor, else B[k*ldb + n].  A and B
+ * are fp32 (mode FP32 or TF32) or bf16 (bf16 != 0, mode BF16; tensor cores
+ * only).  Epilogue per element, in this order: + bias[n]; GELU (out_pre = value,
+ * value = gelu(value)); + residual[m*ldo+n]; * gelu'(gelu_x[m*ldg+n]); stored to
+ * out[m*ldo+n] as fp32, or bf16 when out_bf16.  Pointers may be NULL to skip. */
+typedef struct {
+    int M, N, K;
+    const void* A; int lda; int a_kmajor;
+    const void* B; int ldb; int b_kmajor;
+    int bf16;
+    void* out; int ldo; int out_bf16;
+    float* out_pre;
+    const float* bias;
+    const float* residual;
+    const float* gelu_x; int ldg;
+    int gelu;
+} gpt2_gemm_args;
+int gpt2_op_gemm(const gpt2_gemm_args* args, int mode, int* status, void* stream);
+
+/* fp32 -> bf16, round to nearest even, n values. */
+int gpt2_op_to_bf16(void* dst, const float* src, size_t n, void* stream);
 
 /* Allocation-free bias gradient.  Same result as gpt2_op_bias_grad, but the
  * caller passes no scratch and the library allocates nothing: the partial sums
@@ -125,26 +156,30 @@ int gpt2_op_bias_grad_noalloc(float* db, const float* dout, int N, int OC, int l
 /* Causal self-attention forward over qkv [B,T,3C] (queries, keys, values at
  * column offsets 0, C, 2C; head h owns columns h*hs..h*hs+hs-1 of each):
  * per (b,h), O = softmax(mask(Q K^T / sqrt(hs))) V, heads side by side in
- * y [B,T,C]; lse [B,H,T] receives the row log-sum-exp of the scaled scores.
- * ("GPT-2 from scratch with torch", section 自注意力.)  hs <= 128, hs % 4 == 0. */
-int gpt2_op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C,
+ * y [B,T,C]; lse [B,H,T] (fp32) receives the row log-sum-exp of the scaled
+ * scores.  ("GPT-2 from scratch with torch", section 自注意力.)  hs <= 64,
+ * hs % 4 == 0.  qkv and y are fp32, or bf16 in GPT2_MODE_BF16 (hs 16, 32, 64). */
+int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
                               int H, int mode, int* status, void* stream);
 
 /* Causal self-attention backward: dqkv [B,T,3C] (OVERWRITTEN) from dy [B,T,C],
- * the forward's qkv, y and lse.  scratch: gpt2_op_attention_backward_scratch_bytes. */
+ * the forward's qkv, y and lse; dqkv, dy, qkv, y are bf16 in GPT2_MODE_BF16.
+ * scratch: gpt2_op_attention_backward_scratch_bytes. */
 size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
-int gpt2_op_attention_backward(float* dqkv, const float* dy, const float* qkv, const float* y,
+int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y,
                                const float* lse, int B, int T, int C, int H, void* scratch,
                                size_t scratch_bytes, int mode, int* status, void* stream);
 
 /* Fused softmax cross-entropy over logits z [N, ld] (16B, ld % 4 == 0, ld >= V):
- * losses[n] = logsumexp(z[n,:V]) - z[n,tgt[n]]; then, IN PLACE,
- * z[n,v] = (softmax(z[n,:V])[v] - [v == tgt[n]]) * dscale for v < V and 0 for
- * V <= v < ld.  dscale is 1/(number of positions) for the mean loss; 0 skips
- * the gradient (z is left unchanged).  A target outside [0,V) sets BAD_TARGET
- * and that row's loss and gradient to 0.  ("从头搭建GPT 笔记", section 计算loss.) */
-int gpt2_op_crossentropy(float* losses, float* z, const int* tgt, int N, int V, int ld,
-                         float dscale, int* status, void* stream);
+ * losses[n] = logsumexp(z[n,:V]) - z[n,tgt[n]]; then the gradient
+ * (softmax(z[n,:V])[v] - [v == tgt[n]]) * dscale for v < V and 0 for V <= v < ld
+ * is written IN PLACE over z, or, when dz_bf16 != NULL, to dz_bf16 [N, ld]
+ * (bf16, 8-byte aligned) with z left unchanged.  dscale is 1/(number of
+ * positions) for the mean loss; 0 skips the gradient.  A target outside [0,V)
+ * sets BAD_TARGET and that row's loss and gradient to 0.  ("从头搭建GPT 笔记",
+ * section 计算loss.) */
+int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const int* tgt, int N, int V,
+                         int ld, float dscale, int* status, void* stream);
 
 /* Sum of losses[N] in a fixed order, times `scale`, written to *out (device). */
 int gpt2_op_sum(float* out, const float* losses, int N, float scale, void* stream);

@@ -154,7 +154,7 @@ def test_layernorm_backward(L, B_, o64, N, C):
     db = torch.empty(C, device="cuda")
     nbytes = L.gpt2_op_layernorm_backward_scratch_bytes(N, C)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), B_.ptr(dw), B_.ptr(db), B_.ptr(dev(dy)),
+    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), None, B_.ptr(dw), B_.ptr(db), B_.ptr(dev(dy)),
                                         B_.ptr(dev(x)), B_.ptr(dev(w)), B_.ptr(mean), B_.ptr(rstd),
                                         N, C, B_.ptr(scratch), nbytes, None) == 0
     wdx, wdw, wdb = o64.layernorm_backward(dy, x, w, wm.astype(np.float32), wr.astype(np.float32))
@@ -288,7 +288,7 @@ def test_crossentropy(L, B_, o64, N, V):
     losses = torch.empty(N, device="cuda")
     dz = dev(z)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    assert L.gpt2_op_crossentropy(B_.ptr(losses), B_.ptr(dz), B_.ptr(dev(tgt)), N, V, ld,
+    assert L.gpt2_op_crossentropy(B_.ptr(losses), B_.ptr(dz), None, B_.ptr(dev(tgt)), N, V, ld,
                                   1.0 / N, B_.ptr(st), None) == 0
     mean, wl, probs = o64.crossentropy_forward(z, tgt, V=V)
     wdz = o64.crossentropy_backward(probs, tgt, ld=ld)
@@ -311,7 +311,7 @@ def test_crossentropy_flags_bad_target(L, B_):
     tgt = dev(np.array([1, 10, 2], dtype=np.int32))
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     losses = torch.empty(N, device="cuda")
-    assert L.gpt2_op_crossentropy(B_.ptr(losses), B_.ptr(z), B_.ptr(tgt), N, V, ld, 1.0,
+    assert L.gpt2_op_crossentropy(B_.ptr(losses), B_.ptr(z), None, B_.ptr(tgt), N, V, ld, 1.0,
                                   B_.ptr(st), None) == 0
     assert int(host(st)[0]) & B_.STATUS_BAD_TARGET
     assert np.all(host(z)[1] == 0) and host(losses)[1] == 0

@@ -20,7 +20,7 @@ def _reference(L, B_, dout, N, OC, ld):
     db = torch.empty(OC, device="cuda")
     nbytes = L.gpt2_op_bias_grad_scratch_bytes(N, OC)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    assert L.gpt2_op_bias_grad(B_.ptr(db), B_.ptr(dout), N, OC, ld, B_.ptr(scratch), nbytes,
+    assert L.gpt2_op_bias_grad(B_.ptr(db), B_.ptr(dout), 0, N, OC, ld, B_.ptr(scratch), nbytes,
                                None) == 0
     torch.cuda.synchronize()
     return db.cpu().numpy()
