@@ -2,8 +2,9 @@
 """Throughput of one GPT-2 training step (forward, backward, AdamW) on a B300.
 
 Default workload: GPT-2 124M (V 50257, L 12, H 12, C 768) at B=16, T=1024 with
-tensor-core (tf32) contractions, seeded synthetic parameters and a Zipf(1.1)
-token stream.  Prints one JSON line (rank 0).
+tensor-core contractions on bf16 operands (fp32 accumulation, fp32 master
+weights; --mode tf32 or fp32 for the other arithmetic), seeded synthetic
+parameters and a Zipf(1.1) token stream.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -43,7 +44,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="124M", choices=list(syn.CONFIGS))
-    ap.add_argument("--mode", default="tf32", choices=["tf32", "bf16", "fp32"])
+    ap.add_argument("--mode", default="bf16", choices=["bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
@@ -247,8 +248,6 @@ def run_ours(args, cfg):
         except ValueError:
             pass
     clocks = ClockSampler(gpu_index)
-    if not args.no_trace:
-        model.trace(True)
     barrier()
     clocks.start()
     n_launch0 = binding.lib().gpt2_kernel_launches()
@@ -263,8 +262,18 @@ def run_ours(args, cfg):
     clock_info = clocks.stop()
     launches = binding.lib().gpt2_kernel_launches() - n_launch0
     ms_total = max_over_ranks(e0.elapsed_time(e1))
-    kernels = model.trace_read() if not args.no_trace else {}
-    model.trace(False)
+    # per-kernel times: a second pass of the same steps with CUDA events around
+    # every operation on the model's stream (kept out of the timed region above,
+    # whose value the event records would slow by a few percent)
+    kernels = {}
+    if not args.no_trace:
+        model.trace(True)
+        barrier()
+        for i in range(args.steps):
+            step(*dev_pool[i % len(dev_pool)])
+        barrier()
+        kernels = model.trace_read()
+        model.trace(False)
     st = model.status()
     if st != 0:
         raise RuntimeError(f"timed steps failed: {binding.strerror(st)}")

@@ -63,7 +63,7 @@ SIGNATURES = {
     "gpt2_trace_read": (_i, [_vp, _vp, _vp, _i]),
     "gpt2_kernel_launches": (C.c_longlong, []),
     "gpt2_op_encoder_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
-    "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i]),
+    "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_encoder_backward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "gpt2_op_layernorm_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_op_layernorm_forward_bf16": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),

@@ -17,66 +17,70 @@ namespace gpt2k {
 
 constexpr int CE_THREADS = 512;
 
-__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
-    if (m2 == -INFINITY) return;
-    if (m == -INFINITY) { m = m2; s = s2; return; }
-    if (m2 > m) { s = s * expf(m - m2) + s2; m = m2; }
-    else s += s2 * expf(m2 - m);
+constexpr float CE_LOG2E = 1.4426950408889634f;
+constexpr float CE_LN2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, u) : v + u;
+    }
+    __syncthreads();                       // sh may still be read from the previous reduction
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    float r = sh[0];
+    for (int k = 1; k < CE_THREADS / 32; k++) r = is_max ? fmaxf(r, sh[k]) : r + sh[k];
+    return r;
 }
 
+// Pass 1 reads the row from DRAM (128-bit loads) for its maximum; passes 2
+// (sum of exp) and 3 (gradient) re-read it from L2.  Exponentials are exp2 of
+// log2(e)-scaled differences.
 __global__ void __launch_bounds__(CE_THREADS)
 crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bfloat16* __restrict__ dz16,
                     const int* __restrict__ tgt, int V, int ld, float dscale, int* status) {
-    __shared__ float sm[CE_THREADS / 32], ss[CE_THREADS / 32];
-    __shared__ float s_lse, s_zt;
+    __shared__ float sh[CE_THREADS / 32];
     const int row = blockIdx.x, tid = threadIdx.x;
     float* zr = z + (size_t)row * ld;
     float4* z4 = reinterpret_cast<float4*>(zr);
+    const int nfull = V >> 2;                      // float4s entirely inside [0, V)
     const int n4 = ld >> 2;
-    float m = -INFINITY, s = 0.f;
-    for (int c = tid; c < n4; c += CE_THREADS) {
-        float4 v = z4[c];
-        float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            if (c * 4 + k < V) {
-                float x = e[k];
-                if (x > m) { s = s * expf(m - x) + 1.f; m = x; }
-                else s += expf(x - m);
-            }
-        }
+    float mx = -INFINITY;
+    for (int c = tid; c < nfull; c += CE_THREADS) {
+        const float4 v = z4[c];
+        mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        lse_combine(m, s, m2, s2);
+    for (int v = nfull * 4 + tid; v < V; v += CE_THREADS) mx = fmaxf(mx, zr[v]);
+    const float M = block_reduce(mx, sh, true);
+    const float Ml = M * CE_LOG2E;
+    float sum = 0.f;
+    for (int c = tid; c < nfull; c += CE_THREADS) {
+        const float4 v = z4[c];
+        sum += (exp2f(fmaf(v.x, CE_LOG2E, -Ml)) + exp2f(fmaf(v.y, CE_LOG2E, -Ml))) +
+               (exp2f(fmaf(v.z, CE_LOG2E, -Ml)) + exp2f(fmaf(v.w, CE_LOG2E, -Ml)));
     }
-    if ((tid & 31) == 0) { sm[tid >> 5] = m; ss[tid >> 5] = s; }
-    __syncthreads();
-    if (tid == 0) {
-        float M = sm[0], S = ss[0];
-        for (int w = 1; w < CE_THREADS / 32; w++) lse_combine(M, S, sm[w], ss[w]);
-        float lse = M + logf(S);
-        int t = tgt[row];
-        bool ok = t >= 0 && t < V;
-        if (!ok) set_status(status, GPT2_STATUS_BAD_TARGET);
-        s_lse = ok ? lse : INFINITY;   // INFINITY: gradient row becomes 0 below
-        s_zt = ok ? zr[t] : 0.f;
-        losses[row] = ok ? lse - s_zt : 0.f;
-    }
-    __syncthreads();
-    if (dscale == 0.f) return;
-    const float lse = s_lse;
+    for (int v = nfull * 4 + tid; v < V; v += CE_THREADS) sum += exp2f(fmaf(zr[v], CE_LOG2E, -Ml));
+    const float S = block_reduce(sum, sh, false);
+    const float lse = M + logf(S);
     const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    if (tid == 0) {
+        if (!ok) set_status(status, GPT2_STATUS_BAD_TARGET);
+        losses[row] = ok ? lse - zr[t] : 0.f;
+    }
+    if (dscale == 0.f) return;
+    __syncthreads();                               // zr[t] is read before the row is overwritten
+    const float lsel = lse * CE_LOG2E;
     for (int c = tid; c < n4; c += CE_THREADS) {
-        float4 v = z4[c];
+        const float4 v = z4[c];
         float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            int idx = c * 4 + k;
-            float p = idx < V ? expf(e[k] - lse) : 0.f;
-            e[k] = (p - (idx == t ? 1.f : 0.f)) * dscale;
-            if (idx >= V || lse == INFINITY) e[k] = 0.f;
+            const int idx = c * 4 + k;
+            const float p = exp2f(fmaf(e[k], CE_LOG2E, -lsel));
+            e[k] = (idx < V && ok) ? (p - (idx == t ? 1.f : 0.f)) * dscale : 0.f;
         }
         if (dz16) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(e[0], e[1]), hi = __floats2bfloat162_rn(e[2], e[3]);

@@ -6,8 +6,12 @@
 // Backward: dwte[v,:] += sum_{pos: tok[pos]=v} dx[pos,:] and dwpe[t,:] =
 // sum_b dx[b,t,:].  The token-side scatter-add is made deterministic without
 // float atomics: positions are bucketed by token id with an integer counting
-// sort, each bucket is put in ascending position order, and one thread block
-// per distinct token sums its bucket's rows in that order.
+// sort and each bucket is put in ascending position order.  The sorted list is
+// then cut into fixed segments of 64 entries, one thread block each: a bucket
+// that lies inside one segment is summed and added to dwte there; a bucket
+// that crosses segment boundaries leaves one partial sum per segment, and a
+// fix-up pass adds those in segment order.  A frequent token (a Zipf stream
+// gives the top id ~14% of positions) is thus spread over many blocks.
 #include "common.cuh"
 
 namespace gpt2k {
@@ -96,24 +100,70 @@ __global__ void enc_rank_kernel(int* __restrict__ sorted, const int* __restrict_
     sorted[lo + r] = i;
 }
 
-// One block per distinct token; threads stride over the C/4 float4 columns.
-__global__ void enc_accumulate_kernel(float4* __restrict__ dwte, const float4* __restrict__ dx,
-                                      const int* __restrict__ sorted,
-                                      const int* __restrict__ offset, const int* __restrict__ uniq,
-                                      const int* __restrict__ n_uniq, int C4) {
-    int u = blockIdx.x;
-    if (u >= *n_uniq) return;
-    int id = uniq[u];
-    int lo = offset[id], hi = offset[id + 1];
+constexpr int ENC_SEG = 64;
+
+// One block per segment of the sorted list.  All threads walk the segment's
+// entries in order (same token sequence from shared memory), each thread for
+// its own float4 columns, and flush the running sum at every token change.
+__global__ void enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict__ part,
+                                   const float4* __restrict__ dx, const int* __restrict__ sorted,
+                                   const int* __restrict__ offset, const int* __restrict__ tok, int V,
+                                   int C4) {
+    __shared__ int s_pos[ENC_SEG], s_tok[ENC_SEG];
+    const int seg = blockIdx.x, seg_lo = seg * ENC_SEG;
+    const int total = offset[V];                   // sorted entries (positions with valid ids)
+    const int cnt = min(ENC_SEG, total - seg_lo);
+    if (cnt <= 0) return;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const int pos = sorted[seg_lo + i];
+        s_pos[i] = pos;
+        s_tok[i] = tok[pos];
+    }
+    __syncthreads();
     for (int c = threadIdx.x; c < C4; c += blockDim.x) {
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int e = lo; e < hi; e++) {
-            float4 g = dx[(size_t)sorted[e] * C4 + c];
-            s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int run_start = 0;
+        for (int e = 0; e <= cnt; e++) {
+            if (e == cnt || (e > 0 && s_tok[e] != s_tok[e - 1])) {
+                const int v = s_tok[e - 1];
+                const int lo = offset[v], hi = offset[v + 1];
+                if (lo >= seg_lo && hi <= seg_lo + cnt) {        // whole bucket in this segment
+                    float4 d = dwte[(size_t)v * C4 + c];
+                    d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
+                    dwte[(size_t)v * C4 + c] = d;
+                } else {                                       // slot 0: first run, 1: last run
+                    part[((size_t)seg * 2 + (run_start == 0 ? 0 : 1)) * C4 + c] = acc;
+                }
+                if (e == cnt) break;
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                run_start = e;
+            }
+            const float4 g = dx[(size_t)s_pos[e] * C4 + c];
+            acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
         }
-        float4 d = dwte[(size_t)id * C4 + c];
-        d.x += s.x; d.y += s.y; d.z += s.z; d.w += s.w;
-        dwte[(size_t)id * C4 + c] = d;
+    }
+}
+
+// Buckets that cross segments: add their per-segment partials in segment order.
+__global__ void enc_fixup_kernel(float4* __restrict__ dwte, const float4* __restrict__ part,
+                                 const int* __restrict__ offset, const int* __restrict__ uniq,
+                                 const int* __restrict__ n_uniq, int C4) {
+    const int u = blockIdx.x;
+    if (u >= *n_uniq) return;
+    const int v = uniq[u];
+    const int lo = offset[v], hi = offset[v + 1];
+    const int s0 = lo / ENC_SEG, s1 = (hi - 1) / ENC_SEG;
+    if (s0 == s1) return;
+    for (int c = threadIdx.x; c < C4; c += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sg = s0; sg <= s1; sg++) {
+            const int slot = (sg == s0 && lo != sg * ENC_SEG) ? 1 : 0;
+            const float4 p = part[((size_t)sg * 2 + slot) * C4 + c];
+            acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+        }
+        float4 d = dwte[(size_t)v * C4 + c];
+        d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
+        dwte[(size_t)v * C4 + c] = d;
     }
 }
 
@@ -134,9 +184,10 @@ __global__ void enc_dwpe_kernel(float4* __restrict__ dwpe, const float4* __restr
 
 struct EncScratch {
     int *count, *cursor, *offset, *uniq, *n_uniq, *list, *sorted;
+    float* part;
 };
 
-static size_t enc_layout(int BT, int V, char* base, EncScratch* s) {
+static size_t enc_layout(int BT, int V, int C, char* base, EncScratch* s) {
     size_t off = 0;
     auto take = [&](size_t n) {
         char* p = base ? base + off : nullptr;
@@ -151,6 +202,8 @@ static size_t enc_layout(int BT, int V, char* base, EncScratch* s) {
     t.n_uniq = take(1);
     t.list = take(BT);
     t.sorted = take(BT);
+    const size_t nseg = (size_t)ceil_div(BT, ENC_SEG);
+    t.part = reinterpret_cast<float*>(take(nseg * 2 * (size_t)C));
     if (s) *s = t;
     return off;
 }
@@ -172,9 +225,9 @@ GPT2_API int gpt2_op_encoder_forward(float* x, const int* tok, const float* wte,
     return GPT2_OK;
 }
 
-GPT2_API size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V) {
-    if (BT < 1 || V < 1) return 0;
-    return enc_layout(BT, V, nullptr, nullptr);
+GPT2_API size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V, int C) {
+    if (BT < 1 || V < 1 || C < 1) return 0;
+    return enc_layout(BT, V, C, nullptr, nullptr);
 }
 
 GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx, const int* tok,
@@ -184,10 +237,10 @@ GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx,
         return GPT2_EINVAL;
     if (!aligned16(dwte) || !aligned16(dwpe) || !aligned16(dx)) return GPT2_EINVAL;
     int BT = B * T, C4 = C / 4;
-    if (!scratch || scratch_bytes < gpt2_op_encoder_backward_scratch_bytes(BT, V)) return GPT2_ENOMEM;
+    if (!scratch || scratch_bytes < gpt2_op_encoder_backward_scratch_bytes(BT, V, C)) return GPT2_ENOMEM;
     cudaStream_t st = as_stream(stream);
     EncScratch s;
-    enc_layout(BT, V, reinterpret_cast<char*>(scratch), &s);
+    enc_layout(BT, V, C, reinterpret_cast<char*>(scratch), &s);
     GPT2_CUDA_TRY(cudaMemsetAsync(s.count, 0, sizeof(int) * V, st));
     GPT2_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * V, st));
     int nb = ceil_div(BT, 256);
@@ -195,10 +248,13 @@ GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx,
     count_launch(), enc_scan_kernel<<<1, 1024, 0, st>>>(s.offset, s.uniq, s.n_uniq, s.count, V);
     count_launch(), enc_fill_kernel<<<nb, 256, 0, st>>>(s.list, s.cursor, s.offset, tok, BT, V);
     count_launch(), enc_rank_kernel<<<nb, 256, 0, st>>>(s.sorted, s.list, s.offset, tok, BT, V);
-    int threads = C4 < 256 ? ((C4 + 31) / 32) * 32 : 256;
-    count_launch(), enc_accumulate_kernel<<<min(BT, V), threads, 0, st>>>(
-        reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(dx), s.sorted, s.offset,
-        s.uniq, s.n_uniq, C4);
+    const int threads = C4 < 256 ? ((C4 + 31) / 32) * 32 : 256;
+    count_launch(), enc_segment_kernel<<<ceil_div(BT, ENC_SEG), threads, 0, st>>>(
+        reinterpret_cast<float4*>(dwte), reinterpret_cast<float4*>(s.part),
+        reinterpret_cast<const float4*>(dx), s.sorted, s.offset, tok, V, C4);
+    count_launch(), enc_fixup_kernel<<<min(BT, V), threads, 0, st>>>(
+        reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(s.part), s.offset, s.uniq,
+        s.n_uniq, C4);
     long long n = (long long)maxT * C4;
     count_launch(), enc_dwpe_kernel<<<ceil_div(n, 256), 256, 0, st>>>(reinterpret_cast<float4*>(dwpe),
                                                      reinterpret_cast<const float4*>(dx), B, T,

@@ -170,15 +170,24 @@ ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* _
     for (int c = threadIdx.x; c < 2 * C4; c += blockDim.x) out[c] = sh4[c];
 }
 
-// dw[c] = sum_blk partial[blk][0][c], db[c] = sum_blk partial[blk][1][c], in block order
+// dw[c] = sum_blk partial[blk][0][c], db[c] = sum_blk partial[blk][1][c].
+// Block (32 columns x 16 lanes): lane y sums blocks y, y+16, ... in order, then
+// the 16 lane sums are added in lane order.
 __global__ void ln_bwd_reduce_kernel(float* __restrict__ dw, float* __restrict__ db,
                                      const float* __restrict__ partial, int nblk, int C) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= 2 * C) return;
+    __shared__ float sh[16][33];
+    const int c = blockIdx.x * 32 + threadIdx.x;
     float s = 0.f;
-    for (int k = 0; k < nblk; k++) s += partial[(size_t)k * 2 * C + c];
-    if (c < C) dw[c] = s;
-    else db[c - C] = s;
+    if (c < 2 * C)
+        for (int k = threadIdx.y; k < nblk; k += 16) s += partial[(size_t)k * 2 * C + c];
+    sh[threadIdx.y][threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.y == 0 && c < 2 * C) {
+        float t = sh[0][threadIdx.x];
+        for (int k = 1; k < 16; k++) t += sh[k][threadIdx.x];
+        if (c < C) dw[c] = t;
+        else db[c - C] = t;
+    }
 }
 
 static int ln_bwd_blocks(int N) { return std::min(ceil_div(N, 32), 512); }
@@ -251,7 +260,7 @@ GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, flo
     else if (nv <= 13) LNB(13);
     else LNB(LN_MAXV);
 #undef LNB
-    count_launch(), ln_bwd_reduce_kernel<<<ceil_div(2 * C, 256), 256, 0, st>>>(dw, db, partial, nblk, C);
+    count_launch(), ln_bwd_reduce_kernel<<<ceil_div(2 * C, 32), dim3(32, 16), 0, st>>>(dw, db, partial, nblk, C);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -16,10 +16,24 @@
 namespace gpt2k {
 
 // ---- bias gradient: db[o] = sum_n dout[n*ld + o], fixed order -------------
-// Stage 1: block (32 columns x 8 row-lanes) over one chunk of rows; lane y sums
-// rows y, y+8, ... of the chunk in order; the 8 lanes are combined in order.
+// Stage 1: block (32 x 8) covers 128 columns (4 per thread, one vector load per
+// row) of one chunk of rows; lane y sums rows y, y+8, ... of the chunk in order;
+// the 8 lanes are combined in order.  Stage 2 sums the chunks in order.
 constexpr int BG_ROWS = 256;
 
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
 template <typename T>
 __device__ __forceinline__ float to_f(T v) { return (float)v; }
 template <>
@@ -28,18 +42,42 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 template <typename T>
 __global__ void bias_grad_partial_kernel(float* __restrict__ partial, const T* __restrict__ dout,
                                          int N, int OC, int ld) {
-    __shared__ float sh[8][33];
-    int col = blockIdx.x * 32 + threadIdx.x;
-    int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
-    float s = 0.f;
-    if (col < OC)
-        for (int r = r0 + threadIdx.y; r < r1; r += 8) s += to_f(dout[(size_t)r * ld + col]);
+    __shared__ float4 sh[8][33];
+    const int col = (blockIdx.x * 32 + threadIdx.x) * 4;
+    const int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
+    // vector loads need the 4 columns inside the row and an aligned row stride
+    const bool vec = col + 4 <= OC && (ld & 3) == 0;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col < OC) {
+        if (vec) {
+#pragma unroll 4
+            for (int r = r0 + threadIdx.y; r < r1; r += 8) {
+                const float4 v = load4(dout + (size_t)r * ld + col);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
+        } else {
+            for (int r = r0 + threadIdx.y; r < r1; r += 8) {
+                const T* row = dout + (size_t)r * ld + col;
+                s.x += to_f(row[0]);
+                if (col + 1 < OC) s.y += to_f(row[1]);
+                if (col + 2 < OC) s.z += to_f(row[2]);
+                if (col + 3 < OC) s.w += to_f(row[3]);
+            }
+        }
+    }
     sh[threadIdx.y][threadIdx.x] = s;
     __syncthreads();
     if (threadIdx.y == 0 && col < OC) {
-        float t = sh[0][threadIdx.x];
-        for (int k = 1; k < 8; k++) t += sh[k][threadIdx.x];
-        partial[(size_t)blockIdx.y * OC + col] = t;
+        float4 t = sh[0][threadIdx.x];
+        for (int k = 1; k < 8; k++) {
+            const float4 u = sh[k][threadIdx.x];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        float* out = partial + (size_t)blockIdx.y * OC + col;
+        out[0] = t.x;
+        if (col + 1 < OC) out[1] = t.y;
+        if (col + 2 < OC) out[2] = t.z;
+        if (col + 3 < OC) out[3] = t.w;
     }
 }
 
@@ -60,8 +98,8 @@ template <typename T>
 static int bias_grad(float* db, const T* dout, int N, int OC, int ld, float* scratch,
                      cudaStream_t st) {
     int nchunk = ceil_div(N, BG_ROWS);
-    count_launch(), bias_grad_partial_kernel<T><<<dim3(ceil_div(OC, 32), nchunk), dim3(32, 8), 0, st>>>(scratch, dout,
-                                                                                   N, OC, ld);
+    count_launch(), bias_grad_partial_kernel<T><<<dim3(ceil_div(OC, 128), nchunk), dim3(32, 8), 0, st>>>(
+        scratch, dout, N, OC, ld);
     count_launch(), bias_grad_reduce_kernel<<<ceil_div(OC, 256), 256, 0, st>>>(db, scratch, nchunk, OC);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;

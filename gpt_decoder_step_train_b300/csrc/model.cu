@@ -172,7 +172,7 @@ static size_t plan(gpt2* m, char* base) {
     s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, 4 * Ci, Ci, mode));
     s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, c.V, mode));
     s = std::max(s, gpt2_op_attention_backward_scratch_bytes(c.maxB, c.maxT, c.H));
-    s = std::max(s, gpt2_op_encoder_backward_scratch_bytes(Ri, c.V));
+    s = std::max(s, gpt2_op_encoder_backward_scratch_bytes(Ri, c.V, Ci));
     s = std::max(s, gpt2_op_bias_grad_scratch_bytes(Ri, 4 * Ci));
     m->scratch_bytes = s;
     m->scratch = take(s);

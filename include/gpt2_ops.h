@@ -43,10 +43,11 @@ int gpt2_op_encoder_forward(float* x, const int* tok, const float* wte, const fl
                             int B, int T, int C, int V, int* status, void* stream);
 
 /* Encoder backward, deterministic.  dwte[v,:] += sum over positions with
- * tok == v of dx[pos,:], summed in ascending position order; dwpe[t,:] =
+ * tok == v of dx[pos,:], summed in a fixed order (ascending positions within
+ * segments of 64 sorted entries, then segment order); dwpe[t,:] =
  * sum_b dx[b,t,:] for t < T (rows t >= T of dwpe are set to 0; dwpe has maxT
- * rows).  scratch: gpt2_op_encoder_backward_scratch_bytes(B*T, V) bytes. */
-size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V);
+ * rows).  scratch: gpt2_op_encoder_backward_scratch_bytes(B*T, V, C) bytes. */
+size_t gpt2_op_encoder_backward_scratch_bytes(int BT, int V, int C);
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx, const int* tok,
                              int B, int T, int maxT, int C, int V, void* scratch,
                              size_t scratch_bytes, void* stream);

@@ -84,6 +84,6 @@ def test_strerror_covers_codes(L):
 
 def test_scratch_queries_are_host_only(L):
     assert L.gpt2_op_layernorm_backward_scratch_bytes(16384, 768) > 0
-    assert L.gpt2_op_encoder_backward_scratch_bytes(16384, 50257) > 0
+    assert L.gpt2_op_encoder_backward_scratch_bytes(16384, 50257, 768) > 0
     assert L.gpt2_op_attention_backward_scratch_bytes(16, 1024, 12) >= 16 * 12 * 1024 * 4
     assert L.gpt2_op_linear_backward_weight_scratch_bytes(16384, 768, 3072, 1) > 0

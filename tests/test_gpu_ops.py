@@ -102,7 +102,7 @@ def test_encoder_backward_matches_and_is_deterministic(L, B_, o64, zipf):
         tok = rng.integers(0, V, (B, T)).astype(np.int32)
     dx = rng.normal(size=(B * T, C)).astype(np.float32)
     base = rng.normal(size=(V, C)).astype(np.float32)   # dwte already holds the lm_head part
-    nbytes = L.gpt2_op_encoder_backward_scratch_bytes(B * T, V)
+    nbytes = L.gpt2_op_encoder_backward_scratch_bytes(B * T, V, C)
     outs = []
     for _ in range(2):
         dwte = dev(base.copy())
