@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-trace", action="store_true")
     ap.add_argument("--cpu-sample-T", type=int, default=256,
                     help="positions of the single sequence the CPU baseline runs")
-    ap.add_argument("--op", default=None, choices=sorted(OPS),
+    ap.add_argument("--op", default=None,
                     help="time one kernel of the workload in isolation (prints its own JSON line)")
     return ap.parse_args()
 
@@ -402,6 +402,145 @@ for _k in ("fwd", "dx", "dw"):
         OPS[f"gemm_{_k}_{_nm}"] = (lambda k, ic, oc: (lambda mode: _gemm_case(k, 16384, ic, oc, mode)))(_k, _ic, _oc)
 
 
+def _bgemm_case(name, M=16384, C=768, V=50257, Vp=50304):
+    """One bf16 product of the step, with the epilogue the step gives it."""
+    import ctypes as C_
+    import torch
+    from gpt_decoder_step_train_b300 import binding as B_
+    L = B_.lib()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+
+    def rnd(*shape, dtype=torch.float32, s=1.0):
+        return (torch.randn(*shape, device="cuda", generator=g) * s).to(dtype)
+
+    a = B_.gpt2_gemm_args()
+    keep = []
+
+    def put(field, t):
+        keep.append(t)
+        setattr(a, field, B_.ptr(t))
+    kind, lay = name.split("_", 1)
+    dims = {"qkv": (C, 3 * C), "attproj": (C, C), "fc": (C, 4 * C), "fcproj": (4 * C, C), "lmhead": (C, V)}
+    IC, OC = dims[lay]
+    if kind == "fwd":                                  # out[M, OC] = x[M, IC] W[OC, IC]^T
+        a.M, a.N, a.K = M, OC, IC
+        put("A", rnd(M, IC, dtype=bf)); a.lda = IC; a.a_kmajor = 1
+        put("B", rnd(OC, IC, dtype=bf, s=0.02)); a.ldb = IC; a.b_kmajor = 1
+        ldo = Vp if lay == "lmhead" else OC
+        if lay != "lmhead":
+            put("bias", rnd(OC, s=0.02))
+        if lay in ("attproj", "fcproj"):
+            put("residual", rnd(M, ldo))
+            put("out", rnd(M, ldo)); a.out_bf16 = 0
+        elif lay == "fc":
+            a.gelu = 1
+            put("out_pre", rnd(M, ldo, dtype=bf)); a.pre_bf16 = 1
+            put("out", rnd(M, ldo, dtype=bf)); a.out_bf16 = 1
+        elif lay == "qkv":
+            put("out", rnd(M, ldo, dtype=bf)); a.out_bf16 = 1
+        else:
+            put("out", torch.empty(M, ldo, device="cuda")); a.out_bf16 = 0
+        a.ldo = ldo
+    else:                                              # dx[M, IC] = dy[M, OC] W[OC, IC]
+        a.M, a.N, a.K = M, IC, OC
+        ldy = Vp if lay == "lmhead" else OC
+        put("A", rnd(M, ldy, dtype=bf, s=0.01)); a.lda = ldy; a.a_kmajor = 1
+        put("B", rnd(OC, IC, dtype=bf, s=0.02)); a.ldb = IC; a.b_kmajor = 0
+        if lay == "fcproj":                            # dh = (dy W) * gelu'(h)
+            put("gelu_x", rnd(M, IC, dtype=bf)); a.ldg = IC; a.gelu_x_bf16 = 1
+            put("out", torch.empty(M, IC, device="cuda", dtype=bf)); a.out_bf16 = 1
+        else:
+            put("out", torch.empty(M, IC, device="cuda")); a.out_bf16 = 0
+        a.ldo = IC
+    a.bf16 = 1
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    keep += [st, a]
+    fn = lambda: L.gpt2_op_gemm(C_.byref(a), B_.MODES["bf16"], B_.ptr(st), None)
+    return fn, 2.0 * a.M * a.N * a.K, 0.0, keep
+
+
+for _k in ("fwd", "dx"):
+    for _nm in ("qkv", "attproj", "fc", "fcproj", "lmhead"):
+        OPS[f"bgemm_{_k}_{_nm}"] = (lambda n: (lambda mode: _bgemm_case(n)))(f"{_k}_{_nm}")
+
+
+def _mem_case(name, N=16384, C=768, V=50257, Vp=50304):
+    """One HBM-bound kernel of the step at its GPT-2 124M B16 T1024 size.  Returns
+    the algorithmic bytes of one launch: every input read once, every output
+    written once."""
+    import torch
+    from gpt_decoder_step_train_b300 import binding as B_
+    L = B_.lib()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    dev = "cuda"
+    keep = []
+
+    def k(t):
+        keep.append(t)
+        return B_.ptr(t)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    keep.append(st)
+    if name == "ln_fwd":                               # x fp32 -> y bf16, mean, rstd
+        x = torch.randn(N, C, device=dev, generator=g)
+        w, b = torch.ones(C, device=dev), torch.zeros(C, device=dev)
+        y = torch.empty(N, C, device=dev, dtype=torch.bfloat16)
+        mu, rs = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        fn = lambda: L.gpt2_op_layernorm_forward_bf16(k(y), k(mu), k(rs), k(x), k(w), k(b), N, C, None)
+        nbytes = N * C * (4 + 2) + 8 * N
+    elif name == "ln_bwd":                             # dx += LN'(dy): dx fp32 (read+write) + bf16 copy
+        x = torch.randn(N, C, device=dev, generator=g)
+        dy = torch.randn(N, C, device=dev, generator=g)
+        dx = torch.randn(N, C, device=dev, generator=g)
+        dx16 = torch.empty(N, C, device=dev, dtype=torch.bfloat16)
+        w = torch.ones(C, device=dev)
+        mu, rs = torch.zeros(N, device=dev), torch.ones(N, device=dev)
+        dw, db = torch.empty(C, device=dev), torch.empty(C, device=dev)
+        nsc = L.gpt2_op_layernorm_backward_scratch_bytes(N, C)
+        sc = torch.empty(nsc, dtype=torch.uint8, device=dev)
+        ds = torch.empty(C, device=dev)
+        fn = lambda: L.gpt2_op_layernorm_backward(k(dx), k(dx16), k(dw), k(db), k(ds), k(dy), k(x), k(w), k(mu),
+                                                  k(rs), N, C, 1, k(sc), nsc, k(st), None)
+        nbytes = N * C * (4 + 4 + 4 + 4 + 2) + 8 * N
+    elif name == "crossentropy":                       # logits fp32 read, dlogits bf16 written
+        z = torch.randn(N, Vp, device=dev, generator=g)
+        dz = torch.empty(N, Vp, device=dev, dtype=torch.bfloat16)
+        tgt = torch.randint(0, V, (N,), device=dev, dtype=torch.int32, generator=g)
+        losses = torch.empty(N, device=dev)
+        fn = lambda: L.gpt2_op_crossentropy(k(losses), k(z), k(dz), k(tgt), N, V, Vp, 1.0 / N, k(st), None)
+        nbytes = N * V * (4 + 2) + 8 * N
+    elif name.startswith("bias_grad"):                 # column sums of dY [N, 3C] (bf16) or [N, C] (fp32)
+        bf = name.endswith("bf16")
+        OC = 3 * C if bf else C
+        dout = torch.randn(N, OC, device=dev, generator=g).to(torch.bfloat16 if bf else torch.float32)
+        db = torch.empty(OC, device=dev)
+        nsc = L.gpt2_op_bias_grad_scratch_bytes(N, OC)
+        sc = torch.empty(nsc, dtype=torch.uint8, device=dev)
+        fn = lambda: L.gpt2_op_bias_grad(k(db), k(dout), int(bf), N, OC, OC, k(sc), nsc, None)
+        nbytes = N * OC * (2 if bf else 4)
+    elif name == "adamw":                              # p, g, m, v read; p, m, v written (124M params)
+        n = 124439808
+        p, gr = torch.randn(n, device=dev, generator=g), torch.randn(n, device=dev, generator=g)
+        m_, v_ = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+        fn = lambda: L.gpt2_op_adamw(k(p), k(gr), k(m_), k(v_), n, 1e-4, 0.9, 0.999, 1e-8, 0.0, 0.1, 0.001, None)
+        nbytes = 28 * n
+    elif name == "encoder_fwd":                        # token and position rows gathered, x written
+        B_n, T = 16, 1024
+        wte = torch.randn(V, C, device=dev, generator=g)
+        wpe = torch.randn(1024, C, device=dev, generator=g)
+        tok = torch.randint(0, V, (B_n, T), device=dev, dtype=torch.int32, generator=g)
+        x = torch.empty(B_n * T, C, device=dev)
+        fn = lambda: L.gpt2_op_encoder_forward(k(x), k(tok), k(wte), k(wpe), B_n, T, C, V, k(st), None)
+        nbytes = B_n * T * C * 4 * 3
+    else:
+        raise KeyError(name)
+    return fn, 0.0, float(nbytes), keep
+
+
+for _nm in ("ln_fwd", "ln_bwd", "crossentropy", "bias_grad_bf16", "bias_grad_f32", "adamw", "encoder_fwd"):
+    OPS[f"mem_{_nm}"] = (lambda n: (lambda mode: _mem_case(n)))(_nm)
+
+
 def _attn_case(kind, mode, B=16, T=1024, C=768, H=12):
     import torch
     from gpt_decoder_step_train_b300 import binding as B_
@@ -437,25 +576,37 @@ OPS["attn_bwd"] = lambda mode: _attn_case("bwd", mode)
 
 
 def run_op(args):
+    """Time single operations: --op takes names or prefixes, comma separated."""
     import torch
     torch.cuda.set_device(0)
-    fn, flops, nbytes, keep = OPS[args.op](args.mode)
-    for _ in range(args.warmup):
-        assert fn() == 0
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        assert fn() == 0
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    names = [n for want in args.op.split(",") for n in sorted(OPS) if n == want or n.startswith(want)]
+    if not names:
+        print(f"unknown op {args.op!r}; known: {', '.join(sorted(OPS))}", file=sys.stderr)
+        return 2
     peaks, src = load_peaks()
-    peak = peaks["bf16_tflops"] * TF32_OVER_BF16 if args.mode == "tf32" else None
-    tf = flops / (ms / 1e3) / 1e12
-    print(json.dumps({"op": args.op, "mode": args.mode, "ms": round(ms, 4),
-                      "tflops": round(tf, 1), "frac_of_tf32_burst": round(tf / peak, 3) if peak else None,
-                      "gbs_algorithmic": round(nbytes / (ms / 1e3) / 1e9, 1)}), flush=True)
+    for name in names:
+        fn, flops, nbytes, keep = OPS[name](args.mode)
+        for _ in range(args.warmup):
+            assert fn() == 0
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            assert fn() == 0
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        bf16 = args.mode == "bf16" or name.startswith("bgemm")
+        peak = peaks["bf16_tflops"] * (1.0 if bf16 else TF32_OVER_BF16)
+        tf = flops / (ms / 1e3) / 1e12
+        gbs = nbytes / (ms / 1e3) / 1e9 if nbytes else None
+        print(json.dumps({"op": name, "mode": "bf16" if bf16 else args.mode, "ms": round(ms, 4),
+                          "tflops": round(tf, 1) if flops else None,
+                          "frac_of_burst_peak": round(tf / peak, 3) if flops else None,
+                          "gbs_algorithmic": round(gbs, 1) if gbs else None,
+                          "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3) if gbs else None}),
+              flush=True)
+        del keep
     return 0
 
 

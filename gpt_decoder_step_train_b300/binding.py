@@ -32,7 +32,8 @@ class gpt2_gemm_args(C.Structure):
                 ("bf16", C.c_int),
                 ("out", C.c_void_p), ("ldo", C.c_int), ("out_bf16", C.c_int),
                 ("out_pre", C.c_void_p), ("bias", C.c_void_p), ("residual", C.c_void_p),
-                ("gelu_x", C.c_void_p), ("ldg", C.c_int), ("gelu", C.c_int)]
+                ("gelu_x", C.c_void_p), ("ldg", C.c_int), ("gelu", C.c_int),
+                ("pre_bf16", C.c_int), ("gelu_x_bf16", C.c_int)]
 
 
 class gpt2_config(C.Structure):
@@ -68,8 +69,8 @@ SIGNATURES = {
     "gpt2_op_layernorm_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_op_layernorm_forward_bf16": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
-    "gpt2_op_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp,
-                                        _sz, _vp]),
+    "gpt2_op_layernorm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                        _vp, _sz, _vp, _vp]),
     "gpt2_op_linear_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                     _vp]),
     "gpt2_op_linear_backward_input": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -206,11 +207,12 @@ class GPT2:
         return {name: (ms[i], nl[i]) for i, name in enumerate(TRACE_CLASSES)}
 
     # -- views into the workspace ----------------------------------------
-    def _view(self, addr, n, shape=None):
+    def _view(self, addr, n, shape=None, bf16=False):
         import torch
+        es = 2 if bf16 else 4
         off = addr - self.workspace.data_ptr()
-        assert 0 <= off and off + 4 * n <= self.workspace.numel()
-        t = self.workspace[off:off + 4 * n].view(torch.float32)
+        assert 0 <= off and off + es * n <= self.workspace.numel()
+        t = self.workspace[off:off + es * n].view(torch.bfloat16 if bf16 else torch.float32)
         return t.view(*shape) if shape else t
 
     def grads(self):
@@ -230,8 +232,12 @@ class GPT2:
     def losses(self, rows):
         return self._view(lib().gpt2_losses(self.h), rows)
 
+    # activations held as bf16 in bf16 mode (the tensor-core operands)
+    BF16_ACTIVATIONS = (1, 2, 3, 5, 6, 7, 9)
+
     def activation(self, which, layer, rows):
+        """Activation `which` of block `layer` as a [rows, width] view (bf16 or fp32)."""
         widths = {0: 1, 1: 1, 2: 3, 3: 1, 4: 1, 5: 1, 6: 4, 7: 4, 8: 1, 9: 1}
         w = widths[which] * self.cfg.C
         a = lib().gpt2_activation(self.h, which, layer)
-        return self._view(a, rows * w, (rows, w))
+        return self._view(a, rows * w, (rows, w), bf16=self.mode == "bf16" and which in self.BF16_ACTIVATIONS)

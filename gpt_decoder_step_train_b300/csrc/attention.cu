@@ -118,40 +118,71 @@ attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __res
 }
 
 // D[b,h,i] = dO_i . O_i (bf16 inputs)
-__global__ void attn_bwd_dot_bf16_kernel(float* __restrict__ D, const __nv_bfloat16* __restrict__ dy,
-                                         const __nv_bfloat16* __restrict__ y, int B, int T, int C, int H,
-                                         int hs) {
-    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)B * H * T) return;
-    int i = (int)(idx % T);
-    int h = (int)((idx / T) % H);
-    int b = (int)(idx / ((long long)T * H));
-    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(dy + ((size_t)b * T + i) * C + h * hs);
-    const __nv_bfloat162* o = reinterpret_cast<const __nv_bfloat162*>(y + ((size_t)b * T + i) * C + h * hs);
+// D[b,h,i] = dO_i . O_i over one head's hs elements.  LPR lanes share a
+// (position, head) pair and read 16 bytes at a time; pairs are ordered head
+// fastest, so a warp reads contiguous rows of dO and O.  Each lane sums its
+// chunks in order, then the LPR partial sums meet in a fixed xor tree.
+__device__ __forceinline__ float dot16(uint4 a, uint4 b, __nv_bfloat16) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
     float s = 0.f;
-    for (int d = 0; d < hs / 2; d++) {
-        float2 u = __bfloat1622float2(a[d]), v = __bfloat1622float2(o[d]);
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const float2 u = __bfloat1622float2(x[k]), v = __bfloat1622float2(y[k]);
         s += u.x * v.x + u.y * v.y;
     }
-    D[idx] = s;
+    return s;
+}
+__device__ __forceinline__ float dot16(uint4 a, uint4 b, float) {
+    const float4 u = *reinterpret_cast<const float4*>(&a), v = *reinterpret_cast<const float4*>(&b);
+    return (u.x * v.x + u.y * v.y) + (u.z * v.z + u.w * v.w);
 }
 
-// D[b,h,i] = dO_i . O_i
-__global__ void attn_bwd_dot_kernel(float* __restrict__ D, const float* __restrict__ dy,
-                                    const float* __restrict__ y, int B, int T, int C, int H, int hs) {
-    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)B * H * T) return;
-    int i = (int)(idx % T);
-    int h = (int)((idx / T) % H);
-    int b = (int)(idx / ((long long)T * H));
-    const float* a = dy + ((size_t)b * T + i) * C + h * hs;
-    const float* o = y + ((size_t)b * T + i) * C + h * hs;
+template <typename Tv, int LPR>
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(float* __restrict__ D, const Tv* __restrict__ dy,
+                                                           const Tv* __restrict__ y, int B, int T, int C,
+                                                           int H, int hs) {
+    constexpr int PER = 16 / sizeof(Tv);          // elements per 16-byte chunk
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long pair = gid / LPR;             // ((b * T) + t) * H + h
+    const int sub = (int)(gid % LPR);
+    const bool valid = pair < (long long)B * T * H;
     float s = 0.f;
-    for (int d = 0; d < hs; d += 4) {
-        float4 u = *reinterpret_cast<const float4*>(a + d), v = *reinterpret_cast<const float4*>(o + d);
-        s += (u.x * v.x + u.y * v.y) + (u.z * v.z + u.w * v.w);
+    long long bt = 0;
+    int h = 0;
+    if (valid) {
+        h = (int)(pair % H);
+        bt = pair / H;
+        const Tv* a = dy + bt * C + (size_t)h * hs;
+        const Tv* o = y + bt * C + (size_t)h * hs;
+        for (int d = sub * PER; d < hs; d += LPR * PER)
+            s += dot16(__ldg(reinterpret_cast<const uint4*>(a + d)), __ldg(reinterpret_cast<const uint4*>(o + d)),
+                       Tv{});
     }
-    D[idx] = s;
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (valid && sub == 0) {
+        const int t = (int)(bt % T), b = (int)(bt / T);
+        D[((size_t)b * H + h) * T + t] = s;
+    }
+}
+
+template <typename Tv>
+static void launch_dot(float* D, const void* dy, const void* y, int B, int T, int C, int H, int hs,
+                       cudaStream_t st) {
+    constexpr int PER = 16 / sizeof(Tv);
+    const int chunks = hs / PER;
+    const long long pairs = (long long)B * T * H;
+    const Tv* g = static_cast<const Tv*>(dy);
+    const Tv* o = static_cast<const Tv*>(y);
+#define GPT2_DOT(L)                                                                                        \
+    count_launch(), attn_bwd_dot_kernel<Tv, L><<<(unsigned)ceil_div(pairs * L, 256), 256, 0, st>>>(       \
+        D, g, o, B, T, C, H, hs)
+    if (chunks >= 8) GPT2_DOT(8);
+    else if (chunks >= 4) GPT2_DOT(4);
+    else if (chunks >= 2) GPT2_DOT(2);
+    else GPT2_DOT(1);
+#undef GPT2_DOT
 }
 
 // dQ: one thread per query row i; key/value tiles j <= i in shared memory.
@@ -332,18 +363,16 @@ GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* 
     int hs = C / H;
     cudaStream_t st = as_stream(stream);
     float* D = reinterpret_cast<float*>(scratch);
-    long long n = (long long)B * H * T;
     if (mode == GPT2_MODE_BF16) {
         if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
-        count_launch(), attn_bwd_dot_bf16_kernel<<<ceil_div(n, 256), 256, 0, st>>>(
-            D, static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(y), B, T, C, H, hs);
+        launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
         GPT2_LAUNCH_CHECK();
         return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
     }
     float* dq = static_cast<float*>(dqkv);
     const float* g = static_cast<const float*>(dy);
     const float* x = static_cast<const float*>(qkv);
-    count_launch(), attn_bwd_dot_kernel<<<ceil_div(n, 256), 256, 0, st>>>(D, g, static_cast<const float*>(y), B, T, C, H, hs);
+    launch_dot<float>(D, dy, y, B, T, C, H, hs, st);
     GPT2_LAUNCH_CHECK();
     if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
         return attention_tc_backward(dq, g, x, lse, D, B, T, C, H, status, st);

@@ -6,16 +6,25 @@
 // d(mean loss)/dz_n = (softmax(z_n) - onehot(target_n)) / (number of positions).
 //
 // One block per row.  Pass 1 streams the row once (128-bit loads) keeping a
-// per-thread running maximum and rescaled sum, combined across the block; pass
-// 2 re-reads the row (it is still in L2) and overwrites it with the gradient.
-// DRAM traffic is one read and one write of the logits.
+// per-thread running maximum and rescaled sum, combined across the block, and
+// keeps the row's first 100 KB in shared memory; pass 2 re-reads the row (that
+// part from shared memory, the rest from L2) and overwrites it with the
+// gradient, or writes the gradient in bf16 to a separate buffer for the bf16
+// products.
+// DRAM traffic is one read of the logits and one write of the gradient.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 
 namespace gpt2k {
 
 constexpr int CE_THREADS = 512;
+// Shared-memory cache of a row's first float4s: pass 2 reads that part from
+// here and the rest from L2.  Its size also holds residency to two rows per SM,
+// so the rows in flight (2 x 148 x 200 KB for GPT-2's vocabulary) fit in L2.
+constexpr int CE_CACHE_BYTES = 100 * 1024;
 
 constexpr float CE_LOG2E = 1.4426950408889634f;
 constexpr float CE_LN2 = 0.6931471805599453f;
@@ -35,34 +44,59 @@ __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
     return r;
 }
 
-// Pass 1 reads the row from DRAM (128-bit loads) for its maximum; passes 2
-// (sum of exp) and 3 (gradient) re-read it from L2.  Exponentials are exp2 of
-// log2(e)-scaled differences.
-__global__ void __launch_bounds__(CE_THREADS)
+// Pass 1 reads the row from DRAM (128-bit loads) keeping a per-thread running
+// maximum and a sum of exponentials rescaled whenever the maximum grows; the
+// block combines them into the log-sum-exp.  Pass 2 re-reads the row from L2
+// and writes the gradient.  Exponentials are exp2 of log2(e)-scaled differences.
+__global__ void __launch_bounds__(CE_THREADS, 2)
 crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bfloat16* __restrict__ dz16,
-                    const int* __restrict__ tgt, int V, int ld, float dscale, int* status) {
+                    const int* __restrict__ tgt, int V, int ld, float dscale, int ncache, int* status) {
     __shared__ float sh[CE_THREADS / 32];
+    extern __shared__ float4 zc[];                 // the row's float4s [0, ncache)
     const int row = blockIdx.x, tid = threadIdx.x;
     float* zr = z + (size_t)row * ld;
     float4* z4 = reinterpret_cast<float4*>(zr);
     const int nfull = V >> 2;                      // float4s entirely inside [0, V)
     const int n4 = ld >> 2;
-    float mx = -INFINITY;
-    for (int c = tid; c < nfull; c += CE_THREADS) {
-        const float4 v = z4[c];
-        mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    float mx = -INFINITY, sum = 0.f;               // sum of exp(z - mx) over this thread's elements
+    auto add4 = [&](const float4* v, int n) {      // n float4s: one rescale, then 4n exponentials
+        float m = mx;
+        for (int k = 0; k < n; k++) m = fmaxf(m, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
+        if (m > mx) {
+            sum *= exp2f((mx - m) * CE_LOG2E);
+            mx = m;
+        }
+        const float ml = mx * CE_LOG2E;
+        for (int k = 0; k < n; k++)
+            sum += (exp2f(fmaf(v[k].x, CE_LOG2E, -ml)) + exp2f(fmaf(v[k].y, CE_LOG2E, -ml))) +
+                   (exp2f(fmaf(v[k].z, CE_LOG2E, -ml)) + exp2f(fmaf(v[k].w, CE_LOG2E, -ml)));
+    };
+    int c = tid;
+    for (; c + 3 * CE_THREADS < nfull; c += 4 * CE_THREADS) {
+        // four independent loads in flight before any arithmetic
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) v[k] = z4[c + k * CE_THREADS];
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (c + k * CE_THREADS < ncache) zc[c + k * CE_THREADS] = v[k];
+        add4(v, 4);
     }
-    for (int v = nfull * 4 + tid; v < V; v += CE_THREADS) mx = fmaxf(mx, zr[v]);
+    for (; c < nfull; c += CE_THREADS) {
+        float4 v[1] = {z4[c]};
+        if (c < ncache) zc[c] = v[0];
+        add4(v, 1);
+    }
+    for (int v = nfull * 4 + tid; v < V; v += CE_THREADS) {
+        const float x = zr[v];
+        if (x > mx) {
+            sum *= exp2f((mx - x) * CE_LOG2E);
+            mx = x;
+        }
+        sum += exp2f((x - mx) * CE_LOG2E);
+    }
     const float M = block_reduce(mx, sh, true);
-    const float Ml = M * CE_LOG2E;
-    float sum = 0.f;
-    for (int c = tid; c < nfull; c += CE_THREADS) {
-        const float4 v = z4[c];
-        sum += (exp2f(fmaf(v.x, CE_LOG2E, -Ml)) + exp2f(fmaf(v.y, CE_LOG2E, -Ml))) +
-               (exp2f(fmaf(v.z, CE_LOG2E, -Ml)) + exp2f(fmaf(v.w, CE_LOG2E, -Ml)));
-    }
-    for (int v = nfull * 4 + tid; v < V; v += CE_THREADS) sum += exp2f(fmaf(zr[v], CE_LOG2E, -Ml));
-    const float S = block_reduce(sum, sh, false);
+    const float S = block_reduce(mx == -INFINITY ? 0.f : sum * exp2f((mx - M) * CE_LOG2E), sh, false);
     const float lse = M + logf(S);
     const int t = tgt[row];
     const bool ok = t >= 0 && t < V;
@@ -74,7 +108,7 @@ crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bflo
     __syncthreads();                               // zr[t] is read before the row is overwritten
     const float lsel = lse * CE_LOG2E;
     for (int c = tid; c < n4; c += CE_THREADS) {
-        const float4 v = z4[c];
+        const float4 v = c < ncache ? zc[c] : z4[c];
         float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
@@ -116,8 +150,15 @@ GPT2_API int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const 
     if (!losses || !z || !tgt || N < 1 || V < 1 || ld < V || ld % 4 || !aligned16(z))
         return GPT2_EINVAL;
     if (dz_bf16 && (reinterpret_cast<uintptr_t>(dz_bf16) & 7)) return GPT2_EINVAL;
-    count_launch(), crossentropy_kernel<<<N, CE_THREADS, 0, as_stream(stream)>>>(
-        losses, z, static_cast<__nv_bfloat16*>(dz_bf16), tgt, V, ld, dscale, status);
+    static bool attr = false;
+    if (!attr) {
+        GPT2_CUDA_TRY(cudaFuncSetAttribute(crossentropy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           CE_CACHE_BYTES));
+        attr = true;
+    }
+    const int ncache = std::min(V >> 2, CE_CACHE_BYTES / 16);
+    count_launch(), crossentropy_kernel<<<N, CE_THREADS, (size_t)ncache * 16, as_stream(stream)>>>(
+        losses, z, static_cast<__nv_bfloat16*>(dz_bf16), tgt, V, ld, dscale, ncache, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -19,10 +19,12 @@ struct GemmEpilogue {
     void* out;               // [M, ldo], fp32, or bf16 when out_bf16
     int ldo;
     int out_bf16;
-    float* out_pre;          // GELU: pre-activation written here (same ldo)
+    void* out_pre;           // GELU: pre-activation written here (same ldo), fp32 or bf16
+    int pre_bf16;
     const float* bias;       // [N] or null
     const float* residual;   // [M, ldo] or null: out = residual + (acc + bias)
-    const float* gelu_x;     // [M, ldg] or null: out = acc * gelu'(gelu_x)
+    const void* gelu_x;      // [M, ldg] or null: out = acc * gelu'(gelu_x), fp32 or bf16
+    int gelu_x_bf16;
     int ldg;
     int gelu;                // 1: out_pre = acc + bias, out = gelu(out_pre)
 };
@@ -41,11 +43,16 @@ __device__ __forceinline__ void epilogue_store(const GemmEpilogue& e, int m, int
     float v = acc;
     if (e.bias) v += e.bias[n];
     if (e.gelu) {
-        e.out_pre[o] = v;
+        if (e.pre_bf16) reinterpret_cast<__nv_bfloat16*>(e.out_pre)[o] = __float2bfloat16_rn(v);
+        else reinterpret_cast<float*>(e.out_pre)[o] = v;
         v = gelu_fwd(v);
     }
     if (e.residual) v += e.residual[o];
-    if (e.gelu_x) v *= gelu_grad(e.gelu_x[(size_t)m * e.ldg + n]);
+    if (e.gelu_x) {
+        const size_t g = (size_t)m * e.ldg + n;
+        v *= gelu_grad(e.gelu_x_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(e.gelu_x)[g])
+                                     : reinterpret_cast<const float*>(e.gelu_x)[g]);
+    }
     if (e.out_bf16) reinterpret_cast<__nv_bfloat16*>(e.out)[o] = __float2bfloat16_rn(v);
     else reinterpret_cast<float*>(e.out)[o] = v;
 }
@@ -63,11 +70,12 @@ bool gemm_tc_epilogue_supported(const GemmEpilogue& e);
 
 // Linear-layer products for any operand type (linear.cu); bf16 requires
 // mode GPT2_MODE_BF16.
-int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, const void* w,
+// A bf16 GELU pre-activation (out_pre, gelu_x) goes with bf16 operands (`bf16`).
+int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, const void* w,
                    bool bf16, const float* bias, const float* residual, int N, int IC, int OC,
                    int ld_out, int flags, int mode, int* status, cudaStream_t st);
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
-                          const float* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
+                          const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
                           int* status, cudaStream_t st);
 int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
                            int OC, int ld_dout, void* scratch, size_t scratch_bytes, int mode,

@@ -34,7 +34,8 @@ namespace gpt2k {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                              // two per TMEM lane quarter
+constexpr int THREADS = 64 + 32 * EPI_WARPS;              // producer, MMA issuer, epilogue
 constexpr unsigned long long WAIT_NS = 1000000000ull;   // 1 s
 
 // Per operand type: element bytes, k-block (one 128-byte row), MMA K, and the
@@ -48,6 +49,12 @@ struct Elem {
     static constexpr int BOX_BYTES = 128 * BK;        // 4 KB or 8 KB
 };
 
+// Epilogue staging: each epilogue warp owns EPI_WARP_BYTES of shared memory,
+// cut into boxes of 32 rows x EC columns (1 KB bf16, 2 KB fp32).
+constexpr int EC = 16;
+constexpr int EPI_WARP_BYTES = 4096;
+constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+
 template <int BN, bool BF16>
 struct Shape {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
@@ -55,7 +62,7 @@ struct Shape {
     static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + EPI_BYTES;
 };
 
 struct Params {
@@ -72,8 +79,10 @@ struct Params {
     // epilogue: which tensor maps are live
     int has_aux;            // residual (aux_residual) or GELU-input tile loaded by TMA
     int aux_residual;
+    int aux_bf16;           // the GELU input is bf16
     int gelu;
     int out_bf16;
+    int pre_bf16;           // the GELU pre-activation is stored as bf16
     const float* bias;
 };
 
@@ -162,7 +171,21 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int 
                  : "memory");
 }
 
+// pull a box of a tensor into L2 ahead of its TMA load
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most n (0, 1 or 3) committed store groups may still be reading shared memory
+__device__ __forceinline__ void bulk_wait_read(int n) {
+    if (n >= 3) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+    else if (n == 1) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    else asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -246,18 +269,23 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 16 accumulator columns of this warp's 32 TMEM lanes (thread = lane = row).
+// The wait names the destination registers so nothing reads them before the
+// load has landed.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- scheduling
@@ -281,22 +309,67 @@ __device__ __forceinline__ Unit unit_coords(const Params& p, long long u) {
 }
 
 // ---------------------------------------------------------------- epilogue
-// Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and walks
-// them 32 columns at a time: thread = row.  Per chunk it loads the accumulator
-// from tensor memory, applies the epilogue in registers and writes the chunk
-// into a swizzled shared-memory box that one lane stores with a TMA bulk copy
-// (clipped at the matrix edges).  A residual or GELU-input tile arrives by a
-// TMA load into a second box; for GELU that box holds the pre-activation
-// output instead.  Boxes: fp32 rows of 128 bytes (128-byte swizzle), bf16 rows
-// of 64 bytes (64-byte swizzle).
-constexpr int EPI_WARP_BYTES = 8192;              // 4 KB output box + 4 KB aux box
-constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
-
-__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
+// Eight epilogue warps: warp w reads TMEM lane quarter w % 4 (32 accumulator
+// rows, thread = row) and one half of the tile's columns, EC columns at a time.
+// Per chunk it loads the accumulator from tensor memory, applies the epilogue
+// in registers and writes the chunk into a swizzled shared-memory box that one
+// lane stores with a TMA bulk copy (clipped at the matrix edges).  Two warps
+// per scheduler hide each other's latency; each warp's 4 KB holds as many
+// output boxes as fit, so stores stay in flight while later chunks are
+// written.  An input tile (residual or GELU input) arrives by TMA into a ring
+// of boxes filled ahead of use, and the chunk's output is written back over
+// its own input box and stored from there.  fp32 boxes have 64-byte rows
+// (64-byte swizzle), bf16 boxes 32-byte rows (32-byte swizzle); both keep a
+// warp's 16-byte writes free of bank conflicts.
 __device__ __forceinline__ uint32_t sw64(int row, int chunk) {
     return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ uint32_t sw32(int row, int chunk) {
+    return (uint32_t)(row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4));
+}
+
+// 16 values of one row into a box: fp32 (64-byte rows) or bf16 (32-byte rows)
+__device__ __forceinline__ void put_row16(uint8_t* box, int row, const float (&x)[16], bool bf16) {
+    if (bf16) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(x[8 * h], x[8 * h + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(x[8 * h + 2], x[8 * h + 3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(x[8 * h + 4], x[8 * h + 5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(x[8 * h + 6], x[8 * h + 7]);
+            *reinterpret_cast<uint4*>(box + sw32(row, h)) =
+                make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                           *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            *reinterpret_cast<float4*>(box + sw64(row, j)) =
+                make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+}
+
+// 16 values of one row from a box
+__device__ __forceinline__ void get_row16(const uint8_t* box, int row, float (&a)[16], bool bf16) {
+    if (bf16) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const uint4 v = *reinterpret_cast<const uint4*>(box + sw32(row, h));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+                a[8 * h + 2 * k] = f.x;
+                a[8 * h + 2 * k + 1] = f.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float4 v = *reinterpret_cast<const float4*>(box + sw64(row, j));
+            a[4 * j] = v.x; a[4 * j + 1] = v.y; a[4 * j + 2] = v.z; a[4 * j + 3] = v.w;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -307,9 +380,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmPre, const Params p) {
     using S = Shape<BN, BF16>;
     using E = Elem<BF16>;
+    constexpr int RING_MAX = EPI_WARP_BYTES / 1024;   // input boxes per warp (bf16 boxes)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[S::STAGES], empty_bar[S::STAGES];
-    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, aux_bar[4];
+    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, aux_bar[EPI_WARPS][RING_MAX];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
@@ -328,10 +402,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 4);
+            mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);
         }
         mbar_init(smem_u32(&drain_bar), 1);
-        for (int w = 0; w < 4; w++) mbar_init(smem_u32(&aux_bar[w]), 1);
+        for (int w = 0; w < EPI_WARPS; w++)
+            for (int k = 0; k < RING_MAX; k++) mbar_init(smem_u32(&aux_bar[w][k]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
         prefetch_map(&tmB);
@@ -450,108 +525,143 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int ew = warp - 2;
-        uint8_t* const outb = base_ptr + S::STAGES * S::STAGE_BYTES + ew * EPI_WARP_BYTES;
-        uint8_t* const auxb = outb + 4096;
-        const uint32_t outs = smem_u32(outb), auxs = smem_u32(auxb);
-        const uint32_t abar = smem_u32(&aux_bar[ew]);
-        uint32_t aux_phase = 0;
+        const int col_lo = (ew >> 2) * (BN / 2);     // this warp's half of the tile's columns
+        uint8_t* const wbuf = base_ptr + S::STAGES * S::STAGE_BYTES + ew * EPI_WARP_BYTES;
+        const bool has_aux = p.has_aux != 0;
+        const bool pre = p.gelu && !p.partial;
+        const bool out16 = p.out_bf16 != 0, pre16 = p.pre_bf16 != 0, aux16 = p.aux_bf16 != 0;
+        const int out_bytes = out16 ? 1024 : 2048;
+        // output boxes (no input tile): one chunk = output box (+ pre-activation box)
+        const int chunk_bytes = out_bytes + (pre ? (pre16 ? 1024 : 2048) : 0);
+        const int nbuf = chunk_bytes <= 1024 ? 4 : chunk_bytes <= 2048 ? 2 : 1;
+        // input ring: box g of this warp's sequence uses slot g % ring, phase (g / ring) & 1
+        const int aux_bytes = aux16 && !p.aux_residual ? 1024 : 2048;
+        const int ring = EPI_WARP_BYTES / aux_bytes;
+        uint32_t box_seq = 0;                // output chunks stored so far
+        uint32_t aux_issued = 0;             // input boxes requested (lane 0)
+        uint32_t aux_seq = 0;                // input boxes consumed
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (long long u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             Unit c = unit_coords(p, u);
-            const int m0 = c.m_tile * BM, n0 = c.n_tile * BN;
-            if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, p.status)) break;
-            tc_fence_after();
+            const int m0 = c.m_tile * BM, n0 = c.n_tile * BN + col_lo;
             const int row0 = m0 + q * 32;
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            for (int cc = 0; cc < BN; cc += 32) {
-                const int nc = n0 + cc;
-                if (nc >= p.N) break;
-                if (p.has_aux && lane == 0) {
-                    mbar_expect_tx(abar, 4096);
-                    tma_load_2d(auxs, &tmAux, nc, row0, abar);
+            const int ncols = min(BN / 2, p.N - n0);
+            const int nchunks = ncols > 0 ? (ncols + EC - 1) / EC : 0;
+            auto aux_issue = [&](int k) {    // input box of chunk k of this tile (lane 0)
+                const uint32_t slot = aux_issued % (uint32_t)ring;
+                const uint32_t bar = smem_u32(&aux_bar[ew][slot]);
+                mbar_expect_tx(bar, (uint32_t)aux_bytes);
+                tma_load_2d(smem_u32(wbuf + slot * aux_bytes), &tmAux, n0 + k * EC, row0, bar);
+                aux_issued++;
+            };
+            if (has_aux && lane == 0) {
+                bulk_wait_read(0);           // earlier stores out of the ring are done reading
+                for (int k = 0; k < min(ring - 1, nchunks); k++) aux_issue(k);
+                // the next tile's input rows of this warp go to L2 while this tile runs
+                const long long un = u + gridDim.x;
+                if (un < p.units) {
+                    Unit cn = unit_coords(p, un);
+                    const int nn0 = cn.n_tile * BN + col_lo, nr0 = cn.m_tile * BM + q * 32;
+                    if (nr0 < p.M)
+                        for (int k = 0; k < BN / 2 && nn0 + k < p.N; k += EC) tma_prefetch_l2(&tmAux, nn0 + k, nr0);
                 }
-                uint32_t r[32];
-                tmem_ld32(taddr + (uint32_t)cc, r);
-                // the previous chunk's stores have finished reading both boxes
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-                if (p.has_aux) {
-                    if (!mbar_wait(abar, aux_phase, &s_abort, p.status)) { ok = false; break; }
-                    aux_phase ^= 1u;
-                }
-                float x[32];
+            }
+            if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + col_lo);
+            for (int k = 0; k < nchunks; k++) {
+                const int nc = n0 + k * EC;
+                uint32_t r[16];
+                tmem_ld16(taddr + (uint32_t)(k * EC), r);
+                float x[16];
 #pragma unroll
-                for (int j = 0; j < 32; j++) x[j] = __uint_as_float(r[j]);
-                if (!p.partial) {
-                    if (p.bias) {
-                        if (nc + 32 <= p.N) {
-                            const float4* b4 = reinterpret_cast<const float4*>(p.bias + nc);
+                for (int j = 0; j < 16; j++) x[j] = __uint_as_float(r[j]);
+                if (!p.partial && p.bias) {
+                    if (nc + EC <= p.N) {
+                        const float4* b4 = reinterpret_cast<const float4*>(p.bias + nc);
 #pragma unroll
-                            for (int j = 0; j < 8; j++) {
-                                const float4 bv = __ldg(b4 + j);
-                                x[4 * j] += bv.x; x[4 * j + 1] += bv.y; x[4 * j + 2] += bv.z; x[4 * j + 3] += bv.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; j++) x[j] += nc + j < p.N ? __ldg(p.bias + nc + j) : 0.f;
+                        for (int j = 0; j < 4; j++) {
+                            const float4 bv = __ldg(b4 + j);
+                            x[4 * j] += bv.x; x[4 * j + 1] += bv.y; x[4 * j + 2] += bv.z; x[4 * j + 3] += bv.w;
                         }
-                    }
-                    if (p.gelu) {
+                    } else {
 #pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            *reinterpret_cast<float4*>(auxb + sw128(lane, j)) =
-                                make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; j++) x[j] = gelu_fwd_fast(x[j]);
-                    } else if (p.has_aux) {
-#pragma unroll
-                        for (int j = 0; j < 8; j++) {
-                            const float4 a = *reinterpret_cast<const float4*>(auxb + sw128(lane, j));
-                            if (p.aux_residual) {
-                                x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
-                            } else {
-                                x[4 * j] *= gelu_grad_fast(a.x); x[4 * j + 1] *= gelu_grad_fast(a.y);
-                                x[4 * j + 2] *= gelu_grad_fast(a.z); x[4 * j + 3] *= gelu_grad_fast(a.w);
-                            }
-                        }
+                        for (int j = 0; j < 16; j++) x[j] += nc + j < p.N ? __ldg(p.bias + nc + j) : 0.f;
                     }
                 }
-                if (p.out_bf16) {
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        __nv_bfloat162 h0 = __floats2bfloat162_rn(x[8 * k], x[8 * k + 1]);
-                        __nv_bfloat162 h1 = __floats2bfloat162_rn(x[8 * k + 2], x[8 * k + 3]);
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(x[8 * k + 4], x[8 * k + 5]);
-                        __nv_bfloat162 h3 = __floats2bfloat162_rn(x[8 * k + 6], x[8 * k + 7]);
-                        *reinterpret_cast<uint4*>(outb + sw64(lane, k)) =
-                            make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                                       *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+                uint8_t* outb;
+                if (has_aux) {
+                    // the chunk's input box: read, then overwrite with the output
+                    const uint32_t slot = aux_seq % (uint32_t)ring;
+                    if (!mbar_wait(smem_u32(&aux_bar[ew][slot]), (aux_seq / (uint32_t)ring) & 1u, &s_abort,
+                                   p.status)) {
+                        ok = false;
+                        break;
                     }
+                    aux_seq++;
+                    outb = wbuf + slot * aux_bytes;
+                    float a[16];
+                    get_row16(outb, lane, a, aux_bytes == 1024);
+                    if (p.aux_residual) {
+#pragma unroll
+                        for (int j = 0; j < 16; j++) x[j] += a[j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; j++) x[j] *= gelu_grad_fast(a[j]);
+                    }
+                    __syncwarp();            // every lane has read the box before it is overwritten
                 } else {
+                    const uint32_t b = box_seq % (uint32_t)nbuf;
+                    outb = wbuf + b * chunk_bytes;
+                    // the store that last read this box is done reading
+                    if (lane == 0) bulk_wait_read(nbuf - 1);
+                    __syncwarp();
+                    if (pre) {
+                        put_row16(outb + out_bytes, lane, x, pre16);
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        *reinterpret_cast<float4*>(outb + sw128(lane, j)) =
-                            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        for (int j = 0; j < 16; j++) x[j] = gelu_fwd_fast(x[j]);
+                    }
                 }
+                put_row16(outb, lane, x, out16);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
-                    if (p.partial) tma_store_3d(&tmOut, nc, row0, c.split, outs);
-                    else tma_store_2d(&tmOut, nc, row0, outs);
-                    if (p.gelu && !p.partial) tma_store_2d(&tmPre, nc, row0, auxs);
+                    if (p.partial) tma_store_3d(&tmOut, nc, row0, c.split, smem_u32(outb));
+                    else tma_store_2d(&tmOut, nc, row0, smem_u32(outb));
+                    if (pre && !has_aux) tma_store_2d(&tmPre, nc, row0, smem_u32(outb + out_bytes));
                     bulk_commit();
+                    // refill: the box of chunk k - 1 (stored one chunk ago) takes chunk k + ring - 1
+                    if (has_aux && k + ring - 1 < nchunks) {
+                        bulk_wait_read(1);
+                        aux_issue(k + ring - 1);
+                    }
                 }
+                box_seq++;
             }
+            if (!ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (has_aux && !ok && lane == 0) {
+            // input loads still in flight land in this CTA's shared memory: wait
+            // (bounded, ignoring the abort flag) for each before leaving
+            for (uint32_t g = aux_seq; g != aux_issued; g++) {
+                const uint32_t bar = smem_u32(&aux_bar[ew][g % (uint32_t)ring]);
+                uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(bar, (g / (uint32_t)ring) & 1u) && globaltimer() - t0 < WAIT_NS) {
+                }
+            }
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -622,7 +732,7 @@ static bool make_map_3d(CUtensorMap* map, const float* ptr, int cols, int rows, 
     cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -647,7 +757,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     static bool attr_done = false;
     if (!attr_done) {
         if (cudaFuncSetAttribute(gemm_tc_kernel<BN, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(S::SMEM + EPI_BYTES)) != cudaSuccess) {
+                                 (int)S::SMEM) != cudaSuccess) {
             (void)cudaGetLastError();
             return GPT2_ECUDA;
         }
@@ -661,22 +771,26 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     ok = ok && (g.b_kmajor ? make_map(&mp->b, g.B, BF16, g.K, g.N, g.ldb, E::BK, BN, KSW)
                            : make_map(&mp->b, g.B, BF16, g.N, g.K, g.ldb, E::MN_BOX, E::BK, MSW));
     Params p{};
-    // epilogue maps: output (fp32 128-byte rows or bf16 64-byte rows), aux, pre
+    // epilogue maps, boxes of 32 rows x EC columns: fp32 64-byte rows (64-byte
+    // swizzle) or bf16 32-byte rows (32-byte swizzle)
+    auto swz = [](bool b16) { return b16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B; };
     if (partial) {
-        ok = ok && make_map_3d(&mp->out, partial, g.N, g.M, split, 32, 32);
+        ok = ok && make_map_3d(&mp->out, partial, g.N, g.M, split, EC, 32);
     } else {
-        ok = ok && make_map(&mp->out, e.out, e.out_bf16, g.N, g.M, e.ldo, 32, 32,
-                            e.out_bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && make_map(&mp->out, e.out, e.out_bf16, g.N, g.M, e.ldo, EC, 32, swz(e.out_bf16));
         if (e.residual) {
-            ok = ok && make_map(&mp->aux, e.residual, false, g.N, g.M, e.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+            ok = ok && make_map(&mp->aux, e.residual, false, g.N, g.M, e.ldo, EC, 32, swz(false));
             p.has_aux = 1;
             p.aux_residual = 1;
         } else if (e.gelu_x) {
-            ok = ok && make_map(&mp->aux, e.gelu_x, false, g.N, g.M, e.ldg, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+            ok = ok && make_map(&mp->aux, e.gelu_x, e.gelu_x_bf16, g.N, g.M, e.ldg, EC, 32, swz(e.gelu_x_bf16));
             p.has_aux = 1;
+            p.aux_bf16 = e.gelu_x_bf16 ? 1 : 0;
         }
-        if (e.gelu) ok = ok && make_map(&mp->pre, e.out_pre, false, g.N, g.M, e.ldo, 32, 32,
-                                        CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e.gelu) {
+            ok = ok && make_map(&mp->pre, e.out_pre, e.pre_bf16, g.N, g.M, e.ldo, EC, 32, swz(e.pre_bf16));
+            p.pre_bf16 = e.pre_bf16 ? 1 : 0;
+        }
     }
     if (!ok) return GPT2_ENOTSUP;
     if (!p.has_aux) mp->aux = mp->out;             // unused, but a valid map
@@ -708,7 +822,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
 template <int BN, bool BF16>
 static int run(const Maps& mp, const Params& p, cudaStream_t st) {
     int grid = (int)std::min<long long>(p.units, num_sms());
-    count_launch(), gemm_tc_kernel<BN, BF16><<<grid, THREADS, Shape<BN, BF16>::SMEM + EPI_BYTES, st>>>(
+    count_launch(), gemm_tc_kernel<BN, BF16><<<grid, THREADS, Shape<BN, BF16>::SMEM, st>>>(
         mp.a, mp.b, mp.out, mp.aux, mp.pre, p);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
@@ -745,8 +859,8 @@ bool gemm_tc_epilogue_supported(const GemmEpilogue& e) {
     const int oa = e.out_bf16 ? 8 : 4;
     if (!aligned16(e.out) || e.ldo % oa) return false;
     if (e.residual && (!aligned16(e.residual) || e.ldo % 4)) return false;
-    if (e.gelu && (!aligned16(e.out_pre) || e.ldo % 4)) return false;
-    if (e.gelu_x && (!aligned16(e.gelu_x) || e.ldg % 4)) return false;
+    if (e.gelu && (!aligned16(e.out_pre) || e.ldo % (e.pre_bf16 ? 8 : 4))) return false;
+    if (e.gelu_x && (!aligned16(e.gelu_x) || e.ldg % (e.gelu_x_bf16 ? 8 : 4))) return false;
     if (e.bias && (reinterpret_cast<uintptr_t>(e.bias) & 15)) return false;
     return true;
 }

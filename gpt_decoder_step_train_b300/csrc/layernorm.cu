@@ -9,12 +9,17 @@
 // for every layer): with xhat = (x-mean)*rstd and g = dy*w,
 //   dx += rstd * (g - mean(g) - xhat * mean(g * xhat)),
 //   dw = sum_rows dy * xhat,  db = sum_rows dy.
-// dw/db are reduced deterministically: each block sums its rows in a fixed
-// order into a per-block partial, and a second kernel sums the partials in
-// block order.
+// The backward also returns the column sum of the gradient it leaves in dx,
+// which is the bias gradient of the projection that wrote the residual.  All
+// column sums are deterministic: each block sums its rows in a fixed order
+// into a per-block partial, and a second kernel sums the partials in block
+// order.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gpt2k {
 
@@ -79,60 +84,114 @@ ln_fwd_kernel(void* __restrict__ yv, float* __restrict__ mean, float* __restrict
     }
 }
 
-// Block `blk` handles rows [blk*rpb, min(N, (blk+1)*rpb)); warp w takes rows
-// start+w, start+w+LN_WARPS, ...  partial[blk][0][C] = sum dy*xhat,
-// partial[blk][1][C] = sum dy over the block's rows.
-template <int NV>
-__global__ void __launch_bounds__(LN_WARPS * 32)
+// ---------------------------------------------------------------- backward
+// Persistent: two blocks per SM; block blk owns the rows [blk*rpb, min(N, (blk+1)*rpb)) and
+// walks them in tiles of `rb` rows.  Thread 0 streams each tile's rows of x,
+// dy and (when accumulating) the incoming dx into a ring of shared-memory
+// stages with bulk copies; then
+//   phase 1, one warp per row: the two row means of g = dy*w and g*xhat, the
+//            new dx row (fp32 and optionally bf16) written to global memory
+//            and kept in the stage for phase 2;
+//   phase 2, one thread per column: dw += dy*xhat, db += dy, ds += dx over the
+//            tile's rows, in row order.
+// Each block writes its column sums to partial[blk][3][C]; a second kernel adds
+// the blocks in block order.  ds is the column sum of the gradient leaving the
+// LayerNorm: the bias gradient of the projection that wrote the residual.
+constexpr int LNB_THREADS = 256;
+constexpr int LNB_WARPS = LNB_THREADS / 32;
+constexpr int LNB_BLOCKS_PER_SM = 2;
+constexpr int LNB_MAX_STAGES = 4;
+constexpr int LNB_MAX_BLOCKS = 512;
+constexpr size_t LNB_SMEM_BUDGET = 110 * 1024;    // per block, two blocks per SM
+
+struct LnbPlan {
+    int rb, stages, grid, rpb;
+    size_t stage_bytes;
+};
+
+// The largest tile (8, 4, 2 or 1 rows) that still leaves two stages in the budget.
+static LnbPlan lnb_plan(int N, int C) {
+    LnbPlan p;
+    p.rb = 8;
+    while (p.rb > 1 && 2 * (size_t)3 * p.rb * C * sizeof(float) > LNB_SMEM_BUDGET) p.rb /= 2;
+    p.stage_bytes = (size_t)3 * p.rb * C * sizeof(float);
+    p.stages = (int)std::max<size_t>(1, std::min<size_t>(LNB_MAX_STAGES, LNB_SMEM_BUDGET / p.stage_bytes));
+    p.grid = std::min({LNB_BLOCKS_PER_SM * num_sms(), LNB_MAX_BLOCKS, ceil_div(N, p.rb)});
+    p.rpb = ceil_div(N, p.grid);
+    return p;
+}
+
+template <int CPT>   // columns per thread: ceil(C / LNB_THREADS)
+__global__ void __launch_bounds__(LNB_THREADS, LNB_BLOCKS_PER_SM)
 ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* __restrict__ partial,
-              const float* __restrict__ dy,
-              const float* __restrict__ x, const float* __restrict__ w,
-              const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C,
-              int rpb) {
-    extern __shared__ float4 sh4[];              // [2][C4]
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int C4 = C >> 2;
-    int start = blockIdx.x * rpb, end = min(N, start + rpb);
-    const float4* w4 = reinterpret_cast<const float4*>(w);
-    float4 adw[NV], adb[NV];
-#pragma unroll
-    for (int i = 0; i < NV; i++) {
-        adw[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        adb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ w,
+              const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C, int rpb,
+              int rb, int stages, int accumulate, int* status) {
+    extern __shared__ __align__(128) float lsm[];
+    __shared__ __align__(8) uint64_t full[LNB_MAX_STAGES];
+    __shared__ float s_mu[8], s_rs[8];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C4 = C >> 2;
+    const int r0 = blockIdx.x * rpb, r1 = min(N, r0 + rpb);
+    const int ntiles = r0 < r1 ? (r1 - r0 + rb - 1) / rb : 0;
+    const size_t tile = (size_t)rb * C;                // floats per array per stage
+    auto stage = [&](int s) { return lsm + (size_t)s * 3 * tile; };
+    if (tid == 0) {
+        for (int s = 0; s < stages; s++) ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+        ptx::fence_mbar_init();
     }
-    for (int row = start + warp; row < end; row += LN_WARPS) {
-        const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * C);
-        const float4* gr = reinterpret_cast<const float4*>(dy + (size_t)row * C);
-        float mu = mean[row], r = rstd[row];
-        float sg = 0.f, sgx = 0.f;
+    __syncthreads();
+    int issued = 0;                                    // thread 0: tiles requested
+    auto issue = [&](int t) {
+        const int tr0 = r0 + t * rb, nr = min(rb, r1 - tr0), s = t % stages;
+        const uint32_t bytes = (uint32_t)nr * C * sizeof(float);
+        const uint32_t bar = ptx::smem_u32(&full[s]);
+        float* st = stage(s);
+        ptx::mbar_expect_tx(bar, bytes * (accumulate ? 3 : 2));
+        ptx::bulk_g2s(ptx::smem_u32(st), x + (size_t)tr0 * C, bytes, bar);
+        ptx::bulk_g2s(ptx::smem_u32(st + tile), dy + (size_t)tr0 * C, bytes, bar);
+        if (accumulate) ptx::bulk_g2s(ptx::smem_u32(st + 2 * tile), dx + (size_t)tr0 * C, bytes, bar);
+        issued++;
+    };
+    if (tid == 0)
+        for (int t = 0; t < min(stages, ntiles); t++) issue(t);
+    float aw[CPT], ab[CPT], as[CPT];
 #pragma unroll
-        for (int i = 0; i < NV; i++) {
-            int c = lane + 32 * i;
-            if (c < C4) {
-                float4 xv = xr[c], d = gr[c], ww = w4[c];
-                float4 xh = make_float4((xv.x - mu) * r, (xv.y - mu) * r, (xv.z - mu) * r, (xv.w - mu) * r);
-                float4 g = make_float4(d.x * ww.x, d.y * ww.y, d.z * ww.z, d.w * ww.w);
-                sg += (g.x + g.y) + (g.z + g.w);
-                sgx += (g.x * xh.x + g.y * xh.y) + (g.z * xh.z + g.w * xh.w);
-                adw[i].x += d.x * xh.x; adw[i].y += d.y * xh.y;
-                adw[i].z += d.z * xh.z; adw[i].w += d.w * xh.w;
-                adb[i].x += d.x; adb[i].y += d.y; adb[i].z += d.z; adb[i].w += d.w;
+    for (int j = 0; j < CPT; j++) aw[j] = ab[j] = as[j] = 0.f;
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    int t = 0;
+    for (; t < ntiles; t++) {
+        const int s = t % stages, tr0 = r0 + t * rb, nr = min(rb, r1 - tr0);
+        const bool got = ptx::mbar_wait_bounded(ptx::smem_u32(&full[s]), (uint32_t)(t / stages) & 1u);
+        if (!__syncthreads_and(got)) break;
+        float* xs = stage(s);
+        float* gs = xs + tile;
+        float* os = xs + 2 * tile;                     // incoming dx, then the new dx
+        // phase 1: warp per row
+        for (int r = warp; r < nr; r += LNB_WARPS) {
+            const int row = tr0 + r;
+            const float mu = mean[row], rs = rstd[row];
+            if (lane == 0) { s_mu[r] = mu; s_rs[r] = rs; }
+            const float4* xr = reinterpret_cast<const float4*>(xs + (size_t)r * C);
+            const float4* gr = reinterpret_cast<const float4*>(gs + (size_t)r * C);
+            float4* orow = reinterpret_cast<float4*>(os + (size_t)r * C);
+            float sg = 0.f, sgx = 0.f;
+            for (int c = lane; c < C4; c += 32) {
+                const float4 xv = xr[c], d = gr[c], ww = __ldg(w4 + c);
+                const float gx = d.x * ww.x, gy = d.y * ww.y, gz = d.z * ww.z, gw = d.w * ww.w;
+                sg += (gx + gy) + (gz + gw);
+                sgx += (gx * (xv.x - mu) * rs + gy * (xv.y - mu) * rs) + (gz * (xv.z - mu) * rs + gw * (xv.w - mu) * rs);
             }
-        }
-        float mg = warp_sum(sg) / (float)C, mgx = warp_sum(sgx) / (float)C;
-        float4* dxr = reinterpret_cast<float4*>(dx + (size_t)row * C);
-        // second pass re-reads the row (L1-resident) instead of holding it in registers
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            int c = lane + 32 * i;
-            if (c < C4) {
-                float4 xv = xr[c], d = gr[c], ww = w4[c];
-                float4 o = dxr[c];
-                float xh, g;
-                xh = (xv.x - mu) * r; g = d.x * ww.x; o.x += r * (g - mg - xh * mgx);
-                xh = (xv.y - mu) * r; g = d.y * ww.y; o.y += r * (g - mg - xh * mgx);
-                xh = (xv.z - mu) * r; g = d.z * ww.z; o.z += r * (g - mg - xh * mgx);
-                xh = (xv.w - mu) * r; g = d.w * ww.w; o.w += r * (g - mg - xh * mgx);
+            const float mg = warp_sum(sg) / (float)C, mgx = warp_sum(sgx) / (float)C;
+            float4* dxr = reinterpret_cast<float4*>(dx + (size_t)row * C);
+            for (int c = lane; c < C4; c += 32) {
+                const float4 xv = xr[c], d = gr[c], ww = __ldg(w4 + c);
+                float4 o = accumulate ? orow[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                o.x += rs * (d.x * ww.x - mg - (xv.x - mu) * rs * mgx);
+                o.y += rs * (d.y * ww.y - mg - (xv.y - mu) * rs * mgx);
+                o.z += rs * (d.z * ww.z - mg - (xv.z - mu) * rs * mgx);
+                o.w += rs * (d.w * ww.w - mg - (xv.w - mu) * rs * mgx);
+                orow[c] = o;
                 dxr[c] = o;
                 if (dx16) {
                     __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
@@ -141,56 +200,66 @@ ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* _
                 }
             }
         }
-    }
-    // fixed-order reduction over the block's warps: warp 0 stores, then 1..7 add
-    float4* sdw = sh4;
-    float4* sdb = sh4 + C4;
-    for (int k = 0; k < LN_WARPS; k++) {
-        if (warp == k) {
+        __syncthreads();
+        // phase 2: thread per column, rows in order
 #pragma unroll
-            for (int i = 0; i < NV; i++) {
-                int c = lane + 32 * i;
-                if (c < C4) {
-                    if (k == 0) {
-                        sdw[c] = adw[i];
-                        sdb[c] = adb[i];
-                    } else {
-                        float4 a = sdw[c], bb = sdb[c];
-                        a.x += adw[i].x; a.y += adw[i].y; a.z += adw[i].z; a.w += adw[i].w;
-                        bb.x += adb[i].x; bb.y += adb[i].y; bb.z += adb[i].z; bb.w += adb[i].w;
-                        sdw[c] = a;
-                        sdb[c] = bb;
-                    }
+        for (int j = 0; j < CPT; j++) {
+            const int c = tid + j * LNB_THREADS;
+            if (c < C) {
+                for (int r = 0; r < nr; r++) {
+                    const float d = gs[(size_t)r * C + c];
+                    aw[j] += d * ((xs[(size_t)r * C + c] - s_mu[r]) * s_rs[r]);
+                    ab[j] += d;
+                    as[j] += os[(size_t)r * C + c];
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();                               // the stage is free again
+        if (tid == 0 && t + stages < ntiles) issue(t + stages);
     }
-    float4* out = reinterpret_cast<float4*>(partial) + (size_t)blockIdx.x * 2 * C4;
-    for (int c = threadIdx.x; c < 2 * C4; c += blockDim.x) out[c] = sh4[c];
+    if (t < ntiles) {
+        // a copy never arrived: flag it, and wait (bounded) for the copies still
+        // writing into this block's shared memory before leaving
+        if (tid == 0) {
+            set_status(status, GPT2_STATUS_TIMEOUT);
+            for (int u = t; u < issued; u++)
+                (void)ptx::mbar_wait_bounded(ptx::smem_u32(&full[u % stages]), (uint32_t)(u / stages) & 1u);
+        }
+        return;
+    }
+    float* out = partial + (size_t)blockIdx.x * 3 * C;
+#pragma unroll
+    for (int j = 0; j < CPT; j++) {
+        const int c = tid + j * LNB_THREADS;
+        if (c < C) {
+            out[c] = aw[j];
+            out[C + c] = ab[j];
+            out[2 * C + c] = as[j];
+        }
+    }
 }
 
-// dw[c] = sum_blk partial[blk][0][c], db[c] = sum_blk partial[blk][1][c].
-// Block (32 columns x 16 lanes): lane y sums blocks y, y+16, ... in order, then
-// the 16 lane sums are added in lane order.
-__global__ void ln_bwd_reduce_kernel(float* __restrict__ dw, float* __restrict__ db,
+// out_k[c] = sum_blk partial[blk][k][c] for k = 0 (dw), 1 (db), 2 (ds, when
+// wanted).  Block (32 columns x 16 lanes): lane y sums blocks y, y+16, ... in
+// order, then the 16 lane sums are added in lane order.
+__global__ void ln_bwd_reduce_kernel(float* __restrict__ dw, float* __restrict__ db, float* __restrict__ ds,
                                      const float* __restrict__ partial, int nblk, int C) {
     __shared__ float sh[16][33];
-    const int c = blockIdx.x * 32 + threadIdx.x;
+    const int c = blockIdx.x * 32 + threadIdx.x;       // over 3C
+    const int width = ds ? 3 * C : 2 * C;
     float s = 0.f;
-    if (c < 2 * C)
-        for (int k = threadIdx.y; k < nblk; k += 16) s += partial[(size_t)k * 2 * C + c];
+    if (c < width)
+        for (int k = threadIdx.y; k < nblk; k += 16) s += partial[(size_t)k * 3 * C + c];
     sh[threadIdx.y][threadIdx.x] = s;
     __syncthreads();
-    if (threadIdx.y == 0 && c < 2 * C) {
+    if (threadIdx.y == 0 && c < width) {
         float t = sh[0][threadIdx.x];
         for (int k = 1; k < 16; k++) t += sh[k][threadIdx.x];
         if (c < C) dw[c] = t;
-        else db[c - C] = t;
+        else if (c < 2 * C) db[c - C] = t;
+        else ds[c - 2 * C] = t;
     }
 }
-
-static int ln_bwd_blocks(int N) { return std::min(ceil_div(N, 32), 512); }
 
 }  // namespace gpt2k
 
@@ -232,35 +301,45 @@ GPT2_API int gpt2_op_layernorm_forward_bf16(void* y, float* mean, float* rstd, c
 
 GPT2_API size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C) {
     if (N < 1 || C < 1) return 0;
-    return (size_t)ln_bwd_blocks(N) * 2 * C * sizeof(float);
+    return (size_t)LNB_MAX_BLOCKS * 3 * C * sizeof(float);
 }
 
-GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db,
+GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, float* dx_colsum,
                                         const float* dy, const float* x, const float* w,
-                                        const float* mean, const float* rstd, int N, int C,
-                                        void* scratch, size_t scratch_bytes, void* stream) {
+                                        const float* mean, const float* rstd, int N, int C, int accumulate,
+                                        void* scratch, size_t scratch_bytes, int* status, void* stream) {
     if (!dx || !dw || !db || !dy || !x || !w || !mean || !rstd || N < 1 || C < 4 || C % 4 ||
-        C > 32 * 4 * LN_MAXV)
+        C > LNB_THREADS * 8)
         return GPT2_EINVAL;
     if (!aligned16(dx) || !aligned16(dy) || !aligned16(x) || !aligned16(w) || !aligned16(scratch))
         return GPT2_EINVAL;
     if (!scratch || scratch_bytes < gpt2_op_layernorm_backward_scratch_bytes(N, C)) return GPT2_ENOMEM;
-    int nblk = ln_bwd_blocks(N);
-    int rpb = ceil_div(N, nblk);
-    float* partial = reinterpret_cast<float*>(scratch);
-    size_t smem = 2 * (size_t)C * sizeof(float);
-    int nv = ceil_div(C / 4, 32);
-    cudaStream_t st = as_stream(stream);
     __nv_bfloat16* dx16 = static_cast<__nv_bfloat16*>(dx_bf16);
     if (dx16 && (reinterpret_cast<uintptr_t>(dx16) & 7)) return GPT2_EINVAL;
-#define LNB(NVV) count_launch(), ln_bwd_kernel<NVV><<<nblk, LN_WARPS * 32, smem, st>>>(dx, dx16, partial, dy, x, w, mean, rstd, N, C, rpb)
-    if (nv <= 2) LNB(2);
-    else if (nv <= 6) LNB(6);
-    else if (nv <= 8) LNB(8);
-    else if (nv <= 13) LNB(13);
-    else LNB(LN_MAXV);
+    const LnbPlan pl = lnb_plan(N, C);
+    const size_t smem = (size_t)pl.stages * pl.stage_bytes;
+    float* partial = reinterpret_cast<float*>(scratch);
+    cudaStream_t st = as_stream(stream);
+    const int cpt = ceil_div(C, LNB_THREADS);
+#define LNB(CPT)                                                                                         \
+    do {                                                                                                 \
+        static bool attr = false;                                                                        \
+        if (!attr) {                                                                                     \
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                               (int)(LNB_SMEM_BUDGET)));                                 \
+            attr = true;                                                                                 \
+        }                                                                                                \
+        count_launch(), ln_bwd_kernel<CPT><<<pl.grid, LNB_THREADS, smem, st>>>(                          \
+            dx, dx16, partial, dy, x, w, mean, rstd, N, C, pl.rpb, pl.rb, pl.stages, accumulate ? 1 : 0, status); \
+    } while (0)
+    if (cpt <= 1) LNB(1);
+    else if (cpt <= 2) LNB(2);
+    else if (cpt <= 3) LNB(3);
+    else if (cpt <= 4) LNB(4);
+    else LNB(8);
 #undef LNB
-    count_launch(), ln_bwd_reduce_kernel<<<ceil_div(2 * C, 32), dim3(32, 16), 0, st>>>(dw, db, partial, nblk, C);
+    count_launch(), ln_bwd_reduce_kernel<<<ceil_div(3 * C, 32), dim3(32, 16), 0, st>>>(dw, db, dx_colsum, partial,
+                                                                                       pl.grid, C);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

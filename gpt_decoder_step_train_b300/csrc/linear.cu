@@ -144,7 +144,7 @@ static int run_gemm(const GemmProblem& p, const GemmEpilogue& e, int mode, cudaS
 }
 
 // ---- the three products of a linear layer, for every operand type ---------
-int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, const void* w,
+int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, const void* w,
                    bool bf16, const float* bias, const float* residual, int N, int IC, int OC,
                    int ld_out, int flags, int mode, int* status, cudaStream_t st) {
     if (!out || !inp || !w || N < 1 || IC < 1 || OC < 1 || ld_out < OC) return GPT2_EINVAL;
@@ -155,6 +155,7 @@ int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, co
     e.ldo = ld_out;
     e.out_bf16 = out_bf16;
     e.out_pre = out_pre;
+    e.pre_bf16 = bf16 ? 1 : 0;
     e.bias = bias;
     e.residual = residual;
     e.gelu = (flags & GPT2_LINEAR_GELU) ? 1 : 0;
@@ -169,7 +170,7 @@ int linear_forward(void* out, bool out_bf16, float* out_pre, const void* inp, co
 }
 
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
-                          const float* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
+                          const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
                           int* status, cudaStream_t st) {
     if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
     GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status, bf16};
@@ -178,6 +179,7 @@ int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const vo
     e.ldo = IC;
     e.out_bf16 = dinp_bf16;
     e.gelu_x = gelu_x;
+    e.gelu_x_bf16 = bf16 ? 1 : 0;
     e.ldg = IC;
     return run_gemm(p, e, mode, st);
 }
@@ -270,9 +272,11 @@ GPT2_API int gpt2_op_gemm(const gpt2_gemm_args* a, int mode, int* status, void* 
     e.ldo = a->ldo;
     e.out_bf16 = a->out_bf16;
     e.out_pre = a->out_pre;
+    e.pre_bf16 = a->pre_bf16;
     e.bias = a->bias;
     e.residual = a->residual;
     e.gelu_x = a->gelu_x;
+    e.gelu_x_bf16 = a->gelu_x_bf16;
     e.ldg = a->ldg;
     e.gelu = a->gelu;
     return run_gemm(p, e, mode, as_stream(stream));

@@ -95,10 +95,10 @@ struct gpt2 {
     int *tok, *tgt;
     DevFlags* flags;
     // fp32 activations; per-layer arrays have a fixed stride of R rows
-    float *x0, *ln1_mean, *ln1_rstd, *lse, *res2, *ln2_mean, *ln2_rstd, *fch, *res3;
+    float *x0, *ln1_mean, *ln1_rstd, *lse, *res2, *ln2_mean, *ln2_rstd, *res3;
     float *lnf_mean, *lnf_rstd, *logits, *losses;
     // operand activations (es bytes per element): GEMM / attention inputs
-    char *ln1, *qkv, *atty, *ln2, *fchg, *lnf;
+    char *ln1, *qkv, *atty, *ln2, *fch, *fchg, *lnf;
     // backward: fp32 residual-stream gradient and LN-output gradient; operands
     float *dres, *dln;
     char *dres16, *dz16, *dbig, *datty, *dqkv;
@@ -147,7 +147,7 @@ static size_t plan(gpt2* m, char* base) {
     m->ln2 = O(L * R * C);
     m->ln2_mean = F(L * R);
     m->ln2_rstd = F(L * R);
-    m->fch = F(L * R * 4 * C);
+    m->fch = O(L * R * 4 * C);
     m->fchg = O(L * R * 4 * C);
     m->res3 = F(L * R * C);
     m->lnf = O(R * C);
@@ -232,7 +232,7 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
         char* atty = Orow(m, m->atty, l, C);
         float* res2 = m->res2 + l * R * C;
         char* ln2 = Orow(m, m->ln2, l, C);
-        float* fch = m->fch + l * R * 4 * C;
+        char* fch = Orow(m, m->fch, l, 4 * C);
         char* fchg = Orow(m, m->fchg, l, 4 * C);
         float* res3 = m->res3 + l * R * C;
         const size_t cc = (size_t)C * C;
@@ -285,11 +285,12 @@ static int backward_impl(gpt2* m) {
                                                m->Vp, mode, status, st));
     OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, WTE), dz_op, m->lnf, b16, N, C, c.V, m->Vp, sc, sb,
                                                  mode, status, st));
-    OP(OTHER, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), m->st) == cudaSuccess
-                  ? GPT2_OK : GPT2_ECUDA);
-    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LNFW), G(m, LNFB), m->dln,
+    // ln_f: the residual gradient starts here (written, not accumulated); its
+    // column sum is the last block's MLP c_proj bias gradient
+    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LNFW), G(m, LNFB),
+                                                 G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
                                                  m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW),
-                                                 m->lnf_mean, m->lnf_rstd, N, C, sc, sb, st));
+                                                 m->lnf_mean, m->lnf_rstd, N, C, 0, sc, sb, status, st));
     for (int l = L - 1; l >= 0; l--) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
         const char* ln1 = Orow(m, m->ln1, l, C);
@@ -297,33 +298,34 @@ static int backward_impl(gpt2* m) {
         const char* atty = Orow(m, m->atty, l, C);
         const float* res2 = m->res2 + l * R * C;
         const char* ln2 = Orow(m, m->ln2, l, C);
-        const float* fch = m->fch + l * R * 4 * C;
+        const char* fch = Orow(m, m->fch, l, 4 * C);
         const char* fchg = Orow(m, m->fchg, l, 4 * C);
         auto Wl = [&](int t, size_t per_layer) {
             return static_cast<const void*>(static_cast<const char*>(W(m, t)) + l * per_layer * wes);
         };
-        // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g; dbfp
+        // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g (its bias
+        // gradient came with the LayerNorm backward that produced dres)
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dres_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
                                                    4 * C, C, C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dres_op, fchg, b16, N,
                                                      4 * C, C, C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, bias_grad_any(G(m, FCPROJB) + l * C, m->dres, false, N, C, C, sc, sb, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dbig, Wl(FCW, 4 * cc), b16, nullptr, N,
                                                    C, 4 * C, 4 * C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCW) + l * 4 * cc, m->dbig, ln2, b16, N, C, 4 * C,
                                                      4 * C, sc, sb, mode, status, st));
         OP(BIAS_GRAD, bias_grad_any(G(m, FCB) + l * 4 * C, m->dbig, b16, N, 4 * C, 4 * C, sc, sb, st));
-        // ln_2: dres += LN'(dln2)
+        // ln_2: dres += LN'(dln2); the column sum of the result is the attention
+        // c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN2W) + l * C, G(m, LN2B) + l * C,
-                                                     m->dln, res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
-                                                     m->ln2_rstd + l * R, N, C, sc, sb, st));
-        // attention c_proj
+                                                     G(m, ATTPROJB) + l * C, m->dln, res2, P(m, LN2W) + l * C,
+                                                     m->ln2_mean + l * R, m->ln2_rstd + l * R, N, C, 1, sc, sb,
+                                                     status, st));
+        // attention c_proj (bias gradient: with ln_2's backward above)
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, dres_op, Wl(ATTPROJW, cc), b16, nullptr, N,
                                                    C, C, C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dres_op, atty, b16, N, C, C, C,
                                                      sc, sb, mode, status, st));
-        OP(BIAS_GRAD, bias_grad_any(G(m, ATTPROJB) + l * C, m->dres, false, N, C, C, sc, sb, st));
         // attention
         OP(ATTENTION_BWD, gpt2_op_attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T,
                                                      C, H, sc, sb, mode, status, st));
@@ -333,10 +335,12 @@ static int backward_impl(gpt2* m) {
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, QKVW) + l * 3 * cc, m->dqkv, ln1, b16, N, C, 3 * C,
                                                      3 * C, sc, sb, mode, status, st));
         OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->dqkv, b16, N, 3 * C, 3 * C, sc, sb, st));
-        // ln_1: dres += LN'(dln1)
+        // ln_1: dres += LN'(dln1); the column sum of the result is the previous
+        // block's MLP c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN1W) + l * C, G(m, LN1B) + l * C,
+                                                     l > 0 ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
                                                      m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R,
-                                                     m->ln1_rstd + l * R, N, C, sc, sb, st));
+                                                     m->ln1_rstd + l * R, N, C, 1, sc, sb, status, st));
     }
     OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V,
                                              sc, sb, st));
@@ -552,7 +556,7 @@ GPT2_API const float* gpt2_activation(gpt2* m, int which, int layer) {
         case 3: return op(m->atty, C);
         case 4: return m->res2 + l * R * C;
         case 5: return op(m->ln2, C);
-        case 6: return m->fch + l * R * 4 * C;
+        case 6: return op(m->fch, 4 * C);
         case 7: return op(m->fchg, 4 * C);
         case 8: return m->res3 + l * R * C;
         case 9: return reinterpret_cast<const float*>(m->lnf);

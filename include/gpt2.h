@@ -149,7 +149,8 @@ const float* gpt2_losses(gpt2* m);
  *   0 encoder output [C]   1 ln_1 output [C]   2 qkv [3C]   3 attention out [C]
  *   4 residual after attention [C]   5 ln_2 output [C]   6 c_fc output [4C]
  *   7 GELU output [4C]   8 block output [C]   9 ln_f output [C]
- * NULL for an invalid index. */
+ * fp32, except 1, 2, 3, 5, 6, 7 and 9 in GPT2_MODE_BF16, which are bf16 (the
+ * pointer is then to bf16 values despite its type).  NULL for an invalid index. */
 const float* gpt2_activation(gpt2* m, int which, int layer);
 
 /* ---- tracing -------------------------------------------------------------

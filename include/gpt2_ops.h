@@ -61,16 +61,23 @@ int gpt2_op_layernorm_forward(float* y, float* mean, float* rstd, const float* x
 int gpt2_op_layernorm_forward_bf16(void* y, float* mean, float* rstd, const float* x,
                                    const float* w, const float* b, int N, int C, void* stream);
 
-/* LayerNorm backward.  dx += rstd*(g - mean(g) - xhat*mean(g*xhat)) with
- * g = dy*w and xhat = (x-mean)*rstd (dx is ACCUMULATED: it is the residual
- * stream's gradient); dw = sum_rows dy*xhat, db = sum_rows dy (OVERWRITTEN),
- * reduced in a fixed order.  dx_bf16 [N,C] (8-byte aligned) or NULL: also
- * receives the updated dx in bf16.  scratch: gpt2_op_layernorm_backward_scratch_bytes. */
+/* LayerNorm backward.  With g = dy*w and xhat = (x-mean)*rstd, the row
+ * gradient rstd*(g - mean(g) - xhat*mean(g*xhat)) is ADDED to dx when
+ * accumulate != 0 (dx is the residual stream's gradient) or written over it
+ * when accumulate == 0 (dx is then not read).  dw = sum_rows dy*xhat,
+ * db = sum_rows dy (OVERWRITTEN); dx_colsum [C] or NULL: sum_rows of the
+ * resulting dx (the bias gradient of the projection whose output fed this
+ * residual).  All column sums run in a fixed order (rows within a block, then
+ * blocks).  dx_bf16 [N,C] (8-byte aligned) or NULL: also receives the new dx in
+ * bf16.  C % 4 == 0, C <= 2048; x, dy, dx, w 16-byte aligned.  Rows stream
+ * through shared memory by bulk copy; a copy that does not arrive within a
+ * second sets GPT2_STATUS_TIMEOUT in *status (which may be NULL).
+ * scratch: gpt2_op_layernorm_backward_scratch_bytes. */
 size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C);
-int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, const float* dy,
-                               const float* x, const float* w, const float* mean,
-                               const float* rstd, int N, int C, void* scratch,
-                               size_t scratch_bytes, void* stream);
+int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, float* dx_colsum,
+                               const float* dy, const float* x, const float* w, const float* mean,
+                               const float* rstd, int N, int C, int accumulate, void* scratch,
+                               size_t scratch_bytes, int* status, void* stream);
 
 /* Linear forward: out[n,o] = sum_i inp[n,i]*w[o,i] + bias[o] (w is [OC,IC]).
  *   bias: [OC] or NULL.  residual: [N,ld_out] or NULL -> out = residual + ...
@@ -115,18 +122,21 @@ int gpt2_op_bias_grad(float* db, const void* dout, int dout_bf16, int N, int OC,
  * are fp32 (mode FP32 or TF32) or bf16 (bf16 != 0, mode BF16; tensor cores
  * only).  Epilogue per element, in this order: + bias[n]; GELU (out_pre = value,
  * value = gelu(value)); + residual[m*ldo+n]; * gelu'(gelu_x[m*ldg+n]); stored to
- * out[m*ldo+n] as fp32, or bf16 when out_bf16.  Pointers may be NULL to skip. */
+ * out[m*ldo+n] as fp32, or bf16 when out_bf16.  out_pre is bf16 when pre_bf16,
+ * gelu_x bf16 when gelu_x_bf16 (else fp32).  Pointers may be NULL to skip. */
 typedef struct {
     int M, N, K;
     const void* A; int lda; int a_kmajor;
     const void* B; int ldb; int b_kmajor;
     int bf16;
     void* out; int ldo; int out_bf16;
-    float* out_pre;
+    void* out_pre;
     const float* bias;
     const float* residual;
-    const float* gelu_x; int ldg;
+    const void* gelu_x; int ldg;
     int gelu;
+    int pre_bf16;
+    int gelu_x_bf16;
 } gpt2_gemm_args;
 int gpt2_op_gemm(const gpt2_gemm_args* args, int mode, int* status, void* stream);
 

@@ -80,6 +80,8 @@ def _gemm(B_, M, N, K, A, lda, ak, Bm, ldb, bk, out, ldo, out_bf16, **epi):
         setattr(a, k, t.data_ptr() if t is not None else None)
     a.ldg = epi.get("ldg", 0)
     a.gelu = epi.get("gelu", 0)
+    a.pre_bf16 = epi.get("pre_bf16", 0)
+    a.gelu_x_bf16 = epi.get("gelu_x_bf16", 0)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = B_.lib().gpt2_op_gemm(ctypes.addressof(a), B_.GPT2_MODE_BF16, B_.ptr(st), None)
     torch.cuda.synchronize()
@@ -133,6 +135,17 @@ def test_bf16_gemm_three_products(B_, o64, M, N, K):
     h = rng.normal(size=(M, N))
     _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, gelu_x=f32(h), ldg=N)
     assert rel_l2(host(o16), o64.gelu_backward(h, want)) < BF16_OUT
+    # the step's bf16 forms: pre-activation stored as bf16, GELU input read as bf16,
+    # and a plain bias epilogue into bf16
+    pre16 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, bias=f32(bias), out_pre=pre16, gelu=1,
+          pre_bf16=1)
+    assert rel_l2(host(pre16), want + bias) < BF16_OUT
+    assert rel_l2(host(o16), o64.gelu_forward(want + bias)) < BF16_OUT
+    _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, gelu_x=bf(h), ldg=N, gelu_x_bf16=1)
+    assert rel_l2(host(o16), o64.gelu_backward(rounded(h), want)) < BF16_OUT
+    _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, bias=f32(bias))
+    assert rel_l2(host(o16), want + bias) < BF16_OUT
 
 
 @pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600)])
@@ -155,9 +168,9 @@ def test_bf16_layernorm(B_, o64, N, C):
     dw, db = torch.empty(C, device="cuda"), torch.empty(C, device="cuda")
     nb = L.gpt2_op_layernorm_backward_scratch_bytes(N, C)
     sc = torch.empty(nb, dtype=torch.uint8, device="cuda")
-    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), B_.ptr(dx16), B_.ptr(dw), B_.ptr(db), B_.ptr(f32(dy)),
-                                        B_.ptr(f32(x)), B_.ptr(f32(w)), B_.ptr(mean), B_.ptr(rstd), N, C,
-                                        B_.ptr(sc), nb, None) == 0
+    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), B_.ptr(dx16), B_.ptr(dw), B_.ptr(db), None,
+                                        B_.ptr(f32(dy)), B_.ptr(f32(x)), B_.ptr(f32(w)), B_.ptr(mean),
+                                        B_.ptr(rstd), N, C, 1, B_.ptr(sc), nb, None, None) == 0
     torch.cuda.synchronize()
     assert torch.equal(dx16.cpu().view(torch.int16), dx.cpu().to(torch.bfloat16).view(torch.int16))
 

@@ -139,8 +139,9 @@ def test_layernorm_forward(L, B_, o64, N, C):
     assert rel_l2(host(rstd), wr) < 1e-6
 
 
-@pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600)])
-def test_layernorm_backward(L, B_, o64, N, C):
+@pytest.mark.parametrize("accumulate", [1, 0])
+@pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600), (16384, 768), (3, 2048)])
+def test_layernorm_backward(L, B_, o64, N, C, accumulate):
     rng = np.random.default_rng(3)
     x = rng.normal(size=(N, C)).astype(np.float32)
     w = rng.normal(size=C).astype(np.float32)
@@ -149,18 +150,24 @@ def test_layernorm_backward(L, B_, o64, N, C):
     dx0 = rng.normal(size=(N, C)).astype(np.float32)    # residual gradient accumulated into
     _, wm, wr = o64.layernorm_forward(x, w, b)
     mean, rstd = dev(wm.astype(np.float32)), dev(wr.astype(np.float32))
-    dx = dev(dx0.copy())
+    dx = dev(dx0.copy() if accumulate else np.full((N, C), np.nan, np.float32))
     dw = torch.empty(C, device="cuda")
     db = torch.empty(C, device="cuda")
+    ds = torch.empty(C, device="cuda")
+    st = dev(np.zeros(1, np.int32))
     nbytes = L.gpt2_op_layernorm_backward_scratch_bytes(N, C)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), None, B_.ptr(dw), B_.ptr(db), B_.ptr(dev(dy)),
+    assert L.gpt2_op_layernorm_backward(B_.ptr(dx), None, B_.ptr(dw), B_.ptr(db), B_.ptr(ds), B_.ptr(dev(dy)),
                                         B_.ptr(dev(x)), B_.ptr(dev(w)), B_.ptr(mean), B_.ptr(rstd),
-                                        N, C, B_.ptr(scratch), nbytes, None) == 0
+                                        N, C, accumulate, B_.ptr(scratch), nbytes, B_.ptr(st), None) == 0
     wdx, wdw, wdb = o64.layernorm_backward(dy, x, w, wm.astype(np.float32), wr.astype(np.float32))
-    assert rel_l2(host(dx), dx0 + wdx) < 1e-6
+    want = dx0 + wdx if accumulate else wdx
+    assert int(host(st)[0]) == 0
+    assert rel_l2(host(dx), want) < 1e-6
     assert rel_l2(host(dw), wdw) < 1e-6
     assert rel_l2(host(db), wdb) < 1e-6
+    # the column sum of the resulting gradient (a bias gradient), summed in float64 here
+    assert rel_l2(host(ds), want.astype(np.float64).sum(axis=0)) < 1e-5
 
 
 # ------------------------------------------------------------------ linear

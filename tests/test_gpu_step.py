@@ -85,10 +85,11 @@ def test_step_matches_oracle(name, mode, init):
     assert np.abs(qb_g[:, C:2 * C] - kb0).max() <= cfg.lr * steps * 1.0001 + cfg.wd * cfg.lr * steps
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
 def test_logits_match_oracle(mode, o64):
     from gpt_decoder_step_train_b300.binding import GPT2
-    cfg = RAGGED
+    # bf16 attention takes head sizes 16, 32 and 64
+    cfg = RAGGED.with_(H=3) if mode == "bf16" else RAGGED
     params = syn.init_params(cfg)
     tok, tgt = syn.draw_tokens(cfg)
     m = o64.model(cfg.dims(), cfg.B, cfg.T)
@@ -102,7 +103,7 @@ def test_logits_match_oracle(mode, o64):
     assert np.all(z[:, cfg.V:] == 0)
     # intermediate activations of the first block
     for which, name in [(1, "ln1"), (2, "qkv"), (3, "atty"), (4, "res2"), (6, "h"), (7, "g")]:
-        a = model.activation(which, 0, cfg.B * cfg.T).cpu().numpy()
+        a = model.activation(which, 0, cfg.B * cfg.T).float().cpu().numpy()
         assert rel_l2(a, m.act(name, 0)) <= TOL[mode]["rel"], name
     model.close()
 
