@@ -546,11 +546,12 @@ def _attn_case(kind, mode, B=16, T=1024, C=768, H=12):
     from gpt_decoder_step_train_b300 import binding as B_
     L = B_.lib()
     m = B_.MODES[mode]
+    dt = torch.bfloat16 if mode == "bf16" else torch.float32
     g = torch.Generator(device="cuda").manual_seed(0)
-    qkv = torch.randn(B, T, 3 * C, device="cuda", generator=g)
-    y = torch.empty(B, T, C, device="cuda")
+    qkv = torch.randn(B, T, 3 * C, device="cuda", generator=g).to(dt)
+    y = torch.empty(B, T, C, device="cuda", dtype=dt)
     lse = torch.empty(B, H, T, device="cuda")
-    dy = torch.randn(B, T, C, device="cuda", generator=g)
+    dy = torch.randn(B, T, C, device="cuda", generator=g).to(dt)
     dqkv = torch.empty_like(qkv)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     nbytes = L.gpt2_op_attention_backward_scratch_bytes(B, T, H)
@@ -568,7 +569,7 @@ def _attn_case(kind, mode, B=16, T=1024, C=768, H=12):
                                                   B_.ptr(lse), B, T, C, H, B_.ptr(sc), nbytes, m,
                                                   B_.ptr(st), None)
         flops = 8.0 * hs * causal_pairs
-    return fn, flops, 4.0 * (qkv.numel() + 2 * y.numel()), keep
+    return fn, flops, qkv.element_size() * (qkv.numel() + 2 * y.numel()), keep
 
 
 OPS["attn_fwd"] = lambda mode: _attn_case("fwd", mode)

@@ -315,6 +315,9 @@ int attention_tc_backward(float* dqkv, const float* dy, const float* qkv, const 
                           const float* D, int B, int T, int C, int H, int* status,
                           cudaStream_t st);
 bool attention_tc_supported(int hs);
+bool attention_tc05_supported(int hs, int C);
+int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
+                           cudaStream_t st);
 
 }  // namespace gpt2k
 
@@ -333,6 +336,7 @@ GPT2_API int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int
     int hs = C / H;
     cudaStream_t st = as_stream(stream);
     if (mode == GPT2_MODE_BF16) {
+        if (attention_tc05_supported(hs, C)) return attention_tc05_forward(y, lse, qkv, B, T, C, H, status, st);
         if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
         return attention_bf16_forward(y, lse, qkv, B, T, C, H, st);
     }

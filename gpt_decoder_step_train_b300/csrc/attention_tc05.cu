@@ -1,0 +1,339 @@
+// attention_tc05.cu -- causal self-attention forward on the 5th-generation
+// tensor cores (tcgen05), bf16 operands, head size 64.
+//
+// Per (batch b, head h): S = Q K^T / sqrt(hs), S[i,j] = -inf for j > i,
+// P = softmax_rows(S), O = P V, and the row log-sum-exp of the scaled scores
+// is kept for the backward ("GPT-2 from scratch with torch", section
+// 自注意力; the 1/sqrt(d_k) scaling: "从头搭建GPT(Andrej Karpathy) 笔记",
+// section attention中为什么要做scaling).
+//
+// One CTA per (query tile of 128 rows, head, batch), 192 threads, two CTAs per SM:
+//   warp 0   TMA producer: the Q tile once, then K and V tiles of 64 keys
+//            into a four-stage ring (128-byte swizzle);
+//   warp 1   allocates tensor memory (S: 64 columns, O: 64 columns) and from
+//            one lane issues S = Q K^T (M=128, N=64, K=64) and O += P V
+//            (M=128, N=64, K=64; P from shared memory, V read MN-major);
+//   warps 2-5  softmax, one query row per thread (its TMEM lane): scores
+//            from tensor memory, causal mask on the diagonal tiles, online
+//            maximum and sum in the log2 domain, P written to shared memory as
+//            bf16 in the operand layout.  The running maximum used for P is
+//            only moved when a row's true maximum exceeds it by more than
+//            2^8; O in tensor memory is then rescaled before the next P V.
+//            At the end O / l goes out as bf16 and the log-sum-exp as fp32.
+// Key tiles past the query tile's last row are never visited (causal tile
+// skipping).  While the softmax warps work on S_j, the tensor cores compute
+// S_{j+1} (the scores are in registers by then) and P_{j-1} V_{j-1}.
+// Every wait is bounded (about one second); a wait that gives up raises
+// GPT2_STATUS_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
+// and tensor memory is freed.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace gpt2k {
+namespace at05 {
+
+using namespace ptx;
+
+constexpr int HS = 64;              // head size (one 128-byte swizzle row of bf16)
+constexpr int BQ = 128;             // queries per CTA (TMEM lanes)
+constexpr int BKV = 64;             // keys per tile
+constexpr int KV_STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 128;      // S: [0, 64), O: [64, 128)
+constexpr uint32_t TILE_BYTES = BKV * HS * 2;     // one K or V tile: 8 KB
+constexpr uint32_t Q_BYTES = BQ * HS * 2;         // 16 KB
+constexpr uint32_t P_BYTES = BQ * BKV * 2;        // 16 KB
+// shared memory: Q | K[2] | V[2] | P, each 1024-byte aligned
+constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + Q_BYTES, OFF_V = OFF_K + KV_STAGES * TILE_BYTES,
+                   OFF_P = OFF_V + KV_STAGES * TILE_BYTES, SMEM_USED = OFF_P + P_BYTES;
+constexpr size_t SMEM = SMEM_USED + 1024;          // + alignment slack
+constexpr float RESCALE_LOG2 = 8.f;                // move the running maximum past 2^8 growth
+constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+
+// 128-byte swizzle of a K-major bf16 operand row: 16-byte chunk c of row r
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// 2^x on the special-function unit (inputs far below -126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(THREADS, 2)
+attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
+              int T, int C, int H, float scale_log2, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full, s_free, p_full,
+        pv_done, drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = (T + BQ - 1) / BQ;
+    const int qt = nq - 1 - (int)blockIdx.x;          // longest rows first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * BQ;
+    const int nkv = (min(q0 + BQ, T) + BKV - 1) / BKV;  // key tiles that hold keys <= the last row
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(smem_u32(&q_full), 1);
+        for (int s = 0; s < KV_STAGES; s++) {
+            mbar_init(smem_u32(&kv_full[s]), 1);
+            mbar_init(smem_u32(&kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&s_full), 1);
+        mbar_init(smem_u32(&s_free), 4);
+        mbar_init(smem_u32(&p_full), 4);
+        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&drain), 1);
+        fence_mbar_init();
+        prefetch_map(&tm);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int last_j[KV_STAGES];                     // last tile issued into each stage (abort drain)
+            for (int s = 0; s < KV_STAGES; s++) last_j[s] = -1;
+            bool ok = true;
+            mbar_expect_tx(smem_u32(&q_full), Q_BYTES);
+            tma_load_3d(base + OFF_Q, &tm, h * HS, q0, b, smem_u32(&q_full));
+            tma_load_3d(base + OFF_Q + Q_BYTES / 2, &tm, h * HS, q0 + 64, b, smem_u32(&q_full));
+            for (int j = 0; j < nkv && ok; j++) {
+                const int s = j % KV_STAGES;
+                const uint32_t ph = (uint32_t)(j / KV_STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&kv_empty[s]), ph ^ 1u, &s_abort, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&kv_full[s]);
+                mbar_expect_tx(fb, 2 * TILE_BYTES);
+                last_j[s] = j;
+                tma_load_3d(base + OFF_K + s * TILE_BYTES, &tm, C + h * HS, j * BKV, b, fb);
+                tma_load_3d(base + OFF_V + s * TILE_BYTES, &tm, 2 * C + h * HS, j * BKV, b, fb);
+            }
+            if (!ok) {
+                // wait (bounded, ignoring the abort flag) for every copy this thread issued
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(&q_full), 0) && globaltimer() - t0 < WAIT_NS) {
+                }
+                // earlier copies into a stage completed before it was refilled, so
+                // only each stage's last issue can still be in flight
+                for (int s = 0; s < KV_STAGES; s++) {
+                    if (last_j[s] < 0) continue;
+                    const uint32_t ph = (uint32_t)(last_j[s] / KV_STAGES) & 1u;
+                    const uint64_t t1 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(&kv_full[s]), ph) && globaltimer() - t1 < WAIT_NS) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = instr_desc(BQ, BKV, false, false, true);   // Q K^T: both K-major
+            const uint32_t id_pv = instr_desc(BQ, HS, false, true, true);    // P V: V MN-major
+            const uint32_t t_s = tmem, t_o = tmem + BKV;
+            bool ok = mbar_wait(smem_u32(&q_full), 0, &s_abort, status);
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % KV_STAGES;
+                if (!mbar_wait(smem_u32(&kv_full[s]), (uint32_t)(j / KV_STAGES) & 1u, &s_abort, status))
+                    return false;
+                if (j > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(j - 1) & 1u, &s_abort, status))
+                    return false;
+                tc_fence_after();
+                const uint32_t kb = base + OFF_K + s * TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < HS / 16; k++)
+                    mma_issue<true>(t_s, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&s_full));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; j < nkv && ok; j++) {
+                if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
+                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)j & 1u, &s_abort, status))) break;
+                tc_fence_after();
+                const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BKV / 16; k++)
+                    mma_issue<true>(t_o, smem_desc(base + OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(vb + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_pv,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&pv_done));
+                mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
+            }
+            // every MMA issued has completed once this commit lands
+            mma_commit(smem_u32(&drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&drain), 0) && globaltimer() - t0 < WAIT_NS) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ softmax (warps 2..5)
+        const int quarter = warp & 3;                  // TMEM lanes this warp may access
+        const int r = quarter * 32 + lane;             // row within the tile
+        const int row = q0 + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_base, t_o = tmem + lane_base + BKV;
+        uint8_t* const prow = base_ptr + OFF_P;
+        float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, sum of P
+        bool ok = true;
+        for (int j = 0; j < nkv; j++) {
+            if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
+            tc_fence_after();
+            float s[64];
+            {
+                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
+                float (&c)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
+                tmem_ld32(t_s, a);
+                tmem_ld32(t_s + 32, c);
+                tmem_wait_ld(a);
+                tmem_wait_ld(c);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s_free));
+            // mask (tiles that reach the diagonal or the sequence end), row maximum
+            // of the raw scores; the scale goes into the exponent's FMA
+            const int k0 = j * BKV;
+            if (k0 + BKV - 1 > q0 || k0 + BKV > T) {
+#pragma unroll
+                for (int c = 0; c < 64; c++)
+                    if (k0 + c > row || k0 + c >= T) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 64; c++) mx = fmaxf(mx, s[c]);
+            mx *= scale_log2;                          // log2-domain maximum of this tile
+            float alpha = 1.f;                         // factor on O and l for this tile
+            if (mx > m_run + RESCALE_LOG2 || (m_run == -INFINITY && mx > -INFINITY)) {
+                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+                m_run = mx;
+            }
+            float ps = 0.f;
+            const float mref = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+            for (int c = 0; c < 64; c++) {
+                s[c] = ex2(fmaf(s[c], scale_log2, -mref));
+                ps += s[c];
+            }
+            l_run = l_run * alpha + ps;
+            // O and the P buffer are free once P_{j-1} V_{j-1} has completed
+            if (j > 0) {
+                if (!mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, &s_abort, status)) { ok = false; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {
+                        float o[32];
+                        tmem_ld32(t_o + half * 32, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int c = 0; c < 32; c++) o[c] *= alpha;
+                        tmem_st32(t_o + half * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P row (bf16) into the K-major operand tile
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                const uint4 v = make_uint4(pack_bf16(s[8 * c], s[8 * c + 1]), pack_bf16(s[8 * c + 2], s[8 * c + 3]),
+                                           pack_bf16(s[8 * c + 4], s[8 * c + 5]),
+                                           pack_bf16(s[8 * c + 6], s[8 * c + 7]));
+                *reinterpret_cast<uint4*>(prow + sw128(r, c)) = v;
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_full));
+        }
+        if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(nkv - 1) & 1u, &s_abort, status)) {
+            tc_fence_after();
+            float o[64];
+            {
+                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
+                float (&c)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
+                tmem_ld32(t_o, a);
+                tmem_ld32(t_o + 32, c);
+                tmem_wait_ld(a);
+                tmem_wait_ld(c);
+            }
+            if (row < T) {
+                const float inv = 1.f / l_run;
+                uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)b * T + row) * C + h * HS);
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    yr[c] = make_uint4(pack_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                       pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                       pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                       pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                lse[((size_t)b * H + h) * T + row] = (m_run + log2f(l_run)) * LN2;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace at05
+
+bool attention_tc05_supported(int hs, int C) { return hs == at05::HS && C % 8 == 0; }
+
+// y [B,T,C] and lse [B,H,T] from qkv [B,T,3C] (bf16), head size 64.
+int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
+                           cudaStream_t st) {
+    using namespace at05;
+    if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(attn_fwd_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return GPT2_ECUDA;
+        }
+        attr = true;
+    }
+    // qkv as a 3-D tensor [B][T][3C]: boxes of 64 rows x 64 columns (one head)
+    CUtensorMap tm;
+    const cuuint64_t dims[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)T * 3 * C * 2};
+    const cuuint32_t box[3] = {HS, 64, 1};
+    if (!encode_tensor_map(&tm, true, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GPT2_ENOTSUP;
+    const float scale_log2 = LOG2E / sqrtf((float)HS);
+    count_launch(), attn_fwd_tc05<<<dim3((T + BQ - 1) / BQ, H, B), THREADS, SMEM, st>>>(
+        tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+}  // namespace gpt2k

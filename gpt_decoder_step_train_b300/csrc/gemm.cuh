@@ -9,6 +9,7 @@
 //   dX       dinp = dout . W    A = dout (K-major), B = W (N-major)
 //   dW       dW   = dout^T . inp  A = dout (M-major), B = inp (N-major)
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -56,6 +57,11 @@ __device__ __forceinline__ void epilogue_store(const GemmEpilogue& e, int m, int
     if (e.out_bf16) reinterpret_cast<__nv_bfloat16*>(e.out)[o] = __float2bfloat16_rn(v);
     else reinterpret_cast<float*>(e.out)[o] = v;
 }
+
+// Tiled TMA descriptor over a row-major tensor of `rank` dimensions (dims and
+// box innermost first, strides in bytes for dimensions 1..rank-1), zero fill.
+bool encode_tensor_map(CUtensorMap* map, bool bf16, int rank, const void* ptr, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz);
 
 // CUDA-core fp32 GEMM (strict mode).
 int gemm_simt(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st);

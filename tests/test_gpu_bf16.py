@@ -212,6 +212,40 @@ def test_bf16_bias_grad(B_):
     assert rel_l2(host(db), rounded(d).sum(0)) < 1e-6
 
 
+def _lse_f64(qkv, H):
+    """Row log-sum-exp of the causal scaled scores, [B, H, T], in float64."""
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    hs = C // H
+    q = qkv[..., :C].reshape(B, T, H, hs).transpose(0, 2, 1, 3)
+    k = qkv[..., C:2 * C].reshape(B, T, H, hs).transpose(0, 2, 1, 3)
+    s = q @ k.transpose(0, 1, 3, 2) / np.sqrt(hs)
+    s = np.where(np.tril(np.ones((T, T), bool)), s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    return (m + np.log(np.exp(s - m).sum(axis=-1, keepdims=True)))[..., 0]
+
+
+@pytest.mark.parametrize("B,T,C,H,ramp", [(1, 300, 768, 12, 0.0), (2, 200, 128, 2, 6.0), (1, 1024, 768, 12, 3.0),
+                                          (1, 64, 64, 1, 0.0), (3, 65, 192, 3, 6.0)])
+def test_bf16_attention_forward_lse(B_, o64, B, T, C, H, ramp):
+    """Forward output and log-sum-exp; `ramp` grows the key scale along the
+    sequence so the row maxima keep rising across key tiles."""
+    L = B_.lib()
+    rng = np.random.default_rng(6)
+    qkv = rng.normal(size=(B, T, 3 * C))
+    qkv[..., C:2 * C] *= (1.0 + ramp * np.arange(T) / T)[None, :, None]
+    qr = rounded(qkv)
+    y16 = torch.empty(B, T, C, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, T, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert L.gpt2_op_attention_forward(B_.ptr(y16), B_.ptr(lse), B_.ptr(bf(qkv)), B, T, C, H, B_.GPT2_MODE_BF16,
+                                       B_.ptr(st), None) == 0
+    wy, _ = o64.attention_forward(qr, H)
+    assert rel_l2(host(y16), wy) < 1e-2
+    assert np.abs(host(lse) - _lse_f64(qr, H)).max() < 1e-3 * max(1.0, np.abs(_lse_f64(qr, H)).max())
+    assert int(st.item()) == 0
+
+
 @pytest.mark.parametrize("B,T,C,H", [(2, 37, 64, 4), (1, 300, 768, 12), (2, 129, 192, 3), (1, 1, 64, 4)])
 def test_bf16_attention(B_, o64, B, T, C, H):
     L = B_.lib()
