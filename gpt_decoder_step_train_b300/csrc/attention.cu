@@ -318,6 +318,8 @@ bool attention_tc_supported(int hs);
 bool attention_tc05_supported(int hs, int C);
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
                            cudaStream_t st);
+int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
+                            int B, int T, int C, int H, int* status, cudaStream_t st);
 
 }  // namespace gpt2k
 
@@ -371,6 +373,8 @@ GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* 
         if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
         launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
         GPT2_LAUNCH_CHECK();
+        if (attention_tc05_supported(hs, C))
+            return attention_tc05_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st);
         return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
     }
     float* dq = static_cast<float*>(dqkv);

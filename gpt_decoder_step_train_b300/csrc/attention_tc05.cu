@@ -304,6 +304,503 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
     }
 }
 
+
+// ---------------------------------------------------------------- backward
+// With c = 1/sqrt(hs), lse the forward's row log-sum-exp and D_i = dO_i . O_i:
+//   P = exp(c Q K^T - lse),  dP = dO V^T,  dS = P o (dP - D),
+//   dQ = c dS K,  dK = c dS^T Q,  dV = P^T dO.
+// Two kernels, each output row owned by one CTA (no atomics, deterministic):
+//   attn_bwd_dkv_tc05  one CTA per 128-key tile; TMEM lanes are keys.  Per
+//       64-query tile (from the diagonal on): S^T = K Q^T and dP^T = V dO^T,
+//       then P^T and dS^T as bf16 operand tiles, then dV += P^T dO and
+//       dK += dS^T Q.  The Q and dO tiles serve as K-major operands of the
+//       first two products and as MN-major operands of the last two.
+//   attn_bwd_dq_tc05   one CTA per 128-query tile; TMEM lanes are queries.  Per
+//       64-key tile: S = Q K^T and dP = dO V^T, then dS, then dQ += dS K.
+// Both follow the forward's roles: a TMA warp, one MMA-issuing thread, four
+// warps on the element-wise work (one row per thread).
+
+constexpr uint32_t BOX_BYTES = 64 * HS * 2;        // one 64-row tile of a head: 8 KB
+
+// dK, dV for 128 keys.  Shared memory: K | V (16 KB each) | two stages of
+// Q, dO (8 KB each) and the tile's lse and D | P^T, dS^T (16 KB each).  TMEM:
+// S^T | dP^T | dV | dK.  The producer warp writes each query tile's lse and D
+// into the stage before it arms the stage's barrier, so the element-wise
+// warps need no barrier of their own.
+constexpr int DKV_STAGES = 2;
+// a stage: Q box | dO box | lse*log2(e) [64] | D [64], padded to 1 KB
+constexpr uint32_t DKV_OFF_K = 0, DKV_OFF_V = 16384, DKV_OFF_ST = 32768, DKV_ROWS = 2 * BOX_BYTES,
+                   DKV_STAGE = 2 * BOX_BYTES + 1024, DKV_OFF_P = DKV_OFF_ST + DKV_STAGES * DKV_STAGE,
+                   DKV_OFF_DS = DKV_OFF_P + 16384, DKV_SMEM_USED = DKV_OFF_DS + 16384;
+constexpr size_t DKV_SMEM = DKV_SMEM_USED + 1024;
+
+__global__ void __launch_bounds__(THREADS, 2)
+attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                  __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
+                  int T, int C, int H, float scale, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t k_full, q_full[DKV_STAGES], q_empty[DKV_STAGES], s_full, s_free, p_full,
+        pv_done, drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int k0 = kt * 128;
+    const int i0 = k0 / 64, nq = (T + 63) / 64;   // query tiles i0 .. nq-1 see these keys
+    const int ntile = nq - i0;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(smem_u32(&k_full), 1);
+        for (int s = 0; s < DKV_STAGES; s++) {
+            mbar_init(smem_u32(&q_full[s]), 1);
+            mbar_init(smem_u32(&q_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&s_full), 1);
+        mbar_init(smem_u32(&s_free), 4);
+        mbar_init(smem_u32(&p_full), 4);
+        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&drain), 1);
+        fence_mbar_init();
+        prefetch_map(&tq);
+        prefetch_map(&tdo);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer (whole warp; lane 0 issues)
+        int last_i[DKV_STAGES];
+        for (int s = 0; s < DKV_STAGES; s++) last_i[s] = -1;
+        bool ok = true;
+        const float* lse_bh = lse + ((size_t)b * H + h) * T;
+        const float* D_bh = Dg + ((size_t)b * H + h) * T;
+        if (lane == 0) {
+            mbar_expect_tx(smem_u32(&k_full), 4 * BOX_BYTES);
+            for (int half = 0; half < 2; half++) {
+                tma_load_3d(base + DKV_OFF_K + half * BOX_BYTES, &tq, C + h * HS, k0 + 64 * half, b, smem_u32(&k_full));
+                tma_load_3d(base + DKV_OFF_V + half * BOX_BYTES, &tq, 2 * C + h * HS, k0 + 64 * half, b,
+                            smem_u32(&k_full));
+            }
+        }
+        for (int t = 0; t < ntile && ok; t++) {
+            const int s = t % DKV_STAGES;
+            if (lane == 0)
+                ok = mbar_wait(smem_u32(&q_empty[s]), ((uint32_t)(t / DKV_STAGES) & 1u) ^ 1u, &s_abort, status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            // the tile's lse (as lse*log2 e; +inf past T, which zeroes P) and D
+            float* rows = reinterpret_cast<float*>(base_ptr + DKV_OFF_ST + s * DKV_STAGE + DKV_ROWS);
+            for (int e = lane; e < 64; e += 32) {
+                const int q = (i0 + t) * 64 + e;
+                rows[e] = q < T ? lse_bh[q] * LOG2E : INFINITY;
+                rows[64 + e] = q < T ? D_bh[q] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t fb = smem_u32(&q_full[s]);
+                mbar_expect_tx(fb, 2 * BOX_BYTES);     // the arrive releases the writes above
+                last_i[s] = t;
+                const uint32_t st = base + DKV_OFF_ST + s * DKV_STAGE;
+                tma_load_3d(st, &tq, h * HS, (i0 + t) * 64, b, fb);
+                tma_load_3d(st + BOX_BYTES, &tdo, h * HS, (i0 + t) * 64, b, fb);
+            }
+        }
+        if (lane == 0) {
+            if (!ok) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(&k_full), 0) && globaltimer() - t0 < WAIT_NS) {
+                }
+                for (int s = 0; s < DKV_STAGES; s++) {
+                    if (last_i[s] < 0) continue;
+                    const uint32_t ph = (uint32_t)(last_i[s] / DKV_STAGES) & 1u;
+                    const uint64_t t1 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(&q_full[s]), ph) && globaltimer() - t1 < WAIT_NS) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = instr_desc(128, 64, false, false, true);   // K Q^T, V dO^T
+            const uint32_t id_o = instr_desc(128, HS, false, true, true);    // P^T dO, dS^T Q (MN-major B)
+            const uint32_t t_st = tmem, t_dp = tmem + 64, t_dv = tmem + 128, t_dk = tmem + 192;
+            bool ok = mbar_wait(smem_u32(&k_full), 0, &s_abort, status);
+            auto issue_s = [&](int t) -> bool {
+                const int s = t % DKV_STAGES;
+                if (!mbar_wait(smem_u32(&q_full[s]), (uint32_t)(t / DKV_STAGES) & 1u, &s_abort, status)) return false;
+                if (t > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(t - 1) & 1u, &s_abort, status)) return false;
+                tc_fence_after();
+                const uint32_t st = base + DKV_OFF_ST + s * DKV_STAGE;
+#pragma unroll
+                for (int k = 0; k < HS / 16; k++) {
+                    mma_issue<true>(t_st, smem_desc(base + DKV_OFF_K + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                    mma_issue<true>(t_dp, smem_desc(base + DKV_OFF_V + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
+                                    k > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&s_full));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int t = 0; t < ntile && ok; t++) {
+                if (t + 1 < ntile && !(ok = issue_s(t + 1))) break;
+                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)t & 1u, &s_abort, status))) break;
+                tc_fence_after();
+                const uint32_t st = base + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE;
+#pragma unroll
+                for (int k = 0; k < 64 / 16; k++) {
+                    // dV += P^T dO, dK += dS^T Q: B(n = head dim, k = query) read MN-major
+                    mma_issue<true>(t_dv, smem_desc(base + DKV_OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + BOX_BYTES + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                    (t > 0 || k > 0) ? 1u : 0u);
+                    mma_issue<true>(t_dk, smem_desc(base + DKV_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                    (t > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&pv_done));
+                mma_commit(smem_u32(&q_empty[t % DKV_STAGES]));
+            }
+            mma_commit(smem_u32(&drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&drain), 0) && globaltimer() - t0 < WAIT_NS) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ element-wise (warps 2..5), thread = key
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int key = k0 + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_st = tmem + lane_base, t_dp = t_st + 64, t_dv = t_st + 128, t_dk = t_st + 192;
+        const float c2 = scale * LOG2E;
+        uint8_t* const prow = base_ptr + DKV_OFF_P;
+        uint8_t* const dsrow = base_ptr + DKV_OFF_DS;
+        bool ok = true;
+        for (int t = 0; t < ntile; t++) {
+            // S^T and dP^T ready implies the stage (with lse and D) is full
+            if (!mbar_wait(smem_u32(&s_full), (uint32_t)t & 1u, &s_abort, status)) { ok = false; break; }
+            tc_fence_after();
+            float sv[64], dp[64];
+            {
+                float (&a0)[32] = *reinterpret_cast<float(*)[32]>(&sv[0]);
+                float (&a1)[32] = *reinterpret_cast<float(*)[32]>(&sv[32]);
+                float (&b0)[32] = *reinterpret_cast<float(*)[32]>(&dp[0]);
+                float (&b1)[32] = *reinterpret_cast<float(*)[32]>(&dp[32]);
+                tmem_ld32(t_st, a0);
+                tmem_ld32(t_st + 32, a1);
+                tmem_ld32(t_dp, b0);
+                tmem_ld32(t_dp + 32, b1);
+                tmem_wait_ld(a0);
+                tmem_wait_ld(a1);
+                tmem_wait_ld(b0);
+                tmem_wait_ld(b1);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s_free));
+            const int q0 = (i0 + t) * 64;
+            // acquire the producer's lse and D writes from the stage barrier itself
+            // (its phase for this tile completed before S^T was computed)
+            if (!mbar_wait(smem_u32(&q_full[t % DKV_STAGES]), (uint32_t)(t / DKV_STAGES) & 1u, &s_abort, status)) {
+                ok = false;
+                break;
+            }
+            const float* rows =
+                reinterpret_cast<const float*>(base_ptr + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE + DKV_ROWS);
+            const float4* l4 = reinterpret_cast<const float4*>(rows);
+            const float4* d4 = reinterpret_cast<const float4*>(rows + 64);
+            const bool diag = q0 < k0 + 127;           // some query of the tile precedes some key
+#pragma unroll
+            for (int c4 = 0; c4 < 16; c4++) {
+                const float4 lv = l4[c4], dv = d4[c4];
+                const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int c = 4 * c4 + e;
+                    float pv = ex2(fmaf(sv[c], c2, -lq[e]));
+                    if (diag && q0 + c < key) pv = 0.f;
+                    sv[c] = pv;
+                    dp[c] = pv * (dp[c] - dq[e]);
+                }
+            }
+            // P^T and dS^T buffers are free once the previous tile's products completed
+            if (t > 0) {
+                if (!mbar_wait(smem_u32(&pv_done), (uint32_t)(t - 1) & 1u, &s_abort, status)) { ok = false; break; }
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                *reinterpret_cast<uint4*>(prow + sw128(r, c)) =
+                    make_uint4(pack_bf16(sv[8 * c], sv[8 * c + 1]), pack_bf16(sv[8 * c + 2], sv[8 * c + 3]),
+                               pack_bf16(sv[8 * c + 4], sv[8 * c + 5]), pack_bf16(sv[8 * c + 6], sv[8 * c + 7]));
+                *reinterpret_cast<uint4*>(dsrow + sw128(r, c)) =
+                    make_uint4(pack_bf16(dp[8 * c], dp[8 * c + 1]), pack_bf16(dp[8 * c + 2], dp[8 * c + 3]),
+                               pack_bf16(dp[8 * c + 4], dp[8 * c + 5]), pack_bf16(dp[8 * c + 6], dp[8 * c + 7]));
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_full));
+        }
+        if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(ntile - 1) & 1u, &s_abort, status)) {
+            tc_fence_after();
+            for (int which = 0; which < 2; which++) {  // 0: dK (scaled by c), 1: dV
+                float o[64];
+                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
+                float (&c2v)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
+                const uint32_t src = which == 0 ? t_dk : t_dv;
+                tmem_ld32(src, a);
+                tmem_ld32(src + 32, c2v);
+                tmem_wait_ld(a);
+                tmem_wait_ld(c2v);
+                const float f = which == 0 ? scale : 1.f;
+                if (key < T) {
+                    uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + key) * 3 * C + (1 + which) * C + h * HS);
+#pragma unroll
+                    for (int c = 0; c < 8; c++)
+                        dst[c] = make_uint4(pack_bf16(o[8 * c] * f, o[8 * c + 1] * f),
+                                            pack_bf16(o[8 * c + 2] * f, o[8 * c + 3] * f),
+                                            pack_bf16(o[8 * c + 4] * f, o[8 * c + 5] * f),
+                                            pack_bf16(o[8 * c + 6] * f, o[8 * c + 7] * f));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// dQ for 128 queries.  Shared memory: Q | dO (16 KB each) | three stages of
+// K, V (8 KB each) | dS (16 KB).  TMEM: S | dP | dQ.
+constexpr int DQ_STAGES = 3;
+constexpr uint32_t DQ_OFF_Q = 0, DQ_OFF_DO = 16384, DQ_OFF_ST = 32768, DQ_STAGE = 2 * BOX_BYTES,
+                   DQ_OFF_DS = DQ_OFF_ST + DQ_STAGES * DQ_STAGE, DQ_SMEM_USED = DQ_OFF_DS + 16384;
+constexpr size_t DQ_SMEM = DQ_SMEM_USED + 1024;
+
+__global__ void __launch_bounds__(THREADS, 2)
+attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                 __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
+                 int T, int C, int H, float scale, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t q_full, kv_full[DQ_STAGES], kv_empty[DQ_STAGES], s_full, s_free, p_full,
+        pv_done, drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nqt = (T + BQ - 1) / BQ;
+    const int qt = nqt - 1 - (int)blockIdx.x;         // longest rows first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * BQ;
+    const int nkv = (min(q0 + BQ, T) + 63) / 64;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(smem_u32(&q_full), 1);
+        for (int s = 0; s < DQ_STAGES; s++) {
+            mbar_init(smem_u32(&kv_full[s]), 1);
+            mbar_init(smem_u32(&kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&s_full), 1);
+        mbar_init(smem_u32(&s_free), 4);
+        mbar_init(smem_u32(&p_full), 4);
+        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&drain), 1);
+        fence_mbar_init();
+        prefetch_map(&tq);
+        prefetch_map(&tdo);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int last_j[DQ_STAGES];
+            for (int s = 0; s < DQ_STAGES; s++) last_j[s] = -1;
+            bool ok = true;
+            mbar_expect_tx(smem_u32(&q_full), 4 * BOX_BYTES);
+            for (int half = 0; half < 2; half++) {
+                tma_load_3d(base + DQ_OFF_Q + half * BOX_BYTES, &tq, h * HS, q0 + 64 * half, b, smem_u32(&q_full));
+                tma_load_3d(base + DQ_OFF_DO + half * BOX_BYTES, &tdo, h * HS, q0 + 64 * half, b, smem_u32(&q_full));
+            }
+            for (int j = 0; j < nkv && ok; j++) {
+                const int s = j % DQ_STAGES;
+                if (!mbar_wait(smem_u32(&kv_empty[s]), ((uint32_t)(j / DQ_STAGES) & 1u) ^ 1u, &s_abort, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&kv_full[s]);
+                mbar_expect_tx(fb, 2 * BOX_BYTES);
+                last_j[s] = j;
+                const uint32_t st = base + DQ_OFF_ST + s * DQ_STAGE;
+                tma_load_3d(st, &tq, C + h * HS, j * 64, b, fb);
+                tma_load_3d(st + BOX_BYTES, &tq, 2 * C + h * HS, j * 64, b, fb);
+            }
+            if (!ok) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_u32(&q_full), 0) && globaltimer() - t0 < WAIT_NS) {
+                }
+                for (int s = 0; s < DQ_STAGES; s++) {
+                    if (last_j[s] < 0) continue;
+                    const uint32_t ph = (uint32_t)(last_j[s] / DQ_STAGES) & 1u;
+                    const uint64_t t1 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(&kv_full[s]), ph) && globaltimer() - t1 < WAIT_NS) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = instr_desc(BQ, 64, false, false, true);   // Q K^T, dO V^T
+            const uint32_t id_o = instr_desc(BQ, HS, false, true, true);    // dS K (K read MN-major)
+            const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128;
+            bool ok = mbar_wait(smem_u32(&q_full), 0, &s_abort, status);
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % DQ_STAGES;
+                if (!mbar_wait(smem_u32(&kv_full[s]), (uint32_t)(j / DQ_STAGES) & 1u, &s_abort, status)) return false;
+                if (j > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(j - 1) & 1u, &s_abort, status)) return false;
+                tc_fence_after();
+                const uint32_t st = base + DQ_OFF_ST + s * DQ_STAGE;
+#pragma unroll
+                for (int k = 0; k < HS / 16; k++) {
+                    mma_issue<true>(t_s, smem_desc(base + DQ_OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                    mma_issue<true>(t_dp, smem_desc(base + DQ_OFF_DO + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
+                                    k > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&s_full));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; j < nkv && ok; j++) {
+                if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
+                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)j & 1u, &s_abort, status))) break;
+                tc_fence_after();
+                const uint32_t st = base + DQ_OFF_ST + (j % DQ_STAGES) * DQ_STAGE;
+#pragma unroll
+                for (int k = 0; k < 64 / 16; k++)
+                    mma_issue<true>(t_dq, smem_desc(base + DQ_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
+                                    smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&pv_done));
+                mma_commit(smem_u32(&kv_empty[j % DQ_STAGES]));
+            }
+            mma_commit(smem_u32(&drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&drain), 0) && globaltimer() - t0 < WAIT_NS) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ element-wise (warps 2..5), thread = query
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int row = q0 + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_base, t_dp = t_s + 64, t_dq = t_s + 128;
+        const float c2 = scale * LOG2E;
+        const size_t bh = ((size_t)b * H + h) * T;
+        const float lse2 = row < T ? lse[bh + row] * LOG2E : INFINITY;
+        const float Drow = row < T ? Dg[bh + row] : 0.f;
+        uint8_t* const dsrow = base_ptr + DQ_OFF_DS;
+        bool ok = true;
+        for (int j = 0; j < nkv; j++) {
+            if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
+            tc_fence_after();
+            float sv[64], dp[64];
+            {
+                float (&a0)[32] = *reinterpret_cast<float(*)[32]>(&sv[0]);
+                float (&a1)[32] = *reinterpret_cast<float(*)[32]>(&sv[32]);
+                float (&b0)[32] = *reinterpret_cast<float(*)[32]>(&dp[0]);
+                float (&b1)[32] = *reinterpret_cast<float(*)[32]>(&dp[32]);
+                tmem_ld32(t_s, a0);
+                tmem_ld32(t_s + 32, a1);
+                tmem_ld32(t_dp, b0);
+                tmem_ld32(t_dp + 32, b1);
+                tmem_wait_ld(a0);
+                tmem_wait_ld(a1);
+                tmem_wait_ld(b0);
+                tmem_wait_ld(b1);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s_free));
+            const int k0 = j * 64;
+            const bool diag = k0 + 63 > q0;            // some key of the tile follows some query
+#pragma unroll
+            for (int c = 0; c < 64; c++) {
+                float pv = ex2(fmaf(sv[c], c2, -lse2));
+                if (diag && (k0 + c > row || k0 + c >= T)) pv = 0.f;
+                dp[c] = pv * (dp[c] - Drow);
+            }
+            if (j > 0) {
+                if (!mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, &s_abort, status)) { ok = false; break; }
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int c = 0; c < 8; c++)
+                *reinterpret_cast<uint4*>(dsrow + sw128(r, c)) =
+                    make_uint4(pack_bf16(dp[8 * c], dp[8 * c + 1]), pack_bf16(dp[8 * c + 2], dp[8 * c + 3]),
+                               pack_bf16(dp[8 * c + 4], dp[8 * c + 5]), pack_bf16(dp[8 * c + 6], dp[8 * c + 7]));
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_full));
+        }
+        if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(nkv - 1) & 1u, &s_abort, status)) {
+            tc_fence_after();
+            float o[64];
+            float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
+            float (&c2v)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
+            tmem_ld32(t_dq, a);
+            tmem_ld32(t_dq + 32, c2v);
+            tmem_wait_ld(a);
+            tmem_wait_ld(c2v);
+            if (row < T) {
+                uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + row) * 3 * C + h * HS);
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    dst[c] = make_uint4(pack_bf16(o[8 * c] * scale, o[8 * c + 1] * scale),
+                                        pack_bf16(o[8 * c + 2] * scale, o[8 * c + 3] * scale),
+                                        pack_bf16(o[8 * c + 4] * scale, o[8 * c + 5] * scale),
+                                        pack_bf16(o[8 * c + 6] * scale, o[8 * c + 7] * scale));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
 }  // namespace at05
 
 bool attention_tc05_supported(int hs, int C) { return hs == at05::HS && C % 8 == 0; }
@@ -332,6 +829,46 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
     const float scale_log2 = LOG2E / sqrtf((float)HS);
     count_launch(), attn_fwd_tc05<<<dim3((T + BQ - 1) / BQ, H, B), THREADS, SMEM, st>>>(
         tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+}  // namespace gpt2k
+
+namespace gpt2k {
+
+// dqkv [B,T,3C] (bf16, every element written) from dy [B,T,C], qkv, the
+// forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64.
+int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
+                            int B, int T, int C, int H, int* status, cudaStream_t st) {
+    using namespace at05;
+    if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(attn_bwd_dkv_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKV_SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_dq_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
+                cudaSuccess) {
+            (void)cudaGetLastError();
+            return GPT2_ECUDA;
+        }
+        attr = true;
+    }
+    CUtensorMap tq, tdo;
+    const cuuint64_t dq_[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t sq_[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)T * 3 * C * 2};
+    const cuuint64_t dd_[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t sd_[2] = {(cuuint64_t)C * 2, (cuuint64_t)T * C * 2};
+    const cuuint32_t box[3] = {HS, 64, 1};
+    if (!encode_tensor_map(&tq, true, 3, qkv, dq_, sq_, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&tdo, true, 3, dy, dd_, sd_, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GPT2_ENOTSUP;
+    const float scale = 1.f / sqrtf((float)HS);
+    auto* out = static_cast<__nv_bfloat16*>(dqkv);
+    count_launch(), attn_bwd_dkv_tc05<<<dim3((T + 127) / 128, H, B), THREADS, DKV_SMEM, st>>>(
+        tq, tdo, out, lse, D, T, C, H, scale, status);
+    count_launch(), attn_bwd_dq_tc05<<<dim3((T + BQ - 1) / BQ, H, B), THREADS, DQ_SMEM, st>>>(
+        tq, tdo, out, lse, D, T, C, H, scale, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

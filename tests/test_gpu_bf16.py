@@ -246,7 +246,8 @@ def test_bf16_attention_forward_lse(B_, o64, B, T, C, H, ramp):
     assert int(st.item()) == 0
 
 
-@pytest.mark.parametrize("B,T,C,H", [(2, 37, 64, 4), (1, 300, 768, 12), (2, 129, 192, 3), (1, 1, 64, 4)])
+@pytest.mark.parametrize("B,T,C,H", [(2, 37, 64, 4), (1, 300, 768, 12), (2, 129, 192, 3), (1, 1, 64, 4),
+                                     (1, 1024, 768, 12), (3, 65, 128, 2), (1, 1, 64, 1)])
 def test_bf16_attention(B_, o64, B, T, C, H):
     L = B_.lib()
     rng = np.random.default_rng(5)
