@@ -22,7 +22,8 @@
 //            At the end O / l goes out as bf16 and the log-sum-exp as fp32.
 // Key tiles past the query tile's last row are never visited (causal tile
 // skipping).  While the softmax warps work on S_j, the tensor cores compute
-// S_{j+1} (the scores are in registers by then) and P_{j-1} V_{j-1}.
+// S_{j+1} (the scores are in registers by then) and P_{j-1} V_{j-1}; the MMA
+// thread issues each group the moment its inputs are ready.
 // Every wait is bounded (about one second); a wait that gives up raises
 // GPT2_STATUS_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // and tensor memory is freed.
@@ -70,6 +71,51 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Issue loop of the MMA thread.  Each tile j has two groups of MMAs:
+//   A  needs the tile's operand stage (full[j % stages], phase (j / stages) & 1)
+//      and the score columns released by the element-wise warps after tile
+//      j - 1 (s_free, phase (j - 1) & 1);
+//   B  needs the element-wise warps' operand tile of tile j (p_full, phase j & 1).
+// Each group is issued as soon as its inputs are ready, so B of tile j, which
+// frees the tile's stage, never waits for A of tile j + 1 and its copies.  No
+// phase can be lapped: every barrier's next phase needs this thread to consume
+// the current one first.  Gives up (abort flag, GPT2_STATUS_TIMEOUT) when
+// nothing becomes ready for WAIT_NS.
+template <class IssueA, class IssueB>
+__device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int stages, uint64_t* s_free,
+                                                   uint64_t* p_full, volatile int* abort_flag, int* status,
+                                                   IssueA&& issue_a, IssueB&& issue_b) {
+    int ja = 0, jb = 0;
+    uint64_t t0 = globaltimer();
+    uint32_t spins = 0;
+    while (jb < n) {
+        bool moved = false;
+        if (ja < n && mbar_test_wait(smem_u32(&full[ja % stages]), (uint32_t)(ja / stages) & 1u) &&
+            (ja == 0 || mbar_test_wait(smem_u32(s_free), (uint32_t)(ja - 1) & 1u))) {
+            tc_fence_after();
+            issue_a(ja++);
+            moved = true;
+        }
+        if (jb < ja && mbar_test_wait(smem_u32(p_full), (uint32_t)jb & 1u)) {
+            tc_fence_after();
+            issue_b(jb++);
+            moved = true;
+        }
+        if (moved) {
+            t0 = globaltimer();
+            spins = 0;
+        } else if ((++spins & 255) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_NS) {
+                *abort_flag = 1;
+                set_status(status, GPT2_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(THREADS, 2)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
               int T, int C, int H, float scale_log2, int* status) {
@@ -81,8 +127,9 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nq = (T + BQ - 1) / BQ;
-    const int qt = nq - 1 - (int)blockIdx.x;          // longest rows first
-    const int h = blockIdx.y, b = blockIdx.z;
+    // grid (H, B, query tiles): every head's longest tile is launched first
+    const int qt = nq - 1 - (int)blockIdx.z;
+    const int h = blockIdx.x, b = blockIdx.y;
     const int q0 = qt * BQ;
     const int nkv = (min(q0 + BQ, T) + BKV - 1) / BKV;  // key tiles that hold keys <= the last row
     const uint32_t raw = smem_u32(smem_raw);
@@ -131,6 +178,10 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
                 last_j[s] = j;
                 tma_load_3d(base + OFF_K + s * TILE_BYTES, &tm, C + h * HS, j * BKV, b, fb);
                 tma_load_3d(base + OFF_V + s * TILE_BYTES, &tm, 2 * C + h * HS, j * BKV, b, fb);
+                if (j + KV_STAGES < nkv) {             // this stage's next tile, into L2
+                    tma_prefetch_l2_3d(&tm, C + h * HS, (j + KV_STAGES) * BKV, b);
+                    tma_prefetch_l2_3d(&tm, 2 * C + h * HS, (j + KV_STAGES) * BKV, b);
+                }
             }
             if (!ok) {
                 // wait (bounded, ignoring the abort flag) for every copy this thread issued
@@ -154,35 +205,26 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             const uint32_t id_s = instr_desc(BQ, BKV, false, false, true);   // Q K^T: both K-major
             const uint32_t id_pv = instr_desc(BQ, HS, false, true, true);    // P V: V MN-major
             const uint32_t t_s = tmem, t_o = tmem + BKV;
-            bool ok = mbar_wait(smem_u32(&q_full), 0, &s_abort, status);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % KV_STAGES;
-                if (!mbar_wait(smem_u32(&kv_full[s]), (uint32_t)(j / KV_STAGES) & 1u, &s_abort, status))
-                    return false;
-                if (j > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(j - 1) & 1u, &s_abort, status))
-                    return false;
-                tc_fence_after();
-                const uint32_t kb = base + OFF_K + s * TILE_BYTES;
+            if (mbar_wait(smem_u32(&q_full), 0, &s_abort, status)) {
+                auto issue_s = [&](int j) {            // S = Q K_j^T
+                    const uint32_t kb = base + OFF_K + (j % KV_STAGES) * TILE_BYTES;
 #pragma unroll
-                for (int k = 0; k < HS / 16; k++)
-                    mma_issue<true>(t_s, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&s_full));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; j < nkv && ok; j++) {
-                if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)j & 1u, &s_abort, status))) break;
-                tc_fence_after();
-                const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
+                    for (int k = 0; k < HS / 16; k++)
+                        mma_issue<true>(t_s, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&s_full));
+                };
+                auto issue_pv = [&](int j) {           // O += P V_j
+                    const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
 #pragma unroll
-                for (int k = 0; k < BKV / 16; k++)
-                    mma_issue<true>(t_o, smem_desc(base + OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(vb + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_pv,
-                                    (j > 0 || k > 0) ? 1u : 0u);
-                mma_commit(smem_u32(&pv_done));
-                mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
+                    for (int k = 0; k < BKV / 16; k++)
+                        mma_issue<true>(t_o, smem_desc(base + OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(vb + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_pv,
+                                        (j > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&pv_done));
+                    mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
+                };
+                mma_two_group_loop(nkv, kv_full, KV_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_pv);
             }
             // every MMA issued has completed once this commit lands
             mma_commit(smem_u32(&drain));
@@ -345,7 +387,8 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     __shared__ volatile int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // grid (H, B, key tiles): key tile 0 sees every query, so it goes first
+    const int kt = blockIdx.z, h = blockIdx.x, b = blockIdx.y;
     const int k0 = kt * 128;
     const int i0 = k0 / 64, nq = (T + 63) / 64;   // query tiles i0 .. nq-1 see these keys
     const int ntile = nq - i0;
@@ -382,6 +425,16 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         bool ok = true;
         const float* lse_bh = lse + ((size_t)b * H + h) * T;
         const float* D_bh = Dg + ((size_t)b * H + h) * T;
+        // each lane carries two queries' lse*log2(e) and D, loaded one tile ahead
+        float nl[2], nd[2];
+        auto fetch_rows = [&](int t) {
+            for (int k = 0; k < 2; k++) {
+                const int q = (i0 + t) * 64 + lane + 32 * k;
+                nl[k] = q < T ? __ldg(lse_bh + q) * LOG2E : INFINITY;
+                nd[k] = q < T ? __ldg(D_bh + q) : 0.f;
+            }
+        };
+        fetch_rows(0);
         if (lane == 0) {
             mbar_expect_tx(smem_u32(&k_full), 4 * BOX_BYTES);
             for (int half = 0; half < 2; half++) {
@@ -396,22 +449,27 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 ok = mbar_wait(smem_u32(&q_empty[s]), ((uint32_t)(t / DKV_STAGES) & 1u) ^ 1u, &s_abort, status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            // the tile's lse (as lse*log2 e; +inf past T, which zeroes P) and D
-            float* rows = reinterpret_cast<float*>(base_ptr + DKV_OFF_ST + s * DKV_STAGE + DKV_ROWS);
-            for (int e = lane; e < 64; e += 32) {
-                const int q = (i0 + t) * 64 + e;
-                rows[e] = q < T ? lse_bh[q] * LOG2E : INFINITY;
-                rows[64 + e] = q < T ? D_bh[q] : 0.f;
-            }
-            __syncwarp();
+            const uint32_t fb = smem_u32(&q_full[s]);
             if (lane == 0) {
-                const uint32_t fb = smem_u32(&q_full[s]);
-                mbar_expect_tx(fb, 2 * BOX_BYTES);     // the arrive releases the writes above
+                // copies first; the barrier's phase cannot complete before the arrive below
                 last_i[s] = t;
                 const uint32_t st = base + DKV_OFF_ST + s * DKV_STAGE;
                 tma_load_3d(st, &tq, h * HS, (i0 + t) * 64, b, fb);
                 tma_load_3d(st + BOX_BYTES, &tdo, h * HS, (i0 + t) * 64, b, fb);
+                if (t + DKV_STAGES < ntile) {          // this stage's next tile, into L2
+                    tma_prefetch_l2_3d(&tq, h * HS, (i0 + t + DKV_STAGES) * 64, b);
+                    tma_prefetch_l2_3d(&tdo, h * HS, (i0 + t + DKV_STAGES) * 64, b);
+                }
             }
+            // the tile's lse (as lse*log2 e; +inf past T, which zeroes P) and D
+            float* rows = reinterpret_cast<float*>(base_ptr + DKV_OFF_ST + s * DKV_STAGE + DKV_ROWS);
+            for (int k = 0; k < 2; k++) {
+                rows[lane + 32 * k] = nl[k];
+                rows[64 + lane + 32 * k] = nd[k];
+            }
+            if (t + 1 < ntile) fetch_rows(t + 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(fb, 2 * BOX_BYTES);   // releases the writes above
         }
         if (lane == 0) {
             if (!ok) {
@@ -433,42 +491,34 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t id_s = instr_desc(128, 64, false, false, true);   // K Q^T, V dO^T
             const uint32_t id_o = instr_desc(128, HS, false, true, true);    // P^T dO, dS^T Q (MN-major B)
             const uint32_t t_st = tmem, t_dp = tmem + 64, t_dv = tmem + 128, t_dk = tmem + 192;
-            bool ok = mbar_wait(smem_u32(&k_full), 0, &s_abort, status);
-            auto issue_s = [&](int t) -> bool {
-                const int s = t % DKV_STAGES;
-                if (!mbar_wait(smem_u32(&q_full[s]), (uint32_t)(t / DKV_STAGES) & 1u, &s_abort, status)) return false;
-                if (t > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(t - 1) & 1u, &s_abort, status)) return false;
-                tc_fence_after();
-                const uint32_t st = base + DKV_OFF_ST + s * DKV_STAGE;
+            if (mbar_wait(smem_u32(&k_full), 0, &s_abort, status)) {
+                auto issue_s = [&](int t) {            // S^T = K Q_t^T, dP^T = V dO_t^T
+                    const uint32_t st = base + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE;
 #pragma unroll
-                for (int k = 0; k < HS / 16; k++) {
-                    mma_issue<true>(t_st, smem_desc(base + DKV_OFF_K + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
-                    mma_issue<true>(t_dp, smem_desc(base + DKV_OFF_V + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
-                                    k > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&s_full));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int t = 0; t < ntile && ok; t++) {
-                if (t + 1 < ntile && !(ok = issue_s(t + 1))) break;
-                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)t & 1u, &s_abort, status))) break;
-                tc_fence_after();
-                const uint32_t st = base + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE;
+                    for (int k = 0; k < HS / 16; k++) {
+                        mma_issue<true>(t_st, smem_desc(base + DKV_OFF_K + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                        mma_issue<true>(t_dp, smem_desc(base + DKV_OFF_V + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
+                                        k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&s_full));
+                };
+                auto issue_o = [&](int t) {            // dV += P^T dO_t, dK += dS^T Q_t (B read MN-major)
+                    const uint32_t st = base + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE;
 #pragma unroll
-                for (int k = 0; k < 64 / 16; k++) {
-                    // dV += P^T dO, dK += dS^T Q: B(n = head dim, k = query) read MN-major
-                    mma_issue<true>(t_dv, smem_desc(base + DKV_OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + BOX_BYTES + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
-                                    (t > 0 || k > 0) ? 1u : 0u);
-                    mma_issue<true>(t_dk, smem_desc(base + DKV_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
-                                    (t > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&pv_done));
-                mma_commit(smem_u32(&q_empty[t % DKV_STAGES]));
+                    for (int k = 0; k < 64 / 16; k++) {
+                        mma_issue<true>(t_dv, smem_desc(base + DKV_OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + BOX_BYTES + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                        (t > 0 || k > 0) ? 1u : 0u);
+                        mma_issue<true>(t_dk, smem_desc(base + DKV_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                        (t > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&pv_done));
+                    mma_commit(smem_u32(&q_empty[t % DKV_STAGES]));
+                };
+                mma_two_group_loop(ntile, q_full, DKV_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();
@@ -605,8 +655,8 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (T + BQ - 1) / BQ;
-    const int qt = nqt - 1 - (int)blockIdx.x;         // longest rows first
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int qt = nqt - 1 - (int)blockIdx.z;         // grid (H, B, query tiles): longest first
+    const int h = blockIdx.x, b = blockIdx.y;
     const int q0 = qt * BQ;
     const int nkv = (min(q0 + BQ, T) + 63) / 64;
     const uint32_t raw = smem_u32(smem_raw);
@@ -658,6 +708,10 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const uint32_t st = base + DQ_OFF_ST + s * DQ_STAGE;
                 tma_load_3d(st, &tq, C + h * HS, j * 64, b, fb);
                 tma_load_3d(st + BOX_BYTES, &tq, 2 * C + h * HS, j * 64, b, fb);
+                if (j + DQ_STAGES < nkv) {             // this stage's next tile, into L2
+                    tma_prefetch_l2_3d(&tq, C + h * HS, (j + DQ_STAGES) * 64, b);
+                    tma_prefetch_l2_3d(&tq, 2 * C + h * HS, (j + DQ_STAGES) * 64, b);
+                }
             }
             if (!ok) {
                 const uint64_t t0 = globaltimer();
@@ -678,37 +732,30 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const uint32_t id_s = instr_desc(BQ, 64, false, false, true);   // Q K^T, dO V^T
             const uint32_t id_o = instr_desc(BQ, HS, false, true, true);    // dS K (K read MN-major)
             const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128;
-            bool ok = mbar_wait(smem_u32(&q_full), 0, &s_abort, status);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % DQ_STAGES;
-                if (!mbar_wait(smem_u32(&kv_full[s]), (uint32_t)(j / DQ_STAGES) & 1u, &s_abort, status)) return false;
-                if (j > 0 && !mbar_wait(smem_u32(&s_free), (uint32_t)(j - 1) & 1u, &s_abort, status)) return false;
-                tc_fence_after();
-                const uint32_t st = base + DQ_OFF_ST + s * DQ_STAGE;
+            if (mbar_wait(smem_u32(&q_full), 0, &s_abort, status)) {
+                auto issue_s = [&](int j) {            // S = Q K_j^T, dP = dO V_j^T
+                    const uint32_t st = base + DQ_OFF_ST + (j % DQ_STAGES) * DQ_STAGE;
 #pragma unroll
-                for (int k = 0; k < HS / 16; k++) {
-                    mma_issue<true>(t_s, smem_desc(base + DQ_OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
-                    mma_issue<true>(t_dp, smem_desc(base + DQ_OFF_DO + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
-                                    k > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&s_full));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; j < nkv && ok; j++) {
-                if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-                if (!(ok = mbar_wait(smem_u32(&p_full), (uint32_t)j & 1u, &s_abort, status))) break;
-                tc_fence_after();
-                const uint32_t st = base + DQ_OFF_ST + (j % DQ_STAGES) * DQ_STAGE;
+                    for (int k = 0; k < HS / 16; k++) {
+                        mma_issue<true>(t_s, smem_desc(base + DQ_OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
+                        mma_issue<true>(t_dp, smem_desc(base + DQ_OFF_DO + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + BOX_BYTES + k * 32, 16, 1024, LAYOUT_SW128), id_s,
+                                        k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&s_full));
+                };
+                auto issue_o = [&](int j) {            // dQ += dS K_j (K read MN-major)
+                    const uint32_t st = base + DQ_OFF_ST + (j % DQ_STAGES) * DQ_STAGE;
 #pragma unroll
-                for (int k = 0; k < 64 / 16; k++)
-                    mma_issue<true>(t_dq, smem_desc(base + DQ_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
-                                    smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
-                                    (j > 0 || k > 0) ? 1u : 0u);
-                mma_commit(smem_u32(&pv_done));
-                mma_commit(smem_u32(&kv_empty[j % DQ_STAGES]));
+                    for (int k = 0; k < 64 / 16; k++)
+                        mma_issue<true>(t_dq, smem_desc(base + DQ_OFF_DS + k * 32, 16, 1024, LAYOUT_SW128),
+                                        smem_desc(st + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_o,
+                                        (j > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&pv_done));
+                    mma_commit(smem_u32(&kv_empty[j % DQ_STAGES]));
+                };
+                mma_two_group_loop(nkv, kv_full, DQ_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();
@@ -827,7 +874,7 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
     if (!encode_tensor_map(&tm, true, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return GPT2_ENOTSUP;
     const float scale_log2 = LOG2E / sqrtf((float)HS);
-    count_launch(), attn_fwd_tc05<<<dim3((T + BQ - 1) / BQ, H, B), THREADS, SMEM, st>>>(
+    count_launch(), attn_fwd_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), THREADS, SMEM, st>>>(
         tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
@@ -865,9 +912,9 @@ int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const f
         return GPT2_ENOTSUP;
     const float scale = 1.f / sqrtf((float)HS);
     auto* out = static_cast<__nv_bfloat16*>(dqkv);
-    count_launch(), attn_bwd_dkv_tc05<<<dim3((T + 127) / 128, H, B), THREADS, DKV_SMEM, st>>>(
+    count_launch(), attn_bwd_dkv_tc05<<<dim3(H, B, (T + 127) / 128), THREADS, DKV_SMEM, st>>>(
         tq, tdo, out, lse, D, T, C, H, scale, status);
-    count_launch(), attn_bwd_dq_tc05<<<dim3((T + BQ - 1) / BQ, H, B), THREADS, DQ_SMEM, st>>>(
+    count_launch(), attn_bwd_dq_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), THREADS, DQ_SMEM, st>>>(
         tq, tdo, out, lse, D, T, C, H, scale, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
