@@ -71,6 +71,24 @@ def load_peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def gemm_traffic_per_launch():
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None when the
+    GEMM sources changed since it was taken (the summary records their hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_tc_124M_B16T1024_bf16_dram.md")
+    try:
+        fields = dict(line.split(": ", 1) for line in open(path).read().splitlines() if ": " in line
+                      and line.split(": ", 1)[0] in ("traffic_bytes_per_launch", "sources", "sources_sha256"))
+        h = hashlib.sha256()
+        for f in fields["sources"].split():
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != fields["sources_sha256"].strip():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def gemm_flops(cfg, B, T):
     """Algorithmic FLOPs of every linear layer's forward, dX and dW product."""
     BT = B * T
@@ -322,6 +340,12 @@ def run_ours(args, cfg):
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                     "traffic": None, "peak_source": peak_note,
                     "share_of_step": round(gemm_ms / ms_per_step, 4)}
+        if args.mode == "bf16" and args.config == "124M":
+            # DRAM bytes per launch, from the committed ncu capture of this workload
+            tr = gemm_traffic_per_launch()
+            roofline["traffic"] = tr
+            if tr is not None:
+                roofline["traffic_unit"] = "bytes per launch (dram read + write, ncu)"
 
     mfu = step_flops(cfg, B, T) / (ms_per_step / 1000.0) / 1e12
     line = {
