@@ -533,6 +533,12 @@ def _mem_case(name, N=16384, C=768, V=50257, Vp=50304):
         losses = torch.empty(N, device=dev)
         fn = lambda: L.gpt2_op_crossentropy(k(losses), k(z), k(dz), k(tgt), N, V, Vp, 1.0 / N, k(st), None)
         nbytes = N * V * (4 + 2) + 8 * N
+    elif name == "crossentropy_bf16":                  # bf16 logits read, bf16 gradient written in place
+        z = (torch.randn(N, Vp, device=dev, generator=g) * 2).to(torch.bfloat16)
+        tgt = torch.randint(0, V, (N,), device=dev, dtype=torch.int32, generator=g)
+        losses = torch.empty(N, device=dev)
+        fn = lambda: L.gpt2_op_crossentropy_bf16(k(losses), k(z), k(tgt), N, V, Vp, 1.0 / N, k(st), None)
+        nbytes = N * Vp * (2 + 2) + 8 * N
     elif name.startswith("bias_grad"):                 # column sums of dY [N, 3C] (bf16) or [N, C] (fp32)
         bf = name.endswith("bf16")
         OC = 3 * C if bf else C
@@ -561,7 +567,7 @@ def _mem_case(name, N=16384, C=768, V=50257, Vp=50304):
     return fn, 0.0, float(nbytes), keep
 
 
-for _nm in ("ln_fwd", "ln_bwd", "crossentropy", "bias_grad_bf16", "bias_grad_f32", "adamw", "encoder_fwd"):
+for _nm in ("ln_fwd", "ln_bwd", "crossentropy", "crossentropy_bf16", "bias_grad_bf16", "bias_grad_f32", "adamw", "encoder_fwd"):
     OPS[f"mem_{_nm}"] = (lambda n: (lambda mode: _mem_case(n)))(_nm)
 
 

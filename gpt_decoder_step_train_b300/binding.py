@@ -33,7 +33,7 @@ class gpt2_gemm_args(C.Structure):
                 ("out", C.c_void_p), ("ldo", C.c_int), ("out_bf16", C.c_int),
                 ("out_pre", C.c_void_p), ("bias", C.c_void_p), ("residual", C.c_void_p),
                 ("gelu_x", C.c_void_p), ("ldg", C.c_int), ("gelu", C.c_int),
-                ("pre_bf16", C.c_int), ("gelu_x_bf16", C.c_int)]
+                ("pre_bf16", C.c_int), ("gelu_x_bf16", C.c_int), ("colsum", C.c_void_p)]
 
 
 class gpt2_config(C.Structure):
@@ -87,6 +87,7 @@ SIGNATURES = {
     "gpt2_op_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,
                                         _vp, _vp]),
     "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
+    "gpt2_op_crossentropy_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_sum": (_i, [_vp, _vp, _i, _f, _vp]),
     "gpt2_op_adamw": (_i, [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _f, _f, _vp]),
 }

@@ -319,7 +319,7 @@ bool attention_tc05_supported(int hs, int C);
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
                            cudaStream_t st);
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                            int B, int T, int C, int H, int* status, cudaStream_t st);
+                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum);
 
 }  // namespace gpt2k
 
@@ -358,23 +358,27 @@ GPT2_API size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
     return round_up((size_t)B * H * T * sizeof(float), 256);
 }
 
-GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv,
-                                        const void* y, const float* lse, int B, int T, int C,
-                                        int H, void* scratch, size_t scratch_bytes, int mode,
-                                        int* status, void* stream) {
+namespace gpt2k {
+
+int attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
+                       int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
+                       cudaStream_t st, float* colsum, bool* colsum_done) {
+    if (colsum_done) *colsum_done = false;
     if (!dqkv || !dy || !qkv || !y || !lse || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
     if (!aligned16(dqkv) || !aligned16(dy) || !aligned16(qkv) || !aligned16(y)) return GPT2_EINVAL;
     if (!scratch || scratch_bytes < gpt2_op_attention_backward_scratch_bytes(B, T, H))
         return GPT2_ENOMEM;
     int hs = C / H;
-    cudaStream_t st = as_stream(stream);
     float* D = reinterpret_cast<float*>(scratch);
     if (mode == GPT2_MODE_BF16) {
         if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
         launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
         GPT2_LAUNCH_CHECK();
-        if (attention_tc05_supported(hs, C))
-            return attention_tc05_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st);
+        if (attention_tc05_supported(hs, C)) {
+            if (colsum_done) *colsum_done = colsum != nullptr;
+            return attention_tc05_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st,
+                                           colsum_done ? colsum : nullptr);
+        }
         return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
     }
     float* dq = static_cast<float*>(dqkv);
@@ -389,4 +393,14 @@ GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* 
     else launch_bwd<64>(dq, g, x, lse, D, B, T, C, H, hs, st);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
+}
+
+}  // namespace gpt2k
+
+GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv,
+                                        const void* y, const float* lse, int B, int T, int C,
+                                        int H, void* scratch, size_t scratch_bytes, int mode,
+                                        int* status, void* stream) {
+    return attention_backward(dqkv, dy, qkv, y, lse, B, T, C, H, scratch, scratch_bytes, mode, status,
+                              as_stream(stream), nullptr, nullptr);
 }

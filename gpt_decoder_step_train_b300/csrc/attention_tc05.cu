@@ -71,6 +71,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Column sums of one warp's 32 output rows (lane = row row0 + lane; rows past
+// T hold 0) over the head's 64 columns, for the bias gradient of the qkv
+// projection: colsum [B * ceil(T/32), 3C], row group b * ceil(T/32) + row0/32,
+// columns col0 .. col0+63.  Consumes v.
+__device__ __forceinline__ void store_colsum(float* colsum, float (&v)[64], int lane, int b, int row0, int T,
+                                             int C, int col0) {
+    warp_colsum<64>(v, lane);
+    if (row0 >= T) return;
+    float* dst = colsum + ((size_t)b * ((T + 31) >> 5) + (row0 >> 5)) * 3 * C + col0 + warp_colsum_col<64>(lane);
+    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+}
+
 // Issue loop of the MMA thread.  Each tile j has two groups of MMAs:
 //   A  needs the tile's operand stage (full[j % stages], phase (j / stages) & 1)
 //      and the score columns released by the element-wise warps after tile
@@ -379,7 +391,7 @@ constexpr size_t DKV_SMEM = DKV_SMEM_USED + 1024;
 __global__ void __launch_bounds__(THREADS, 2)
 attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                   __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
-                  int T, int C, int H, float scale, int* status) {
+                  int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t k_full, q_full[DKV_STAGES], q_empty[DKV_STAGES], s_full, s_free, p_full,
         pv_done, drain;
@@ -614,15 +626,16 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tmem_wait_ld(a);
                 tmem_wait_ld(c2v);
                 const float f = which == 0 ? scale : 1.f;
+#pragma unroll
+                for (int c = 0; c < 64; c++) o[c] = key < T ? o[c] * f : 0.f;
                 if (key < T) {
                     uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + key) * 3 * C + (1 + which) * C + h * HS);
 #pragma unroll
                     for (int c = 0; c < 8; c++)
-                        dst[c] = make_uint4(pack_bf16(o[8 * c] * f, o[8 * c + 1] * f),
-                                            pack_bf16(o[8 * c + 2] * f, o[8 * c + 3] * f),
-                                            pack_bf16(o[8 * c + 4] * f, o[8 * c + 5] * f),
-                                            pack_bf16(o[8 * c + 6] * f, o[8 * c + 7] * f));
+                        dst[c] = make_uint4(pack_bf16(o[8 * c], o[8 * c + 1]), pack_bf16(o[8 * c + 2], o[8 * c + 3]),
+                                            pack_bf16(o[8 * c + 4], o[8 * c + 5]), pack_bf16(o[8 * c + 6], o[8 * c + 7]));
                 }
+                if (colsum) store_colsum(colsum, o, lane, b, k0 + quarter * 32, T, C, (1 + which) * C + h * HS);
             }
         }
     }
@@ -646,7 +659,7 @@ constexpr size_t DQ_SMEM = DQ_SMEM_USED + 1024;
 __global__ void __launch_bounds__(THREADS, 2)
 attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                  __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
-                 int T, int C, int H, float scale, int* status) {
+                 int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, kv_full[DQ_STAGES], kv_empty[DQ_STAGES], s_full, s_free, p_full,
         pv_done, drain;
@@ -827,15 +840,16 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             tmem_ld32(t_dq + 32, c2v);
             tmem_wait_ld(a);
             tmem_wait_ld(c2v);
+#pragma unroll
+            for (int c = 0; c < 64; c++) o[c] = row < T ? o[c] * scale : 0.f;
             if (row < T) {
                 uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + row) * 3 * C + h * HS);
 #pragma unroll
                 for (int c = 0; c < 8; c++)
-                    dst[c] = make_uint4(pack_bf16(o[8 * c] * scale, o[8 * c + 1] * scale),
-                                        pack_bf16(o[8 * c + 2] * scale, o[8 * c + 3] * scale),
-                                        pack_bf16(o[8 * c + 4] * scale, o[8 * c + 5] * scale),
-                                        pack_bf16(o[8 * c + 6] * scale, o[8 * c + 7] * scale));
+                    dst[c] = make_uint4(pack_bf16(o[8 * c], o[8 * c + 1]), pack_bf16(o[8 * c + 2], o[8 * c + 3]),
+                                        pack_bf16(o[8 * c + 4], o[8 * c + 5]), pack_bf16(o[8 * c + 6], o[8 * c + 7]));
             }
+            if (colsum) store_colsum(colsum, o, lane, b, q0 + quarter * 32, T, C, h * HS);
         }
     }
 
@@ -885,9 +899,11 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
 namespace gpt2k {
 
 // dqkv [B,T,3C] (bf16, every element written) from dy [B,T,C], qkv, the
-// forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64.
+// forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64.  With
+// colsum != null also the column sums of dqkv per 32-row group
+// ([B * ceil(T/32), 3C], fp32, before bf16 rounding).
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                            int B, int T, int C, int H, int* status, cudaStream_t st) {
+                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
     static bool attr = false;
@@ -913,9 +929,9 @@ int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const f
     const float scale = 1.f / sqrtf((float)HS);
     auto* out = static_cast<__nv_bfloat16*>(dqkv);
     count_launch(), attn_bwd_dkv_tc05<<<dim3(H, B, (T + 127) / 128), THREADS, DKV_SMEM, st>>>(
-        tq, tdo, out, lse, D, T, C, H, scale, status);
+        tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
     count_launch(), attn_bwd_dq_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), THREADS, DQ_SMEM, st>>>(
-        tq, tdo, out, lse, D, T, C, H, scale, status);
+        tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

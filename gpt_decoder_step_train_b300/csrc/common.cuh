@@ -70,6 +70,49 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// Column sums over a warp whose lane i holds row i of a 32 x NV block (NV a
+// power of two, 16 <= NV <= 64), in a fixed butterfly order (bit-reproducible).
+// Each step halves the values a lane keeps: at offset o the lane keeps the upper
+// half if (lane & o), the lower half otherwise, and adds its partner's copy of
+// the kept half.  After the last step v[0 .. NV/32) (NV >= 32), or v[0] (NV 16,
+// then duplicated in lanes 2j and 2j+1), hold whole-warp sums; the column of
+// v[j] is warp_colsum_col<NV>(lane) + j.
+template <int NV>
+__device__ __forceinline__ void warp_colsum(float (&v)[NV], int lane) {
+    static_assert(NV == 16 || NV == 32 || NV == 64, "16, 32 or 64 columns");
+    int n = NV;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        if (n == 1) {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+            continue;
+        }
+        const int h = n >> 1;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < NV / 2; j++) {
+            if (j < h) {
+                const float send = upper ? v[j] : v[h + j];
+                const float keep = upper ? v[h + j] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        n = h;
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ int warp_colsum_col(int lane) {
+    // the kept half at offset 16, 8, ... supplies the column's bits from the top
+    int col = 0, n = NV;
+#pragma unroll
+    for (int o = 16; o > 0 && n > 1; o >>= 1) {
+        n >>= 1;
+        if (lane & o) col += n;
+    }
+    return col;
+}
+
 __device__ __forceinline__ void set_status(int* status, int bit) {
     if (status) atomicOr(status, bit);
 }

@@ -126,6 +126,89 @@ crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bflo
     }
 }
 
+// bf16 logits, gradient written in place (bf16).  One block per row: the row
+// is staged once into shared memory with 16-byte asynchronous copies, so DRAM
+// sees one read and one write of two bytes per logit.  Pass 1 takes the row
+// maximum, pass 2 the sum of exponentials (both from shared memory), pass 3
+// writes the gradient.  Two blocks per SM: one row's copy overlaps the other
+// row's arithmetic.
+constexpr int CE16_THREADS = 512;
+constexpr int CE16_MAX_ROW_BYTES = GPT2_CE_BF16_MAX_LD * 2;   // 110 KB: two rows per SM
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(CE16_THREADS, 2)
+crossentropy_bf16_kernel(float* __restrict__ losses, __nv_bfloat16* __restrict__ z,
+                         const int* __restrict__ tgt, int V, int ld, float dscale, int* status) {
+    __shared__ float sh[CE16_THREADS / 32];
+    extern __shared__ uint4 zs[];                   // the row, 8 logits per entry
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int n8 = ld >> 3, nfull = V >> 3;         // 16-byte chunks: in the row, entirely inside [0, V)
+    uint4* zr = reinterpret_cast<uint4*>(z + (size_t)row * ld);
+    for (int c = tid; c < n8; c += CE16_THREADS)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(&zs[c])),
+                     "l"(zr + c)
+                     : "memory");
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    const __nv_bfloat16* zsh = reinterpret_cast<const __nv_bfloat16*>(zs);
+    float mx = -INFINITY;
+    for (int c = tid; c < nfull; c += CE16_THREADS) {
+        float f[8];
+        unpack8(zs[c], f);
+#pragma unroll
+        for (int k = 0; k < 8; k++) mx = fmaxf(mx, f[k]);
+    }
+    for (int v = nfull * 8 + tid; v < V; v += CE16_THREADS) mx = fmaxf(mx, __bfloat162float(zsh[v]));
+    const float M = block_reduce(mx, sh, true);
+    const float ml = M * CE_LOG2E;
+    float sum = 0.f;
+    for (int c = tid; c < nfull; c += CE16_THREADS) {
+        float f[8];
+        unpack8(zs[c], f);
+        float s2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 8; k++) s2[k & 1] += exp2f(fmaf(f[k], CE_LOG2E, -ml));
+        sum += s2[0] + s2[1];
+    }
+    for (int v = nfull * 8 + tid; v < V; v += CE16_THREADS)
+        sum += exp2f(fmaf(__bfloat162float(zsh[v]), CE_LOG2E, -ml));
+    const float S = block_reduce(sum, sh, false);
+    const float lse = M + logf(S);
+    const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    if (tid == 0) {
+        if (!ok) set_status(status, GPT2_STATUS_BAD_TARGET);
+        losses[row] = ok ? lse - __bfloat162float(zsh[t]) : 0.f;
+    }
+    if (dscale == 0.f) return;
+    const float lsel = lse * CE_LOG2E;
+    for (int c = tid; c < n8; c += CE16_THREADS) {
+        float f[8];
+        unpack8(zs[c], f);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const int idx = c * 8 + k;
+            const float p = exp2f(fmaf(f[k], CE_LOG2E, -lsel));
+            f[k] = (idx < V && ok) ? (p - (idx == t ? 1.f : 0.f)) * dscale : 0.f;
+        }
+        zr[c] = make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    }
+}
+
 // One block: thread t sums elements t, t+1024, ... in order; then a fixed tree.
 __global__ void __launch_bounds__(1024) sum_kernel(float* __restrict__ out, const float* __restrict__ x,
                                                    int N, float scale) {
@@ -159,6 +242,23 @@ GPT2_API int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const 
     const int ncache = std::min(V >> 2, CE_CACHE_BYTES / 16);
     count_launch(), crossentropy_kernel<<<N, CE_THREADS, (size_t)ncache * 16, as_stream(stream)>>>(
         losses, z, static_cast<__nv_bfloat16*>(dz_bf16), tgt, V, ld, dscale, ncache, status);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+GPT2_API int gpt2_op_crossentropy_bf16(float* losses, void* z, const int* tgt, int N, int V, int ld,
+                                       float dscale, int* status, void* stream) {
+    if (!losses || !z || !tgt || N < 1 || V < 1 || ld < V || ld % 8 || !aligned16(z) ||
+        (size_t)ld * 2 > (size_t)CE16_MAX_ROW_BYTES)
+        return GPT2_EINVAL;
+    static bool attr = false;
+    if (!attr) {
+        GPT2_CUDA_TRY(cudaFuncSetAttribute(crossentropy_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           CE16_MAX_ROW_BYTES));
+        attr = true;
+    }
+    count_launch(), crossentropy_bf16_kernel<<<N, CE16_THREADS, (size_t)ld * 2, as_stream(stream)>>>(
+        losses, static_cast<__nv_bfloat16*>(z), tgt, V, ld, dscale, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

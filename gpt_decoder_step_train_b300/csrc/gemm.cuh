@@ -28,6 +28,8 @@ struct GemmEpilogue {
     int gelu_x_bf16;
     int ldg;
     int gelu;                // 1: out_pre = acc + bias, out = gelu(out_pre)
+    float* colsum;           // [ceil(M/32), N] or null: per 32-row group, the column sums of the
+                             // stored values (before any bf16 rounding); tensor-core kernel only
 };
 
 struct GemmProblem {
@@ -80,14 +82,25 @@ bool gemm_tc_epilogue_supported(const GemmEpilogue& e);
 int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, const void* w,
                    bool bf16, const float* bias, const float* residual, int N, int IC, int OC,
                    int ld_out, int flags, int mode, int* status, cudaStream_t st);
+// With db != null, db[i] = sum over rows of dinp[:, i] as well: from the
+// epilogue's per-32-row column sums on the tensor cores, else by a pass over
+// dinp; cs is scratch of linear_colsum_bytes(N, IC) bytes.
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
-                          int* status, cudaStream_t st);
+                          int* status, cudaStream_t st, float* db = nullptr, void* cs = nullptr,
+                          size_t cs_bytes = 0);
+size_t linear_colsum_bytes(int N, int IC);
 int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
                            int OC, int ld_dout, void* scratch, size_t scratch_bytes, int mode,
                            int* status, cudaStream_t st);
 int bias_grad_any(float* db, const void* dout, bool bf16, int N, int OC, int ld, void* scratch,
                   size_t scratch_bytes, cudaStream_t st);
+// Attention backward (gpt2_op_attention_backward); with colsum != null the
+// tcgen05 kernels also leave per-32-row column sums of dqkv in colsum
+// ([B * ceil(T/32), 3C]) and set *colsum_done; other paths leave it false.
+int attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
+                       int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
+                       cudaStream_t st, float* colsum, bool* colsum_done);
 int layernorm_forward(void* y, bool out_bf16, float* mean, float* rstd, const float* x,
                       const float* w, const float* b, int N, int C, cudaStream_t st);
 int to_bf16(void* dst, const float* src, size_t n, cudaStream_t st);

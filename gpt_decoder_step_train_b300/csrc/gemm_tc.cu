@@ -450,6 +450,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int j = 0; j < 16; j++) x[j] = gelu_fwd_fast(x[j]);
                     }
                 }
+                if (p.e.colsum && row0 < p.M) {
+                    // this chunk's column sums over the warp's 32 rows (rows past M count 0;
+                    // a group that starts past M has no slot)
+                    float cs[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++) cs[j] = row0 + lane < p.M ? x[j] : 0.f;
+                    warp_colsum<16>(cs, lane);
+                    const int col = nc + warp_colsum_col<16>(lane);
+                    if (!(lane & 1) && col < p.N) p.e.colsum[(size_t)(row0 >> 5) * p.N + col] = cs[0];
+                }
                 put_row16(outb, lane, x, out16);
                 fence_proxy_async();
                 __syncwarp();

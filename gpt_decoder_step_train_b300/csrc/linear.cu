@@ -118,14 +118,34 @@ __global__ void splitk_reduce_kernel(float4* __restrict__ out, const float4* __r
     out[i] = s;
 }
 
-// Number of K slices for the tensor-core dW product: enough output tiles to
-// cover the SMs about twice, each slice at least 1024 rows of the reduction.
-static int dw_split(int N, int IC, int OC) {
-    long long tiles = (long long)ceil_div(OC, 128) * ceil_div(IC, 256);
-    int sms = num_sms();
-    int split = 1;
-    while (tiles * split < 2LL * sms && N / (split * 2) >= 1024 && split < 16) split *= 2;
-    return split;
+// Number of K slices for the tensor-core dW product (M = OC, N = IC, K = the N
+// rows), from a small cost model in microseconds: waves of units times the
+// k-blocks of a unit (about 0.45 us per 128 x 256 x 128-byte k-block on one
+// SM) plus about 1 us per wave of prologue and exposed epilogue, plus the fp32
+// partial slices written and summed again (S + 1 tile-sized passes at about
+// 5 TB/s).  More slices fill more SMs but move more partial bytes; no slice
+// is left empty.
+static int dw_split(int N, int IC, int OC, int mode) {
+    const int bn = IC <= 128 ? 128 : 256;
+    const long long tiles = (long long)ceil_div(OC, 128) * ceil_div(IC, bn);
+    const int nkb = ceil_div(N, mode == GPT2_MODE_BF16 ? 64 : 32);
+    const double t_kb = 0.45 * bn / 256.0, t_wave = 1.0, bytes_per_us = 5.0e6;
+    const double tile_bytes = 128.0 * bn * 4.0;
+    const long long sms = num_sms();
+    int best = 1;
+    double best_t = 0.0;
+    for (int split = 1; split <= 16; split++) {
+        const int kbps = ceil_div(nkb, split);
+        if (ceil_div(nkb, kbps) != split) continue;          // a slice would be empty
+        const long long waves = (tiles * split + sms - 1) / sms;
+        double t = (double)waves * (kbps * t_kb + t_wave);
+        if (split > 1) t += (split + 1) * (double)tiles * tile_bytes / bytes_per_us;
+        if (split == 1 || t < best_t) {
+            best_t = t;
+            best = split;
+        }
+    }
+    return best;
 }
 
 static int run_gemm(const GemmProblem& p, const GemmEpilogue& e, int mode, cudaStream_t st) {
@@ -169,10 +189,18 @@ int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, con
     return GPT2_OK;
 }
 
+// Bytes of the column-sum buffer of linear_backward_input for a bias gradient.
+size_t linear_colsum_bytes(int N, int IC) {
+    const int groups = ceil_div(N, 32);
+    return std::max(round_up((size_t)groups * IC * sizeof(float), 256) + bias_scratch_bytes(groups, IC),
+                    bias_scratch_bytes(N, IC));
+}
+
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
-                          int* status, cudaStream_t st) {
+                          int* status, cudaStream_t st, float* db, void* cs, size_t cs_bytes) {
     if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
+    if (db && (!cs || cs_bytes < linear_colsum_bytes(N, IC))) return GPT2_ENOMEM;
     GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status, bf16};
     GemmEpilogue e{};
     e.out = dinp;
@@ -181,7 +209,21 @@ int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const vo
     e.gelu_x = gelu_x;
     e.gelu_x_bf16 = bf16 ? 1 : 0;
     e.ldg = IC;
-    return run_gemm(p, e, mode, st);
+    // the tensor-core epilogue leaves per-32-row column sums of dinp in cs; the
+    // bias gradient is then their sum over the groups, in group order
+    const bool fused = db && (bf16 || (mode == GPT2_MODE_TF32 && gemm_tc_supported(p) &&
+                                       gemm_tc_epilogue_supported(e)));
+    const int groups = ceil_div(N, 32);
+    float* part = static_cast<float*>(cs);
+    if (fused) e.colsum = part;
+    int rc = run_gemm(p, e, mode, st);
+    if (rc || !db) return rc;
+    if (fused) {
+        float* tail = part + round_up((size_t)groups * IC, 64);
+        return bias_grad(db, static_cast<const float*>(part), groups, IC, IC, tail, st);
+    }
+    if (dinp_bf16) return bias_grad(db, static_cast<const __nv_bfloat16*>(dinp), N, IC, IC, part, st);
+    return bias_grad(db, static_cast<const float*>(dinp), N, IC, IC, part, st);
 }
 
 int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
@@ -191,7 +233,7 @@ int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf
     if (scratch_bytes < gpt2_op_linear_backward_weight_scratch_bytes(N, IC, OC, mode) || !scratch)
         return GPT2_ENOMEM;
     GemmProblem p{OC, IC, N, dout, ld_dout, false, inp, IC, false, status, bf16};
-    int split = mode != GPT2_MODE_FP32 ? dw_split(N, IC, OC) : 1;
+    int split = mode != GPT2_MODE_FP32 ? dw_split(N, IC, OC, mode) : 1;
     if (split > 1 && gemm_tc_supported(p) && (size_t)OC * IC % 4 == 0 && aligned16(dw)) {
         float* partial = reinterpret_cast<float*>(scratch);
         int rc = gemm_tc_splitk(p, partial, split, st);
@@ -241,7 +283,7 @@ GPT2_API size_t gpt2_op_linear_backward_weight_scratch_bytes(int N, int IC, int 
     if (N < 1 || IC < 1 || OC < 1) return 0;
     size_t s = bias_scratch_bytes(N, OC);
     if (mode != GPT2_MODE_FP32) {
-        int split = dw_split(N, IC, OC);
+        int split = dw_split(N, IC, OC, mode);
         if (split > 1) s = std::max(s, (size_t)split * OC * IC * sizeof(float));
     }
     return s;
@@ -279,6 +321,9 @@ GPT2_API int gpt2_op_gemm(const gpt2_gemm_args* a, int mode, int* status, void* 
     e.gelu_x_bf16 = a->gelu_x_bf16;
     e.ldg = a->ldg;
     e.gelu = a->gelu;
+    e.colsum = a->colsum;
+    if (e.colsum && !(p.bf16 || (mode == GPT2_MODE_TF32 && gemm_tc_supported(p) && gemm_tc_epilogue_supported(e))))
+        return GPT2_ENOTSUP;
     return run_gemm(p, e, mode, as_stream(stream));
 }
 

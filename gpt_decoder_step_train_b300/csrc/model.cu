@@ -104,6 +104,8 @@ struct gpt2 {
     char *dres16, *dz16, *dbig, *datty, *dqkv;
     void* scratch;
     size_t scratch_bytes;
+    float* colsum;              // per-32-row column sums for the fused bias gradients
+    size_t colsum_bytes;
     int B, T;
     bool fwd_targets, have_grads;
     int err;
@@ -176,6 +178,13 @@ static size_t plan(gpt2* m, char* base) {
     s = std::max(s, gpt2_op_bias_grad_scratch_bytes(Ri, 4 * Ci));
     m->scratch_bytes = s;
     m->scratch = take(s);
+    // column sums of the fused bias gradients: the MLP c_fc bias from the c_proj
+    // dX epilogue, the qkv bias from the attention backward
+    const int att_groups = c.maxB * ceil_div(c.maxT, 32);
+    m->colsum_bytes = std::max(linear_colsum_bytes(Ri, 4 * Ci),
+                               round_up((size_t)att_groups * 3 * C * sizeof(float), 256) +
+                                   gpt2_op_bias_grad_scratch_bytes(att_groups, 3 * Ci));
+    m->colsum = F(m->colsum_bytes / sizeof(float));
     return off;
 }
 
@@ -257,13 +266,22 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
     const float* xL = m->res3 + (size_t)(L - 1) * R * C;
     OP(LAYERNORM_FWD, layernorm_forward(m->lnf, b16, m->lnf_mean, m->lnf_rstd, xL, P(m, LNFW), P(m, LNFB),
                                         N, C, st));
-    OP(MATMUL_FWD, linear_forward(m->logits, false, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N, C,
-                                  c.V, m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
-    if (with_targets) {
-        OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->dz16, m->tgt, N, c.V, m->Vp,
-                                              1.0f / (float)N, status, st));
-        OP(CROSSENTROPY, gpt2_op_sum(&m->flags->loss, m->losses, N, 1.0f / (float)N, st));
+    if (b16 && with_targets && m->Vp <= GPT2_CE_BF16_MAX_LD) {
+        // training forward in BF16 mode: the logits go to the bf16 buffer and
+        // the cross-entropy overwrites them with their gradient (the padded
+        // columns are zeroed there), the operand of the lm_head backward
+        OP(MATMUL_FWD, linear_forward(m->dz16, true, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N, C,
+                                      c.V, m->Vp, 0, mode, status, st));
+        OP(CROSSENTROPY, gpt2_op_crossentropy_bf16(m->losses, m->dz16, m->tgt, N, c.V, m->Vp, 1.0f / (float)N,
+                                                   status, st));
+    } else {
+        OP(MATMUL_FWD, linear_forward(m->logits, false, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N,
+                                      C, c.V, m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
+        if (with_targets)
+            OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->dz16, m->tgt, N, c.V, m->Vp,
+                                                  1.0f / (float)N, status, st));
     }
+    if (with_targets) OP(CROSSENTROPY, gpt2_op_sum(&m->flags->loss, m->losses, N, 1.0f / (float)N, st));
     return GPT2_OK;
 }
 
@@ -305,8 +323,10 @@ static int backward_impl(gpt2* m) {
         };
         // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g (its bias
         // gradient came with the LayerNorm backward that produced dres)
+        // (with the c_fc bias gradient: the column sums of dh)
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dres_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
-                                                   4 * C, C, C, mode, status, st));
+                                                   4 * C, C, C, mode, status, st, G(m, FCB) + l * 4 * C,
+                                                   m->colsum, m->colsum_bytes));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dres_op, fchg, b16, N,
                                                      4 * C, C, C, sc, sb, mode, status, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
@@ -314,7 +334,6 @@ static int backward_impl(gpt2* m) {
                                                    C, 4 * C, 4 * C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCW) + l * 4 * cc, m->dbig, ln2, b16, N, C, 4 * C,
                                                      4 * C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, bias_grad_any(G(m, FCB) + l * 4 * C, m->dbig, b16, N, 4 * C, 4 * C, sc, sb, st));
         // ln_2: dres += LN'(dln2); the column sum of the result is the attention
         // c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN2W) + l * C, G(m, LN2B) + l * C,
@@ -326,15 +345,24 @@ static int backward_impl(gpt2* m) {
                                                    C, C, C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dres_op, atty, b16, N, C, C, C,
                                                      sc, sb, mode, status, st));
-        // attention
-        OP(ATTENTION_BWD, gpt2_op_attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T,
-                                                     C, H, sc, sb, mode, status, st));
+        // attention; the tcgen05 path also leaves the column sums of dqkv per
+        // 32 rows, which give the qkv bias gradient at once
+        bool qkv_colsum = false;
+        OP(ATTENTION_BWD, attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C, H, sc,
+                                             sb, mode, status, st, m->colsum, &qkv_colsum));
+        if (qkv_colsum) {
+            const int groups = B * ceil_div(T, 32);
+            const size_t part = round_up((size_t)groups * 3 * C * sizeof(float), 256);
+            OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->colsum, false, groups, 3 * C, 3 * C,
+                                        reinterpret_cast<char*>(m->colsum) + part, m->colsum_bytes - part, st));
+        }
         // c_attn
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dqkv, Wl(QKVW, 3 * cc), b16, nullptr, N,
                                                    C, 3 * C, 3 * C, mode, status, st));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, QKVW) + l * 3 * cc, m->dqkv, ln1, b16, N, C, 3 * C,
                                                      3 * C, sc, sb, mode, status, st));
-        OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->dqkv, b16, N, 3 * C, 3 * C, sc, sb, st));
+        if (!qkv_colsum)
+            OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->dqkv, b16, N, 3 * C, 3 * C, sc, sb, st));
         // ln_1: dres += LN'(dln1); the column sum of the result is the previous
         // block's MLP c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN1W) + l * C, G(m, LN1B) + l * C,

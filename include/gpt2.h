@@ -101,7 +101,7 @@ int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out);
 /* Forward pass on tokens[B,T] (device or host int32, row-major), 1 <= B <= maxB,
  * 1 <= T <= maxT.  targets[B,T] (device or host int32, or NULL): the next-token
  * ids.  With targets, returns the mean cross-entropy over the B*T positions
- * (natural log) and leaves d(loss)/d(logits) in the logits buffer for the
+ * (natural log) and leaves d(loss)/d(logits) in the workspace for the
  * backward; without targets, keeps the logits and returns NaN.  The inputs are
  * copied into the workspace, so the caller may reuse its buffers at once.
  * Returns NaN on error; gpt2_status() then gives the code (EINVAL, ETOKEN,
@@ -137,7 +137,9 @@ const char* gpt2_strerror(int code);
  * gpt2_logits: [B*T, row_stride] floats of the last forward; row_stride is the
  * vocabulary padded to a multiple of 128 and written to *row_stride.  Columns
  * >= V hold 0.  After a forward WITH targets the buffer holds d(loss)/d(logits)
- * instead (padded columns 0).  gpt2_losses: the B*T per-position losses. */
+ * instead (padded columns 0), except in GPT2_MODE_BF16 (padded vocabulary up to
+ * GPT2_CE_BF16_MAX_LD), where the training forward keeps logits and gradient
+ * in an internal bf16 buffer and leaves this one as it was.  gpt2_losses: the B*T per-position losses. */
 const float* gpt2_grads(gpt2* m);
 float* gpt2_adam_m(gpt2* m);
 float* gpt2_adam_v(gpt2* m);

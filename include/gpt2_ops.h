@@ -123,7 +123,11 @@ int gpt2_op_bias_grad(float* db, const void* dout, int dout_bf16, int N, int OC,
  * only).  Epilogue per element, in this order: + bias[n]; GELU (out_pre = value,
  * value = gelu(value)); + residual[m*ldo+n]; * gelu'(gelu_x[m*ldg+n]); stored to
  * out[m*ldo+n] as fp32, or bf16 when out_bf16.  out_pre is bf16 when pre_bf16,
- * gelu_x bf16 when gelu_x_bf16 (else fp32).  Pointers may be NULL to skip. */
+ * gelu_x bf16 when gelu_x_bf16 (else fp32).  Pointers may be NULL to skip.
+ * colsum [ceil(M/32), N] fp32 (tensor-core paths only; ENOTSUP on the CUDA
+ * cores): row g receives the column sums of the final values (before bf16
+ * rounding) of rows 32g .. 32g+31, summed in a fixed order -- a bias gradient
+ * of the product's output is the sum of these rows. */
 typedef struct {
     int M, N, K;
     const void* A; int lda; int a_kmajor;
@@ -137,6 +141,7 @@ typedef struct {
     int gelu;
     int pre_bf16;
     int gelu_x_bf16;
+    float* colsum;
 } gpt2_gemm_args;
 int gpt2_op_gemm(const gpt2_gemm_args* args, int mode, int* status, void* stream);
 
@@ -191,6 +196,17 @@ int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv, cons
  * section 计算loss.) */
 int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const int* tgt, int N, int V,
                          int ld, float dscale, int* status, void* stream);
+
+/* The same cross-entropy on bf16 logits z [N, ld] (16B, ld % 8 == 0, ld >= V,
+ * ld <= GPT2_CE_BF16_MAX_LD): losses as above, computed from the stored bf16 values in
+ * fp32; then the gradient, rounded to bf16, is written IN PLACE over z
+ * (columns V <= v < ld set to 0).  dscale 0 skips the gradient and leaves z
+ * unchanged.  A target outside [0,V) sets BAD_TARGET and that row's loss and
+ * gradient to 0.  ("从头搭建GPT 笔记", section 计算loss.)  EINVAL for a row
+ * longer than the limit or a misaligned z. */
+#define GPT2_CE_BF16_MAX_LD 56320
+int gpt2_op_crossentropy_bf16(float* losses, void* z, const int* tgt, int N, int V, int ld,
+                              float dscale, int* status, void* stream);
 
 /* Sum of losses[N] in a fixed order, times `scale`, written to *out (device). */
 int gpt2_op_sum(float* out, const float* losses, int N, float scale, void* stream);

@@ -75,7 +75,7 @@ def _gemm(B_, M, N, K, A, lda, ak, Bm, ldb, bk, out, ldo, out_bf16, **epi):
     a.B, a.ldb, a.b_kmajor = Bm.data_ptr(), ldb, bk
     a.bf16 = 1
     a.out, a.ldo, a.out_bf16 = out.data_ptr(), ldo, out_bf16
-    for k in ("out_pre", "bias", "residual", "gelu_x"):
+    for k in ("out_pre", "bias", "residual", "gelu_x", "colsum"):
         t = epi.get(k)
         setattr(a, k, t.data_ptr() if t is not None else None)
     a.ldg = epi.get("ldg", 0)
@@ -142,8 +142,17 @@ def test_bf16_gemm_three_products(B_, o64, M, N, K):
           pre_bf16=1)
     assert rel_l2(host(pre16), want + bias) < BF16_OUT
     assert rel_l2(host(o16), o64.gelu_forward(want + bias)) < BF16_OUT
-    _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, gelu_x=bf(h), ldg=N, gelu_x_bf16=1)
-    assert rel_l2(host(o16), o64.gelu_backward(rounded(h), want)) < BF16_OUT
+    groups = (M + 31) // 32
+    cs = torch.full((groups, N), 7.0, device="cuda")
+    _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, gelu_x=bf(h), ldg=N, gelu_x_bf16=1, colsum=cs)
+    dh = o64.gelu_backward(rounded(h), want)
+    assert rel_l2(host(o16), dh) < BF16_OUT
+    # per-32-row column sums of the unrounded values (the fused bias gradient)
+    pad = np.zeros((groups * 32, N))
+    pad[:M] = dh
+    want_cs = pad.reshape(groups, 32, N).sum(1)
+    assert rel_l2(host(cs), want_cs) < BF16_OUT
+    assert rel_l2(host(cs).sum(0), dh.sum(0)) < BF16_OUT
     _gemm(B_, M, N, K, bf(a), K, 1, bf(b), K, 1, o16, N, 1, bias=f32(bias))
     assert rel_l2(host(o16), want + bias) < BF16_OUT
 
@@ -198,6 +207,57 @@ def test_bf16_crossentropy_gradient(B_, o64, N, V):
     assert rel_l2(g, wdz) < BF16_OUT
     assert np.all(g[:, V:] == 0)
     assert np.array_equal(np.argmin(g[:, :V], axis=1), tgt)
+
+
+@pytest.mark.parametrize("N,V", [(37, 65), (300, 50257)])
+def test_bf16_logits_crossentropy_in_place(B_, o64, N, V):
+    """bf16 logits: losses from the stored bf16 values, gradient written over them."""
+    L = B_.lib()
+    rng = np.random.default_rng(5)
+    ld = (V + 127) // 128 * 128
+    z = np.zeros((N, ld), dtype=np.float32)
+    z[:, :V] = rng.normal(size=(N, V)) * 3
+    z[:, V:] = 9.0                                         # padding garbage: ignored, then zeroed
+    tgt = rng.integers(0, V, N).astype(np.int32)
+    zt = bf(z)
+    losses = torch.empty(N, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tg = torch.from_numpy(tgt).cuda()
+    # dscale 0: losses only, logits untouched
+    assert L.gpt2_op_crossentropy_bf16(B_.ptr(losses), B_.ptr(zt), B_.ptr(tg), N, V, ld, 0.0,
+                                       B_.ptr(st), None) == 0
+    zr = rounded(z)
+    mean, wl, probs = o64.crossentropy_forward(zr, tgt, V=V)
+    assert rel_l2(host(losses), wl) < 1e-6
+    assert np.array_equal(host(zt), zr)
+    assert L.gpt2_op_crossentropy_bf16(B_.ptr(losses), B_.ptr(zt), B_.ptr(tg), N, V, ld, 1.0 / N,
+                                       B_.ptr(st), None) == 0
+    wdz = o64.crossentropy_backward(probs, tgt, ld=ld)
+    g = host(zt)
+    assert rel_l2(host(losses), wl) < 1e-6
+    assert rel_l2(g, wdz) < BF16_OUT
+    assert np.all(g[:, V:] == 0)
+    assert np.array_equal(np.argmin(g[:, :V], axis=1), tgt)   # target selection
+    assert int(st.item()) == 0
+
+
+def test_bf16_logits_crossentropy_flags_bad_target(B_):
+    L = B_.lib()
+    N, V, ld = 4, 65, 128
+    z = bf(np.ones((N, ld)))
+    tgt = torch.tensor([0, 65, -1, 64], dtype=torch.int32, device="cuda")
+    losses = torch.empty(N, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert L.gpt2_op_crossentropy_bf16(B_.ptr(losses), B_.ptr(z), B_.ptr(tgt), N, V, ld, 1.0,
+                                       B_.ptr(st), None) == 0
+    lo, g = host(losses), host(z)
+    assert int(st.item()) & 2
+    assert lo[1] == 0 and lo[2] == 0 and np.all(g[1:3] == 0)
+    assert abs(lo[0] - np.log(65)) < 1e-5 and abs(lo[3] - np.log(65)) < 1e-5
+    assert L.gpt2_op_crossentropy_bf16(B_.ptr(losses), B_.ptr(z), B_.ptr(tgt), N, V, 8, 1.0,
+                                       B_.ptr(st), None) != 0            # ld < V
+    assert L.gpt2_op_crossentropy_bf16(B_.ptr(losses), B_.ptr(z), B_.ptr(tgt), N, 60000, 60032, 1.0,
+                                       B_.ptr(st), None) != 0            # row above the limit
 
 
 def test_bf16_bias_grad(B_):
