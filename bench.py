@@ -445,6 +445,8 @@ def _bgemm_case(name, M=16384, C=768, V=50257, Vp=50304):
         keep.append(t)
         setattr(a, field, B_.ptr(t))
     kind, lay = name.split("_", 1)
+    colsum = lay.endswith("cs")                        # with the per-32-row column sums (bias gradient)
+    lay = lay[:-2] if colsum else lay
     dims = {"qkv": (C, 3 * C), "attproj": (C, C), "fc": (C, 4 * C), "fcproj": (4 * C, C), "lmhead": (C, V)}
     IC, OC = dims[lay]
     if kind == "fwd":                                  # out[M, OC] = x[M, IC] W[OC, IC]^T
@@ -477,6 +479,8 @@ def _bgemm_case(name, M=16384, C=768, V=50257, Vp=50304):
         else:
             put("out", torch.empty(M, IC, device="cuda")); a.out_bf16 = 0
         a.ldo = IC
+    if colsum:
+        put("colsum", torch.empty((a.M + 31) // 32, a.N, device="cuda"))
     a.bf16 = 1
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     keep += [st, a]
@@ -487,6 +491,7 @@ def _bgemm_case(name, M=16384, C=768, V=50257, Vp=50304):
 for _k in ("fwd", "dx"):
     for _nm in ("qkv", "attproj", "fc", "fcproj", "lmhead"):
         OPS[f"bgemm_{_k}_{_nm}"] = (lambda n: (lambda mode: _bgemm_case(n)))(f"{_k}_{_nm}")
+OPS["bgemm_dx_fcprojcs"] = lambda mode: _bgemm_case("dx_fcprojcs")
 
 
 def _mem_case(name, N=16384, C=768, V=50257, Vp=50304):

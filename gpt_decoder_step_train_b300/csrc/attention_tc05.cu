@@ -7,16 +7,17 @@
 // 自注意力; the 1/sqrt(d_k) scaling: "从头搭建GPT(Andrej Karpathy) 笔记",
 // section attention中为什么要做scaling).
 //
-// One CTA per (query tile of 128 rows, head, batch), 192 threads, two CTAs per SM:
+// One CTA per (query tile of 128 rows, head, batch), 320 threads, two CTAs per SM:
 //   warp 0   TMA producer: the Q tile once, then K and V tiles of 64 keys
 //            into a four-stage ring (128-byte swizzle);
 //   warp 1   allocates tensor memory (S: 64 columns, O: 64 columns) and from
 //            one lane issues S = Q K^T (M=128, N=64, K=64) and O += P V
 //            (M=128, N=64, K=64; P from shared memory, V read MN-major);
-//   warps 2-5  softmax, one query row per thread (its TMEM lane): scores
-//            from tensor memory, causal mask on the diagonal tiles, online
-//            maximum and sum in the log2 domain, P written to shared memory as
-//            bf16 in the operand layout.  The running maximum used for P is
+//   warps 2-9  softmax, one query row per thread (its TMEM lane), two warps
+//            per row (32 key columns each, the row maximum combined through
+//            shared memory): scores from tensor memory, causal mask on the
+//            diagonal tiles, online maximum and sum in the log2 domain, P
+//            written to shared memory as bf16 in the operand layout.  The running maximum used for P is
 //            only moved when a row's true maximum exceeds it by more than
 //            2^8; O in tensor memory is then rescaled before the next P V.
 //            At the end O / l goes out as bf16 and the log-sum-exp as fp32.
@@ -41,15 +42,22 @@ using namespace ptx;
 constexpr int HS = 64;              // head size (one 128-byte swizzle row of bf16)
 constexpr int BQ = 128;             // queries per CTA (TMEM lanes)
 constexpr int BKV = 64;             // keys per tile
-constexpr int KV_STAGES = 4;
-constexpr int THREADS = 192;
+constexpr int KV_STAGES = 3;
+// forward: producer, MMA issuer and eight softmax warps (two per TMEM lane
+// quarter, one per half of the key tile's columns)
+constexpr int FWD_EW_WARPS = 8;
+constexpr int FWD_THREADS = 64 + 32 * FWD_EW_WARPS;
+// backward kernels: producer, MMA issuer and eight element-wise warps (two per
+// TMEM lane quarter, one per half of the tile's 64 columns)
+constexpr int BWD_EW_WARPS = 8;
+constexpr int BWD_THREADS = 64 + 32 * BWD_EW_WARPS;
 constexpr int TMEM_COLS = 128;      // S: [0, 64), O: [64, 128)
 constexpr uint32_t TILE_BYTES = BKV * HS * 2;     // one K or V tile: 8 KB
 constexpr uint32_t Q_BYTES = BQ * HS * 2;         // 16 KB
 constexpr uint32_t P_BYTES = BQ * BKV * 2;        // 16 KB
 // shared memory: Q | K[2] | V[2] | P, each 1024-byte aligned
 constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + Q_BYTES, OFF_V = OFF_K + KV_STAGES * TILE_BYTES,
-                   OFF_P = OFF_V + KV_STAGES * TILE_BYTES, SMEM_USED = OFF_P + P_BYTES;
+                   OFF_P = OFF_V + KV_STAGES * TILE_BYTES, SMEM_USED = OFF_P + 2 * P_BYTES;
 constexpr size_t SMEM = SMEM_USED + 1024;          // + alignment slack
 constexpr float RESCALE_LOG2 = 8.f;                // move the running maximum past 2^8 growth
 constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
@@ -72,22 +80,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // Column sums of one warp's 32 output rows (lane = row row0 + lane; rows past
-// T hold 0) over the head's 64 columns, for the bias gradient of the qkv
-// projection: colsum [B * ceil(T/32), 3C], row group b * ceil(T/32) + row0/32,
-// columns col0 .. col0+63.  Consumes v.
-__device__ __forceinline__ void store_colsum(float* colsum, float (&v)[64], int lane, int b, int row0, int T,
+// T hold 0) over 32 columns, for the bias gradient of the qkv projection:
+// colsum [B * ceil(T/32), 3C], row group b * ceil(T/32) + row0/32, columns
+// col0 .. col0+31.  Consumes v.
+__device__ __forceinline__ void store_colsum(float* colsum, float (&v)[32], int lane, int b, int row0, int T,
                                              int C, int col0) {
-    warp_colsum<64>(v, lane);
+    warp_colsum<32>(v, lane);
     if (row0 >= T) return;
-    float* dst = colsum + ((size_t)b * ((T + 31) >> 5) + (row0 >> 5)) * 3 * C + col0 + warp_colsum_col<64>(lane);
-    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+    colsum[((size_t)b * ((T + 31) >> 5) + (row0 >> 5)) * 3 * C + col0 + warp_colsum_col<32>(lane)] = v[0];
 }
 
 // Issue loop of the MMA thread.  Each tile j has two groups of MMAs:
 //   A  needs the tile's operand stage (full[j % stages], phase (j / stages) & 1)
 //      and the score columns released by the element-wise warps after tile
 //      j - 1 (s_free, phase (j - 1) & 1);
-//   B  needs the element-wise warps' operand tile of tile j (p_full, phase j & 1).
+//   B  needs the element-wise warps' operand tile of tile j (p_full[j % np],
+//      phase (j / np) & 1; np operand buffers used in turn).
 // Each group is issued as soon as its inputs are ready, so B of tile j, which
 // frees the tile's stage, never waits for A of tile j + 1 and its copies.  No
 // phase can be lapped: every barrier's next phase needs this thread to consume
@@ -95,7 +103,7 @@ __device__ __forceinline__ void store_colsum(float* colsum, float (&v)[64], int 
 // nothing becomes ready for WAIT_NS.
 template <class IssueA, class IssueB>
 __device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int stages, uint64_t* s_free,
-                                                   uint64_t* p_full, volatile int* abort_flag, int* status,
+                                                   uint64_t* p_full, int np, volatile int* abort_flag, int* status,
                                                    IssueA&& issue_a, IssueB&& issue_b) {
     int ja = 0, jb = 0;
     uint64_t t0 = globaltimer();
@@ -108,7 +116,7 @@ __device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int st
             issue_a(ja++);
             moved = true;
         }
-        if (jb < ja && mbar_test_wait(smem_u32(p_full), (uint32_t)jb & 1u)) {
+        if (jb < ja && mbar_test_wait(smem_u32(&p_full[jb % np]), (uint32_t)(jb / np) & 1u)) {
             tc_fence_after();
             issue_b(jb++);
             moved = true;
@@ -128,12 +136,14 @@ __device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int st
     return true;
 }
 
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(FWD_THREADS, 2)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
               int T, int C, int H, float scale_log2, int* status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full, s_free, p_full,
-        pv_done, drain;
+    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full, s_free, p_full[2],
+        pv_done[2], drain;
+    __shared__ __align__(8) uint64_t pair_bar[4][2];
+    __shared__ float pair_val[2][2][BQ];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
@@ -156,9 +166,13 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             mbar_init(smem_u32(&kv_empty[s]), 1);
         }
         mbar_init(smem_u32(&s_full), 1);
-        mbar_init(smem_u32(&s_free), 4);
-        mbar_init(smem_u32(&p_full), 4);
-        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&s_free), FWD_EW_WARPS);
+        for (int k = 0; k < 2; k++) {
+            mbar_init(smem_u32(&p_full[k]), FWD_EW_WARPS);
+            mbar_init(smem_u32(&pv_done[k]), 1);
+        }
+        for (int q = 0; q < 4; q++)
+            for (int k = 0; k < 2; k++) mbar_init(smem_u32(&pair_bar[q][k]), 2);
         mbar_init(smem_u32(&drain), 1);
         fence_mbar_init();
         prefetch_map(&tm);
@@ -226,17 +240,18 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
                                         smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
                     mma_commit(smem_u32(&s_full));
                 };
-                auto issue_pv = [&](int j) {           // O += P V_j
+                auto issue_pv = [&](int j) {           // O += P_j V_j (P_j in buffer j & 1)
                     const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
+                    const uint32_t pb = base + OFF_P + (uint32_t)(j & 1) * P_BYTES;
 #pragma unroll
                     for (int k = 0; k < BKV / 16; k++)
-                        mma_issue<true>(t_o, smem_desc(base + OFF_P + k * 32, 16, 1024, LAYOUT_SW128),
+                        mma_issue<true>(t_o, smem_desc(pb + k * 32, 16, 1024, LAYOUT_SW128),
                                         smem_desc(vb + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_pv,
                                         (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&pv_done));
+                    mma_commit(smem_u32(&pv_done[j & 1]));
                     mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
                 };
-                mma_two_group_loop(nkv, kv_full, KV_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_pv);
+                mma_two_group_loop(nkv, kv_full, KV_STAGES, &s_free, p_full, 2, &s_abort, status, issue_s, issue_pv);
             }
             // every MMA issued has completed once this commit lands
             mma_commit(smem_u32(&drain));
@@ -245,106 +260,126 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             }
         }
     } else {
-        // ------------------------------------------------ softmax (warps 2..5)
-        const int quarter = warp & 3;                  // TMEM lanes this warp may access
+        // ------------------------------------------------ softmax (warps 2..9)
+        // warps w and w + 4 share a TMEM lane quarter (32 rows); each takes 32 of
+        // the tile's 64 key columns and 32 of O's 64 columns.  The pair combines
+        // its row maxima every tile through shared memory and a two-warp
+        // mbarrier (double-buffered by tile parity), so both use the same
+        // running maximum; each keeps its own part of the row sum.
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;             // row within the tile
         const int row = q0 + r;
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t lane_base = ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half);
         const uint32_t t_s = tmem + lane_base, t_o = tmem + lane_base + BKV;
-        uint8_t* const prow = base_ptr + OFF_P;
-        float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, sum of P
+        uint8_t* const pbuf = base_ptr + OFF_P;    // two P buffers, tile j in buffer j & 1
+        float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, this half's sum of P
         bool ok = true;
+        // exchange slot of tile j: pair_val[j & 1][half][r]; barrier pair_bar[quarter][j & 1]
+        auto exchange = [&](int j, float v, float* other) -> bool {
+            pair_val[j & 1][half][r] = v;
+            __syncwarp();
+            const uint32_t bar = smem_u32(&pair_bar[quarter][j & 1]);
+            if (lane == 0) mbar_arrive(bar);
+            if (!mbar_wait(bar, (uint32_t)(j >> 1) & 1u, &s_abort, status)) return false;
+            *other = pair_val[j & 1][half ^ 1][r];
+            return true;
+        };
         for (int j = 0; j < nkv; j++) {
             if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
-            float s[64];
-            {
-                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&s[0]);
-                float (&c)[32] = *reinterpret_cast<float(*)[32]>(&s[32]);
-                tmem_ld32(t_s, a);
-                tmem_ld32(t_s + 32, c);
-                tmem_wait_ld(a);
-                tmem_wait_ld(c);
-            }
+            float s[32];
+            tmem_ld32(t_s, s);
+            tmem_wait_ld(s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s_free));
             // mask (tiles that reach the diagonal or the sequence end), row maximum
             // of the raw scores; the scale goes into the exponent's FMA
-            const int k0 = j * BKV;
-            if (k0 + BKV - 1 > q0 || k0 + BKV > T) {
+            const int k0 = j * BKV + 32 * half;        // first key of this warp's columns
+            if (k0 + 31 > q0 || k0 + 32 > T) {
 #pragma unroll
-                for (int c = 0; c < 64; c++)
+                for (int c = 0; c < 32; c++)
                     if (k0 + c > row || k0 + c >= T) s[c] = -INFINITY;
             }
-            float mx = s[0];
+            float m8[8];
 #pragma unroll
-            for (int c = 1; c < 64; c++) mx = fmaxf(mx, s[c]);
-            mx *= scale_log2;                          // log2-domain maximum of this tile
+            for (int c = 0; c < 8; c++) m8[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
+            float pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float om;
+            if (!exchange(j, pm, &om)) { ok = false; break; }
+            const float mx = fmaxf(pm, om) * scale_log2;    // log2-domain maximum of the tile's row
             float alpha = 1.f;                         // factor on O and l for this tile
             if (mx > m_run + RESCALE_LOG2 || (m_run == -INFINITY && mx > -INFINITY)) {
                 alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
                 m_run = mx;
             }
-            float ps = 0.f;
             const float mref = m_run == -INFINITY ? 0.f : m_run;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 64; c++) {
+            for (int c = 0; c < 32; c++) {
                 s[c] = ex2(fmaf(s[c], scale_log2, -mref));
-                ps += s[c];
+                ps[c & 3] += s[c];
             }
-            l_run = l_run * alpha + ps;
-            // O and the P buffer are free once P_{j-1} V_{j-1} has completed
-            if (j > 0) {
-                if (!mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, &s_abort, status)) { ok = false; break; }
+            l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+            // a rescale of O needs every earlier P V complete (the last is P_{j-1} V_{j-1})
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (!mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, &s_abort, status)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                {
+                    float o[32];
+                    tmem_ld32(t_o, o);
+                    tmem_wait_ld(o);
 #pragma unroll
-                    for (int half = 0; half < 2; half++) {
-                        float o[32];
-                        tmem_ld32(t_o + half * 32, o);
-                        tmem_wait_ld(o);
-#pragma unroll
-                        for (int c = 0; c < 32; c++) o[c] *= alpha;
-                        tmem_st32(t_o + half * 32, o);
-                    }
+                    for (int c = 0; c < 32; c++) o[c] *= alpha;
+                    tmem_st32(t_o, o);
                     tmem_wait_st();
                 }
             }
-            // P row (bf16) into the K-major operand tile
+            // buffer j & 1 is free once P_{j-2} V_{j-2} has completed
+            if (j > 1) {
+                if (!mbar_wait(smem_u32(&pv_done[j & 1]), (uint32_t)((j - 2) >> 1) & 1u, &s_abort, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            uint8_t* const prow = pbuf + (size_t)(j & 1) * P_BYTES;
+            // this half of the P row (bf16) into the K-major operand tile
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
+            for (int c = 0; c < 4; c++) {
                 const uint4 v = make_uint4(pack_bf16(s[8 * c], s[8 * c + 1]), pack_bf16(s[8 * c + 2], s[8 * c + 3]),
                                            pack_bf16(s[8 * c + 4], s[8 * c + 5]),
                                            pack_bf16(s[8 * c + 6], s[8 * c + 7]));
-                *reinterpret_cast<uint4*>(prow + sw128(r, c)) = v;
+                *reinterpret_cast<uint4*>(prow + sw128(r, 4 * half + c)) = v;
             }
             fence_proxy_async();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
         }
-        if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(nkv - 1) & 1u, &s_abort, status)) {
+        // the row sum: this half's part plus the partner's (same order in both warps)
+        float l_other = 0.f;
+        if (ok && !exchange(nkv, l_run, &l_other)) ok = false;
+        if (ok && mbar_wait(smem_u32(&pv_done[(nkv - 1) & 1]), (uint32_t)((nkv - 1) >> 1) & 1u, &s_abort, status)) {
             tc_fence_after();
-            float o[64];
-            {
-                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
-                float (&c)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
-                tmem_ld32(t_o, a);
-                tmem_ld32(t_o + 32, c);
-                tmem_wait_ld(a);
-                tmem_wait_ld(c);
-            }
+            float o[32];
+            tmem_ld32(t_o, o);
+            tmem_wait_ld(o);
             if (row < T) {
-                const float inv = 1.f / l_run;
-                uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)b * T + row) * C + h * HS);
+                const float l = half == 0 ? l_run + l_other : l_other + l_run;
+                const float inv = 1.f / l;
+                uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)b * T + row) * C + h * HS + 32 * half);
 #pragma unroll
-                for (int c = 0; c < 8; c++)
+                for (int c = 0; c < 4; c++)
                     yr[c] = make_uint4(pack_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
                                        pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                                        pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
                                        pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-                lse[((size_t)b * H + h) * T + row] = (m_run + log2f(l_run)) * LN2;
+                if (half == 0) lse[((size_t)b * H + h) * T + row] = (m_run + log2f(l)) * LN2;
             }
         }
     }
@@ -371,8 +406,10 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
 //       first two products and as MN-major operands of the last two.
 //   attn_bwd_dq_tc05   one CTA per 128-query tile; TMEM lanes are queries.  Per
 //       64-key tile: S = Q K^T and dP = dO V^T, then dS, then dQ += dS K.
-// Both follow the forward's roles: a TMA warp, one MMA-issuing thread, four
-// warps on the element-wise work (one row per thread).
+// Both follow the forward's roles: a TMA warp, one MMA-issuing thread, eight
+// warps on the element-wise work (one row per thread, two warps per row with
+// 32 of the tile's 64 columns each; no row reduction is needed here, since lse
+// and D come from the forward and the D kernel).
 
 constexpr uint32_t BOX_BYTES = 64 * HS * 2;        // one 64-row tile of a head: 8 KB
 
@@ -388,7 +425,7 @@ constexpr uint32_t DKV_OFF_K = 0, DKV_OFF_V = 16384, DKV_OFF_ST = 32768, DKV_ROW
                    DKV_OFF_DS = DKV_OFF_P + 16384, DKV_SMEM_USED = DKV_OFF_DS + 16384;
 constexpr size_t DKV_SMEM = DKV_SMEM_USED + 1024;
 
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(BWD_THREADS, 2)
 attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                   __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
                   int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
@@ -416,8 +453,8 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(smem_u32(&q_empty[s]), 1);
         }
         mbar_init(smem_u32(&s_full), 1);
-        mbar_init(smem_u32(&s_free), 4);
-        mbar_init(smem_u32(&p_full), 4);
+        mbar_init(smem_u32(&s_free), BWD_EW_WARPS);
+        mbar_init(smem_u32(&p_full), BWD_EW_WARPS);
         mbar_init(smem_u32(&pv_done), 1);
         mbar_init(smem_u32(&drain), 1);
         fence_mbar_init();
@@ -530,7 +567,7 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mma_commit(smem_u32(&pv_done));
                     mma_commit(smem_u32(&q_empty[t % DKV_STAGES]));
                 };
-                mma_two_group_loop(ntile, q_full, DKV_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_o);
+                mma_two_group_loop(ntile, q_full, DKV_STAGES, &s_free, &p_full, 1, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();
@@ -538,11 +575,13 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
         }
     } else {
-        // ------------------------------------------------ element-wise (warps 2..5), thread = key
-        const int quarter = warp & 3;
+        // ------------------------------------------------ element-wise (warps 2..9), thread = key
+        // warps w and w + 4 share a TMEM lane quarter; each takes 32 of the
+        // tile's 64 query columns
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int key = k0 + r;
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t lane_base = ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half);
         const uint32_t t_st = tmem + lane_base, t_dp = t_st + 64, t_dv = t_st + 128, t_dk = t_st + 192;
         const float c2 = scale * LOG2E;
         uint8_t* const prow = base_ptr + DKV_OFF_P;
@@ -552,38 +591,28 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // S^T and dP^T ready implies the stage (with lse and D) is full
             if (!mbar_wait(smem_u32(&s_full), (uint32_t)t & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
-            float sv[64], dp[64];
-            {
-                float (&a0)[32] = *reinterpret_cast<float(*)[32]>(&sv[0]);
-                float (&a1)[32] = *reinterpret_cast<float(*)[32]>(&sv[32]);
-                float (&b0)[32] = *reinterpret_cast<float(*)[32]>(&dp[0]);
-                float (&b1)[32] = *reinterpret_cast<float(*)[32]>(&dp[32]);
-                tmem_ld32(t_st, a0);
-                tmem_ld32(t_st + 32, a1);
-                tmem_ld32(t_dp, b0);
-                tmem_ld32(t_dp + 32, b1);
-                tmem_wait_ld(a0);
-                tmem_wait_ld(a1);
-                tmem_wait_ld(b0);
-                tmem_wait_ld(b1);
-            }
+            float sv[32], dp[32];
+            tmem_ld32(t_st, sv);
+            tmem_ld32(t_dp, dp);
+            tmem_wait_ld(sv);
+            tmem_wait_ld(dp);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s_free));
-            const int q0 = (i0 + t) * 64;
+            const int q0 = (i0 + t) * 64 + 32 * half;  // first query of this warp's columns
             // acquire the producer's lse and D writes from the stage barrier itself
             // (its phase for this tile completed before S^T was computed)
             if (!mbar_wait(smem_u32(&q_full[t % DKV_STAGES]), (uint32_t)(t / DKV_STAGES) & 1u, &s_abort, status)) {
                 ok = false;
                 break;
             }
-            const float* rows =
-                reinterpret_cast<const float*>(base_ptr + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE + DKV_ROWS);
+            const float* rows = reinterpret_cast<const float*>(base_ptr + DKV_OFF_ST + (t % DKV_STAGES) * DKV_STAGE +
+                                                               DKV_ROWS) + 32 * half;
             const float4* l4 = reinterpret_cast<const float4*>(rows);
             const float4* d4 = reinterpret_cast<const float4*>(rows + 64);
-            const bool diag = q0 < k0 + 127;           // some query of the tile precedes some key
+            const bool diag = q0 < k0 + 127;           // some query of these columns precedes some key
 #pragma unroll
-            for (int c4 = 0; c4 < 16; c4++) {
+            for (int c4 = 0; c4 < 8; c4++) {
                 const float4 lv = l4[c4], dv = d4[c4];
                 const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -601,11 +630,11 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_after();
             }
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
-                *reinterpret_cast<uint4*>(prow + sw128(r, c)) =
+            for (int c = 0; c < 4; c++) {
+                *reinterpret_cast<uint4*>(prow + sw128(r, 4 * half + c)) =
                     make_uint4(pack_bf16(sv[8 * c], sv[8 * c + 1]), pack_bf16(sv[8 * c + 2], sv[8 * c + 3]),
                                pack_bf16(sv[8 * c + 4], sv[8 * c + 5]), pack_bf16(sv[8 * c + 6], sv[8 * c + 7]));
-                *reinterpret_cast<uint4*>(dsrow + sw128(r, c)) =
+                *reinterpret_cast<uint4*>(dsrow + sw128(r, 4 * half + c)) =
                     make_uint4(pack_bf16(dp[8 * c], dp[8 * c + 1]), pack_bf16(dp[8 * c + 2], dp[8 * c + 3]),
                                pack_bf16(dp[8 * c + 4], dp[8 * c + 5]), pack_bf16(dp[8 * c + 6], dp[8 * c + 7]));
             }
@@ -617,25 +646,21 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(ntile - 1) & 1u, &s_abort, status)) {
             tc_fence_after();
             for (int which = 0; which < 2; which++) {  // 0: dK (scaled by c), 1: dV
-                float o[64];
-                float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
-                float (&c2v)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
-                const uint32_t src = which == 0 ? t_dk : t_dv;
-                tmem_ld32(src, a);
-                tmem_ld32(src + 32, c2v);
-                tmem_wait_ld(a);
-                tmem_wait_ld(c2v);
+                float o[32];
+                tmem_ld32(which == 0 ? t_dk : t_dv, o);
+                tmem_wait_ld(o);
                 const float f = which == 0 ? scale : 1.f;
 #pragma unroll
-                for (int c = 0; c < 64; c++) o[c] = key < T ? o[c] * f : 0.f;
+                for (int c = 0; c < 32; c++) o[c] = key < T ? o[c] * f : 0.f;
+                const int col0 = (1 + which) * C + h * HS + 32 * half;
                 if (key < T) {
-                    uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + key) * 3 * C + (1 + which) * C + h * HS);
+                    uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + key) * 3 * C + col0);
 #pragma unroll
-                    for (int c = 0; c < 8; c++)
+                    for (int c = 0; c < 4; c++)
                         dst[c] = make_uint4(pack_bf16(o[8 * c], o[8 * c + 1]), pack_bf16(o[8 * c + 2], o[8 * c + 3]),
                                             pack_bf16(o[8 * c + 4], o[8 * c + 5]), pack_bf16(o[8 * c + 6], o[8 * c + 7]));
                 }
-                if (colsum) store_colsum(colsum, o, lane, b, k0 + quarter * 32, T, C, (1 + which) * C + h * HS);
+                if (colsum) store_colsum(colsum, o, lane, b, k0 + quarter * 32, T, C, col0);
             }
         }
     }
@@ -656,7 +681,7 @@ constexpr uint32_t DQ_OFF_Q = 0, DQ_OFF_DO = 16384, DQ_OFF_ST = 32768, DQ_STAGE 
                    DQ_OFF_DS = DQ_OFF_ST + DQ_STAGES * DQ_STAGE, DQ_SMEM_USED = DQ_OFF_DS + 16384;
 constexpr size_t DQ_SMEM = DQ_SMEM_USED + 1024;
 
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(BWD_THREADS, 2)
 attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                  __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
                  int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
@@ -684,8 +709,8 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             mbar_init(smem_u32(&kv_empty[s]), 1);
         }
         mbar_init(smem_u32(&s_full), 1);
-        mbar_init(smem_u32(&s_free), 4);
-        mbar_init(smem_u32(&p_full), 4);
+        mbar_init(smem_u32(&s_free), BWD_EW_WARPS);
+        mbar_init(smem_u32(&p_full), BWD_EW_WARPS);
         mbar_init(smem_u32(&pv_done), 1);
         mbar_init(smem_u32(&drain), 1);
         fence_mbar_init();
@@ -768,7 +793,7 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     mma_commit(smem_u32(&pv_done));
                     mma_commit(smem_u32(&kv_empty[j % DQ_STAGES]));
                 };
-                mma_two_group_loop(nkv, kv_full, DQ_STAGES, &s_free, &p_full, &s_abort, status, issue_s, issue_o);
+                mma_two_group_loop(nkv, kv_full, DQ_STAGES, &s_free, &p_full, 1, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();
@@ -776,11 +801,13 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             }
         }
     } else {
-        // ------------------------------------------------ element-wise (warps 2..5), thread = query
-        const int quarter = warp & 3;
+        // ------------------------------------------------ element-wise (warps 2..9), thread = query
+        // warps w and w + 4 share a TMEM lane quarter; each takes 32 of the
+        // tile's 64 key columns
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int row = q0 + r;
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t lane_base = ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half);
         const uint32_t t_s = tmem + lane_base, t_dp = t_s + 64, t_dq = t_s + 128;
         const float c2 = scale * LOG2E;
         const size_t bh = ((size_t)b * H + h) * T;
@@ -791,28 +818,18 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         for (int j = 0; j < nkv; j++) {
             if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
-            float sv[64], dp[64];
-            {
-                float (&a0)[32] = *reinterpret_cast<float(*)[32]>(&sv[0]);
-                float (&a1)[32] = *reinterpret_cast<float(*)[32]>(&sv[32]);
-                float (&b0)[32] = *reinterpret_cast<float(*)[32]>(&dp[0]);
-                float (&b1)[32] = *reinterpret_cast<float(*)[32]>(&dp[32]);
-                tmem_ld32(t_s, a0);
-                tmem_ld32(t_s + 32, a1);
-                tmem_ld32(t_dp, b0);
-                tmem_ld32(t_dp + 32, b1);
-                tmem_wait_ld(a0);
-                tmem_wait_ld(a1);
-                tmem_wait_ld(b0);
-                tmem_wait_ld(b1);
-            }
+            float sv[32], dp[32];
+            tmem_ld32(t_s, sv);
+            tmem_ld32(t_dp, dp);
+            tmem_wait_ld(sv);
+            tmem_wait_ld(dp);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s_free));
-            const int k0 = j * 64;
-            const bool diag = k0 + 63 > q0;            // some key of the tile follows some query
+            const int k0 = j * 64 + 32 * half;        // first key of this warp's columns
+            const bool diag = k0 + 31 > q0;            // some key of these columns follows some query
 #pragma unroll
-            for (int c = 0; c < 64; c++) {
+            for (int c = 0; c < 32; c++) {
                 float pv = ex2(fmaf(sv[c], c2, -lse2));
                 if (diag && (k0 + c > row || k0 + c >= T)) pv = 0.f;
                 dp[c] = pv * (dp[c] - Drow);
@@ -822,8 +839,8 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tc_fence_after();
             }
 #pragma unroll
-            for (int c = 0; c < 8; c++)
-                *reinterpret_cast<uint4*>(dsrow + sw128(r, c)) =
+            for (int c = 0; c < 4; c++)
+                *reinterpret_cast<uint4*>(dsrow + sw128(r, 4 * half + c)) =
                     make_uint4(pack_bf16(dp[8 * c], dp[8 * c + 1]), pack_bf16(dp[8 * c + 2], dp[8 * c + 3]),
                                pack_bf16(dp[8 * c + 4], dp[8 * c + 5]), pack_bf16(dp[8 * c + 6], dp[8 * c + 7]));
             fence_proxy_async();
@@ -833,23 +850,20 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         }
         if (ok && mbar_wait(smem_u32(&pv_done), (uint32_t)(nkv - 1) & 1u, &s_abort, status)) {
             tc_fence_after();
-            float o[64];
-            float (&a)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
-            float (&c2v)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
-            tmem_ld32(t_dq, a);
-            tmem_ld32(t_dq + 32, c2v);
-            tmem_wait_ld(a);
-            tmem_wait_ld(c2v);
+            float o[32];
+            tmem_ld32(t_dq, o);
+            tmem_wait_ld(o);
 #pragma unroll
-            for (int c = 0; c < 64; c++) o[c] = row < T ? o[c] * scale : 0.f;
+            for (int c = 0; c < 32; c++) o[c] = row < T ? o[c] * scale : 0.f;
+            const int col0 = h * HS + 32 * half;
             if (row < T) {
-                uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + row) * 3 * C + h * HS);
+                uint4* dst = reinterpret_cast<uint4*>(dqkv + ((size_t)b * T + row) * 3 * C + col0);
 #pragma unroll
-                for (int c = 0; c < 8; c++)
+                for (int c = 0; c < 4; c++)
                     dst[c] = make_uint4(pack_bf16(o[8 * c], o[8 * c + 1]), pack_bf16(o[8 * c + 2], o[8 * c + 3]),
                                         pack_bf16(o[8 * c + 4], o[8 * c + 5]), pack_bf16(o[8 * c + 6], o[8 * c + 7]));
             }
-            if (colsum) store_colsum(colsum, o, lane, b, q0 + quarter * 32, T, C, h * HS);
+            if (colsum) store_colsum(colsum, o, lane, b, q0 + quarter * 32, T, C, col0);
         }
     }
 
@@ -888,7 +902,7 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
     if (!encode_tensor_map(&tm, true, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return GPT2_ENOTSUP;
     const float scale_log2 = LOG2E / sqrtf((float)HS);
-    count_launch(), attn_fwd_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), THREADS, SMEM, st>>>(
+    count_launch(), attn_fwd_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), FWD_THREADS, SMEM, st>>>(
         tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
@@ -928,9 +942,9 @@ int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const f
         return GPT2_ENOTSUP;
     const float scale = 1.f / sqrtf((float)HS);
     auto* out = static_cast<__nv_bfloat16*>(dqkv);
-    count_launch(), attn_bwd_dkv_tc05<<<dim3(H, B, (T + 127) / 128), THREADS, DKV_SMEM, st>>>(
+    count_launch(), attn_bwd_dkv_tc05<<<dim3(H, B, (T + 127) / 128), BWD_THREADS, DKV_SMEM, st>>>(
         tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
-    count_launch(), attn_bwd_dq_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), THREADS, DQ_SMEM, st>>>(
+    count_launch(), attn_bwd_dq_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), BWD_THREADS, DQ_SMEM, st>>>(
         tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;

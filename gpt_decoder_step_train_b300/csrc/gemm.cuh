@@ -90,6 +90,8 @@ int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const vo
                           int* status, cudaStream_t st, float* db = nullptr, void* cs = nullptr,
                           size_t cs_bytes = 0);
 size_t linear_colsum_bytes(int N, int IC);
+// db[c] = sum over g of part[g * OC + c], in group order.
+int colsum_reduce(float* db, const float* part, int groups, int OC, cudaStream_t st);
 int linear_backward_weight(float* dw, const void* dout, const void* inp, bool bf16, int N, int IC,
                            int OC, int ld_dout, void* scratch, size_t scratch_bytes, int mode,
                            int* status, cudaStream_t st);

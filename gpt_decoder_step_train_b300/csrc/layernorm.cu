@@ -239,6 +239,103 @@ ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* _
     }
 }
 
+// Register-streaming backward for rows of at most 32 * 4 * V4 (<= 768) columns: one block
+// of LNR_WARPS warps per SM, each warp walking its own rows one at a time with
+// every load of the row in flight at once (x, dy and the incoming dx as
+// float4), no shared-memory staging and no block barrier until the end.  Lane
+// l owns the float4 columns l, l+32, ...; its column sums of dy*xhat, dy and
+// the new dx stay in registers across the warp's rows (rows in order), then
+// the block adds its warps' sums in warp order through shared memory into
+// partial[blk][3][C], the same partial layout the tiled kernel above writes.
+constexpr int LNR_WARPS = 12;
+
+template <int V4>
+__global__ void __launch_bounds__(LNR_WARPS * 32, 1)
+ln_bwd_rows_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* __restrict__ partial,
+                   const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ w,
+                   const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C, int rpb,
+                   int accumulate) {
+    extern __shared__ __align__(16) float red[];       // [LNR_WARPS][3][C]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C4 = C >> 2;
+    const int r0 = blockIdx.x * rpb, r1 = min(N, r0 + rpb);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float4 aw[V4], ab[V4], as[V4];
+#pragma unroll
+    for (int k = 0; k < V4; k++) aw[k] = ab[k] = as[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float inv_c = 1.f / (float)C;
+    for (int row = r0 + warp; row < r1; row += LNR_WARPS) {
+        const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * C);
+        const float4* gr = reinterpret_cast<const float4*>(dy + (size_t)row * C);
+        float4* dr = reinterpret_cast<float4*>(dx + (size_t)row * C);
+        float4 xv[V4], gv[V4], ov[V4];
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            const bool in = c < C4;
+            xv[k] = in ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[k] = in ? __ldcs(gr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ov[k] = in && accumulate ? __ldcs(dr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float mu = __ldg(mean + row), rs = __ldg(rstd + row);
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            if (c < C4) {
+                const float4 ww = __ldg(w4 + c);
+                const float gx = gv[k].x * ww.x, gy = gv[k].y * ww.y, gz = gv[k].z * ww.z, gw = gv[k].w * ww.w;
+                // xv becomes xhat from here on
+                xv[k].x = (xv[k].x - mu) * rs; xv[k].y = (xv[k].y - mu) * rs;
+                xv[k].z = (xv[k].z - mu) * rs; xv[k].w = (xv[k].w - mu) * rs;
+                sg += (gx + gy) + (gz + gw);
+                sgx += (gx * xv[k].x + gy * xv[k].y) + (gz * xv[k].z + gw * xv[k].w);
+            }
+        }
+        const float mg = warp_sum(sg) * inv_c, mgx = warp_sum(sgx) * inv_c;
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            if (c < C4) {
+                const float4 ww = __ldg(w4 + c);
+                float4 o = ov[k];
+                o.x += rs * (gv[k].x * ww.x - mg - xv[k].x * mgx);
+                o.y += rs * (gv[k].y * ww.y - mg - xv[k].y * mgx);
+                o.z += rs * (gv[k].z * ww.z - mg - xv[k].z * mgx);
+                o.w += rs * (gv[k].w * ww.w - mg - xv[k].w * mgx);
+                dr[c] = o;
+                if (dx16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                    reinterpret_cast<uint2*>(dx16 + (size_t)row * C)[c] =
+                        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                }
+                aw[k].x += gv[k].x * xv[k].x; aw[k].y += gv[k].y * xv[k].y;
+                aw[k].z += gv[k].z * xv[k].z; aw[k].w += gv[k].w * xv[k].w;
+                ab[k].x += gv[k].x; ab[k].y += gv[k].y; ab[k].z += gv[k].z; ab[k].w += gv[k].w;
+                as[k].x += o.x; as[k].y += o.y; as[k].z += o.z; as[k].w += o.w;
+            }
+        }
+    }
+    // the warps' column sums, added in warp order
+    float4* mine = reinterpret_cast<float4*>(red + (size_t)warp * 3 * C);
+#pragma unroll
+    for (int k = 0; k < V4; k++) {
+        const int c = lane + 32 * k;
+        if (c < C4) {
+            mine[c] = aw[k];
+            mine[C4 + c] = ab[k];
+            mine[2 * C4 + c] = as[k];
+        }
+    }
+    __syncthreads();
+    float* out = partial + (size_t)blockIdx.x * 3 * C;
+    for (int i = threadIdx.x; i < 3 * C; i += LNR_WARPS * 32) {
+        float t = red[i];
+        for (int k = 1; k < LNR_WARPS; k++) t += red[(size_t)k * 3 * C + i];
+        out[i] = t;
+    }
+}
+
 // out_k[c] = sum_blk partial[blk][k][c] for k = 0 (dw), 1 (db), 2 (ds, when
 // wanted).  Block (32 columns x 16 lanes): lane y sums blocks y, y+16, ... in
 // order, then the 16 lane sums are added in lane order.
@@ -332,14 +429,38 @@ GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, flo
         count_launch(), ln_bwd_kernel<CPT><<<pl.grid, LNB_THREADS, smem, st>>>(                          \
             dx, dx16, partial, dy, x, w, mean, rstd, N, C, pl.rpb, pl.rb, pl.stages, accumulate ? 1 : 0, status); \
     } while (0)
-    if (cpt <= 1) LNB(1);
+    int nblk = pl.grid;
+    const int v4 = ceil_div(C / 4, 32);
+    if (v4 <= 6) {
+        // rows of up to 768 columns: the register-streaming kernel, one block per SM
+        nblk = std::min({num_sms(), LNB_MAX_BLOCKS, N});
+        const int rpb = ceil_div(N, nblk);
+        nblk = ceil_div(N, rpb);
+        const size_t rsm = (size_t)LNR_WARPS * 3 * C * sizeof(float);
+#define LNR(V4)                                                                                      \
+    do {                                                                                             \
+        static bool attr = false;                                                                    \
+        if (!attr) {                                                                                 \
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_rows_kernel<V4>,                               \
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,          \
+                                               (int)((size_t)LNR_WARPS * 3 * 768 * sizeof(float)))); \
+            attr = true;                                                                             \
+        }                                                                                            \
+        count_launch(), ln_bwd_rows_kernel<V4><<<nblk, LNR_WARPS * 32, rsm, st>>>(                  \
+            dx, dx16, partial, dy, x, w, mean, rstd, N, C, rpb, accumulate ? 1 : 0);                 \
+    } while (0)
+        if (v4 <= 2) LNR(2);
+        else if (v4 <= 4) LNR(4);
+        else LNR(6);
+#undef LNR
+    } else if (cpt <= 1) LNB(1);
     else if (cpt <= 2) LNB(2);
     else if (cpt <= 3) LNB(3);
     else if (cpt <= 4) LNB(4);
     else LNB(8);
 #undef LNB
     count_launch(), ln_bwd_reduce_kernel<<<ceil_div(3 * C, 32), dim3(32, 16), 0, st>>>(dw, db, dx_colsum, partial,
-                                                                                       pl.grid, C);
+                                                                                       nblk, C);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -105,6 +105,32 @@ static int bias_grad(float* db, const T* dout, int N, int OC, int ld, float* scr
     return GPT2_OK;
 }
 
+// ---- column sums of per-group partial sums: db[c] = sum_g part[g][c] --------
+// Block (32 columns x 32 lanes): lane y sums groups y, y+32, ... in order, then
+// the 32 lane sums are added in lane order; one block per 32 columns.
+__global__ void __launch_bounds__(1024) colsum_reduce_kernel(float* __restrict__ db, const float* __restrict__ part,
+                                                             int groups, int OC) {
+    __shared__ float sh[32][33];
+    const int c = blockIdx.x * 32 + threadIdx.x;
+    float s = 0.f;
+    if (c < OC)
+        for (int g = threadIdx.y; g < groups; g += 32) s += part[(size_t)g * OC + c];
+    sh[threadIdx.y][threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.y == 0 && c < OC) {
+        float t = sh[0][threadIdx.x];
+        for (int k = 1; k < 32; k++) t += sh[k][threadIdx.x];
+        db[c] = t;
+    }
+}
+
+int colsum_reduce(float* db, const float* part, int groups, int OC, cudaStream_t st) {
+    if (!db || !part || groups < 1 || OC < 1) return GPT2_EINVAL;
+    count_launch(), colsum_reduce_kernel<<<ceil_div(OC, 32), dim3(32, 32), 0, st>>>(db, part, groups, OC);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
 // ---- split-K sum: out[i] = sum_s partial[s][i], in slice order -------------
 __global__ void splitk_reduce_kernel(float4* __restrict__ out, const float4* __restrict__ partial,
                                      int split, size_t n4) {
@@ -191,9 +217,7 @@ int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, con
 
 // Bytes of the column-sum buffer of linear_backward_input for a bias gradient.
 size_t linear_colsum_bytes(int N, int IC) {
-    const int groups = ceil_div(N, 32);
-    return std::max(round_up((size_t)groups * IC * sizeof(float), 256) + bias_scratch_bytes(groups, IC),
-                    bias_scratch_bytes(N, IC));
+    return std::max(round_up((size_t)ceil_div(N, 32) * IC * sizeof(float), 256), bias_scratch_bytes(N, IC));
 }
 
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
@@ -218,10 +242,7 @@ int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const vo
     if (fused) e.colsum = part;
     int rc = run_gemm(p, e, mode, st);
     if (rc || !db) return rc;
-    if (fused) {
-        float* tail = part + round_up((size_t)groups * IC, 64);
-        return bias_grad(db, static_cast<const float*>(part), groups, IC, IC, tail, st);
-    }
+    if (fused) return colsum_reduce(db, part, groups, IC, st);
     if (dinp_bf16) return bias_grad(db, static_cast<const __nv_bfloat16*>(dinp), N, IC, IC, part, st);
     return bias_grad(db, static_cast<const float*>(dinp), N, IC, IC, part, st);
 }

@@ -181,9 +181,7 @@ static size_t plan(gpt2* m, char* base) {
     // column sums of the fused bias gradients: the MLP c_fc bias from the c_proj
     // dX epilogue, the qkv bias from the attention backward
     const int att_groups = c.maxB * ceil_div(c.maxT, 32);
-    m->colsum_bytes = std::max(linear_colsum_bytes(Ri, 4 * Ci),
-                               round_up((size_t)att_groups * 3 * C * sizeof(float), 256) +
-                                   gpt2_op_bias_grad_scratch_bytes(att_groups, 3 * Ci));
+    m->colsum_bytes = std::max(linear_colsum_bytes(Ri, 4 * Ci), (size_t)att_groups * 3 * C * sizeof(float));
     m->colsum = F(m->colsum_bytes / sizeof(float));
     return off;
 }
@@ -350,12 +348,8 @@ static int backward_impl(gpt2* m) {
         bool qkv_colsum = false;
         OP(ATTENTION_BWD, attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C, H, sc,
                                              sb, mode, status, st, m->colsum, &qkv_colsum));
-        if (qkv_colsum) {
-            const int groups = B * ceil_div(T, 32);
-            const size_t part = round_up((size_t)groups * 3 * C * sizeof(float), 256);
-            OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->colsum, false, groups, 3 * C, 3 * C,
-                                        reinterpret_cast<char*>(m->colsum) + part, m->colsum_bytes - part, st));
-        }
+        if (qkv_colsum)
+            OP(BIAS_GRAD, colsum_reduce(G(m, QKVB) + l * 3 * C, m->colsum, B * ceil_div(T, 32), 3 * C, st));
         // c_attn
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dqkv, Wl(QKVW, 3 * cc), b16, nullptr, N,
                                                    C, 3 * C, 3 * C, mode, status, st));
