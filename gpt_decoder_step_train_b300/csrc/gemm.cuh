@@ -74,6 +74,10 @@ int gemm_simt(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st);
 int gemm_tc(const GemmProblem& p, const GemmEpilogue& e, cudaStream_t st);
 int gemm_tc_splitk(const GemmProblem& p, float* partial, int split, cudaStream_t st);
 bool gemm_tc_supported(const GemmProblem& p);
+// Whether a bf16 product runs on CTA pairs (cta_group::2, 256 x 256 tiles), and
+// how many pairs the persistent grid holds.
+bool gemm_tc_pair(const GemmProblem& p);
+int gemm_tc_pair_slots();
 bool gemm_tc_epilogue_supported(const GemmEpilogue& e);
 
 // Linear-layer products for any operand type (linear.cu); bf16 requires

@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "gemm.cuh"
 #include "ptx.cuh"
 
@@ -55,11 +57,16 @@ constexpr int EC = 16;
 constexpr int EPI_WARP_BYTES = 4096;
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 
-template <int BN, bool BF16>
+// PAIR: two CTAs of a cluster share a 256-row tile through cta_group::2 MMAs;
+// each holds 128 rows of A and BN/2 rows of B per stage, and 128 rows of the
+// accumulator.
+template <int BN, bool BF16, bool PAIR = false>
 struct Shape {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = PAIR ? 6 : (BN == 256 ? 4 : 6);
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // rows of A per tile
     static constexpr int A_BYTES = BM * 128;          // BM rows x 128 bytes
-    static constexpr int B_BYTES = BN * 128;
+    static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + EPI_BYTES;
@@ -192,12 +199,13 @@ __device__ __forceinline__ void get_row16(const uint8_t* box, int row, float (&a
 }
 
 // ---------------------------------------------------------------- kernel
-template <int BN, bool BF16>
+template <int BN, bool BF16, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux,
                const __grid_constant__ CUtensorMap tmPre, const Params p) {
-    using S = Shape<BN, BF16>;
+    static_assert(!PAIR || (BF16 && BN == 256), "CTA pairs: bf16, 256-column tiles");
+    using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
     constexpr int RING_MAX = EPI_WARP_BYTES / 1024;   // input boxes per warp (bf16 boxes)
     extern __shared__ uint8_t smem_raw[];
@@ -207,6 +215,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ volatile int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // pair mode: rank 0 issues the MMAs; both CTAs walk the same units
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const long long u_first = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const long long u_step = PAIR ? gridDim.x / 2 : gridDim.x;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
@@ -221,7 +233,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);
+            mbar_init(smem_u32(&tempty_bar[a]), PAIR ? 2 * EPI_WARPS : EPI_WARPS);   // both CTAs' epilogues
         }
         mbar_init(smem_u32(&drain_bar), 1);
         for (int w = 0; w < EPI_WARPS; w++)
@@ -232,14 +244,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_map(&tmOut);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&s_tmem)),
-                     "r"(S::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            tmem_alloc_pair(&s_tmem, S::TMEM_COLS);
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&s_tmem)),
+                         "r"(S::TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();            // the peer's barriers exist before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = s_tmem;
 
@@ -250,9 +267,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             uint32_t armed = 0, armed_phase = 0;   // per-stage bits, for the abort drain
             bool ok = true;
-            for (long long u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            // a load of this CTA's shared memory counted on barrier `bar` (pair mode:
+            // rank 0's barrier, which expects both CTAs' bytes)
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+                if (PAIR) tma_load_2d_pair(dst, map, x, y, bar);
+                else tma_load_2d(dst, map, x, y, bar);
+            };
+            for (long long u = u_first; u < p.units && ok; u += u_step) {
                 Unit c = unit_coords(p, u);
-                const int m0 = c.m_tile * BM, n0 = c.n_tile * BN;
+                const int m0 = c.m_tile * S::TILE_M + (int)rank * BM, n0 = c.n_tile * BN + (int)rank * S::B_ROWS;
                 const int kb0 = c.split * p.kb_per_split;
                 const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -260,24 +283,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_expect_tx(fb, S::STAGE_BYTES);
-                    armed |= 1u << stage;
-                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    const uint32_t fb_local = smem_u32(&full_bar[stage]);
+                    const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
+                    if (rank == 0) {
+                        mbar_expect_tx(fb_local, PAIR ? 2 * S::STAGE_BYTES : S::STAGE_BYTES);
+                        armed |= 1u << stage;
+                        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    }
                     const int k0 = kb * E::BK;
                     if (p.a_kmajor) {
-                        tma_load_2d(stage_a(stage), &tmA, k0, m0, fb);
+                        load(stage_a(stage), &tmA, k0, m0, fb);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / E::MN_BOX; j++)
-                            tma_load_2d(stage_a(stage) + j * E::BOX_BYTES, &tmA, m0 + E::MN_BOX * j, k0, fb);
+                            load(stage_a(stage) + j * E::BOX_BYTES, &tmA, m0 + E::MN_BOX * j, k0, fb);
                     }
                     if (p.b_kmajor) {
-                        tma_load_2d(stage_b(stage), &tmB, k0, n0, fb);
+                        load(stage_b(stage), &tmB, k0, n0, fb);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / E::MN_BOX; j++)
-                            tma_load_2d(stage_b(stage) + j * E::BOX_BYTES, &tmB, n0 + E::MN_BOX * j, k0, fb);
+                        for (int j = 0; j < S::B_ROWS / E::MN_BOX; j++)
+                            load(stage_b(stage) + j * E::BOX_BYTES, &tmB, n0 + E::MN_BOX * j, k0, fb);
                     }
                     if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -294,9 +320,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = instr_desc(BM, BN, !p.a_kmajor, !p.b_kmajor, BF16);
+        // ------------------------------------------------ MMA issuer (pair mode: rank 0 only)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = instr_desc(S::TILE_M, BN, !p.a_kmajor, !p.b_kmajor, BF16);
             // one MMA consumes UMMA_K elements: 32 bytes of a K-major row, or UMMA_K
             // 128-byte rows of an MN-major box
             constexpr uint32_t KMAJ_STEP = E::UMMA_K * E::BYTES;
@@ -306,7 +332,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            for (long long u = u_first; u < p.units && ok; u += u_step) {
                 Unit c = unit_coords(p, u);
                 const int kb0 = c.split * p.kb_per_split;
                 const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
@@ -328,17 +354,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         uint64_t bd = p.b_kmajor
                                           ? smem_desc(b0 + k * KMAJ_STEP, 16, 1024, LAYOUT_SW128)
                                           : smem_desc(b0 + k * MN_STEP, p.mn_lbo, p.mn_sbo, p.mn_layout);
-                        mma_issue<BF16>(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (PAIR) mma_issue_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        else mma_issue<BF16>(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&empty_bar[stage]));
+                    // the stage is free in both CTAs once these MMAs have read it
+                    if (PAIR) mma_commit_pair(smem_u32(&empty_bar[stage]), 0x3);
+                    else mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&tfull_bar[acc]));
+                if (PAIR) mma_commit_pair(smem_u32(&tfull_bar[acc]), 0x3);
+                else mma_commit(smem_u32(&tfull_bar[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             // every MMA this thread issued has completed once drain_bar fires
-            mma_commit(smem_u32(&drain_bar));
+            if (PAIR) mma_commit_pair(smem_u32(&drain_bar), 0x1);
+            else mma_commit(smem_u32(&drain_bar));
             uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer() - t0 < WAIT_NS) {
             }
@@ -365,9 +396,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (long long u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        for (long long u = u_first; u < p.units && ok; u += u_step) {
             Unit c = unit_coords(p, u);
-            const int m0 = c.m_tile * BM, n0 = c.n_tile * BN + col_lo;
+            const int m0 = c.m_tile * S::TILE_M + (int)rank * BM, n0 = c.n_tile * BN + col_lo;
             const int row0 = m0 + q * 32;
             const int ncols = min(BN / 2, p.N - n0);
             const int nchunks = ncols > 0 ? (ncols + EC - 1) / EC : 0;
@@ -382,10 +413,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 bulk_wait_read(0);           // earlier stores out of the ring are done reading
                 for (int k = 0; k < min(ring - 1, nchunks); k++) aux_issue(k);
                 // the next tile's input rows of this warp go to L2 while this tile runs
-                const long long un = u + gridDim.x;
+                const long long un = u + u_step;
                 if (un < p.units) {
                     Unit cn = unit_coords(p, un);
-                    const int nn0 = cn.n_tile * BN + col_lo, nr0 = cn.m_tile * BM + q * 32;
+                    const int nn0 = cn.n_tile * BN + col_lo, nr0 = cn.m_tile * S::TILE_M + (int)rank * BM + q * 32;
                     if (nr0 < p.M)
                         for (int k = 0; k < BN / 2 && nn0 + k < p.N; k += EC) tma_prefetch_l2(&tmAux, nn0 + k, nr0);
                 }
@@ -479,7 +510,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+            if (lane == 0) {
+                // pair mode: rank 0's MMA thread waits for both CTAs' epilogues
+                if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+                else mbar_arrive(smem_u32(&tempty_bar[acc]));
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (has_aux && !ok && lane == 0) {
@@ -498,12 +533,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
+    // pair mode: neither CTA frees its tensor memory or leaves while the peer may
+    // still signal its barriers
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(S::TMEM_COLS)
-                     : "memory");
+        if (PAIR) {
+            tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+        } else {
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(S::TMEM_COLS)
+                         : "memory");
+        }
     }
 }
 
@@ -578,14 +620,14 @@ struct Maps {
     CUtensorMap a, b, out, aux, pre;
 };
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, bool PAIR>
 static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split, Maps* mp,
                    Params* pp) {
-    using S = Shape<BN, BF16>;
+    using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
     static bool attr_done = false;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<BN, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_tc_kernel<BN, BF16, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)S::SMEM) != cudaSuccess) {
             (void)cudaGetLastError();
             return GPT2_ECUDA;
@@ -597,7 +639,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     // A: K-major [M, K] (box {BK, 128}); M-major [K, M] (box {MN_BOX, BK})
     bool ok = g.a_kmajor ? make_map(&mp->a, g.A, BF16, g.K, g.M, g.lda, E::BK, BM, KSW)
                          : make_map(&mp->a, g.A, BF16, g.M, g.K, g.lda, E::MN_BOX, E::BK, MSW);
-    ok = ok && (g.b_kmajor ? make_map(&mp->b, g.B, BF16, g.K, g.N, g.ldb, E::BK, BN, KSW)
+    ok = ok && (g.b_kmajor ? make_map(&mp->b, g.B, BF16, g.K, g.N, g.ldb, E::BK, S::B_ROWS, KSW)
                            : make_map(&mp->b, g.B, BF16, g.N, g.K, g.ldb, E::MN_BOX, E::BK, MSW));
     Params p{};
     // epilogue maps, boxes of 32 rows x EC columns: fp32 64-byte rows (64-byte
@@ -626,7 +668,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     if (!e.gelu || partial) mp->pre = mp->out;
     p.M = g.M; p.N = g.N; p.K = g.K;
     p.a_kmajor = g.a_kmajor; p.b_kmajor = g.b_kmajor;
-    p.tiles_m = ceil_div(g.M, BM);
+    p.tiles_m = ceil_div(g.M, S::TILE_M);
     p.tiles_n = ceil_div(g.N, BN);
     p.num_kb = ceil_div(g.K, E::BK);
     p.split = split;
@@ -634,7 +676,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     if (ceil_div(p.num_kb, p.kb_per_split) != split) return GPT2_EINVAL;   // an empty K slice
     p.units = (long long)p.tiles_m * p.tiles_n * split;
     // group enough m-tiles that their A rows stay in L2 while B streams past
-    p.group_m = std::max(1, std::min(p.tiles_m, 16));
+    p.group_m = std::max(1, std::min(p.tiles_m, PAIR ? 8 : 16));
     p.e = e;
     p.partial = partial;
     p.status = g.status;
@@ -648,33 +690,99 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     return GPT2_OK;
 }
 
-template <int BN, bool BF16>
-static int run(const Maps& mp, const Params& p, cudaStream_t st) {
-    int grid = (int)std::min<long long>(p.units, num_sms());
-    count_launch(), gemm_tc_kernel<BN, BF16><<<grid, THREADS, Shape<BN, BF16>::SMEM, st>>>(
-        mp.a, mp.b, mp.out, mp.aux, mp.pre, p);
-    GPT2_LAUNCH_CHECK();
-    return GPT2_OK;
+// Clusters of two CTAs that can be resident at once for the pair kernel (one
+// CTA per SM): the persistent grid's size.
+static int pair_clusters() {
+    static int n = -1;
+    if (n < 0) {
+        using S = Shape<256, true, true>;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = S::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaFuncSetAttribute(gemm_tc_kernel<256, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)S::SMEM) == cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<256, true, true>, &cfg) == cudaSuccess && c > 0)
+            n = c;
+        else {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+    }
+    return n;
 }
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, bool PAIR>
+static int run(const Maps& mp, const Params& p, cudaStream_t st) {
+    if constexpr (!PAIR) {
+        int grid = (int)std::min<long long>(p.units, num_sms());
+        count_launch(), gemm_tc_kernel<BN, BF16, false><<<grid, THREADS, Shape<BN, BF16, false>::SMEM, st>>>(
+            mp.a, mp.b, mp.out, mp.aux, mp.pre, p);
+        GPT2_LAUNCH_CHECK();
+        return GPT2_OK;
+    } else {
+    const int clusters = (int)std::min<long long>(p.units, pair_clusters());
+    if (clusters < 1) return GPT2_ENOTSUP;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Shape<BN, BF16, true>::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launch();
+    GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, BF16, true>, mp.a, mp.b, mp.out, mp.aux, mp.pre, p));
+    return GPT2_OK;
+    }
+}
+
+template <int BN, bool BF16, bool PAIR>
 static int launch(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
                   cudaStream_t st) {
     Maps mp;
     Params p;
-    int rc = prepare<BN, BF16>(g, e, partial, split, &mp, &p);
+    int rc = prepare<BN, BF16, PAIR>(g, e, partial, split, &mp, &p);
     if (rc) return rc;
-    return run<BN, BF16>(mp, p, st);
+    return run<BN, BF16, PAIR>(mp, p, st);
 }
 
 template <bool BF16>
 static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
                       cudaStream_t st) {
-    if (g.N <= 128) return launch<128, BF16>(g, e, partial, split, st);
-    return launch<256, BF16>(g, e, partial, split, st);
+    if constexpr (BF16)
+        if (gemm_tc_pair(g)) return launch<256, true, true>(g, e, partial, split, st);
+    if (g.N <= 128) return launch<128, BF16, false>(g, e, partial, split, st);
+    return launch<256, BF16, false>(g, e, partial, split, st);
 }
 
 }  // namespace tc
+
+// bf16 products with at least 256 rows and 256 columns run on CTA pairs
+// (cta_group::2, 256 x 256 tiles) unless GPT2_GEMM_CTA_PAIRS=0 is set in the
+// environment (the single-CTA kernel, 128 x 256 tiles, then takes them).
+bool gemm_tc_pair(const GemmProblem& g) {
+    static int on = -1;
+    if (on < 0) {
+        const char* v = getenv("GPT2_GEMM_CTA_PAIRS");
+        on = (v && v[0] == '0') ? 0 : 1;
+    }
+    return on && g.bf16 && g.M >= 256 && g.N >= 256 && tc::pair_clusters() > 0;
+}
+
+int gemm_tc_pair_slots() { return tc::pair_clusters(); }
 
 bool encode_tensor_map(CUtensorMap* map, bool bf16, int rank, const void* ptr, const cuuint64_t* dims,
                        const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {

@@ -152,12 +152,16 @@ __global__ void splitk_reduce_kernel(float4* __restrict__ out, const float4* __r
 // 5 TB/s).  More slices fill more SMs but move more partial bytes; no slice
 // is left empty.
 static int dw_split(int N, int IC, int OC, int mode) {
-    const int bn = IC <= 128 ? 128 : 256;
-    const long long tiles = (long long)ceil_div(OC, 128) * ceil_div(IC, bn);
+    // the product is M = OC, N = IC, K = N rows; CTA pairs take 256 x 256 tiles
+    // (a pair moves through a k-block in the time one CTA takes for 128 x 256)
+    GemmProblem probe{OC, IC, N, nullptr, 0, false, nullptr, 0, false, nullptr, mode == GPT2_MODE_BF16};
+    const bool pair = gemm_tc_pair(probe);
+    const int bm = pair ? 256 : 128, bn = (IC <= 128 && !pair) ? 128 : 256;
+    const long long tiles = (long long)ceil_div(OC, bm) * ceil_div(IC, bn);
     const int nkb = ceil_div(N, mode == GPT2_MODE_BF16 ? 64 : 32);
     const double t_kb = 0.45 * bn / 256.0, t_wave = 1.0, bytes_per_us = 5.0e6;
-    const double tile_bytes = 128.0 * bn * 4.0;
-    const long long sms = num_sms();
+    const double tile_bytes = (double)bm * bn * 4.0;
+    const long long sms = pair ? gemm_tc_pair_slots() : num_sms();
     int best = 1;
     double best_t = 0.0;
     for (int split = 1; split <= 16; split++) {

@@ -65,7 +65,9 @@ def test_to_bf16_is_round_to_nearest_even(B_):
     assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
 
 
-GEMM_SHAPES = [(300, 192, 64), (257, 2304, 768), (129, 768, 3072), (128, 65, 64), (64, 50304, 768)]
+# shapes of at least 256 x 256 run on CTA pairs (cta_group::2), the others on single CTAs
+GEMM_SHAPES = [(300, 192, 64), (257, 2304, 768), (129, 768, 3072), (128, 65, 64), (64, 50304, 768),
+               (512, 768, 3072), (1024, 2304, 768), (384, 520, 256), (512, 50304, 768)]
 
 
 def _gemm(B_, M, N, K, A, lda, ak, Bm, ldb, bk, out, ldo, out_bf16, **epi):
