@@ -13,6 +13,7 @@
 // products.
 // DRAM traffic is one read of the logits and one write of the gradient.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -27,7 +28,6 @@ constexpr int CE_THREADS = 512;
 constexpr int CE_CACHE_BYTES = 100 * 1024;
 
 constexpr float CE_LOG2E = 1.4426950408889634f;
-constexpr float CE_LN2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -129,9 +129,12 @@ crossentropy_kernel(float* __restrict__ losses, float* __restrict__ z, __nv_bflo
 // bf16 logits, gradient written in place (bf16).  One block per row: the row
 // is staged once into shared memory with 16-byte asynchronous copies, so DRAM
 // sees one read and one write of two bytes per logit.  Pass 1 takes the row
-// maximum, pass 2 the sum of exponentials (both from shared memory), pass 3
-// writes the gradient.  Two blocks per SM: one row's copy overlaps the other
-// row's arithmetic.
+// maximum M; pass 2 computes e = exp(z - M) once per logit, sums it, and keeps
+// it in shared memory over the logit as fp16 (e is in (0, 1]; fp16's 11-bit
+// significand is finer than the bf16 gradient it feeds; e below 2^-24 becomes
+// 0, a gradient term below 2^-24 / positions); pass 3 writes the gradient
+// e / sum - [v == target], scaled.  One exponential per logit.  Two blocks per
+// SM: one row's copy overlaps the other row's arithmetic.
 constexpr int CE16_THREADS = 512;
 constexpr int CE16_MAX_ROW_BYTES = GPT2_CE_BF16_MAX_LD * 2;   // 110 KB: two rows per SM
 
@@ -145,8 +148,23 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
     }
 }
 
+__device__ __forceinline__ void unpack8_h(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack2_h(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
@@ -154,7 +172,7 @@ __global__ void __launch_bounds__(CE16_THREADS, 2)
 crossentropy_bf16_kernel(float* __restrict__ losses, __nv_bfloat16* __restrict__ z,
                          const int* __restrict__ tgt, int V, int ld, float dscale, int* status) {
     __shared__ float sh[CE16_THREADS / 32];
-    extern __shared__ uint4 zs[];                   // the row, 8 logits per entry
+    extern __shared__ uint4 zs[];                   // the row, 8 logits per entry; later 8 fp16 e values
     const int row = blockIdx.x, tid = threadIdx.x;
     const int n8 = ld >> 3, nfull = V >> 3;         // 16-byte chunks: in the row, entirely inside [0, V)
     uint4* zr = reinterpret_cast<uint4*>(z + (size_t)row * ld);
@@ -165,6 +183,10 @@ crossentropy_bf16_kernel(float* __restrict__ losses, __nv_bfloat16* __restrict__
     asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
     __syncthreads();
     const __nv_bfloat16* zsh = reinterpret_cast<const __nv_bfloat16*>(zs);
+    __half* esh = reinterpret_cast<__half*>(zs);
+    const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    const float zt = ok ? __bfloat162float(zsh[t]) : 0.f;   // read before the row is overwritten
     float mx = -INFINITY;
     for (int c = tid; c < nfull; c += CE16_THREADS) {
         float f[8];
@@ -173,7 +195,7 @@ crossentropy_bf16_kernel(float* __restrict__ losses, __nv_bfloat16* __restrict__
         for (int k = 0; k < 8; k++) mx = fmaxf(mx, f[k]);
     }
     for (int v = nfull * 8 + tid; v < V; v += CE16_THREADS) mx = fmaxf(mx, __bfloat162float(zsh[v]));
-    const float M = block_reduce(mx, sh, true);
+    const float M = block_reduce(mx, sh, true);     // its barriers also order the read of zsh[t]
     const float ml = M * CE_LOG2E;
     float sum = 0.f;
     for (int c = tid; c < nfull; c += CE16_THREADS) {
@@ -181,29 +203,32 @@ crossentropy_bf16_kernel(float* __restrict__ losses, __nv_bfloat16* __restrict__
         unpack8(zs[c], f);
         float s2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 8; k++) s2[k & 1] += exp2f(fmaf(f[k], CE_LOG2E, -ml));
+        for (int k = 0; k < 8; k++) {
+            f[k] = exp2f(fmaf(f[k], CE_LOG2E, -ml));
+            s2[k & 1] += f[k];
+        }
         sum += s2[0] + s2[1];
+        zs[c] = make_uint4(pack2_h(f[0], f[1]), pack2_h(f[2], f[3]), pack2_h(f[4], f[5]), pack2_h(f[6], f[7]));
     }
-    for (int v = nfull * 8 + tid; v < V; v += CE16_THREADS)
-        sum += exp2f(fmaf(__bfloat162float(zsh[v]), CE_LOG2E, -ml));
-    const float S = block_reduce(sum, sh, false);
-    const float lse = M + logf(S);
-    const int t = tgt[row];
-    const bool ok = t >= 0 && t < V;
+    for (int v = nfull * 8 + tid; v < V; v += CE16_THREADS) {
+        const float e = exp2f(fmaf(__bfloat162float(zsh[v]), CE_LOG2E, -ml));
+        sum += e;
+        esh[v] = __float2half_rn(e);
+    }
+    const float S = block_reduce(sum, sh, false);   // also: every e is in shared memory
     if (tid == 0) {
         if (!ok) set_status(status, GPT2_STATUS_BAD_TARGET);
-        losses[row] = ok ? lse - __bfloat162float(zsh[t]) : 0.f;
+        losses[row] = ok ? M + logf(S) - zt : 0.f;
     }
     if (dscale == 0.f) return;
-    const float lsel = lse * CE_LOG2E;
+    const float pscale = dscale / S;
     for (int c = tid; c < n8; c += CE16_THREADS) {
         float f[8];
-        unpack8(zs[c], f);
+        unpack8_h(zs[c], f);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
             const int idx = c * 8 + k;
-            const float p = exp2f(fmaf(f[k], CE_LOG2E, -lsel));
-            f[k] = (idx < V && ok) ? (p - (idx == t ? 1.f : 0.f)) * dscale : 0.f;
+            f[k] = (idx < V && ok) ? f[k] * pscale - (idx == t ? dscale : 0.f) : 0.f;
         }
         zr[c] = make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
     }
