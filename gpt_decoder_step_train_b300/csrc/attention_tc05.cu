@@ -9,9 +9,9 @@
 //
 // One CTA per (query tile of 128 rows, head, batch), 320 threads, two CTAs per SM:
 //   warp 0   TMA producer: the Q tile once, then K and V tiles of 64 keys
-//            into a four-stage ring (128-byte swizzle);
-//   warp 1   allocates tensor memory (S: 64 columns, O: 64 columns) and from
-//            one lane issues S = Q K^T (M=128, N=64, K=64) and O += P V
+//            into a three-stage ring (128-byte swizzle);
+//   warp 1   allocates tensor memory (S: two buffers of 64 columns, O: 64
+//            columns) and from one lane issues S = Q K^T (M=128, N=64, K=64) and O += P V
 //            (M=128, N=64, K=64; P from shared memory, V read MN-major);
 //   warps 2-9  softmax, one query row per thread (its TMEM lane), two warps
 //            per row (32 key columns each, the row maximum combined through
@@ -23,8 +23,9 @@
 //            At the end O / l goes out as bf16 and the log-sum-exp as fp32.
 // Key tiles past the query tile's last row are never visited (causal tile
 // skipping).  While the softmax warps work on S_j, the tensor cores compute
-// S_{j+1} (the scores are in registers by then) and P_{j-1} V_{j-1}; the MMA
-// thread issues each group the moment its inputs are ready.
+// S_{j+1} into the other score buffer and P_{j-1} V_{j-1} (P is double-buffered
+// in shared memory too), so the softmax warps wait on the tensor cores only
+// when O must be rescaled.
 // Every wait is bounded (about one second); a wait that gives up raises
 // GPT2_STATUS_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // and tensor memory is freed.
@@ -51,7 +52,7 @@ constexpr int FWD_THREADS = 64 + 32 * FWD_EW_WARPS;
 // TMEM lane quarter, one per half of the tile's 64 columns)
 constexpr int BWD_EW_WARPS = 8;
 constexpr int BWD_THREADS = 64 + 32 * BWD_EW_WARPS;
-constexpr int TMEM_COLS = 128;      // S: [0, 64), O: [64, 128)
+constexpr int TMEM_COLS = 256;      // S (two buffers): [0, 64), [64, 128); O: [128, 192)
 constexpr uint32_t TILE_BYTES = BKV * HS * 2;     // one K or V tile: 8 KB
 constexpr uint32_t Q_BYTES = BQ * HS * 2;         // 16 KB
 constexpr uint32_t P_BYTES = BQ * BKV * 2;        // 16 KB
@@ -92,45 +93,39 @@ __device__ __forceinline__ void store_colsum(float* colsum, float (&v)[32], int 
 
 // Issue loop of the MMA thread.  Each tile j has two groups of MMAs:
 //   A  needs the tile's operand stage (full[j % stages], phase (j / stages) & 1)
-//      and the score columns released by the element-wise warps after tile
-//      j - 1 (s_free, phase (j - 1) & 1);
+//      and its score columns, buffer j % ns of ns, released by the element-wise
+//      warps after tile j - ns (s_free[j % ns], phase ((j - ns) / ns) & 1);
 //   B  needs the element-wise warps' operand tile of tile j (p_full[j % np],
 //      phase (j / np) & 1; np operand buffers used in turn).
-// Each group is issued as soon as its inputs are ready, so B of tile j, which
-// frees the tile's stage, never waits for A of tile j + 1 and its copies.  No
-// phase can be lapped: every barrier's next phase needs this thread to consume
-// the current one first.  Gives up (abort flag, GPT2_STATUS_TIMEOUT) when
-// nothing becomes ready for WAIT_NS.
+// Issue order A(0), A(1), B(0), A(2), B(1), ...: the scores of tile j + 1 are
+// computed while the element-wise warps work on tile j (with ns = 2 the
+// element-wise warps never wait for them: the buffer of tile j + 1 was
+// released two tiles earlier).  Every wait blocks
+// (the thread is suspended, taking no issue slots from the element-wise warps
+// on its scheduler) and is bounded.  No deadlock: A(j + 1) needs only the
+// release of S_{j+1-ns}, which the warps give before they wait for B(j - 1); no phase
+// can be lapped, since every barrier's next phase needs this thread to have
+// consumed the current one.  Gives up (abort flag, GPT2_STATUS_TIMEOUT) when a
+// wait runs out.
 template <class IssueA, class IssueB>
-__device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int stages, uint64_t* s_free,
+__device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int stages, uint64_t* s_free, int ns,
                                                    uint64_t* p_full, int np, volatile int* abort_flag, int* status,
                                                    IssueA&& issue_a, IssueB&& issue_b) {
-    int ja = 0, jb = 0;
-    uint64_t t0 = globaltimer();
-    uint32_t spins = 0;
-    while (jb < n) {
-        bool moved = false;
-        if (ja < n && mbar_test_wait(smem_u32(&full[ja % stages]), (uint32_t)(ja / stages) & 1u) &&
-            (ja == 0 || mbar_test_wait(smem_u32(s_free), (uint32_t)(ja - 1) & 1u))) {
-            tc_fence_after();
-            issue_a(ja++);
-            moved = true;
-        }
-        if (jb < ja && mbar_test_wait(smem_u32(&p_full[jb % np]), (uint32_t)(jb / np) & 1u)) {
-            tc_fence_after();
-            issue_b(jb++);
-            moved = true;
-        }
-        if (moved) {
-            t0 = globaltimer();
-            spins = 0;
-        } else if ((++spins & 255) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_NS) {
-                *abort_flag = 1;
-                set_status(status, GPT2_STATUS_TIMEOUT);
+    for (int j = 0; j <= n; j++) {
+        if (j < n) {
+            if (!mbar_wait(smem_u32(&full[j % stages]), (uint32_t)(j / stages) & 1u, abort_flag, status))
                 return false;
-            }
+            if (j >= ns &&
+                !mbar_wait(smem_u32(&s_free[j % ns]), (uint32_t)((j - ns) / ns) & 1u, abort_flag, status))
+                return false;
+            tc_fence_after();
+            issue_a(j);
+        }
+        if (j > 0) {
+            const int jb = j - 1;
+            if (!mbar_wait(smem_u32(&p_full[jb % np]), (uint32_t)(jb / np) & 1u, abort_flag, status)) return false;
+            tc_fence_after();
+            issue_b(jb);
         }
     }
     return true;
@@ -140,7 +135,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
               int T, int C, int H, float scale_log2, int* status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full, s_free, p_full[2],
+    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], s_free[2], p_full[2],
         pv_done[2], drain;
     __shared__ __align__(8) uint64_t pair_bar[4][2];
     __shared__ float pair_val[2][2][BQ];
@@ -165,8 +160,10 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             mbar_init(smem_u32(&kv_full[s]), 1);
             mbar_init(smem_u32(&kv_empty[s]), 1);
         }
-        mbar_init(smem_u32(&s_full), 1);
-        mbar_init(smem_u32(&s_free), FWD_EW_WARPS);
+        for (int k = 0; k < 2; k++) {
+            mbar_init(smem_u32(&s_full[k]), 1);
+            mbar_init(smem_u32(&s_free[k]), FWD_EW_WARPS);
+        }
         for (int k = 0; k < 2; k++) {
             mbar_init(smem_u32(&p_full[k]), FWD_EW_WARPS);
             mbar_init(smem_u32(&pv_done[k]), 1);
@@ -230,15 +227,15 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
         if (lane == 0) {
             const uint32_t id_s = instr_desc(BQ, BKV, false, false, true);   // Q K^T: both K-major
             const uint32_t id_pv = instr_desc(BQ, HS, false, true, true);    // P V: V MN-major
-            const uint32_t t_s = tmem, t_o = tmem + BKV;
+            const uint32_t t_s = tmem, t_o = tmem + 2 * BKV;   // S_j in columns (j & 1) * 64
             if (mbar_wait(smem_u32(&q_full), 0, &s_abort, status)) {
                 auto issue_s = [&](int j) {            // S = Q K_j^T
                     const uint32_t kb = base + OFF_K + (j % KV_STAGES) * TILE_BYTES;
 #pragma unroll
                     for (int k = 0; k < HS / 16; k++)
-                        mma_issue<true>(t_s, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
+                        mma_issue<true>(t_s + (uint32_t)(j & 1) * BKV, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
                                         smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
-                    mma_commit(smem_u32(&s_full));
+                    mma_commit(smem_u32(&s_full[j & 1]));
                 };
                 auto issue_pv = [&](int j) {           // O += P_j V_j (P_j in buffer j & 1)
                     const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
@@ -251,7 +248,7 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
                     mma_commit(smem_u32(&pv_done[j & 1]));
                     mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
                 };
-                mma_two_group_loop(nkv, kv_full, KV_STAGES, &s_free, p_full, 2, &s_abort, status, issue_s, issue_pv);
+                mma_two_group_loop(nkv, kv_full, KV_STAGES, s_free, 2, p_full, 2, &s_abort, status, issue_s, issue_pv);
             }
             // every MMA issued has completed once this commit lands
             mma_commit(smem_u32(&drain));
@@ -270,7 +267,7 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
         const int r = quarter * 32 + lane;             // row within the tile
         const int row = q0 + r;
         const uint32_t lane_base = ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half);
-        const uint32_t t_s = tmem + lane_base, t_o = tmem + lane_base + BKV;
+        const uint32_t t_s = tmem + lane_base, t_o = tmem + lane_base + 2 * BKV;
         uint8_t* const pbuf = base_ptr + OFF_P;    // two P buffers, tile j in buffer j & 1
         float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, this half's sum of P
         bool ok = true;
@@ -285,14 +282,14 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             return true;
         };
         for (int j = 0; j < nkv; j++) {
-            if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(&s_full[j & 1]), (uint32_t)(j >> 1) & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
             float s[32];
-            tmem_ld32(t_s, s);
+            tmem_ld32(t_s + (uint32_t)(j & 1) * BKV, s);
             tmem_wait_ld(s);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free));
+            if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
             // mask (tiles that reach the diagonal or the sequence end), row maximum
             // of the raw scores; the scale goes into the exponent's FMA
             const int k0 = j * BKV + 32 * half;        // first key of this warp's columns
@@ -567,7 +564,7 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mma_commit(smem_u32(&pv_done));
                     mma_commit(smem_u32(&q_empty[t % DKV_STAGES]));
                 };
-                mma_two_group_loop(ntile, q_full, DKV_STAGES, &s_free, &p_full, 1, &s_abort, status, issue_s, issue_o);
+                mma_two_group_loop(ntile, q_full, DKV_STAGES, &s_free, 1, &p_full, 1, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();
@@ -793,7 +790,7 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     mma_commit(smem_u32(&pv_done));
                     mma_commit(smem_u32(&kv_empty[j % DQ_STAGES]));
                 };
-                mma_two_group_loop(nkv, kv_full, DQ_STAGES, &s_free, &p_full, 1, &s_abort, status, issue_s, issue_o);
+                mma_two_group_loop(nkv, kv_full, DQ_STAGES, &s_free, 1, &p_full, 1, &s_abort, status, issue_s, issue_o);
             }
             mma_commit(smem_u32(&drain));
             const uint64_t t0 = globaltimer();

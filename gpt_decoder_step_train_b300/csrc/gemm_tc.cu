@@ -51,25 +51,25 @@ struct Elem {
     static constexpr int BOX_BYTES = 128 * BK;        // 4 KB or 8 KB
 };
 
-// Epilogue staging: each epilogue warp owns EPI_WARP_BYTES of shared memory,
-// cut into boxes of 32 rows x EC columns (1 KB bf16, 2 KB fp32).
+// Epilogue staging: each epilogue warp owns Shape::EPI_WARP bytes of shared
+// memory (4 KB, or 8 KB on CTA pairs), cut into boxes of 32 rows x EC columns
+// (1 KB bf16, 2 KB fp32).
 constexpr int EC = 16;
-constexpr int EPI_WARP_BYTES = 4096;
-constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 
 // PAIR: two CTAs of a cluster share a 256-row tile through cta_group::2 MMAs;
 // each holds 128 rows of A and BN/2 rows of B per stage, and 128 rows of the
 // accumulator.
 template <int BN, bool BF16, bool PAIR = false>
 struct Shape {
-    static constexpr int STAGES = PAIR ? 6 : (BN == 256 ? 4 : 6);
+    static constexpr int STAGES = PAIR ? 5 : (BN == 256 ? 4 : 6);
+    static constexpr int EPI_WARP = PAIR ? 8192 : 4096;   // epilogue bytes per warp
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // rows of A per tile
     static constexpr int A_BYTES = BM * 128;          // BM rows x 128 bytes
     static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + EPI_BYTES;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + EPI_WARPS * EPI_WARP;
 };
 
 struct Params {
@@ -207,7 +207,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     static_assert(!PAIR || (BF16 && BN == 256), "CTA pairs: bf16, 256-column tiles");
     using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
-    constexpr int RING_MAX = EPI_WARP_BYTES / 1024;   // input boxes per warp (bf16 boxes)
+    constexpr int RING_MAX = S::EPI_WARP / 1024;      // input boxes per warp (bf16 boxes)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[S::STAGES], empty_bar[S::STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, aux_bar[EPI_WARPS][RING_MAX];
@@ -379,17 +379,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int ew = warp - 2;
         const int col_lo = (ew >> 2) * (BN / 2);     // this warp's half of the tile's columns
-        uint8_t* const wbuf = base_ptr + S::STAGES * S::STAGE_BYTES + ew * EPI_WARP_BYTES;
+        uint8_t* const wbuf = base_ptr + S::STAGES * S::STAGE_BYTES + ew * S::EPI_WARP;
         const bool has_aux = p.has_aux != 0;
         const bool pre = p.gelu && !p.partial;
         const bool out16 = p.out_bf16 != 0, pre16 = p.pre_bf16 != 0, aux16 = p.aux_bf16 != 0;
         const int out_bytes = out16 ? 1024 : 2048;
         // output boxes (no input tile): one chunk = output box (+ pre-activation box)
         const int chunk_bytes = out_bytes + (pre ? (pre16 ? 1024 : 2048) : 0);
-        const int nbuf = chunk_bytes <= 1024 ? 4 : chunk_bytes <= 2048 ? 2 : 1;
+        const int nbuf = min(8, S::EPI_WARP / chunk_bytes);     // 1, 2, 4 or 8
         // input ring: box g of this warp's sequence uses slot g % ring, phase (g / ring) & 1
         const int aux_bytes = aux16 && !p.aux_residual ? 1024 : 2048;
-        const int ring = EPI_WARP_BYTES / aux_bytes;
+        const int ring = S::EPI_WARP / aux_bytes;
         uint32_t box_seq = 0;                // output chunks stored so far
         uint32_t aux_issued = 0;             // input boxes requested (lane 0)
         uint32_t aux_seq = 0;                // input boxes consumed
@@ -421,6 +421,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int k = 0; k < BN / 2 && nn0 + k < p.N; k += EC) tma_prefetch_l2(&tmAux, nn0 + k, nr0);
                 }
             }
+            // the bias of this warp's columns: lane l holds columns n0 + 4l .. n0 + 4l + 3
+            // (loaded before the accumulator is ready; shuffled out chunk by chunk)
+            float4 bl = make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool use_bias = !p.partial && p.bias;
+            if (use_bias && 4 * lane < BN / 2) {
+                const int c0 = n0 + 4 * lane;
+                if (c0 + 4 <= p.N) {
+                    bl = __ldg(reinterpret_cast<const float4*>(p.bias + c0));
+                } else {
+                    if (c0 < p.N) bl.x = __ldg(p.bias + c0);
+                    if (c0 + 1 < p.N) bl.y = __ldg(p.bias + c0 + 1);
+                    if (c0 + 2 < p.N) bl.z = __ldg(p.bias + c0 + 2);
+                }
+            }
             if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, p.status)) {
                 ok = false;
                 break;
@@ -435,17 +449,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 float x[16];
 #pragma unroll
                 for (int j = 0; j < 16; j++) x[j] = __uint_as_float(r[j]);
-                if (!p.partial && p.bias) {
-                    if (nc + EC <= p.N) {
-                        const float4* b4 = reinterpret_cast<const float4*>(p.bias + nc);
+                if (use_bias) {
 #pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const float4 bv = __ldg(b4 + j);
-                            x[4 * j] += bv.x; x[4 * j + 1] += bv.y; x[4 * j + 2] += bv.z; x[4 * j + 3] += bv.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; j++) x[j] += nc + j < p.N ? __ldg(p.bias + nc + j) : 0.f;
+                    for (int j = 0; j < 4; j++) {
+                        const int src = 4 * k + j;       // the lane holding columns nc + 4j .. nc + 4j + 3
+                        x[4 * j] += __shfl_sync(0xffffffffu, bl.x, src);
+                        x[4 * j + 1] += __shfl_sync(0xffffffffu, bl.y, src);
+                        x[4 * j + 2] += __shfl_sync(0xffffffffu, bl.z, src);
+                        x[4 * j + 3] += __shfl_sync(0xffffffffu, bl.w, src);
                     }
                 }
                 uint8_t* outb;

@@ -158,9 +158,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// at most n (0, 1 or 3) committed store groups may still be reading shared memory
+// at most n (0, 1, 3 or 7) committed store groups may still be reading shared memory
 __device__ __forceinline__ void bulk_wait_read(int n) {
-    if (n >= 3) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+    if (n >= 7) asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory");
+    else if (n >= 3) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
     else if (n == 1) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
     else asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
