@@ -49,6 +49,8 @@ SIGNATURES = {
     "gpt2_workspace_bytes": (_sz, [_vp]),
     "gpt2_create": (_i, [_vp, _vp, _vp]),
     "gpt2_forward": (_f, [_vp, _vp, _vp, _i, _i]),
+    "gpt2_eval": (_f, [_vp, _vp, _vp, _i, _i]),
+    "gpt2_decode": (_i, [_vp, _vp, _i, _i, _vp]),
     "gpt2_backward": (_i, [_vp]),
     "gpt2_adamw": (_i, [_vp, _f, _f, _f, _f, _f, _i]),
     "gpt2_destroy": (_i, [_vp]),
@@ -88,6 +90,7 @@ SIGNATURES = {
                                         _vp, _vp]),
     "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_crossentropy_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
+    "gpt2_op_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp]),
     "gpt2_op_sum": (_i, [_vp, _vp, _i, _f, _vp]),
     "gpt2_op_adamw": (_i, [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _f, _f, _vp]),
 }
@@ -185,6 +188,15 @@ class GPT2:
     def forward(self, tokens, targets=None):
         B, T = tokens.shape
         return lib().gpt2_forward(self.h, ptr(tokens), ptr(targets), B, T)
+
+    def eval(self, tokens, targets):
+        """Mean loss only (no gradient of the logits is left for a backward)."""
+        B, T = tokens.shape
+        return lib().gpt2_eval(self.h, ptr(tokens), ptr(targets), B, T)
+
+    def decode(self, tokens, pos, logits):
+        """Advance len(tokens) sequences by one position; logits [B, V] (device) receives the new row."""
+        return lib().gpt2_decode(self.h, ptr(tokens), int(tokens.shape[0]), pos, ptr(logits))
 
     def backward(self):
         return lib().gpt2_backward(self.h)

@@ -774,7 +774,7 @@ template <bool BF16>
 static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
                       cudaStream_t st) {
     if constexpr (BF16)
-        if (gemm_tc_pair(g)) return launch<256, true, true>(g, e, partial, split, st);
+        if (gemm_tc_pair(g, partial ? nullptr : &e)) return launch<256, true, true>(g, e, partial, split, st);
     if (g.N <= 128) return launch<128, BF16, false>(g, e, partial, split, st);
     return launch<256, BF16, false>(g, e, partial, split, st);
 }
@@ -782,15 +782,20 @@ static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partia
 }  // namespace tc
 
 // bf16 products with at least 256 rows and 256 columns run on CTA pairs
-// (cta_group::2, 256 x 256 tiles) unless GPT2_GEMM_CTA_PAIRS=0 is set in the
-// environment (the single-CTA kernel, 128 x 256 tiles, then takes them).
-bool gemm_tc_pair(const GemmProblem& g) {
+// (cta_group::2, 256 x 256 tiles) when the reduction is long (K >= 2048) or the
+// epilogue only converts and stores; short products with a bias, GELU, residual
+// or GELU' epilogue run on single CTAs (128 x 256 tiles), which measured faster
+// for them.  GPT2_GEMM_CTA_PAIRS=0 in the environment sends everything to
+// single CTAs.
+bool gemm_tc_pair(const GemmProblem& g, const GemmEpilogue* e) {
     static int on = -1;
     if (on < 0) {
         const char* v = getenv("GPT2_GEMM_CTA_PAIRS");
         on = (v && v[0] == '0') ? 0 : 1;
     }
-    return on && g.bf16 && g.M >= 256 && g.N >= 256 && tc::pair_clusters() > 0;
+    if (!on || !g.bf16 || g.M < 256 || g.N < 256 || tc::pair_clusters() <= 0) return false;
+    const bool plain = !e || (!e->bias && !e->residual && !e->gelu_x && !e->gelu);
+    return g.K >= 2048 || plain;
 }
 
 int gemm_tc_pair_slots() { return tc::pair_clusters(); }

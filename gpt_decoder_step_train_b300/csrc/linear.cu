@@ -155,7 +155,7 @@ static int dw_split(int N, int IC, int OC, int mode) {
     // the product is M = OC, N = IC, K = N rows; CTA pairs take 256 x 256 tiles
     // (a pair moves through a k-block in the time one CTA takes for 128 x 256)
     GemmProblem probe{OC, IC, N, nullptr, 0, false, nullptr, 0, false, nullptr, mode == GPT2_MODE_BF16};
-    const bool pair = gemm_tc_pair(probe);
+    const bool pair = gemm_tc_pair(probe, nullptr);
     const int bm = pair ? 256 : 128, bn = (IC <= 128 && !pair) ? 128 : 256;
     const long long tiles = (long long)ceil_div(OC, bm) * ceil_div(IC, bn);
     const int nkb = ceil_div(N, mode == GPT2_MODE_BF16 ? 64 : 32);

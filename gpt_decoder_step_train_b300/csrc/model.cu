@@ -106,6 +106,12 @@ struct gpt2 {
     size_t scratch_bytes;
     float* colsum;              // per-32-row column sums for the fused bias gradients
     size_t colsum_bytes;
+    // decoding: key/value cache [L][maxB][maxT][2C] and the rows of one step,
+    // allocated by the first gpt2_decode
+    char* dec;
+    float *kv, *sx, *sx2, *sln, *sqkv, *satt, *sh, *smean, *srstd;
+    int* stok;
+    int dec_B, dec_next;
     int B, T;
     bool fwd_targets, have_grads;
     int err;
@@ -223,7 +229,8 @@ static int trace_op(gpt2* m, int cls, const std::function<int()>& f) {
         if (rc_) return rc_;                                               \
     } while (0)
 
-static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
+// with_targets: the cross-entropy runs; grad: it also leaves d(loss)/d(logits)
+static int forward_impl(gpt2* m, int B, int T, bool with_targets, bool grad) {
     const gpt2_config& c = m->cfg;
     const int C = c.C, L = c.L, H = c.H, N = B * T, mode = c.mode;
     const bool b16 = m->bf16;
@@ -270,14 +277,14 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets) {
         // columns are zeroed there), the operand of the lm_head backward
         OP(MATMUL_FWD, linear_forward(m->dz16, true, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N, C,
                                       c.V, m->Vp, 0, mode, status, st));
-        OP(CROSSENTROPY, gpt2_op_crossentropy_bf16(m->losses, m->dz16, m->tgt, N, c.V, m->Vp, 1.0f / (float)N,
-                                                   status, st));
+        OP(CROSSENTROPY, gpt2_op_crossentropy_bf16(m->losses, m->dz16, m->tgt, N, c.V, m->Vp,
+                                                   grad ? 1.0f / (float)N : 0.f, status, st));
     } else {
         OP(MATMUL_FWD, linear_forward(m->logits, false, nullptr, m->lnf, W(m, WTE), b16, nullptr, nullptr, N,
                                       C, c.V, m->Vp, GPT2_LINEAR_ZERO_PAD, mode, status, st));
         if (with_targets)
             OP(CROSSENTROPY, gpt2_op_crossentropy(m->losses, m->logits, m->dz16, m->tgt, N, c.V, m->Vp,
-                                                  1.0f / (float)N, status, st));
+                                                  grad ? 1.0f / (float)N : 0.f, status, st));
     }
     if (with_targets) OP(CROSSENTROPY, gpt2_op_sum(&m->flags->loss, m->losses, N, 1.0f / (float)N, st));
     return GPT2_OK;
@@ -439,7 +446,8 @@ GPT2_API int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out) {
     return GPT2_OK;
 }
 
-GPT2_API float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int B, int T) {
+namespace gpt2k {
+static float forward_common(gpt2* m, const int* tokens, const int* targets, int B, int T, bool grad) {
     if (!m) return NAN;
     if (!tokens || B < 1 || T < 1 || B > m->cfg.maxB || T > m->cfg.maxT) {
         record(m, GPT2_EINVAL);
@@ -462,7 +470,7 @@ GPT2_API float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int 
     }
     m->B = B;
     m->T = T;
-    int rc = forward_impl(m, B, T, targets != nullptr);
+    int rc = forward_impl(m, B, T, targets != nullptr, grad);
     if (rc) { record(m, rc); return NAN; }
     DevFlags h{};
     if (cudaMemcpyAsync(&h, m->flags, sizeof(h), cudaMemcpyDeviceToHost, m->st) != cudaSuccess ||
@@ -480,8 +488,21 @@ GPT2_API float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int 
         return NAN;
     }
     if (!targets) return NAN;
-    m->fwd_targets = true;
+    m->fwd_targets = grad;
     return h.loss;
+}
+}  // namespace gpt2k
+
+GPT2_API float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int B, int T) {
+    return forward_common(m, tokens, targets, B, T, true);
+}
+
+GPT2_API float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, int T) {
+    if (m && !targets) {
+        record(m, GPT2_EINVAL);
+        return NAN;
+    }
+    return forward_common(m, tokens, targets, B, T, false);
 }
 
 GPT2_API int gpt2_backward(gpt2* m) {
@@ -517,11 +538,92 @@ GPT2_API int gpt2_adamw(gpt2* m, float lr, float b1, float b2, float eps, float 
     return GPT2_OK;
 }
 
+namespace gpt2k {
+constexpr int DECODE_MAXB = 16;
+
+// Carve the decoding state (cache and step rows) from one allocation.
+static int decode_alloc(gpt2* m) {
+    const gpt2_config& c = m->cfg;
+    const size_t C = c.C, RB = DECODE_MAXB;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += round_up(bytes, 256); return o; };
+    const size_t o_kv = take((size_t)c.L * c.maxB * c.maxT * 2 * C * sizeof(float));
+    const size_t o_x = take(RB * C * 4), o_x2 = take(RB * C * 4), o_ln = take(RB * C * 4);
+    const size_t o_qkv = take(RB * 3 * C * 4), o_att = take(RB * C * 4), o_h = take(RB * 4 * C * 4);
+    const size_t o_mu = take(RB * 4), o_rs = take(RB * 4), o_tok = take(RB * 4);
+    if (cudaMalloc(&m->dec, off) != cudaSuccess) { (void)cudaGetLastError(); m->dec = nullptr; return GPT2_ENOMEM; }
+    auto F = [&](size_t o) { return reinterpret_cast<float*>(m->dec + o); };
+    m->kv = F(o_kv); m->sx = F(o_x); m->sx2 = F(o_x2); m->sln = F(o_ln); m->sqkv = F(o_qkv);
+    m->satt = F(o_att); m->sh = F(o_h); m->smean = F(o_mu); m->srstd = F(o_rs);
+    m->stok = reinterpret_cast<int*>(m->dec + o_tok);
+    return GPT2_OK;
+}
+
+static int decode_impl(gpt2* m, int B, int pos, float* logits) {
+    const gpt2_config& c = m->cfg;
+    const int C = c.C, L = c.L, H = c.H;
+    cudaStream_t st = m->st;
+    int* status = &m->flags->status;
+    int rc = decode_embed(m->sx, m->stok, P(m, WTE), P(m, WPE), B, C, c.V, pos, status, st);
+    for (int l = 0; l < L && !rc; l++) {
+        const size_t cc = (size_t)C * C;
+        float* kv = m->kv + (size_t)l * c.maxB * c.maxT * 2 * C;
+        rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx, P(m, LN1W) + l * C, P(m, LN1B) + l * C,
+                               B, C, st);
+        if (!rc) rc = decode_gemv(m->sqkv, 3 * C, m->sln, P(m, QKVW) + l * 3 * cc, P(m, QKVB) + l * 3 * C,
+                                  nullptr, B, C, 3 * C, 0, st);
+        if (!rc) rc = decode_kv_store(kv, m->sqkv, B, C, c.maxT, pos, st);
+        if (!rc) rc = decode_attention(m->satt, m->sqkv, kv, B, C, H, c.maxT, pos, st);
+        if (!rc) rc = decode_gemv(m->sx2, C, m->satt, P(m, ATTPROJW) + l * cc, P(m, ATTPROJB) + l * C, m->sx, B,
+                                  C, C, 0, st);
+        if (!rc) rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx2, P(m, LN2W) + l * C,
+                                        P(m, LN2B) + l * C, B, C, st);
+        if (!rc) rc = decode_gemv(m->sh, 4 * C, m->sln, P(m, FCW) + l * 4 * cc, P(m, FCB) + l * 4 * C, nullptr,
+                                  B, C, 4 * C, 1, st);
+        if (!rc) rc = decode_gemv(m->sx, C, m->sh, P(m, FCPROJW) + l * 4 * cc, P(m, FCPROJB) + l * C, m->sx2,
+                                  B, 4 * C, C, 0, st);
+    }
+    if (!rc) rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx, P(m, LNFW), P(m, LNFB), B, C, st);
+    if (!rc) rc = decode_gemv(logits, c.V, m->sln, P(m, WTE), nullptr, nullptr, B, C, c.V, 0, st);
+    return rc;
+}
+}  // namespace gpt2k
+
+GPT2_API int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logits) {
+    if (!m) return GPT2_EINVAL;
+    const int maxb = std::min(m->cfg.maxB, DECODE_MAXB);
+    if (!tokens || !logits || B < 1 || B > maxb || pos < 0 || pos >= std::min(m->cfg.maxT, 1024) ||
+        m->cfg.C / m->cfg.H > 64) {
+        record(m, GPT2_EINVAL);
+        return GPT2_EINVAL;
+    }
+    if (pos > 0 && (B != m->dec_B || pos != m->dec_next)) {
+        record(m, GPT2_ESTATE);
+        return GPT2_ESTATE;
+    }
+    if (!m->dec) {
+        int rc = decode_alloc(m);
+        if (rc) { record(m, rc); return rc; }
+    }
+    if (cudaMemcpyAsync(m->stok, tokens, (size_t)B * sizeof(int), cudaMemcpyDefault, m->st) != cudaSuccess) {
+        (void)cudaGetLastError();
+        record(m, GPT2_ECUDA);
+        return GPT2_ECUDA;
+    }
+    m->fwd_targets = false;                 // the step rows are not a training forward
+    int rc = decode_impl(m, B, pos, logits);
+    if (rc) { record(m, rc); m->dec_next = -1; return rc; }
+    m->dec_B = B;
+    m->dec_next = pos + 1;
+    return GPT2_OK;
+}
+
 GPT2_API int gpt2_destroy(gpt2* m) {
     if (!m) return GPT2_OK;
     int rc = GPT2_OK;
     if (cudaStreamSynchronize(m->st) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->owns_ws && cudaFree(m->ws) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    if (m->dec && cudaFree(m->dec) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     for (cudaEvent_t e : m->trace_events) cudaEventDestroy(e);
     delete m;
     return rc;

@@ -108,6 +108,34 @@ int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out);
  * ECUDA).  Synchronises the stream once to read the loss. */
 float gpt2_forward(gpt2* m, const int* tokens, const int* targets, int B, int T);
 
+/* Forward-only evaluation: the mean cross-entropy of tokens[B,T] against
+ * targets[B,T] (both required; same layout and rules as gpt2_forward), without
+ * d(loss)/d(logits): the validation loss of the training loop ("1000 行 C 代码
+ * 完成 GPT-2 训练的 LLM.c", section 快速开始吧: the run log reports a validation
+ * loss before the first step and every few steps).  The same
+ * kernels as gpt2_forward; the cross-entropy skips the gradient pass.  A
+ * following gpt2_backward returns ESTATE.  Returns NaN on error (EINVAL,
+ * ETOKEN, ECUDA via gpt2_status).  Synchronises the stream once. */
+float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, int T);
+
+/* Autoregressive decoding with a key/value cache: advance B sequences
+ * (1 <= B <= min(maxB, 16)) by one position.  tokens[B] (device or host int32)
+ * are the tokens at position pos (0 <= pos < min(maxT, 1024)); pos 0 starts
+ * new sequences, every later call must continue them (same B, pos one more than
+ * the last call), else ESTATE.  The keys and values of every layer for position
+ * pos are appended to the cache (library memory, allocated by the first call:
+ * L * maxB * maxT * 2C floats; call it before any stream capture), and the
+ * logits of position pos are written to logits[B, V] (device, row stride V):
+ * exactly the last row of a full forward over positions 0..pos.  Computed in
+ * fp32 from the fp32 parameters in every mode.  Generation feeds the chosen
+ * token back at pos + 1 ("GPT-2 from scratch with torch", section 生成样本;
+ * only the new row is computed: "GPT-2ベースの3000バイトCで実装された
+ * ChatGPTクローン（2023）", section KVキャッシュ方式).  Asynchronous; an id
+ * outside [0, V) shows up as ETOKEN in gpt2_status.  A pending backward is
+ * dropped (the next gpt2_backward returns ESTATE).  Errors: EINVAL, ESTATE,
+ * ENOMEM, ECUDA. */
+int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logits);
+
 /* Backward pass of the last forward (which must have had targets).
  * Overwrites the gradient buffer (no accumulation across calls); gradients
  * are those of the mean loss.  Errors: ESTATE, ECUDA. */

@@ -208,6 +208,12 @@ int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const int* tgt,
 int gpt2_op_crossentropy_bf16(float* losses, void* z, const int* tgt, int N, int V, int ld,
                               float dscale, int* status, void* stream);
 
+/* Greedy token choice: out[n] = the index of the largest of logits[n, 0..V)
+ * (row stride ld >= V), the lowest index on ties; NaN entries never win (a row
+ * of NaN gives 0).  ("GPT-2 from scratch with torch", section 生成样本: the
+ * next token is taken from the highest scores of the last position.) */
+int gpt2_op_argmax(int* out, const float* logits, int N, int V, int ld, void* stream);
+
 /* Sum of losses[N] in a fixed order, times `scale`, written to *out (device). */
 int gpt2_op_sum(float* out, const float* losses, int N, float scale, void* stream);
 

@@ -197,3 +197,33 @@ def test_host_token_buffers_give_same_loss():
     c = model.forward(torch.from_numpy(tok), torch.from_numpy(tgt))   # pageable
     assert a == b == c
     model.close()
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+def test_eval_gives_the_forward_loss_and_no_gradient(mode):
+    """gpt2_eval: the same mean loss as the training forward (bit for bit: the
+    cross-entropy only skips its gradient pass), no backward after it, and in the
+    fp32 modes the logits are left as a forward without targets leaves them."""
+    from gpt_decoder_step_train_b300 import binding as B_
+    from gpt_decoder_step_train_b300.binding import GPT2
+    cfg = syn.CONFIGS["tiny"]
+    params = torch.from_numpy(syn.init_params(cfg)).cuda()
+    tok, tgt = syn.draw_tokens(cfg)
+    t_tok, t_tgt = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    model = GPT2(cfg, params, mode=mode)
+    train = model.forward(t_tok, t_tgt)
+    ev = model.eval(t_tok, t_tgt)
+    assert ev == train and np.isfinite(ev)
+    assert model.backward() == B_.GPT2_ESTATE
+    assert model.status() == B_.GPT2_ESTATE
+    if mode != "bf16":
+        z_eval = model.logits(cfg.B * cfg.T).cpu().numpy().copy()
+        model.forward(t_tok)                                   # no targets: logits kept
+        assert np.array_equal(model.logits(cfg.B * cfg.T).cpu().numpy(), z_eval)
+    # targets are required
+    assert np.isnan(model.eval(t_tok, None))
+    assert model.status() == B_.GPT2_EINVAL
+    # a training forward after an eval still trains
+    assert model.forward(t_tok, t_tgt) == train
+    assert model.backward() == 0
+    model.close()
