@@ -112,6 +112,17 @@ struct gpt2 {
     float *kv, *sx, *sx2, *sln, *sqkv, *satt, *sh, *smean, *srstd;
     int* stok;
     int dec_B, dec_next;
+    // CUDA graphs of the forward and backward, one per (kind, B, T), replayed on a
+    // private stream ordered after and before the caller's stream by events
+    struct Graph {
+        int kind, B, T, seen;
+        cudaGraphExec_t exec;
+        long long launches;
+    };
+    std::vector<Graph> graphs;
+    cudaStream_t gst;
+    cudaEvent_t g_in, g_out;
+    bool graphs_off;
     int B, T;
     bool fwd_targets, have_grads;
     int err;
@@ -380,6 +391,64 @@ static void record(gpt2* m, int rc) {
     if (rc && !m->err) m->err = rc;
 }
 
+// Run fn (the operations of a forward or backward, issued on m->st) through a
+// CUDA graph.  The first call of a (kind, B, T) runs fn directly (one-time
+// set-up happens outside any capture); the second captures it on the private
+// stream and later calls replay the graph.  Tracing, or a failed capture,
+// runs fn directly from then on.
+static int run_graphed(gpt2* m, int kind, int B, int T, const std::function<int()>& fn) {
+    if (m->trace_on || m->graphs_off || !m->gst) return fn();
+    // inside the caller's own stream capture the operations go into that graph
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(m->st, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fn();
+    }
+    if (cs != cudaStreamCaptureStatusNone) return fn();
+    gpt2::Graph* g = nullptr;
+    for (auto& e : m->graphs)
+        if (e.kind == kind && e.B == B && e.T == T) g = &e;
+    if (!g) {
+        m->graphs.push_back(gpt2::Graph{kind, B, T, 0, nullptr, 0});
+        g = &m->graphs.back();
+    }
+    if (!g->exec && g->seen++ == 0) return fn();
+    if (!g->exec) {
+        cudaStream_t user = m->st;
+        if (cudaStreamBeginCapture(m->gst, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+            (void)cudaGetLastError();
+            m->graphs_off = true;
+            return fn();
+        }
+        m->st = m->gst;
+        const long long n0 = g_launches.load(std::memory_order_relaxed);
+        int rc = fn();
+        const long long n = g_launches.load(std::memory_order_relaxed) - n0;
+        m->st = user;
+        cudaGraph_t graph = nullptr;
+        cudaError_t ce = cudaStreamEndCapture(m->gst, &graph);
+        g_launches.fetch_sub(n, std::memory_order_relaxed);     // counted when replayed
+        if (rc || ce != cudaSuccess || !graph ||
+            cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            if (graph) cudaGraphDestroy(graph);
+            g->exec = nullptr;
+            m->graphs_off = true;
+            return fn();
+        }
+        cudaGraphDestroy(graph);
+        g->launches = n;
+    }
+    if (cudaEventRecord(m->g_in, m->st) != cudaSuccess || cudaStreamWaitEvent(m->gst, m->g_in, 0) != cudaSuccess ||
+        cudaGraphLaunch(g->exec, m->gst) != cudaSuccess || cudaEventRecord(m->g_out, m->gst) != cudaSuccess ||
+        cudaStreamWaitEvent(m->st, m->g_out, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GPT2_ECUDA;
+    }
+    g_launches.fetch_add(g->launches, std::memory_order_relaxed);
+    return GPT2_OK;
+}
+
 }  // namespace gpt2k
 
 // ============================================================================
@@ -442,6 +511,14 @@ GPT2_API int gpt2_create(const gpt2_config* cfg, float* params, gpt2** out) {
         delete m;
         return GPT2_ECUDA;
     }
+    // the private stream that replays the step's graphs (none: no graphs)
+    if (cudaStreamCreateWithFlags(&m->gst, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&m->g_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&m->g_out, cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
+        m->graphs_off = true;
+    }
+    (void)gemm_tc_pair_slots();     // one-time occupancy query, outside any capture
     *out = m;
     return GPT2_OK;
 }
@@ -470,7 +547,8 @@ static float forward_common(gpt2* m, const int* tokens, const int* targets, int 
     }
     m->B = B;
     m->T = T;
-    int rc = forward_impl(m, B, T, targets != nullptr, grad);
+    const int kind = targets ? (grad ? 0 : 2) : 1;
+    int rc = run_graphed(m, kind, B, T, [&]() -> int { return forward_impl(m, B, T, targets != nullptr, grad); });
     if (rc) { record(m, rc); return NAN; }
     DevFlags h{};
     if (cudaMemcpyAsync(&h, m->flags, sizeof(h), cudaMemcpyDeviceToHost, m->st) != cudaSuccess ||
@@ -508,7 +586,7 @@ GPT2_API float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, 
 GPT2_API int gpt2_backward(gpt2* m) {
     if (!m) return GPT2_EINVAL;
     if (!m->fwd_targets) { record(m, GPT2_ESTATE); return GPT2_ESTATE; }
-    int rc = backward_impl(m);
+    int rc = run_graphed(m, 3, m->B, m->T, [&]() -> int { return backward_impl(m); });
     if (rc) { record(m, rc); return rc; }
     m->fwd_targets = false;     // dlogits were consumed; a new forward is needed
     m->have_grads = true;
@@ -624,6 +702,12 @@ GPT2_API int gpt2_destroy(gpt2* m) {
     if (cudaStreamSynchronize(m->st) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->owns_ws && cudaFree(m->ws) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->dec && cudaFree(m->dec) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    if (m->gst && cudaStreamSynchronize(m->gst) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    for (auto& g : m->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (m->gst) cudaStreamDestroy(m->gst);
+    if (m->g_in) cudaEventDestroy(m->g_in);
+    if (m->g_out) cudaEventDestroy(m->g_out);
     for (cudaEvent_t e : m->trace_events) cudaEventDestroy(e);
     delete m;
     return rc;

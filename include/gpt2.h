@@ -136,6 +136,13 @@ float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, int T);
  * ENOMEM, ECUDA. */
 int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logits);
 
+/* Graphs: gpt2_forward, gpt2_eval and gpt2_backward record their kernels into a
+ * CUDA graph on the second call with the same kind of call and (B, T), and
+ * replay it from the third on, on a library stream ordered after earlier work
+ * of the caller's stream and before later work (events); nothing else changes.
+ * Called while the caller's stream is being captured, or with tracing on, they
+ * launch their kernels directly. */
+
 /* Backward pass of the last forward (which must have had targets).
  * Overwrites the gradient buffer (no accumulation across calls); gradients
  * are those of the mean loss.  Errors: ESTATE, ECUDA. */
