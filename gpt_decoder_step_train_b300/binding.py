@@ -91,6 +91,7 @@ SIGNATURES = {
     "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_crossentropy_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp]),
+    "gpt2_op_sample_topk": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gpt2_op_sum": (_i, [_vp, _vp, _i, _f, _vp]),
     "gpt2_op_adamw": (_i, [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _f, _f, _vp]),
 }

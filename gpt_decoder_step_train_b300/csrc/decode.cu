@@ -154,6 +154,84 @@ __global__ void argmax_kernel(int* __restrict__ out, const float* __restrict__ z
     }
 }
 
+// Top-k sampling of one row per block ("GPT-2 from scratch with torch", section
+// 生成样本: keep the k highest scores, softmax, draw from the distribution).
+// The k largest of logits[n, 0..V) are found one by one in the order (value
+// descending, index ascending), NaN entries skipped; the kept tokens, taken in
+// ascending index order, get p = exp(z - zmax) / sum; the token is the first
+// whose cumulative p exceeds the caller's draw u[n] in [0, 1) (the last kept
+// token when rounding leaves u at or above the total).
+constexpr int TOPK_MAX = 64;
+
+__device__ __forceinline__ bool topk_better(float v, int i, float bv, int bi) {
+    return bi < 0 || v > bv || (v == bv && i < bi);
+}
+
+__global__ void sample_topk_kernel(int* __restrict__ out, const float* __restrict__ z, int V, int ld, int k,
+                                   const float* __restrict__ u) {
+    __shared__ float sv[TOPK_MAX], wv[32];
+    __shared__ int si[TOPK_MAX], wi[32];
+    const float* zr = z + (size_t)blockIdx.x * ld;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float pv = INFINITY;                 // the last kept (value, index): later picks rank below it
+    int pi = -1;
+    int n = 0;
+    for (int j = 0; j < k; j++) {
+        float bv = -INFINITY;
+        int bi = -1;
+        for (int v = threadIdx.x; v < V; v += blockDim.x) {
+            const float x = zr[v];
+            const bool below = x < pv || (x == pv && v > pi);
+            if (x == x && below && topk_better(x, v, bv, bi)) { bv = x; bi = v; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi >= 0 && topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) { wv[w] = bv; wi[w] = bi; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float b2 = wv[0];
+            int i2 = wi[0];
+            for (int q = 1; q < nw; q++)
+                if (wi[q] >= 0 && topk_better(wv[q], wi[q], b2, i2)) { b2 = wv[q]; i2 = wi[q]; }
+            sv[j] = b2;
+            si[j] = i2;
+        }
+        __syncthreads();
+        pv = sv[j];
+        pi = si[j];
+        __syncthreads();                 // wv, wi are rewritten by the next pick
+        if (pi < 0) break;               // fewer than k candidates
+        n = j + 1;
+    }
+    if (threadIdx.x == 0) {
+        if (n == 0) { out[blockIdx.x] = 0; return; }
+        const float zmax = sv[0];
+        // ascending index order (insertion sort of at most 64)
+        for (int a = 1; a < n; a++) {
+            const float tv = sv[a];
+            const int ti = si[a];
+            int b = a - 1;
+            while (b >= 0 && si[b] > ti) { sv[b + 1] = sv[b]; si[b + 1] = si[b]; b--; }
+            sv[b + 1] = tv;
+            si[b + 1] = ti;
+        }
+        float S = 0.f;
+        for (int a = 0; a < n; a++) S += expf(sv[a] - zmax);
+        const float target = u[blockIdx.x] * S;
+        float c = 0.f;
+        int pick = si[n - 1];
+        for (int a = 0; a < n; a++) {
+            c += expf(sv[a] - zmax);
+            if (c > target) { pick = si[a]; break; }
+        }
+        out[blockIdx.x] = pick;
+    }
+}
+
 // ---- launchers ----------------------------------------------------------------
 int decode_embed(float* x, const int* tok, const float* wte, const float* wpe, int B, int C, int V, int pos,
                  int* status, cudaStream_t st) {
@@ -191,6 +269,14 @@ int decode_attention(float* y, const float* qkv, const float* cache, int B, int 
 }  // namespace gpt2k
 
 using namespace gpt2k;
+
+GPT2_API int gpt2_op_sample_topk(int* out, const float* logits, int N, int V, int ld, int k, const float* u,
+                                  void* stream) {
+    if (!out || !logits || !u || N < 1 || V < 1 || ld < V || k < 1 || k > TOPK_MAX) return GPT2_EINVAL;
+    count_launch(), sample_topk_kernel<<<N, 256, 0, as_stream(stream)>>>(out, logits, V, ld, k, u);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
 
 GPT2_API int gpt2_op_argmax(int* out, const float* logits, int N, int V, int ld, void* stream) {
     if (!out || !logits || N < 1 || V < 1 || ld < V) return GPT2_EINVAL;

@@ -3,18 +3,26 @@
 // tf32 (kind::tf32, K = 8 per MMA) and bf16 (kind::f16, K = 16 per MMA); a
 // k-block is one 128-byte swizzle row either way (32 fp32 or 64 bf16).
 //
-// Persistent, warp-specialised kernel, one CTA per SM, 192 threads:
-//   warp 0  TMA producer: fills a ring of shared-memory stages (A: 128 x 32,
-//           B: BN x 32 fp32, 128-byte swizzle) and arms each stage's "full"
-//           mbarrier with the expected byte count;
+// Persistent, warp-specialised kernel, one CTA per SM, 320 threads:
+//   warp 0  TMA producer: fills a ring of shared-memory stages (A: 128 rows,
+//           B: BN rows, one 128-byte swizzle row of K each) and arms each
+//           stage's "full" mbarrier with the expected byte count;
 //   warp 1  allocates tensor memory and, from one lane, issues tcgen05.mma
-//           (M=128, N=BN, K=8) per k-slice; tcgen05.commit frees each stage
-//           and finally signals the accumulator as ready;
-//   warps 2-5  epilogue: tcgen05.ld rows of the accumulator (one TMEM lane per
-//           output row), apply bias / GELU / residual / GELU' and store.
+//           per K step; tcgen05.commit frees each stage and finally signals
+//           the accumulator as ready;
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (one column half
+//           each): tcgen05.ld rows of the accumulator (one TMEM lane per
+//           output row), apply bias / GELU / residual / GELU' / column sums
+//           and store through swizzled shared boxes with TMA stores.
 // Two accumulators (2 x BN TMEM columns) let the epilogue of one tile overlap
 // the main loop of the next.  Tiles are visited in groups of m-tiles so the
 // B operand (the weights) is reused from L2 by concurrently running CTAs.
+//
+// CTA pairs (PAIR, bf16): a cluster of two CTAs shares each 256 x 256 tile.
+// Rank 0 issues tcgen05.mma.cta_group::2 (M = 256); each CTA holds 128 rows of
+// A and 128 rows of B per stage and 128 rows of the accumulator; both CTAs'
+// loads complete on rank 0's stage barrier, the MMA commits are multicast to
+// both CTAs, and both epilogues release the accumulator on rank 0's barrier.
 //
 // Operand majorness follows gemm.cuh: a K-major operand is copied as one box
 // {32 k, rows}; an MN-major operand as boxes {32 rows-of-MN, 32 k}, each box a

@@ -208,6 +208,20 @@ int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const int* tgt,
 int gpt2_op_crossentropy_bf16(float* losses, void* z, const int* tgt, int N, int V, int ld,
                               float dscale, int* status, void* stream);
 
+/* Top-k sampling ("GPT-2 from scratch with torch", section 生成样本: keep the
+ * k highest scores, turn them into probabilities, draw the next token):
+ * out[n] = a token of row n of logits [N, ld] (ld >= V), drawn with the
+ * caller's uniform number u[n] in [0, 1) (device, one per row; the library
+ * draws no random numbers).  The kept set is the k largest of logits[n, 0..V)
+ * (1 <= k <= 64), taken in the order value descending, index ascending (so the
+ * lower index wins a tie at the cut), NaN entries skipped; with p_v =
+ * exp(z_v - max) / sum over the kept set, out[n] is the smallest kept index v
+ * whose cumulative p (over kept indices <= v) exceeds u[n], or the largest kept
+ * index when rounding leaves u[n] at or above the total.  k = 1 is the greedy
+ * choice.  A row with no candidate gives 0.  EINVAL for k outside [1, 64]. */
+int gpt2_op_sample_topk(int* out, const float* logits, int N, int V, int ld, int k, const float* u,
+                        void* stream);
+
 /* Greedy token choice: out[n] = the index of the largest of logits[n, 0..V)
  * (row stride ld >= V), the lowest index on ties; NaN entries never win (a row
  * of NaN gives 0).  ("GPT-2 from scratch with torch", section 生成样本: the

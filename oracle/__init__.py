@@ -299,6 +299,43 @@ class OracleModel:
         return self._view(self.o.lib.oracle_act(self.h, ACT[name], layer), n).reshape(shp)
 
 
+def sample_topk(logits, k, u):
+    """Top-k sampling of each row ("GPT-2 from scratch with torch", section
+    生成样本): keep the k highest scores, turn them into probabilities with a
+    softmax, and draw from them; the draw is the caller's uniform number u[n] in
+    [0, 1), applied as an inverse cumulative distribution over the kept tokens in
+    ascending index order (the order in which a multinomial draw over the whole
+    vocabulary walks the tokens).  Ties at the cut keep the lower index; NaN
+    scores are never kept.  Plain loops in float64.  Returns (tokens, cumulative
+    boundaries per row) so that tests can tell draws that sit on a boundary."""
+    import math
+    z = np.asarray(logits, dtype=np.float64)
+    N, V = z.shape
+    out = np.zeros(N, dtype=np.int32)
+    bounds = []
+    for n in range(N):
+        cand = [v for v in range(V) if z[n, v] == z[n, v]]
+        cand.sort(key=lambda v: (-z[n, v], v))
+        keep = sorted(cand[:k])
+        if not keep:
+            bounds.append([])
+            continue
+        zmax = max(z[n, v] for v in keep)
+        p = [math.exp(z[n, v] - zmax) for v in keep]
+        s = sum(p)
+        cum, c = [], 0.0
+        out[n] = keep[-1]
+        chosen = False
+        for v, pv in zip(keep, p):
+            c += pv / s
+            cum.append(c)
+            if not chosen and c > u[n]:
+                out[n] = v
+                chosen = True
+        bounds.append(cum)
+    return out, bounds
+
+
 def split_params(flat, sizes):
     """Views of the 16 tensors of a flat parameter array, by name."""
     out, off = {}, 0

@@ -1,7 +1,7 @@
 """Autoregressive decoding with the key/value cache, against the oracle: the
 logits of position t from gpt2_decode equal the oracle's last-row logits of a
 full forward over the prefix 0..t (causality makes the two the same function),
-plus greedy token choice and the call-order rules."""
+plus greedy and top-k token choice and the call-order rules."""
 import numpy as np
 import pytest
 
@@ -160,3 +160,36 @@ def test_decode_call_order_and_errors():
     loss = model.forward(torch.from_numpy(tt[:4]).cuda(), torch.from_numpy(tg[:4]).cuda())
     assert np.isfinite(loss) and model.backward() == 0
     model.close()
+
+
+@pytest.mark.parametrize("k", [1, 5, 50, 64])
+def test_sample_topk_matches_oracle(k):
+    """gpt2_op_sample_topk against the oracle's definition on the same logits and
+    draws: the same token, except where a draw sits within 1e-6 of a cumulative
+    boundary (fp32 on the GPU, float64 in the oracle), where either neighbour is
+    accepted."""
+    from gpt_decoder_step_train_b300 import binding as B_
+    from oracle import sample_topk
+    L = B_.lib()
+    rng = np.random.default_rng(13 + k)
+    N, V, ld = 12, 50257, 50304
+    z = np.zeros((N, ld), dtype=np.float32)
+    z[:, :V] = (rng.normal(size=(N, V)) * 2).astype(np.float32)
+    z[3, 1000:1000 + 2 * k] = 9.0                          # ties across the cut
+    z[4, 5] = np.nan
+    z[:, V:] = 1e9                                          # padding is never a candidate
+    u = rng.random(N).astype(np.float32)
+    zt, ut = torch.from_numpy(z).cuda(), torch.from_numpy(u).cuda()
+    out = torch.empty(N, dtype=torch.int32, device="cuda")
+    assert L.gpt2_op_sample_topk(B_.ptr(out), B_.ptr(zt), N, V, ld, k, B_.ptr(ut), None) == 0
+    got = out.cpu().numpy()
+    want, bounds = sample_topk(z[:, :V], k, u.astype(np.float64))
+    for n in range(N):
+        if got[n] == want[n]:
+            continue
+        near = [abs(b - u[n]) < 1e-6 for b in bounds[n]]
+        assert any(near), (n, got[n], want[n])
+    if k == 1:
+        assert np.array_equal(got, np.argmax(np.where(np.isnan(z[:, :V]), -np.inf, z[:, :V]), axis=1))
+    assert L.gpt2_op_sample_topk(B_.ptr(out), B_.ptr(zt), N, V, ld, 65, B_.ptr(ut), None) == B_.GPT2_EINVAL
+    assert L.gpt2_op_sample_topk(B_.ptr(out), B_.ptr(zt), N, V, ld, 0, B_.ptr(ut), None) == B_.GPT2_EINVAL

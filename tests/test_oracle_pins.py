@@ -463,3 +463,63 @@ def test_float_build_tracks_double_build(o32, o64):
     g64 = m64.backward(params)
     g32 = m32.backward(params.astype(np.float32))
     assert np.linalg.norm(g32 - g64) / np.linalg.norm(g64) < 1e-5
+
+
+# ---- top-k sampling (generation: keep the k highest scores, softmax, draw) ----
+def test_sample_topk_k1_is_argmax():
+    from oracle import sample_topk
+    rng = np.random.default_rng(11)
+    z = rng.normal(size=(20, 300))
+    tok, _ = sample_topk(z, 1, rng.random(20))
+    assert np.array_equal(tok, np.argmax(z, axis=1))
+
+
+def test_sample_topk_equal_scores_are_uniform_over_kept_indices():
+    """k equal maxima: each kept token has probability 1/k, so u in [j/k, (j+1)/k)
+    selects the j-th smallest kept index (closed form)."""
+    from oracle import sample_topk
+    V, k = 97, 4
+    z = np.full((1, V), -3.0)
+    kept = [5, 17, 60, 90]
+    z[0, kept] = 2.5
+    for j in range(k):
+        for frac in (0.05, 0.5, 0.95):
+            tok, _ = sample_topk(z, k, np.array([(j + frac) / k]))
+            assert tok[0] == kept[j]
+
+
+def test_sample_topk_two_tokens_closed_form_boundary():
+    from oracle import sample_topk
+    z = np.full((1, 10), -50.0)
+    z[0, 7], z[0, 2] = 1.0, 0.25                      # kept in index order: 2 then 7
+    p2 = np.exp(0.25) / (np.exp(0.25) + np.exp(1.0))
+    assert sample_topk(z, 2, np.array([p2 - 1e-9]))[0][0] == 2
+    assert sample_topk(z, 2, np.array([p2 + 1e-9]))[0][0] == 7
+    assert sample_topk(z, 2, np.array([0.999999999]))[0][0] == 7
+
+
+def test_sample_topk_tie_at_cut_keeps_lower_index_and_skips_nan():
+    from oracle import sample_topk
+    z = np.array([[3.0, 5.0, 3.0, 3.0, np.nan, 3.0]])
+    # k = 2 keeps 1 (5.0) and 0 (the lowest-index 3.0); u near 1 picks the larger index kept
+    tok, bounds = sample_topk(z, 2, np.array([0.999999]))
+    assert tok[0] == 1 and len(bounds[0]) == 2
+    tok, _ = sample_topk(z, 2, np.array([0.0]))
+    assert tok[0] == 0
+    tok, _ = sample_topk(np.array([[np.nan, np.nan, 1.0]]), 3, np.array([0.5]))
+    assert tok[0] == 2
+
+
+def test_sample_topk_frequencies_follow_the_kept_softmax():
+    """Draws on a fine grid of u reproduce the softmax of the kept scores."""
+    from oracle import sample_topk
+    rng = np.random.default_rng(12)
+    z = rng.normal(size=(1, 40)) * 2
+    k = 6
+    grid = (np.arange(4000) + 0.5) / 4000
+    toks = np.array([sample_topk(z, k, np.array([g]))[0][0] for g in grid])
+    kept = np.argsort(-z[0], kind="stable")[:k]
+    p = np.exp(z[0, kept] - z[0, kept].max())
+    p /= p.sum()
+    for v, pv in zip(kept, p):
+        assert abs(np.mean(toks == v) - pv) < 1e-3
