@@ -65,6 +65,15 @@ class Oracle:
         L.oracle_matmul_backward.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i]
         L.oracle_attention_forward.argtypes = [vp, vp, vp, i, i, i, i]
         L.oracle_attention_backward.argtypes = [vp, vp, vp, vp, i, i, i, i]
+        L.oracle_attention_forward_dropout.argtypes = [vp, vp, vp, i, i, i, i, vp, C.c_double]
+        L.oracle_attention_backward_dropout.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, C.c_double]
+        L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+        L.oracle_dropout_keep.argtypes = [vp, sz, C.c_uint64, C.c_uint32, C.c_uint32, C.c_double]
+        L.oracle_dropout_apply.argtypes = [vp, vp, vp, sz, C.c_double]
+        L.oracle_set_dropout.restype = i
+        L.oracle_set_dropout.argtypes = [vp, C.c_double, C.c_uint64, C.c_uint32]
+        L.oracle_keep.restype = vp
+        L.oracle_keep.argtypes = [vp, i, i]
         L.oracle_gelu_forward.argtypes = [vp, vp, sz]
         L.oracle_gelu_backward.argtypes = [vp, vp, vp, sz]
         L.oracle_crossentropy_forward.restype = r
@@ -162,22 +171,59 @@ class Oracle:
                                         _ptr(x), _ptr(self.arr(w)), N, IC, OC)
         return dx, dw, db
 
-    def attention_forward(self, qkv, NH):
+    def attention_forward(self, qkv, NH, keep=None, p=0.0):
+        """keep: optional uint8 flags [B,NH,T,T] of attention dropout with probability p."""
         qkv = self.arr(qkv)
         B, T, C3 = qkv.shape
         Cc = C3 // 3
         y = np.zeros((B, T, Cc), dtype=self.dtype)
         P = np.zeros((B, NH, T, T), dtype=self.dtype)
-        self.lib.oracle_attention_forward(_ptr(y), _ptr(P), _ptr(qkv), B, T, Cc, NH)
+        if keep is None:
+            self.lib.oracle_attention_forward(_ptr(y), _ptr(P), _ptr(qkv), B, T, Cc, NH)
+        else:
+            keep = np.ascontiguousarray(keep, dtype=np.uint8)
+            assert keep.size == B * NH * T * T
+            self.lib.oracle_attention_forward_dropout(_ptr(y), _ptr(P), _ptr(qkv), B, T, Cc, NH,
+                                                      _ptr(keep), float(p))
         return y, P
 
-    def attention_backward(self, dy, qkv, P, NH):
+    def attention_backward(self, dy, qkv, P, NH, keep=None, p=0.0):
         qkv = self.arr(qkv)
         B, T, C3 = qkv.shape
         dqkv = np.zeros_like(qkv)
-        self.lib.oracle_attention_backward(_ptr(dqkv), _ptr(self.arr(dy)), _ptr(qkv),
-                                           _ptr(self.arr(P)), B, T, C3 // 3, NH)
+        if keep is None:
+            self.lib.oracle_attention_backward(_ptr(dqkv), _ptr(self.arr(dy)), _ptr(qkv),
+                                               _ptr(self.arr(P)), B, T, C3 // 3, NH)
+        else:
+            keep = np.ascontiguousarray(keep, dtype=np.uint8)
+            self.lib.oracle_attention_backward_dropout(_ptr(dqkv), _ptr(self.arr(dy)), _ptr(qkv),
+                                                       _ptr(self.arr(P)), B, T, C3 // 3, NH,
+                                                       _ptr(keep), float(p))
         return dqkv
+
+    # ---- dropout ------------------------------------------------------
+    def philox(self, ctr, key):
+        """Philox4x32-10 of one counter (4 words) under one key (2 words)."""
+        c = np.ascontiguousarray(ctr, dtype=np.uint32)
+        k = np.ascontiguousarray(key, dtype=np.uint32)
+        assert c.size == 4 and k.size == 2
+        out = np.zeros(4, dtype=np.uint32)
+        self.lib.oracle_philox4x32_10(_ptr(out), _ptr(c), _ptr(k))
+        return out
+
+    def dropout_keep(self, n, seed, site, step, p):
+        """uint8 keep flags of elements 0..n-1 of one dropout site."""
+        keep = np.zeros(int(n), dtype=np.uint8)
+        self.lib.oracle_dropout_keep(_ptr(keep), int(n), int(seed), int(site), int(step), float(p))
+        return keep
+
+    def dropout_apply(self, x, keep, p):
+        x = self.arr(x)
+        keep = np.ascontiguousarray(keep, dtype=np.uint8)
+        assert keep.size == x.size
+        y = np.zeros_like(x)
+        self.lib.oracle_dropout_apply(_ptr(y), _ptr(x), _ptr(keep), x.size, float(p))
+        return y
 
     def gelu_forward(self, x):
         x = self.arr(x)
@@ -254,6 +300,22 @@ class OracleModel:
             tgt_arr = np.ascontiguousarray(tgt, dtype=np.int32)
             assert tgt_arr.shape == (self.B, self.T)
         return float(self.o.lib.oracle_forward(self.h, _ptr(params), _ptr(tok), _ptr(tgt_arr)))
+
+    def set_dropout(self, p, seed=0, step=0):
+        """Dropout for the following forwards (p < 0 turns it off)."""
+        if self.o.lib.oracle_set_dropout(self.h, float(p), int(seed), int(step)) != 0:
+            raise ValueError("oracle_set_dropout: p must be below 1")
+
+    def keep(self, which, layer=0):
+        """Keep flags of the last forward: 'emb', 'att' [B,NH,T,T], 'attproj', 'fcproj'."""
+        c = self.cfg
+        N = self.B * self.T
+        idx = {"emb": 0, "att": 1, "attproj": 2, "fcproj": 3}[which]
+        n = self.B * c["H"] * self.T * self.T if which == "att" else N * c["C"]
+        addr = self.o.lib.oracle_keep(self.h, idx, layer)
+        if not addr:
+            return None
+        return np.frombuffer((C.c_uint8 * n).from_address(addr), dtype=np.uint8, count=n).copy()
 
     def backward(self, params):
         grads = np.zeros(self.nparams, dtype=self.o.dtype)

@@ -27,7 +27,9 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *   LayerNorm uses the biased variance with eps = 1e-5 inside the square root;
  *   GELU uses sqrt(2/pi) at full precision; positions are 0..T-1; dropout is
- *   zero; the loss is the mean over all B*T positions; the update is decoupled
+ *   off unless oracle_set_dropout turns it on (then inverted dropout at the
+ *   four sites the pages name, with Philox4x32-10 draws: see the dropout
+ *   section below); the loss is the mean over all B*T positions; the update is decoupled
  *   AdamW with bias correction, decay only on 2-D weight tensors, applied to
  *   the pre-update parameter value.
  *
@@ -258,22 +260,100 @@ void oracle_matmul_backward(real* dx, real* dw, real* dbias, const real* dy,
     }
 }
 
+/* ---- dropout ----------------------------------------------------------------
+ * Where: after the token + position embeddings, on the attention weights after
+ * the softmax, and on the output of each block's two c_proj layers before the
+ * residual addition ("GPT-2 from scratch with torch", sections 总体架构,
+ * 近看 Transformer block：自注意力 and 近看 Transformer block：前馈网络（MLP）;
+ * "从头搭建GPT(Andrej Karpathy) 笔记", section 继续增加改进的点).  In training
+ * each element is kept with probability 1 - p and the kept ones are scaled by
+ * 1/(1 - p) (inverted dropout, so evaluation uses every element unscaled).
+ *
+ * The pages fix no random stream, so the draws come from the counter-based
+ * generator Philox4x32-10 (J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC 2011), written from its definition:
+ * ten rounds of
+ *     (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57 and 32x32->64-bit products, the key
+ * (k0, k1) advanced by (0x9E3779B9, 0xBB67AE85) before every round but the
+ * first.  Element e (row-major index) of dropout site `site` in forward call
+ * `step` under the 64-bit seed:
+ *     (w0, w1, w2, w3) = Philox4x32-10(counter (lo32(e/4), hi32(e/4), site, step),
+ *                                       key (lo32(seed), hi32(seed)))
+ *     keep(e) = w[e mod 4] >= floor(p * 2^32)
+ * Sites: 0 the embedding output [B,T,C]; for layer l, 1 + 3l the attention
+ * weights [B,NH,T,T], 2 + 3l the attention c_proj output [B,T,C] and 3 + 3l
+ * the MLP c_proj output [B,T,C]. */
+static void philox_round(uint32_t c[4], const uint32_t k[2]) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k[0];
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = (uint32_t)p1;
+    c[2] = n2;
+    c[3] = (uint32_t)p0;
+}
+
+void oracle_philox4x32_10(uint32_t out[4], const uint32_t ctr[4], const uint32_t key[2]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int r = 0; r < 10; r++) {
+        if (r > 0) {
+            k[0] += 0x9E3779B9u;
+            k[1] += 0xBB67AE85u;
+        }
+        philox_round(c, k);
+    }
+    for (int i = 0; i < 4; i++) out[i] = c[i];
+}
+
+/* keep[e] for elements e = 0 .. n-1 of one site (1 = kept). */
+void oracle_dropout_keep(uint8_t* keep, size_t n, uint64_t seed, uint32_t site, uint32_t step,
+                         double p) {
+    const uint32_t thr = (uint32_t)floor(p * 4294967296.0);
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    #pragma omp parallel for schedule(static)
+    for (long long g = 0; g < (long long)((n + 3) / 4); g++) {
+        const uint64_t q = (uint64_t)g;
+        const uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), site, step};
+        uint32_t w[4];
+        oracle_philox4x32_10(w, ctr, key);
+        for (int i = 0; i < 4; i++) {
+            const size_t e = 4 * (size_t)q + i;
+            if (e < n) keep[e] = w[i] >= thr;
+        }
+    }
+}
+
+static real dropout_scale(double p) { return (real)1 / ((real)1 - (real)p); }
+
+/* y = x o keep / (1 - p)  (y may be x) */
+void oracle_dropout_apply(real* y, const real* x, const uint8_t* keep, size_t n, double p) {
+    const real ks = dropout_scale(p);
+    for (size_t i = 0; i < n; i++) y[i] = keep[i] ? x[i] * ks : 0;
+}
+
 /* Causal multi-head self-attention over qkv[B,T,3C]; columns [0,C) are the
  * queries, [C,2C) the keys, [2C,3C) the values, and head h owns columns
  * h*hs .. h*hs+hs-1 of each (split at C, then viewed as (B,T,NH,hs)).
  * For each (b,h): S = Q K^T / sqrt(hs); S[i,j] = -inf for j > i;
  * P = row softmax(S) (max-subtracted, exact in real arithmetic); O = P V.
  * O is written with the heads side by side: y[b,t,h*hs+d].
- * P is kept, [B,NH,T,T], for the backward (entries above the diagonal are 0). */
-void oracle_attention_forward(real* y, real* P, const real* qkv, int B, int T, int C,
-                              int NH) {
+ * P is kept, [B,NH,T,T], for the backward (entries above the diagonal are 0).
+ * With dropout on the attention weights (keep != NULL, flags [B,NH,T,T]):
+ * O = (P o K / (1 - p)) V, K the keep flags; P itself is stored undropped. */
+void oracle_attention_forward_dropout(real* y, real* P, const real* qkv, int B, int T, int C,
+                                      int NH, const uint8_t* keep, double p) {
     int hs = C / NH;
+    real ks = keep ? dropout_scale(p) : (real)1;
     real scale = 1 / R_SQRT((real)hs);
     size_t C3 = (size_t)3 * C;
     #pragma omp parallel for collapse(2) schedule(static)
     for (int b = 0; b < B; b++)
         for (int h = 0; h < NH; h++) {
             real* Pbh = P + ((size_t)b * NH + h) * T * T;
+            const uint8_t* Kbh = keep ? keep + ((size_t)b * NH + h) * T * T : NULL;
             for (int i = 0; i < T; i++) {
                 const real* q = qkv + ((size_t)b * T + i) * C3 + h * hs;
                 real* prow = Pbh + (size_t)i * T;
@@ -293,29 +373,44 @@ void oracle_attention_forward(real* y, real* P, const real* qkv, int B, int T, i
                 real* out = y + ((size_t)b * T + i) * C + h * hs;
                 for (int d = 0; d < hs; d++) {
                     real s = 0;
-                    for (int j = 0; j <= i; j++)
-                        s += prow[j] * qkv[((size_t)b * T + j) * C3 + 2 * C + h * hs + d];
+                    for (int j = 0; j <= i; j++) {
+                        real a = prow[j];
+                        if (Kbh) a = Kbh[(size_t)i * T + j] ? a * ks : 0;
+                        s += a * qkv[((size_t)b * T + j) * C3 + 2 * C + h * hs + d];
+                    }
                     out[d] = s;
                 }
             }
         }
 }
 
+void oracle_attention_forward(real* y, real* P, const real* qkv, int B, int T, int C, int NH) {
+    oracle_attention_forward_dropout(y, P, qkv, B, T, C, NH, NULL, 0);
+}
+
 /* Backward of the attention above, from dy (heads side by side) and the saved P:
  *   dV = P^T dO;  dP = dO V^T;  dS = P o (dP - rowsum(P o dP));
- *   dQ = dS K / sqrt(hs);  dK = dS^T Q / sqrt(hs).   Added into dqkv. */
-void oracle_attention_backward(real* dqkv, const real* dy, const real* qkv, const real* P,
-                               int B, int T, int C, int NH) {
+ *   dQ = dS K / sqrt(hs);  dK = dS^T Q / sqrt(hs).   Added into dqkv.
+ * With dropout (keep flags K, A = P o K / (1 - p) the weights that met V):
+ *   dV = A^T dO;  dP = (dO V^T) o K / (1 - p);  dS as above. */
+void oracle_attention_backward_dropout(real* dqkv, const real* dy, const real* qkv, const real* P,
+                                       int B, int T, int C, int NH, const uint8_t* keep,
+                                       double p) {
     int hs = C / NH;
+    real ks = keep ? dropout_scale(p) : (real)1;
     real scale = 1 / R_SQRT((real)hs);
     size_t C3 = (size_t)3 * C;
     #pragma omp parallel for collapse(2) schedule(static)
     for (int b = 0; b < B; b++)
         for (int h = 0; h < NH; h++) {
             const real* Pbh = P + ((size_t)b * NH + h) * T * T;
+            const uint8_t* Kbh = keep ? keep + ((size_t)b * NH + h) * T * T : NULL;
             real* dS = (real*)malloc(sizeof(real) * (size_t)T);
+            real* A = (real*)malloc(sizeof(real) * (size_t)T);
             for (int i = 0; i < T; i++) {
                 const real* prow = Pbh + (size_t)i * T;
+                for (int j = 0; j <= i; j++)
+                    A[j] = Kbh ? (Kbh[(size_t)i * T + j] ? prow[j] * ks : 0) : prow[j];
                 const real* dO = dy + ((size_t)b * T + i) * C + h * hs;
                 /* dP[i,j] = dO_i . v_j,   D = sum_j P[i,j] dP[i,j] */
                 real D = 0;
@@ -323,6 +418,7 @@ void oracle_attention_backward(real* dqkv, const real* dy, const real* qkv, cons
                     const real* v = qkv + ((size_t)b * T + j) * C3 + 2 * C + h * hs;
                     real dp = 0;
                     for (int d = 0; d < hs; d++) dp += dO[d] * v[d];
+                    if (Kbh) dp = Kbh[(size_t)i * T + j] ? dp * ks : 0;
                     dS[j] = dp;
                     D += prow[j] * dp;
                 }
@@ -336,12 +432,18 @@ void oracle_attention_backward(real* dqkv, const real* dy, const real* qkv, cons
                     for (int d = 0; d < hs; d++) {
                         dq[d] += dS[j] * k[d] * scale;
                         dk[d] += dS[j] * q[d] * scale;
-                        dv[d] += prow[j] * dO[d];
+                        dv[d] += A[j] * dO[d];
                     }
                 }
             }
             free(dS);
+            free(A);
         }
+}
+
+void oracle_attention_backward(real* dqkv, const real* dy, const real* qkv, const real* P,
+                               int B, int T, int C, int NH) {
+    oracle_attention_backward_dropout(dqkv, dy, qkv, P, B, T, C, NH, NULL, 0);
 }
 
 /* GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
@@ -444,6 +546,15 @@ typedef struct {
     int *tok, *tgt;     /* [N] copies */
     int has_targets;
     real loss;
+    /* dropout (off unless oracle_set_dropout turned it on) */
+    int drop_on;
+    double pdrop;
+    uint64_t seed;
+    uint32_t step;
+    uint8_t *keep_emb;  /* [N,C]          site 0        */
+    uint8_t *keep_att;  /* [L,B,NH,T,T]   sites 1 + 3l  */
+    uint8_t *keep_ap;   /* [L,N,C]        sites 2 + 3l  */
+    uint8_t *keep_fp;   /* [L,N,C]        sites 3 + 3l  */
 } OracleModel;
 
 static real* zalloc(size_t n) { return (real*)calloc(n ? n : 1, sizeof(real)); }
@@ -484,7 +595,43 @@ void oracle_free(OracleModel* m) {
                     m->ln2, m->ln2_mean, m->ln2_rstd, m->h, m->g, m->res3, m->lnf,
                     m->lnf_mean, m->lnf_rstd, m->logits, m->probs, m->losses};
     for (size_t i = 0; i < sizeof(bufs) / sizeof(bufs[0]); i++) free(bufs[i]);
-    free(m->tok); free(m->tgt); free(m);
+    free(m->tok); free(m->tgt);
+    free(m->keep_emb); free(m->keep_att); free(m->keep_ap); free(m->keep_fp);
+    free(m);
+}
+
+/* Dropout for the following forward calls: probability p in [0, 1) of zeroing
+ * an element, draws from (seed, step) as the dropout section above defines.
+ * p < 0 turns dropout off.  p = 0 keeps every element (scale 1).  Returns 0,
+ * or -1 when p >= 1 or memory runs out. */
+int oracle_set_dropout(OracleModel* m, double p, uint64_t seed, uint32_t step) {
+    if (p >= 1) return -1;
+    m->drop_on = p >= 0;
+    m->pdrop = p;
+    m->seed = seed;
+    m->step = step;
+    if (!m->drop_on || m->keep_emb) return 0;
+    size_t N = (size_t)m->B * m->T, NC = N * m->C, l = (size_t)m->L;
+    m->keep_emb = (uint8_t*)calloc(NC, 1);
+    m->keep_att = (uint8_t*)calloc(l * m->B * m->NH * (size_t)m->T * m->T, 1);
+    m->keep_ap = (uint8_t*)calloc(l * NC, 1);
+    m->keep_fp = (uint8_t*)calloc(l * NC, 1);
+    if (!m->keep_emb || !m->keep_att || !m->keep_ap || !m->keep_fp) return -1;
+    return 0;
+}
+
+/* The keep flags of the last forward: which 0 embedding, 1 attention weights,
+ * 2 attention c_proj, 3 MLP c_proj; layer l for 1..3. */
+const uint8_t* oracle_keep(const OracleModel* m, int which, int l) {
+    size_t NC = (size_t)m->B * m->T * m->C;
+    if (!m->drop_on) return NULL;
+    switch (which) {
+        case 0: return m->keep_emb;
+        case 1: return m->keep_att + (size_t)l * m->B * m->NH * m->T * m->T;
+        case 2: return m->keep_ap + l * NC;
+        case 3: return m->keep_fp + l * NC;
+        default: return NULL;
+    }
 }
 
 /* The block input of layer l: the encoder output for l = 0, else the output
@@ -504,6 +651,12 @@ real oracle_forward(OracleModel* m, real* params, const int* tok, const int* tgt
     if (tgt) memcpy(m->tgt, tgt, N * sizeof(int));
 
     oracle_encoder_forward(m->x0, tok, w.wte, w.wpe, B, T, C);
+    const int drop = m->drop_on;
+    const size_t att_n = (size_t)B * NH * T * T;
+    if (drop) {
+        oracle_dropout_keep(m->keep_emb, NC, m->seed, 0, m->step, m->pdrop);
+        oracle_dropout_apply(m->x0, m->x0, m->keep_emb, NC, m->pdrop);
+    }
     for (int l = 0; l < L; l++) {
         const real* x = block_input(m, l);
         real* ln1 = m->ln1 + l * NC;
@@ -519,14 +672,24 @@ real oracle_forward(OracleModel* m, real* params, const int* tok, const int* tgt
         oracle_layernorm_forward(ln1, m->ln1_mean + l * N, m->ln1_rstd + l * N, x,
                                  w.ln1w + l * C, w.ln1b + l * C, (int)N, C);
         oracle_matmul_forward(qkv, ln1, w.qkvw + l * 3 * cc, w.qkvb + l * 3 * C, (int)N, C, 3 * C);
-        oracle_attention_forward(atty, P, qkv, B, T, C, NH);
+        const uint8_t* katt = NULL;
+        if (drop) {
+            uint8_t* ka = m->keep_att + l * att_n;
+            oracle_dropout_keep(ka, att_n, m->seed, 1 + 3 * (uint32_t)l, m->step, m->pdrop);
+            oracle_dropout_keep(m->keep_ap + l * NC, NC, m->seed, 2 + 3 * (uint32_t)l, m->step, m->pdrop);
+            oracle_dropout_keep(m->keep_fp + l * NC, NC, m->seed, 3 + 3 * (uint32_t)l, m->step, m->pdrop);
+            katt = ka;
+        }
+        oracle_attention_forward_dropout(atty, P, qkv, B, T, C, NH, katt, m->pdrop);
         oracle_matmul_forward(res2, atty, w.attprojw + l * cc, w.attprojb + l * C, (int)N, C, C);
+        if (drop) oracle_dropout_apply(res2, res2, m->keep_ap + l * NC, NC, m->pdrop);
         for (size_t i = 0; i < NC; i++) res2[i] += x[i];            /* residual */
         oracle_layernorm_forward(ln2, m->ln2_mean + l * N, m->ln2_rstd + l * N, res2,
                                  w.ln2w + l * C, w.ln2b + l * C, (int)N, C);
         oracle_matmul_forward(h, ln2, w.fcw + l * 4 * cc, w.fcb + l * 4 * C, (int)N, C, 4 * C);
         oracle_gelu_forward(g, h, 4 * NC);
         oracle_matmul_forward(res3, g, w.fcprojw + l * 4 * cc, w.fcprojb + l * C, (int)N, 4 * C, C);
+        if (drop) oracle_dropout_apply(res3, res3, m->keep_fp + l * NC, NC, m->pdrop);
         for (size_t i = 0; i < NC; i++) res3[i] += res2[i];         /* residual */
     }
     const real* xL = block_input(m, L);
@@ -574,6 +737,9 @@ int oracle_backward(OracleModel* m, real* params, real* grads) {
     real* dh = zalloc(4 * NC);
     real* datty = zalloc(NC);
     real* dqkv = zalloc(3 * NC);
+    real* dbr = zalloc(NC);      /* gradient w.r.t. a c_proj output (through dropout) */
+    const int drop = m->drop_on;
+    const size_t att_n = (size_t)B * NH * T * T;
 
     oracle_crossentropy_backward(dz, m->probs, m->tgt, (int)N, V, V);
     oracle_matmul_backward(dlnf, d.wte, NULL, dz, m->lnf, w.wte, (int)N, C, V);
@@ -585,7 +751,8 @@ int oracle_backward(OracleModel* m, real* params, real* grads) {
         memset(dg, 0, 4 * NC * sizeof(real));
         memset(dh, 0, 4 * NC * sizeof(real));
         memset(dtmp, 0, NC * sizeof(real));
-        oracle_matmul_backward(dg, d.fcprojw + l * 4 * cc, d.fcprojb + l * C, dres,
+        if (drop) oracle_dropout_apply(dbr, dres, m->keep_fp + l * NC, NC, m->pdrop);
+        oracle_matmul_backward(dg, d.fcprojw + l * 4 * cc, d.fcprojb + l * C, drop ? dbr : dres,
                                m->g + l * 4 * NC, w.fcprojw + l * 4 * cc, (int)N, 4 * C, C);
         oracle_gelu_backward(dh, m->h + l * 4 * NC, dg, 4 * NC);
         oracle_matmul_backward(dtmp, d.fcw + l * 4 * cc, d.fcb + l * 4 * C, dh,
@@ -597,18 +764,22 @@ int oracle_backward(OracleModel* m, real* params, real* grads) {
         memset(datty, 0, NC * sizeof(real));
         memset(dqkv, 0, 3 * NC * sizeof(real));
         memset(dtmp, 0, NC * sizeof(real));
-        oracle_matmul_backward(datty, d.attprojw + l * cc, d.attprojb + l * C, dres,
+        if (drop) oracle_dropout_apply(dbr, dres, m->keep_ap + l * NC, NC, m->pdrop);
+        oracle_matmul_backward(datty, d.attprojw + l * cc, d.attprojb + l * C, drop ? dbr : dres,
                                m->atty + l * NC, w.attprojw + l * cc, (int)N, C, C);
-        oracle_attention_backward(dqkv, datty, m->qkv + l * 3 * NC,
-                                  m->P + (size_t)l * B * NH * T * T, B, T, C, NH);
+        oracle_attention_backward_dropout(dqkv, datty, m->qkv + l * 3 * NC,
+                                          m->P + (size_t)l * att_n, B, T, C, NH,
+                                          drop ? m->keep_att + l * att_n : NULL, m->pdrop);
         oracle_matmul_backward(dtmp, d.qkvw + l * 3 * cc, d.qkvb + l * 3 * C, dqkv,
                                m->ln1 + l * NC, w.qkvw + l * 3 * cc, (int)N, C, 3 * C);
         oracle_layernorm_backward(dres, d.ln1w + l * C, d.ln1b + l * C, dtmp, x,
                                   w.ln1w + l * C, m->ln1_mean + l * N, m->ln1_rstd + l * N,
                                   (int)N, C);
     }
+    if (drop) oracle_dropout_apply(dres, dres, m->keep_emb, NC, m->pdrop);
     oracle_encoder_backward(d.wte, d.wpe, dres, m->tok, B, T, C);
     free(dz); free(dlnf); free(dres); free(dtmp); free(dg); free(dh); free(datty); free(dqkv);
+    free(dbr);
     return 0;
 }
 

@@ -523,3 +523,167 @@ def test_sample_topk_frequencies_follow_the_kept_softmax():
     p /= p.sum()
     for v, pv in zip(kept, p):
         assert abs(np.mean(toks == v) - pv) < 1e-3
+
+
+# ---- dropout (inverted dropout at the four sites; Philox4x32-10 draws) ----
+def _philox_kat():
+    from conftest import GOLDEN
+    import os
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                rows.append([int(w, 16) for w in line])
+    return rows
+
+
+def test_philox_known_answer_vectors(o64):
+    rows = _philox_kat()
+    assert len(rows) == 3
+    for r in rows:
+        assert list(o64.philox(r[0:4], r[4:6])) == r[6:10]
+
+
+def test_dropout_keep_is_the_counter_word_against_the_threshold(o64):
+    """Element e uses word e mod 4 of the draw at counter (e/4, 0, site, step);
+    a word equal to the threshold is kept, one below it is dropped."""
+    seed, site, step = 0x1234_5678_9ABC_DEF0, 7, 3
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    n = 37
+    words = np.concatenate([o64.philox([q, 0, site, step], key) for q in range((n + 3) // 4)])[:n]
+    w = int(words[5])
+    for p, want5 in ((w / 2.0**32, 1), ((w + 1) / 2.0**32, 0)):
+        keep = o64.dropout_keep(n, seed, site, step, p)
+        assert keep[5] == want5
+        thr = math.floor(p * 2.0**32)
+        assert np.array_equal(keep, (words >= thr).astype(np.uint8))
+    assert np.all(o64.dropout_keep(n, seed, site, step, 0.0) == 1)
+
+
+def test_dropout_keep_fraction_and_expectation(o64):
+    n = 1 << 20
+    for p in (0.1, 0.5):
+        keep = o64.dropout_keep(n, 99, 1, 0, p)
+        sigma = math.sqrt(p * (1 - p) / n)
+        assert abs(keep.mean() - (1 - p)) < 6 * sigma, (p, keep.mean())
+        # inverted dropout: the mean of the dropped-out ones stays 1
+        y = o64.dropout_apply(np.ones(n), keep, p)
+        assert abs(y.mean() - 1.0) < 6 * sigma / (1 - p)
+        assert set(np.unique(y)) <= {0.0, 1.0 / (1.0 - p)}
+
+
+def test_dropout_seed_site_and_step_each_change_the_mask(o64):
+    """Two masks that differ in seed, site or step agree on a fraction
+    p^2 + (1-p)^2 of the elements, as independent draws do."""
+    n, p = 1 << 18, 0.3
+    ref = o64.dropout_keep(n, 5, 4, 2, p)
+    expect = p * p + (1 - p) * (1 - p)
+    sigma = math.sqrt(expect * (1 - expect) / n)
+    for seed, site, step in ((6, 4, 2), (5 + (1 << 32), 4, 2), (5, 5, 2), (5, 4, 3)):
+        other = o64.dropout_keep(n, seed, site, step, p)
+        agree = (other == ref).mean()
+        assert abs(agree - expect) < 6 * sigma, (seed, site, step, agree)
+    assert np.array_equal(o64.dropout_keep(n, 5, 4, 2, p), ref)
+
+
+def test_dropout_p0_equals_no_dropout_exactly(o64):
+    params, tok, tgt = tiny_inputs()
+    m = o64.model(TINY.dims(), TINY.B, TINY.T)
+    loss = m.forward(params, tok, tgt)
+    g = m.backward(params)
+    md = o64.model(TINY.dims(), TINY.B, TINY.T)
+    md.set_dropout(0.0, seed=3)
+    assert md.forward(params, tok, tgt) == loss
+    assert np.array_equal(md.backward(params), g)
+    assert np.all(md.keep("att", 1) == 1)
+
+
+def _torch_dropout_step(cfg, params, tok, tgt, keeps, p):
+    """Second opinion for dropout: the architecture in torch float64 with the
+    given keep flags applied where the pages put dropout (embedding output,
+    attention weights after the softmax, each c_proj output before its residual
+    addition), scaled by 1/(1-p); loss and autograd gradients."""
+    import torch
+    import torch.nn.functional as F
+    shapes = syn.tensor_shapes(cfg)
+    ts, off = {}, 0
+    for name in syn.TENSOR_NAMES:
+        n = int(np.prod(shapes[name]))
+        ts[name] = torch.tensor(params[off:off + n].reshape(shapes[name]), dtype=torch.float64,
+                                requires_grad=True)
+        off += n
+    B, T = tok.shape
+    Cc, H, V = cfg.C, cfg.H, cfg.V
+    hs = Cc // H
+    s = 1.0 / (1.0 - p)
+
+    def drop(x, k):
+        return x * torch.tensor(k.reshape(x.shape), dtype=torch.float64) * s
+
+    tok_t = torch.tensor(tok, dtype=torch.long)
+    x = drop(ts["wte"][tok_t] + ts["wpe"][:T], keeps["emb"])
+    causal = torch.ones(T, T, dtype=torch.bool).tril()
+    for l in range(cfg.L):
+        a = F.layer_norm(x, (Cc,), ts["ln1w"][l], ts["ln1b"][l], eps=1e-5)
+        qkv = F.linear(a, ts["qkvw"][l], ts["qkvb"][l])
+        q, k, v = (z.view(B, T, H, hs).transpose(1, 2) for z in qkv.split(Cc, dim=-1))
+        att = (q @ k.transpose(-2, -1)) / math.sqrt(hs)
+        att = torch.softmax(att.masked_fill(~causal, float("-inf")), dim=-1)
+        att = drop(att, keeps["att"][l])
+        y = (att @ v).transpose(1, 2).reshape(B, T, Cc)
+        x = x + drop(F.linear(y, ts["attprojw"][l], ts["attprojb"][l]), keeps["attproj"][l])
+        a = F.layer_norm(x, (Cc,), ts["ln2w"][l], ts["ln2b"][l], eps=1e-5)
+        hmid = F.gelu(F.linear(a, ts["fcw"][l], ts["fcb"][l]), approximate="tanh")
+        x = x + drop(F.linear(hmid, ts["fcprojw"][l], ts["fcprojb"][l]), keeps["fcproj"][l])
+    x = F.layer_norm(x, (Cc,), ts["lnfw"], ts["lnfb"], eps=1e-5)
+    loss = F.cross_entropy((x @ ts["wte"].T).reshape(-1, V), torch.tensor(tgt, dtype=torch.long).reshape(-1))
+    loss.backward()
+    grads = np.concatenate([ts[k].grad.detach().numpy().reshape(-1) for k in syn.TENSOR_NAMES])
+    return float(loss.detach()), grads
+
+
+@pytest.mark.parametrize("cfg", [
+    TINY,
+    syn.Config("ragged", V=97, maxT=24, L=3, H=6, C=48, B=3, T=19, lr=3e-3, wd=0.1),
+])
+def test_dropout_step_matches_torch_autograd(o64, cfg):
+    params = syn.init_params(cfg).astype(np.float64)
+    tok, tgt = syn.draw_tokens(cfg)
+    p = 0.25
+    m = o64.model(cfg.dims(), cfg.B, cfg.T)
+    m.set_dropout(p, seed=2024, step=1)
+    loss = m.forward(params, tok, tgt)
+    g = m.backward(params)
+    keeps = {"emb": m.keep("emb"),
+             "att": [m.keep("att", l) for l in range(cfg.L)],
+             "attproj": [m.keep("attproj", l) for l in range(cfg.L)],
+             "fcproj": [m.keep("fcproj", l) for l in range(cfg.L)]}
+    # the masks are the oracle's definition at each site (site numbering 0, 1 + 3l, ...)
+    N = cfg.B * cfg.T
+    assert np.array_equal(keeps["emb"], o64.dropout_keep(N * cfg.C, 2024, 0, 1, p))
+    assert np.array_equal(keeps["att"][1], o64.dropout_keep(cfg.B * cfg.H * cfg.T ** 2, 2024, 4, 1, p))
+    assert np.array_equal(keeps["fcproj"][0], o64.dropout_keep(N * cfg.C, 2024, 3, 1, p))
+    t_loss, t_grads = _torch_dropout_step(cfg, params, tok, tgt, keeps, p)
+    assert abs(loss - t_loss) < 1e-12
+    assert np.abs(g - t_grads).max() < 1e-12 * max(1.0, np.abs(t_grads).max())
+    # dropout changed the loss (the masks are in effect)
+    m0 = o64.model(cfg.dims(), cfg.B, cfg.T)
+    assert abs(m0.forward(params, tok, tgt) - loss) > 1e-6
+
+
+def test_dropout_gradcheck_directional(o64):
+    """With the masks fixed by (seed, step), the dropout loss is a smooth
+    function of the parameters: central differences match the backward."""
+    params, tok, tgt = tiny_inputs()
+    m = o64.model(TINY.dims(), TINY.B, TINY.T)
+    m.set_dropout(0.4, seed=77, step=5)
+    m.forward(params, tok, tgt)
+    grads = m.backward(params)
+    rng = np.random.default_rng(16)
+    for _ in range(2):
+        d = rng.normal(size=params.size)
+        h = 1e-6
+        f = lambda s: m.forward(params + s * h * d, tok, tgt)
+        fd = (-f(2) + 8 * f(1) - 8 * f(-1) + f(-2)) / (12 * h)
+        assert abs(fd - grads @ d) <= 1e-6 * abs(grads @ d) + 1e-9
