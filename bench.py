@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="124M", choices=list(syn.CONFIGS))
     ap.add_argument("--mode", default="bf16", choices=["bf16", "tf32", "fp32"])
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability of the training step (default 0: the step without dropout)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
@@ -215,6 +217,10 @@ def run_ours(args, cfg):
 
     params = torch.from_numpy(syn.init_params(cfg)).to(dev)
     model = GPT2(cfg, params, maxB=B, mode=args.mode)
+    if args.dropout > 0:
+        rc = model.set_dropout(args.dropout, 1234 + rank)
+        if rc != 0:
+            raise RuntimeError(f"set_dropout failed: {binding.strerror(rc)}")
     stream = model.stream
     # a pool of distinct batches (seeded per rank), resident on the device
     pool = []
@@ -356,6 +362,7 @@ def run_ours(args, cfg):
         "data": "synthetic (seeded N(0,0.02) init, Zipf(1.1) tokens, next-token targets)",
         "config": {"workload": cfg.name, "global_batch": B * world, "seq_len": T,
                    "mode": args.mode, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "dropout": args.dropout,
                    "l2": "working set ~15 GB >> 126 MB L2, no flush"},
         "loss_first_last": [round(losses[0], 5), round(losses[-1], 5)],
         "step_tflops": round(mfu, 1),

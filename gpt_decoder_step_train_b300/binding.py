@@ -22,7 +22,7 @@ STATUS_BAD_TOKEN, STATUS_BAD_TARGET, STATUS_TIMEOUT = 1, 2, 4
 BIAS_GRAD_NOALLOC_MAX_PARTIALS = 1 << 20
 TRACE_CLASSES = ("encoder_fwd", "layernorm_fwd", "matmul_fwd", "attention_fwd", "crossentropy",
                  "matmul_bwd_input", "matmul_bwd_weight", "layernorm_bwd", "attention_bwd",
-                 "encoder_bwd", "adamw", "other", "bias_grad")
+                 "encoder_bwd", "adamw", "other", "bias_grad", "dropout")
 
 
 class gpt2_gemm_args(C.Structure):
@@ -50,6 +50,7 @@ SIGNATURES = {
     "gpt2_create": (_i, [_vp, _vp, _vp]),
     "gpt2_forward": (_f, [_vp, _vp, _vp, _i, _i]),
     "gpt2_eval": (_f, [_vp, _vp, _vp, _i, _i]),
+    "gpt2_set_dropout": (_i, [_vp, _f, C.c_ulonglong]),
     "gpt2_decode": (_i, [_vp, _vp, _i, _i, _vp]),
     "gpt2_backward": (_i, [_vp]),
     "gpt2_adamw": (_i, [_vp, _f, _f, _f, _f, _f, _i]),
@@ -88,6 +89,13 @@ SIGNATURES = {
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,
                                         _vp, _vp]),
+    "gpt2_op_attention_forward_dropout": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _vp, _vp]),
+    "gpt2_op_attention_backward_dropout": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i,
+                                                _vp, _f, _vp, _vp]),
+    "gpt2_op_dropout_mask_words": (_sz, [C.c_longlong, _i]),
+    "gpt2_op_dropout_mask": (_i, [_vp, C.c_longlong, _i, _i, C.c_ulonglong, C.c_uint, C.c_uint, _f, _vp]),
+    "gpt2_op_dropout_residual": (_i, [_vp, _vp, _vp, _i, _i, _f, _vp]),
+    "gpt2_op_dropout_backward": (_i, [_vp, _i, _vp, _vp, _i, _i, _f, _vp]),
     "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_crossentropy_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp]),
@@ -198,6 +206,10 @@ class GPT2:
     def decode(self, tokens, pos, logits):
         """Advance len(tokens) sequences by one position; logits [B, V] (device) receives the new row."""
         return lib().gpt2_decode(self.h, ptr(tokens), int(tokens.shape[0]), pos, ptr(logits))
+
+    def set_dropout(self, p, seed=0):
+        """Dropout with probability p for the following training forwards (0: off)."""
+        return lib().gpt2_set_dropout(self.h, float(p), int(seed))
 
     def backward(self):
         return lib().gpt2_backward(self.h)

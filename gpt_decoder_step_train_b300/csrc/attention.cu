@@ -22,31 +22,54 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "dropout.cuh"
 
 namespace gpt2k {
 
 constexpr int AT_ROWS = 128;   // rows (threads) per block
 constexpr int AT_KT = 32;      // rows of the other side per shared-memory tile
 
-// Load `HSP` floats of row r of a [.., ld] matrix at column c0, hs of them real.
-template <int HSP>
-__device__ __forceinline__ void load_row(float* dst, const float* src, int hs, float mul) {
+// Four consecutive elements as floats, and back.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+// Load `HSP` values of one row (hs of them real) as floats times mul.
+template <int HSP, typename Tv>
+__device__ __forceinline__ void load_row(float* dst, const Tv* src, int hs, float mul) {
 #pragma unroll
     for (int d = 0; d < HSP; d += 4) {
-        float4 v = d < hs ? *reinterpret_cast<const float4*>(src + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = d < hs ? ld4(src + d) : make_float4(0.f, 0.f, 0.f, 0.f);
         dst[d] = v.x * mul; dst[d + 1] = v.y * mul; dst[d + 2] = v.z * mul; dst[d + 3] = v.w * mul;
     }
 }
 
-// Cooperative load of rows [r0, r0+AT_KT) (zeros past T) of up to two column
-// blocks into shared tiles [AT_KT][HSP].
-template <int HSP>
-__device__ __forceinline__ void load_tile(float (*dst)[HSP], const float* base, size_t ld, int r0,
-                                          int T, int hs) {
+template <int HSP, typename Tv>
+__device__ __forceinline__ void store_row(Tv* dst, const float* v, int hs, float mul) {
+#pragma unroll
+    for (int d = 0; d < HSP; d += 4)
+        if (d < hs) st4(dst + d, make_float4(v[d] * mul, v[d + 1] * mul, v[d + 2] * mul, v[d + 3] * mul));
+}
+
+// Cooperative load of rows [r0, r0+AT_KT) (zeros past T) into a shared tile [AT_KT][HSP].
+template <int HSP, typename Tv>
+__device__ __forceinline__ void load_tile(float (*dst)[HSP], const Tv* base, size_t ld, int r0, int T, int hs) {
     for (int idx = threadIdx.x; idx < AT_KT * (HSP / 4); idx += blockDim.x) {
         int r = idx / (HSP / 4), d = (idx % (HSP / 4)) * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r0 + r < T && d < hs) v = *reinterpret_cast<const float4*>(base + (size_t)(r0 + r) * ld + d);
+        if (r0 + r < T && d < hs) v = ld4(base + (size_t)(r0 + r) * ld + d);
         *reinterpret_cast<float4*>(&dst[r][d]) = v;
     }
 }
@@ -59,17 +82,23 @@ __device__ __forceinline__ float dot_row(const float* a, const float* b) {
     return s;
 }
 
-template <int HSP>
+// Dropout on the attention weights: `bits` holds one keep bit per (b, h, i, j),
+// rows (b, h, i) of W = ceil(T/32) words (null: no dropout); kept weights are
+// scaled by ks = 1/(1-p).  The softmax normaliser and the saved log-sum-exp
+// are those of the undropped weights.
+template <int HSP, typename Tv>
 __global__ void __launch_bounds__(AT_ROWS)
-attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __restrict__ qkv, int T,
-              int C, int H, int hs, float scale) {
+attn_fwd_simt(Tv* __restrict__ y, float* __restrict__ lse, const Tv* __restrict__ qkv, int T,
+              int C, int H, int hs, float scale, const uint32_t* __restrict__ bits, float ks) {
     __shared__ __align__(16) float Ks[AT_KT][HSP];
     __shared__ __align__(16) float Vs[AT_KT][HSP];
     const int b = blockIdx.z, h = blockIdx.y, q0 = blockIdx.x * AT_ROWS;
     const int i = q0 + threadIdx.x;
     const bool active = i < T;
     const size_t ld = 3 * (size_t)C;
-    const float* base = qkv + (size_t)b * T * ld;
+    const Tv* base = qkv + (size_t)b * T * ld;
+    const uint32_t* brow =
+        bits && active ? bits + (((size_t)b * H + h) * T + i) * (size_t)((T + 31) >> 5) : nullptr;
     float q[HSP], o[HSP];
     if (active) load_row<HSP>(q, base + (size_t)i * ld + h * hs, hs, scale);
 #pragma unroll
@@ -84,6 +113,7 @@ attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __res
         if (!active) continue;
         const int jn = min(AT_KT, i - k0 + 1);
         if (jn <= 0) continue;
+        const uint32_t mw = brow ? brow[k0 >> 5] : 0xffffffffu;
         float s[AT_KT];
         float tmax = m;
 #pragma unroll
@@ -102,6 +132,7 @@ attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __res
             if (j < jn) {
                 float p = expf(s[j] - tmax);
                 l += p;
+                if (!((mw >> j) & 1u)) p = 0.f;
 #pragma unroll
                 for (int d = 0; d < HSP; d++) o[d] = fmaf(p, Vs[j][d], o[d]);
             }
@@ -109,11 +140,7 @@ attn_fwd_simt(float* __restrict__ y, float* __restrict__ lse, const float* __res
         m = tmax;
     }
     if (!active) return;
-    const float inv = 1.f / l;
-    float* yr = y + ((size_t)b * T + i) * C + h * hs;
-#pragma unroll
-    for (int d = 0; d < HSP; d += 4)
-        if (d < hs) *reinterpret_cast<float4*>(yr + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+    store_row<HSP>(y + ((size_t)b * T + i) * C + h * hs, o, hs, ks / l);
     lse[((size_t)b * H + h) * T + i] = m + logf(l);
 }
 
@@ -186,18 +213,21 @@ static void launch_dot(float* D, const void* dy, const void* y, int B, int T, in
 }
 
 // dQ: one thread per query row i; key/value tiles j <= i in shared memory.
-template <int HSP>
+// With dropout, dP_ij = keep_ij * ks * (dO_i . V_j).
+template <int HSP, typename Tv>
 __global__ void __launch_bounds__(AT_ROWS)
-attn_bwd_dq_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
-                 const float* __restrict__ qkv, const float* __restrict__ lse,
-                 const float* __restrict__ D, int T, int C, int H, int hs, float scale) {
+attn_bwd_dq_simt(Tv* __restrict__ dqkv, const Tv* __restrict__ dy, const Tv* __restrict__ qkv,
+                 const float* __restrict__ lse, const float* __restrict__ D, int T, int C, int H, int hs,
+                 float scale, const uint32_t* __restrict__ bits, float ks) {
     __shared__ __align__(16) float Ks[AT_KT][HSP];
     __shared__ __align__(16) float Vs[AT_KT][HSP];
     const int b = blockIdx.z, h = blockIdx.y, q0 = blockIdx.x * AT_ROWS;
     const int i = q0 + threadIdx.x;
     const bool active = i < T;
     const size_t ld = 3 * (size_t)C;
-    const float* base = qkv + (size_t)b * T * ld;
+    const Tv* base = qkv + (size_t)b * T * ld;
+    const uint32_t* brow =
+        bits && active ? bits + (((size_t)b * H + h) * T + i) * (size_t)((T + 31) >> 5) : nullptr;
     float q[HSP], g[HSP], dq[HSP];
     float li = 0.f, Di = 0.f;
     if (active) {
@@ -216,38 +246,42 @@ attn_bwd_dq_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
         __syncthreads();
         if (!active) continue;
         const int jn = min(AT_KT, i - k0 + 1);
+        const uint32_t mw = brow && jn > 0 ? brow[k0 >> 5] : 0xffffffffu;
 #pragma unroll 4
         for (int j = 0; j < jn; j++) {
             float p = expf(dot_row<HSP>(q, Ks[j]) - li);
-            float ds = p * (dot_row<HSP>(g, Vs[j]) - Di);
+            float dp = dot_row<HSP>(g, Vs[j]);
+            if (brow) dp = ((mw >> j) & 1u) ? dp * ks : 0.f;
+            float ds = p * (dp - Di);
 #pragma unroll
             for (int d = 0; d < HSP; d++) dq[d] = fmaf(ds, Ks[j][d], dq[d]);
         }
     }
     if (!active) return;
-    float* out = dqkv + ((size_t)b * T + i) * ld + h * hs;
-#pragma unroll
-    for (int d = 0; d < HSP; d += 4)
-        if (d < hs) *reinterpret_cast<float4*>(out + d) = make_float4(dq[d] * scale, dq[d + 1] * scale, dq[d + 2] * scale, dq[d + 3] * scale);
+    store_row<HSP>(dqkv + ((size_t)b * T + i) * ld + h * hs, dq, hs, scale);
 }
 
 // dK and dV: one thread per key row j; query tiles i >= j in shared memory.
-// WANT_DK selects dK (needs V_j too) or dV.
-template <int HSP, bool WANT_DK>
+// WANT_DK selects dK (needs V_j too) or dV.  With dropout the keep bits of a
+// query tile's rows for this block's 128 keys are staged in shared memory.
+template <int HSP, typename Tv, bool WANT_DK>
 __global__ void __launch_bounds__(AT_ROWS)
-attn_bwd_dkv_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
-                  const float* __restrict__ qkv, const float* __restrict__ lse,
-                  const float* __restrict__ D, int T, int C, int H, int hs, float scale) {
+attn_bwd_dkv_simt(Tv* __restrict__ dqkv, const Tv* __restrict__ dy, const Tv* __restrict__ qkv,
+                  const float* __restrict__ lse, const float* __restrict__ D, int T, int C, int H, int hs,
+                  float scale, const uint32_t* __restrict__ bits, float ks) {
     __shared__ __align__(16) float Qs[AT_KT][HSP];
     __shared__ __align__(16) float Gs[AT_KT][HSP];
     __shared__ float Ls[AT_KT], Ds[AT_KT];
+    __shared__ uint32_t Ms[AT_KT][AT_ROWS / 32];
     const int b = blockIdx.z, h = blockIdx.y, k0b = blockIdx.x * AT_ROWS;
     const int j = k0b + threadIdx.x;
     const bool active = j < T;
     const size_t ld = 3 * (size_t)C;
-    const float* base = qkv + (size_t)b * T * ld;
+    const Tv* base = qkv + (size_t)b * T * ld;
     const float* lse_bh = lse + ((size_t)b * H + h) * T;
     const float* D_bh = D + ((size_t)b * H + h) * T;
+    const int W = (T + 31) >> 5;
+    const uint32_t* bits_bh = bits ? bits + ((size_t)b * H + h) * T * (size_t)W : nullptr;
     float k[HSP], v[HSP], acc[HSP];
     if (active) {
         load_row<HSP>(k, base + (size_t)j * ld + C + h * hs, hs, scale);
@@ -264,45 +298,74 @@ attn_bwd_dkv_simt(float* __restrict__ dqkv, const float* __restrict__ dy,
             Ls[threadIdx.x] = ii < T ? lse_bh[ii] : 0.f;
             Ds[threadIdx.x] = ii < T ? D_bh[ii] : 0.f;
         }
+        if (bits_bh) {
+            for (int idx = threadIdx.x; idx < AT_KT * (AT_ROWS / 32); idx += blockDim.x) {
+                const int r = idx / (AT_ROWS / 32), kw = (k0b >> 5) + idx % (AT_ROWS / 32);
+                Ms[r][idx % (AT_ROWS / 32)] = i0 + r < T && kw < W ? bits_bh[(size_t)(i0 + r) * W + kw] : 0u;
+            }
+        }
         __syncthreads();
         if (!active) continue;
         const int ibeg = max(0, j - i0), iend = min(AT_KT, T - i0);
 #pragma unroll 4
         for (int r = ibeg; r < iend; r++) {
             float p = expf(dot_row<HSP>(k, Qs[r]) - Ls[r]);
+            const bool kept = !bits_bh || ((Ms[r][threadIdx.x >> 5] >> (threadIdx.x & 31)) & 1u);
             if (WANT_DK) {
-                float ds = p * (dot_row<HSP>(v, Gs[r]) - Ds[r]);
+                float dp = dot_row<HSP>(v, Gs[r]);
+                if (bits_bh) dp = kept ? dp * ks : 0.f;
+                float ds = p * (dp - Ds[r]);
 #pragma unroll
                 for (int d = 0; d < HSP; d++) acc[d] = fmaf(ds, Qs[r][d], acc[d]);
             } else {
+                const float a = bits_bh ? (kept ? p * ks : 0.f) : p;
 #pragma unroll
-                for (int d = 0; d < HSP; d++) acc[d] = fmaf(p, Gs[r][d], acc[d]);
+                for (int d = 0; d < HSP; d++) acc[d] = fmaf(a, Gs[r][d], acc[d]);
             }
         }
     }
     if (!active) return;
-    const float mul = WANT_DK ? scale : 1.f;
-    float* out = dqkv + ((size_t)b * T + j) * ld + (WANT_DK ? C : 2 * C) + h * hs;
-#pragma unroll
-    for (int d = 0; d < HSP; d += 4)
-        if (d < hs) *reinterpret_cast<float4*>(out + d) = make_float4(acc[d] * mul, acc[d + 1] * mul, acc[d + 2] * mul, acc[d + 3] * mul);
+    store_row<HSP>(dqkv + ((size_t)b * T + j) * ld + (WANT_DK ? C : 2 * C) + h * hs, acc, hs,
+                   WANT_DK ? scale : 1.f);
 }
 
-template <int HSP>
-static void launch_fwd(float* y, float* lse, const float* qkv, int B, int T, int C, int H, int hs,
-                       cudaStream_t st) {
+template <int HSP, typename Tv>
+static void launch_fwd(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int hs,
+                       const uint32_t* bits, float ks, cudaStream_t st) {
     dim3 grid(ceil_div(T, AT_ROWS), H, B);
-    count_launch(), attn_fwd_simt<HSP><<<grid, AT_ROWS, 0, st>>>(y, lse, qkv, T, C, H, hs, 1.f / sqrtf((float)hs));
+    count_launch(), attn_fwd_simt<HSP, Tv><<<grid, AT_ROWS, 0, st>>>(
+        static_cast<Tv*>(y), lse, static_cast<const Tv*>(qkv), T, C, H, hs, 1.f / sqrtf((float)hs), bits, ks);
 }
 
-template <int HSP>
-static void launch_bwd(float* dqkv, const float* dy, const float* qkv, const float* lse,
-                       const float* D, int B, int T, int C, int H, int hs, cudaStream_t st) {
+template <int HSP, typename Tv>
+static void launch_bwd(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D, int B,
+                       int T, int C, int H, int hs, const uint32_t* bits, float ks, cudaStream_t st) {
     dim3 grid(ceil_div(T, AT_ROWS), H, B);
     float scale = 1.f / sqrtf((float)hs);
-    count_launch(), attn_bwd_dq_simt<HSP><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
-    count_launch(), attn_bwd_dkv_simt<HSP, true><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
-    count_launch(), attn_bwd_dkv_simt<HSP, false><<<grid, AT_ROWS, 0, st>>>(dqkv, dy, qkv, lse, D, T, C, H, hs, scale);
+    Tv* o = static_cast<Tv*>(dqkv);
+    const Tv* g = static_cast<const Tv*>(dy);
+    const Tv* x = static_cast<const Tv*>(qkv);
+    count_launch(), attn_bwd_dq_simt<HSP, Tv><<<grid, AT_ROWS, 0, st>>>(o, g, x, lse, D, T, C, H, hs, scale, bits, ks);
+    count_launch(), attn_bwd_dkv_simt<HSP, Tv, true><<<grid, AT_ROWS, 0, st>>>(o, g, x, lse, D, T, C, H, hs, scale,
+                                                                               bits, ks);
+    count_launch(), attn_bwd_dkv_simt<HSP, Tv, false><<<grid, AT_ROWS, 0, st>>>(o, g, x, lse, D, T, C, H, hs, scale,
+                                                                                bits, ks);
+}
+
+template <typename Tv>
+static void simt_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int hs,
+                         const uint32_t* bits, float ks, cudaStream_t st) {
+    if (hs <= 16) launch_fwd<16, Tv>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
+    else if (hs <= 32) launch_fwd<32, Tv>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
+    else launch_fwd<64, Tv>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
+}
+
+template <typename Tv>
+static void simt_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D, int B,
+                          int T, int C, int H, int hs, const uint32_t* bits, float ks, cudaStream_t st) {
+    if (hs <= 16) launch_bwd<16, Tv>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, bits, ks, st);
+    else if (hs <= 32) launch_bwd<32, Tv>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, bits, ks, st);
+    else launch_bwd<64, Tv>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, bits, ks, st);
 }
 
 int attention_tc_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int H,
@@ -317,13 +380,10 @@ int attention_tc_backward(float* dqkv, const float* dy, const float* qkv, const 
 bool attention_tc_supported(int hs);
 bool attention_tc05_supported(int hs, int C);
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
-                           cudaStream_t st);
+                           cudaStream_t st, const uint32_t* bits, float ks);
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum);
-
-}  // namespace gpt2k
-
-using namespace gpt2k;
+                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum,
+                            const uint32_t* bits, float ks);
 
 static bool attn_args_ok(int B, int T, int C, int H) {
     if (B < 1 || T < 1 || C < 4 || H < 1 || C % H) return false;
@@ -331,26 +391,89 @@ static bool attn_args_ok(int B, int T, int C, int H) {
     return hs % 4 == 0 && hs <= 64;
 }
 
-GPT2_API int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
-                                       int H, int mode, int* status, void* stream) {
+// Dispatch: BF16 mode takes the tcgen05 kernels for head size 64, the
+// mma.sync kernels for head sizes 16 and 32 (no dropout), else the CUDA-core
+// kernels on bf16; FP32 and TF32 modes take the mma.sync TF32 kernels where
+// they apply (no dropout), else the CUDA-core kernels on fp32.
+int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int mode, int* status,
+                      cudaStream_t st, const uint32_t* bits, float p) {
     if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
-    if (!aligned16(y) || !aligned16(qkv)) return GPT2_EINVAL;
+    if (!aligned16(y) || !aligned16(qkv) || !(p >= 0.f && p < 1.f)) return GPT2_EINVAL;
     int hs = C / H;
-    cudaStream_t st = as_stream(stream);
+    const float ks = bits ? dropout_scale(p) : 1.f;
     if (mode == GPT2_MODE_BF16) {
-        if (attention_tc05_supported(hs, C)) return attention_tc05_forward(y, lse, qkv, B, T, C, H, status, st);
-        if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
-        return attention_bf16_forward(y, lse, qkv, B, T, C, H, st);
+        if (attention_tc05_supported(hs, C))
+            return attention_tc05_forward(y, lse, qkv, B, T, C, H, status, st, bits, ks);
+        if (!bits && attention_tc_supported(hs)) return attention_bf16_forward(y, lse, qkv, B, T, C, H, st);
+        simt_forward<__nv_bfloat16>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
+        GPT2_LAUNCH_CHECK();
+        return GPT2_OK;
     }
-    float* yf = static_cast<float*>(y);
-    const float* qf = static_cast<const float*>(qkv);
-    if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
-        return attention_tc_forward(yf, lse, qf, B, T, C, H, status, st);
-    if (hs <= 16) launch_fwd<16>(yf, lse, qf, B, T, C, H, hs, st);
-    else if (hs <= 32) launch_fwd<32>(yf, lse, qf, B, T, C, H, hs, st);
-    else launch_fwd<64>(yf, lse, qf, B, T, C, H, hs, st);
+    if (mode == GPT2_MODE_TF32 && !bits && attention_tc_supported(hs))
+        return attention_tc_forward(static_cast<float*>(y), lse, static_cast<const float*>(qkv), B, T, C, H,
+                                    status, st);
+    simt_forward<float>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
+}
+
+int attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
+                               int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
+                               cudaStream_t st, float* colsum, bool* colsum_done, const uint32_t* bits, float p) {
+    if (colsum_done) *colsum_done = false;
+    if (!dqkv || !dy || !qkv || !y || !lse || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
+    if (!aligned16(dqkv) || !aligned16(dy) || !aligned16(qkv) || !aligned16(y) || !(p >= 0.f && p < 1.f))
+        return GPT2_EINVAL;
+    if (!scratch || scratch_bytes < round_up((size_t)B * H * T * sizeof(float), 256)) return GPT2_ENOMEM;
+    int hs = C / H;
+    const float ks = bits ? dropout_scale(p) : 1.f;
+    // D = rowsum(dO o O) with O the output that met dO (after dropout)
+    float* D = reinterpret_cast<float*>(scratch);
+    if (mode == GPT2_MODE_BF16) {
+        launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
+        GPT2_LAUNCH_CHECK();
+        if (attention_tc05_supported(hs, C)) {
+            if (colsum_done) *colsum_done = colsum != nullptr;
+            return attention_tc05_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st,
+                                           colsum_done ? colsum : nullptr, bits, ks);
+        }
+        if (!bits && attention_tc_supported(hs))
+            return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
+        simt_backward<__nv_bfloat16>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, bits, ks, st);
+        GPT2_LAUNCH_CHECK();
+        return GPT2_OK;
+    }
+    launch_dot<float>(D, dy, y, B, T, C, H, hs, st);
+    GPT2_LAUNCH_CHECK();
+    if (mode == GPT2_MODE_TF32 && !bits && attention_tc_supported(hs))
+        return attention_tc_backward(static_cast<float*>(dqkv), static_cast<const float*>(dy),
+                                     static_cast<const float*>(qkv), lse, D, B, T, C, H, status, st);
+    simt_backward<float>(dqkv, dy, qkv, lse, D, B, T, C, H, hs, bits, ks, st);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+int attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
+                       int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
+                       cudaStream_t st, float* colsum, bool* colsum_done) {
+    return attention_backward_dropout(dqkv, dy, qkv, y, lse, B, T, C, H, scratch, scratch_bytes, mode, status, st,
+                                      colsum, colsum_done, nullptr, 0.f);
+}
+
+}  // namespace gpt2k
+
+using namespace gpt2k;
+
+GPT2_API int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
+                                       int H, int mode, int* status, void* stream) {
+    return attention_forward(y, lse, qkv, B, T, C, H, mode, status, as_stream(stream), nullptr, 0.f);
+}
+
+GPT2_API int gpt2_op_attention_forward_dropout(void* y, float* lse, const void* qkv, int B, int T, int C, int H,
+                                               int mode, const uint32_t* bits, float p, int* status,
+                                               void* stream) {
+    if (!bits) return GPT2_EINVAL;
+    return attention_forward(y, lse, qkv, B, T, C, H, mode, status, as_stream(stream), bits, p);
 }
 
 GPT2_API size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
@@ -358,44 +481,14 @@ GPT2_API size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
     return round_up((size_t)B * H * T * sizeof(float), 256);
 }
 
-namespace gpt2k {
-
-int attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
-                       int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
-                       cudaStream_t st, float* colsum, bool* colsum_done) {
-    if (colsum_done) *colsum_done = false;
-    if (!dqkv || !dy || !qkv || !y || !lse || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
-    if (!aligned16(dqkv) || !aligned16(dy) || !aligned16(qkv) || !aligned16(y)) return GPT2_EINVAL;
-    if (!scratch || scratch_bytes < gpt2_op_attention_backward_scratch_bytes(B, T, H))
-        return GPT2_ENOMEM;
-    int hs = C / H;
-    float* D = reinterpret_cast<float*>(scratch);
-    if (mode == GPT2_MODE_BF16) {
-        if (!attention_tc_supported(hs)) return GPT2_ENOTSUP;
-        launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
-        GPT2_LAUNCH_CHECK();
-        if (attention_tc05_supported(hs, C)) {
-            if (colsum_done) *colsum_done = colsum != nullptr;
-            return attention_tc05_backward(dqkv, dy, qkv, lse, D, B, T, C, H, status, st,
-                                           colsum_done ? colsum : nullptr);
-        }
-        return attention_bf16_backward(dqkv, dy, qkv, lse, D, B, T, C, H, st);
-    }
-    float* dq = static_cast<float*>(dqkv);
-    const float* g = static_cast<const float*>(dy);
-    const float* x = static_cast<const float*>(qkv);
-    launch_dot<float>(D, dy, y, B, T, C, H, hs, st);
-    GPT2_LAUNCH_CHECK();
-    if (mode == GPT2_MODE_TF32 && attention_tc_supported(hs))
-        return attention_tc_backward(dq, g, x, lse, D, B, T, C, H, status, st);
-    if (hs <= 16) launch_bwd<16>(dq, g, x, lse, D, B, T, C, H, hs, st);
-    else if (hs <= 32) launch_bwd<32>(dq, g, x, lse, D, B, T, C, H, hs, st);
-    else launch_bwd<64>(dq, g, x, lse, D, B, T, C, H, hs, st);
-    GPT2_LAUNCH_CHECK();
-    return GPT2_OK;
+GPT2_API int gpt2_op_attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, const void* y,
+                                                const float* lse, int B, int T, int C, int H, void* scratch,
+                                                size_t scratch_bytes, int mode, const uint32_t* bits, float p,
+                                                int* status, void* stream) {
+    if (!bits) return GPT2_EINVAL;
+    return attention_backward_dropout(dqkv, dy, qkv, y, lse, B, T, C, H, scratch, scratch_bytes, mode, status,
+                                      as_stream(stream), nullptr, nullptr, bits, p);
 }
-
-}  // namespace gpt2k
 
 GPT2_API int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv,
                                         const void* y, const float* lse, int B, int T, int C,

@@ -131,9 +131,10 @@ __device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int st
     return true;
 }
 
+template <bool DROP>
 __global__ void __launch_bounds__(FWD_THREADS, 2)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
-              int T, int C, int H, float scale_log2, int* status) {
+              int T, int C, int H, float scale_log2, int* status, const uint32_t* __restrict__ bits, float ks) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], s_free[2], p_full[2],
         pv_done[2], drain;
@@ -271,6 +272,10 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
         uint8_t* const pbuf = base_ptr + OFF_P;    // two P buffers, tile j in buffer j & 1
         float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, this half's sum of P
         bool ok = true;
+        // dropout: this row's keep bits, one word per 32 keys
+        const uint32_t* brow = nullptr;
+        if constexpr (DROP)
+            if (row < T) brow = bits + (((size_t)b * H + h) * T + row) * (size_t)((T + 31) >> 5);
         // exchange slot of tile j: pair_val[j & 1][half][r]; barrier pair_bar[quarter][j & 1]
         auto exchange = [&](int j, float v, float* other) -> bool {
             pair_val[j & 1][half][r] = v;
@@ -282,6 +287,11 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             return true;
         };
         for (int j = 0; j < nkv; j++) {
+            uint32_t keep_w = 0xffffffffu;
+            if constexpr (DROP) {
+                const int kw = j * BKV + 32 * half;
+                keep_w = brow && kw < T ? __ldg(brow + (kw >> 5)) : 0u;
+            }
             if (!mbar_wait(smem_u32(&s_full[j & 1]), (uint32_t)(j >> 1) & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
             float s[32];
@@ -319,6 +329,12 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
                 ps[c & 3] += s[c];
             }
             l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+            // dropped weights leave the sum (the softmax normaliser) and miss V
+            if constexpr (DROP) {
+#pragma unroll
+                for (int c = 0; c < 32; c++)
+                    if (!((keep_w >> c) & 1u)) s[c] = 0.f;
+            }
             // a rescale of O needs every earlier P V complete (the last is P_{j-1} V_{j-1})
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 if (!mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, &s_abort, status)) {
@@ -368,7 +384,7 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             tmem_wait_ld(o);
             if (row < T) {
                 const float l = half == 0 ? l_run + l_other : l_other + l_run;
-                const float inv = 1.f / l;
+                const float inv = (DROP ? ks : 1.f) / l;
                 uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)b * T + row) * C + h * HS + 32 * half);
 #pragma unroll
                 for (int c = 0; c < 4; c++)
@@ -422,10 +438,12 @@ constexpr uint32_t DKV_OFF_K = 0, DKV_OFF_V = 16384, DKV_OFF_ST = 32768, DKV_ROW
                    DKV_OFF_DS = DKV_OFF_P + 16384, DKV_SMEM_USED = DKV_OFF_DS + 16384;
 constexpr size_t DKV_SMEM = DKV_SMEM_USED + 1024;
 
+template <bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 2)
 attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                   __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
-                  int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
+                  int T, int C, int H, float scale, int* status, float* __restrict__ colsum,
+                  const uint32_t* __restrict__ bits, float ks) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t k_full, q_full[DKV_STAGES], q_empty[DKV_STAGES], s_full, s_free, p_full,
         pv_done, drain;
@@ -584,7 +602,19 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         uint8_t* const prow = base_ptr + DKV_OFF_P;
         uint8_t* const dsrow = base_ptr + DKV_OFF_DS;
         bool ok = true;
+        // dropout: keep bits are stored by query row (one word per 32 keys); lane
+        // c loads the word of query q0 + c that holds this warp's 32 keys, and a
+        // ballot per key turns the 32 words around so that bit c of keep_t is
+        // the flag of (query q0 + c, this thread's key)
+        const int W = (T + 31) >> 5, kw = (k0 + quarter * 32) >> 5;
+        const uint32_t* bits_bh = nullptr;
+        if constexpr (DROP) bits_bh = bits + ((size_t)b * H + h) * T * (size_t)W;
         for (int t = 0; t < ntile; t++) {
+            uint32_t keep_q = 0u;
+            if constexpr (DROP) {
+                const int qq = (i0 + t) * 64 + 32 * half + lane;
+                keep_q = qq < T && kw < W ? __ldg(bits_bh + (size_t)qq * W + kw) : 0u;
+            }
             // S^T and dP^T ready implies the stage (with lse and D) is full
             if (!mbar_wait(smem_u32(&s_full), (uint32_t)t & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
@@ -608,6 +638,14 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const float4* l4 = reinterpret_cast<const float4*>(rows);
             const float4* d4 = reinterpret_cast<const float4*>(rows + 64);
             const bool diag = q0 < k0 + 127;           // some query of these columns precedes some key
+            uint32_t keep_t = 0xffffffffu;
+            if constexpr (DROP) {
+#pragma unroll
+                for (int kl = 0; kl < 32; kl++) {
+                    const uint32_t v = __ballot_sync(0xffffffffu, (keep_q >> kl) & 1u);
+                    if (lane == kl) keep_t = v;
+                }
+            }
 #pragma unroll
             for (int c4 = 0; c4 < 8; c4++) {
                 const float4 lv = l4[c4], dv = d4[c4];
@@ -617,8 +655,15 @@ attn_bwd_dkv_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     const int c = 4 * c4 + e;
                     float pv = ex2(fmaf(sv[c], c2, -lq[e]));
                     if (diag && q0 + c < key) pv = 0.f;
-                    sv[c] = pv;
-                    dp[c] = pv * (dp[c] - dq[e]);
+                    if constexpr (DROP) {
+                        // dV takes the dropped weight; dP passes the same mask
+                        const bool kept = (keep_t >> c) & 1u;
+                        sv[c] = kept ? pv * ks : 0.f;
+                        dp[c] = pv * ((kept ? dp[c] * ks : 0.f) - dq[e]);
+                    } else {
+                        sv[c] = pv;
+                        dp[c] = pv * (dp[c] - dq[e]);
+                    }
                 }
             }
             // P^T and dS^T buffers are free once the previous tile's products completed
@@ -678,10 +723,12 @@ constexpr uint32_t DQ_OFF_Q = 0, DQ_OFF_DO = 16384, DQ_OFF_ST = 32768, DQ_STAGE 
                    DQ_OFF_DS = DQ_OFF_ST + DQ_STAGES * DQ_STAGE, DQ_SMEM_USED = DQ_OFF_DS + 16384;
 constexpr size_t DQ_SMEM = DQ_SMEM_USED + 1024;
 
+template <bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 2)
 attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                  __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg,
-                 int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
+                 int T, int C, int H, float scale, int* status, float* __restrict__ colsum,
+                 const uint32_t* __restrict__ bits, float ks) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, kv_full[DQ_STAGES], kv_empty[DQ_STAGES], s_full, s_free, p_full,
         pv_done, drain;
@@ -812,7 +859,15 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const float Drow = row < T ? Dg[bh + row] : 0.f;
         uint8_t* const dsrow = base_ptr + DQ_OFF_DS;
         bool ok = true;
+        const uint32_t* brow = nullptr;
+        if constexpr (DROP)
+            if (row < T) brow = bits + (bh + row) * (size_t)((T + 31) >> 5);
         for (int j = 0; j < nkv; j++) {
+            uint32_t keep_w = 0xffffffffu;
+            if constexpr (DROP) {
+                const int kw = j * 64 + 32 * half;
+                keep_w = brow && kw < T ? __ldg(brow + (kw >> 5)) : 0u;
+            }
             if (!mbar_wait(smem_u32(&s_full), (uint32_t)j & 1u, &s_abort, status)) { ok = false; break; }
             tc_fence_after();
             float sv[32], dp[32];
@@ -829,7 +884,8 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int c = 0; c < 32; c++) {
                 float pv = ex2(fmaf(sv[c], c2, -lse2));
                 if (diag && (k0 + c > row || k0 + c >= T)) pv = 0.f;
-                dp[c] = pv * (dp[c] - Drow);
+                if constexpr (DROP) dp[c] = pv * ((((keep_w >> c) & 1u) ? dp[c] * ks : 0.f) - Drow);
+                else dp[c] = pv * (dp[c] - Drow);
             }
             if (j > 0) {
                 if (!mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, &s_abort, status)) { ok = false; break; }
@@ -878,14 +934,18 @@ attn_bwd_dq_tc05(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 bool attention_tc05_supported(int hs, int C) { return hs == at05::HS && C % 8 == 0; }
 
 // y [B,T,C] and lse [B,H,T] from qkv [B,T,3C] (bf16), head size 64.
+// With bits != null: dropout on the attention weights (keep bits by query row,
+// one word per 32 keys), kept weights scaled by ks.
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(attn_fwd_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
-            cudaSuccess) {
+        if (cudaFuncSetAttribute(attn_fwd_tc05<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_fwd_tc05<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
+                cudaSuccess) {
             (void)cudaGetLastError();
             return GPT2_ECUDA;
         }
@@ -899,8 +959,13 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
     if (!encode_tensor_map(&tm, true, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return GPT2_ENOTSUP;
     const float scale_log2 = LOG2E / sqrtf((float)HS);
-    count_launch(), attn_fwd_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), FWD_THREADS, SMEM, st>>>(
-        tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status);
+    const dim3 grid(H, B, (T + BQ - 1) / BQ);
+    if (bits)
+        count_launch(), attn_fwd_tc05<true><<<grid, FWD_THREADS, SMEM, st>>>(
+            tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status, bits, ks);
+    else
+        count_launch(), attn_fwd_tc05<false><<<grid, FWD_THREADS, SMEM, st>>>(
+            tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status, nullptr, 1.f);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }
@@ -914,15 +979,18 @@ namespace gpt2k {
 // colsum != null also the column sums of dqkv per 32-row group
 // ([B * ceil(T/32), 3C], fp32, before bf16 rounding).
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum) {
+                            int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum,
+                            const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(attn_bwd_dkv_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKV_SMEM) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_dq_tc05, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
-                cudaSuccess) {
+        const int ds = (int)DKV_SMEM, qs = (int)DQ_SMEM;
+        const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        if (cudaFuncSetAttribute(attn_bwd_dkv_tc05<false>, a, ds) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_dkv_tc05<true>, a, ds) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_dq_tc05<false>, a, qs) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_dq_tc05<true>, a, qs) != cudaSuccess) {
             (void)cudaGetLastError();
             return GPT2_ECUDA;
         }
@@ -939,10 +1007,18 @@ int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const f
         return GPT2_ENOTSUP;
     const float scale = 1.f / sqrtf((float)HS);
     auto* out = static_cast<__nv_bfloat16*>(dqkv);
-    count_launch(), attn_bwd_dkv_tc05<<<dim3(H, B, (T + 127) / 128), BWD_THREADS, DKV_SMEM, st>>>(
-        tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
-    count_launch(), attn_bwd_dq_tc05<<<dim3(H, B, (T + BQ - 1) / BQ), BWD_THREADS, DQ_SMEM, st>>>(
-        tq, tdo, out, lse, D, T, C, H, scale, status, colsum);
+    const dim3 gk(H, B, (T + 127) / 128), gq(H, B, (T + BQ - 1) / BQ);
+    if (bits) {
+        count_launch(), attn_bwd_dkv_tc05<true><<<gk, BWD_THREADS, DKV_SMEM, st>>>(tq, tdo, out, lse, D, T, C, H, scale,
+                                                                                 status, colsum, bits, ks);
+        count_launch(), attn_bwd_dq_tc05<true><<<gq, BWD_THREADS, DQ_SMEM, st>>>(tq, tdo, out, lse, D, T, C, H, scale,
+                                                                               status, colsum, bits, ks);
+    } else {
+        count_launch(), attn_bwd_dkv_tc05<false><<<gk, BWD_THREADS, DKV_SMEM, st>>>(tq, tdo, out, lse, D, T, C, H,
+                                                                                  scale, status, colsum, nullptr, 1.f);
+        count_launch(), attn_bwd_dq_tc05<false><<<gq, BWD_THREADS, DQ_SMEM, st>>>(tq, tdo, out, lse, D, T, C, H,
+                                                                                scale, status, colsum, nullptr, 1.f);
+    }
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

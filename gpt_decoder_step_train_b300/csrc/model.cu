@@ -18,6 +18,7 @@
 #include <functional>
 #include <vector>
 
+#include "dropout.cuh"
 #include "gemm.cuh"
 
 namespace gpt2k {
@@ -126,6 +127,15 @@ struct gpt2 {
     int B, T;
     bool fwd_targets, have_grads;
     int err;
+    // dropout (gpt2_set_dropout): probability, seed, training forwards drawn
+    // under this seed so far, whether the last forward used it, and the device
+    // buffer {key0, key1, step, 0} followed by the keep bits of every site
+    float pdrop;
+    unsigned long long dseed;
+    uint32_t dstep;
+    bool drop_fwd;
+    uint32_t* dbuf;
+    size_t dbuf_words;
     // tracing: event pairs recorded around each operation, with its class and launches
     bool trace_on;
     std::vector<cudaEvent_t> trace_events;
@@ -240,6 +250,25 @@ static int trace_op(gpt2* m, int cls, const std::function<int()>& f) {
         if (rc_) return rc_;                                               \
     } while (0)
 
+// Keep bits of dropout site `site` for a forward of B x T: the embedding output
+// (site 0), then per layer l the attention weights (1 + 3l, rows (b, h, i) of
+// ceil(T/32) words), the attention c_proj output (2 + 3l) and the MLP c_proj
+// output (3 + 3l), rows (b, t) of ceil(C/32) words.  The first four words of
+// the buffer hold the draw state.
+static size_t drop_words(const gpt2_config& c, int B, int T) {
+    const size_t N = (size_t)B * T, wc = (size_t)(c.C + 31) / 32, wt = (size_t)(T + 31) / 32;
+    return 4 + N * wc + (size_t)c.L * ((size_t)B * c.H * T * wt + 2 * N * wc);
+}
+static uint32_t* drop_bits(gpt2* m, int site) {
+    const gpt2_config& c = m->cfg;
+    const size_t N = (size_t)m->B * m->T, wc = (size_t)(c.C + 31) / 32, wt = (size_t)(m->T + 31) / 32;
+    const size_t att = (size_t)m->B * c.H * m->T * wt, layer = att + 2 * N * wc;
+    uint32_t* base = m->dbuf + 4;
+    if (site == 0) return base;
+    const int l = (site - 1) / 3, k = (site - 1) % 3;
+    return base + N * wc + (size_t)l * layer + (k == 0 ? 0 : att + (size_t)(k - 1) * N * wc);
+}
+
 // with_targets: the cross-entropy runs; grad: it also leaves d(loss)/d(logits)
 static int forward_impl(gpt2* m, int B, int T, bool with_targets, bool grad) {
     const gpt2_config& c = m->cfg;
@@ -249,7 +278,20 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets, bool grad) {
     cudaStream_t st = m->st;
     int* status = &m->flags->status;
     if (b16) OP(OTHER, to_bf16(m->w16, m->params, m->nparams, st));
+    // dropout: draw every site's keep bits (key and step from the device state)
+    const bool drop = m->drop_fwd;
+    const float pd = m->pdrop;
+    if (drop) {
+        OP(DROPOUT, dropout_mask(drop_bits(m, 0), N, C, 0, m->dbuf, 0, 0, 0, pd, st));
+        for (int l = 0; l < L; l++) {
+            OP(DROPOUT, dropout_mask(drop_bits(m, 1 + 3 * l), (long long)B * H * T, T, T, m->dbuf, 0, 1 + 3 * l, 0,
+                                     pd, st));
+            OP(DROPOUT, dropout_mask(drop_bits(m, 2 + 3 * l), N, C, 0, m->dbuf, 0, 2 + 3 * l, 0, pd, st));
+            OP(DROPOUT, dropout_mask(drop_bits(m, 3 + 3 * l), N, C, 0, m->dbuf, 0, 3 + 3 * l, 0, pd, st));
+        }
+    }
     OP(ENCODER_FWD, gpt2_op_encoder_forward(m->x0, m->tok, P(m, WTE), P(m, WPE), B, T, C, c.V, status, st));
+    if (drop) OP(DROPOUT, dropout_residual(m->x0, nullptr, drop_bits(m, 0), N, C, pd, st));
     for (int l = 0; l < L; l++) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
         char* ln1 = Orow(m, m->ln1, l, C);
@@ -269,15 +311,20 @@ static int forward_impl(gpt2* m, int B, int T, bool with_targets, bool grad) {
                                             P(m, LN1W) + l * C, P(m, LN1B) + l * C, N, C, st));
         OP(MATMUL_FWD, linear_forward(qkv, b16, nullptr, ln1, Wl(QKVW, 3 * cc), b16, P(m, QKVB) + l * 3 * C,
                                       nullptr, N, C, 3 * C, 3 * C, 0, mode, status, st));
-        OP(ATTENTION_FWD, gpt2_op_attention_forward(atty, m->lse + l * R * H, qkv, B, T, C, H, mode, status, st));
+        OP(ATTENTION_FWD, attention_forward(atty, m->lse + l * R * H, qkv, B, T, C, H, mode, status, st,
+                                            drop ? drop_bits(m, 1 + 3 * l) : nullptr, drop ? pd : 0.f));
+        // with dropout the residual is added after the c_proj output is dropped
         OP(MATMUL_FWD, linear_forward(res2, false, nullptr, atty, Wl(ATTPROJW, cc), b16, P(m, ATTPROJB) + l * C,
-                                      x, N, C, C, C, 0, mode, status, st));
+                                      drop ? nullptr : x, N, C, C, C, 0, mode, status, st));
+        if (drop) OP(DROPOUT, dropout_residual(res2, x, drop_bits(m, 2 + 3 * l), N, C, pd, st));
         OP(LAYERNORM_FWD, layernorm_forward(ln2, b16, m->ln2_mean + l * R, m->ln2_rstd + l * R, res2,
                                             P(m, LN2W) + l * C, P(m, LN2B) + l * C, N, C, st));
         OP(MATMUL_FWD, linear_forward(fchg, b16, fch, ln2, Wl(FCW, 4 * cc), b16, P(m, FCB) + l * 4 * C, nullptr,
                                       N, C, 4 * C, 4 * C, GPT2_LINEAR_GELU, mode, status, st));
         OP(MATMUL_FWD, linear_forward(res3, false, nullptr, fchg, Wl(FCPROJW, 4 * cc), b16,
-                                      P(m, FCPROJB) + l * C, res2, N, 4 * C, C, C, 0, mode, status, st));
+                                      P(m, FCPROJB) + l * C, drop ? nullptr : res2, N, 4 * C, C, C, 0, mode, status,
+                                      st));
+        if (drop) OP(DROPOUT, dropout_residual(res3, res2, drop_bits(m, 3 + 3 * l), N, C, pd, st));
     }
     const float* xL = m->res3 + (size_t)(L - 1) * R * C;
     OP(LAYERNORM_FWD, layernorm_forward(m->lnf, b16, m->lnf_mean, m->lnf_rstd, xL, P(m, LNFW), P(m, LNFB),
@@ -314,6 +361,13 @@ static int backward_impl(gpt2* m) {
     const void* dres_op = b16 ? static_cast<const void*>(m->dres16) : static_cast<const void*>(m->dres);
     const void* dz_op = b16 ? static_cast<const void*>(m->dz16) : static_cast<const void*>(m->logits);
     const size_t wes = b16 ? 2 : 4;
+    // dropout: the gradient of a dropped c_proj output is keep o dres / (1 - p),
+    // written over the operand copy of dres (BF16 mode) or into dln, which is
+    // free at that point; the bias gradient is then its own column sum
+    const bool drop = m->drop_fwd;
+    const float pd = m->pdrop;
+    void* dbr = b16 ? static_cast<void*>(m->dres16) : static_cast<void*>(m->dln);
+    const void* dbr_op = drop ? static_cast<const void*>(dbr) : dres_op;
     // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
     OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, dz_op, W(m, WTE), b16, nullptr, N, C, c.V,
                                                m->Vp, mode, status, st));
@@ -322,7 +376,7 @@ static int backward_impl(gpt2* m) {
     // ln_f: the residual gradient starts here (written, not accumulated); its
     // column sum is the last block's MLP c_proj bias gradient
     OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LNFW), G(m, LNFB),
-                                                 G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
+                                                 drop ? nullptr : G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
                                                  m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW),
                                                  m->lnf_mean, m->lnf_rstd, N, C, 0, sc, sb, status, st));
     for (int l = L - 1; l >= 0; l--) {
@@ -340,10 +394,14 @@ static int backward_impl(gpt2* m) {
         // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g (its bias
         // gradient came with the LayerNorm backward that produced dres)
         // (with the c_fc bias gradient: the column sums of dh)
-        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dres_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
+        if (drop) {
+            OP(DROPOUT, dropout_backward(dbr, b16, m->dres, drop_bits(m, 3 + 3 * l), N, C, pd, st));
+            OP(BIAS_GRAD, bias_grad_any(G(m, FCPROJB) + l * C, dbr, b16, N, C, C, sc, sb, st));
+        }
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dbr_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
                                                    4 * C, C, C, mode, status, st, G(m, FCB) + l * 4 * C,
                                                    m->colsum, m->colsum_bytes));
-        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dres_op, fchg, b16, N,
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dbr_op, fchg, b16, N,
                                                      4 * C, C, C, sc, sb, mode, status, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dbig, Wl(FCW, 4 * cc), b16, nullptr, N,
@@ -353,19 +411,25 @@ static int backward_impl(gpt2* m) {
         // ln_2: dres += LN'(dln2); the column sum of the result is the attention
         // c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN2W) + l * C, G(m, LN2B) + l * C,
-                                                     G(m, ATTPROJB) + l * C, m->dln, res2, P(m, LN2W) + l * C,
+                                                     drop ? nullptr : G(m, ATTPROJB) + l * C, m->dln, res2,
+                                                     P(m, LN2W) + l * C,
                                                      m->ln2_mean + l * R, m->ln2_rstd + l * R, N, C, 1, sc, sb,
                                                      status, st));
         // attention c_proj (bias gradient: with ln_2's backward above)
-        OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, dres_op, Wl(ATTPROJW, cc), b16, nullptr, N,
+        if (drop) {
+            OP(DROPOUT, dropout_backward(dbr, b16, m->dres, drop_bits(m, 2 + 3 * l), N, C, pd, st));
+            OP(BIAS_GRAD, bias_grad_any(G(m, ATTPROJB) + l * C, dbr, b16, N, C, C, sc, sb, st));
+        }
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, dbr_op, Wl(ATTPROJW, cc), b16, nullptr, N,
                                                    C, C, C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dres_op, atty, b16, N, C, C, C,
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dbr_op, atty, b16, N, C, C, C,
                                                      sc, sb, mode, status, st));
         // attention; the tcgen05 path also leaves the column sums of dqkv per
         // 32 rows, which give the qkv bias gradient at once
         bool qkv_colsum = false;
-        OP(ATTENTION_BWD, attention_backward(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C, H, sc,
-                                             sb, mode, status, st, m->colsum, &qkv_colsum));
+        OP(ATTENTION_BWD, attention_backward_dropout(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C, H,
+                                                     sc, sb, mode, status, st, m->colsum, &qkv_colsum,
+                                                     drop ? drop_bits(m, 1 + 3 * l) : nullptr, drop ? pd : 0.f));
         if (qkv_colsum)
             OP(BIAS_GRAD, colsum_reduce(G(m, QKVB) + l * 3 * C, m->colsum, B * ceil_div(T, 32), 3 * C, st));
         // c_attn
@@ -378,10 +442,11 @@ static int backward_impl(gpt2* m) {
         // ln_1: dres += LN'(dln1); the column sum of the result is the previous
         // block's MLP c_proj bias gradient
         OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN1W) + l * C, G(m, LN1B) + l * C,
-                                                     l > 0 ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
+                                                     l > 0 && !drop ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
                                                      m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R,
                                                      m->ln1_rstd + l * R, N, C, 1, sc, sb, status, st));
     }
+    if (drop) OP(DROPOUT, dropout_backward(m->dres, false, m->dres, drop_bits(m, 0), N, C, pd, st));
     OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V,
                                              sc, sb, st));
     return GPT2_OK;
@@ -547,6 +612,18 @@ static float forward_common(gpt2* m, const int* tokens, const int* targets, int 
     }
     m->B = B;
     m->T = T;
+    // dropout in the training forward (not in evaluation): this call's draw
+    // state goes to the device before the step, so a replayed graph draws anew
+    m->drop_fwd = grad && m->pdrop > 0.f && m->dbuf;
+    if (m->drop_fwd) {
+        const uint32_t h[4] = {(uint32_t)m->dseed, (uint32_t)(m->dseed >> 32), m->dstep, 0u};
+        if (cudaMemcpyAsync(m->dbuf, h, sizeof(h), cudaMemcpyHostToDevice, m->st) != cudaSuccess) {
+            (void)cudaGetLastError();
+            record(m, GPT2_ECUDA);
+            return NAN;
+        }
+        m->dstep++;
+    }
     const int kind = targets ? (grad ? 0 : 2) : 1;
     int rc = run_graphed(m, kind, B, T, [&]() -> int { return forward_impl(m, B, T, targets != nullptr, grad); });
     if (rc) { record(m, rc); return NAN; }
@@ -696,12 +773,42 @@ GPT2_API int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logi
     return GPT2_OK;
 }
 
+GPT2_API int gpt2_set_dropout(gpt2* m, float p, unsigned long long seed) {
+    if (!m) return GPT2_EINVAL;
+    if (!(p >= 0.f && p < 1.f)) { record(m, GPT2_EINVAL); return GPT2_EINVAL; }
+    if (p > 0.f && !m->dbuf) {
+        const size_t words = drop_words(m->cfg, m->cfg.maxB, m->cfg.maxT);
+        if (cudaStreamSynchronize(m->st) != cudaSuccess ||
+            cudaMalloc(reinterpret_cast<void**>(&m->dbuf), words * sizeof(uint32_t)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            m->dbuf = nullptr;
+            record(m, GPT2_ENOMEM);
+            return GPT2_ENOMEM;
+        }
+        m->dbuf_words = words;
+    }
+    if (p != m->pdrop) {
+        // the captured forward and backward differ with and without dropout
+        // and carry p in their launches: capture them again
+        if (m->gst && cudaStreamSynchronize(m->gst) != cudaSuccess) (void)cudaGetLastError();
+        for (auto& g : m->graphs)
+            if (g.exec) cudaGraphExecDestroy(g.exec);
+        m->graphs.clear();
+    }
+    m->pdrop = p;
+    m->dseed = seed;
+    m->dstep = 0;
+    m->fwd_targets = false;     // a backward needs a forward under these settings
+    return GPT2_OK;
+}
+
 GPT2_API int gpt2_destroy(gpt2* m) {
     if (!m) return GPT2_OK;
     int rc = GPT2_OK;
     if (cudaStreamSynchronize(m->st) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->owns_ws && cudaFree(m->ws) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->dec && cudaFree(m->dec) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
+    if (m->dbuf && cudaFree(m->dbuf) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     if (m->gst && cudaStreamSynchronize(m->gst) != cudaSuccess) { (void)cudaGetLastError(); rc = GPT2_ECUDA; }
     for (auto& g : m->graphs)
         if (g.exec) cudaGraphExecDestroy(g.exec);

@@ -136,6 +136,28 @@ float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, int T);
  * ENOMEM, ECUDA. */
 int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logits);
 
+/* Dropout for the following gpt2_forward calls (training), not for gpt2_eval or
+ * gpt2_decode: with probability p in [0, 1) an element is zeroed and the kept
+ * ones are scaled by 1/(1 - p), at the four places the pages put it: the
+ * token + position embedding output, the attention weights after the softmax,
+ * and each block's attention and MLP c_proj outputs before their residual
+ * additions ("GPT-2 from scratch with torch", sections 总体架构,
+ * 近看 Transformer block：自注意力 and 近看 Transformer block：前馈网络（MLP）;
+ * "从头搭建GPT(Andrej Karpathy) 笔记", section 继续增加改进的点).
+ * Draws: Philox4x32-10 under the 64-bit seed as key; the n-th gpt2_forward
+ * after this call (n = 0, 1, ...) draws element e (row-major) of site s
+ * (0 the embedding output [B,T,C]; for layer l: 1 + 3l the attention weights
+ * [B,H,T,T], 2 + 3l the attention c_proj output, 3 + 3l the MLP c_proj output)
+ * as word e mod 4 of Philox4x32-10(counter (lo32(e/4), hi32(e/4), s, n),
+ * key (lo32(seed), hi32(seed))) and keeps it when that word is at least
+ * floor(p * 2^32).  gpt2_backward uses the masks of the last forward.
+ * p = 0 turns dropout off (the step is then exactly the one without dropout).
+ * The first call with p > 0 allocates the mask memory (about
+ * L * maxB * H * maxT * ceil(maxT/32) * 4 bytes); changing p makes the next
+ * calls capture their graphs again.  A pending backward is dropped.  Errors:
+ * EINVAL (p outside [0, 1)), ENOMEM. */
+int gpt2_set_dropout(gpt2* m, float p, unsigned long long seed);
+
 /* Graphs: gpt2_forward, gpt2_eval and gpt2_backward record their kernels into a
  * CUDA graph on the second call with the same kind of call and (B, T), and
  * replay it from the third on, on a library stream ordered after earlier work
@@ -207,7 +229,8 @@ const float* gpt2_activation(gpt2* m, int which, int layer);
 #define GPT2_TRACE_ADAMW           10
 #define GPT2_TRACE_OTHER           11   /* input copies and memsets               */
 #define GPT2_TRACE_BIAS_GRAD       12   /* column sums for the bias gradients     */
-#define GPT2_TRACE_CLASSES         13
+#define GPT2_TRACE_DROPOUT         13   /* dropout masks and their application   */
+#define GPT2_TRACE_CLASSES         14
 
 /* Turn tracing on (1) or off (0); turning it on discards earlier records. */
 int gpt2_trace_enable(gpt2* m, int on);

@@ -25,6 +25,7 @@
 #define GPT2_B300_OPS_H
 
 #include <stddef.h>
+#include <stdint.h>
 #include "gpt2.h"
 
 #ifdef __cplusplus
@@ -174,7 +175,7 @@ int gpt2_op_bias_grad_noalloc(float* db, const float* dout, int N, int OC, int l
  * per (b,h), O = softmax(mask(Q K^T / sqrt(hs))) V, heads side by side in
  * y [B,T,C]; lse [B,H,T] (fp32) receives the row log-sum-exp of the scaled
  * scores.  ("GPT-2 from scratch with torch", section 自注意力.)  hs <= 64,
- * hs % 4 == 0.  qkv and y are fp32, or bf16 in GPT2_MODE_BF16 (hs 16, 32, 64). */
+ * hs % 4 == 0.  qkv and y are fp32, or bf16 in GPT2_MODE_BF16. */
 int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
                               int H, int mode, int* status, void* stream);
 
@@ -185,6 +186,58 @@ size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
 int gpt2_op_attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y,
                                const float* lse, int B, int T, int C, int H, void* scratch,
                                size_t scratch_bytes, int mode, int* status, void* stream);
+
+/* ---- dropout ---------------------------------------------------------------
+ * Inverted dropout ("GPT-2 from scratch with torch", sections 总体架构,
+ * 近看 Transformer block：自注意力, 近看 Transformer block：前馈网络（MLP）;
+ * "从头搭建GPT(Andrej Karpathy) 笔记", section 继续增加改进的点): an element
+ * is kept with probability 1 - p (0 <= p < 1) and scaled by 1/(1 - p).
+ * Keep masks are bit-packed by rows: a row of `cols` elements takes
+ * ceil(cols/32) uint32 words, bit b of word k is column 32k + b, bits past the
+ * row's end are 0.  Element e = row * cols + col is kept when word e mod 4 of
+ * Philox4x32-10(counter (lo32(e/4), hi32(e/4), site, step),
+ * key (lo32(seed), hi32(seed))) is at least floor(p * 2^32) (Philox4x32-10:
+ * Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC 2011).  gpt2_set_dropout in gpt2.h gives the sites and steps the
+ * training step uses. */
+
+/* Words of a mask of `rows` rows of `cols` elements (0 for invalid sizes). */
+size_t gpt2_op_dropout_mask_words(long long rows, int cols);
+
+/* Draw the keep bits of rows x cols elements into bits (device, that many
+ * words).  causal_T > 0 marks the attention weights: cols == causal_T, rows =
+ * B*H*T are (b, h, i) with i = row % T, and words whose first column is past
+ * the diagonal (32k > i) are written as 0 without drawing.  Asynchronous.
+ * Errors: EINVAL (bad sizes, p outside [0, 1)). */
+int gpt2_op_dropout_mask(uint32_t* bits, long long rows, int cols, int causal_T, unsigned long long seed,
+                         unsigned int site, unsigned int step, float p, void* stream);
+
+/* out[N, C] = res + keep o out / (1 - p)  (res NULL: out = keep o out / (1 - p)),
+ * in place; fp32, 16-byte aligned, C % 4 == 0; bits from gpt2_op_dropout_mask
+ * with rows N, cols C.  The forward of a dropped c_proj output added to the
+ * residual stream, and of the dropped embedding output.  Errors: EINVAL. */
+int gpt2_op_dropout_residual(float* out, const float* res, const uint32_t* bits, int N, int C, float p,
+                             void* stream);
+
+/* dst[N, C] = keep o src / (1 - p): the backward of the dropout above.  src
+ * fp32 (16-byte aligned); dst fp32 (may be src) or, with dst_bf16 != 0, bf16
+ * (8-byte aligned); C % 4 == 0.  Errors: EINVAL. */
+int gpt2_op_dropout_backward(void* dst, int dst_bf16, const float* src, const uint32_t* bits, int N, int C,
+                             float p, void* stream);
+
+/* Attention forward and backward with dropout on the attention weights: as
+ * gpt2_op_attention_forward / _backward, with A = P o K / (1 - p) in place of
+ * the softmax weights P (K the keep bits of gpt2_op_dropout_mask with rows
+ * B*H*T, cols = causal_T = T):  O = A V;  the backward gives dV = A^T dO,
+ * dP = (dO V^T) o K / (1 - p), dS = P o (dP - rowsum(dO o O)).  lse stays the
+ * log-sum-exp of the undropped scores.  bits must not be NULL.  Errors as the
+ * calls without dropout, and EINVAL for p outside [0, 1). */
+int gpt2_op_attention_forward_dropout(void* y, float* lse, const void* qkv, int B, int T, int C, int H,
+                                      int mode, const uint32_t* bits, float p, int* status, void* stream);
+int gpt2_op_attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, const void* y,
+                                       const float* lse, int B, int T, int C, int H, void* scratch,
+                                       size_t scratch_bytes, int mode, const uint32_t* bits, float p,
+                                       int* status, void* stream);
 
 /* Fused softmax cross-entropy over logits z [N, ld] (16B, ld % 4 == 0, ld >= V):
  * losses[n] = logsumexp(z[n,:V]) - z[n,tgt[n]]; then the gradient
