@@ -96,6 +96,8 @@ SIGNATURES = {
     "gpt2_op_dropout_mask": (_i, [_vp, C.c_longlong, _i, _i, C.c_ulonglong, C.c_uint, C.c_uint, _f, _vp]),
     "gpt2_op_dropout_residual": (_i, [_vp, _vp, _vp, _i, _i, _f, _vp]),
     "gpt2_op_dropout_backward": (_i, [_vp, _i, _vp, _vp, _i, _i, _f, _vp]),
+    "gpt2_op_layernorm_backward_dropout": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                                _vp, _f, _vp, _sz, _vp, _vp]),
     "gpt2_op_crossentropy": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_crossentropy_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2_op_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp]),

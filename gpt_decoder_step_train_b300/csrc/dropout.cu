@@ -54,6 +54,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // One thread per mask word.  The key and the step come from `state`
 // ({key0, key1, step}, device memory) when it is given, so that a captured
 // graph draws new masks each call; else from the arguments.
+//
+// ALIGNED (cols % 4 == 0): a word's first element is a multiple of 4, so its
+// 32 elements are exactly the 4 words of 8 consecutive draws (fewer at a row
+// end); the 8 draws are independent and unrolled.  Otherwise a word's elements
+// may start and end inside a draw, and each element finds its own word.
+template <bool ALIGNED>
 __global__ void __launch_bounds__(256)
 dropout_mask_kernel(uint32_t* __restrict__ bits, long long rows, int cols, int W, int causal_T,
                     const uint32_t* __restrict__ state, uint32_t key0, uint32_t key1, uint32_t step,
@@ -66,21 +72,48 @@ dropout_mask_kernel(uint32_t* __restrict__ bits, long long rows, int cols, int W
     const long long total = rows * W;
     for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < total;
          w += (long long)gridDim.x * blockDim.x) {
-        const long long row = w / W;
-        const int k = (int)(w - row * W);
+        long long row;
+        int k, i_diag = 0;
+        if (total <= 0x7fffffffLL) {            // 32-bit division (the usual case)
+            const uint32_t wu = (uint32_t)w, ru = wu / (uint32_t)W;
+            row = ru;
+            k = (int)(wu - ru * (uint32_t)W);
+            if (causal_T) i_diag = (int)(ru % (uint32_t)causal_T);
+        } else {
+            row = w / W;
+            k = (int)(w - row * W);
+            if (causal_T) i_diag = (int)(row % causal_T);
+        }
         const int c0 = 32 * k;
         uint32_t out = 0;
-        if (causal_T == 0 || c0 <= (int)(row % causal_T)) {
+        if (causal_T == 0 || c0 <= i_diag) {
             const int nb = min(32, cols - c0);
             const unsigned long long e0 = (unsigned long long)row * (unsigned long long)cols + (unsigned long long)c0;
-            const unsigned long long q1 = (e0 + (unsigned long long)nb - 1) >> 2;
-            for (unsigned long long q = e0 >> 2; q <= q1; q++) {
-                const uint4 r = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), site, step), key0, key1);
-                const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+            if constexpr (ALIGNED) {
+                const unsigned long long q0 = e0 >> 2;
+                const int nq = nb >> 2;
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const long long b = (long long)(4 * q + (unsigned long long)i) - (long long)e0;
-                    if (b >= 0 && b < nb && wv[i] >= thr) out |= 1u << b;
+                for (int j = 0; j < 8; j++) {
+                    if (j < nq) {
+                        const unsigned long long q = q0 + (unsigned long long)j;
+                        const uint4 r =
+                            philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), site, step), key0, key1);
+                        out |= ((uint32_t)(r.x >= thr) | ((uint32_t)(r.y >= thr) << 1) |
+                                ((uint32_t)(r.z >= thr) << 2) | ((uint32_t)(r.w >= thr) << 3))
+                               << (4 * j);
+                    }
+                }
+            } else {
+                const unsigned long long q1 = (e0 + (unsigned long long)nb - 1) >> 2;
+                for (unsigned long long q = e0 >> 2; q <= q1; q++) {
+                    const uint4 r =
+                        philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), site, step), key0, key1);
+                    const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const long long b = (long long)(4 * q + (unsigned long long)i) - (long long)e0;
+                        if (b >= 0 && b < nb && wv[i] >= thr) out |= 1u << b;
+                    }
                 }
             }
         }
@@ -94,8 +127,16 @@ __global__ void __launch_bounds__(256)
 dropout_residual_kernel(float4* __restrict__ out, const float4* __restrict__ res, const uint32_t* __restrict__ bits,
                         long long n4, int C4, int W, float ks) {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-        const long long row = i / C4;
-        const int c = 4 * (int)(i - row * C4);
+        long long row;
+        int c;
+        if (n4 <= 0x7fffffffLL) {               // 32-bit division (the usual case)
+            const uint32_t iu = (uint32_t)i, ru = iu / (uint32_t)C4;
+            row = ru;
+            c = 4 * (int)(iu - ru * (uint32_t)C4);
+        } else {
+            row = i / C4;
+            c = 4 * (int)(i - row * C4);
+        }
         const uint32_t m = __ldg(bits + row * W + (c >> 5)) >> (c & 31);
         float4 v = out[i];
         const float4 r = res ? res[i] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -113,8 +154,16 @@ __global__ void __launch_bounds__(256)
 dropout_backward_kernel(void* dst, const float4* src, const uint32_t* __restrict__ bits,
                         long long n4, int C4, int W, float ks) {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-        const long long row = i / C4;
-        const int c = 4 * (int)(i - row * C4);
+        long long row;
+        int c;
+        if (n4 <= 0x7fffffffLL) {               // 32-bit division (the usual case)
+            const uint32_t iu = (uint32_t)i, ru = iu / (uint32_t)C4;
+            row = ru;
+            c = 4 * (int)(iu - ru * (uint32_t)C4);
+        } else {
+            row = i / C4;
+            c = 4 * (int)(i - row * C4);
+        }
         const uint32_t m = __ldg(bits + row * W + (c >> 5)) >> (c & 31);
         const float4 g = src[i];
         const float4 v = make_float4((m & 1u) ? g.x * ks : 0.f, (m & 2u) ? g.y * ks : 0.f, (m & 4u) ? g.z * ks : 0.f,
@@ -149,9 +198,13 @@ int dropout_mask(uint32_t* bits, long long rows, int cols, int causal_T, const u
     const long long total = rows * W;
     const long long want = (total + 255) / 256;
     const unsigned blocks = (unsigned)(want < 148LL * 32 ? want : 148LL * 32);
-    count_launch(), dropout_mask_kernel<<<blocks, 256, 0, st>>>(bits, rows, cols, W, causal_T, state,
-                                                                 (uint32_t)seed, (uint32_t)(seed >> 32), step, site,
-                                                                 dropout_threshold(p));
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32), thr = dropout_threshold(p);
+    if (cols % 4 == 0)
+        count_launch(), dropout_mask_kernel<true><<<blocks, 256, 0, st>>>(bits, rows, cols, W, causal_T, state, k0,
+                                                                          k1, step, site, thr);
+    else
+        count_launch(), dropout_mask_kernel<false><<<blocks, 256, 0, st>>>(bits, rows, cols, W, causal_T, state, k0,
+                                                                           k1, step, site, thr);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -30,4 +30,14 @@ int attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, cons
                                int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
                                cudaStream_t st, float* colsum, bool* colsum_done, const uint32_t* bits, float p);
 
+// LayerNorm backward (layernorm.cu) with the operand copy dxo of dx in bf16 or
+// fp32; with bits != null that copy is keep o dx / (1 - p) and dx_colsum its
+// column sum (the bias gradient of the dropped branch it feeds).  The fused
+// form needs layernorm_backward_fuses_dropout(C).
+bool layernorm_backward_fuses_dropout(int C);
+int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db, float* dx_colsum, const float* dy,
+                       const float* x, const float* w, const float* mean, const float* rstd, int N, int C,
+                       int accumulate, void* scratch, size_t scratch_bytes, int* status, cudaStream_t st,
+                       const uint32_t* bits, float p);
+
 }  // namespace gpt2k

@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "dropout.cuh"
 #include "ptx.cuh"
 
 namespace gpt2k {
@@ -249,12 +250,18 @@ ln_bwd_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* _
 // partial[blk][3][C], the same partial layout the tiled kernel above writes.
 constexpr int LNR_WARPS = 12;
 
-template <int V4>
+//
+// DROP: the residual-stream gradient dx also feeds a dropped branch (a c_proj
+// output that went through dropout before the residual addition).  The copy
+// dxo then holds keep o dx / (1 - p) (bf16 or fp32), and the third column sum
+// is that of the copy: the branch's bias gradient.  bits: keep bits of the
+// branch, rows of ceil(C/32) words.
+template <int V4, bool DROP>
 __global__ void __launch_bounds__(LNR_WARPS * 32, 1)
-ln_bwd_rows_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* __restrict__ partial,
+ln_bwd_rows_kernel(float* __restrict__ dx, void* __restrict__ dxo, int dxo_bf16, float* __restrict__ partial,
                    const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ w,
                    const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C, int rpb,
-                   int accumulate) {
+                   int accumulate, const uint32_t* __restrict__ bits, float ks) {
     extern __shared__ __align__(16) float red[];       // [LNR_WARPS][3][C]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C4 = C >> 2;
@@ -304,15 +311,27 @@ ln_bwd_rows_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, flo
                 o.z += rs * (gv[k].z * ww.z - mg - xv[k].z * mgx);
                 o.w += rs * (gv[k].w * ww.w - mg - xv[k].w * mgx);
                 dr[c] = o;
-                if (dx16) {
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-                    reinterpret_cast<uint2*>(dx16 + (size_t)row * C)[c] =
-                        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                float4 om = o;
+                if constexpr (DROP) {
+                    const uint32_t mb = __ldg(bits + (size_t)row * ((C + 31) >> 5) + ((4 * c) >> 5)) >> ((4 * c) & 31);
+                    om.x = (mb & 1u) ? o.x * ks : 0.f;
+                    om.y = (mb & 2u) ? o.y * ks : 0.f;
+                    om.z = (mb & 4u) ? o.z * ks : 0.f;
+                    om.w = (mb & 8u) ? o.w * ks : 0.f;
+                }
+                if (dxo) {
+                    if (!DROP || dxo_bf16) {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(om.x, om.y), hi = __floats2bfloat162_rn(om.z, om.w);
+                        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dxo) + (size_t)row * C)[c] =
+                            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                    } else {
+                        reinterpret_cast<float4*>(static_cast<float*>(dxo) + (size_t)row * C)[c] = om;
+                    }
                 }
                 aw[k].x += gv[k].x * xv[k].x; aw[k].y += gv[k].y * xv[k].y;
                 aw[k].z += gv[k].z * xv[k].z; aw[k].w += gv[k].w * xv[k].w;
                 ab[k].x += gv[k].x; ab[k].y += gv[k].y; ab[k].z += gv[k].z; ab[k].w += gv[k].w;
-                as[k].x += o.x; as[k].y += o.y; as[k].z += o.z; as[k].w += o.w;
+                as[k].x += om.x; as[k].y += om.y; as[k].z += om.z; as[k].w += om.w;
             }
         }
     }
@@ -401,22 +420,31 @@ GPT2_API size_t gpt2_op_layernorm_backward_scratch_bytes(int N, int C) {
     return (size_t)LNB_MAX_BLOCKS * 3 * C * sizeof(float);
 }
 
-GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, float* dx_colsum,
-                                        const float* dy, const float* x, const float* w,
-                                        const float* mean, const float* rstd, int N, int C, int accumulate,
-                                        void* scratch, size_t scratch_bytes, int* status, void* stream) {
+namespace gpt2k {
+
+bool layernorm_backward_fuses_dropout(int C) { return C >= 4 && C % 4 == 0 && ceil_div(C / 4, 32) <= 6; }
+
+// gpt2_op_layernorm_backward, with the operand copy dxo of dx in bf16 or fp32
+// (dxo_bf16) and, when bits != null, dropout applied to that copy and to its
+// column sum (rows of up to 768 columns: layernorm_backward_fuses_dropout).
+int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db, float* dx_colsum, const float* dy,
+                       const float* x, const float* w, const float* mean, const float* rstd, int N, int C,
+                       int accumulate, void* scratch, size_t scratch_bytes, int* status, cudaStream_t st,
+                       const uint32_t* bits, float p) {
     if (!dx || !dw || !db || !dy || !x || !w || !mean || !rstd || N < 1 || C < 4 || C % 4 ||
         C > LNB_THREADS * 8)
         return GPT2_EINVAL;
     if (!aligned16(dx) || !aligned16(dy) || !aligned16(x) || !aligned16(w) || !aligned16(scratch))
         return GPT2_EINVAL;
     if (!scratch || scratch_bytes < gpt2_op_layernorm_backward_scratch_bytes(N, C)) return GPT2_ENOMEM;
-    __nv_bfloat16* dx16 = static_cast<__nv_bfloat16*>(dx_bf16);
-    if (dx16 && (reinterpret_cast<uintptr_t>(dx16) & 7)) return GPT2_EINVAL;
+    if (dxo && (reinterpret_cast<uintptr_t>(dxo) & (dxo_bf16 ? 7u : 15u))) return GPT2_EINVAL;
+    if (!dxo_bf16 && !bits && dxo) return GPT2_EINVAL;     // without dropout the copy is bf16
+    if (bits && (!layernorm_backward_fuses_dropout(C) || !(p >= 0.f && p < 1.f))) return GPT2_ENOTSUP;
+    __nv_bfloat16* dx16 = static_cast<__nv_bfloat16*>(dxo);
+    const float ks = bits ? dropout_scale(p) : 1.f;
     const LnbPlan pl = lnb_plan(N, C);
     const size_t smem = (size_t)pl.stages * pl.stage_bytes;
     float* partial = reinterpret_cast<float*>(scratch);
-    cudaStream_t st = as_stream(stream);
     const int cpt = ceil_div(C, LNB_THREADS);
 #define LNB(CPT)                                                                                         \
     do {                                                                                                 \
@@ -437,21 +465,28 @@ GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, flo
         const int rpb = ceil_div(N, nblk);
         nblk = ceil_div(N, rpb);
         const size_t rsm = (size_t)LNR_WARPS * 3 * C * sizeof(float);
-#define LNR(V4)                                                                                      \
+#define LNR(V4, DROP)                                                                                \
     do {                                                                                             \
         static bool attr = false;                                                                    \
         if (!attr) {                                                                                 \
-            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_rows_kernel<V4>,                               \
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_rows_kernel<V4, DROP>,                         \
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,          \
                                                (int)((size_t)LNR_WARPS * 3 * 768 * sizeof(float)))); \
             attr = true;                                                                             \
         }                                                                                            \
-        count_launch(), ln_bwd_rows_kernel<V4><<<nblk, LNR_WARPS * 32, rsm, st>>>(                  \
-            dx, dx16, partial, dy, x, w, mean, rstd, N, C, rpb, accumulate ? 1 : 0);                 \
+        count_launch(), ln_bwd_rows_kernel<V4, DROP><<<nblk, LNR_WARPS * 32, rsm, st>>>(            \
+            dx, dxo, dxo_bf16 ? 1 : 0, partial, dy, x, w, mean, rstd, N, C, rpb, accumulate ? 1 : 0,  \
+            bits, ks);                                                                               \
     } while (0)
-        if (v4 <= 2) LNR(2);
-        else if (v4 <= 4) LNR(4);
-        else LNR(6);
+        if (bits) {
+            if (v4 <= 2) LNR(2, true);
+            else if (v4 <= 4) LNR(4, true);
+            else LNR(6, true);
+        } else {
+            if (v4 <= 2) LNR(2, false);
+            else if (v4 <= 4) LNR(4, false);
+            else LNR(6, false);
+        }
 #undef LNR
     } else if (cpt <= 1) LNB(1);
     else if (cpt <= 2) LNB(2);
@@ -463,4 +498,24 @@ GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, flo
                                                                                        nblk, C);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
+}
+
+}  // namespace gpt2k
+
+GPT2_API int gpt2_op_layernorm_backward(float* dx, void* dx_bf16, float* dw, float* db, float* dx_colsum,
+                                        const float* dy, const float* x, const float* w,
+                                        const float* mean, const float* rstd, int N, int C, int accumulate,
+                                        void* scratch, size_t scratch_bytes, int* status, void* stream) {
+    return layernorm_backward(dx, dx_bf16, true, dw, db, dx_colsum, dy, x, w, mean, rstd, N, C, accumulate, scratch,
+                              scratch_bytes, status, as_stream(stream), nullptr, 0.f);
+}
+
+GPT2_API int gpt2_op_layernorm_backward_dropout(float* dx, void* dx_drop, int dx_drop_bf16, float* dw, float* db,
+                                                float* drop_colsum, const float* dy, const float* x, const float* w,
+                                                const float* mean, const float* rstd, int N, int C, int accumulate,
+                                                const uint32_t* bits, float p, void* scratch, size_t scratch_bytes,
+                                                int* status, void* stream) {
+    if (!bits || !dx_drop) return GPT2_EINVAL;
+    return layernorm_backward(dx, dx_drop, dx_drop_bf16 != 0, dw, db, drop_colsum, dy, x, w, mean, rstd, N, C,
+                              accumulate, scratch, scratch_bytes, status, as_stream(stream), bits, p);
 }

@@ -361,13 +361,19 @@ static int backward_impl(gpt2* m) {
     const void* dres_op = b16 ? static_cast<const void*>(m->dres16) : static_cast<const void*>(m->dres);
     const void* dz_op = b16 ? static_cast<const void*>(m->dz16) : static_cast<const void*>(m->logits);
     const size_t wes = b16 ? 2 : 4;
-    // dropout: the gradient of a dropped c_proj output is keep o dres / (1 - p),
-    // written over the operand copy of dres (BF16 mode) or into dln, which is
-    // free at that point; the bias gradient is then its own column sum
+    // dropout: the gradient of a dropped c_proj output is keep o dres / (1 - p)
+    // and its bias gradient the column sum of that.  It goes over the operand
+    // copy of dres (BF16 mode), else into an operand buffer that is free at that
+    // point (datty before the MLP c_proj backward, dbig before the attention
+    // c_proj backward).  The LayerNorm backward that produces dres writes it
+    // with the column sum (rows up to 768 wide), else a separate pass does.
     const bool drop = m->drop_fwd;
+    const bool fuse = drop && layernorm_backward_fuses_dropout(C);
     const float pd = m->pdrop;
-    void* dbr = b16 ? static_cast<void*>(m->dres16) : static_cast<void*>(m->dln);
-    const void* dbr_op = drop ? static_cast<const void*>(dbr) : dres_op;
+    void* const dbr_mlp = b16 ? static_cast<void*>(m->dres16) : static_cast<void*>(m->datty);
+    void* const dbr_att = b16 ? static_cast<void*>(m->dres16) : static_cast<void*>(m->dbig);
+    const void* const op_mlp = drop ? static_cast<const void*>(dbr_mlp) : dres_op;
+    const void* const op_att = drop ? static_cast<const void*>(dbr_att) : dres_op;
     // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
     OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, dz_op, W(m, WTE), b16, nullptr, N, C, c.V,
                                                m->Vp, mode, status, st));
@@ -375,10 +381,10 @@ static int backward_impl(gpt2* m) {
                                                  mode, status, st));
     // ln_f: the residual gradient starts here (written, not accumulated); its
     // column sum is the last block's MLP c_proj bias gradient
-    OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LNFW), G(m, LNFB),
-                                                 drop ? nullptr : G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
-                                                 m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW),
-                                                 m->lnf_mean, m->lnf_rstd, N, C, 0, sc, sb, status, st));
+    OP(LAYERNORM_BWD, layernorm_backward(m->dres, fuse ? dbr_mlp : m->dres16, !fuse || b16, G(m, LNFW), G(m, LNFB),
+                                         drop && !fuse ? nullptr : G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
+                                         m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW), m->lnf_mean, m->lnf_rstd, N,
+                                         C, 0, sc, sb, status, st, fuse ? drop_bits(m, 3 * L) : nullptr, pd));
     for (int l = L - 1; l >= 0; l--) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
         const char* ln1 = Orow(m, m->ln1, l, C);
@@ -394,14 +400,14 @@ static int backward_impl(gpt2* m) {
         // MLP c_proj: dh = (dres . Wfp) * gelu'(h); dWfp = dres^T . g (its bias
         // gradient came with the LayerNorm backward that produced dres)
         // (with the c_fc bias gradient: the column sums of dh)
-        if (drop) {
-            OP(DROPOUT, dropout_backward(dbr, b16, m->dres, drop_bits(m, 3 + 3 * l), N, C, pd, st));
-            OP(BIAS_GRAD, bias_grad_any(G(m, FCPROJB) + l * C, dbr, b16, N, C, C, sc, sb, st));
+        if (drop && !fuse) {
+            OP(DROPOUT, dropout_backward(dbr_mlp, b16, m->dres, drop_bits(m, 3 + 3 * l), N, C, pd, st));
+            OP(BIAS_GRAD, bias_grad_any(G(m, FCPROJB) + l * C, dbr_mlp, b16, N, C, C, sc, sb, st));
         }
-        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, dbr_op, Wl(FCPROJW, 4 * cc), b16, fch, N,
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, op_mlp, Wl(FCPROJW, 4 * cc), b16, fch, N,
                                                    4 * C, C, C, mode, status, st, G(m, FCB) + l * 4 * C,
                                                    m->colsum, m->colsum_bytes));
-        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, dbr_op, fchg, b16, N,
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, op_mlp, fchg, b16, N,
                                                      4 * C, C, C, sc, sb, mode, status, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dbig, Wl(FCW, 4 * cc), b16, nullptr, N,
@@ -410,19 +416,19 @@ static int backward_impl(gpt2* m) {
                                                      4 * C, sc, sb, mode, status, st));
         // ln_2: dres += LN'(dln2); the column sum of the result is the attention
         // c_proj bias gradient
-        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN2W) + l * C, G(m, LN2B) + l * C,
-                                                     drop ? nullptr : G(m, ATTPROJB) + l * C, m->dln, res2,
-                                                     P(m, LN2W) + l * C,
-                                                     m->ln2_mean + l * R, m->ln2_rstd + l * R, N, C, 1, sc, sb,
-                                                     status, st));
+        OP(LAYERNORM_BWD, layernorm_backward(m->dres, fuse ? dbr_att : m->dres16, !fuse || b16, G(m, LN2W) + l * C,
+                                             G(m, LN2B) + l * C, drop && !fuse ? nullptr : G(m, ATTPROJB) + l * C,
+                                             m->dln, res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
+                                             m->ln2_rstd + l * R, N, C, 1, sc, sb, status, st,
+                                             fuse ? drop_bits(m, 2 + 3 * l) : nullptr, pd));
         // attention c_proj (bias gradient: with ln_2's backward above)
-        if (drop) {
-            OP(DROPOUT, dropout_backward(dbr, b16, m->dres, drop_bits(m, 2 + 3 * l), N, C, pd, st));
-            OP(BIAS_GRAD, bias_grad_any(G(m, ATTPROJB) + l * C, dbr, b16, N, C, C, sc, sb, st));
+        if (drop && !fuse) {
+            OP(DROPOUT, dropout_backward(dbr_att, b16, m->dres, drop_bits(m, 2 + 3 * l), N, C, pd, st));
+            OP(BIAS_GRAD, bias_grad_any(G(m, ATTPROJB) + l * C, dbr_att, b16, N, C, C, sc, sb, st));
         }
-        OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, dbr_op, Wl(ATTPROJW, cc), b16, nullptr, N,
+        OP(MATMUL_BWD_INPUT, linear_backward_input(m->datty, b16, op_att, Wl(ATTPROJW, cc), b16, nullptr, N,
                                                    C, C, C, mode, status, st));
-        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, dbr_op, atty, b16, N, C, C, C,
+        OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, ATTPROJW) + l * cc, op_att, atty, b16, N, C, C, C,
                                                      sc, sb, mode, status, st));
         // attention; the tcgen05 path also leaves the column sums of dqkv per
         // 32 rows, which give the qkv bias gradient at once
@@ -441,10 +447,14 @@ static int backward_impl(gpt2* m) {
             OP(BIAS_GRAD, bias_grad_any(G(m, QKVB) + l * 3 * C, m->dqkv, b16, N, 3 * C, 3 * C, sc, sb, st));
         // ln_1: dres += LN'(dln1); the column sum of the result is the previous
         // block's MLP c_proj bias gradient
-        OP(LAYERNORM_BWD, gpt2_op_layernorm_backward(m->dres, m->dres16, G(m, LN1W) + l * C, G(m, LN1B) + l * C,
-                                                     l > 0 && !drop ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
-                                                     m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R,
-                                                     m->ln1_rstd + l * R, N, C, 1, sc, sb, status, st));
+        // (with dropout: the previous block's dropped MLP c_proj branch; the
+        // first block's ln_1 feeds the dropped embedding output instead)
+        const bool fuse1 = fuse && l > 0;
+        OP(LAYERNORM_BWD, layernorm_backward(m->dres, fuse1 ? dbr_mlp : m->dres16, !fuse1 || b16, G(m, LN1W) + l * C,
+                                             G(m, LN1B) + l * C,
+                                             l > 0 && (!drop || fuse) ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
+                                             m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R, m->ln1_rstd + l * R,
+                                             N, C, 1, sc, sb, status, st, fuse1 ? drop_bits(m, 3 * l) : nullptr, pd));
     }
     if (drop) OP(DROPOUT, dropout_backward(m->dres, false, m->dres, drop_bits(m, 0), N, C, pd, st));
     OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V,

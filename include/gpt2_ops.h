@@ -225,6 +225,19 @@ int gpt2_op_dropout_residual(float* out, const float* res, const uint32_t* bits,
 int gpt2_op_dropout_backward(void* dst, int dst_bf16, const float* src, const uint32_t* bits, int N, int C,
                              float p, void* stream);
 
+/* LayerNorm backward whose residual gradient also feeds a dropped branch (a
+ * c_proj output that went through dropout before the residual addition): as
+ * gpt2_op_layernorm_backward, and dx_drop [N,C] receives keep o dx / (1 - p)
+ * (bf16 with dx_drop_bf16 != 0, 8-byte aligned; else fp32, 16-byte aligned),
+ * drop_colsum [C] (or NULL) the column sums of dx_drop in fixed order: that
+ * branch's bias gradient.  bits: keep bits with rows N, cols C.  C <= 768.
+ * Errors: EINVAL, ENOMEM, ENOTSUP (C > 768). */
+int gpt2_op_layernorm_backward_dropout(float* dx, void* dx_drop, int dx_drop_bf16, float* dw, float* db,
+                                       float* drop_colsum, const float* dy, const float* x, const float* w,
+                                       const float* mean, const float* rstd, int N, int C, int accumulate,
+                                       const uint32_t* bits, float p, void* scratch, size_t scratch_bytes,
+                                       int* status, void* stream);
+
 /* Attention forward and backward with dropout on the attention weights: as
  * gpt2_op_attention_forward / _backward, with A = P o K / (1 - p) in place of
  * the softmax weights P (K the keep bits of gpt2_op_dropout_mask with rows

@@ -125,6 +125,51 @@ def test_dropout_residual_and_backward_match_oracle(B_, o64):
     assert L.gpt2_op_dropout_mask(B_.ptr(bits), 10, 5, 0, 1, 1, 0, -0.1, None) == B_.GPT2_EINVAL
 
 
+@pytest.mark.parametrize("N,C", [(300, 768), (37, 100)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_layernorm_backward_feeding_a_dropped_branch(B_, o64, N, C, bf16):
+    """The LayerNorm backward that also writes the dropped branch's gradient
+    keep o dx / (1 - p) and its column sum, against the oracle's LayerNorm
+    backward followed by its dropout."""
+    L = B_.lib()
+    p, seed = 0.25, 42
+    rng = np.random.default_rng(8)
+    x = rng.normal(size=(N, C)).astype(np.float32)
+    w = rng.normal(size=C).astype(np.float32)
+    b = rng.normal(size=C).astype(np.float32)
+    dy = rng.normal(size=(N, C)).astype(np.float32)
+    dx0 = rng.normal(size=(N, C)).astype(np.float32)
+    _, wm, wr = o64.layernorm_forward(x, w, b)
+    bits = gpu_mask(B_, N, C, 0, seed, 6, 1, p)
+    keep = o64.dropout_keep(N * C, seed, 6, 1, p).reshape(N, C)
+    dx = dev(dx0.copy())
+    dxd = torch.empty(N, C, dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
+    dw, db, ds = (torch.empty(C, device="cuda") for _ in range(3))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nb = L.gpt2_op_layernorm_backward_scratch_bytes(N, C)
+    sc = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    assert L.gpt2_op_layernorm_backward_dropout(
+        B_.ptr(dx), B_.ptr(dxd), int(bf16), B_.ptr(dw), B_.ptr(db), B_.ptr(ds), B_.ptr(dev(dy)), B_.ptr(dev(x)),
+        B_.ptr(dev(w)), B_.ptr(dev(wm.astype(np.float32))), B_.ptr(dev(wr.astype(np.float32))), N, C, 1,
+        B_.ptr(bits), p, B_.ptr(sc), nb, B_.ptr(st), None) == 0
+    wdx, wdw, wdb = o64.layernorm_backward(dy, x, w, wm.astype(np.float32), wr.astype(np.float32))
+    want = dx0 + wdx
+    want_d = o64.dropout_apply(want, keep, p)
+    assert rel_l2(host(dx), want) < 1e-6
+    assert rel_l2(host(dw), wdw) < 1e-6 and rel_l2(host(db), wdb) < 1e-6
+    assert rel_l2(host(dxd), want_d) < (4e-3 if bf16 else 1e-6)
+    assert np.array_equal(host(dxd) == 0, keep == 0)
+    assert rel_l2(host(ds), want_d.sum(axis=0)) < 1e-5
+    assert int(st.item()) == 0
+    if C > 768 or bf16:
+        return
+    big = 1024
+    assert L.gpt2_op_layernorm_backward_dropout(
+        B_.ptr(dx), B_.ptr(dxd), 0, B_.ptr(dw), B_.ptr(db), B_.ptr(ds), B_.ptr(dev(dy)), B_.ptr(dev(x)),
+        B_.ptr(dev(w)), B_.ptr(dev(wm.astype(np.float32))), B_.ptr(dev(wr.astype(np.float32))), 1, big, 1,
+        B_.ptr(bits), p, B_.ptr(sc), nb, B_.ptr(st), None) in (B_.GPT2_ENOTSUP, B_.GPT2_ENOMEM)
+
+
 # mode, B, T, C, H: the CUDA-core kernels (fp32; tf32, which takes them under
 # dropout; bf16 with head sizes other than 64) and the tcgen05 kernels (bf16, hs 64)
 ATT_CASES = [
