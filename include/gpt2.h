@@ -154,8 +154,11 @@ int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logits);
  * p = 0 turns dropout off (the step is then exactly the one without dropout).
  * The first call with p > 0 allocates the mask memory (about
  * L * maxB * H * maxT * ceil(maxT/32) * 4 bytes); changing p makes the next
- * calls capture their graphs again.  A pending backward is dropped.  Errors:
- * EINVAL (p outside [0, 1)), ENOMEM. */
+ * calls capture their graphs again (the library's own graphs read the draw
+ * state from device memory, so every replay draws new masks).  With p > 0,
+ * gpt2_forward first copies that state from host memory, so a stream capture
+ * of the caller's own that records gpt2_forward fails (ECUDA).  A pending
+ * backward is dropped.  Errors: EINVAL (p outside [0, 1)), ENOMEM. */
 int gpt2_set_dropout(gpt2* m, float p, unsigned long long seed);
 
 /* Graphs: gpt2_forward, gpt2_eval and gpt2_backward record their kernels into a

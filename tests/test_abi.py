@@ -87,3 +87,30 @@ def test_scratch_queries_are_host_only(L):
     assert L.gpt2_op_encoder_backward_scratch_bytes(16384, 50257, 768) > 0
     assert L.gpt2_op_attention_backward_scratch_bytes(16, 1024, 12) >= 16 * 12 * 1024 * 4
     assert L.gpt2_op_linear_backward_weight_scratch_bytes(16384, 768, 3072, 1) > 0
+
+
+def test_dropout_host_logic(L):
+    """Mask sizes and argument checks of the dropout calls, which return before
+    any device work (no GPU needed)."""
+    from gpt_decoder_step_train_b300 import binding as B_
+    words = L.gpt2_op_dropout_mask_words
+    assert words(37, 100) == 37 * 4            # ceil(100 / 32) words per row
+    assert words(16 * 12 * 1024, 1024) == 16 * 12 * 1024 * 32
+    assert words(5, 32) == 5 and words(5, 33) == 10 and words(0, 7) == 0
+    assert words(-1, 7) == 0 and words(3, 0) == 0
+    fake = ctypes.c_void_p(16)                 # never dereferenced: every call below is rejected
+    mask = L.gpt2_op_dropout_mask
+    assert mask(None, 4, 8, 0, 1, 0, 0, 0.1, None) == B_.GPT2_EINVAL
+    assert mask(fake, 4, 8, 0, 1, 0, 0, 1.0, None) == B_.GPT2_EINVAL          # p must be below 1
+    assert mask(fake, 4, 8, 0, 1, 0, 0, -0.01, None) == B_.GPT2_EINVAL
+    assert mask(fake, 10, 7, 7, 1, 0, 0, 0.1, None) == B_.GPT2_EINVAL         # rows not a multiple of T
+    assert mask(fake, 14, 8, 7, 1, 0, 0, 0.1, None) == B_.GPT2_EINVAL         # cols != T
+    res = L.gpt2_op_dropout_residual
+    assert res(fake, None, fake, 4, 6, 0.1, None) == B_.GPT2_EINVAL          # C % 4
+    assert res(ctypes.c_void_p(20), None, fake, 4, 8, 0.1, None) == B_.GPT2_EINVAL   # alignment
+    bwd = L.gpt2_op_dropout_backward
+    assert bwd(fake, 0, fake, fake, 4, 8, 1.5, None) == B_.GPT2_EINVAL
+    assert bwd(ctypes.c_void_p(24), 0, fake, fake, 4, 8, 0.1, None) == B_.GPT2_EINVAL  # fp32 dst 16 B
+    assert L.gpt2_set_dropout(None, 0.1, 0) == B_.GPT2_EINVAL
+    assert L.gpt2_op_attention_forward_dropout(fake, fake, fake, 1, 8, 64, 1, B_.GPT2_MODE_BF16, None, 0.1,
+                                               None, None) == B_.GPT2_EINVAL  # bits required
