@@ -64,6 +64,37 @@ def dist_info():
     return world, rank, local
 
 
+# ------------------------------------------------------------------ ranks
+# One process per GPU, each running an independent replica of the step (the path
+# has no data exchange on one GPU per rank).  These helpers take the device of the
+# process group's backend: a CUDA device under NCCL, the CPU under gloo.
+def barrier(world, cuda=True):
+    """All ranks meet here; with cuda, the device is idle on both sides."""
+    import torch
+    if cuda:
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if cuda:
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(x, world, device):
+    """The largest x over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, B, T, steps, ms_total):
+    """Whole-job throughput: the tokens of every rank's timed steps over the
+    slowest rank's time (weak scaling: B x T per rank)."""
+    return world * B * T * steps / (ms_total / 1000.0)
+
+
 def load_peaks():
     try:
         with open(MEASURED_PEAKS) as f:
@@ -244,19 +275,6 @@ def run_ours(args, cfg):
             raise RuntimeError(f"adamw failed: {binding.strerror(rc)}")
         return loss
 
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     for i in range(args.warmup):
         loss = step(*dev_pool[i % len(dev_pool)])
     st = model.status()
@@ -272,7 +290,7 @@ def run_ours(args, cfg):
         except ValueError:
             pass
     clocks = ClockSampler(gpu_index)
-    barrier()
+    barrier(world)
     clocks.start()
     n_launch0 = binding.lib().gpt2_kernel_launches()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -282,20 +300,20 @@ def run_ours(args, cfg):
     for i in range(args.steps):
         losses.append(step(*dev_pool[i % len(dev_pool)]))
     e1.record(stream)
-    barrier()
+    barrier(world)
     clock_info = clocks.stop()
     launches = binding.lib().gpt2_kernel_launches() - n_launch0
-    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     # per-kernel times: a second pass of the same steps with CUDA events around
     # every operation on the model's stream (kept out of the timed region above,
     # whose value the event records would slow by a few percent)
     kernels = {}
     if not args.no_trace:
         model.trace(True)
-        barrier()
+        barrier(world)
         for i in range(args.steps):
             step(*dev_pool[i % len(dev_pool)])
-        barrier()
+        barrier(world)
         kernels = model.trace_read()
         model.trace(False)
     st = model.status()
@@ -305,19 +323,18 @@ def run_ours(args, cfg):
         raise RuntimeError(f"non-finite loss: {losses}")
 
     ms_per_step = ms_total / args.steps
-    tokens_total = world * B * T * args.steps
-    value = tokens_total / (ms_total / 1000.0)
+    value = job_tokens_per_s(world, B, T, args.steps, ms_total)
 
     # ---- end to end: pinned host inputs copied every step, loss read back ---
     e2e = None
     if not args.no_e2e:
         ke = max(3, min(args.steps, 10))
-        barrier()
+        barrier(world)
         t0 = time.perf_counter()
         for i in range(ke):
             step(*host_pool[i % len(host_pool)])
-        barrier()
-        wall = max_over_ranks(time.perf_counter() - t0)
+        barrier(world)
+        wall = max_over_ranks(time.perf_counter() - t0, world, dev)
         e2e = {"value": world * B * T * ke / wall, "unit": UNIT,
                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 4, "steps": ke}
 
