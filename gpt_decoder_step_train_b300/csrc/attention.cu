@@ -393,8 +393,10 @@ static bool attn_args_ok(int B, int T, int C, int H) {
 
 // Dispatch: BF16 mode takes the tcgen05 kernels for head size 64, the
 // mma.sync kernels for head sizes 16 and 32 (no dropout), else the CUDA-core
-// kernels on bf16; FP32 and TF32 modes take the mma.sync TF32 kernels where
-// they apply (no dropout), else the CUDA-core kernels on fp32.
+// kernels on bf16 (head sizes that are multiples of 8: the backward's
+// rowsum(dO o O) reads a head's slice 16 bytes at a time); FP32 and TF32 modes
+// take the mma.sync TF32 kernels where they apply (no dropout), else the
+// CUDA-core kernels on fp32.
 int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int mode, int* status,
                       cudaStream_t st, const uint32_t* bits, float p) {
     if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
@@ -405,6 +407,7 @@ int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
         if (attention_tc05_supported(hs, C))
             return attention_tc05_forward(y, lse, qkv, B, T, C, H, status, st, bits, ks);
         if (!bits && attention_tc_supported(hs)) return attention_bf16_forward(y, lse, qkv, B, T, C, H, st);
+        if (hs % 8) return GPT2_ENOTSUP;
         simt_forward<__nv_bfloat16>(y, lse, qkv, B, T, C, H, hs, bits, ks, st);
         GPT2_LAUNCH_CHECK();
         return GPT2_OK;
@@ -430,6 +433,7 @@ int attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, cons
     // D = rowsum(dO o O) with O the output that met dO (after dropout)
     float* D = reinterpret_cast<float*>(scratch);
     if (mode == GPT2_MODE_BF16) {
+        if (hs % 8) return GPT2_ENOTSUP;
         launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
         GPT2_LAUNCH_CHECK();
         if (attention_tc05_supported(hs, C)) {

@@ -175,7 +175,8 @@ int gpt2_op_bias_grad_noalloc(float* db, const float* dout, int N, int OC, int l
  * per (b,h), O = softmax(mask(Q K^T / sqrt(hs))) V, heads side by side in
  * y [B,T,C]; lse [B,H,T] (fp32) receives the row log-sum-exp of the scaled
  * scores.  ("GPT-2 from scratch with torch", section 自注意力.)  hs <= 64,
- * hs % 4 == 0.  qkv and y are fp32, or bf16 in GPT2_MODE_BF16. */
+ * hs % 4 == 0.  qkv and y are fp32, or bf16 in GPT2_MODE_BF16 (there hs % 8 == 0,
+ * else ENOTSUP). */
 int gpt2_op_attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
                               int H, int mode, int* status, void* stream);
 
