@@ -35,6 +35,37 @@ def test_param_count_matches_run_log(o64):
     assert n + cfg.V * cfg.C != g["num_parameters"]
 
 
+def test_activation_count_of_run_log_fixes_the_small_batch_shape():
+    """The run log prints num_activations = 73,323,776: the floats of the C
+    trainer's per-layer activation tensors (LayerNorm outputs and statistics,
+    qkv, attention scores and probabilities, one T x T matrix each per head,
+    attention output and projection, residuals, the MLP's pre-activation and
+    GELU output, its projection), the final LayerNorm, logits, probabilities and
+    losses.  With the model's widths (qkv 3C, MLP 4C, V unpadded) the count
+    holds for B = 4 sequences of T = 64 positions, the small 124M configuration,
+    and for no other batch shape of up to 4096 positions."""
+    g = read_golden("gpt2_124m_run_log.txt")
+    cfg = syn.CONFIGS["124M_small"]
+    L, C, H, V = cfg.L, cfg.C, cfg.H, cfg.V
+
+    def count(B, T):
+        N = B * T
+        per_layer = (N * C + 2 * N            # ln_1 output, mean, rstd
+                     + N * 3 * C              # qkv
+                     + 2 * B * H * T * T      # scores, probabilities
+                     + N * C + N * C          # attention output, its projection
+                     + N * C                  # residual after attention
+                     + N * C + 2 * N          # ln_2 output, mean, rstd
+                     + 2 * N * 4 * C          # MLP pre-activation, GELU output
+                     + N * C + N * C)         # MLP projection, block output
+        return N * C + L * per_layer + N * C + 2 * N + 2 * N * V + N
+
+    assert count(cfg.B, cfg.T) == g["num_activations"]
+    others = [(B, T) for B in range(1, 65) for T in range(1, 1025)
+              if B * T <= 4096 and (B, T) != (cfg.B, cfg.T) and count(B, T) == g["num_activations"]]
+    assert others == []
+
+
 def test_uniform_logits_give_printed_loss(o64):
     """wte = 0 makes every tied logit exactly 0, so the loss is exactly ln V."""
     g = read_golden("uniform_char_loss.txt")
