@@ -114,3 +114,16 @@ def test_dropout_host_logic(L):
     assert L.gpt2_set_dropout(None, 0.1, 0) == B_.GPT2_EINVAL
     assert L.gpt2_op_attention_forward_dropout(fake, fake, fake, 1, 8, 64, 1, B_.GPT2_MODE_BF16, None, 0.1,
                                                None, None) == B_.GPT2_EINVAL  # bits required
+
+
+def test_missing_library_fails_loudly():
+    """Without the built CUDA library the binding raises; there is no fallback."""
+    import subprocess
+    import sys
+    code = ("import gpt_decoder_step_train_b300.binding as b\n"
+            "b.LIB_PATH = '/nonexistent/libgpt2_b300.so'\n"
+            "b._lib = None\n"
+            "try:\n    b.lib()\nexcept RuntimeError as e:\n    print('raised', 'missing' in str(e))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=120)
+    assert r.stdout.strip() == "raised True", (r.stdout, r.stderr[-1000:])
