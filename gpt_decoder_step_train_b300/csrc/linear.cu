@@ -41,43 +41,49 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 
 template <typename T>
 __global__ void bias_grad_partial_kernel(float* __restrict__ partial, const T* __restrict__ dout,
-                                         int N, int OC, int ld) {
+                                         int N, int OC, int ld, int nchunk) {
     __shared__ float4 sh[8][33];
     const int col = (blockIdx.x * 32 + threadIdx.x) * 4;
-    const int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
-    // vector loads need the 4 columns inside the row and an aligned row stride
-    const bool vec = col + 4 <= OC && (ld & 3) == 0;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < OC) {
-        if (vec) {
+    // vector loads need the 4 columns inside the row, an aligned row stride and
+    // an aligned base (a column slice of a wider matrix may start anywhere)
+    const bool vec = col + 4 <= OC && (ld & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(dout) & (4 * sizeof(T) - 1)) == 0;
+    // chunks of BG_ROWS rows, grid-strided over blockIdx.y (at most 65535 blocks high)
+    for (int chunk = blockIdx.y; chunk < nchunk; chunk += gridDim.y) {
+        const int r0 = chunk * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < OC) {
+            if (vec) {
 #pragma unroll 4
-            for (int r = r0 + threadIdx.y; r < r1; r += 8) {
-                const float4 v = load4(dout + (size_t)r * ld + col);
-                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-            }
-        } else {
-            for (int r = r0 + threadIdx.y; r < r1; r += 8) {
-                const T* row = dout + (size_t)r * ld + col;
-                s.x += to_f(row[0]);
-                if (col + 1 < OC) s.y += to_f(row[1]);
-                if (col + 2 < OC) s.z += to_f(row[2]);
-                if (col + 3 < OC) s.w += to_f(row[3]);
+                for (int r = r0 + threadIdx.y; r < r1; r += 8) {
+                    const float4 v = load4(dout + (size_t)r * ld + col);
+                    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+                }
+            } else {
+                for (int r = r0 + threadIdx.y; r < r1; r += 8) {
+                    const T* row = dout + (size_t)r * ld + col;
+                    s.x += to_f(row[0]);
+                    if (col + 1 < OC) s.y += to_f(row[1]);
+                    if (col + 2 < OC) s.z += to_f(row[2]);
+                    if (col + 3 < OC) s.w += to_f(row[3]);
+                }
             }
         }
-    }
-    sh[threadIdx.y][threadIdx.x] = s;
-    __syncthreads();
-    if (threadIdx.y == 0 && col < OC) {
-        float4 t = sh[0][threadIdx.x];
-        for (int k = 1; k < 8; k++) {
-            const float4 u = sh[k][threadIdx.x];
-            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        sh[threadIdx.y][threadIdx.x] = s;
+        __syncthreads();
+        if (threadIdx.y == 0 && col < OC) {
+            float4 t = sh[0][threadIdx.x];
+            for (int k = 1; k < 8; k++) {
+                const float4 u = sh[k][threadIdx.x];
+                t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+            }
+            float* out = partial + (size_t)chunk * OC + col;
+            out[0] = t.x;
+            if (col + 1 < OC) out[1] = t.y;
+            if (col + 2 < OC) out[2] = t.z;
+            if (col + 3 < OC) out[3] = t.w;
         }
-        float* out = partial + (size_t)blockIdx.y * OC + col;
-        out[0] = t.x;
-        if (col + 1 < OC) out[1] = t.y;
-        if (col + 2 < OC) out[2] = t.z;
-        if (col + 3 < OC) out[3] = t.w;
+        __syncthreads();
     }
 }
 
@@ -97,9 +103,9 @@ static size_t bias_scratch_bytes(int N, int OC) {
 template <typename T>
 static int bias_grad(float* db, const T* dout, int N, int OC, int ld, float* scratch,
                      cudaStream_t st) {
-    int nchunk = ceil_div(N, BG_ROWS);
-    count_launch(), bias_grad_partial_kernel<T><<<dim3(ceil_div(OC, 128), nchunk), dim3(32, 8), 0, st>>>(
-        scratch, dout, N, OC, ld);
+    const int nchunk = ceil_div(N, BG_ROWS);
+    count_launch(), bias_grad_partial_kernel<T><<<dim3(ceil_div(OC, 128), std::min(nchunk, 65535)), dim3(32, 8), 0,
+                                                  st>>>(scratch, dout, N, OC, ld, nchunk);
     count_launch(), bias_grad_reduce_kernel<<<ceil_div(OC, 256), 256, 0, st>>>(db, scratch, nchunk, OC);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;

@@ -111,7 +111,9 @@ int gpt2_op_linear_backward_weight(float* dw, float* dbias, const float* dout,
 
 /* Bias gradient alone: db[o] = sum_n dout[n*ld_dout + o] for o < OC,
  * OVERWRITTEN, summed in fp32 in a fixed order (row chunks, then chunk order).
- * dout is fp32, or bf16 when dout_bf16 != 0.
+ * dout is fp32, or bf16 when dout_bf16 != 0, with any element alignment (a
+ * column slice of a wider matrix is fine: unaligned rows are read one element
+ * at a time, which gives the same sums).  Any N >= 1.
  * scratch: gpt2_op_bias_grad_scratch_bytes(N, OC) bytes. */
 size_t gpt2_op_bias_grad_scratch_bytes(int N, int OC);
 int gpt2_op_bias_grad(float* db, const void* dout, int dout_bf16, int N, int OC, int ld_dout,
