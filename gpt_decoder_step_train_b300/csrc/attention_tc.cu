@@ -935,18 +935,10 @@ constexpr size_t dkv_smem_bf16() { return sizeof(__nv_bfloat16) * 4 * 32 * (HS +
 
 template <int HS>
 static int set_smem_attrs_bf16() {
-    static int done = 0;
-    if (done) return GPT2_OK;
-    if (cudaFuncSetAttribute(attn_fwd_bf16<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)fwd_smem_bf16<HS>()) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dq_bf16<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dq_smem_bf16<HS>()) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dkv_bf16<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dkv_smem_bf16<HS>()) != cudaSuccess) {
-        (void)cudaGetLastError();
+    if (smem_limit(reinterpret_cast<const void*>(attn_fwd_bf16<HS>), (int)fwd_smem_bf16<HS>()) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_bf16<HS>), (int)dq_smem_bf16<HS>()) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_bf16<HS>), (int)dkv_smem_bf16<HS>()))
         return GPT2_ECUDA;
-    }
-    done = 1;
     return GPT2_OK;
 }
 
@@ -984,18 +976,10 @@ constexpr size_t dkv_smem() { return sizeof(float) * (2 * 32 * ((HS + 4) + (HS +
 
 template <int HS>
 static int set_smem_attrs() {
-    static int done = 0;
-    if (done) return GPT2_OK;
-    if (cudaFuncSetAttribute(attn_fwd_tc<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)fwd_smem<HS>()) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dq_tc<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dq_smem<HS>()) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dkv_tc<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dkv_smem<HS>()) != cudaSuccess) {
-        (void)cudaGetLastError();
+    if (smem_limit(reinterpret_cast<const void*>(attn_fwd_tc<HS>), (int)fwd_smem<HS>()) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_tc<HS>), (int)dq_smem<HS>()) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc<HS>), (int)dkv_smem<HS>()))
         return GPT2_ECUDA;
-    }
-    done = 1;
     return GPT2_OK;
 }
 

@@ -940,17 +940,9 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
                            cudaStream_t st, const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(attn_fwd_tc05<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(attn_fwd_tc05<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
-                cudaSuccess) {
-            (void)cudaGetLastError();
-            return GPT2_ECUDA;
-        }
-        attr = true;
-    }
+    if (smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<false>), (int)SMEM) ||
+        smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<true>), (int)SMEM))
+        return GPT2_ECUDA;
     // qkv as a 3-D tensor [B][T][3C]: boxes of 64 rows x 64 columns (one head)
     CUtensorMap tm;
     const cuuint64_t dims[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
@@ -983,19 +975,11 @@ int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const f
                             const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
-    static bool attr = false;
-    if (!attr) {
-        const int ds = (int)DKV_SMEM, qs = (int)DQ_SMEM;
-        const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-        if (cudaFuncSetAttribute(attn_bwd_dkv_tc05<false>, a, ds) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_dkv_tc05<true>, a, ds) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_dq_tc05<false>, a, qs) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_dq_tc05<true>, a, qs) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return GPT2_ECUDA;
-        }
-        attr = true;
-    }
+    if (smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<false>), (int)DKV_SMEM) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<true>), (int)DKV_SMEM) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_tc05<false>), (int)DQ_SMEM) ||
+        smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_tc05<true>), (int)DQ_SMEM))
+        return GPT2_ECUDA;
     CUtensorMap tq, tdo;
     const cuuint64_t dq_[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t sq_[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)T * 3 * C * 2};

@@ -42,6 +42,10 @@ int num_sms();
 // Count one kernel launch (process-wide total, read by gpt2_kernel_launches).
 void count_launch();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, bytes); thread-safe.  GPT2_OK or GPT2_ECUDA.
+int smem_limit(const void* kernel, int bytes);
+
 // tanh-form GELU and its derivative, fp32.  s = sqrt(2/pi).
 #define GPT2_GELU_S 0.7978845608028654f
 #define GPT2_GELU_K 0.044715f

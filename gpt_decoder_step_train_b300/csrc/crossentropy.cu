@@ -258,12 +258,7 @@ GPT2_API int gpt2_op_crossentropy(float* losses, float* z, void* dz_bf16, const 
     if (!losses || !z || !tgt || N < 1 || V < 1 || ld < V || ld % 4 || !aligned16(z))
         return GPT2_EINVAL;
     if (dz_bf16 && (reinterpret_cast<uintptr_t>(dz_bf16) & 7)) return GPT2_EINVAL;
-    static bool attr = false;
-    if (!attr) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(crossentropy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           CE_CACHE_BYTES));
-        attr = true;
-    }
+    if (smem_limit(reinterpret_cast<const void*>(crossentropy_kernel), CE_CACHE_BYTES)) return GPT2_ECUDA;
     const int ncache = std::min(V >> 2, CE_CACHE_BYTES / 16);
     count_launch(), crossentropy_kernel<<<N, CE_THREADS, (size_t)ncache * 16, as_stream(stream)>>>(
         losses, z, static_cast<__nv_bfloat16*>(dz_bf16), tgt, V, ld, dscale, ncache, status);
@@ -276,12 +271,7 @@ GPT2_API int gpt2_op_crossentropy_bf16(float* losses, void* z, const int* tgt, i
     if (!losses || !z || !tgt || N < 1 || V < 1 || ld < V || ld % 8 || !aligned16(z) ||
         (size_t)ld * 2 > (size_t)CE16_MAX_ROW_BYTES)
         return GPT2_EINVAL;
-    static bool attr = false;
-    if (!attr) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(crossentropy_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           CE16_MAX_ROW_BYTES));
-        attr = true;
-    }
+    if (smem_limit(reinterpret_cast<const void*>(crossentropy_bf16_kernel), CE16_MAX_ROW_BYTES)) return GPT2_ECUDA;
     count_launch(), crossentropy_bf16_kernel<<<N, CE16_THREADS, (size_t)ld * 2, as_stream(stream)>>>(
         losses, static_cast<__nv_bfloat16*>(z), tgt, V, ld, dscale, status);
     GPT2_LAUNCH_CHECK();

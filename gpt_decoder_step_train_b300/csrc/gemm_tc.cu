@@ -644,15 +644,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
                    Params* pp) {
     using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<BN, BF16, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)S::SMEM) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return GPT2_ECUDA;
-        }
-        attr_done = true;
-    }
+    if (smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<BN, BF16, PAIR>), (int)S::SMEM)) return GPT2_ECUDA;
     const CUtensorMapSwizzle KSW = CU_TENSOR_MAP_SWIZZLE_128B;
     const CUtensorMapSwizzle MSW = BF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
     // A: K-major [M, K] (box {BK, 128}); M-major [K, M] (box {MN_BOX, BK})

@@ -448,12 +448,8 @@ int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db
     const int cpt = ceil_div(C, LNB_THREADS);
 #define LNB(CPT)                                                                                         \
     do {                                                                                                 \
-        static bool attr = false;                                                                        \
-        if (!attr) {                                                                                     \
-            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                               (int)(LNB_SMEM_BUDGET)));                                 \
-            attr = true;                                                                                 \
-        }                                                                                                \
+        if (smem_limit(reinterpret_cast<const void*>(ln_bwd_kernel<CPT>), (int)(LNB_SMEM_BUDGET)))     \
+            return GPT2_ECUDA;                                                                           \
         count_launch(), ln_bwd_kernel<CPT><<<pl.grid, LNB_THREADS, smem, st>>>(                          \
             dx, dx16, partial, dy, x, w, mean, rstd, N, C, pl.rpb, pl.rb, pl.stages, accumulate ? 1 : 0, status); \
     } while (0)
@@ -467,13 +463,9 @@ int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db
         const size_t rsm = (size_t)LNR_WARPS * 3 * C * sizeof(float);
 #define LNR(V4, DROP)                                                                                \
     do {                                                                                             \
-        static bool attr = false;                                                                    \
-        if (!attr) {                                                                                 \
-            GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_rows_kernel<V4, DROP>,                         \
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,          \
-                                               (int)((size_t)LNR_WARPS * 3 * 768 * sizeof(float)))); \
-            attr = true;                                                                             \
-        }                                                                                            \
+        if (smem_limit(reinterpret_cast<const void*>(ln_bwd_rows_kernel<V4, DROP>),                  \
+                       (int)((size_t)LNR_WARPS * 3 * 768 * sizeof(float))))                          \
+            return GPT2_ECUDA;                                                                       \
         count_launch(), ln_bwd_rows_kernel<V4, DROP><<<nblk, LNR_WARPS * 32, rsm, st>>>(            \
             dx, dxo, dxo_bf16 ? 1 : 0, partial, dy, x, w, mean, rstd, N, C, rpb, accumulate ? 1 : 0,  \
             bits, ks);                                                                               \

@@ -16,6 +16,7 @@
 #include <new>
 #include <atomic>
 #include <functional>
+#include <mutex>
 #include <vector>
 
 #include "dropout.cuh"
@@ -38,6 +39,26 @@ int num_sms() {
 
 static std::atomic<long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int smem_limit(const void* kernel, int bytes) {
+    struct Done {
+        const void* k;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Done> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Done& d : done)
+        if (d.k == kernel && d.dev == dev && d.bytes == bytes) return GPT2_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GPT2_ECUDA;
+    }
+    done.push_back(Done{kernel, dev, bytes});
+    return GPT2_OK;
+}
 
 constexpr int NT = 16;
 static const bool kDecay[NT] = {true, true, false, false, true, false, true, false,
@@ -827,6 +848,17 @@ GPT2_API int gpt2_destroy(gpt2* m) {
     if (m->g_out) cudaEventDestroy(m->g_out);
     for (cudaEvent_t e : m->trace_events) cudaEventDestroy(e);
     delete m;
+    return rc;
+}
+
+namespace gpt2k {
+int wait_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
+}
+
+GPT2_API int gpt2_wait_probe(gpt2* m, int wait_us) {
+    if (!m || wait_us < 1 || wait_us > 1000000) return GPT2_EINVAL;
+    int rc = wait_probe(&m->flags->status, (unsigned long long)wait_us * 1000ull, m->st);
+    if (rc) record(m, rc);
     return rc;
 }
 
