@@ -56,6 +56,7 @@ SIGNATURES = {
     "gpt2_adamw": (_i, [_vp, _f, _f, _f, _f, _f, _i]),
     "gpt2_destroy": (_i, [_vp]),
     "gpt2_status": (_i, [_vp]),
+    "gpt2_wait_probe": (_i, [_vp, _i]),
     "gpt2_strerror": (C.c_char_p, [_i]),
     "gpt2_grads": (_vp, [_vp]),
     "gpt2_adam_m": (_vp, [_vp]),

@@ -71,17 +71,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait shared by the roles of one CTA.  Returns false when the CTA is
-// aborting: this wait timed out (then it raises GPT2_STATUS_TIMEOUT in *status
-// and sets *abort_flag for the other roles) or another role already gave up.
+// aborting: this wait timed out after limit_ns (then it raises
+// GPT2_STATUS_TIMEOUT in *status and sets *abort_flag for the other roles) or
+// another role already gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, unsigned long long limit_ns = WAIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; i++) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_NS) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 set_status(status, GPT2_STATUS_TIMEOUT);
                 return false;

@@ -189,6 +189,19 @@ int gpt2_destroy(gpt2* m);
  * (including device-side status bits), then clear it. */
 int gpt2_status(gpt2* m);
 
+/* Check of the failure path of the bounded device waits (no counterpart on the
+ * pages; failure detection).  Every barrier wait of the tensor-core and
+ * bulk-copy kernels gives up after a limit, raises a timeout bit in the
+ * model's device status word, makes the other roles of its block leave, and the
+ * kernel returns instead of hanging.  This call launches, on the model's
+ * stream, one block that runs that same wait on two barriers nothing ever
+ * completes: the first wait is limited to wait_us microseconds (1 .. 10^6),
+ * the second to the library's one-second limit, and it leaves as soon as the
+ * first has given up.  Afterwards gpt2_status(m) returns GPT2_ETIMEOUT (and
+ * clears it); the device context and the model stay usable.  Returns EINVAL
+ * for a wait_us outside the range, ECUDA if the launch failed, else OK. */
+int gpt2_wait_probe(gpt2* m, int wait_us);
+
 /* Static description of a status code. */
 const char* gpt2_strerror(int code);
 
