@@ -348,20 +348,25 @@ def run_ours(args, cfg):
                                "launches_per_step": nl / args.steps}
         gemm_names = ("matmul_fwd", "matmul_bwd_input", "matmul_bwd_weight")
         gemm_ms = sum(kernels[n][0] for n in gemm_names) / args.steps
-        if args.mode == "tf32":
-            peak = peaks["bf16_tflops_sustained"] * TF32_OVER_BF16
-            peak_note = f"tf32 = bf16 sustained x 1.1/2.25 ({peak_src})"
-        elif args.mode == "bf16":
-            peak = peaks["bf16_tflops_sustained"]
-            peak_note = f"bf16 sustained ({peak_src})"
+        # the timed region is well under a second at full clocks: the burst peak
+        # is the denominator; the sustained (power-capped) figure is given beside it
+        ratio = {"tf32": TF32_OVER_BF16, "bf16": 1.0}.get(args.mode)
+        if ratio is not None:
+            peak = peaks["bf16_tflops"] * ratio
+            peak_sus = peaks["bf16_tflops_sustained"] * ratio
+            peak_note = (f"{args.mode} = bf16 burst x 1.1/2.25 (of {peak_src})" if args.mode == "tf32"
+                         else f"bf16 burst (of {peak_src})")
         else:
-            peak = None
+            peak = peak_sus = None
             peak_note = "fp32 SIMT mode"
         achieved = gemm_flops(cfg, B, T) / (gemm_ms / 1000.0) / 1e12
+        step_tf = step_flops(cfg, B, T) / (ms_per_step / 1000.0) / 1e12
         roofline = {"kernel": f"gemm_tc<{args.mode}> (all linear fwd/dX/dW products)", "bound": "tensor",
                     "achieved": round(achieved, 1), "peak": round(peak, 1) if peak else None,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                     "traffic": None, "peak_source": peak_note,
+                    "frac_of_sustained": round(achieved / peak_sus, 4) if peak_sus else None,
+                    "step_frac_of_burst": round(step_tf / peak, 4) if peak else None,
                     "share_of_step": round(gemm_ms / ms_per_step, 4)}
         if args.mode == "bf16" and args.config == "124M":
             # DRAM bytes per launch, from the committed ncu capture of this workload

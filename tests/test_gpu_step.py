@@ -227,3 +227,29 @@ def test_eval_gives_the_forward_loss_and_no_gradient(mode):
     assert model.forward(t_tok, t_tgt) == train
     assert model.backward() == 0
     model.close()
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("name", ["tiny", "124M_small"])
+def test_eval_matches_oracle(name, mode):
+    """gpt2_eval (forward-only evaluation, no gradient) against the oracle's
+    forward on the same inputs: the mean loss within the mode's loss bar, and
+    the per-position losses within its relative bar."""
+    from gpt_decoder_step_train_b300.binding import GPT2
+    cfg, _ = CASES[name]
+    o_losses, _, _ = oracle_result(name, False)
+    params = syn.init_params(cfg)
+    tok, tgt = syn.draw_tokens(cfg)
+    p = torch.from_numpy(params.copy()).cuda()
+    model = GPT2(cfg, p, mode=mode)
+    ev = model.eval(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+    assert model.status() == 0 and np.isfinite(ev)
+    assert abs(ev - o_losses[0]) <= TOL[mode]["loss"], (ev, o_losses[0])
+    g_pos = model.losses(cfg.B * cfg.T).cpu().numpy()
+    from oracle import Oracle
+    om = Oracle("f64").model(cfg.dims(), cfg.B, cfg.T)
+    om.forward(params.astype(np.float64), tok, tgt)
+    assert rel_l2(g_pos, om.losses()) <= TOL[mode]["rel"]
+    # evaluation leaves the parameters as they were
+    assert np.array_equal(p.cpu().numpy(), params)
+    model.close()
