@@ -1,31 +1,12 @@
-// attention_tc05.cu -- causal self-attention forward on the 5th-generation
-// tensor cores (tcgen05), bf16 operands, head size 64.
+// attention_tc05.cu -- causal self-attention, forward and backward, on the
+// 5th-generation tensor cores (tcgen05), bf16 operands, head size 64.
 //
 // Per (batch b, head h): S = Q K^T / sqrt(hs), S[i,j] = -inf for j > i,
 // P = softmax_rows(S), O = P V, and the row log-sum-exp of the scaled scores
 // is kept for the backward ("GPT-2 from scratch with torch", section
 // 自注意力; the 1/sqrt(d_k) scaling: "从头搭建GPT(Andrej Karpathy) 笔记",
-// section attention中为什么要做scaling).
-//
-// One CTA per (query tile of 128 rows, head, batch), 320 threads, two CTAs per SM:
-//   warp 0   TMA producer: the Q tile once, then K and V tiles of 64 keys
-//            into a three-stage ring (128-byte swizzle);
-//   warp 1   allocates tensor memory (S: two buffers of 64 columns, O: 64
-//            columns) and from one lane issues S = Q K^T (M=128, N=64, K=64) and O += P V
-//            (M=128, N=64, K=64; P from shared memory, V read MN-major);
-//   warps 2-9  softmax, one query row per thread (its TMEM lane), two warps
-//            per row (32 key columns each, the row maximum combined through
-//            shared memory): scores from tensor memory, causal mask on the
-//            diagonal tiles, online maximum and sum in the log2 domain, P
-//            written to shared memory as bf16 in the operand layout.  The running maximum used for P is
-//            only moved when a row's true maximum exceeds it by more than
-//            2^8; O in tensor memory is then rescaled before the next P V.
-//            At the end O / l goes out as bf16 and the log-sum-exp as fp32.
-// Key tiles past the query tile's last row are never visited (causal tile
-// skipping).  While the softmax warps work on S_j, the tensor cores compute
-// S_{j+1} into the other score buffer and P_{j-1} V_{j-1} (P is double-buffered
-// in shared memory too), so the softmax warps wait on the tensor cores only
-// when O must be rescaled.
+// section attention中为什么要做scaling).  The kernels' layouts are described
+// above each of them.
 // Every wait is bounded (about one second); a wait that gives up raises
 // GPT2_STATUS_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // and tensor memory is freed.
@@ -41,25 +22,11 @@ namespace at05 {
 using namespace ptx;
 
 constexpr int HS = 64;              // head size (one 128-byte swizzle row of bf16)
-constexpr int BQ = 128;             // queries per CTA (TMEM lanes)
-constexpr int BKV = 64;             // keys per tile
-constexpr int KV_STAGES = 3;
-// forward: producer, MMA issuer and eight softmax warps (two per TMEM lane
-// quarter, one per half of the key tile's columns)
-constexpr int FWD_EW_WARPS = 8;
-constexpr int FWD_THREADS = 64 + 32 * FWD_EW_WARPS;
+constexpr int BQ = 128;             // queries per tile (TMEM lanes)
 // backward kernels: producer, MMA issuer and eight element-wise warps (two per
 // TMEM lane quarter, one per half of the tile's 64 columns)
 constexpr int BWD_EW_WARPS = 8;
 constexpr int BWD_THREADS = 64 + 32 * BWD_EW_WARPS;
-constexpr int TMEM_COLS = 256;      // S (two buffers): [0, 64), [64, 128); O: [128, 192)
-constexpr uint32_t TILE_BYTES = BKV * HS * 2;     // one K or V tile: 8 KB
-constexpr uint32_t Q_BYTES = BQ * HS * 2;         // 16 KB
-constexpr uint32_t P_BYTES = BQ * BKV * 2;        // 16 KB
-// shared memory: Q | K[2] | V[2] | P, each 1024-byte aligned
-constexpr uint32_t OFF_Q = 0, OFF_K = OFF_Q + Q_BYTES, OFF_V = OFF_K + KV_STAGES * TILE_BYTES,
-                   OFF_P = OFF_V + KV_STAGES * TILE_BYTES, SMEM_USED = OFF_P + 2 * P_BYTES;
-constexpr size_t SMEM = SMEM_USED + 1024;          // + alignment slack
 constexpr float RESCALE_LOG2 = 8.f;                // move the running maximum past 2^8 growth
 constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
 
@@ -131,92 +98,210 @@ __device__ __forceinline__ bool mma_two_group_loop(int n, uint64_t* full, int st
     return true;
 }
 
+// ---------------------------------------------------------------- forward
+// Persistent: one CTA per SM (384 threads) walks work items, each a pair of
+// adjacent 128-row query tiles of one (batch, head) (rows 256 p .. 256 p + 255),
+// heaviest pairs first:
+//   warp 0     TMA producer: both query tiles of an item into one of two query
+//              buffers (the next item's load overlaps the current item), then
+//              the K and V tiles of 128 keys into a five-stage ring (128-byte
+//              swizzle);
+//   warp 1     from one lane issues the MMAs of both query tiles as their
+//              inputs become ready (a polling loop over the barriers):
+//              S_g = Q_g K_j^T (M 128, N 128, K 64) as soon as the softmax
+//              warps have read S_g(j - 1) and K_j has landed, so it runs while
+//              they compute; O_g += P_g V_j (M 128, N 64, K 128; P_g read
+//              from tensor memory, V from shared memory read MN-major) as
+//              soon as P_g(j) is written;
+//   warp 2     allocates and frees the tensor memory (S_0, S_1: 128 columns
+//              each; O_0, O_1: 64 columns each; P_0, P_1: 64 columns each,
+//              bf16 pairs);
+//   warps 4-7  softmax of query tile 0, warps 8-11 of query tile 1: one row
+//              per thread (its TMEM lane) over all 128 keys of a tile, so no
+//              row reduction crosses threads.  Causal mask only on the
+//              diagonal tile (and past T), online maximum and sum in the log2
+//              domain with the scale folded into one packed FMA before ex2,
+//              the running maximum moved only when a row's maximum grows past
+//              2^8 (O in tensor memory is then rescaled first), P written to
+//              its tensor-memory columns as bf16 pairs (the MMA's A operand:
+//              no shared-memory traffic for P).
+// Per query tile the softmax warps signal s_free (S read) and p_full (P
+// written); the MMA thread signals s_full (S ready) and pv_done (PV done:
+// O and P may be touched again).  Key tiles past a query tile's last row are
+// never visited.
+constexpr int F_BK = 128;                          // keys per tile
+constexpr int F_STAGES = 5;
+constexpr int F_THREADS = 384;
+constexpr uint32_t F_Q_BYTES = 128 * HS * 2;       // one query tile: 16 KB
+constexpr uint32_t F_KV_BYTES = F_BK * HS * 2;     // one K or V tile: 16 KB
+// two query buffers (the next item's pair of query tiles loads while the
+// current one runs), then the K and V rings
+constexpr uint32_t F_OFF_Q = 0, F_OFF_K = 4 * F_Q_BYTES, F_OFF_V = F_OFF_K + F_STAGES * F_KV_BYTES,
+                   F_SMEM_USED = F_OFF_V + F_STAGES * F_KV_BYTES;
+constexpr size_t F_SMEM = F_SMEM_USED + 1024;
+constexpr uint32_t F_TMEM_COLS = 512;   // S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0, P_1 [384,512)
+
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// (a, b) * s + c on both lanes of a packed pair
+__device__ __forceinline__ void fma2(float& a, float& b, uint64_t s, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(a, b)), "l"(s), "l"(c));
+    f2unpack(r, a, b);
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 128 consecutive accumulator columns of this warp's 32 TMEM lanes into v
+// (four loads, one wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+    float (&a)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
+    float (&b)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
+    float (&c)[32] = *reinterpret_cast<float(*)[32]>(&v[64]);
+    float (&d)[32] = *reinterpret_cast<float(*)[32]>(&v[96]);
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+    tmem_ld32(taddr + 64, c);
+    tmem_ld32(taddr + 96, d);
+    tmem_wait_ld(a);
+    tmem_wait_ld(b);
+    tmem_wait_ld(c);
+    tmem_wait_ld(d);
+}
+
+// Work items, heaviest first: item i is the query-tile pair npair - 1 - i / (B H)
+// of (batch, head) number i % (B H); the CTAs of the persistent grid take items
+// blockIdx.x, blockIdx.x + gridDim.x, ...
+struct FwdItem {
+    int b, h, qrow0, nkv0, nkv1, nkv;
+};
+__host__ __device__ __forceinline__ int fwd_items(int B, int T, int H) {
+    return B * H * (((T + 127) / 128 + 1) / 2);
+}
+__device__ __forceinline__ FwdItem fwd_item(int i, int B, int T, int H) {
+    const int npair = ((T + 127) / 128 + 1) / 2, nkt = (T + F_BK - 1) / F_BK;
+    const int pi = npair - 1 - i / (B * H), bh = i % (B * H);
+    FwdItem w;
+    w.b = bh / H;
+    w.h = bh % H;
+    w.qrow0 = pi * 256;
+    // key tiles each query tile needs (tile g ends at row qrow0 + 128 g + 127)
+    w.nkv0 = min(2 * pi + 1, nkt);
+    w.nkv1 = w.qrow0 + 128 < T ? min(2 * pi + 2, nkt) : 0;
+    w.nkv = max(w.nkv0, w.nkv1);
+    return w;
+}
+
 template <bool DROP>
-__global__ void __launch_bounds__(FWD_THREADS, 2)
+__global__ void __launch_bounds__(F_THREADS, 1)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,
-              int T, int C, int H, float scale_log2, int* status, const uint32_t* __restrict__ bits, float ks) {
+              int B, int T, int C, int H, float scale_log2, int* status, const uint32_t* __restrict__ bits,
+              float ks) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], s_free[2], p_full[2],
-        pv_done[2], drain;
-    __shared__ __align__(8) uint64_t pair_bar[4][2];
-    __shared__ float pair_val[2][2][BQ];
+    __shared__ __align__(8) uint64_t q_full[2], q_empty[2], kv_full[F_STAGES], kv_empty[F_STAGES], s_full[2],
+        s_free[2], p_full[2], pv_done[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nq = (T + BQ - 1) / BQ;
-    // grid (H, B, query tiles): every head's longest tile is launched first
-    const int qt = nq - 1 - (int)blockIdx.z;
-    const int h = blockIdx.x, b = blockIdx.y;
-    const int q0 = qt * BQ;
-    const int nkv = (min(q0 + BQ, T) + BKV - 1) / BKV;  // key tiles that hold keys <= the last row
+    const int nitems = fwd_items(B, T, H);
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* const base_ptr = smem_raw + (base - raw);
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        mbar_init(smem_u32(&q_full), 1);
-        for (int s = 0; s < KV_STAGES; s++) {
+        for (int q = 0; q < 2; q++) {
+            mbar_init(smem_u32(&q_full[q]), 1);
+            mbar_init(smem_u32(&q_empty[q]), 1);
+        }
+        for (int s = 0; s < F_STAGES; s++) {
             mbar_init(smem_u32(&kv_full[s]), 1);
             mbar_init(smem_u32(&kv_empty[s]), 1);
         }
-        for (int k = 0; k < 2; k++) {
-            mbar_init(smem_u32(&s_full[k]), 1);
-            mbar_init(smem_u32(&s_free[k]), FWD_EW_WARPS);
+        for (int g = 0; g < 2; g++) {
+            mbar_init(smem_u32(&s_full[g]), 1);
+            mbar_init(smem_u32(&s_free[g]), 4);
+            mbar_init(smem_u32(&p_full[g]), 4);
+            mbar_init(smem_u32(&pv_done[g]), 1);
         }
-        for (int k = 0; k < 2; k++) {
-            mbar_init(smem_u32(&p_full[k]), FWD_EW_WARPS);
-            mbar_init(smem_u32(&pv_done[k]), 1);
-        }
-        for (int q = 0; q < 4; q++)
-            for (int k = 0; k < 2; k++) mbar_init(smem_u32(&pair_bar[q][k]), 2);
         mbar_init(smem_u32(&drain), 1);
         fence_mbar_init();
         prefetch_map(&tm);
     }
-    if (warp == 1) tmem_alloc(&s_tmem, TMEM_COLS);
+    if (warp == 2) tmem_alloc(&s_tmem, F_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-
+    // registers: the producer / MMA warpgroup gives most of its share to the two
+    // softmax warpgroups (launched with 168 per thread: 4 x 32 x 88 +
+    // 8 x 32 x 208 = 64512 = 384 x 168)
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int last_j[KV_STAGES];                     // last tile issued into each stage (abort drain)
-            for (int s = 0; s < KV_STAGES; s++) last_j[s] = -1;
+            int last_kc[F_STAGES], last_ic[2];         // last fill of each buffer (abort drain)
+            for (int s = 0; s < F_STAGES; s++) last_kc[s] = -1;
+            last_ic[0] = last_ic[1] = -1;
             bool ok = true;
-            mbar_expect_tx(smem_u32(&q_full), Q_BYTES);
-            tma_load_3d(base + OFF_Q, &tm, h * HS, q0, b, smem_u32(&q_full));
-            tma_load_3d(base + OFF_Q + Q_BYTES / 2, &tm, h * HS, q0 + 64, b, smem_u32(&q_full));
-            for (int j = 0; j < nkv && ok; j++) {
-                const int s = j % KV_STAGES;
-                const uint32_t ph = (uint32_t)(j / KV_STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&kv_empty[s]), ph ^ 1u, &s_abort, status)) {
+            int kc = 0, ic = 0;                        // K/V tiles and items loaded so far
+            for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x, ic++) {
+                const FwdItem w = fwd_item(it, B, T, H);
+                const int qb = ic & 1;
+                if (!mbar_wait(smem_u32(&q_empty[qb]), ((uint32_t)(ic >> 1) & 1u) ^ 1u, &s_abort, status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_u32(&kv_full[s]);
-                mbar_expect_tx(fb, 2 * TILE_BYTES);
-                last_j[s] = j;
-                tma_load_3d(base + OFF_K + s * TILE_BYTES, &tm, C + h * HS, j * BKV, b, fb);
-                tma_load_3d(base + OFF_V + s * TILE_BYTES, &tm, 2 * C + h * HS, j * BKV, b, fb);
-                if (j + KV_STAGES < nkv) {             // this stage's next tile, into L2
-                    tma_prefetch_l2_3d(&tm, C + h * HS, (j + KV_STAGES) * BKV, b);
-                    tma_prefetch_l2_3d(&tm, 2 * C + h * HS, (j + KV_STAGES) * BKV, b);
+                mbar_expect_tx(smem_u32(&q_full[qb]), 2 * F_Q_BYTES);
+                last_ic[qb] = ic;
+                for (int k = 0; k < 4; k++)            // four 64-row boxes: tile 0, then tile 1
+                    tma_load_3d(base + F_OFF_Q + qb * 2 * F_Q_BYTES + k * (F_Q_BYTES / 2), &tm, w.h * HS,
+                                w.qrow0 + 64 * k, w.b, smem_u32(&q_full[qb]));
+                for (int j = 0; j < w.nkv; j++, kc++) {
+                    const int s = kc % F_STAGES;
+                    if (!mbar_wait(smem_u32(&kv_empty[s]), ((uint32_t)(kc / F_STAGES) & 1u) ^ 1u, &s_abort, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&kv_full[s]);
+                    mbar_expect_tx(fb, 2 * F_KV_BYTES);
+                    last_kc[s] = kc;
+                    for (int k = 0; k < 2; k++) {
+                        tma_load_3d(base + F_OFF_K + s * F_KV_BYTES + k * (F_KV_BYTES / 2), &tm, C + w.h * HS,
+                                    j * F_BK + 64 * k, w.b, fb);
+                        tma_load_3d(base + F_OFF_V + s * F_KV_BYTES + k * (F_KV_BYTES / 2), &tm, 2 * C + w.h * HS,
+                                    j * F_BK + 64 * k, w.b, fb);
+                    }
                 }
             }
             if (!ok) {
-                // wait (bounded, ignoring the abort flag) for every copy this thread issued
-                const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(smem_u32(&q_full), 0) && globaltimer() - t0 < WAIT_NS) {
+                // wait (bounded, ignoring the abort flag) for every copy this thread issued;
+                // earlier fills of a buffer completed before it was refilled
+                for (int q = 0; q < 2; q++) {
+                    if (last_ic[q] < 0) continue;
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(&q_full[q]), (uint32_t)(last_ic[q] >> 1) & 1u) &&
+                           globaltimer() - t0 < WAIT_NS) {
+                    }
                 }
-                // earlier copies into a stage completed before it was refilled, so
-                // only each stage's last issue can still be in flight
-                for (int s = 0; s < KV_STAGES; s++) {
-                    if (last_j[s] < 0) continue;
-                    const uint32_t ph = (uint32_t)(last_j[s] / KV_STAGES) & 1u;
+                for (int s = 0; s < F_STAGES; s++) {
+                    if (last_kc[s] < 0) continue;
+                    const uint32_t ph = (uint32_t)(last_kc[s] / F_STAGES) & 1u;
                     const uint64_t t1 = globaltimer();
                     while (!mbar_try_wait(smem_u32(&kv_full[s]), ph) && globaltimer() - t1 < WAIT_NS) {
                     }
@@ -226,30 +311,97 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id_s = instr_desc(BQ, BKV, false, false, true);   // Q K^T: both K-major
-            const uint32_t id_pv = instr_desc(BQ, HS, false, true, true);    // P V: V MN-major
-            const uint32_t t_s = tmem, t_o = tmem + 2 * BKV;   // S_j in columns (j & 1) * 64
-            if (mbar_wait(smem_u32(&q_full), 0, &s_abort, status)) {
-                auto issue_s = [&](int j) {            // S = Q K_j^T
-                    const uint32_t kb = base + OFF_K + (j % KV_STAGES) * TILE_BYTES;
-#pragma unroll
-                    for (int k = 0; k < HS / 16; k++)
-                        mma_issue<true>(t_s + (uint32_t)(j & 1) * BKV, smem_desc(base + OFF_Q + k * 32, 16, 1024, LAYOUT_SW128),
-                                        smem_desc(kb + k * 32, 16, 1024, LAYOUT_SW128), id_s, k > 0 ? 1u : 0u);
-                    mma_commit(smem_u32(&s_full[j & 1]));
+            const uint32_t id_s = instr_desc(128, F_BK, false, false, true);   // Q K^T: both K-major
+            const uint32_t id_pv = instr_desc(128, HS, false, true, true);     // P V: V MN-major
+            // descriptors precomputed; a K step of 16 bf16 is 32 bytes along a
+            // K-major row (2 units of 16 bytes) or 16 rows of an MN-major V tile
+            // (2048 bytes, 128 units)
+            const uint64_t dq0 = smem_desc(base + F_OFF_Q, 16, 1024, LAYOUT_SW128);
+            const uint64_t dk0 = smem_desc(base + F_OFF_K, 16, 1024, LAYOUT_SW128);
+            const uint64_t dv0 = smem_desc(base + F_OFF_V, 8192, 1024, LAYOUT_SW128);
+            bool ok = true;
+            int kc = 0, ic = 0;                        // K/V tiles and items consumed so far
+            int cs[2] = {0, 0}, cpv[2] = {0, 0};       // S and PV groups issued so far, per query tile
+            uint64_t t_last = globaltimer();
+            for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x, ic++) {
+                const FwdItem w = fwd_item(it, B, T, H);
+                const int qb = ic & 1;
+                if (!mbar_wait(smem_u32(&q_full[qb]), (uint32_t)(ic >> 1) & 1u, &s_abort, status)) { ok = false; break; }
+                auto issue_s = [&](int g, int j) {     // S_g = Q_g K_j^T (4 MMAs, K = 64)
+                    mma4_ss(tmem + g * F_BK, dq0 + (uint64_t)((qb * 2 + g) * (F_Q_BYTES >> 4)),
+                            dk0 + (uint64_t)(((kc + j) % F_STAGES) * (F_KV_BYTES >> 4)), 2, 2, id_s, 0u);
+                    mma_commit(smem_u32(&s_full[g]));
                 };
-                auto issue_pv = [&](int j) {           // O += P_j V_j (P_j in buffer j & 1)
-                    const uint32_t vb = base + OFF_V + (j % KV_STAGES) * TILE_BYTES;
-                    const uint32_t pb = base + OFF_P + (uint32_t)(j & 1) * P_BYTES;
-#pragma unroll
-                    for (int k = 0; k < BKV / 16; k++)
-                        mma_issue<true>(t_o, smem_desc(pb + k * 32, 16, 1024, LAYOUT_SW128),
-                                        smem_desc(vb + k * 16 * 128, 8192, 1024, LAYOUT_SW128), id_pv,
-                                        (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&pv_done[j & 1]));
-                    mma_commit(smem_u32(&kv_empty[j % KV_STAGES]));
+                auto issue_pv = [&](int g, int j) {    // O_g += P_g V_j (8 MMAs, P_g in tensor memory)
+                    const uint64_t vb = dv0 + (uint64_t)(((kc + j) % F_STAGES) * (F_KV_BYTES >> 4));
+                    const uint32_t d = tmem + 2 * F_BK + g * HS, a = tmem + 2 * F_BK + 2 * HS + g * 64;
+                    mma4_ts(d, a, vb, 128, id_pv, j > 0 ? 1u : 0u);
+                    mma4_ts(d, a + 32, vb + 512, 128, id_pv, 1u);
+                    mma_commit(smem_u32(&pv_done[g]));
                 };
-                mma_two_group_loop(nkv, kv_full, KV_STAGES, s_free, 2, p_full, 2, &s_abort, status, issue_s, issue_pv);
+                // a K/V stage is released once every MMA group of this item that reads it
+                // was issued (S and PV of each query tile that needs the key tile)
+                auto tile_uses = [&](int j) { return (j < w.nkv0 ? 2 : 0) + (j < w.nkv1 ? 2 : 0); };
+                int uses[F_STAGES];
+                for (int st = 0; st < F_STAGES; st++) uses[st] = st < w.nkv ? tile_uses(st) : 0;
+                auto used = [&](int j) {
+                    const int st = j % F_STAGES;
+                    if (--uses[st] == 0) {
+                        mma_commit(smem_u32(&kv_empty[(kc + j) % F_STAGES]));
+                        if (j + F_STAGES < w.nkv) uses[st] = tile_uses(j + F_STAGES);
+                    }
+                };
+                const int n[2] = {w.nkv0, w.nkv1};
+                int ns[2] = {0, 0}, npv[2] = {0, 0};
+                for (uint32_t spin = 1; ok && (npv[0] < n[0] || npv[1] < n[1]); spin++) {
+                    bool progress = false;
+#pragma unroll
+                    for (int g = 0; g < 2; g++) {
+                        if (ns[g] < n[g]) {
+                            const int j = ns[g], gs = cs[g] + j;   // this S's index over the whole run
+                            if (mbar_test_wait(smem_u32(&kv_full[(kc + j) % F_STAGES]),
+                                               (uint32_t)((kc + j) / F_STAGES) & 1u) &&
+                                (gs == 0 || mbar_test_wait(smem_u32(&s_free[g]), (uint32_t)(gs - 1) & 1u))) {
+                                tc_fence_after();
+                                issue_s(g, j);
+                                used(j);
+                                ns[g]++;
+                                progress = true;
+                            }
+                        }
+                        if (npv[g] < ns[g]) {
+                            const int j = npv[g];
+                            if (mbar_test_wait(smem_u32(&p_full[g]), (uint32_t)(cpv[g] + j) & 1u)) {
+                                tc_fence_after();
+                                issue_pv(g, j);
+                                used(j);
+                                npv[g]++;
+                                progress = true;
+                            }
+                        }
+                    }
+                    if (progress) {
+                        t_last = globaltimer();
+                    } else {
+                        // nothing ready: poll again (non-blocking checks only; a
+                        // suspended try_wait resumes too late here)
+                        if ((spin & 255) == 0) {
+                            if (s_abort) ok = false;
+                            else if (globaltimer() - t_last > WAIT_NS) {
+                                s_abort = 1;
+                                set_status(status, GPT2_STATUS_TIMEOUT);
+                                ok = false;
+                            }
+                        }
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&q_empty[qb]));    // the item's S products have read Q
+                cs[0] += n[0];
+                cs[1] += n[1];
+                cpv[0] += n[0];
+                cpv[1] += n[1];
+                kc += w.nkv;
             }
             // every MMA issued has completed once this commit lands
             mma_commit(smem_u32(&drain));
@@ -257,155 +409,171 @@ attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict_
             while (!mbar_try_wait(smem_u32(&drain), 0) && globaltimer() - t0 < WAIT_NS) {
             }
         }
+    }
     } else {
-        // ------------------------------------------------ softmax (warps 2..9)
-        // warps w and w + 4 share a TMEM lane quarter (32 rows); each takes 32 of
-        // the tile's 64 key columns and 32 of O's 64 columns.  The pair combines
-        // its row maxima every tile through shared memory and a two-warp
-        // mbarrier (double-buffered by tile parity), so both use the same
-        // running maximum; each keeps its own part of the row sum.
-        const int quarter = warp & 3, half = (warp - 2) >> 2;
-        const int r = quarter * 32 + lane;             // row within the tile
-        const int row = q0 + r;
-        const uint32_t lane_base = ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * half);
-        const uint32_t t_s = tmem + lane_base, t_o = tmem + lane_base + 2 * BKV;
-        uint8_t* const pbuf = base_ptr + OFF_P;    // two P buffers, tile j in buffer j & 1
-        float m_run = -INFINITY, l_run = 0.f;          // log2-domain maximum in use, this half's sum of P
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
+        // ------------------------------------------------ softmax (warps 4-7: tile 0, 8-11: tile 1)
+        const int g = (warp - 4) >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;             // row within the query tile
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + g * F_BK, t_o = tmem + lane_base + 2 * F_BK + g * HS;
+        const uint32_t t_p = tmem + lane_base + 2 * F_BK + 2 * HS + g * 64;
+        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
         bool ok = true;
-        // dropout: this row's keep bits, one word per 32 keys
-        const uint32_t* brow = nullptr;
-        if constexpr (DROP)
-            if (row < T) brow = bits + (((size_t)b * H + h) * T + row) * (size_t)((T + 31) >> 5);
-        // exchange slot of tile j: pair_val[j & 1][half][r]; barrier pair_bar[quarter][j & 1]
-        auto exchange = [&](int j, float v, float* other) -> bool {
-            pair_val[j & 1][half][r] = v;
-            __syncwarp();
-            const uint32_t bar = smem_u32(&pair_bar[quarter][j & 1]);
-            if (lane == 0) mbar_arrive(bar);
-            if (!mbar_wait(bar, (uint32_t)(j >> 1) & 1u, &s_abort, status)) return false;
-            *other = pair_val[j & 1][half ^ 1][r];
-            return true;
-        };
-        for (int j = 0; j < nkv; j++) {
-            uint32_t keep_w = 0xffffffffu;
-            if constexpr (DROP) {
-                const int kw = j * BKV + 32 * half;
-                keep_w = brow && kw < T ? __ldg(brow + (kw >> 5)) : 0u;
-            }
-            if (!mbar_wait(smem_u32(&s_full[j & 1]), (uint32_t)(j >> 1) & 1u, &s_abort, status)) { ok = false; break; }
-            tc_fence_after();
-            float s[32];
-            tmem_ld32(t_s + (uint32_t)(j & 1) * BKV, s);
-            tmem_wait_ld(s);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free[j & 1]));
-            // mask (tiles that reach the diagonal or the sequence end), row maximum
-            // of the raw scores; the scale goes into the exponent's FMA
-            const int k0 = j * BKV + 32 * half;        // first key of this warp's columns
-            if (k0 + 31 > q0 || k0 + 32 > T) {
+        int cs = 0, cpv = 0;                           // S tiles read and PV products waited for, so far
+        for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+            const FwdItem w = fwd_item(it, B, T, H);
+            const int row = w.qrow0 + 128 * g + r;
+            const int n = g == 0 ? w.nkv0 : w.nkv1;
+            float m_run = -INFINITY;                   // log2-domain maximum in use
+            uint64_t l2 = f2pack(0.f, 0.f);            // this row's sum of P, two partial lanes
+            const uint32_t* brow = nullptr;
+            if constexpr (DROP)
+                if (row < T) brow = bits + (((size_t)w.b * H + w.h) * T + row) * (size_t)((T + 31) >> 5);
+            for (int j = 0; j < n; j++) {
+                uint32_t keep_w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                if constexpr (DROP) {
 #pragma unroll
-                for (int c = 0; c < 32; c++)
-                    if (k0 + c > row || k0 + c >= T) s[c] = -INFINITY;
-            }
-            float m8[8];
-#pragma unroll
-            for (int c = 0; c < 8; c++) m8[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
-            float pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            float om;
-            if (!exchange(j, pm, &om)) { ok = false; break; }
-            const float mx = fmaxf(pm, om) * scale_log2;    // log2-domain maximum of the tile's row
-            float alpha = 1.f;                         // factor on O and l for this tile
-            if (mx > m_run + RESCALE_LOG2 || (m_run == -INFINITY && mx > -INFINITY)) {
-                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
-                m_run = mx;
-            }
-            const float mref = m_run == -INFINITY ? 0.f : m_run;
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 32; c++) {
-                s[c] = ex2(fmaf(s[c], scale_log2, -mref));
-                ps[c & 3] += s[c];
-            }
-            l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-            // dropped weights leave the sum (the softmax normaliser) and miss V
-            if constexpr (DROP) {
-#pragma unroll
-                for (int c = 0; c < 32; c++)
-                    if (!((keep_w >> c) & 1u)) s[c] = 0.f;
-            }
-            // a rescale of O needs every earlier P V complete (the last is P_{j-1} V_{j-1})
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                if (!mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, &s_abort, status)) {
-                    ok = false;
-                    break;
+                    for (int q = 0; q < 4; q++) {
+                        const int kw = j * F_BK + 32 * q;
+                        keep_w[q] = brow && kw < T ? __ldg(brow + (kw >> 5)) : 0u;
+                    }
                 }
+                if (!mbar_wait(smem_u32(&s_full[g]), (uint32_t)(cs + j) & 1u, &s_abort, status)) { ok = false; break; }
                 tc_fence_after();
-                {
-                    float o[32];
-                    tmem_ld32(t_o, o);
-                    tmem_wait_ld(o);
+                float sv[128];
+                tmem_ld128(t_s, sv);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s_free[g]));   // the next S_g may be computed now
+                // mask: the diagonal tile and the sequence end
+                const int k0 = j * F_BK;
+                if (k0 + F_BK - 1 > row || k0 + F_BK > T) {
 #pragma unroll
-                    for (int c = 0; c < 32; c++) o[c] *= alpha;
-                    tmem_st32(t_o, o);
+                    for (int c = 0; c < 128; c++)
+                        if (k0 + c > row || k0 + c >= T) sv[c] = -INFINITY;
+                }
+                float mx;
+                {
+                    float m43[43];
+#pragma unroll
+                    for (int c = 0; c < 42; c++) m43[c] = max3(sv[3 * c], sv[3 * c + 1], sv[3 * c + 2]);
+                    m43[42] = fmaxf(sv[126], sv[127]);
+                    float m15[15];
+#pragma unroll
+                    for (int c = 0; c < 14; c++) m15[c] = max3(m43[3 * c], m43[3 * c + 1], m43[3 * c + 2]);
+                    m15[14] = m43[42];
+                    float m5[5];
+#pragma unroll
+                    for (int c = 0; c < 5; c++) m5[c] = max3(m15[3 * c], m15[3 * c + 1], m15[3 * c + 2]);
+                    mx = fmaxf(max3(m5[0], m5[1], m5[2]), fmaxf(m5[3], m5[4])) * scale_log2;
+                }
+                float alpha = 1.f;                     // factor on O and l for this tile
+                if (mx > m_run + RESCALE_LOG2 || (m_run == -INFINITY && mx > -INFINITY)) {
+                    alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+                    m_run = mx;
+                }
+                const float mref = m_run == -INFINITY ? 0.f : m_run;
+                const uint64_t nm2 = f2pack(-mref, -mref);
+                uint64_t acc[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    fma2(sv[c], sv[c + 1], sc2, nm2);
+                    sv[c] = ex2(sv[c]);
+                    sv[c + 1] = ex2(sv[c + 1]);
+                    acc[(c >> 1) & 3] = add2(acc[(c >> 1) & 3], f2pack(sv[c], sv[c + 1]));
+                }
+                {
+                    float a0, a1;
+                    f2unpack(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), a0, a1);
+                    float l0, l1;
+                    f2unpack(l2, l0, l1);
+                    l2 = f2pack(l0 * alpha + a0, l1 * alpha + a1);
+                }
+                // O_g and the P_g columns are free once the previous PV_g has completed
+                // (at j = 0 the previous item's epilogue waited for it)
+                if (j > 0) {
+                    if (!mbar_wait(smem_u32(&pv_done[g]), (uint32_t)(cpv + j - 1) & 1u, &s_abort, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        float o[32];
+                        tmem_ld32(t_o + 32 * hh, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int c = 0; c < 32; c++) o[c] *= alpha;
+                        tmem_st32(t_o + 32 * hh, o);
+                    }
                     tmem_wait_st();
                 }
-            }
-            // buffer j & 1 is free once P_{j-2} V_{j-2} has completed
-            if (j > 1) {
-                if (!mbar_wait(smem_u32(&pv_done[j & 1]), (uint32_t)((j - 2) >> 1) & 1u, &s_abort, status)) {
-                    ok = false;
-                    break;
+                if constexpr (DROP) {
+#pragma unroll
+                    for (int c = 0; c < 128; c++)
+                        if (!((keep_w[c >> 5] >> (c & 31)) & 1u)) sv[c] = 0.f;
                 }
-                tc_fence_after();
-            }
-            uint8_t* const prow = pbuf + (size_t)(j & 1) * P_BYTES;
-            // this half of the P row (bf16) into the K-major operand tile
+                // the P row as bf16 pairs into the P_g columns
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const uint4 v = make_uint4(pack_bf16(s[8 * c], s[8 * c + 1]), pack_bf16(s[8 * c + 2], s[8 * c + 3]),
-                                           pack_bf16(s[8 * c + 4], s[8 * c + 5]),
-                                           pack_bf16(s[8 * c + 6], s[8 * c + 7]));
-                *reinterpret_cast<uint4*>(prow + sw128(r, 4 * half + c)) = v;
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; c++) pk[c] = pack_bf16(sv[64 * hh + 2 * c], sv[64 * hh + 2 * c + 1]);
+                    tmem_st32u(t_p + 32 * hh, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&p_full[g]));
             }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
-        }
-        // the row sum: this half's part plus the partner's (same order in both warps)
-        float l_other = 0.f;
-        if (ok && !exchange(nkv, l_run, &l_other)) ok = false;
-        if (ok && mbar_wait(smem_u32(&pv_done[(nkv - 1) & 1]), (uint32_t)((nkv - 1) >> 1) & 1u, &s_abort, status)) {
+            if (!ok || n == 0) continue;
+            if (!mbar_wait(smem_u32(&pv_done[g]), (uint32_t)(cpv + n - 1) & 1u, &s_abort, status)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            float o[32];
-            tmem_ld32(t_o, o);
-            tmem_wait_ld(o);
+            cs += n;
+            cpv += n;
+            float o[64];
+            {
+                float (&oa)[32] = *reinterpret_cast<float(*)[32]>(&o[0]);
+                float (&ob)[32] = *reinterpret_cast<float(*)[32]>(&o[32]);
+                tmem_ld32(t_o, oa);
+                tmem_ld32(t_o + 32, ob);
+                tmem_wait_ld(oa);
+                tmem_wait_ld(ob);
+            }
             if (row < T) {
-                const float l = half == 0 ? l_run + l_other : l_other + l_run;
+                float l0, l1;
+                f2unpack(l2, l0, l1);
+                const float l = l0 + l1;
                 const float inv = (DROP ? ks : 1.f) / l;
-                uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)b * T + row) * C + h * HS + 32 * half);
+                uint4* yr = reinterpret_cast<uint4*>(y + ((size_t)w.b * T + row) * C + w.h * HS);
 #pragma unroll
-                for (int c = 0; c < 4; c++)
+                for (int c = 0; c < 8; c++)
                     yr[c] = make_uint4(pack_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
                                        pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                                        pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
                                        pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-                if (half == 0) lse[((size_t)b * H + h) * T + row] = (m_run + log2f(l)) * LN2;
+                lse[((size_t)w.b * H + w.h) * T + row] = (m_run + log2f(l)) * LN2;
             }
+            // the next item's PV_g(0) overwrites O_g: every lane has read it
+            tc_fence_before();
+            __syncwarp();
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, F_TMEM_COLS);
     }
 }
-
 
 // ---------------------------------------------------------------- backward
 // With c = 1/sqrt(hs), lse the forward's row log-sum-exp and D_i = dO_i . O_i:
@@ -940,8 +1108,8 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
                            cudaStream_t st, const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
-    if (smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<false>), (int)SMEM) ||
-        smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<true>), (int)SMEM))
+    if (smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<false>), (int)F_SMEM) ||
+        smem_limit(reinterpret_cast<const void*>(attn_fwd_tc05<true>), (int)F_SMEM))
         return GPT2_ECUDA;
     // qkv as a 3-D tensor [B][T][3C]: boxes of 64 rows x 64 columns (one head)
     CUtensorMap tm;
@@ -951,13 +1119,14 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
     if (!encode_tensor_map(&tm, true, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return GPT2_ENOTSUP;
     const float scale_log2 = LOG2E / sqrtf((float)HS);
-    const dim3 grid(H, B, (T + BQ - 1) / BQ);
+    const int nitems = fwd_items(B, T, H);
+    const dim3 grid(std::min(nitems, num_sms()));
     if (bits)
-        count_launch(), attn_fwd_tc05<true><<<grid, FWD_THREADS, SMEM, st>>>(
-            tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status, bits, ks);
+        count_launch(), attn_fwd_tc05<true><<<grid, F_THREADS, F_SMEM, st>>>(
+            tm, static_cast<__nv_bfloat16*>(y), lse, B, T, C, H, scale_log2, status, bits, ks);
     else
-        count_launch(), attn_fwd_tc05<false><<<grid, FWD_THREADS, SMEM, st>>>(
-            tm, static_cast<__nv_bfloat16*>(y), lse, T, C, H, scale_log2, status, nullptr, 1.f);
+        count_launch(), attn_fwd_tc05<false><<<grid, F_THREADS, F_SMEM, st>>>(
+            tm, static_cast<__nv_bfloat16*>(y), lse, B, T, C, H, scale_log2, status, nullptr, 1.f);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

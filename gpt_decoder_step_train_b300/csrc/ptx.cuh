@@ -91,6 +91,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// try_wait whose suspension is limited to about `ns` nanoseconds
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// The same bounded wait with short suspensions (about 20 ns each): for a lone
+// issuing thread whose reaction time matters (a try_wait left to the default
+// limit can resume well after the phase flips), without a busy loop taking
+// issue slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+    if (mbar_try_wait_ns(bar, parity, 20)) return true;
+    uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; i++) {
+        if (mbar_try_wait_ns(bar, parity, 20)) return true;
+        if ((i & 255) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_NS) {
+                *abort_flag = 1;
+                set_status(status, GPT2_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -290,6 +323,63 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
         "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
         "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers
+// (packed bf16 pairs, for an MMA operand held in tensor memory).
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// Four kind::f16 MMAs into one accumulator, operands from shared memory: the
+// descriptors of MMA i are a + i * a_step and b + i * b_step (start-address
+// units of 16 bytes); only the first takes `accumulate`, the rest accumulate.
+// One asm block, so nothing is scheduled between the issues.
+__device__ __forceinline__ void mma4_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t a_step, uint32_t b_step,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "l"(a + a_step), "l"(b + b_step), "l"(a + 2 * a_step),
+        "l"(b + 2 * b_step), "l"(a + 3 * a_step), "l"(b + 3 * b_step)
+        : "memory");
+}
+
+// Four kind::f16 MMAs into one accumulator with A in tensor memory (columns
+// a_tmem + 8 i for MMA i) and B descriptors b + i * b_step.
+__device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t b_step, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8), "l"(b + b_step), "r"(a_tmem + 16),
+        "l"(b + 2 * b_step), "r"(a_tmem + 24), "l"(b + 3 * b_step)
+        : "memory");
+}
+
+// One kind::f16 MMA whose A operand (M rows x 16 bf16) sits in tensor memory
+// at a_tmem (row = lane, two bf16 per 32-bit column), B from shared memory.
+__device__ __forceinline__ void mma_issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 

@@ -288,7 +288,8 @@ def _lse_f64(qkv, H):
 
 
 @pytest.mark.parametrize("B,T,C,H,ramp", [(1, 300, 768, 12, 0.0), (2, 200, 128, 2, 6.0), (1, 1024, 768, 12, 3.0),
-                                          (1, 64, 64, 1, 0.0), (3, 65, 192, 3, 6.0)])
+                                          (1, 64, 64, 1, 0.0), (3, 65, 192, 3, 6.0), (2, 384, 128, 2, 6.0),
+                                          (1, 513, 64, 1, 3.0), (4, 1024, 128, 2, 0.0)])
 def test_bf16_attention_forward_lse(B_, o64, B, T, C, H, ramp):
     """Forward output and log-sum-exp; `ramp` grows the key scale along the
     sequence so the row maxima keep rising across key tiles."""
