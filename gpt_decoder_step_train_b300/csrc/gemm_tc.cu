@@ -45,8 +45,15 @@ namespace gpt2k {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int EPI_WARPS = 8;                              // two per TMEM lane quarter
-constexpr int THREADS = 64 + 32 * EPI_WARPS;              // producer, MMA issuer, epilogue
+// Epilogue warps: two per TMEM lane quarter on single CTAs, four on CTA pairs
+// (each warp takes 32 accumulator rows and 1/2 or 1/4 of the tile's columns).
+// Threads: producer, MMA issuer, epilogue.
+template <bool PAIR>
+struct Epi {
+    static constexpr int WARPS = PAIR ? 16 : 8;
+    static constexpr int PER_QUARTER = WARPS / 4;
+    static constexpr int THREADS = 64 + 32 * WARPS;
+};
 
 // Per operand type: element bytes, k-block (one 128-byte row), MMA K, and the
 // MN-major box (128 bytes of MN x BK k-rows).
@@ -70,14 +77,14 @@ constexpr int EC = 16;
 template <int BN, bool BF16, bool PAIR = false>
 struct Shape {
     static constexpr int STAGES = PAIR ? 5 : (BN == 256 ? 4 : 6);
-    static constexpr int EPI_WARP = PAIR ? 8192 : 4096;   // epilogue bytes per warp
+    static constexpr int EPI_WARP = 4096;                  // epilogue bytes per warp
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // rows of A per tile
     static constexpr int A_BYTES = BM * 128;          // BM rows x 128 bytes
     static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + EPI_WARPS * EPI_WARP;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + Epi<PAIR>::WARPS * EPI_WARP;
 };
 
 struct Params {
@@ -208,7 +215,7 @@ __device__ __forceinline__ void get_row16(const uint8_t* box, int row, float (&a
 
 // ---------------------------------------------------------------- kernel
 template <int BN, bool BF16, bool PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Epi<PAIR>::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux,
                const __grid_constant__ CUtensorMap tmPre, const Params p) {
@@ -216,6 +223,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
     constexpr int RING_MAX = S::EPI_WARP / 1024;      // input boxes per warp (bf16 boxes)
+    constexpr int EPI_WARPS = Epi<PAIR>::WARPS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[S::STAGES], empty_bar[S::STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, aux_bar[EPI_WARPS][RING_MAX];
@@ -383,10 +391,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..9)
+        // ------------------------------------------------ epilogue (warps 2 ..)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int ew = warp - 2;
-        const int col_lo = (ew >> 2) * (BN / 2);     // this warp's half of the tile's columns
+        constexpr int WCOLS = BN / Epi<PAIR>::PER_QUARTER;   // this warp's share of the tile's columns
+        const int col_lo = (ew >> 2) * WCOLS;
         uint8_t* const wbuf = base_ptr + S::STAGES * S::STAGE_BYTES + ew * S::EPI_WARP;
         const bool has_aux = p.has_aux != 0;
         const bool pre = p.gelu && !p.partial;
@@ -408,7 +417,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             Unit c = unit_coords(p, u);
             const int m0 = c.m_tile * S::TILE_M + (int)rank * BM, n0 = c.n_tile * BN + col_lo;
             const int row0 = m0 + q * 32;
-            const int ncols = min(BN / 2, p.N - n0);
+            const int ncols = min(WCOLS, p.N - n0);
             const int nchunks = ncols > 0 ? (ncols + EC - 1) / EC : 0;
             auto aux_issue = [&](int k) {    // input box of chunk k of this tile (lane 0)
                 const uint32_t slot = aux_issued % (uint32_t)ring;
@@ -426,14 +435,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     Unit cn = unit_coords(p, un);
                     const int nn0 = cn.n_tile * BN + col_lo, nr0 = cn.m_tile * S::TILE_M + (int)rank * BM + q * 32;
                     if (nr0 < p.M)
-                        for (int k = 0; k < BN / 2 && nn0 + k < p.N; k += EC) tma_prefetch_l2(&tmAux, nn0 + k, nr0);
+                        for (int k = 0; k < WCOLS && nn0 + k < p.N; k += EC) tma_prefetch_l2(&tmAux, nn0 + k, nr0);
                 }
             }
             // the bias of this warp's columns: lane l holds columns n0 + 4l .. n0 + 4l + 3
             // (loaded before the accumulator is ready; shuffled out chunk by chunk)
             float4 bl = make_float4(0.f, 0.f, 0.f, 0.f);
             const bool use_bias = !p.partial && p.bias;
-            if (use_bias && 4 * lane < BN / 2) {
+            if (use_bias && 4 * lane < WCOLS) {
                 const int c0 = n0 + 4 * lane;
                 if (c0 + 4 <= p.N) {
                     bl = __ldg(reinterpret_cast<const float4*>(p.bias + c0));
@@ -450,10 +459,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_after();
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + col_lo);
-            for (int k = 0; k < nchunks; k++) {
+            // chunk k: its accumulator columns were loaded into r one chunk ahead;
+            // the next chunk's load goes out before this one is processed
+            auto chunk = [&](int k, uint32_t (&r)[16], uint32_t (&rn)[16]) -> bool {
+                tmem_wait16(r);
+                if (k + 1 < nchunks) tmem_ld16_async(taddr + (uint32_t)((k + 1) * EC), rn);
                 const int nc = n0 + k * EC;
-                uint32_t r[16];
-                tmem_ld16(taddr + (uint32_t)(k * EC), r);
                 float x[16];
 #pragma unroll
                 for (int j = 0; j < 16; j++) x[j] = __uint_as_float(r[j]);
@@ -473,8 +484,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t slot = aux_seq % (uint32_t)ring;
                     if (!mbar_wait(smem_u32(&aux_bar[ew][slot]), (aux_seq / (uint32_t)ring) & 1u, &s_abort,
                                    p.status)) {
-                        ok = false;
-                        break;
+                        return false;
                     }
                     aux_seq++;
                     outb = wbuf + slot * aux_bytes;
@@ -525,8 +535,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 box_seq++;
+                return true;
+            };
+            uint32_t ra[16], rb[16];
+            if (nchunks > 0) tmem_ld16_async(taddr, ra);
+            for (int k = 0; k < nchunks && ok; k += 2) {
+                if (!chunk(k, ra, rb) || (k + 1 < nchunks && !chunk(k + 1, rb, ra))) ok = false;
             }
-            if (!ok) break;
+            if (!ok) {
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");   // no load left in flight
+                break;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -714,7 +733,7 @@ static int pair_clusters() {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2));
-        cfg.blockDim = dim3(THREADS);
+        cfg.blockDim = dim3(Epi<true>::THREADS);
         cfg.dynamicSmemBytes = S::SMEM;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -735,7 +754,7 @@ template <int BN, bool BF16, bool PAIR>
 static int run(const Maps& mp, const Params& p, cudaStream_t st) {
     if constexpr (!PAIR) {
         int grid = (int)std::min<long long>(p.units, num_sms());
-        count_launch(), gemm_tc_kernel<BN, BF16, false><<<grid, THREADS, Shape<BN, BF16, false>::SMEM, st>>>(
+        count_launch(), gemm_tc_kernel<BN, BF16, false><<<grid, Epi<false>::THREADS, Shape<BN, BF16, false>::SMEM, st>>>(
             mp.a, mp.b, mp.out, mp.aux, mp.pre, p);
         GPT2_LAUNCH_CHECK();
         return GPT2_OK;
@@ -749,7 +768,7 @@ static int run(const Maps& mp, const Params& p, cudaStream_t st) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(Epi<true>::THREADS);
     cfg.dynamicSmemBytes = Shape<BN, BF16, true>::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -794,8 +813,8 @@ bool gemm_tc_pair(const GemmProblem& g, const GemmEpilogue* e) {
         on = (v && v[0] == '0') ? 0 : 1;
     }
     if (!on || !g.bf16 || g.M < 256 || g.N < 256 || tc::pair_clusters() <= 0) return false;
-    const bool plain = !e || (!e->bias && !e->residual && !e->gelu_x && !e->gelu);
-    return g.K >= 2048 || plain;
+    (void)e;
+    return true;
 }
 
 int gemm_tc_pair_slots() { return tc::pair_clusters(); }
