@@ -801,11 +801,9 @@ static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partia
 }  // namespace tc
 
 // bf16 products with at least 256 rows and 256 columns run on CTA pairs
-// (cta_group::2, 256 x 256 tiles) when the reduction is long (K >= 2048) or the
-// epilogue only converts and stores; short products with a bias, GELU, residual
-// or GELU' epilogue run on single CTAs (128 x 256 tiles), which measured faster
-// for them.  GPT2_GEMM_CTA_PAIRS=0 in the environment sends everything to
-// single CTAs.
+// (cta_group::2, 256 x 256 tiles, sixteen epilogue warps per CTA); smaller ones
+// on single CTAs (128 x 256 or 128 x 128 tiles).  GPT2_GEMM_CTA_PAIRS=0 in the
+// environment sends everything to single CTAs.
 bool gemm_tc_pair(const GemmProblem& g, const GemmEpilogue* e) {
     static int on = -1;
     if (on < 0) {
