@@ -15,48 +15,12 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "ptx.cuh"
+#include "attention_tc05.cuh"
 
 namespace gpt2k {
 namespace at05 {
 
 using namespace ptx;
-
-constexpr int HS = 64;              // head size (one 128-byte swizzle row of bf16)
-constexpr int BQ = 128;             // queries per tile (TMEM lanes)
-// backward kernels: producer, MMA issuer and eight element-wise warps (two per
-// TMEM lane quarter, one per half of the tile's 64 columns)
-constexpr int BWD_EW_WARPS = 8;
-constexpr int BWD_THREADS = 64 + 32 * BWD_EW_WARPS;
-constexpr float RESCALE_LOG2 = 8.f;                // move the running maximum past 2^8 growth
-constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
-
-// 128-byte swizzle of a K-major bf16 operand row: 16-byte chunk c of row r
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// 2^x on the special-function unit (inputs far below -126 flush to 0)
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Column sums of one warp's 32 output rows (lane = row row0 + lane; rows past
-// T hold 0) over 32 columns, for the bias gradient of the qkv projection:
-// colsum [B * ceil(T/32), 3C], row group b * ceil(T/32) + row0/32, columns
-// col0 .. col0+31.  Consumes v.
-__device__ __forceinline__ void store_colsum(float* colsum, float (&v)[32], int lane, int b, int row0, int T,
-                                             int C, int col0) {
-    warp_colsum<32>(v, lane);
-    if (row0 >= T) return;
-    colsum[((size_t)b * ((T + 31) >> 5) + (row0 >> 5)) * 3 * C + col0 + warp_colsum_col<32>(lane)] = v[0];
-}
 
 // Issue loop of the MMA thread.  Each tile j has two groups of MMAs:
 //   A  needs the tile's operand stage (full[j % stages], phase (j / stages) & 1)
@@ -140,48 +104,6 @@ constexpr uint32_t F_OFF_Q = 0, F_OFF_K = 4 * F_Q_BYTES, F_OFF_V = F_OFF_K + F_S
                    F_SMEM_USED = F_OFF_V + F_STAGES * F_KV_BYTES;
 constexpr size_t F_SMEM = F_SMEM_USED + 1024;
 constexpr uint32_t F_TMEM_COLS = 512;   // S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0, P_1 [384,512)
-
-__device__ __forceinline__ uint64_t f2pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-// (a, b) * s + c on both lanes of a packed pair
-__device__ __forceinline__ void fma2(float& a, float& b, uint64_t s, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(a, b)), "l"(s), "l"(c));
-    f2unpack(r, a, b);
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// 128 consecutive accumulator columns of this warp's 32 TMEM lanes into v
-// (four loads, one wait).
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
-    float (&a)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
-    float (&b)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
-    float (&c)[32] = *reinterpret_cast<float(*)[32]>(&v[64]);
-    float (&d)[32] = *reinterpret_cast<float(*)[32]>(&v[96]);
-    tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
-    tmem_ld32(taddr + 64, c);
-    tmem_ld32(taddr + 96, d);
-    tmem_wait_ld(a);
-    tmem_wait_ld(b);
-    tmem_wait_ld(c);
-    tmem_wait_ld(d);
-}
 
 // Work items, heaviest first: item i is the query-tile pair npair - 1 - i / (B H)
 // of (batch, head) number i % (B H); the CTAs of the persistent grid take items
@@ -1139,11 +1061,16 @@ namespace gpt2k {
 // forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64.  With
 // colsum != null also the column sums of dqkv per 32-row group
 // ([B * ceil(T/32), 3C], fp32, before bf16 rounding).
+int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
+                                   int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum);
+
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
                             int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum,
                             const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
+    // without dropout: the persistent 128 x 128 kernels (attention_bwd_tc05.cu)
+    if (!bits) return attention_tc05_backward_nodrop(dqkv, dy, qkv, lse, D, B, T, C, H, status, st, colsum);
     if (smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<false>), (int)DKV_SMEM) ||
         smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<true>), (int)DKV_SMEM) ||
         smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_tc05<false>), (int)DQ_SMEM) ||
