@@ -101,6 +101,7 @@ __global__ void enc_rank_kernel(int* __restrict__ sorted, const int* __restrict_
 }
 
 constexpr int ENC_SEG = 64;
+constexpr int ENC_PF = 8;              // gradient rows loaded together in the segment kernel
 
 // One block per segment of the sorted list.  All threads walk the segment's
 // entries in order (same token sequence from shared memory), each thread for
@@ -123,23 +124,33 @@ __global__ void enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict
     for (int c = threadIdx.x; c < C4; c += blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         int run_start = 0;
-        for (int e = 0; e <= cnt; e++) {
-            if (e == cnt || (e > 0 && s_tok[e] != s_tok[e - 1])) {
-                const int v = s_tok[e - 1];
-                const int lo = offset[v], hi = offset[v + 1];
-                if (lo >= seg_lo && hi <= seg_lo + cnt) {        // whole bucket in this segment
-                    float4 d = dwte[(size_t)v * C4 + c];
-                    d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
-                    dwte[(size_t)v * C4 + c] = d;
-                } else {                                       // slot 0: first run, 1: last run
-                    part[((size_t)seg * 2 + (run_start == 0 ? 0 : 1)) * C4 + c] = acc;
+        // the gradient rows of the segment, ENC_PF at a time: all loads of a group
+        // are in flight together, then added in entry order
+        float4 g[ENC_PF];
+        for (int e0 = 0; e0 <= cnt; e0 += ENC_PF) {
+#pragma unroll
+            for (int k = 0; k < ENC_PF; k++)
+                if (e0 + k < cnt) g[k] = __ldg(dx + (size_t)s_pos[e0 + k] * C4 + c);
+#pragma unroll
+            for (int k = 0; k < ENC_PF; k++) {
+                const int e = e0 + k;
+                if (e > cnt) break;
+                if (e == cnt || (e > 0 && s_tok[e] != s_tok[e - 1])) {
+                    const int v = s_tok[e - 1];
+                    const int lo = offset[v], hi = offset[v + 1];
+                    if (lo >= seg_lo && hi <= seg_lo + cnt) {        // whole bucket in this segment
+                        float4 d = dwte[(size_t)v * C4 + c];
+                        d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
+                        dwte[(size_t)v * C4 + c] = d;
+                    } else {                                       // slot 0: first run, 1: last run
+                        part[((size_t)seg * 2 + (run_start == 0 ? 0 : 1)) * C4 + c] = acc;
+                    }
+                    if (e == cnt) break;
+                    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    run_start = e;
                 }
-                if (e == cnt) break;
-                acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                run_start = e;
+                acc.x += g[k].x; acc.y += g[k].y; acc.z += g[k].z; acc.w += g[k].w;
             }
-            const float4 g = dx[(size_t)s_pos[e] * C4 + c];
-            acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
         }
     }
 }

@@ -310,3 +310,35 @@ def test_set_dropout_rules(B_):
     assert model.backward() == 0
     assert model.status() == 0
     model.close()
+
+
+def test_fullsize_dropout_row0_matches_oracle(B_, o64):
+    """The training forward of the GPT-2 124M B16 T1024 workload in bf16 mode
+    with dropout p = 0.1 at all four sites: row 0's losses equal a one-row
+    oracle forward under the same seed and step (element e of every site has
+    the same index in a one-row run for row 0: (0 T + t) C + c, and
+    ((0 H + h) T + i) T + j for the attention weights), and the masks matter
+    (the GPU row is nearer the dropped oracle row than the undropped one)."""
+    from gpt_decoder_step_train_b300.binding import GPT2
+    cfg = syn.CONFIGS["124M"]
+    p, seed = 0.1, 777
+    params = syn.init_params(cfg)
+    tok, tgt = syn.draw_tokens(cfg)
+    tp = torch.from_numpy(params.copy()).cuda()
+    model = GPT2(cfg, tp, maxB=cfg.B, mode="bf16")
+    assert model.set_dropout(p, seed) == 0
+    loss = model.forward(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+    assert model.status() == 0 and np.isfinite(loss)
+    g_row = model.losses(cfg.B * cfg.T).cpu().numpy().reshape(cfg.B, cfg.T)[0].astype(np.float64)
+    model.close()
+    om = o64.model(cfg.dims(), 1, cfg.T)
+    p64 = params.astype(np.float64)
+    om.set_dropout(p, seed=seed, step=0)
+    o_mean = om.forward(p64, tok[:1], tgt[:1])
+    o_row = om.losses().astype(np.float64)
+    assert abs(g_row.mean() - o_mean) <= TOL["bf16"]["loss"], (g_row.mean(), o_mean)
+    assert rel_l2(g_row, o_row) <= TOL["bf16"]["rel"]
+    # the masks matter: the row is nearer the dropped oracle row than the undropped one
+    om.set_dropout(-1)
+    om.forward(p64, tok[:1], tgt[:1])
+    assert rel_l2(g_row, o_row) < rel_l2(g_row, om.losses().astype(np.float64))
