@@ -381,6 +381,9 @@ bool attention_tc_supported(int hs);
 bool attention_tc05_supported(int hs, int C);
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
                            cudaStream_t st, const uint32_t* bits, float ks);
+int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse,
+                                   float* D, int B, int T, int C, int H, int* status, cudaStream_t st,
+                                   float* colsum);
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
                             int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum,
                             const uint32_t* bits, float ks);
@@ -434,6 +437,12 @@ int attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, cons
     float* D = reinterpret_cast<float*>(scratch);
     if (mode == GPT2_MODE_BF16) {
         if (hs % 8) return GPT2_ENOTSUP;
+        // without dropout, head size 64: the tcgen05 kernels compute D themselves
+        if (!bits && attention_tc05_supported(hs, C)) {
+            if (colsum_done) *colsum_done = colsum != nullptr;
+            return attention_tc05_backward_nodrop(dqkv, dy, qkv, y, lse, D, B, T, C, H, status, st,
+                                                  colsum_done ? colsum : nullptr);
+        }
         launch_dot<__nv_bfloat16>(D, dy, y, B, T, C, H, hs, st);
         GPT2_LAUNCH_CHECK();
         if (attention_tc05_supported(hs, C)) {

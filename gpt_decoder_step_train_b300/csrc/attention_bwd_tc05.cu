@@ -13,7 +13,9 @@
 //                  pairs, then dV += P^T dO and dK += dS^T Q (M 128, N 64,
 //                  K 128, A from tensor memory, B = the query tile's dO and Q
 //                  read MN-major).
-//   attn_bwd_dq2   items are 128-query tiles (longest first); per 128-key tile
+//   attn_bwd_dq2   items are 128-query tiles (longest first); first D for the
+//                  tile's rows from its dO and O tiles (written out for the
+//                  dK/dV kernel, which runs after it); per 128-key tile
 //                  S = Q K^T and dP = dO V^T, then dS to tensor memory, then
 //                  dQ += dS K (K read MN-major).
 // Roles, 576 threads, one CTA per SM: warp 0 loads with TMA (the item's fixed
@@ -44,9 +46,11 @@ constexpr uint32_t B2_OFF_STAGE = 2 * B2_FIXED;             // two item buffers,
 // dK/dV stage: Q tile | dO tile | lse * log2(e) [128] | D [128]
 constexpr uint32_t KV2_STAGE = 2 * B2_TILE + 1024;
 constexpr size_t KV2_SMEM = B2_OFF_STAGE + (size_t)B2_STAGES * KV2_STAGE + 1024;
-// dQ stage: K tile | V tile
+// dQ: the item's Q, dO and O tiles (two buffers), then stages of K tile | V tile
+constexpr uint32_t Q2_FIXED = 3 * B2_TILE;
+constexpr uint32_t Q2_OFF_STAGE = 2 * Q2_FIXED;
 constexpr uint32_t Q2_STAGE = 2 * B2_TILE;
-constexpr size_t Q2_SMEM = B2_OFF_STAGE + (size_t)B2_STAGES * Q2_STAGE + 1024;
+constexpr size_t Q2_SMEM = Q2_OFF_STAGE + (size_t)B2_STAGES * Q2_STAGE + 1024;
 
 // Work items, heaviest first: item i is tile number (dK/dV: i / (B H); dQ:
 // ntiles - 1 - i / (B H)) of (batch, head) number i % (B H).
@@ -379,13 +383,16 @@ attn_bwd_dkv2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 }
 
 // ---------------------------------------------------------------- dQ
-// Shared memory: Q | dO of the item (two buffers) | four stages of K, V.
+// Shared memory: Q | dO | O of the item (two buffers) | four stages of K, V.
+// An item buffer is free again once the MMAs have read Q and dO and every
+// element-wise warp has read dO and O (for D).
 // Tensor memory: S [0, 128) | dP [128, 256) | dQ [256, 320) | dS [320, 384)
 // (bf16 pairs).
 __global__ void __launch_bounds__(B2_THREADS, 1)
 attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-             __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg, int B,
-             int T, int C, int H, float scale, int* status, float* __restrict__ colsum) {
+             const __grid_constant__ CUtensorMap to, __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse,
+             float* __restrict__ Dg, int B, int T, int C, int H, float scale, int* status,
+             float* __restrict__ colsum) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full[2], q_empty[2], st_full[B2_STAGES], st_empty[B2_STAGES], s_full, s_free,
         p_full, pv_done, drain;
@@ -401,7 +408,7 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         s_abort = 0;
         for (int k = 0; k < 2; k++) {
             mbar_init(smem_u32(&q_full[k]), 1);
-            mbar_init(smem_u32(&q_empty[k]), 1);
+            mbar_init(smem_u32(&q_empty[k]), 1 + B2_EW);      // the MMA thread and the element-wise warps
         }
         for (int s = 0; s < B2_STAGES; s++) {
             mbar_init(smem_u32(&st_full[s]), 1);
@@ -415,6 +422,7 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         fence_mbar_init();
         prefetch_map(&tq);
         prefetch_map(&tdo);
+        prefetch_map(&to);
     }
     if (warp == 1) tmem_alloc(&s_tmem, 512);
     tc_fence_before();
@@ -438,10 +446,11 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     break;
                 }
                 const uint32_t fb = smem_u32(&q_full[qb]);
-                mbar_expect_tx(fb, B2_FIXED);
+                mbar_expect_tx(fb, Q2_FIXED);
                 last_ic[qb] = ic;
-                load_tile(base + qb * B2_FIXED, &tq, w.h * HS, w.tile * 128, w.b, fb);
-                load_tile(base + qb * B2_FIXED + B2_TILE, &tdo, w.h * HS, w.tile * 128, w.b, fb);
+                load_tile(base + qb * Q2_FIXED, &tq, w.h * HS, w.tile * 128, w.b, fb);
+                load_tile(base + qb * Q2_FIXED + B2_TILE, &tdo, w.h * HS, w.tile * 128, w.b, fb);
+                load_tile(base + qb * Q2_FIXED + 2 * B2_TILE, &to, w.h * HS, w.tile * 128, w.b, fb);
                 for (int j = 0; j < w.n; j++, kc++) {
                     const int s = kc % B2_STAGES;
                     if (!mbar_wait(smem_u32(&st_empty[s]), ((uint32_t)(kc / B2_STAGES) & 1u) ^ 1u, &s_abort,
@@ -452,7 +461,7 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     const uint32_t sb = smem_u32(&st_full[s]);
                     mbar_expect_tx(sb, 2 * B2_TILE);
                     last_kc[s] = kc;
-                    const uint32_t st = base + B2_OFF_STAGE + s * Q2_STAGE;
+                    const uint32_t st = base + Q2_OFF_STAGE + s * Q2_STAGE;
                     load_tile(st, &tq, C + w.h * HS, j * 128, w.b, sb);
                     load_tile(st + B2_TILE, &tq, 2 * C + w.h * HS, j * 128, w.b, sb);
                 }
@@ -470,9 +479,9 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             const uint32_t id_s = instr_desc(128, 128, false, false, true);   // Q K^T, dO V^T: K-major
             const uint32_t id_o = instr_desc(128, HS, false, true, true);     // dS K: B MN-major
             const uint64_t dfix = smem_desc(base, 16, 1024, LAYOUT_SW128);
-            const uint64_t dst_k = smem_desc(base + B2_OFF_STAGE, 16, 1024, LAYOUT_SW128);
-            const uint64_t dst_mn = smem_desc(base + B2_OFF_STAGE, 8192, 1024, LAYOUT_SW128);
-            constexpr uint32_t FIX_U = B2_FIXED >> 4, TILE_U = B2_TILE >> 4, STAGE_U = Q2_STAGE >> 4;
+            const uint64_t dst_k = smem_desc(base + Q2_OFF_STAGE, 16, 1024, LAYOUT_SW128);
+            const uint64_t dst_mn = smem_desc(base + Q2_OFF_STAGE, 8192, 1024, LAYOUT_SW128);
+            constexpr uint32_t FIX_U = Q2_FIXED >> 4, TILE_U = B2_TILE >> 4, STAGE_U = Q2_STAGE >> 4;
             bool ok = true;
             int kc = 0, ic = 0, cs = 0;
             uint64_t t_last = globaltimer();
@@ -537,13 +546,40 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         const float c2 = scale * LOG2E;
         const uint64_t c2x2 = f2pack(c2, c2);
         bool ok = true;
-        int cs = 0;
-        for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        int cs = 0, ic = 0;
+        const uint8_t* const base_ptr = smem_raw + (base - raw);
+        for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x, ic++) {
             const BwdItem w = dq_item(it, B, T, H);
             const int row = w.tile * 128 + r;
             const size_t bh = ((size_t)w.b * H + w.h) * T;
             const float lse2 = row < T ? __ldg(lse + bh + row) * LOG2E : INFINITY;   // +inf zeroes P past T
-            const float Drow = row < T ? __ldg(Dg + bh + row) : 0.f;
+            // D = dO . O over the row's 64 head columns, from the item's tiles (every
+            // warp of the row computes it; the first writes it out for dK/dV)
+            const int qb = ic & 1;
+            if (!mbar_wait(smem_u32(&q_full[qb]), (uint32_t)(ic >> 1) & 1u, &s_abort, status)) { ok = false; break; }
+            float Drow = 0.f;
+            {
+                const uint8_t* tdo_s = base_ptr + qb * Q2_FIXED + B2_TILE + (r >> 6) * B2_BOX + (r & 63) * 128;
+                const uint8_t* to_s = tdo_s + B2_TILE;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint32_t off = (uint32_t)((c ^ (r & 7)) << 4);
+                    const uint4 a = *reinterpret_cast<const uint4*>(tdo_s + off);
+                    const uint4 o = *reinterpret_cast<const uint4*>(to_s + off);
+                    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+                        const float2 fo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+                        Drow = fmaf(fa.x, fo.x, Drow);
+                        Drow = fmaf(fa.y, fo.y, Drow);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&q_empty[qb]));     // this warp is done with dO and O
+            if (row >= T) Drow = 0.f;
+            else if (grp == 0) Dg[bh + row] = Drow;
             const uint64_t nl2 = f2pack(-lse2, -lse2), nd2 = f2pack(-Drow, -Drow);
             for (int j = 0; j < w.n; j++) {
                 if (!mbar_wait(smem_u32(&s_full), (uint32_t)(cs + j) & 1u, &s_abort, status)) { ok = false; break; }
@@ -617,33 +653,36 @@ attn_bwd_dq2(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 }  // namespace at05
 
 // dqkv [B,T,3C] (bf16, every element written) from dy [B,T,C], qkv, the
-// forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64, no
-// dropout.  With colsum != null also the column sums of dqkv per 32-row group
+// forward's output y [B,T,C] and lse [B,H,T]; D [B,H,T] = rowsum(dO o O) is
+// computed on the way (scratch, written by the dQ kernel, read by the dK/dV
+// kernel); head size 64, no dropout.  With colsum != null also the column sums of dqkv per 32-row group
 // ([B * ceil(T/32), 3C], fp32, before bf16 rounding).
-int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                                   int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum) {
+int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse,
+                                   float* D, int B, int T, int C, int H, int* status, cudaStream_t st,
+                                   float* colsum) {
     using namespace at05;
     if (C / H != HS || C % H || C % 8) return GPT2_ENOTSUP;
     if (smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv2), (int)KV2_SMEM) ||
         smem_limit(reinterpret_cast<const void*>(attn_bwd_dq2), (int)Q2_SMEM))
         return GPT2_ECUDA;
-    CUtensorMap tq, tdo;
+    CUtensorMap tq, tdo, to;
     const cuuint64_t dq_[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t sq_[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)T * 3 * C * 2};
     const cuuint64_t dd_[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t sd_[2] = {(cuuint64_t)C * 2, (cuuint64_t)T * C * 2};
     const cuuint32_t box[3] = {HS, 64, 1};
     if (!encode_tensor_map(&tq, true, 3, qkv, dq_, sq_, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map(&tdo, true, 3, dy, dd_, sd_, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tensor_map(&tdo, true, 3, dy, dd_, sd_, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&to, true, 3, y, dd_, sd_, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return GPT2_ENOTSUP;
     const float scale = 1.f / sqrtf((float)HS);
     auto* out = static_cast<__nv_bfloat16*>(dqkv);
     const int nitems = B * H * ((T + 127) / 128);
     const int grid = std::min(nitems, num_sms());
+    count_launch(), attn_bwd_dq2<<<grid, B2_THREADS, Q2_SMEM, st>>>(tq, tdo, to, out, lse, D, B, T, C, H, scale,
+                                                                    status, colsum);
     count_launch(), attn_bwd_dkv2<<<grid, B2_THREADS, KV2_SMEM, st>>>(tq, tdo, out, lse, D, B, T, C, H, scale, status,
                                                                       colsum);
-    count_launch(), attn_bwd_dq2<<<grid, B2_THREADS, Q2_SMEM, st>>>(tq, tdo, out, lse, D, B, T, C, H, scale, status,
-                                                                    colsum);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -1061,16 +1061,11 @@ namespace gpt2k {
 // forward's lse [B,H,T] and D [B,H,T] = rowsum(dO o O); head size 64.  With
 // colsum != null also the column sums of dqkv per 32-row group
 // ([B * ceil(T/32), 3C], fp32, before bf16 rounding).
-int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
-                                   int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum);
-
 int attention_tc05_backward(void* dqkv, const void* dy, const void* qkv, const float* lse, const float* D,
                             int B, int T, int C, int H, int* status, cudaStream_t st, float* colsum,
                             const uint32_t* bits, float ks) {
     using namespace at05;
     if (C / H != HS || C % H || !attention_tc05_supported(HS, C)) return GPT2_ENOTSUP;
-    // without dropout: the persistent 128 x 128 kernels (attention_bwd_tc05.cu)
-    if (!bits) return attention_tc05_backward_nodrop(dqkv, dy, qkv, lse, D, B, T, C, H, status, st, colsum);
     if (smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<false>), (int)DKV_SMEM) ||
         smem_limit(reinterpret_cast<const void*>(attn_bwd_dkv_tc05<true>), (int)DKV_SMEM) ||
         smem_limit(reinterpret_cast<const void*>(attn_bwd_dq_tc05<false>), (int)DQ_SMEM) ||
