@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gemm.cuh"
+
 namespace gpt2k {
 
 // floor(p * 2^32): a draw w keeps its element when w >= this
@@ -38,6 +40,6 @@ bool layernorm_backward_fuses_dropout(int C);
 int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db, float* dx_colsum, const float* dy,
                        const float* x, const float* w, const float* mean, const float* rstd, int N, int C,
                        int accumulate, void* scratch, size_t scratch_bytes, int* status, cudaStream_t st,
-                       const uint32_t* bits, float p);
+                       const uint32_t* bits, float p, ColReduce* defer = nullptr);
 
 }  // namespace gpt2k

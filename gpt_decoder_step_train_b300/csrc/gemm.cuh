@@ -81,6 +81,19 @@ bool gemm_tc_pair(const GemmProblem& p, const GemmEpilogue* e);
 int gemm_tc_pair_slots();
 bool gemm_tc_epilogue_supported(const GemmEpilogue& e);
 
+// A column reduction left for later: dst[k][c] = sum over g of part[g * ld +
+// k * seg + c] for c < seg, k < width / seg (groups summed in a fixed order).
+// Ops that produce per-group partial sums (the LayerNorm backward, the fused
+// bias gradients) can describe them with one of these instead of launching
+// their own reduction, and the training step then sums all of them in one
+// launch (colsum_batch).
+struct ColReduce {
+    const float* part;
+    int groups, ld, width, seg;
+    float* dst[3];
+};
+int colsum_batch(const ColReduce* r, int n, cudaStream_t st);
+
 // Linear-layer products for any operand type (linear.cu); bf16 requires
 // mode GPT2_MODE_BF16.
 // A bf16 GELU pre-activation (out_pre, gelu_x) goes with bf16 operands (`bf16`).
@@ -90,10 +103,13 @@ int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, con
 // With db != null, db[i] = sum over rows of dinp[:, i] as well: from the
 // epilogue's per-32-row column sums on the tensor cores, else by a pass over
 // dinp; cs is scratch of linear_colsum_bytes(N, IC) bytes.
+// With defer != null and the column sums fused into the tensor-core epilogue,
+// their reduction is described in *defer (defer->part == null otherwise)
+// instead of launched.
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
                           int* status, cudaStream_t st, float* db = nullptr, void* cs = nullptr,
-                          size_t cs_bytes = 0);
+                          size_t cs_bytes = 0, ColReduce* defer = nullptr);
 size_t linear_colsum_bytes(int N, int IC);
 // db[c] = sum over g of part[g * OC + c], in group order.
 int colsum_reduce(float* db, const float* part, int groups, int OC, cudaStream_t st);

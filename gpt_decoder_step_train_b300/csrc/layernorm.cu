@@ -430,7 +430,7 @@ bool layernorm_backward_fuses_dropout(int C) { return C >= 4 && C % 4 == 0 && ce
 int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db, float* dx_colsum, const float* dy,
                        const float* x, const float* w, const float* mean, const float* rstd, int N, int C,
                        int accumulate, void* scratch, size_t scratch_bytes, int* status, cudaStream_t st,
-                       const uint32_t* bits, float p) {
+                       const uint32_t* bits, float p, ColReduce* defer) {
     if (!dx || !dw || !db || !dy || !x || !w || !mean || !rstd || N < 1 || C < 4 || C % 4 ||
         C > LNB_THREADS * 8)
         return GPT2_EINVAL;
@@ -486,6 +486,11 @@ int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db
     else if (cpt <= 4) LNB(4);
     else LNB(8);
 #undef LNB
+    GPT2_LAUNCH_CHECK();
+    if (defer) {                                   // the caller sums the partials later
+        *defer = ColReduce{partial, nblk, 3 * C, dx_colsum ? 3 * C : 2 * C, C, {dw, db, dx_colsum}};
+        return GPT2_OK;
+    }
     count_launch(), ln_bwd_reduce_kernel<<<ceil_div(3 * C, 32), dim3(32, 16), 0, st>>>(dw, db, dx_colsum, partial,
                                                                                        nblk, C);
     GPT2_LAUNCH_CHECK();

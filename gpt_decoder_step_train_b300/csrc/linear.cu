@@ -137,6 +137,46 @@ int colsum_reduce(float* db, const float* part, int groups, int OC, cudaStream_t
     return GPT2_OK;
 }
 
+// ---- many column reductions in one launch ---------------------------------
+// Block (32 columns x 16 lanes) per (reduction, 32 columns): lane y sums groups
+// y, y+16, ... in order, then the 16 lane sums are added in lane order.
+constexpr int COLB_MAX = 400;                    // reductions per launch (kernel parameter space)
+struct ColReduceBatch {
+    int n;
+    ColReduce r[COLB_MAX];
+};
+
+__global__ void __launch_bounds__(512) colsum_batch_kernel(const __grid_constant__ ColReduceBatch b) {
+    __shared__ float sh[16][33];
+    const ColReduce& r = b.r[blockIdx.y];
+    const int c = blockIdx.x * 32 + threadIdx.x;
+    float s = 0.f;
+    if (c < r.width)
+        for (int g = threadIdx.y; g < r.groups; g += 16) s += r.part[(size_t)g * r.ld + c];
+    sh[threadIdx.y][threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.y == 0 && c < r.width) {
+        float t = sh[0][threadIdx.x];
+        for (int k = 1; k < 16; k++) t += sh[k][threadIdx.x];
+        r.dst[c / r.seg][c % r.seg] = t;
+    }
+}
+
+int colsum_batch(const ColReduce* r, int n, cudaStream_t st) {
+    for (int i0 = 0; i0 < n; i0 += COLB_MAX) {
+        ColReduceBatch b;
+        b.n = std::min(COLB_MAX, n - i0);
+        int wmax = 1;
+        for (int i = 0; i < b.n; i++) {
+            b.r[i] = r[i0 + i];
+            wmax = std::max(wmax, b.r[i].width);
+        }
+        count_launch(), colsum_batch_kernel<<<dim3(ceil_div(wmax, 32), b.n), dim3(32, 16), 0, st>>>(b);
+        GPT2_LAUNCH_CHECK();
+    }
+    return GPT2_OK;
+}
+
 // ---- split-K sum: out[i] = sum_s partial[s][i], in slice order -------------
 __global__ void splitk_reduce_kernel(float4* __restrict__ out, const float4* __restrict__ partial,
                                      int split, size_t n4) {
@@ -232,7 +272,8 @@ size_t linear_colsum_bytes(int N, int IC) {
 
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
-                          int* status, cudaStream_t st, float* db, void* cs, size_t cs_bytes) {
+                          int* status, cudaStream_t st, float* db, void* cs, size_t cs_bytes, ColReduce* defer) {
+    if (defer) defer->part = nullptr;
     if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
     if (db && (!cs || cs_bytes < linear_colsum_bytes(N, IC))) return GPT2_ENOMEM;
     GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status, bf16};
@@ -252,6 +293,10 @@ int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const vo
     if (fused) e.colsum = part;
     int rc = run_gemm(p, e, mode, st);
     if (rc || !db) return rc;
+    if (fused && defer) {
+        *defer = ColReduce{part, groups, IC, IC, IC, {db, nullptr, nullptr}};
+        return GPT2_OK;
+    }
     if (fused) return colsum_reduce(db, part, groups, IC, st);
     if (dinp_bf16) return bias_grad(db, static_cast<const __nv_bfloat16*>(dinp), N, IC, IC, part, st);
     return bias_grad(db, static_cast<const float*>(dinp), N, IC, IC, part, st);

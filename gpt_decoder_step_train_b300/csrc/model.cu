@@ -126,8 +126,10 @@ struct gpt2 {
     char *dres16, *dz16, *dbig, *datty, *dqkv;
     void* scratch;
     size_t scratch_bytes;
-    float* colsum;              // per-32-row column sums for the fused bias gradients
-    size_t colsum_bytes;
+    float* colsum;              // per-layer per-32-row column sums for the fused bias gradients
+    size_t colsum_fc_bytes, colsum_qkv_bytes;
+    char* lnpart;               // per-call partial sums of the LayerNorm backwards
+    size_t lnpart_bytes;
     // decoding: key/value cache [L][maxB][maxT][2C] and the rows of one step,
     // allocated by the first gpt2_decode
     char* dec;
@@ -226,11 +228,16 @@ static size_t plan(gpt2* m, char* base) {
     s = std::max(s, gpt2_op_bias_grad_scratch_bytes(Ri, 4 * Ci));
     m->scratch_bytes = s;
     m->scratch = take(s);
-    // column sums of the fused bias gradients: the MLP c_fc bias from the c_proj
-    // dX epilogue, the qkv bias from the attention backward
+    // per-group partial sums, kept until one reduction at the end of the
+    // backward: the MLP c_fc bias (c_proj dX epilogue) and the qkv bias
+    // (attention backward) of every layer, and every LayerNorm backward's
+    // gamma / beta / residual-gradient column sums
     const int att_groups = c.maxB * ceil_div(c.maxT, 32);
-    m->colsum_bytes = std::max(linear_colsum_bytes(Ri, 4 * Ci), (size_t)att_groups * 3 * C * sizeof(float));
-    m->colsum = F(m->colsum_bytes / sizeof(float));
+    m->colsum_fc_bytes = round_up(linear_colsum_bytes(Ri, 4 * Ci), 256);
+    m->colsum_qkv_bytes = round_up((size_t)att_groups * 3 * C * sizeof(float), 256);
+    m->colsum = reinterpret_cast<float*>(take(L * (m->colsum_fc_bytes + m->colsum_qkv_bytes)));
+    m->lnpart_bytes = round_up(gpt2_op_layernorm_backward_scratch_bytes(Ri, Ci), 256);
+    m->lnpart = take((2 * L + 1) * m->lnpart_bytes);
     return off;
 }
 
@@ -395,6 +402,17 @@ static int backward_impl(gpt2* m) {
     void* const dbr_att = b16 ? static_cast<void*>(m->dres16) : static_cast<void*>(m->dbig);
     const void* const op_mlp = drop ? static_cast<const void*>(dbr_mlp) : dres_op;
     const void* const op_att = drop ? static_cast<const void*>(dbr_att) : dres_op;
+    // column reductions left for one launch at the end
+    std::vector<ColReduce> red;
+    red.reserve(4 * L + 2);
+    ColReduce cr{};
+    auto keep = [&]() { if (cr.part) red.push_back(cr); cr = ColReduce{}; };
+    auto lnpart = [&](int k) { return static_cast<void*>(m->lnpart + (size_t)k * m->lnpart_bytes); };
+    auto cs_fc = [&](int l) { return reinterpret_cast<float*>(reinterpret_cast<char*>(m->colsum) + l * m->colsum_fc_bytes); };
+    auto cs_qkv = [&](int l) {
+        return reinterpret_cast<float*>(reinterpret_cast<char*>(m->colsum) + L * m->colsum_fc_bytes +
+                                        l * m->colsum_qkv_bytes);
+    };
     // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
     OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, dz_op, W(m, WTE), b16, nullptr, N, C, c.V,
                                                m->Vp, mode, status, st));
@@ -405,7 +423,9 @@ static int backward_impl(gpt2* m) {
     OP(LAYERNORM_BWD, layernorm_backward(m->dres, fuse ? dbr_mlp : m->dres16, !fuse || b16, G(m, LNFW), G(m, LNFB),
                                          drop && !fuse ? nullptr : G(m, FCPROJB) + (size_t)(L - 1) * C, m->dln,
                                          m->res3 + (size_t)(L - 1) * R * C, P(m, LNFW), m->lnf_mean, m->lnf_rstd, N,
-                                         C, 0, sc, sb, status, st, fuse ? drop_bits(m, 3 * L) : nullptr, pd));
+                                         C, 0, lnpart(0), m->lnpart_bytes, status, st,
+                                         fuse ? drop_bits(m, 3 * L) : nullptr, pd, &cr));
+    keep();
     for (int l = L - 1; l >= 0; l--) {
         const float* x = l == 0 ? m->x0 : m->res3 + (size_t)(l - 1) * R * C;
         const char* ln1 = Orow(m, m->ln1, l, C);
@@ -427,7 +447,8 @@ static int backward_impl(gpt2* m) {
         }
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dbig, b16, op_mlp, Wl(FCPROJW, 4 * cc), b16, fch, N,
                                                    4 * C, C, C, mode, status, st, G(m, FCB) + l * 4 * C,
-                                                   m->colsum, m->colsum_bytes));
+                                                   cs_fc(l), m->colsum_fc_bytes, &cr));
+        keep();
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCPROJW) + l * 4 * cc, op_mlp, fchg, b16, N,
                                                      4 * C, C, C, sc, sb, mode, status, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
@@ -440,8 +461,9 @@ static int backward_impl(gpt2* m) {
         OP(LAYERNORM_BWD, layernorm_backward(m->dres, fuse ? dbr_att : m->dres16, !fuse || b16, G(m, LN2W) + l * C,
                                              G(m, LN2B) + l * C, drop && !fuse ? nullptr : G(m, ATTPROJB) + l * C,
                                              m->dln, res2, P(m, LN2W) + l * C, m->ln2_mean + l * R,
-                                             m->ln2_rstd + l * R, N, C, 1, sc, sb, status, st,
-                                             fuse ? drop_bits(m, 2 + 3 * l) : nullptr, pd));
+                                             m->ln2_rstd + l * R, N, C, 1, lnpart(1 + 2 * l), m->lnpart_bytes, status,
+                                             st, fuse ? drop_bits(m, 2 + 3 * l) : nullptr, pd, &cr));
+        keep();
         // attention c_proj (bias gradient: with ln_2's backward above)
         if (drop && !fuse) {
             OP(DROPOUT, dropout_backward(dbr_att, b16, m->dres, drop_bits(m, 2 + 3 * l), N, C, pd, st));
@@ -455,10 +477,11 @@ static int backward_impl(gpt2* m) {
         // 32 rows, which give the qkv bias gradient at once
         bool qkv_colsum = false;
         OP(ATTENTION_BWD, attention_backward_dropout(m->dqkv, m->datty, qkv, atty, m->lse + l * R * H, B, T, C, H,
-                                                     sc, sb, mode, status, st, m->colsum, &qkv_colsum,
+                                                     sc, sb, mode, status, st, cs_qkv(l), &qkv_colsum,
                                                      drop ? drop_bits(m, 1 + 3 * l) : nullptr, drop ? pd : 0.f));
         if (qkv_colsum)
-            OP(BIAS_GRAD, colsum_reduce(G(m, QKVB) + l * 3 * C, m->colsum, B * ceil_div(T, 32), 3 * C, st));
+            red.push_back(ColReduce{cs_qkv(l), B * ceil_div(T, 32), 3 * C, 3 * C, 3 * C,
+                                    {G(m, QKVB) + l * 3 * C, nullptr, nullptr}});
         // c_attn
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dqkv, Wl(QKVW, 3 * cc), b16, nullptr, N,
                                                    C, 3 * C, 3 * C, mode, status, st));
@@ -475,11 +498,15 @@ static int backward_impl(gpt2* m) {
                                              G(m, LN1B) + l * C,
                                              l > 0 && (!drop || fuse) ? G(m, FCPROJB) + (size_t)(l - 1) * C : nullptr,
                                              m->dln, x, P(m, LN1W) + l * C, m->ln1_mean + l * R, m->ln1_rstd + l * R,
-                                             N, C, 1, sc, sb, status, st, fuse1 ? drop_bits(m, 3 * l) : nullptr, pd));
+                                             N, C, 1, lnpart(2 + 2 * l), m->lnpart_bytes, status, st,
+                                             fuse1 ? drop_bits(m, 3 * l) : nullptr, pd, &cr));
+        keep();
     }
     if (drop) OP(DROPOUT, dropout_backward(m->dres, false, m->dres, drop_bits(m, 0), N, C, pd, st));
     OP(ENCODER_BWD, gpt2_op_encoder_backward(G(m, WTE), G(m, WPE), m->dres, m->tok, B, T, c.maxT, C, c.V,
                                              sc, sb, st));
+    // every deferred column sum (bias and LayerNorm gradients), in one launch
+    OP(BIAS_GRAD, colsum_batch(red.data(), (int)red.size(), st));
     return GPT2_OK;
 }
 
