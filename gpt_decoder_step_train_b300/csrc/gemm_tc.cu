@@ -106,6 +106,7 @@ struct Params {
     int out_bf16;
     int pre_bf16;           // the GELU pre-activation is stored as bf16
     const float* bias;
+    int bias_vec;           // bias is 16-byte aligned
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -127,6 +128,66 @@ __device__ __forceinline__ float gelu_grad_fast(float x) {
     const float x2 = x * x;
     const float th = tanh_fast(GPT2_GELU_S * (x + GPT2_GELU_K * x2 * x));
     return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GPT2_GELU_S * (1.0f + 3.0f * GPT2_GELU_K * x2);
+}
+
+// Packed pairs of fp32 (two lanes of one 64-bit register) for the CTA-pair
+// epilogue: one f32x2 instruction works on two columns.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t splat2(float a) { return f2pack(a, a); }
+__device__ __forceinline__ uint32_t bf16x2(uint64_t v) {
+    float a, b;
+    f2unpack(v, a, b);
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// tanh-form GELU of a pair: 0.5 x (1 + tanh(u)), u = s (x + k x^3) = x (s + s k x^2)
+__device__ __forceinline__ uint64_t gelu2(uint64_t x) {
+    const uint64_t x2 = mul2(x, x);
+    const uint64_t u = mul2(x, fma2(x2, splat2(GPT2_GELU_S * GPT2_GELU_K), splat2(GPT2_GELU_S)));
+    float u0, u1;
+    f2unpack(u, u0, u1);
+    const uint64_t th = f2pack(tanh_fast(u0), tanh_fast(u1));
+    const uint64_t h = mul2(x, splat2(0.5f));
+    return fma2(h, th, h);
+}
+// its derivative: 0.5 (1 + th) + 0.5 x (1 - th^2) (s + 3 s k x^2)
+__device__ __forceinline__ uint64_t gelu_grad2(uint64_t x) {
+    const uint64_t x2 = mul2(x, x);
+    const uint64_t u = mul2(x, fma2(x2, splat2(GPT2_GELU_S * GPT2_GELU_K), splat2(GPT2_GELU_S)));
+    float u0, u1;
+    f2unpack(u, u0, u1);
+    const float t0 = tanh_fast(u0), t1 = tanh_fast(u1);
+    const uint64_t th = f2pack(t0, t1);
+    const uint64_t om = fma2(f2pack(-t0, -t1), th, splat2(1.f));
+    const uint64_t d1 = fma2(x2, splat2(3.f * GPT2_GELU_S * GPT2_GELU_K), splat2(GPT2_GELU_S));
+    const uint64_t g = mul2(mul2(mul2(x, splat2(0.5f)), om), d1);
+    return add2(fma2(th, splat2(0.5f), splat2(0.5f)), g);
+}
+// 128-byte swizzle: 16-byte unit `unit` of row `row` of a box with 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int row, int unit) {
+    return (uint32_t)(row * 128 + ((unit ^ (row & 7)) << 4));
 }
 
 // ---------------------------------------------------------------- scheduling
@@ -390,8 +451,180 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer() - t0 < WAIT_NS) {
             }
         }
+    } else if (PAIR && p.out_bf16 && !p.partial && !p.aux_residual) {
+        // ------------------------------------------------ epilogue, CTA pairs, bf16 output (warps 2 ..)
+        // Warp ew reads TMEM lane quarter q (32 accumulator rows, thread = row) and
+        // 64 of the tile's 256 columns, 16 at a time, with the next load in flight,
+        // and fills one box of 32 rows x 64 columns (128-byte rows, 128-byte
+        // swizzle) that one lane stores with one TMA copy: few, large stores leave
+        // the copy engine to the operand loads.  The arithmetic runs on packed fp32
+        // pairs.  A GELU input tile arrives by TMA into the box before the tile
+        // (issued once the previous tile's store has read it) and is overwritten in
+        // place.  With GELU the tile takes two passes over the accumulator: the
+        // pre-activation first, then (once that store has read the box) the
+        // activation.  The accumulator goes back to the MMA thread as soon as the
+        // last pass has loaded its last columns.
+        const int q = warp & 3;
+        const int ew = warp - 2;
+        const int col_lo = (ew >> 2) * 64;
+        uint8_t* const box = base_ptr + S::STAGES * S::STAGE_BYTES + ew * S::EPI_WARP;
+        const uint32_t box_s = smem_u32(box);
+        const bool pre = p.gelu != 0;
+        const bool gx = p.has_aux != 0;
+        const bool use_bias = p.bias != nullptr;
+        const uint32_t aux_bar_s = smem_u32(&aux_bar[ew][0]);
+        uint32_t aux_issued = 0, aux_done = 0;
+        // GELU input box of tile u (lane 0)
+        auto aux_issue = [&](long long u) {
+            Unit c = unit_coords(p, u);
+            const int x0 = c.n_tile * BN + col_lo, y0 = c.m_tile * S::TILE_M + (int)rank * BM + q * 32;
+            mbar_expect_tx(aux_bar_s, 4096u);
+            tma_load_2d(box_s, &tmAux, x0, y0, aux_bar_s);
+            aux_issued++;
+        };
+        if (gx && lane == 0 && u_first < p.units) aux_issue(u_first);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (long long u = u_first; u < p.units && ok; u += u_step) {
+            Unit c = unit_coords(p, u);
+            const int m0 = c.m_tile * S::TILE_M + (int)rank * BM, n0 = c.n_tile * BN + col_lo;
+            const int row0 = m0 + q * 32;
+            const int ncols = min(64, p.N - n0);
+            const int nchunks = ncols > 0 ? (ncols + EC - 1) / EC : 0;
+            const bool row_ok = row0 + lane < p.M;
+            if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (gx) {
+                if (!mbar_wait(aux_bar_s, aux_done & 1u, &s_abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                aux_done++;
+            }
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + col_lo);
+            const int npass = pre ? 2 : 1;
+            for (int pass = 0; pass < npass; pass++) {
+                // pass 0 of a GELU tile writes the pre-activation, the last pass the output
+                const bool act = pre && pass == 1, pre_pass = pre && pass == 0;
+                if (!gx) {
+                    if (lane == 0) bulk_wait_read(0);        // the box's last store has read it
+                    __syncwarp();
+                }
+                auto chunk = [&](int k, uint32_t (&r)[16], uint32_t (&rn)[16]) {
+                    const int nc = n0 + k * EC;
+                    tmem_wait16(r);
+                    if (k + 1 < nchunks) {
+                        tmem_ld16_async(taddr + (uint32_t)((k + 1) * EC), rn);
+                    } else if (pass == npass - 1) {
+                        // every column is in registers: the accumulator goes back to the MMA thread
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+                    }
+                    uint64_t x[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        x[j] = f2pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    if (use_bias) {
+                        // the same 16 bias values in every lane (broadcast loads)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            float4 v;
+                            if (nc + 16 <= p.N && p.bias_vec) {
+                                v = __ldg(reinterpret_cast<const float4*>(p.bias + nc) + j);
+                            } else {
+                                const int c0 = nc + 4 * j;
+                                v.x = c0 < p.N ? __ldg(p.bias + c0) : 0.f;
+                                v.y = c0 + 1 < p.N ? __ldg(p.bias + c0 + 1) : 0.f;
+                                v.z = c0 + 2 < p.N ? __ldg(p.bias + c0 + 2) : 0.f;
+                                v.w = c0 + 3 < p.N ? __ldg(p.bias + c0 + 3) : 0.f;
+                            }
+                            x[2 * j] = add2(x[2 * j], f2pack(v.x, v.y));
+                            x[2 * j + 1] = add2(x[2 * j + 1], f2pack(v.z, v.w));
+                        }
+                    }
+                    if (gx) {
+                        // out = acc * gelu'(x), x read from this lane's own row of the box
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(box + sw128(lane, 2 * k + h));
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                                x[4 * h + i] = mul2(x[4 * h + i], gelu_grad2(f2pack(g.x, g.y)));
+                            }
+                        }
+                    }
+                    if (act) {
+#pragma unroll
+                        for (int j = 0; j < 8; j++) x[j] = gelu2(x[j]);
+                    }
+                    if (p.e.colsum && !pre_pass && row0 < p.M) {
+                        // this chunk's column sums over the warp's 32 rows (rows past M count 0)
+                        float cs[16];
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            float a0, a1;
+                            f2unpack(x[j], a0, a1);
+                            cs[2 * j] = row_ok ? a0 : 0.f;
+                            cs[2 * j + 1] = row_ok ? a1 : 0.f;
+                        }
+                        warp_colsum<16>(cs, lane);
+                        const int col = nc + warp_colsum_col<16>(lane);
+                        if (!(lane & 1) && col < p.N) p.e.colsum[(size_t)(row0 >> 5) * p.N + col] = cs[0];
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; h++)
+                        *reinterpret_cast<uint4*>(box + sw128(lane, 2 * k + h)) =
+                            make_uint4(bf16x2(x[4 * h]), bf16x2(x[4 * h + 1]), bf16x2(x[4 * h + 2]),
+                                       bf16x2(x[4 * h + 3]));
+                };
+                uint32_t ra[16], rb[16];
+                if (nchunks > 0) {
+                    tmem_ld16_async(taddr, ra);
+                    for (int k = 0; k < nchunks; k += 2) {
+                        chunk(k, ra, rb);
+                        if (k + 1 < nchunks) chunk(k + 1, rb, ra);
+                    }
+                } else if (pass == npass - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    if (nchunks > 0 && row0 < p.M) tma_store_2d(pre_pass ? &tmPre : &tmOut, n0, row0, box_s);
+                    bulk_commit();
+                }
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            // the next tile's GELU input, once this tile's store has read the box
+            const long long un = u + u_step;
+            if (gx && lane == 0 && un < p.units) {
+                bulk_wait_read(0);
+                aux_issue(un);
+            }
+        }
+        if (gx && !ok && lane == 0) {
+            // an input load still in flight lands in this CTA's shared memory: wait
+            // (bounded, ignoring the abort flag) for it before leaving
+            for (uint32_t g = aux_done; g != aux_issued; g++) {
+                uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(aux_bar_s, g & 1u) && globaltimer() - t0 < WAIT_NS) {
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2 ..)
+        // ------------------------------------------------ epilogue, fp32 outputs on CTA pairs and
+        // every single-CTA product (warps 2 ..)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int ew = warp - 2;
         constexpr int WCOLS = BN / Epi<PAIR>::PER_QUARTER;   // this warp's share of the tile's columns
@@ -622,18 +855,10 @@ static bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int cols, int
     return r == CUDA_SUCCESS;
 }
 
-// MN-major operand tiles are boxes of 128 bytes of MN x BK k-rows, side by side
-// along MN.  Descriptor: LBO = stride between MN boxes, SBO = stride between the
-// k-row groups of the swizzle atom.
-//   tf32: 128-byte swizzle of 32-byte chunks (UMMA layout 1, TMA ATOM_32B), 4-row
-//         groups: LBO 4096, SBO 512 (the layout the tensor core reads tf32
-//         MN-major operands in; with the 16-byte-chunk swizzle it returns zeros).
-//   bf16: 128-byte swizzle of 16-byte chunks (UMMA layout 2, TMA 128B), 8-row
-//         groups: LBO 8192, SBO 1024.
 // 3-D fp32 tensor map [z][rows][cols] (plain, contiguous slices) with box
 // {box_cols, box_rows, 1}: the split-K partial slices, clipped per slice.
 static bool make_map_3d(CUtensorMap* map, const float* ptr, int cols, int rows, int depth, int box_cols,
-                        int box_rows) {
+                        int box_rows, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)depth};
@@ -641,7 +866,7 @@ static bool make_map_3d(CUtensorMap* map, const float* ptr, int cols, int rows, 
     cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -672,11 +897,25 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     ok = ok && (g.b_kmajor ? make_map(&mp->b, g.B, BF16, g.K, g.N, g.ldb, E::BK, S::B_ROWS, KSW)
                            : make_map(&mp->b, g.B, BF16, g.N, g.K, g.ldb, E::MN_BOX, E::BK, MSW));
     Params p{};
-    // epilogue maps, boxes of 32 rows x EC columns: fp32 64-byte rows (64-byte
-    // swizzle) or bf16 32-byte rows (32-byte swizzle)
+    // epilogue maps.  bf16 outputs on CTA pairs: boxes of 32 rows x 64 columns
+    // (128-byte rows, 128-byte swizzle); everything else: boxes of 32 rows x EC
+    // columns, fp32 64-byte rows (64-byte swizzle) or bf16 32-byte rows (32-byte
+    // swizzle)
     auto swz = [](bool b16) { return b16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B; };
-    if (partial) {
-        ok = ok && make_map_3d(&mp->out, partial, g.N, g.M, split, EC, 32);
+    if (PAIR && !partial && e.out_bf16 && !e.residual) {
+        const CUtensorMapSwizzle W = CU_TENSOR_MAP_SWIZZLE_128B;
+        ok = ok && make_map(&mp->out, e.out, true, g.N, g.M, e.ldo, 64, 32, W);
+        if (e.gelu_x) {
+            ok = ok && make_map(&mp->aux, e.gelu_x, true, g.N, g.M, e.ldg, 64, 32, W);
+            p.has_aux = 1;
+            p.aux_bf16 = 1;
+        }
+        if (e.gelu) {
+            ok = ok && make_map(&mp->pre, e.out_pre, true, g.N, g.M, e.ldo, 64, 32, W);
+            p.pre_bf16 = 1;
+        }
+    } else if (partial) {
+        ok = ok && make_map_3d(&mp->out, partial, g.N, g.M, split, EC, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     } else {
         ok = ok && make_map(&mp->out, e.out, e.out_bf16, g.N, g.M, e.ldo, EC, 32, swz(e.out_bf16));
         if (e.residual) {
@@ -716,6 +955,7 @@ static int prepare(const GemmProblem& g, const GemmEpilogue& e, float* partial, 
     p.gelu = partial ? 0 : e.gelu;
     p.out_bf16 = partial ? 0 : e.out_bf16;
     p.bias = partial ? nullptr : e.bias;
+    p.bias_vec = p.bias && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     *pp = p;
     return GPT2_OK;
 }
@@ -811,7 +1051,11 @@ bool gemm_tc_pair(const GemmProblem& g, const GemmEpilogue* e) {
         on = (v && v[0] == '0') ? 0 : 1;
     }
     if (!on || !g.bf16 || g.M < 256 || g.N < 256 || tc::pair_clusters() <= 0) return false;
-    (void)e;
+    // a bf16 output with GELU takes a bf16 pre-activation and a bf16 GELU input
+    // on pairs (both go through the output's box)
+    if (e && e->out_bf16 && !e->residual &&
+        ((e->gelu && (!e->pre_bf16 || e->gelu_x)) || (e->gelu_x && !e->gelu_x_bf16)))
+        return false;
     return true;
 }
 
