@@ -6,12 +6,15 @@
 // Backward: dwte[v,:] += sum_{pos: tok[pos]=v} dx[pos,:] and dwpe[t,:] =
 // sum_b dx[b,t,:].  The token-side scatter-add is made deterministic without
 // float atomics: positions are bucketed by token id with an integer counting
-// sort and each bucket is put in ascending position order.  The sorted list is
-// then cut into fixed segments of 64 entries, one thread block each: a bucket
-// that lies inside one segment is summed and added to dwte there; a bucket
-// that crosses segment boundaries leaves one partial sum per segment, and a
-// fix-up pass adds those in segment order.  A frequent token (a Zipf stream
-// gives the top id ~14% of positions) is thus spread over many blocks.
+// sort (histogram, a two-pass scan, fill) and each bucket is put in ascending
+// position order: small buckets by counting, per position, the bucket entries
+// below it; buckets of more than ENC_BIG entries by a bitmap of positions in
+// shared memory, one block each.  The sorted list is then cut into fixed
+// segments of ENC_SEG entries, one thread block each: a bucket that lies inside
+// one segment is summed and added to dwte there; a bucket that crosses segment
+// boundaries leaves one partial sum per segment, and a fix-up pass adds those
+// in a fixed order.  A frequent token (a Zipf stream gives the top id ~14% of
+// positions) is thus spread over many blocks.
 #include "common.cuh"
 
 namespace gpt2k {
@@ -44,35 +47,89 @@ __global__ void enc_histogram_kernel(int* __restrict__ count, const int* __restr
     if (id >= 0 && id < V) atomicAdd(&count[id], 1);
 }
 
-// One block: exclusive scan of count[0..V) into offset[], and the list of
-// distinct ids present (in increasing id order) into uniq[]; *n_uniq its length.
-__global__ void enc_scan_kernel(int* __restrict__ offset, int* __restrict__ uniq,
-                                int* __restrict__ n_uniq, const int* __restrict__ count, int V) {
-    __shared__ int s_sum[1024], s_nz[1024];
-    int tid = threadIdx.x, nt = blockDim.x;
-    int per = (V + nt - 1) / nt;
-    int lo = min(V, tid * per), hi = min(V, lo + per);
-    int sum = 0, nz = 0;
-    for (int v = lo; v < hi; v++) { sum += count[v]; nz += count[v] > 0; }
-    s_sum[tid] = sum;
-    s_nz[tid] = nz;
+constexpr int ENC_BIG = 256;           // buckets above this size are ordered by a bitmap
+constexpr int ENC_SCAN_BLOCK = 1024;   // ids per block of the scan
+constexpr int ENC_BITMAP_MAX_BT = 1 << 20;   // positions a shared-memory bitmap covers (128 KB)
+
+// Exclusive scan of one value per thread over the block (at most 32 warps):
+// warp shuffles, then the warp totals; returns the block total in `total`.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) s_warp[warp] = inc;
     __syncthreads();
-    // Hillis-Steele inclusive scan over the per-thread totals
-    for (int o = 1; o < nt; o <<= 1) {
-        int a = tid >= o ? s_sum[tid - o] : 0;
-        int b = tid >= o ? s_nz[tid - o] : 0;
-        __syncthreads();
-        s_sum[tid] += a;
-        s_nz[tid] += b;
-        __syncthreads();
+    if (warp == 0) {
+        const int w = lane < nwarps ? s_warp[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        if (lane < nwarps) s_warp[lane] = wi - w;     // exclusive prefix of the warp totals
+        if (lane == 31) s_warp[32] = wi;
     }
-    int run = s_sum[tid] - sum, runu = s_nz[tid] - nz;
-    for (int v = lo; v < hi; v++) {
-        offset[v] = run;
-        run += count[v];
-        if (count[v] > 0) uniq[runu++] = v;
+    __syncthreads();
+    const int r = s_warp[warp] + inc - v;
+    total = s_warp[32];
+    __syncthreads();                         // s_warp is reused by the next call
+    return r;
+}
+
+// The scan of count[0..V) in two passes over blocks of ENC_SCAN_BLOCK ids.
+// Pass 1: per block, the number of positions and of ids with more than
+// ENC_BIG positions.
+__global__ void __launch_bounds__(ENC_SCAN_BLOCK) enc_scan_sums_kernel(int* __restrict__ sums,
+                                                                      const int* __restrict__ count, int V) {
+    __shared__ int s_warp[33];
+    const int v = blockIdx.x * ENC_SCAN_BLOCK + threadIdx.x;
+    const int c = v < V ? count[v] : 0;
+    int tot, totb;
+    block_exclusive_scan(c, s_warp, tot);
+    block_exclusive_scan(c > ENC_BIG ? 1 : 0, s_warp, totb);
+    if (threadIdx.x == 0) {
+        sums[2 * blockIdx.x] = tot;
+        sums[2 * blockIdx.x + 1] = totb;
     }
-    if (tid == nt - 1) { offset[V] = s_sum[tid]; *n_uniq = s_nz[tid]; }
+}
+
+// Pass 2: each block adds the sums of the blocks before it, then writes
+// offset[] (exclusive scan of count; offset[V] = the total) and the ids with
+// more than ENC_BIG positions, in increasing order, into big[] (*n_big).
+__global__ void __launch_bounds__(ENC_SCAN_BLOCK) enc_scan_kernel(int* __restrict__ offset, int* __restrict__ big,
+                                                                 int* __restrict__ n_big,
+                                                                 const int* __restrict__ count,
+                                                                 const int* __restrict__ sums, int V) {
+    __shared__ int s_warp[33], s_pre[2];
+    if (threadIdx.x < 32) {                   // warp 0: the two sums over the blocks before this one
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            int a = 0;
+            for (int k = threadIdx.x; k < (int)blockIdx.x; k += 32) a += sums[2 * k + q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (threadIdx.x == 0) s_pre[q] = a;
+        }
+    }
+    const int v = blockIdx.x * ENC_SCAN_BLOCK + threadIdx.x;
+    const int c = v < V ? count[v] : 0;
+    int tot, totb;
+    const int ex = block_exclusive_scan(c, s_warp, tot);          // its barriers also publish s_pre
+    const int exb = block_exclusive_scan(c > ENC_BIG ? 1 : 0, s_warp, totb);
+    const int run = s_pre[0], runb = s_pre[1];
+    if (v < V) {
+        offset[v] = run + ex;
+        if (c > ENC_BIG) big[runb + exb] = v;
+    }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+        offset[V] = run + tot;
+        *n_big = runb + totb;
+    }
 }
 
 __global__ void enc_fill_kernel(int* __restrict__ list, int* __restrict__ cursor,
@@ -89,18 +146,62 @@ __global__ void enc_fill_kernel(int* __restrict__ list, int* __restrict__ cursor
 // is the number of bucket entries smaller than it (positions are distinct).
 __global__ void enc_rank_kernel(int* __restrict__ sorted, const int* __restrict__ list,
                                 const int* __restrict__ offset, const int* __restrict__ tok, int BT,
-                                int V) {
+                                int V, int skip_big) {
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= BT) return;
     int id = tok[i];
     if (id < 0 || id >= V) return;
     int lo = offset[id], hi = offset[id + 1];
+    if (skip_big && hi - lo > ENC_BIG) return;     // enc_sort_big_kernel orders this bucket
     int r = 0;
     for (int e = lo; e < hi; e++) r += list[e] < i;
     sorted[lo + r] = i;
 }
 
-constexpr int ENC_SEG = 64;
+// Buckets of more than ENC_BIG entries: one block per bucket (grid-strided over
+// big[]) marks the bucket's positions (distinct, below BT) in a shared-memory
+// bitmap of BT bits, then each thread takes a run of consecutive words, counts
+// their bits, and after an exclusive scan of the counts writes its positions
+// in ascending order to sorted[].
+__global__ void __launch_bounds__(512) enc_sort_big_kernel(int* __restrict__ sorted, const int* __restrict__ list,
+                                                          const int* __restrict__ offset,
+                                                          const int* __restrict__ big,
+                                                          const int* __restrict__ n_big, int BT) {
+    extern __shared__ uint32_t s_bits[];
+    __shared__ int s_warp[33];
+    const int nw = (BT + 31) >> 5;
+    const int wpt = (nw + blockDim.x - 1) / blockDim.x;      // words per thread
+    const int w0 = min(nw, (int)threadIdx.x * wpt), w1 = min(nw, w0 + wpt);
+    const int nb = *n_big;
+    for (int k = blockIdx.x; k < nb; k += gridDim.x) {
+        const int v = big[k];
+        const int lo = offset[v], n = offset[v + 1] - lo;
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) s_bits[i] = 0u;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int pos = list[lo + i];
+            atomicOr(&s_bits[pos >> 5], 1u << (pos & 31));
+        }
+        __syncthreads();
+        int cnt = 0;
+        for (int w = w0; w < w1; w++) cnt += __popc(s_bits[w]);
+        int tot;
+        int at = lo + block_exclusive_scan(cnt, s_warp, tot);
+        for (int w = w0; w < w1; w++) {
+            uint32_t bits = s_bits[w];
+            while (bits) {
+                const int bpos = __ffs(bits) - 1;
+                sorted[at++] = 32 * w + bpos;
+                bits &= bits - 1;
+            }
+        }
+        __syncthreads();                          // the bitmap is cleared for the next bucket
+    }
+}
+
+constexpr int ENC_SEG = 16;
+constexpr int ENC_FIX = 4;             // partial sums per fix-up thread loaded together ...
+constexpr int ENC_FIX_Y = 4;           // ... by each of this many threads per column
 constexpr int ENC_PF = 8;              // gradient rows loaded together in the segment kernel
 
 // One block per segment of the sorted list.  All threads walk the segment's
@@ -155,26 +256,61 @@ __global__ void enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict
     }
 }
 
-// Buckets that cross segments: add their per-segment partials in segment order.
+// Buckets that cross segments.  Block b looks at the boundary after segment b
+// and takes the bucket that crosses it if that is the bucket's first boundary;
+// it adds the bucket's per-segment partial sums into dwte.  Thread (x, y)
+// takes column float4s x, x + blockDim.x, ... and segments s0 + y, s0 + y +
+// ENC_FIX_Y, ..., with ENC_FIX interleaved running sums so that their loads are
+// in flight together; the sums are added in a fixed order (k, then y through
+// shared memory), so the result does not depend on timing.
 __global__ void enc_fixup_kernel(float4* __restrict__ dwte, const float4* __restrict__ part,
-                                 const int* __restrict__ offset, const int* __restrict__ uniq,
-                                 const int* __restrict__ n_uniq, int C4) {
-    const int u = blockIdx.x;
-    if (u >= *n_uniq) return;
-    const int v = uniq[u];
+                                 const int* __restrict__ sorted, const int* __restrict__ offset,
+                                 const int* __restrict__ tok, int V, int C4) {
+    __shared__ float4 s_acc[ENC_FIX_Y][256];
+    const int bnd = blockIdx.x, e = (bnd + 1) * ENC_SEG;     // first entry after the boundary
+    if (e >= offset[V]) return;
+    const int v = tok[sorted[e]];
+    if (tok[sorted[e - 1]] != v) return;                      // no bucket crosses here
     const int lo = offset[v], hi = offset[v + 1];
     const int s0 = lo / ENC_SEG, s1 = (hi - 1) / ENC_SEG;
-    if (s0 == s1) return;
-    for (int c = threadIdx.x; c < C4; c += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sg = s0; sg <= s1; sg++) {
-            const int slot = (sg == s0 && lo != sg * ENC_SEG) ? 1 : 0;
-            const float4 p = part[((size_t)sg * 2 + slot) * C4 + c];
-            acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    if (s0 != bnd) return;                                    // not the bucket's first boundary
+    const int y = threadIdx.y;
+    for (int c0 = 0; c0 < C4; c0 += blockDim.x) {
+        const int c = c0 + threadIdx.x;
+        float4 a[ENC_FIX];
+#pragma unroll
+        for (int k = 0; k < ENC_FIX; k++) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < C4) {
+            for (int sg0 = s0 + y; sg0 <= s1; sg0 += ENC_FIX * ENC_FIX_Y) {
+#pragma unroll
+                for (int k = 0; k < ENC_FIX; k++) {
+                    const int sg = sg0 + k * ENC_FIX_Y;
+                    if (sg <= s1) {
+                        const int slot = (sg == s0 && lo != sg * ENC_SEG) ? 1 : 0;
+                        const float4 p = part[((size_t)sg * 2 + slot) * C4 + c];
+                        a[k].x += p.x; a[k].y += p.y; a[k].z += p.z; a[k].w += p.w;
+                    }
+                }
+            }
         }
-        float4 d = dwte[(size_t)v * C4 + c];
-        d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
-        dwte[(size_t)v * C4 + c] = d;
+        float4 acc = a[0];
+#pragma unroll
+        for (int k = 1; k < ENC_FIX; k++) {
+            acc.x += a[k].x; acc.y += a[k].y; acc.z += a[k].z; acc.w += a[k].w;
+        }
+        s_acc[y][threadIdx.x] = acc;
+        __syncthreads();
+        if (y == 0 && c < C4) {
+#pragma unroll
+            for (int j = 1; j < ENC_FIX_Y; j++) {
+                const float4 t = s_acc[j][threadIdx.x];
+                acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+            }
+            float4 d = dwte[(size_t)v * C4 + c];
+            d.x += acc.x; d.y += acc.y; d.z += acc.z; d.w += acc.w;
+            dwte[(size_t)v * C4 + c] = d;
+        }
+        __syncthreads();
     }
 }
 
@@ -194,7 +330,7 @@ __global__ void enc_dwpe_kernel(float4* __restrict__ dwpe, const float4* __restr
 }
 
 struct EncScratch {
-    int *count, *cursor, *offset, *uniq, *n_uniq, *list, *sorted;
+    int *count, *cursor, *offset, *sums, *big, *n_big, *list, *sorted;
     float* part;
 };
 
@@ -209,8 +345,9 @@ static size_t enc_layout(int BT, int V, int C, char* base, EncScratch* s) {
     t.count = take(V);
     t.cursor = take(V);
     t.offset = take((size_t)V + 1);
-    t.uniq = take(BT);
-    t.n_uniq = take(1);
+    t.sums = take(2 * (size_t)ceil_div(V, ENC_SCAN_BLOCK));
+    t.big = take(BT / ENC_BIG + 1);
+    t.n_big = take(1);
     t.list = take(BT);
     t.sorted = take(BT);
     const size_t nseg = (size_t)ceil_div(BT, ENC_SEG);
@@ -256,16 +393,26 @@ GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx,
     GPT2_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * V, st));
     int nb = ceil_div(BT, 256);
     count_launch(), enc_histogram_kernel<<<nb, 256, 0, st>>>(s.count, tok, BT, V);
-    count_launch(), enc_scan_kernel<<<1, 1024, 0, st>>>(s.offset, s.uniq, s.n_uniq, s.count, V);
+    const int nsb = ceil_div(V, ENC_SCAN_BLOCK);
+    count_launch(), enc_scan_sums_kernel<<<nsb, ENC_SCAN_BLOCK, 0, st>>>(s.sums, s.count, V);
+    count_launch(), enc_scan_kernel<<<nsb, ENC_SCAN_BLOCK, 0, st>>>(s.offset, s.big, s.n_big, s.count, s.sums, V);
     count_launch(), enc_fill_kernel<<<nb, 256, 0, st>>>(s.list, s.cursor, s.offset, tok, BT, V);
-    count_launch(), enc_rank_kernel<<<nb, 256, 0, st>>>(s.sorted, s.list, s.offset, tok, BT, V);
+    const bool bitmap = BT > ENC_BIG && BT <= ENC_BITMAP_MAX_BT;
+    count_launch(), enc_rank_kernel<<<nb, 256, 0, st>>>(s.sorted, s.list, s.offset, tok, BT, V, bitmap ? 1 : 0);
+    if (bitmap) {
+        const int smem = ceil_div(BT, 32) * (int)sizeof(uint32_t);
+        if (smem_limit(reinterpret_cast<const void*>(enc_sort_big_kernel), smem)) return GPT2_ECUDA;
+        count_launch(), enc_sort_big_kernel<<<std::min(BT / ENC_BIG, 2 * num_sms()), 512, smem, st>>>(
+            s.sorted, s.list, s.offset, s.big, s.n_big, BT);
+    }
     const int threads = C4 < 256 ? ((C4 + 31) / 32) * 32 : 256;
     count_launch(), enc_segment_kernel<<<ceil_div(BT, ENC_SEG), threads, 0, st>>>(
         reinterpret_cast<float4*>(dwte), reinterpret_cast<float4*>(s.part),
         reinterpret_cast<const float4*>(dx), s.sorted, s.offset, tok, V, C4);
-    count_launch(), enc_fixup_kernel<<<min(BT, V), threads, 0, st>>>(
-        reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(s.part), s.offset, s.uniq,
-        s.n_uniq, C4);
+    if (BT > ENC_SEG)
+        count_launch(), enc_fixup_kernel<<<ceil_div(BT, ENC_SEG) - 1, dim3(threads, ENC_FIX_Y), 0, st>>>(
+            reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(s.part), s.sorted, s.offset, tok, V,
+            C4);
     long long n = (long long)maxT * C4;
     count_launch(), enc_dwpe_kernel<<<ceil_div(n, 256), 256, 0, st>>>(reinterpret_cast<float4*>(dwpe),
                                                      reinterpret_cast<const float4*>(dx), B, T,

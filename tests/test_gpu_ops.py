@@ -8,6 +8,8 @@ import pytest
 
 from gpu_util import rel_l2
 
+from gpt_decoder_step_train_b300 import synthetic as syn
+
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
@@ -92,12 +94,18 @@ def test_encoder_forward_flags_bad_token(L, B_):
     assert np.all(host(x)[2:] == 0)
 
 
-@pytest.mark.parametrize("zipf", [False, True])
-def test_encoder_backward_matches_and_is_deterministic(L, B_, o64, zipf):
+@pytest.mark.parametrize("kind", ["uniform", "zipf", "one_id", "zipf_full"])
+def test_encoder_backward_matches_and_is_deterministic(L, B_, o64, kind):
     rng = np.random.default_rng(1)
     V, maxT, C, B, T = 5000, 200, 64, 4, 199
-    if zipf:   # heavy repetition of a few ids, like the training token stream
+    if kind == "zipf":         # heavy repetition of a few ids, like the training token stream
         tok = np.minimum(rng.zipf(1.3, (B, T)) - 1, V - 1).astype(np.int32)
+    elif kind == "one_id":     # one bucket of 2048 entries: the shared-memory sort of large buckets
+        V, maxT, B, T = 50, 1024, 2, 1024
+        tok = np.full((B, T), 7, dtype=np.int32)
+    elif kind == "zipf_full":  # the GPT-2 124M B16 T1024 shape: several buckets above 256 entries
+        V, maxT, C, B, T = 50257, 1024, 768, 16, 1024
+        tok = syn.draw_tokens(syn.CONFIGS["124M"])[0]
     else:
         tok = rng.integers(0, V, (B, T)).astype(np.int32)
     dx = rng.normal(size=(B * T, C)).astype(np.float32)
