@@ -42,8 +42,8 @@ int num_sms();
 // Count one kernel launch (process-wide total, read by gpt2_kernel_launches).
 void count_launch();
 
-// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
-// device, once per (kernel, device, bytes); thread-safe.  GPT2_OK or GPT2_ECUDA.
+// Raise a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes` (never lowers it); thread-safe.  GPT2_OK or GPT2_ECUDA.
 int smem_limit(const void* kernel, int bytes);
 
 // tanh-form GELU and its derivative, fp32.  s = sqrt(2/pi).

@@ -207,7 +207,7 @@ constexpr int ENC_PF = 8;              // gradient rows loaded together in the s
 // One block per segment of the sorted list.  All threads walk the segment's
 // entries in order (same token sequence from shared memory), each thread for
 // its own float4 columns, and flush the running sum at every token change.
-__global__ void enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict__ part,
+__global__ void __launch_bounds__(256) enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict__ part,
                                    const float4* __restrict__ dx, const int* __restrict__ sorted,
                                    const int* __restrict__ offset, const int* __restrict__ tok, int V,
                                    int C4) {
@@ -263,7 +263,7 @@ __global__ void enc_segment_kernel(float4* __restrict__ dwte, float4* __restrict
 // ENC_FIX_Y, ..., with ENC_FIX interleaved running sums so that their loads are
 // in flight together; the sums are added in a fixed order (k, then y through
 // shared memory), so the result does not depend on timing.
-__global__ void enc_fixup_kernel(float4* __restrict__ dwte, const float4* __restrict__ part,
+__global__ void __launch_bounds__(1024) enc_fixup_kernel(float4* __restrict__ dwte, const float4* __restrict__ part,
                                  const int* __restrict__ sorted, const int* __restrict__ offset,
                                  const int* __restrict__ tok, int V, int C4) {
     __shared__ float4 s_acc[ENC_FIX_Y][256];
@@ -391,28 +391,39 @@ GPT2_API int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dx,
     enc_layout(BT, V, C, reinterpret_cast<char*>(scratch), &s);
     GPT2_CUDA_TRY(cudaMemsetAsync(s.count, 0, sizeof(int) * V, st));
     GPT2_CUDA_TRY(cudaMemsetAsync(s.cursor, 0, sizeof(int) * V, st));
+    // every launch is checked at once: a launch that fails must not leave the
+    // kernels after it reading positions it did not write
     int nb = ceil_div(BT, 256);
     count_launch(), enc_histogram_kernel<<<nb, 256, 0, st>>>(s.count, tok, BT, V);
+    GPT2_LAUNCH_CHECK();
     const int nsb = ceil_div(V, ENC_SCAN_BLOCK);
     count_launch(), enc_scan_sums_kernel<<<nsb, ENC_SCAN_BLOCK, 0, st>>>(s.sums, s.count, V);
+    GPT2_LAUNCH_CHECK();
     count_launch(), enc_scan_kernel<<<nsb, ENC_SCAN_BLOCK, 0, st>>>(s.offset, s.big, s.n_big, s.count, s.sums, V);
+    GPT2_LAUNCH_CHECK();
     count_launch(), enc_fill_kernel<<<nb, 256, 0, st>>>(s.list, s.cursor, s.offset, tok, BT, V);
+    GPT2_LAUNCH_CHECK();
     const bool bitmap = BT > ENC_BIG && BT <= ENC_BITMAP_MAX_BT;
     count_launch(), enc_rank_kernel<<<nb, 256, 0, st>>>(s.sorted, s.list, s.offset, tok, BT, V, bitmap ? 1 : 0);
+    GPT2_LAUNCH_CHECK();
     if (bitmap) {
         const int smem = ceil_div(BT, 32) * (int)sizeof(uint32_t);
         if (smem_limit(reinterpret_cast<const void*>(enc_sort_big_kernel), smem)) return GPT2_ECUDA;
         count_launch(), enc_sort_big_kernel<<<std::min(BT / ENC_BIG, 2 * num_sms()), 512, smem, st>>>(
             s.sorted, s.list, s.offset, s.big, s.n_big, BT);
+        GPT2_LAUNCH_CHECK();
     }
     const int threads = C4 < 256 ? ((C4 + 31) / 32) * 32 : 256;
     count_launch(), enc_segment_kernel<<<ceil_div(BT, ENC_SEG), threads, 0, st>>>(
         reinterpret_cast<float4*>(dwte), reinterpret_cast<float4*>(s.part),
         reinterpret_cast<const float4*>(dx), s.sorted, s.offset, tok, V, C4);
-    if (BT > ENC_SEG)
+    GPT2_LAUNCH_CHECK();
+    if (BT > ENC_SEG) {
         count_launch(), enc_fixup_kernel<<<ceil_div(BT, ENC_SEG) - 1, dim3(threads, ENC_FIX_Y), 0, st>>>(
             reinterpret_cast<float4*>(dwte), reinterpret_cast<const float4*>(s.part), s.sorted, s.offset, tok, V,
             C4);
+        GPT2_LAUNCH_CHECK();
+    }
     long long n = (long long)maxT * C4;
     count_launch(), enc_dwpe_kernel<<<ceil_div(n, 256), 256, 0, st>>>(reinterpret_cast<float4*>(dwpe),
                                                      reinterpret_cast<const float4*>(dx), B, T,

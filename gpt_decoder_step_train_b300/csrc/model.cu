@@ -50,13 +50,19 @@ int smem_limit(const void* kernel, int bytes) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return GPT2_ECUDA; }
     std::lock_guard<std::mutex> lock(mu);
-    for (const Done& d : done)
-        if (d.k == kernel && d.dev == dev && d.bytes == bytes) return GPT2_OK;
+    // the attribute only grows: a launch with fewer bytes than the recorded
+    // limit needs no call, and lowering it would break a later larger launch
+    // that an earlier call already cleared
+    Done* rec = nullptr;
+    for (Done& d : done)
+        if (d.k == kernel && d.dev == dev) rec = &d;
+    if (rec && rec->bytes >= bytes) return GPT2_OK;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return GPT2_ECUDA;
     }
-    done.push_back(Done{kernel, dev, bytes});
+    if (rec) rec->bytes = bytes;
+    else done.push_back(Done{kernel, dev, bytes});
     return GPT2_OK;
 }
 

@@ -128,6 +128,30 @@ def test_encoder_backward_matches_and_is_deterministic(L, B_, o64, kind):
     assert np.all(outs[0][1][T:] == 0)
 
 
+def test_encoder_backward_sizes_up_down_up(L, B_, o64):
+    """The same process runs the encoder backward on 16 x 1024 positions, then
+    1 x 1024, then 16 x 1024 again (the bitmap kernel's shared memory shrinks
+    and grows back), each against the oracle: a kernel's shared-memory limit
+    must never be left below a size that an earlier call already set up."""
+    V, maxT, C = 50257, 1024, 768
+    tok_full = syn.draw_tokens(syn.CONFIGS["124M"])[0]
+    rng = np.random.default_rng(3)
+    for B in (16, 1, 16):
+        tok = np.ascontiguousarray(tok_full[:B])
+        T = tok.shape[1]
+        dx = rng.normal(size=(B * T, C)).astype(np.float32)
+        nbytes = L.gpt2_op_encoder_backward_scratch_bytes(B * T, V, C)
+        dwte = torch.zeros(V, C, device="cuda")
+        dwpe = torch.zeros(maxT, C, device="cuda")
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        rc = L.gpt2_op_encoder_backward(B_.ptr(dwte), B_.ptr(dwpe), B_.ptr(dev(dx)), B_.ptr(dev(tok)), B, T,
+                                        maxT, C, V, B_.ptr(scratch), nbytes, None)
+        assert rc == 0
+        w_dwte, w_dwpe = o64.encoder_backward(dx.reshape(B, T, C), tok, V, maxT)
+        assert rel_l2(host(dwte), w_dwte) < 1e-6
+        assert rel_l2(host(dwpe), w_dwpe) < 1e-6
+
+
 # ------------------------------------------------------------------ layernorm
 
 @pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600), (5, 4)])
