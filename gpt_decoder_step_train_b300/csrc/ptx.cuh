@@ -91,39 +91,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// try_wait whose suspension is limited to about `ns` nanoseconds
-__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-// The same bounded wait with short suspensions (about 20 ns each): for a lone
-// issuing thread whose reaction time matters (a try_wait left to the default
-// limit can resume well after the phase flips), without a busy loop taking
-// issue slots from the warps that share its scheduler.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               int* status) {
-    if (mbar_try_wait_ns(bar, parity, 20)) return true;
-    uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; i++) {
-        if (mbar_try_wait_ns(bar, parity, 20)) return true;
-        if ((i & 255) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_NS) {
-                *abort_flag = 1;
-                set_status(status, GPT2_STATUS_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
