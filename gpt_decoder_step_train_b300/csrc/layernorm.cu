@@ -377,6 +377,92 @@ __global__ void ln_bwd_reduce_kernel(float* __restrict__ dw, float* __restrict__
     }
 }
 
+// The same register streaming for rows of up to 2048 columns (V4 float4 per
+// lane, V4 > 6): the row's x, dy and incoming dx stay in registers, but the
+// column sums go to the warp's own [3][C] region of shared memory after every
+// row (each lane updates its own columns, so no two lanes touch one word), which
+// leaves the registers to the row itself; LNR_WIDE_WARPS warps per block.  The
+// block then adds its warps' regions in warp order, as above.  No dropout.
+constexpr int LNR_WIDE_WARPS = 8;
+
+template <int V4>
+__global__ void __launch_bounds__(LNR_WIDE_WARPS * 32, 1)
+ln_bwd_rows_wide_kernel(float* __restrict__ dx, __nv_bfloat16* __restrict__ dx16, float* __restrict__ partial,
+                        const float* __restrict__ dy, const float* __restrict__ x, const float* __restrict__ w,
+                        const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C, int rpb,
+                        int accumulate) {
+    extern __shared__ __align__(16) float red[];       // [LNR_WIDE_WARPS][3][C]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C4 = C >> 2;
+    const int r0 = blockIdx.x * rpb, r1 = min(N, r0 + rpb);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float4* acc = reinterpret_cast<float4*>(red + (size_t)warp * 3 * C);   // this warp's sums
+    for (int c = lane; c < 3 * C4; c += 32) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float inv_c = 1.f / (float)C;
+    for (int row = r0 + warp; row < r1; row += LNR_WIDE_WARPS) {
+        const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * C);
+        const float4* gr = reinterpret_cast<const float4*>(dy + (size_t)row * C);
+        float4* dr = reinterpret_cast<float4*>(dx + (size_t)row * C);
+        float4 xv[V4], gv[V4], ov[V4];
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            const bool in = c < C4;
+            xv[k] = in ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[k] = in ? __ldcs(gr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ov[k] = in && accumulate ? __ldcs(dr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float mu = __ldg(mean + row), rs = __ldg(rstd + row);
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            if (c < C4) {
+                const float4 ww = __ldg(w4 + c);
+                const float gx = gv[k].x * ww.x, gy = gv[k].y * ww.y, gz = gv[k].z * ww.z, gw = gv[k].w * ww.w;
+                xv[k].x = (xv[k].x - mu) * rs; xv[k].y = (xv[k].y - mu) * rs;
+                xv[k].z = (xv[k].z - mu) * rs; xv[k].w = (xv[k].w - mu) * rs;
+                sg += (gx + gy) + (gz + gw);
+                sgx += (gx * xv[k].x + gy * xv[k].y) + (gz * xv[k].z + gw * xv[k].w);
+            }
+        }
+        const float mg = warp_sum(sg) * inv_c, mgx = warp_sum(sgx) * inv_c;
+#pragma unroll
+        for (int k = 0; k < V4; k++) {
+            const int c = lane + 32 * k;
+            if (c < C4) {
+                const float4 ww = __ldg(w4 + c);
+                float4 o = ov[k];
+                o.x += rs * (gv[k].x * ww.x - mg - xv[k].x * mgx);
+                o.y += rs * (gv[k].y * ww.y - mg - xv[k].y * mgx);
+                o.z += rs * (gv[k].z * ww.z - mg - xv[k].z * mgx);
+                o.w += rs * (gv[k].w * ww.w - mg - xv[k].w * mgx);
+                dr[c] = o;
+                if (dx16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                    reinterpret_cast<uint2*>(dx16 + (size_t)row * C)[c] =
+                        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                }
+                float4 a = acc[c], b = acc[C4 + c], d = acc[2 * C4 + c];
+                a.x += gv[k].x * xv[k].x; a.y += gv[k].y * xv[k].y;
+                a.z += gv[k].z * xv[k].z; a.w += gv[k].w * xv[k].w;
+                b.x += gv[k].x; b.y += gv[k].y; b.z += gv[k].z; b.w += gv[k].w;
+                d.x += o.x; d.y += o.y; d.z += o.z; d.w += o.w;
+                acc[c] = a;
+                acc[C4 + c] = b;
+                acc[2 * C4 + c] = d;
+            }
+        }
+    }
+    __syncthreads();
+    float* out = partial + (size_t)blockIdx.x * 3 * C;
+    for (int i = threadIdx.x; i < 3 * C; i += LNR_WIDE_WARPS * 32) {
+        float t = red[i];
+        for (int k = 1; k < LNR_WIDE_WARPS; k++) t += red[(size_t)k * 3 * C + i];
+        out[i] = t;
+    }
+}
+
 }  // namespace gpt2k
 
 using namespace gpt2k;
@@ -480,6 +566,24 @@ int layernorm_backward(float* dx, void* dxo, bool dxo_bf16, float* dw, float* db
             else LNR(6, false);
         }
 #undef LNR
+    } else if (!bits && v4 <= 16) {
+        // rows of up to 2048 columns: register streaming with the column sums in shared memory
+        nblk = std::min({num_sms(), LNB_MAX_BLOCKS, N});
+        const int rpb = ceil_div(N, nblk);
+        nblk = ceil_div(N, rpb);
+        const size_t wsm = (size_t)LNR_WIDE_WARPS * 3 * C * sizeof(float);
+#define LNW(V4)                                                                                      \
+    do {                                                                                             \
+        if (smem_limit(reinterpret_cast<const void*>(ln_bwd_rows_wide_kernel<V4>),                   \
+                       (int)((size_t)LNR_WIDE_WARPS * 3 * 128 * V4 * sizeof(float))))                \
+            return GPT2_ECUDA;                                                                       \
+        count_launch(), ln_bwd_rows_wide_kernel<V4><<<nblk, LNR_WIDE_WARPS * 32, wsm, st>>>(        \
+            dx, dx16, partial, dy, x, w, mean, rstd, N, C, rpb, accumulate ? 1 : 0);                 \
+    } while (0)
+        if (v4 <= 8) LNW(8);
+        else if (v4 <= 13) LNW(13);
+        else LNW(16);
+#undef LNW
     } else if (cpt <= 1) LNB(1);
     else if (cpt <= 2) LNB(2);
     else if (cpt <= 3) LNB(3);

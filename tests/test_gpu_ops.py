@@ -172,7 +172,7 @@ def test_layernorm_forward(L, B_, o64, N, C):
 
 
 @pytest.mark.parametrize("accumulate", [1, 0])
-@pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600), (16384, 768), (3, 2048)])
+@pytest.mark.parametrize("N,C", [(1000, 768), (37, 64), (513, 1600), (16384, 768), (3, 2048), (300, 1024), (4096, 1600)])
 def test_layernorm_backward(L, B_, o64, N, C, accumulate):
     rng = np.random.default_rng(3)
     x = rng.normal(size=(N, C)).astype(np.float32)
