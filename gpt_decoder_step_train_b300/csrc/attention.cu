@@ -381,6 +381,8 @@ bool attention_tc_supported(int hs);
 bool attention_tc05_supported(int hs, int C);
 int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int* status,
                            cudaStream_t st, const uint32_t* bits, float ks);
+int attention_tc05_tf32_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int H, int* status,
+                                cudaStream_t st);
 int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse,
                                    float* D, int B, int T, int C, int H, int* status, cudaStream_t st,
                                    float* colsum);
@@ -397,9 +399,10 @@ static bool attn_args_ok(int B, int T, int C, int H) {
 // Dispatch: BF16 mode takes the tcgen05 kernels for head size 64, the
 // mma.sync kernels for head sizes 16 and 32 (no dropout), else the CUDA-core
 // kernels on bf16 (head sizes that are multiples of 8: the backward's
-// rowsum(dO o O) reads a head's slice 16 bytes at a time); FP32 and TF32 modes
-// take the mma.sync TF32 kernels where they apply (no dropout), else the
-// CUDA-core kernels on fp32.
+// rowsum(dO o O) reads a head's slice 16 bytes at a time); TF32 mode takes the
+// tcgen05 tf32 forward for head size 64 and the mma.sync TF32 kernels for the
+// other head sizes and the backward (no dropout); otherwise (FP32 mode,
+// dropout) the CUDA-core kernels on fp32.
 int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int mode, int* status,
                       cudaStream_t st, const uint32_t* bits, float p) {
     if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
@@ -415,6 +418,9 @@ int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C,
         GPT2_LAUNCH_CHECK();
         return GPT2_OK;
     }
+    if (mode == GPT2_MODE_TF32 && !bits && attention_tc05_supported(hs, C))
+        return attention_tc05_tf32_forward(static_cast<float*>(y), lse, static_cast<const float*>(qkv), B, T, C,
+                                           H, status, st);
     if (mode == GPT2_MODE_TF32 && !bits && attention_tc_supported(hs))
         return attention_tc_forward(static_cast<float*>(y), lse, static_cast<const float*>(qkv), B, T, C, H,
                                     status, st);

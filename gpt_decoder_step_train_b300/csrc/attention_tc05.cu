@@ -105,29 +105,6 @@ constexpr uint32_t F_OFF_Q = 0, F_OFF_K = 4 * F_Q_BYTES, F_OFF_V = F_OFF_K + F_S
 constexpr size_t F_SMEM = F_SMEM_USED + 1024;
 constexpr uint32_t F_TMEM_COLS = 512;   // S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384) P_0, P_1 [384,512)
 
-// Work items, heaviest first: item i is the query-tile pair npair - 1 - i / (B H)
-// of (batch, head) number i % (B H); the CTAs of the persistent grid take items
-// blockIdx.x, blockIdx.x + gridDim.x, ...
-struct FwdItem {
-    int b, h, qrow0, nkv0, nkv1, nkv;
-};
-__host__ __device__ __forceinline__ int fwd_items(int B, int T, int H) {
-    return B * H * (((T + 127) / 128 + 1) / 2);
-}
-__device__ __forceinline__ FwdItem fwd_item(int i, int B, int T, int H) {
-    const int npair = ((T + 127) / 128 + 1) / 2, nkt = (T + F_BK - 1) / F_BK;
-    const int pi = npair - 1 - i / (B * H), bh = i % (B * H);
-    FwdItem w;
-    w.b = bh / H;
-    w.h = bh % H;
-    w.qrow0 = pi * 256;
-    // key tiles each query tile needs (tile g ends at row qrow0 + 128 g + 127)
-    w.nkv0 = min(2 * pi + 1, nkt);
-    w.nkv1 = w.qrow0 + 128 < T ? min(2 * pi + 2, nkt) : 0;
-    w.nkv = max(w.nkv0, w.nkv1);
-    return w;
-}
-
 template <bool DROP>
 __global__ void __launch_bounds__(F_THREADS, 1)
 attn_fwd_tc05(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ y, float* __restrict__ lse,

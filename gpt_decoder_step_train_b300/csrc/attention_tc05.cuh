@@ -23,6 +23,30 @@ constexpr int BWD_THREADS = 64 + 32 * BWD_EW_WARPS;
 constexpr float RESCALE_LOG2 = 8.f;                // move the running maximum past 2^8 growth
 constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
 
+// Forward work items (both forward kernels: 128-key tiles), heaviest first:
+// item i is the query-tile pair npair - 1 - i / (B H) of (batch, head) number
+// i % (B H); the CTAs of the persistent grid take items blockIdx.x,
+// blockIdx.x + gridDim.x, ...
+struct FwdItem {
+    int b, h, qrow0, nkv0, nkv1, nkv;
+};
+__host__ __device__ __forceinline__ int fwd_items(int B, int T, int H) {
+    return B * H * (((T + 127) / 128 + 1) / 2);
+}
+__device__ __forceinline__ FwdItem fwd_item(int i, int B, int T, int H) {
+    const int npair = ((T + 127) / 128 + 1) / 2, nkt = (T + BQ - 1) / BQ;
+    const int pi = npair - 1 - i / (B * H), bh = i % (B * H);
+    FwdItem w;
+    w.b = bh / H;
+    w.h = bh % H;
+    w.qrow0 = pi * 256;
+    // key tiles each query tile needs (tile g ends at row qrow0 + 128 g + 127)
+    w.nkv0 = min(2 * pi + 1, nkt);
+    w.nkv1 = w.qrow0 + 128 < T ? min(2 * pi + 2, nkt) : 0;
+    w.nkv = max(w.nkv0, w.nkv1);
+    return w;
+}
+
 // 128-byte swizzle of a K-major bf16 operand row: 16-byte chunk c of row r
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));

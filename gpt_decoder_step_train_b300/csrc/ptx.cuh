@@ -359,6 +359,33 @@ __device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// The same two groups for kind::tf32 (K = 8 per MMA: 32 bytes of a K-major
+// row, or 8 columns of an A operand in tensor memory, one tf32 per column).
+__device__ __forceinline__ void mma4_ss_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t a_step,
+                                             uint32_t b_step, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %5, %6, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %7, %8, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %9, %10, %3, q;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "l"(a + a_step), "l"(b + b_step), "l"(a + 2 * a_step),
+        "l"(b + 2 * b_step), "l"(a + 3 * a_step), "l"(b + 3 * b_step)
+        : "memory");
+}
+__device__ __forceinline__ void mma4_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t b_step,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, 0, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%5], %6, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%7], %8, %3, q;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%9], %10, %3, q;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8), "l"(b + b_step), "r"(a_tmem + 16),
+        "l"(b + 2 * b_step), "r"(a_tmem + 24), "l"(b + 3 * b_step)
+        : "memory");
+}
+
 // 16 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers.
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(

@@ -275,7 +275,12 @@ def test_linear_backward(L, B_, o64, mode, N, IC, OC):
 
 # ------------------------------------------------------------------ attention
 
-ATT_SHAPES = [(2, 37, 64, 4), (1, 300, 768, 12), (2, 129, 192, 3), (1, 1, 64, 4), (3, 64, 48, 6)]
+# head size 64 (tcgen05 forward in tf32 mode): T = 300 and 129 (ragged query and
+# key tiles; at T = 300 an item's second query tile is empty), T = 1024 (eight
+# key tiles, four items per (batch, head)), 300 items of T = 128 (two or three
+# items per CTA of the persistent grid)
+ATT_SHAPES = [(2, 37, 64, 4), (1, 300, 768, 12), (2, 129, 192, 3), (1, 1, 64, 4), (3, 64, 48, 6),
+              (2, 1024, 256, 4), (25, 128, 768, 12)]
 
 
 @pytest.mark.parametrize("mode", MODES)
