@@ -383,6 +383,8 @@ int attention_tc05_forward(void* y, float* lse, const void* qkv, int B, int T, i
                            cudaStream_t st, const uint32_t* bits, float ks);
 int attention_tc05_tf32_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int H, int* status,
                                 cudaStream_t st);
+int attention_tc05_tf32_backward(float* dqkv, const float* dy, const float* qkv, const float* lse, const float* D,
+                                 int B, int T, int C, int H, int* status, cudaStream_t st);
 int attention_tc05_backward_nodrop(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse,
                                    float* D, int B, int T, int C, int H, int* status, cudaStream_t st,
                                    float* colsum);
@@ -400,9 +402,9 @@ static bool attn_args_ok(int B, int T, int C, int H) {
 // mma.sync kernels for head sizes 16 and 32 (no dropout), else the CUDA-core
 // kernels on bf16 (head sizes that are multiples of 8: the backward's
 // rowsum(dO o O) reads a head's slice 16 bytes at a time); TF32 mode takes the
-// tcgen05 tf32 forward for head size 64 and the mma.sync TF32 kernels for the
-// other head sizes and the backward (no dropout); otherwise (FP32 mode,
-// dropout) the CUDA-core kernels on fp32.
+// tcgen05 tf32 kernels for head size 64 and the mma.sync TF32 kernels for
+// head sizes 16 and 32 (no dropout); otherwise (FP32 mode, dropout) the
+// CUDA-core kernels on fp32.
 int attention_forward(void* y, float* lse, const void* qkv, int B, int T, int C, int H, int mode, int* status,
                       cudaStream_t st, const uint32_t* bits, float p) {
     if (!y || !lse || !qkv || !attn_args_ok(B, T, C, H)) return GPT2_EINVAL;
@@ -464,6 +466,9 @@ int attention_backward_dropout(void* dqkv, const void* dy, const void* qkv, cons
     }
     launch_dot<float>(D, dy, y, B, T, C, H, hs, st);
     GPT2_LAUNCH_CHECK();
+    if (mode == GPT2_MODE_TF32 && !bits && attention_tc05_supported(hs, C))
+        return attention_tc05_tf32_backward(static_cast<float*>(dqkv), static_cast<const float*>(dy),
+                                            static_cast<const float*>(qkv), lse, D, B, T, C, H, status, st);
     if (mode == GPT2_MODE_TF32 && !bits && attention_tc_supported(hs))
         return attention_tc_backward(static_cast<float*>(dqkv), static_cast<const float*>(dy),
                                      static_cast<const float*>(qkv), lse, D, B, T, C, H, status, st);

@@ -76,14 +76,6 @@ __device__ __forceinline__ BwdItem dq_item(int i, int B, int T, int H) {
     return w;
 }
 
-// Wait, bounded and ignoring the abort flag, for a barrier phase that copies
-// this thread issued will complete (the drain before an aborting CTA leaves).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < WAIT_NS) {
-    }
-}
-
 // Two 64-row TMA boxes of a head's 128-row tile: columns col .. col + 63 of rows
 // row0 .. row0 + 127 of batch b.
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, int col, int row0, int b,

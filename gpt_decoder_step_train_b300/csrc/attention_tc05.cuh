@@ -47,6 +47,14 @@ __device__ __forceinline__ FwdItem fwd_item(int i, int B, int T, int H) {
     return w;
 }
 
+// Wait, bounded and ignoring the abort flag, for a barrier phase that copies
+// this thread issued will complete (the drain before an aborting CTA leaves).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < WAIT_NS) {
+    }
+}
+
 // 128-byte swizzle of a K-major bf16 operand row: 16-byte chunk c of row r
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
