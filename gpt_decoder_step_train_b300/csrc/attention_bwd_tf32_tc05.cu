@@ -43,10 +43,11 @@ constexpr uint32_t T3_HALF = 2 * T3_BOX;                   // 32 columns of a 12
 constexpr uint32_t T3_TILE = 2 * T3_HALF;                  // a 128-row fixed tile: 32 KB
 constexpr uint32_t T3_STILE = 2 * T3_BOX;                  // a 64-row streamed tile (one copy): 16 KB
 constexpr uint32_t T3_FIXED = 2 * T3_TILE;                 // an item's two fixed tiles: 64 KB
-// dK/dV stage: Q, dO (K-major) | Q, dO (MN-major) | lse * log2(e) [64], D [64]
-constexpr uint32_t KV3_STAGE = 4 * T3_STILE + 1024;
-constexpr int KV3_STAGES = 2;
-constexpr size_t KV3_SMEM = T3_FIXED + (size_t)KV3_STAGES * KV3_STAGE + 1024;
+// dK/dV: the fixed K, V | three slots of Q, dO K-major | two slots of Q, dO MN-major
+constexpr int KV3_KS = 3, KV3_MS = 2;
+constexpr uint32_t KV3_KSLOT = 2 * T3_STILE, KV3_MSLOT = 2 * T3_STILE;
+constexpr uint32_t KV3_OFF_K = T3_FIXED, KV3_OFF_M = KV3_OFF_K + KV3_KS * KV3_KSLOT;
+constexpr size_t KV3_SMEM = KV3_OFF_M + (size_t)KV3_MS * KV3_MSLOT + 1024;
 // dQ stage: K, V (K-major) | K (MN-major)
 constexpr uint32_t Q3_STAGE = 3 * T3_STILE;
 constexpr int Q3_STAGES = 3;
@@ -124,18 +125,23 @@ __device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16])
 }
 
 // ---------------------------------------------------------------- dK, dV
-// Shared memory: K | V of the item | two stages of Q, dO (K-major), Q, dO
-// (MN-major), lse and D of the tile's 64 queries.  Tensor memory: score buffer
-// u in [128 u, 128 u + 128): S^T then P^T in its first 64 columns, dP^T then
-// dS^T in the next 64 | dV [256, 320) | dK [320, 384).
+// Shared memory: K | V of the item | a ring of three K-major Q, dO tile pairs
+// (released once the score products have read them) | a ring of two MN-major
+// Q, dO tile pairs (released once dV, dK have read them), with each MN slot a
+// small static slot holding the tile's lse * log2(e) and D (the element-wise
+// warps read them; the slot is reused only after the products of its tile,
+// which follow the warps' P^T / dS^T).  Tensor memory: score buffer u in
+// [128 u, 128 u + 128): S^T then P^T in its first 64 columns, dP^T then dS^T
+// in the next 64 | dV [256, 320) | dK [320, 384).
 __global__ void __launch_bounds__(T3_THREADS, 1)
 attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tqm,
                   const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tdom,
                   float* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Dg, int B, int T,
                   int C, int H, float scale, int* status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t kv_full, kv_empty, st_full[KV3_STAGES], st_empty[KV3_STAGES], s_full[2],
-        p_full[2], pv_done[2], drain;
+    __shared__ __align__(8) uint64_t kv_full, kv_empty, kf_full[KV3_KS], kf_empty[KV3_KS], mn_full[KV3_MS],
+        mn_empty[KV3_MS], rows_full[KV3_MS], s_full[2], p_full[2], pv_done[2], drain;
+    __shared__ __align__(16) float s_rows[KV3_MS][2 * T3_BS];   // per MN slot: lse * log2(e) [64], D [64]
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
@@ -143,15 +149,19 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int nitems = B * H * ((T + 127) / 128);
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* const base_ptr = smem_raw + (base - raw);
 
     if (threadIdx.x == 0) {
         s_abort = 0;
         mbar_init(smem_u32(&kv_full), 1);
         mbar_init(smem_u32(&kv_empty), 1);
-        for (int s = 0; s < KV3_STAGES; s++) {
-            mbar_init(smem_u32(&st_full[s]), 1);
-            mbar_init(smem_u32(&st_empty[s]), 1);
+        for (int s = 0; s < KV3_KS; s++) {
+            mbar_init(smem_u32(&kf_full[s]), 1);
+            mbar_init(smem_u32(&kf_empty[s]), 1);
+        }
+        for (int s = 0; s < KV3_MS; s++) {
+            mbar_init(smem_u32(&mn_full[s]), 1);
+            mbar_init(smem_u32(&mn_empty[s]), 1);
+            mbar_init(smem_u32(&rows_full[s]), 1);
         }
         for (int u = 0; u < 2; u++) {
             mbar_init(smem_u32(&s_full[u]), 1);
@@ -173,10 +183,66 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------ producer (whole warp; lane 0 issues the copies)
-        int last_kc[KV3_STAGES], last_ic = -1;
-        for (int s = 0; s < KV3_STAGES; s++) last_kc[s] = -1;
+        // order per item: fixed K, V; K-major tile 0; then MN-major tile t after
+        // K-major tile t + 1, so the K-major copies run a tile ahead
+        int last_k[KV3_KS], last_m[KV3_MS], last_ic = -1;
+        for (int s = 0; s < KV3_KS; s++) last_k[s] = -1;
+        for (int s = 0; s < KV3_MS; s++) last_m[s] = -1;
         bool ok = true;
-        int kc = 0, ic = 0;
+        int kc = 0, ic = 0;                            // tiles and items loaded so far
+        auto k_load = [&](const Bwd3Item& w, int t, int g) -> bool {   // K-major tile t (global index g)
+            const int s = g % KV3_KS;
+            bool r = true;
+            if (lane == 0) {
+                r = mbar_wait(smem_u32(&kf_empty[s]), ((uint32_t)(g / KV3_KS) & 1u) ^ 1u, &s_abort, status);
+                if (r) {
+                    const uint32_t fb = smem_u32(&kf_full[s]);
+                    const uint32_t dst = base + KV3_OFF_K + s * KV3_KSLOT;
+                    const int q0 = (2 * w.tile + t) * T3_BS;
+                    mbar_expect_tx(fb, KV3_KSLOT);
+                    last_k[s] = g;
+                    load_stile(dst, &tq, w.h * HS, q0, w.b, fb);
+                    load_stile(dst + T3_STILE, &tdo, w.h * HS, q0, w.b, fb);
+                }
+            }
+            return __shfl_sync(0xffffffffu, r, 0);
+        };
+        auto m_load = [&](const Bwd3Item& w, int t, int g) -> bool {   // MN-major tile t, with its lse and D
+            const int s = g % KV3_MS;
+            const int q0 = (2 * w.tile + t) * T3_BS;
+            // the tile's lse * log2(e) (+inf past T, which zeroes P) and D, loaded before the wait
+            const float* lse_bh = lse + ((size_t)w.b * H + w.h) * T;
+            const float* D_bh = Dg + ((size_t)w.b * H + w.h) * T;
+            float lv[2], dv[2];
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int q = q0 + lane + 32 * k;
+                lv[k] = q < T ? __ldg(lse_bh + q) * LOG2E : INFINITY;
+                dv[k] = q < T ? __ldg(D_bh + q) : 0.f;
+            }
+            bool r = true;
+            if (lane == 0) {
+                r = mbar_wait(smem_u32(&mn_empty[s]), ((uint32_t)(g / KV3_MS) & 1u) ^ 1u, &s_abort, status);
+                if (r) {
+                    const uint32_t fb = smem_u32(&mn_full[s]);
+                    const uint32_t dst = base + KV3_OFF_M + s * KV3_MSLOT;
+                    mbar_expect_tx(fb, KV3_MSLOT);
+                    last_m[s] = g;
+                    load_stile(dst, &tqm, w.h * HS, q0, w.b, fb);
+                    load_stile(dst + T3_STILE, &tdom, w.h * HS, q0, w.b, fb);
+                }
+            }
+            r = __shfl_sync(0xffffffffu, r, 0);
+            if (!r) return false;
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                s_rows[s][lane + 32 * k] = lv[k];
+                s_rows[s][T3_BS + lane + 32 * k] = dv[k];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&rows_full[s]));   // releases the writes above
+            return true;
+        };
         for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x, ic++) {
             const Bwd3Item w = dkv3_item(it, B, T, H);
             if (lane == 0) {
@@ -190,41 +256,19 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            const float* lse_bh = lse + ((size_t)w.b * H + w.h) * T;
-            const float* D_bh = Dg + ((size_t)w.b * H + w.h) * T;
-            for (int t = 0; t < w.n && ok; t++, kc++) {
-                const int s = kc % KV3_STAGES;
-                if (lane == 0)
-                    ok = mbar_wait(smem_u32(&st_empty[s]), ((uint32_t)(kc / KV3_STAGES) & 1u) ^ 1u, &s_abort, status);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                const uint32_t fb = smem_u32(&st_full[s]);
-                const uint32_t st = base + T3_FIXED + s * KV3_STAGE;
-                const int q0 = (2 * w.tile + t) * T3_BS;
-                if (lane == 0) {
-                    // copies first; the phase cannot complete before the arrive below
-                    last_kc[s] = kc;
-                    load_stile(st, &tq, w.h * HS, q0, w.b, fb);
-                    load_stile(st + T3_STILE, &tdo, w.h * HS, q0, w.b, fb);
-                    load_stile(st + 2 * T3_STILE, &tqm, w.h * HS, q0, w.b, fb);
-                    load_stile(st + 3 * T3_STILE, &tdom, w.h * HS, q0, w.b, fb);
-                }
-                // the tile's lse * log2(e) (+inf past T, which zeroes P) and D
-                float* rows = reinterpret_cast<float*>(base_ptr + T3_FIXED + s * KV3_STAGE + 4 * T3_STILE);
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const int q = q0 + lane + 32 * k;
-                    rows[lane + 32 * k] = q < T ? __ldg(lse_bh + q) * LOG2E : INFINITY;
-                    rows[64 + lane + 32 * k] = q < T ? __ldg(D_bh + q) : 0.f;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(fb, 4 * T3_STILE);   // releases the writes above
+            if (ok) ok = k_load(w, 0, kc);
+            for (int t = 0; t < w.n && ok; t++) {
+                if (t + 1 < w.n) ok = k_load(w, t + 1, kc + t + 1);
+                if (ok) ok = m_load(w, t, kc + t);
             }
+            kc += w.n;
         }
         if (lane == 0 && !ok) {
             if (last_ic >= 0) drain_wait(smem_u32(&kv_full), (uint32_t)last_ic & 1u);
-            for (int s = 0; s < KV3_STAGES; s++)
-                if (last_kc[s] >= 0) drain_wait(smem_u32(&st_full[s]), (uint32_t)(last_kc[s] / KV3_STAGES) & 1u);
+            for (int s = 0; s < KV3_KS; s++)
+                if (last_k[s] >= 0) drain_wait(smem_u32(&kf_full[s]), (uint32_t)(last_k[s] / KV3_KS) & 1u);
+            for (int s = 0; s < KV3_MS; s++)
+                if (last_m[s] >= 0) drain_wait(smem_u32(&mn_full[s]), (uint32_t)(last_m[s] / KV3_MS) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -232,12 +276,12 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t id_s = instr_desc(128, T3_BS, false, false, false);   // K Q^T, V dO^T: K-major
             const uint32_t id_o = instr_desc(128, HS, false, true, false);       // P^T dO, dS^T Q: B MN-major
             const uint64_t dfix = smem_desc(base, 16, 1024, LAYOUT_SW128);
-            const uint64_t dst_k = smem_desc(base + T3_FIXED, 16, 1024, LAYOUT_SW128);
-            const uint64_t dst_mn = smem_desc(base + T3_FIXED + 2 * T3_STILE, T3_BOX, 512, LAYOUT_SW128_32B);
+            const uint64_t dk = smem_desc(base + KV3_OFF_K, 16, 1024, LAYOUT_SW128);
+            const uint64_t dm = smem_desc(base + KV3_OFF_M, T3_BOX, 512, LAYOUT_SW128_32B);
             constexpr uint32_t HALF_U = T3_HALF >> 4, BOX_U = T3_BOX >> 4, TILE_U = T3_TILE >> 4,
-                               STILE_U = T3_STILE >> 4, STAGE_U = KV3_STAGE >> 4;
+                               STILE_U = T3_STILE >> 4, KSLOT_U = KV3_KSLOT >> 4, MSLOT_U = KV3_MSLOT >> 4;
             bool ok = true;
-            int kc = 0, cs = 0;
+            int kc = 0;                                // tiles of earlier items (also the score-buffer count)
             uint64_t t_last = globaltimer();
             for (int it = blockIdx.x, ic = 0; it < nitems && ok; it += gridDim.x, ic++) {
                 const Bwd3Item w = dkv3_item(it, B, T, H);
@@ -250,29 +294,30 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     bool progress = false;
                     if (ns < w.n) {
                         // tile g goes to score buffer g & 1, free once the products of tile g - 2 completed
-                        const int s = (kc + ns) % KV3_STAGES, g = cs + ns, u = g & 1;
-                        if (mbar_test_wait(smem_u32(&st_full[s]), (uint32_t)((kc + ns) / KV3_STAGES) & 1u) &&
+                        const int g = kc + ns, s = g % KV3_KS, u = g & 1;
+                        if (mbar_test_wait(smem_u32(&kf_full[s]), (uint32_t)(g / KV3_KS) & 1u) &&
                             (g < 2 || mbar_test_wait(smem_u32(&pv_done[u]), (uint32_t)((g - 2) >> 1) & 1u))) {
                             tc_fence_after();
-                            const uint64_t q = dst_k + (uint64_t)(s * STAGE_U);
+                            const uint64_t q = dk + (uint64_t)(s * KSLOT_U);
                             score8(tmem + 128 * u, dfix, HALF_U, q, BOX_U, id_s);                   // S^T = K Q^T
                             score8(tmem + 128 * u + 64, dfix + TILE_U, HALF_U, q + STILE_U, BOX_U, id_s);   // dP^T
                             mma_commit(smem_u32(&s_full[u]));
+                            mma_commit(smem_u32(&kf_empty[s]));
                             if (++ns == w.n) mma_commit(smem_u32(&kv_empty));   // K, V read for the last time
                             progress = true;
                         }
                     }
                     if (no < ns) {
-                        const int g = cs + no, u = g & 1;
-                        if (mbar_test_wait(smem_u32(&p_full[u]), (uint32_t)(g >> 1) & 1u)) {
+                        const int g = kc + no, s = g % KV3_MS, u = g & 1;
+                        if (mbar_test_wait(smem_u32(&p_full[u]), (uint32_t)(g >> 1) & 1u) &&
+                            mbar_test_wait(smem_u32(&mn_full[s]), (uint32_t)(g / KV3_MS) & 1u)) {
                             tc_fence_after();
-                            const int s = (kc + no) % KV3_STAGES;
-                            const uint64_t qmn = dst_mn + (uint64_t)(s * STAGE_U);
+                            const uint64_t qmn = dm + (uint64_t)(s * MSLOT_U);
                             const uint32_t acc = no > 0 ? 1u : 0u;
                             acc8(tmem + 256, tmem + 128 * u, qmn + STILE_U, id_o, acc);       // dV += P^T dO
                             acc8(tmem + 320, tmem + 128 * u + 64, qmn, id_o, acc);            // dK += dS^T Q
                             mma_commit(smem_u32(&pv_done[u]));
-                            mma_commit(smem_u32(&st_empty[s]));
+                            mma_commit(smem_u32(&mn_empty[s]));
                             no++;
                             progress = true;
                         }
@@ -289,7 +334,6 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
                 }
                 kc += w.n;
-                cs += w.n;
             }
             mma_commit(smem_u32(&drain));
             drain_wait(smem_u32(&drain), 0);
@@ -302,34 +346,35 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const float c2 = scale * LOG2E;
         const uint64_t c2x2 = f2pack(c2, c2);
         bool ok = true;
-        int kc = 0, cs = 0;
+        int kc = 0;
         for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
             const Bwd3Item w = dkv3_item(it, B, T, H);
             const int key = w.tile * 128 + r;
             for (int t = 0; t < w.n; t++) {
-                const int s = (kc + t) % KV3_STAGES, g = cs + t, u = g & 1;
+                const int g = kc + t, s = g % KV3_MS, u = g & 1;
                 if (!mbar_wait(smem_u32(&s_full[u]), (uint32_t)(g >> 1) & 1u, &s_abort, status)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t su[16], du[16];
                 const uint32_t ts = tmem + lb + 128 * u + 16 * grp;
                 tmem_ld16_async(ts, su);
                 tmem_ld16_async(ts + 64, du);
-                tmem_wait16(su);
-                tmem_wait16(du);
-                // the stage's lse and D were written before its barrier completed (acquire it)
-                if (!mbar_wait(smem_u32(&st_full[s]), (uint32_t)((kc + t) / KV3_STAGES) & 1u, &s_abort, status)) {
+                // the tile's lse and D (written by the producer before rows_full; acquire them)
+                if (!mbar_wait(smem_u32(&rows_full[s]), (uint32_t)(g / KV3_MS) & 1u, &s_abort, status)) {
+                    tmem_wait16(su);
+                    tmem_wait16(du);
                     ok = false;
                     break;
                 }
-                const float* rows = reinterpret_cast<const float*>(base_ptr + T3_FIXED + s * KV3_STAGE +
-                                                                   4 * T3_STILE) + 16 * grp;
+                tmem_wait16(su);
+                tmem_wait16(du);
+                const float* rows = &s_rows[s][16 * grp];
                 const int q0 = (2 * w.tile + t) * T3_BS + 16 * grp;   // first query of this warp's columns
                 const bool diag = q0 < key;                            // some query of these columns precedes the key
                 float pv[16], dv[16];
 #pragma unroll
                 for (int c4 = 0; c4 < 4; c4++) {
                     const float4 lv = reinterpret_cast<const float4*>(rows)[c4];
-                    const float4 dd = reinterpret_cast<const float4*>(rows + 64)[c4];
+                    const float4 dd = reinterpret_cast<const float4*>(rows + T3_BS)[c4];
                     const int c = 4 * c4;
                     float a0 = __uint_as_float(su[c]), a1 = __uint_as_float(su[c + 1]);
                     float a2 = __uint_as_float(su[c + 2]), a3 = __uint_as_float(su[c + 3]);
@@ -358,12 +403,11 @@ attn_bwd_dkv_tf32(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (!ok) break;
             {
-                const int g = cs + w.n - 1;
+                const int g = kc + w.n - 1;
                 if (!mbar_wait(smem_u32(&pv_done[g & 1]), (uint32_t)(g >> 1) & 1u, &s_abort, status)) break;
             }
             tc_fence_after();
             kc += w.n;
-            cs += w.n;
             {                                              // groups 0, 1: dK (times c); 2, 3: dV
                 const int which = grp >> 1, half = grp & 1;
                 float o[32];
