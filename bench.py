@@ -640,6 +640,32 @@ OPS["attn_fwd"] = lambda mode: _attn_case("fwd", mode)
 OPS["attn_bwd"] = lambda mode: _attn_case("bwd", mode)
 
 
+def _decode_case(mode, B=1, steps=64):
+    """Autoregressive decoding with the key/value cache: one call decodes positions
+    0 .. steps-1 of B rows (GPT-2 124M); every step reads each fp32 weight once."""
+    import numpy as np
+    import torch
+    from gpt_decoder_step_train_b300 import synthetic as syn
+    from gpt_decoder_step_train_b300.binding import GPT2
+    cfg = syn.CONFIGS["124M"]
+    params = torch.from_numpy(syn.init_params(cfg)).cuda()
+    model = GPT2(cfg, params, maxB=B, mode=mode)
+    tok = torch.from_numpy(np.asarray(syn.draw_tokens(cfg)[0][:B, :steps], dtype=np.int32)).cuda()
+    cols = [tok[:, t].contiguous() for t in range(steps)]
+    out = torch.empty(B, cfg.V, device="cuda")
+
+    def fn():
+        rc = 0
+        for t in range(steps):
+            rc = rc or model.decode(cols[t], t, out)
+        return rc
+    n = syn.num_params(cfg)
+    return fn, 2.0 * n * B * steps, 4.0 * n * steps, [model, params, tok, cols, out]
+
+
+OPS["decode"] = _decode_case
+
+
 def run_op(args):
     """Time single operations: --op takes names or prefixes, comma separated."""
     import torch

@@ -21,105 +21,164 @@ namespace gpt2k {
 
 constexpr int DEC_MAXB = 16;
 
+// The decoding position lives in device memory (*dpos), so that one captured
+// graph serves every position: the step's kernels read it and the last one
+// advances it.
+
 // x[b, :] = wte[tok[b], :] + wpe[pos, :]; an id outside [0, V) gives zeros and BAD_TOKEN
 __global__ void decode_embed_kernel(float* __restrict__ x, const int* __restrict__ tok,
                                     const float* __restrict__ wte, const float* __restrict__ wpe, int B,
-                                    int C, int V, int pos, int* status) {
+                                    int C, int V, const int* __restrict__ dpos, int* status) {
     const int b = blockIdx.x;
-    const int t = tok[b];
+    const int t = tok[b], pos = *dpos;
     const bool ok = t >= 0 && t < V;
     if (!ok && threadIdx.x == 0) set_status(status, GPT2_STATUS_BAD_TOKEN);
     for (int c = threadIdx.x; c < C; c += blockDim.x)
         x[(size_t)b * C + c] = ok ? wte[(size_t)t * C + c] + wpe[(size_t)pos * C + c] : 0.f;
 }
 
-// out[b, o] = act(sum_k in[b, k] W[o, k] + bias[o]) + resid[b, o] for b < B <= 16.
-// One warp per output column: the weight row is read once (16-byte loads) and
-// applied to every input row; lane partial sums are combined in a fixed tree.
-// act: 0 none, 1 tanh-GELU.  in [B, IC] (row stride IC), out / resid [B, ld].
-__global__ void decode_gemv_kernel(float* __restrict__ out, int ld, const float* __restrict__ in,
-                                   const float* __restrict__ W, const float* __restrict__ bias,
-                                   const float* __restrict__ resid, int B, int IC, int OC, int act) {
-    const int o = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (o >= OC) return;
-    float acc[DEC_MAXB];
+// out[b, o] = act(sum_k in[b, k] W[o, k] + bias[o]) + resid[b, o] for b < B <= 16;
+// the qkv product also stores its key and value columns (o >= kv_c) into the
+// cache row of position *dpos.
+// HBM-bound (each weight read once per step, applied to every row).  A block of
+// 8 warps covers 8 / S output columns with S warps per column, each warp one
+// S-th of the row: its lanes issue up to eight 16-byte weight loads at once,
+// then apply them to every input row; the S partial sums of a column are added
+// in warp order through shared memory.  S > 1 keeps enough loads in flight when
+// there are few columns.  The row count is a template parameter NB >= B
+// (the rows B .. NB-1 of the input buffer are computed and dropped), so the
+// inner loops carry no per-row tests.  act: 0 none, 1 tanh-GELU.  in [NB, IC]
+// (row stride IC), out / resid [B, ld].
+constexpr int DEC_GEMV_WARPS = 8, DEC_GEMV_U = 8;
+
+struct DecGemv {
+    float* out;
+    int ld;
+    const float *in, *W, *bias, *resid;
+    int B, IC, OC, act, S;
+    float* cache;               // key/value cache of the layer, or null
+    int kv_c, maxT;             // first cached column (C); positions per cache row
+    const int* dpos;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(32 * DEC_GEMV_WARPS) decode_gemv_kernel(const DecGemv p) {
+    __shared__ float red[DEC_GEMV_WARPS][NB];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.S, IC = p.IC;
+    const int o = blockIdx.x * (DEC_GEMV_WARPS / S) + w / S, part = w % S;
+    const int k4n = IC >> 2, per = k4n / S, k4a = part * per, k4b = k4a + per;
+    const float4* x4 = reinterpret_cast<const float4*>(p.in);
+    float acc[NB];
 #pragma unroll
-    for (int b = 0; b < DEC_MAXB; b++) acc[b] = 0.f;
-    const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)o * IC);
-    const int k4n = IC >> 2;
-    for (int k4 = lane; k4 < k4n; k4 += 32) {
-        const float4 w = __ldg(w4 + k4);
+    for (int b = 0; b < NB; b++) acc[b] = 0.f;
+    if (o < p.OC) {
+        const float4* w4 = reinterpret_cast<const float4*>(p.W + (size_t)o * IC);
+        for (int k0 = k4a; k0 < k4b; k0 += 32 * DEC_GEMV_U) {
+            float4 wv[DEC_GEMV_U];
 #pragma unroll
-        for (int b = 0; b < DEC_MAXB; b++) {
-            if (b < B) {
-                const float4 xv = __ldg(reinterpret_cast<const float4*>(in + (size_t)b * IC) + k4);
-                acc[b] += (w.x * xv.x + w.y * xv.y) + (w.z * xv.z + w.w * xv.w);
+            for (int u = 0; u < DEC_GEMV_U; u++) {
+                const int k4 = k0 + 32 * u + lane;
+                wv[u] = k4 < k4b ? __ldg(w4 + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < DEC_GEMV_U; u++) {
+                const int k4 = k0 + 32 * u + lane;
+                if (k4 < k4b) {
+#pragma unroll
+                    for (int b = 0; b < NB; b++) {
+                        const float4 xv = __ldg(x4 + (size_t)b * k4n + k4);
+                        acc[b] += (wv[u].x * xv.x + wv[u].y * xv.y) + (wv[u].z * xv.z + wv[u].w * xv.w);
+                    }
+                }
             }
         }
     }
+    // lane b ends with row b's sum of this warp's part
+    float mine = 0.f;
 #pragma unroll
-    for (int b = 0; b < DEC_MAXB; b++) {
-        if (b < B) {
-            float v = warp_sum(acc[b]);
-            if (lane == b) {
-                if (bias) v += bias[o];
-                if (act == 1) v = gelu_fwd(v);
-                if (resid) v += resid[(size_t)b * ld + o];
-                out[(size_t)b * ld + o] = v;
-            }
+    for (int b = 0; b < NB; b++) {
+        const float v = warp_sum(acc[b]);
+        if (lane == b) mine = v;
+    }
+    if (S > 1) {
+        if (lane < NB) red[w][lane] = mine;
+        __syncthreads();
+        if (part == 0 && lane < p.B) {
+            float v = 0.f;
+            for (int q = 0; q < S; q++) v += red[w + q][lane];
+            mine = v;
         }
+    }
+    if (part == 0 && o < p.OC && lane < p.B) {
+        float v = mine;
+        if (p.bias) v += p.bias[o];
+        if (p.act == 1) v = gelu_fwd(v);
+        if (p.resid) v += p.resid[(size_t)lane * p.ld + o];
+        p.out[(size_t)lane * p.ld + o] = v;
+        if (p.cache && o >= p.kv_c)
+            p.cache[((size_t)lane * p.maxT + *p.dpos) * 2 * p.kv_c + (o - p.kv_c)] = v;
     }
 }
 
-// The new position's key and value rows into the cache: cache[b][pos] = qkv[b, C:3C].
-__global__ void decode_kv_store_kernel(float* __restrict__ cache, const float* __restrict__ qkv, int B, int C,
-                                       int maxT, int pos) {
-    const int b = blockIdx.x;
-    float* dst = cache + ((size_t)b * maxT + pos) * 2 * C;
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) dst[c] = qkv[(size_t)b * 3 * C + C + c];
-}
-
-// One warp per (row b, head h): scores of the new query against keys 0..pos,
-// softmax (maximum subtracted), weighted sum of the values.  hs <= 64.
+// One block per (row b, head h), four warps splitting the keys 0..pos (warp w
+// takes keys w, w + 4, ...): the score of a key is the warp's sum of the
+// lanes' products over the head's dimensions (lane d holds dimensions d and
+// d + 32), softmax with the block's maximum subtracted, then each warp sums
+// its keys' weighted values and the four partial rows and sums are added in
+// warp order.  hs <= 64.
 constexpr int DEC_ATT_WARPS = 4;
 constexpr int DEC_MAXT = 1024;
 
-__global__ void decode_attn_kernel(float* __restrict__ y, const float* __restrict__ qkv,
-                                   const float* __restrict__ cache, int B, int C, int H, int maxT, int pos,
-                                   float scale) {
-    __shared__ float sp[DEC_ATT_WARPS][DEC_MAXT];
+__global__ void __launch_bounds__(32 * DEC_ATT_WARPS)
+decode_attn_kernel(float* __restrict__ y, const float* __restrict__ qkv, const float* __restrict__ cache, int B,
+                   int C, int H, int maxT, const int* __restrict__ dpos, float scale) {
+    __shared__ float sp[DEC_MAXT];
+    __shared__ float sred[DEC_ATT_WARPS];
+    __shared__ float sacc[DEC_ATT_WARPS][64];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x * DEC_ATT_WARPS + w;
-    if (bh >= B * H) return;
-    const int b = bh / H, h = bh % H, hs = C / H;
+    const int pos = min(*dpos, DEC_MAXT - 1);
+    const int b = blockIdx.x / H, h = blockIdx.x % H, hs = C / H;
     const float* q = qkv + (size_t)b * 3 * C + h * hs;
-    const float* kb = cache + (size_t)b * maxT * 2 * C + h * hs;          // key j at kb + j * 2C
-    float* p = sp[w];
+    const float* kb = cache + (size_t)b * maxT * 2 * C + h * hs;          // key j at kb + j * 2C, value at + C
+    const bool d0 = lane < hs, d1 = lane + 32 < hs;
+    const float q0 = d0 ? q[lane] * scale : 0.f, q1 = d1 ? q[lane + 32] * scale : 0.f;
     float mx = -INFINITY;
-    for (int j = lane; j <= pos; j += 32) {
+#pragma unroll 4
+    for (int j = w; j <= pos; j += DEC_ATT_WARPS) {
         const float* kr = kb + (size_t)j * 2 * C;
-        float s = 0.f;
-        for (int d = 0; d < hs; d++) s += q[d] * kr[d];
-        s *= scale;
-        p[j] = s;
+        float s = (d0 ? q0 * kr[lane] : 0.f) + (d1 ? q1 * kr[lane + 32] : 0.f);
+        s = warp_sum(s);
+        if (lane == 0) sp[j] = s;
         mx = fmaxf(mx, s);
     }
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j <= pos; j += 32) {
-        const float e = expf(p[j] - mx);
-        p[j] = e;
+    if (lane == 0) sred[w] = mx;
+    __syncthreads();
+    mx = sred[0];
+    for (int k = 1; k < DEC_ATT_WARPS; k++) mx = fmaxf(mx, sred[k]);
+    __syncthreads();                                                    // sred is reused below
+    float a0 = 0.f, a1 = 0.f, sum = 0.f;
+#pragma unroll 4
+    for (int j = w; j <= pos; j += DEC_ATT_WARPS) {
+        const float e = expf(sp[j] - mx);
+        const float* vr = kb + (size_t)j * 2 * C + C;
+        if (d0) a0 += e * vr[lane];
+        if (d1) a1 += e * vr[lane + 32];
         sum += e;
     }
-    sum = warp_sum(sum);
-    __syncwarp();
-    const float inv = 1.f / sum;
-    for (int d = lane; d < hs; d += 32) {
-        const float* vb = kb + C + d;                                       // value j, column d
-        float acc = 0.f;
-        for (int j = 0; j <= pos; j++) acc += p[j] * vb[(size_t)j * 2 * C];
-        y[(size_t)b * C + h * hs + d] = acc * inv;
+    if (lane == 0) sred[w] = sum;
+    if (d0) sacc[w][lane] = a0;
+    if (d1) sacc[w][lane + 32] = a1;
+    __syncthreads();
+    if (w == 0) {
+        float l = 0.f;
+        for (int k = 0; k < DEC_ATT_WARPS; k++) l += sred[k];
+        const float inv = 1.f / l;
+        for (int d = lane; d < hs; d += 32) {
+            float v = 0.f;
+            for (int k = 0; k < DEC_ATT_WARPS; k++) v += sacc[k][d];
+            y[(size_t)b * C + h * hs + d] = v * inv;
+        }
     }
 }
 
@@ -233,35 +292,52 @@ __global__ void sample_topk_kernel(int* __restrict__ out, const float* __restric
 }
 
 // ---- launchers ----------------------------------------------------------------
-int decode_embed(float* x, const int* tok, const float* wte, const float* wpe, int B, int C, int V, int pos,
-                 int* status, cudaStream_t st) {
-    count_launch(), decode_embed_kernel<<<B, 256, 0, st>>>(x, tok, wte, wpe, B, C, V, pos, status);
+// The step's last kernel: the next call decodes the following position.
+__global__ void decode_advance_kernel(int* dpos) { *dpos += 1; }
+
+int decode_embed(float* x, const int* tok, const float* wte, const float* wpe, int B, int C, int V,
+                 const int* dpos, int* status, cudaStream_t st) {
+    count_launch(), decode_embed_kernel<<<B, 256, 0, st>>>(x, tok, wte, wpe, B, C, V, dpos, status);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }
 
+// decode_gemv with an optional store of the key and value columns into the
+// cache (the qkv product: cache != null).
 int decode_gemv(float* out, int ld, const float* in, const float* W, const float* bias, const float* resid,
-                int B, int IC, int OC, int act, cudaStream_t st) {
+                int B, int IC, int OC, int act, float* cache, int maxT, const int* dpos, cudaStream_t st) {
     if (B < 1 || B > DEC_MAXB || IC % 4 || !aligned16(in) || !aligned16(W)) return GPT2_EINVAL;
-    constexpr int WARPS = 8;
-    count_launch(), decode_gemv_kernel<<<ceil_div(OC, WARPS), 32 * WARPS, 0, st>>>(out, ld, in, W, bias, resid, B,
-                                                                                IC, OC, act);
+    if (cache && (OC % 3 || !dpos)) return GPT2_EINVAL;
+    // warps per column: enough warps for every SM (about 16 each), splitting the
+    // row evenly
+    int S = 1;
+    while (S < DEC_GEMV_WARPS && (long long)OC * S < 16LL * num_sms() && (IC / 4) % (2 * S) == 0) S *= 2;
+    const DecGemv p{out, ld, in, W, bias, resid, B, IC, OC, act, S, cache, OC / 3, maxT, dpos};
+    const dim3 grid(ceil_div(OC, DEC_GEMV_WARPS / S)), block(32 * DEC_GEMV_WARPS);
+    const int nb = B == 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+    if (nb == 1) count_launch(), decode_gemv_kernel<1><<<grid, block, 0, st>>>(p);
+    else if (nb == 2) count_launch(), decode_gemv_kernel<2><<<grid, block, 0, st>>>(p);
+    else if (nb == 4) count_launch(), decode_gemv_kernel<4><<<grid, block, 0, st>>>(p);
+    else if (nb == 8) count_launch(), decode_gemv_kernel<8><<<grid, block, 0, st>>>(p);
+    else count_launch(), decode_gemv_kernel<16><<<grid, block, 0, st>>>(p);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }
 
-int decode_kv_store(float* cache, const float* qkv, int B, int C, int maxT, int pos, cudaStream_t st) {
-    count_launch(), decode_kv_store_kernel<<<B, 256, 0, st>>>(cache, qkv, B, C, maxT, pos);
-    GPT2_LAUNCH_CHECK();
-    return GPT2_OK;
-}
-
-int decode_attention(float* y, const float* qkv, const float* cache, int B, int C, int H, int maxT, int pos,
-                     cudaStream_t st) {
-    if (pos >= DEC_MAXT || C / H > 64) return GPT2_EINVAL;
+// Positions are below min(maxT, DEC_MAXT): checked by the caller before the
+// step (the kernel clamps as well).
+int decode_attention(float* y, const float* qkv, const float* cache, int B, int C, int H, int maxT,
+                     const int* dpos, cudaStream_t st) {
+    if (C / H > 64) return GPT2_EINVAL;
     const float scale = 1.f / sqrtf((float)(C / H));
-    count_launch(), decode_attn_kernel<<<ceil_div(B * H, DEC_ATT_WARPS), 32 * DEC_ATT_WARPS, 0, st>>>(
-        y, qkv, cache, B, C, H, maxT, pos, scale);
+    count_launch(), decode_attn_kernel<<<B * H, 32 * DEC_ATT_WARPS, 0, st>>>(y, qkv, cache, B, C, H, maxT, dpos,
+                                                                             scale);
+    GPT2_LAUNCH_CHECK();
+    return GPT2_OK;
+}
+
+int decode_advance(int* dpos, cudaStream_t st) {
+    count_launch(), decode_advance_kernel<<<1, 1, 0, st>>>(dpos);
     GPT2_LAUNCH_CHECK();
     return GPT2_OK;
 }

@@ -124,14 +124,15 @@ int bias_grad_any(float* db, const void* dout, bool bf16, int N, int OC, int ld,
 int attention_backward(void* dqkv, const void* dy, const void* qkv, const void* y, const float* lse, int B,
                        int T, int C, int H, void* scratch, size_t scratch_bytes, int mode, int* status,
                        cudaStream_t st, float* colsum, bool* colsum_done);
-// Decoding with a key/value cache (decode.cu), fp32, at most 16 rows.
-int decode_embed(float* x, const int* tok, const float* wte, const float* wpe, int B, int C, int V, int pos,
-                 int* status, cudaStream_t st);
+// Decoding with a key/value cache (decode.cu), fp32, at most 16 rows; the
+// position is read from device memory (*dpos) and advanced by decode_advance.
+int decode_embed(float* x, const int* tok, const float* wte, const float* wpe, int B, int C, int V,
+                 const int* dpos, int* status, cudaStream_t st);
 int decode_gemv(float* out, int ld, const float* in, const float* W, const float* bias, const float* resid,
-                int B, int IC, int OC, int act, cudaStream_t st);
-int decode_kv_store(float* cache, const float* qkv, int B, int C, int maxT, int pos, cudaStream_t st);
-int decode_attention(float* y, const float* qkv, const float* cache, int B, int C, int H, int maxT, int pos,
-                     cudaStream_t st);
+                int B, int IC, int OC, int act, float* cache, int maxT, const int* dpos, cudaStream_t st);
+int decode_attention(float* y, const float* qkv, const float* cache, int B, int C, int H, int maxT,
+                     const int* dpos, cudaStream_t st);
+int decode_advance(int* dpos, cudaStream_t st);
 int layernorm_forward(void* y, bool out_bf16, float* mean, float* rstd, const float* x,
                       const float* w, const float* b, int N, int C, cudaStream_t st);
 int to_bf16(void* dst, const float* src, size_t n, cudaStream_t st);

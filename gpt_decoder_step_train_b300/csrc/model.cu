@@ -139,11 +139,12 @@ struct gpt2 {
     // decoding: key/value cache [L][maxB][maxT][2C] and the rows of one step,
     // allocated by the first gpt2_decode
     char* dec;
-    float *kv, *sx, *sx2, *sln, *sqkv, *satt, *sh, *smean, *srstd;
-    int* stok;
+    float *kv, *sx, *sx2, *sln, *sqkv, *satt, *sh, *smean, *srstd, *slog;
+    int *stok, *dpos;           // the step's token ids; the position being decoded
     int dec_B, dec_next;
-    // CUDA graphs of the forward and backward, one per (kind, B, T), replayed on a
-    // private stream ordered after and before the caller's stream by events
+    // CUDA graphs of the forward, backward and decoding step, one per (kind, B,
+    // T), replayed on a private stream ordered after and before the caller's
+    // stream by events
     struct Graph {
         int kind, B, T, seen;
         cudaGraphExec_t exec;
@@ -769,41 +770,50 @@ static int decode_alloc(gpt2* m) {
     const size_t o_kv = take((size_t)c.L * c.maxB * c.maxT * 2 * C * sizeof(float));
     const size_t o_x = take(RB * C * 4), o_x2 = take(RB * C * 4), o_ln = take(RB * C * 4);
     const size_t o_qkv = take(RB * 3 * C * 4), o_att = take(RB * C * 4), o_h = take(RB * 4 * C * 4);
-    const size_t o_mu = take(RB * 4), o_rs = take(RB * 4), o_tok = take(RB * 4);
+    const size_t o_mu = take(RB * 4), o_rs = take(RB * 4), o_tok = take(RB * 4), o_pos = take(4);
+    const size_t o_log = take(RB * c.V * 4);
     if (cudaMalloc(&m->dec, off) != cudaSuccess) { (void)cudaGetLastError(); m->dec = nullptr; return GPT2_ENOMEM; }
     auto F = [&](size_t o) { return reinterpret_cast<float*>(m->dec + o); };
     m->kv = F(o_kv); m->sx = F(o_x); m->sx2 = F(o_x2); m->sln = F(o_ln); m->sqkv = F(o_qkv);
     m->satt = F(o_att); m->sh = F(o_h); m->smean = F(o_mu); m->srstd = F(o_rs);
+    m->slog = F(o_log);
     m->stok = reinterpret_cast<int*>(m->dec + o_tok);
+    m->dpos = reinterpret_cast<int*>(m->dec + o_pos);
     return GPT2_OK;
 }
 
-static int decode_impl(gpt2* m, int B, int pos, float* logits) {
+// One decoding step of B rows at the position *dpos (the same operations for
+// every position, so a captured graph replays for each): the logits go to the
+// step buffer slog [B, V].
+static int decode_impl(gpt2* m, int B) {
     const gpt2_config& c = m->cfg;
     const int C = c.C, L = c.L, H = c.H;
     cudaStream_t st = m->st;
     int* status = &m->flags->status;
-    int rc = decode_embed(m->sx, m->stok, P(m, WTE), P(m, WPE), B, C, c.V, pos, status, st);
+    int rc = decode_embed(m->sx, m->stok, P(m, WTE), P(m, WPE), B, C, c.V, m->dpos, status, st);
+    // per layer: LayerNorm 1, qkv (+ the key/value cache store), attention,
+    // projection + residual, LayerNorm 2, c_fc + GELU, c_proj + residual
     for (int l = 0; l < L && !rc; l++) {
         const size_t cc = (size_t)C * C;
         float* kv = m->kv + (size_t)l * c.maxB * c.maxT * 2 * C;
         rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx, P(m, LN1W) + l * C, P(m, LN1B) + l * C,
                                B, C, st);
         if (!rc) rc = decode_gemv(m->sqkv, 3 * C, m->sln, P(m, QKVW) + l * 3 * cc, P(m, QKVB) + l * 3 * C,
-                                  nullptr, B, C, 3 * C, 0, st);
-        if (!rc) rc = decode_kv_store(kv, m->sqkv, B, C, c.maxT, pos, st);
-        if (!rc) rc = decode_attention(m->satt, m->sqkv, kv, B, C, H, c.maxT, pos, st);
+                                  nullptr, B, C, 3 * C, 0, kv, c.maxT, m->dpos, st);
+        if (!rc) rc = decode_attention(m->satt, m->sqkv, kv, B, C, H, c.maxT, m->dpos, st);
         if (!rc) rc = decode_gemv(m->sx2, C, m->satt, P(m, ATTPROJW) + l * cc, P(m, ATTPROJB) + l * C, m->sx, B,
-                                  C, C, 0, st);
+                                  C, C, 0, nullptr, 0, nullptr, st);
         if (!rc) rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx2, P(m, LN2W) + l * C,
                                         P(m, LN2B) + l * C, B, C, st);
         if (!rc) rc = decode_gemv(m->sh, 4 * C, m->sln, P(m, FCW) + l * 4 * cc, P(m, FCB) + l * 4 * C, nullptr,
-                                  B, C, 4 * C, 1, st);
+                                  B, C, 4 * C, 1, nullptr, 0, nullptr, st);
         if (!rc) rc = decode_gemv(m->sx, C, m->sh, P(m, FCPROJW) + l * 4 * cc, P(m, FCPROJB) + l * C, m->sx2,
-                                  B, 4 * C, C, 0, st);
+                                  B, 4 * C, C, 0, nullptr, 0, nullptr, st);
     }
     if (!rc) rc = layernorm_forward(m->sln, false, m->smean, m->srstd, m->sx, P(m, LNFW), P(m, LNFB), B, C, st);
-    if (!rc) rc = decode_gemv(logits, c.V, m->sln, P(m, WTE), nullptr, nullptr, B, C, c.V, 0, st);
+    if (!rc) rc = decode_gemv(m->slog, c.V, m->sln, P(m, WTE), nullptr, nullptr, B, C, c.V, 0, nullptr, 0, nullptr,
+                              st);
+    if (!rc) rc = decode_advance(m->dpos, st);
     return rc;
 }
 }  // namespace gpt2k
@@ -830,8 +840,13 @@ GPT2_API int gpt2_decode(gpt2* m, const int* tokens, int B, int pos, float* logi
         return GPT2_ECUDA;
     }
     m->fwd_targets = false;                 // the step rows are not a training forward
-    int rc = decode_impl(m, B, pos, logits);
-    if (rc) { record(m, rc); m->dec_next = -1; return rc; }
+    // a new sequence starts the device-side position at 0; later calls follow it
+    int rc = pos == 0 && cudaMemsetAsync(m->dpos, 0, sizeof(int), m->st) != cudaSuccess ? GPT2_ECUDA : GPT2_OK;
+    if (!rc) rc = run_graphed(m, 8, B, 0, [&]() -> int { return decode_impl(m, B); });
+    if (!rc && cudaMemcpyAsync(logits, m->slog, (size_t)B * m->cfg.V * sizeof(float), cudaMemcpyDefault, m->st) !=
+                   cudaSuccess)
+        rc = GPT2_ECUDA;
+    if (rc) { (void)cudaGetLastError(); record(m, rc); m->dec_next = -1; return rc; }
     m->dec_B = B;
     m->dec_next = pos + 1;
     return GPT2_OK;
