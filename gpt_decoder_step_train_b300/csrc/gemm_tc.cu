@@ -18,7 +18,7 @@
 // the main loop of the next.  Tiles are visited in groups of m-tiles so the
 // B operand (the weights) is reused from L2 by concurrently running CTAs.
 //
-// CTA pairs (PAIR, bf16): a cluster of two CTAs shares each 256 x 256 tile.
+// CTA pairs (PAIR, bf16 or tf32): a cluster of two CTAs shares each 256 x 256 tile.
 // Rank 0 issues tcgen05.mma.cta_group::2 (M = 256); each CTA holds 128 rows of
 // A and 128 rows of B per stage and 128 rows of the accumulator; both CTAs'
 // loads complete on rank 0's stage barrier, the MMA commits are multicast to
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(Epi<PAIR>::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAux,
                const __grid_constant__ CUtensorMap tmPre, const Params p) {
-    static_assert(!PAIR || (BF16 && BN == 256), "CTA pairs: bf16, 256-column tiles");
+    static_assert(!PAIR || BN == 256, "CTA pairs: 256-column tiles");
     using S = Shape<BN, BF16, PAIR>;
     using E = Elem<BF16>;
     constexpr int RING_MAX = S::EPI_WARP / 1024;      // input boxes per warp (bf16 boxes)
@@ -431,7 +431,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         uint64_t bd = p.b_kmajor
                                           ? smem_desc(b0 + k * KMAJ_STEP, 16, 1024, LAYOUT_SW128)
                                           : smem_desc(b0 + k * MN_STEP, p.mn_lbo, p.mn_sbo, p.mn_layout);
-                        if (PAIR) mma_issue_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (PAIR) mma_issue_pair<BF16>(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         else mma_issue<BF16>(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     // the stage is free in both CTAs once these MMAs have read it
@@ -1032,25 +1032,24 @@ static int launch(const GemmProblem& g, const GemmEpilogue& e, float* partial, i
 template <bool BF16>
 static int launch_any(const GemmProblem& g, const GemmEpilogue& e, float* partial, int split,
                       cudaStream_t st) {
-    if constexpr (BF16)
-        if (gemm_tc_pair(g, partial ? nullptr : &e)) return launch<256, true, true>(g, e, partial, split, st);
+    if (gemm_tc_pair(g, partial ? nullptr : &e)) return launch<256, BF16, true>(g, e, partial, split, st);
     if (g.N <= 128) return launch<128, BF16, false>(g, e, partial, split, st);
     return launch<256, BF16, false>(g, e, partial, split, st);
 }
 
 }  // namespace tc
 
-// bf16 products with at least 256 rows and 256 columns run on CTA pairs
-// (cta_group::2, 256 x 256 tiles, sixteen epilogue warps per CTA); smaller ones
-// on single CTAs (128 x 256 or 128 x 128 tiles).  GPT2_GEMM_CTA_PAIRS=0 in the
-// environment sends everything to single CTAs.
+// bf16 and tf32 products with at least 256 rows and 256 columns run on CTA
+// pairs (cta_group::2, 256 x 256 tiles, sixteen epilogue warps per CTA);
+// smaller ones on single CTAs (128 x 256 or 128 x 128 tiles).
+// GPT2_GEMM_CTA_PAIRS=0 in the environment sends everything to single CTAs.
 bool gemm_tc_pair(const GemmProblem& g, const GemmEpilogue* e) {
     static int on = -1;
     if (on < 0) {
         const char* v = getenv("GPT2_GEMM_CTA_PAIRS");
         on = (v && v[0] == '0') ? 0 : 1;
     }
-    if (!on || !g.bf16 || g.M < 256 || g.N < 256 || tc::pair_clusters() <= 0) return false;
+    if (!on || g.M < 256 || g.N < 256 || tc::pair_clusters() <= 0) return false;
     // a bf16 output with GELU takes a bf16 pre-activation and a bf16 GELU input
     // on pairs (both go through the output's box)
     if (e && e->out_bf16 && !e->residual &&

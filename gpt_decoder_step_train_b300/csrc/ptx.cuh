@@ -465,13 +465,22 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 // One cta_group::2 MMA (issued by rank 0): A rows 0-127 and B rows 0..N/2-1
 // from rank 0's shared memory, the other halves from rank 1's at the same
 // offsets; D rows 0-127 in rank 0's tensor memory, 128-255 in rank 1's.
+template <bool BF16>
 __device__ __forceinline__ void mma_issue_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                                uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if (BF16) {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 // When every earlier cta_group::2 MMA of this thread has completed, arrive once
