@@ -121,6 +121,53 @@ dropout_mask_kernel(uint32_t* __restrict__ bits, long long rows, int cols, int W
     }
 }
 
+// The attention sites (causal_T > 0, cols % 4 == 0): a block of 32 x 32
+// threads covers 32 consecutive rows and 32 consecutive words; a warp takes one
+// word of the 32 rows (lane = row), so the rows of one 32-row group of a
+// (batch, head) share the decision "left of the diagonal or not" and the warp
+// draws or writes zeros as a whole.  The words go through a shared tile and are
+// written row by row (32 words, 128 bytes, per warp).  Same bits as the
+// kernel above.
+__global__ void __launch_bounds__(1024)
+dropout_mask_causal_kernel(uint32_t* __restrict__ bits, long long rows, int cols, int W, int causal_T,
+                           const uint32_t* __restrict__ state, uint32_t key0, uint32_t key1, uint32_t step,
+                           uint32_t site, uint32_t thr) {
+    __shared__ uint32_t tile[32][33];
+    if (state) {
+        key0 = state[0];
+        key1 = state[1];
+        step = state[2];
+    }
+    const int r = threadIdx.x, kk = threadIdx.y;
+    const long long row0 = 32LL * blockIdx.x, row = row0 + r;
+    const int k = 32 * (int)blockIdx.y + kk;
+    uint32_t out = 0;
+    if (row < rows && k < W) {
+        const int i = (int)(row % causal_T), c0 = 32 * k;
+        if (c0 <= i) {
+            const int nq = min(32, cols - c0) >> 2;
+            const unsigned long long q0 =
+                ((unsigned long long)row * (unsigned long long)cols + (unsigned long long)c0) >> 2;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (j < nq) {
+                    const unsigned long long q = q0 + (unsigned long long)j;
+                    const uint4 v = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), site, step), key0, key1);
+                    out |= ((uint32_t)(v.x >= thr) | ((uint32_t)(v.y >= thr) << 1) | ((uint32_t)(v.z >= thr) << 2) |
+                            ((uint32_t)(v.w >= thr) << 3))
+                           << (4 * j);
+                }
+            }
+        }
+    }
+    tile[kk][r] = out;
+    __syncthreads();
+    // thread (x, y) writes word 32 blockIdx.y + x of row row0 + y
+    const long long wrow = row0 + threadIdx.y;
+    const int wk = 32 * (int)blockIdx.y + threadIdx.x;
+    if (wrow < rows && wk < W) bits[wrow * W + wk] = tile[threadIdx.x][threadIdx.y];
+}
+
 // out = res + keep o out / (1 - p)  (res may be null: out = keep o out / (1 - p));
 // rows of C columns, C % 4 == 0, one float4 per thread.
 __global__ void __launch_bounds__(256)
@@ -199,7 +246,11 @@ int dropout_mask(uint32_t* bits, long long rows, int cols, int causal_T, const u
     const long long want = (total + 255) / 256;
     const unsigned blocks = (unsigned)(want < 148LL * 32 ? want : 148LL * 32);
     const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32), thr = dropout_threshold(p);
-    if (cols % 4 == 0)
+    if (causal_T > 0 && cols % 4 == 0 && (rows + 31) / 32 <= 0x7fffffffLL)
+        count_launch(), dropout_mask_causal_kernel<<<dim3((unsigned)((rows + 31) / 32), (unsigned)((W + 31) / 32)),
+                                                     dim3(32, 32), 0, st>>>(bits, rows, cols, W, causal_T, state, k0,
+                                                                           k1, step, site, thr);
+    else if (cols % 4 == 0)
         count_launch(), dropout_mask_kernel<true><<<blocks, 256, 0, st>>>(bits, rows, cols, W, causal_T, state, k0,
                                                                           k1, step, site, thr);
     else

@@ -58,7 +58,10 @@ def gpu_mask(B_, rows, cols, causal_T, seed, site, step, p):
     return bits
 
 
-@pytest.mark.parametrize("rows,cols,causal_T", [(37, 100, 0), (1, 3, 0), (2 * 3 * 77, 77, 77), (4 * 64, 64, 64)])
+# causal rows with cols % 4 == 0 take the transposed kernel: T = 64; T = 100 (32-row
+# groups straddle (batch, head) boundaries); T = 1100 (more than 32 words per row)
+@pytest.mark.parametrize("rows,cols,causal_T", [(37, 100, 0), (1, 3, 0), (2 * 3 * 77, 77, 77), (4 * 64, 64, 64),
+                                                (2 * 3 * 100, 100, 100), (1100, 1100, 1100)])
 @pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
 def test_mask_bits_equal_the_oracle_draws(B_, o64, rows, cols, causal_T, p):
     seed, site, step = 0xDEADBEEF12345678, 5, 3
