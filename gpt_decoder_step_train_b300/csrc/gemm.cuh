@@ -106,10 +106,15 @@ int linear_forward(void* out, bool out_bf16, void* out_pre, const void* inp, con
 // With defer != null and the column sums fused into the tensor-core epilogue,
 // their reduction is described in *defer (defer->part == null otherwise)
 // instead of launched.
+// ks / ks_bytes: optional scratch for K slices of a plain dX product (fp32
+// output, no GELU' or bias sums); linear_backward_input_scratch_bytes sizes it
+// for every row count up to N.
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
                           int* status, cudaStream_t st, float* db = nullptr, void* cs = nullptr,
-                          size_t cs_bytes = 0, ColReduce* defer = nullptr);
+                          size_t cs_bytes = 0, ColReduce* defer = nullptr, void* ks = nullptr,
+                          size_t ks_bytes = 0);
+size_t linear_backward_input_scratch_bytes(int N, int IC, int OC, int mode);
 size_t linear_colsum_bytes(int N, int IC);
 // db[c] = sum over g of part[g * OC + c], in group order.
 int colsum_reduce(float* db, const float* part, int groups, int OC, cudaStream_t st);

@@ -270,13 +270,45 @@ size_t linear_colsum_bytes(int N, int IC) {
     return std::max(round_up((size_t)ceil_div(N, 32) * IC * sizeof(float), 256), bias_scratch_bytes(N, IC));
 }
 
+// K slices for a plain dX product (fp32 output, no GELU' or bias sums), by the
+// dW cost model (M = N rows, N = IC, K = OC): few row tiles and a long K (the
+// lm_head at small B·T) leave most SMs idle without it.  Scratch for the slices.
+static int dx_split(int N, int IC, int OC, int mode) {
+    return mode == GPT2_MODE_FP32 ? 1 : dw_split(OC, IC, N, mode);
+}
+size_t linear_backward_input_scratch_bytes(int N, int IC, int OC, int mode) {
+    size_t s = 0;
+    for (int n = N; n >= 1; n = n / 2) {               // every row count up to N
+        const int split = dx_split(n, IC, OC, mode);
+        if (split > 1) s = std::max(s, (size_t)split * n * IC * sizeof(float));
+        if (n == 1) break;
+    }
+    return s;
+}
+
 int linear_backward_input(void* dinp, bool dinp_bf16, const void* dout, const void* w, bool bf16,
                           const void* gelu_x, int N, int IC, int OC, int ld_dout, int mode,
-                          int* status, cudaStream_t st, float* db, void* cs, size_t cs_bytes, ColReduce* defer) {
+                          int* status, cudaStream_t st, float* db, void* cs, size_t cs_bytes, ColReduce* defer,
+                          void* ks, size_t ks_bytes) {
     if (defer) defer->part = nullptr;
     if (!dinp || !dout || !w || N < 1 || IC < 1 || OC < 1 || ld_dout < OC) return GPT2_EINVAL;
     if (db && (!cs || cs_bytes < linear_colsum_bytes(N, IC))) return GPT2_ENOMEM;
     GemmProblem p{N, IC, OC, dout, ld_dout, true, w, IC, false, status, bf16};
+    if (ks && !gelu_x && !db && !dinp_bf16) {
+        // split K over fp32 partial slices summed in slice order
+        const int split = dx_split(N, IC, OC, mode);
+        if (split > 1 && (size_t)split * N * IC * sizeof(float) <= ks_bytes && gemm_tc_supported(p) &&
+            (size_t)N * IC % 4 == 0 && aligned16(dinp)) {
+            float* partial = reinterpret_cast<float*>(ks);
+            int rc = gemm_tc_splitk(p, partial, split, st);
+            if (rc) return rc;
+            const size_t n4 = (size_t)N * IC / 4;
+            count_launch(), splitk_reduce_kernel<<<ceil_div((long long)n4, 256), 256, 0, st>>>(
+                reinterpret_cast<float4*>(dinp), reinterpret_cast<const float4*>(partial), split, n4);
+            GPT2_LAUNCH_CHECK();
+            return GPT2_OK;
+        }
+    }
     GemmEpilogue e{};
     e.out = dinp;
     e.ldo = IC;

@@ -230,6 +230,9 @@ static size_t plan(gpt2* m, char* base) {
     s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, 4 * Ci, mode));
     s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, 4 * Ci, Ci, mode));
     s = std::max(s, gpt2_op_linear_backward_weight_scratch_bytes(Ri, Ci, c.V, mode));
+    s = std::max(s, linear_backward_input_scratch_bytes(Ri, Ci, c.V, mode));
+    s = std::max(s, linear_backward_input_scratch_bytes(Ri, Ci, 3 * Ci, mode));
+    s = std::max(s, linear_backward_input_scratch_bytes(Ri, Ci, 4 * Ci, mode));
     s = std::max(s, gpt2_op_attention_backward_scratch_bytes(c.maxB, c.maxT, c.H));
     s = std::max(s, gpt2_op_encoder_backward_scratch_bytes(Ri, c.V, Ci));
     s = std::max(s, gpt2_op_bias_grad_scratch_bytes(Ri, 4 * Ci));
@@ -422,7 +425,7 @@ static int backward_impl(gpt2* m) {
     };
     // tied lm_head: d(lnf) = dz . wte ; d(wte) = dz^T . lnf (first write of dwte)
     OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, dz_op, W(m, WTE), b16, nullptr, N, C, c.V,
-                                               m->Vp, mode, status, st));
+                                               m->Vp, mode, status, st, nullptr, nullptr, 0, nullptr, sc, sb));
     OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, WTE), dz_op, m->lnf, b16, N, C, c.V, m->Vp, sc, sb,
                                                  mode, status, st));
     // ln_f: the residual gradient starts here (written, not accumulated); its
@@ -460,7 +463,8 @@ static int backward_impl(gpt2* m) {
                                                      4 * C, C, C, sc, sb, mode, status, st));
         // MLP c_fc: dln2 = dh . Wfc; dWfc = dh^T . ln2; dbfc
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dbig, Wl(FCW, 4 * cc), b16, nullptr, N,
-                                                   C, 4 * C, 4 * C, mode, status, st));
+                                                   C, 4 * C, 4 * C, mode, status, st, nullptr, nullptr, 0, nullptr,
+                                                   sc, sb));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, FCW) + l * 4 * cc, m->dbig, ln2, b16, N, C, 4 * C,
                                                      4 * C, sc, sb, mode, status, st));
         // ln_2: dres += LN'(dln2); the column sum of the result is the attention
@@ -491,7 +495,8 @@ static int backward_impl(gpt2* m) {
                                     {G(m, QKVB) + l * 3 * C, nullptr, nullptr}});
         // c_attn
         OP(MATMUL_BWD_INPUT, linear_backward_input(m->dln, false, m->dqkv, Wl(QKVW, 3 * cc), b16, nullptr, N,
-                                                   C, 3 * C, 3 * C, mode, status, st));
+                                                   C, 3 * C, 3 * C, mode, status, st, nullptr, nullptr, 0, nullptr,
+                                                   sc, sb));
         OP(MATMUL_BWD_WEIGHT, linear_backward_weight(G(m, QKVW) + l * 3 * cc, m->dqkv, ln1, b16, N, C, 3 * C,
                                                      3 * C, sc, sb, mode, status, st));
         if (!qkv_colsum)
