@@ -125,9 +125,12 @@ float gpt2_eval(gpt2* m, const int* tokens, const int* targets, int B, int T);
  * the last call), else ESTATE.  The keys and values of every layer for position
  * pos are appended to the cache (library memory, allocated by the first call:
  * L * maxB * maxT * 2C floats; call it before any stream capture), and the
- * logits of position pos are written to logits[B, V] (device, row stride V):
- * exactly the last row of a full forward over positions 0..pos.  Computed in
- * fp32 from the fp32 parameters in every mode.  Generation feeds the chosen
+ * logits of position pos are copied to logits[B, V] (device or host, row
+ * stride V) from the library's step buffer: exactly the last row of a full
+ * forward over positions 0..pos.  Computed in fp32 from the fp32 parameters in
+ * every mode.  The step's kernels read the position from device memory, so the
+ * second call with a given B records them as one CUDA graph that later calls
+ * with that B replay.  Generation feeds the chosen
  * token back at pos + 1 ("GPT-2 from scratch with torch", section 生成样本;
  * only the new row is computed: "GPT-2ベースの3000バイトCで実装された
  * ChatGPTクローン（2023）", section KVキャッシュ方式).  Asynchronous; an id
